@@ -1,0 +1,191 @@
+"""Latent-cache quantizers (oracle; test infrastructure only).
+
+Sources (page title, section):
+
+* "DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化 — 完整实验报告" (the Chinese report),
+  §3.2 "量化方案对比": per-channel INT8 in 32 blocks, per-tensor INT8,
+  per-token INT8, symmetric and asymmetric INT4 in 32 blocks, k_pe INT8 in
+  8 blocks, k_pe symmetric INT4 in 8 blocks.
+* "Absorbed MLA Cache Optimization on DeepSeek-V2-Lite — Technical Report"
+  (the English report), §4.2 "Quantization Error Comparison" and §5.1
+  (more blocks give lower error; 32 blocks recommended).
+* "DeepSeek的MLA技术：极致压缩KV Cache的创新方案" (the juejin tutorial),
+  section "量化压缩": scale = absmax / 127, code = round(x / scale),
+  x_hat = code * scale.
+
+Readings taken where the pages are open (each is listed in the design doc):
+
+* "32 blocks" of the 512-dim latent are 32 groups of 16 consecutive channels
+  with one scale per (token, group): a scale computed across future tokens is
+  impossible when quantizing on write.
+* Symmetric INT8: s = absmax / 127 in fp32, q = clamp(rint(x / s), -127, 127).
+  A group whose absmax is 0 gets s = 0 and q = 0.
+* Asymmetric INT4: s = (max - min) / 15 (one fp32 subtraction, one fp32
+  division), z = rint(-min / s) stored as an integer-valued fp32,
+  q = clamp(rint(x / s) + z, 0, 15).  x_hat = (q - z) * s.  When s comes out
+  0: if min == 0 then s = z = q = 0; otherwise s = |min|, z = rint(-min / s)
+  (= -1 or +1) and q = 0, which reconstructs the constant group exactly.
+* All arithmetic is IEEE fp32 with round-half-even (NumPy float32 ops and
+  ``np.rint``); no fused multiply-add.
+
+Parity status: pinned (round-trip bound, brute-force nearest level,
+hand-built half-way ties, degenerate groups, the pages' error ordering).
+"""
+
+import numpy as np
+
+F32 = np.float32
+
+
+def _groups(x, group):
+    x = np.asarray(x, dtype=np.float32)
+    if x.ndim != 2 or x.shape[1] % group:
+        raise ValueError("x must be [rows, channels] with channels % group == 0")
+    return x.reshape(x.shape[0], x.shape[1] // group, group)
+
+
+def quantize_sym_int8(x, group):
+    """Symmetric INT8 with one fp32 scale per (row, group of `group` channels).
+
+    Chinese report §3.2 row "per-channel INT8 (32块)" (group 16 on the
+    512-dim latent) and row "k_pe INT8 (8块)" (group 8 on the 64-dim k_pe);
+    tutorial "量化压缩" for scale = absmax/127 and code = round(x/scale).
+
+    Returns (codes int8 [rows, channels], scale float32 [rows, groups]).
+    """
+    g = _groups(x, group)
+    a = np.max(np.abs(g), axis=2)
+    s = a / F32(127)
+    live = s > 0
+    safe = np.where(live, s, F32(1)).astype(np.float32)
+    q = np.rint(g / safe[..., None])
+    q = np.clip(q, -127, 127)
+    q = np.where(live[..., None], q, F32(0))
+    return q.astype(np.int8).reshape(x.shape[0], -1), s.astype(np.float32)
+
+
+def dequantize_sym_int8(codes, scale, group):
+    """x_hat = float(code) * scale in fp32 (tutorial "量化压缩", dequantize line)."""
+    codes = np.asarray(codes)
+    rows, ch = codes.shape
+    q = codes.astype(np.float32).reshape(rows, ch // group, group)
+    return (q * np.asarray(scale, np.float32)[..., None]).reshape(rows, ch)
+
+
+def quantize_asym_int4(x, group=16):
+    """Asymmetric INT4 with fp32 scale and zero-point per (row, group).
+
+    Chinese report §3.2 row "非对称 INT4 (32块)" and §4.1 (the 7.6 KB scheme);
+    the scale / zero formulas are the plain affine min-max rule
+    s = (max - min) / 15, z = round(-min / s).
+
+    Returns (codes uint8 in [0, 15] [rows, channels] - one code per channel,
+    not packed; scale float32 [rows, groups]; zero float32 [rows, groups]).
+    """
+    g = _groups(x, group)
+    mn = np.min(g, axis=2)
+    mx = np.max(g, axis=2)
+    s = ((mx - mn).astype(np.float32) / F32(15)).astype(np.float32)
+    deg = s == 0
+    # degenerate group: s = |min| (or 0 when min == 0)
+    s = np.where(deg, np.abs(mn), s).astype(np.float32)
+    live = s > 0
+    safe = np.where(live, s, F32(1)).astype(np.float32)
+    z = np.rint(-mn / safe)
+    z = np.where(live, z, F32(0)).astype(np.float32)
+    r = np.rint(g / safe[..., None]).astype(np.float32)
+    q = np.clip(r + z[..., None], 0, 15)
+    q = np.where(live[..., None], q, F32(0))
+    return q.astype(np.uint8).reshape(x.shape[0], -1), s, z
+
+
+def dequantize_asym_int4(codes, scale, zero, group=16):
+    """x_hat = (float(code) - zero) * scale, both steps in fp32."""
+    codes = np.asarray(codes)
+    rows, ch = codes.shape
+    q = codes.astype(np.float32).reshape(rows, ch // group, group)
+    d = q - np.asarray(zero, np.float32)[..., None]
+    return (d * np.asarray(scale, np.float32)[..., None]).reshape(rows, ch)
+
+
+# ---------------------------------------------------------------------------
+# Comparison quantizers: rows of the pages' error tables that the cache does
+# not store, used only to pin the ordering the tables state.
+# ---------------------------------------------------------------------------
+
+def quantize_per_tensor_int8(x):
+    """One scale for the whole tensor: Chinese report §3.2 "per-tensor INT8";
+    tutorial "量化压缩" (its code takes abs().max() over the whole tensor)."""
+    x = np.asarray(x, np.float32)
+    s = np.max(np.abs(x)) / F32(127)
+    if s == 0:
+        return np.zeros(x.shape, np.int8), F32(0)
+    q = np.clip(np.rint(x / s), -127, 127)
+    return q.astype(np.int8), F32(s)
+
+
+def quantize_per_token_int8(x):
+    """One scale per row (token): Chinese report §3.2 "per-token INT8"."""
+    x = np.asarray(x, np.float32)
+    return quantize_sym_int8(x, x.shape[1])
+
+
+def quantize_sym_int4(x, group=16):
+    """Symmetric INT4, s = absmax / 7, codes in [-7, 7]: Chinese report §3.2
+    "对称 INT4 (32块)" (the row the asymmetric scheme is said to beat)."""
+    g = _groups(x, group)
+    a = np.max(np.abs(g), axis=2)
+    s = (a / F32(7)).astype(np.float32)
+    live = s > 0
+    safe = np.where(live, s, F32(1)).astype(np.float32)
+    q = np.clip(np.rint(g / safe[..., None]), -7, 7)
+    q = np.where(live[..., None], q, F32(0))
+    return q.astype(np.int8).reshape(x.shape[0], -1), s
+
+
+def relative_error(x, x_hat):
+    """Mean and max of |x - x_hat| / mean|x| over the tensor.
+
+    The pages' error column ("平均误差 / Mean Relative Error") is not defined
+    on them; this is the reading used for the ordering checks.
+    """
+    x = np.asarray(x, np.float64)
+    e = np.abs(x - np.asarray(x_hat, np.float64))
+    denom = np.mean(np.abs(x))
+    return float(np.mean(e) / denom), float(np.max(e) / denom)
+
+
+# ---------------------------------------------------------------------------
+# Whole-token helpers used by tests: latent (512) + k_pe (64) in one call.
+# ---------------------------------------------------------------------------
+
+FMT_BF16, FMT_INT8, FMT_INT4 = 0, 1, 2
+LATENT_GROUP, KPE_GROUP = 16, 8
+
+
+def quantize_token_rows(c, kpe, latent_fmt, kpe_fmt):
+    """Quantize latent rows c [N, 512] and k_pe rows kpe [N, 64] as the cache
+    stores them.  Returns a dict of the stored fields plus the dequantized
+    fp32 values the attention reads ("c_hat", "kpe_hat")."""
+    c = np.asarray(c, np.float32)
+    kpe = np.asarray(kpe, np.float32)
+    out = {}
+    if latent_fmt == FMT_BF16:
+        out["c_hat"] = c.copy()
+    elif latent_fmt == FMT_INT8:
+        q, s = quantize_sym_int8(c, LATENT_GROUP)
+        out.update(c_codes=q, c_scale=s, c_hat=dequantize_sym_int8(q, s, LATENT_GROUP))
+    elif latent_fmt == FMT_INT4:
+        q, s, z = quantize_asym_int4(c, LATENT_GROUP)
+        out.update(c_codes=q, c_scale=s, c_zero=z,
+                   c_hat=dequantize_asym_int4(q, s, z, LATENT_GROUP))
+    else:
+        raise ValueError("latent_fmt")
+    if kpe_fmt == FMT_BF16:
+        out["kpe_hat"] = kpe.copy()
+    elif kpe_fmt == FMT_INT8:
+        q, s = quantize_sym_int8(kpe, KPE_GROUP)
+        out.update(kpe_codes=q, kpe_scale=s, kpe_hat=dequantize_sym_int8(q, s, KPE_GROUP))
+    else:
+        raise ValueError("kpe_fmt")
+    return out

@@ -1,0 +1,209 @@
+"""Pins for the oracle's quantizers.
+
+They tie the oracle to what the pages and arithmetic fix, not to itself:
+brute-force nearest level, hand-built half-way ties with literal expected
+codes, degenerate groups, the round-trip bound, and the error ordering of the
+Chinese report's §3.2 table ("DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化 — 完整实验报告")
+and the English report's §4.2 / §5.1.
+"""
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import quant as Q
+
+RNG = np.random.default_rng(1234)
+
+
+def ulp32(x):
+    x = np.abs(np.asarray(x, np.float32))
+    return np.spacing(x).astype(np.float64)
+
+
+def synth_latent(T=512, layer=0, seed=7):
+    return synth.bf16_to_f32(synth.latent_bf16(seed, layer, 0, 0, T))
+
+
+def synth_kpe(T=512, layer=0, seed=7):
+    cos, sin = synth.rope_tables(T)
+    return synth.bf16_to_f32(synth.kpe_bf16(seed, layer, 0, 0, T, cos, sin))
+
+
+# --------------------------------------------------------------- INT8 --------
+
+@pytest.mark.parametrize("group", [16, 8])
+def test_int8_codes_are_nearest_levels_brute_force(group):
+    x = np.concatenate([synth_latent(64)[:, :128], RNG.standard_normal((64, 128)).astype(np.float32) * 3])
+    q, s = Q.quantize_sym_int8(x, group)
+    assert q.dtype == np.int8 and s.dtype == np.float32
+    sg = np.repeat(s, group, axis=1)
+    ratio = (x / sg).astype(np.float64)          # the fp32 quotient the definition rounds
+    levels = np.arange(-127, 128, dtype=np.float64)
+    d = np.abs(ratio[..., None] - levels)        # distance to every code
+    best = d.min(axis=-1)
+    chosen = np.abs(ratio - q.astype(np.float64))
+    assert np.all(chosen == best)
+    # exact ties go to the even code
+    tie = np.sum(d == best[..., None], axis=-1) > 1
+    assert np.all(q[tie] % 2 == 0)
+
+
+def test_int8_scale_is_absmax_over_127():
+    x = synth_latent(32)
+    q, s = Q.quantize_sym_int8(x, 16)
+    a = np.abs(x).reshape(32, 32, 16).max(axis=2).astype(np.float64)
+    assert np.all(np.abs(s.astype(np.float64) * 127 - a) <= 2 * ulp32(a))
+    # the absmax element of every group codes to +-127
+    g = np.abs(q.reshape(32, 32, 16).astype(np.int32)).max(axis=2)
+    assert np.all(g == 127)
+
+
+def test_int8_half_even_ties_literal():
+    # s = 127 / 127 = 1 exactly, so x / s = x and the ties are exact.
+    row = np.array([127, 0.5, 1.5, 2.5, 3.5, -0.5, -1.5, -2.5, 126.5, -126.5, 0, 7, -7, 0.25, 0.75, 100.49],
+                   np.float32)[None, :]
+    q, s = Q.quantize_sym_int8(row, 16)
+    assert s[0, 0] == np.float32(1.0)
+    expect = [127, 0, 2, 2, 4, 0, -2, -2, 126, -126, 0, 7, -7, 0, 1, 100]
+    assert q[0].tolist() == expect
+
+
+def test_int8_degenerate_and_extreme_groups():
+    rows = np.zeros((4, 16), np.float32)
+    rows[1, :] = 3.25                         # constant group
+    rows[2, 0] = -1000.0                      # single outlier, rest tiny
+    rows[2, 1:] = 1e-3
+    rows[3, :] = np.array([127, -127] * 8, np.float32)
+    q, s = Q.quantize_sym_int8(rows, 16)
+    assert s[0, 0] == 0 and np.all(q[0] == 0)                       # all-zero group
+    assert np.all(q[1] == 127)
+    x_hat = Q.dequantize_sym_int8(q, s, 16)
+    assert np.all(np.abs(x_hat[1] - 3.25) <= 2 * ulp32(3.25))
+    assert q[2, 0] == -127 and np.all(q[2, 1:] == 0)
+    assert q[3].tolist() == [127, -127] * 8
+
+
+@pytest.mark.parametrize("group", [16, 8])
+def test_int8_round_trip_bound(group):
+    x = np.concatenate([synth_latent(256), synth_latent(256, layer=3)])[:, :512]
+    q, s = Q.quantize_sym_int8(x, group)
+    x_hat = Q.dequantize_sym_int8(q, s, group)
+    sg = np.repeat(s, group, axis=1).astype(np.float64)
+    ag = np.repeat(np.abs(x).reshape(x.shape[0], -1, group).max(axis=2), group, axis=1)
+    err = np.abs(x.astype(np.float64) - x_hat)
+    # 0.5 scale in exact arithmetic; a few fp32 ulps of the group absmax for
+    # the rounded quotient and product.
+    assert np.all(err <= 0.5 * sg + 4 * ulp32(ag))
+
+
+# --------------------------------------------------------------- INT4 --------
+
+def test_int4_codes_are_nearest_levels_brute_force():
+    x = np.concatenate([synth_latent(64), RNG.standard_normal((64, 512)).astype(np.float32) + 2.0])
+    q, s, z = Q.quantize_asym_int4(x, 16)
+    assert q.dtype == np.uint8 and q.max() <= 15
+    sg = np.repeat(s, 16, axis=1)
+    zg = np.repeat(z, 16, axis=1).astype(np.float64)
+    ratio = (x / sg).astype(np.float64)
+    levels = np.arange(16, dtype=np.float64)
+    d = np.abs(ratio[..., None] - (levels - zg[..., None]))
+    best = d.min(axis=-1)
+    chosen = np.abs(ratio - (q.astype(np.float64) - zg))
+    assert np.all(chosen == best)
+    tie = np.sum(d == best[..., None], axis=-1) > 1
+    assert np.all((q[tie].astype(np.int64) - zg[tie].astype(np.int64)) % 2 == 0)
+
+
+def test_int4_scale_zero_and_endpoints():
+    x = synth_latent(64)
+    q, s, z = Q.quantize_asym_int4(x, 16)
+    g = x.reshape(64, 32, 16).astype(np.float64)
+    mn, mx = g.min(axis=2), g.max(axis=2)
+    assert np.all(np.abs(s * 15.0 - (mx - mn)) <= 4 * ulp32(np.maximum(np.abs(mx), np.abs(mn))))
+    assert np.all(z == np.round(z)) and z.dtype == np.float32
+    qg = q.reshape(64, 32, 16)
+    imin, imax = g.argmin(axis=2), g.argmax(axis=2)
+    qmin = np.take_along_axis(qg, imin[..., None], 2)[..., 0]
+    qmax = np.take_along_axis(qg, imax[..., None], 2)[..., 0]
+    assert np.all(qmin <= 1) and np.all(qmax >= 14)
+    # groups straddling zero have their zero-point inside the code range
+    straddle = (mn < 0) & (mx > 0)
+    assert np.all((z[straddle] >= 0) & (z[straddle] <= 15))
+
+
+def test_int4_degenerate_groups_reconstruct_exactly():
+    rows = np.zeros((4, 16), np.float32)
+    rows[1, :] = 2.5
+    rows[2, :] = -0.75
+    rows[3, :8] = 1.0
+    rows[3, 8:] = 4.0
+    q, s, z = Q.quantize_asym_int4(rows, 16)
+    assert s[0, 0] == 0 and z[0, 0] == 0 and np.all(q[0] == 0)
+    assert s[1, 0] == 2.5 and z[1, 0] == -1 and np.all(q[1] == 0)
+    assert s[2, 0] == 0.75 and z[2, 0] == 1 and np.all(q[2] == 0)
+    x_hat = Q.dequantize_asym_int4(q, s, z, 16)
+    assert np.array_equal(x_hat[:3], rows[:3])
+    # two-level group: min 1 -> code 0, max 4 -> code 15, s = 0.2, z = -5
+    assert np.isclose(s[3, 0], 0.2) and z[3, 0] == -5
+    assert np.all(q[3, :8] == 0) and np.all(q[3, 8:] == 15)
+
+
+def test_int4_half_even_tie_literal():
+    # min = -1, max = 14 -> s = 1, z = 1; x / s = 2.5 -> rint 2 (even) -> q = 3
+    row = np.array([-1, 14, 2.5, 3.5, -0.5, 0.5, 0, 13.5, 1, 1, 1, 1, 1, 1, 1, 1], np.float32)[None, :]
+    q, s, z = Q.quantize_asym_int4(row, 16)
+    assert s[0, 0] == 1 and z[0, 0] == 1
+    assert q[0, :8].tolist() == [0, 15, 3, 5, 1, 1, 1, 15]
+
+
+def test_int4_round_trip_bound():
+    x = np.concatenate([synth_latent(256), RNG.standard_normal((64, 512)).astype(np.float32) * 50 + 100])
+    q, s, z = Q.quantize_asym_int4(x, 16)
+    x_hat = Q.dequantize_asym_int4(q, s, z, 16)
+    sg = np.repeat(s, 16, axis=1).astype(np.float64)
+    ag = np.repeat(np.abs(x).reshape(x.shape[0], -1, 16).max(axis=2), 16, axis=1)
+    err = np.abs(x.astype(np.float64) - x_hat)
+    assert np.all(err <= 0.5 * sg + 8 * ulp32(ag))
+
+
+# ------------------------------------------------- the pages' error ordering --
+
+def test_error_ordering_per_group_per_token_per_tensor():
+    """CN §3.2 / EN §4.2: per-group (0.0109) < per-token (0.0636) < per-tensor
+    (0.2979) on a latent with per-channel outliers."""
+    x = synth_latent(512)
+    e_group = Q.relative_error(x, Q.dequantize_sym_int8(*Q.quantize_sym_int8(x, 16), 16))[0]
+    qt, st = Q.quantize_per_token_int8(x)
+    e_token = Q.relative_error(x, Q.dequantize_sym_int8(qt, st, 512))[0]
+    qa, sa = Q.quantize_per_tensor_int8(x)
+    e_tensor = Q.relative_error(x, qa.astype(np.float32) * sa)[0]
+    assert e_group < e_token < e_tensor
+    assert e_tensor / e_group > 5
+
+
+def test_error_more_groups_is_better():
+    """EN §5.1: 8 blocks worse than 32 blocks worse than 64 blocks."""
+    x = synth_latent(512)
+    errs = [Q.relative_error(x, Q.dequantize_sym_int8(*Q.quantize_sym_int8(x, 512 // n), 512 // n))[0]
+            for n in (8, 32, 64)]
+    assert errs[0] > errs[1] > errs[2]
+
+
+def test_error_asym_int4_beats_sym_int4():
+    """CN §3.2: asymmetric INT4 (0.0786) better than symmetric INT4 (0.1116)."""
+    x = synth_latent(512)
+    q, s, z = Q.quantize_asym_int4(x, 16)
+    e_asym = Q.relative_error(x, Q.dequantize_asym_int4(q, s, z, 16))[0]
+    qs, ss = Q.quantize_sym_int4(x, 16)
+    e_sym = Q.relative_error(x, Q.dequantize_sym_int8(qs, ss, 16))[0]
+    assert e_asym < e_sym
+
+
+def test_error_kpe_int8_below_latent_int8():
+    """CN §3.2: k_pe INT8 in 8 blocks (0.0051) beats the latent INT8 (0.0109)."""
+    x = synth_latent(512)
+    k = synth_kpe(512)
+    e_lat = Q.relative_error(x, Q.dequantize_sym_int8(*Q.quantize_sym_int8(x, 16), 16))[0]
+    e_kpe = Q.relative_error(k, Q.dequantize_sym_int8(*Q.quantize_sym_int8(k, 8), 8))[0]
+    assert e_kpe < e_lat
