@@ -1,0 +1,464 @@
+"""Benchmark: absorbed MLA decode over a quantized paged latent cache.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one decode step of the whole model: for every layer, append the new
+token of every sequence (quantize-on-write), absorb the query, run the
+split-K decode + log-sum-exp combine, and un-absorb the output.  The step is
+captured in a CUDA graph and timed with CUDA events on its stream after W
+warm-up replays; the per-step working set (the whole cache) is larger than
+L2, so no flush is needed between steps.  Inputs are synthetic and seeded
+(DeepSeek-V2-Lite shapes, random-init weights); caches are resident in HBM
+before the timed region.  Prints one JSON line on rank 0.
+
+--impl reference times the CPU oracle (NumPy, fp64 attention) on the same
+workload: each step is a bounded sample (one sequence through all layers,
+layers spread over the host cores).
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+# name -> (layers, heads, seq_lens spec, latent fmt, kpe fmt, description)
+CONFIGS = {
+    "v2lite_int8": dict(layers=27, heads=16, batch=8, ctx=4096, latent="int8", kpe="int8",
+                        desc="DeepSeek-V2-Lite shapes, 27 layers, 16 heads, batch 8, context 4096, "
+                             "INT8 latent (32 groups) + INT8 k_pe, 64-token pages"),
+    "v2lite_int4_32k": dict(layers=27, heads=16, batch=32, ctx=32768, latent="int4", kpe="int8",
+                            desc="V2-Lite shapes, batch 32, context 32768, asymmetric INT4 latent + INT8 k_pe"),
+    "long_int4_1m": dict(layers=27, heads=16, batch=1, ctx=1048576, latent="int4", kpe="int8",
+                         desc="V2-Lite shapes, batch 1, context 1,048,576, asymmetric INT4 latent + INT8 k_pe"),
+    "long_bf16_256k": dict(layers=27, heads=16, batch=1, ctx=262144, latent="bf16", kpe="bf16",
+                           desc="V2-Lite shapes, batch 1, context 262,144, bf16 latent + bf16 k_pe"),
+    "mixed_h64_int8": dict(layers=1, heads=64, batch=64, ctx="loguniform", latent="int8", kpe="int8",
+                           desc="64 heads, batch 64, context log-uniform in [1K, 64K], INT8 latent + k_pe"),
+    "mixed_h64_int4": dict(layers=1, heads=64, batch=64, ctx="loguniform", latent="int4", kpe="int8",
+                           desc="64 heads, batch 64, context log-uniform in [1K, 64K], INT4 latent + INT8 k_pe"),
+    "mixed_h64_bf16": dict(layers=1, heads=64, batch=64, ctx="loguniform", latent="bf16", kpe="bf16",
+                           desc="64 heads, batch 64, context log-uniform in [1K, 64K], bf16 latent + k_pe"),
+    "tiny": dict(layers=1, heads=16, batch=1, ctx=256, latent="int8", kpe="int8",
+                 desc="1 layer, 16 heads, batch 1, context 256"),
+}
+FMT = {"bf16": 0, "int8": 1, "int4": 2}
+BETA = {("bf16", "bf16"): 1152, ("int8", "int8"): 736, ("int4", "int8"): 608, ("int8", "bf16"): 800,
+        ("int4", "bf16"): 672, ("bf16", "int8"): 1088}
+METRIC = "decode tokens/s & achieved HBM GB/s (% of GB300 peak) for absorbed MLA decode"
+SEED = 0x4D4C41
+FALLBACK_HBM_GBS = 6800.0
+
+
+def seq_lens_for(cfg, seed):
+    if cfg["ctx"] == "loguniform":
+        import synth
+        return [int(t) for t in synth.log_uniform_lengths(seed, cfg["batch"], 1024, 65536)]
+    return [int(cfg["ctx"])] * cfg["batch"]
+
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash():
+    h = hashlib.sha256()
+    for name in ("decode.cu", "decode_mma.cu", "mla_internal.cuh"):
+        p = os.path.join(ROOT, "mla_latent_kv_append_gb300", "csrc", name)
+        if os.path.exists(p):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config_name):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode source; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+        e = rec.get(config_name)
+        if e and e.get("source_hash") == decode_source_hash():
+            return e.get("bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------
+# the oracle on the host (cpu_baseline and --impl reference)
+# ----------------------------------------------------------------------------------
+def _oracle_worker(conn, cfg, seq_lens, tasks, seed):
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import numpy as np
+    import synth
+    from oracle import attention as A
+    from oracle import quant as Q
+    lf, kf = FMT[cfg["latent"]], FMT[cfg["kpe"]]
+    H, B = cfg["heads"], len(seq_lens)
+    state = []
+    for (l, b) in tasks:                     # untimed: the cache as the step finds it
+        T = seq_lens[b]
+        cos, sin = synth.rope_tables(max(1, T))
+        c_bits, k_bits = synth.sequence_bf16(seed, l, b, T, cos, sin)
+        c, k = synth.bf16_to_f32(c_bits), synth.bf16_to_f32(k_bits)
+        stored = Q.quantize_token_rows(c[:T - 1], k[:T - 1], lf, kf)
+        q = [synth.bf16_to_f32(a) for a in (synth.q_nope_bf16(seed, l, B, H)[b:b + 1],
+                                             synth.q_pe_bf16(seed, l, B, H)[b:b + 1],
+                                             synth.w_uk_bf16(seed, l, H), synth.w_uv_bf16(seed, l, H))]
+        state.append((stored, c[T - 1:], k[T - 1:], q))
+    conn.send("ready")
+    while True:
+        msg = conn.recv()
+        if msg == "stop":
+            break
+        t0 = time.perf_counter()
+        for stored, c_new, k_new, (qn, qp, wuk, wuv) in state:
+            new = Q.quantize_token_rows(c_new, k_new, lf, kf)      # append the new token
+            c_hat = np.concatenate([_dequant_latent(Q, stored, lf), new["c_hat"]])
+            kpe_hat = np.concatenate([_dequant_kpe(Q, stored, kf), new["kpe_hat"]])
+            A.absorbed_decode_full(qn[0], qp[0], wuk, wuv, c_hat, kpe_hat)
+        conn.send(time.perf_counter() - t0)
+
+
+def _dequant_latent(Q, stored, lf):
+    if lf == 1:
+        return Q.dequantize_sym_int8(stored["c_codes"], stored["c_scale"], 16)
+    if lf == 2:
+        return Q.dequantize_asym_int4(stored["c_codes"], stored["c_scale"], stored["c_zero"], 16)
+    return stored["c_hat"]                      # bf16 cache: the values themselves
+
+
+def _dequant_kpe(Q, stored, kf):
+    if kf == 1:
+        return Q.dequantize_sym_int8(stored["kpe_codes"], stored["kpe_scale"], 8)
+    return stored["kpe_hat"]
+
+
+class OracleRunner:
+    """Worker processes (spawned, one BLAS thread each) that together run the
+    oracle's decode step for one sequence through all layers."""
+
+    def __init__(self, cfg, seq_lens, seed, workers=None):
+        n = workers or min(os.cpu_count() or 1, cfg["layers"], 16)
+        self.n = n
+        tasks = [[] for _ in range(n)]
+        for l in range(cfg["layers"]):
+            tasks[l % n].append((l, 0))
+        ctx = mp.get_context("spawn")
+        self.procs, self.conns = [], []
+        for w in range(n):
+            a, b = ctx.Pipe()
+            p = ctx.Process(target=_oracle_worker, args=(b, cfg, seq_lens, tasks[w], seed), daemon=True)
+            p.start()
+            self.procs.append(p)
+            self.conns.append(a)
+        for c in self.conns:
+            assert c.recv() == "ready"
+
+    def step(self):
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send("go")
+        for c in self.conns:
+            c.recv()
+        return time.perf_counter() - t0
+
+    def close(self):
+        for c in self.conns:
+            c.send("stop")
+        for p in self.procs:
+            p.join(timeout=10)
+
+
+def cpu_baseline(cfg, seq_lens, min_seconds=8.0, steps=None, warmup=1):
+    r = OracleRunner(cfg, seq_lens, SEED)
+    for _ in range(warmup):
+        r.step()
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        times.append(r.step())
+        if steps is not None and len(times) >= steps:
+            break
+        if steps is None and time.perf_counter() - t_start >= min_seconds and len(times) >= 2:
+            break
+    r.close()
+    total = sum(times)
+    return {"value": len(times) / total, "unit": "tokens/s", "cores": r.n, "kind": "oracle",
+            "sample": "sequence 0 through all %d layers per step (context %d), layers spread over %d "
+                      "spawned single-BLAS-thread processes; %d steps, %.1f s" % (
+                          cfg["layers"], seq_lens[0], r.n, len(times), total),
+            "ms_per_step": 1000 * total / len(times), "steps": len(times)}
+
+
+# ----------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+    import mla_latent_kv_append_gb300 as mla
+    from synth.workload import DecodeStep, Workload
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    seed = SEED + rank
+    seq_lens = seq_lens_for(cfg, seed)
+    layers = args.layers or cfg["layers"]
+    t_setup = time.time()
+    wl = Workload(layers, cfg["heads"], seq_lens, FMT[cfg["latent"]], FMT[cfg["kpe"]], seed, device=dev)
+    step = DecodeStep(wl, num_splits=args.num_splits)
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        step.run()                                    # eager once (configures kernels)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step.run()
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local_rank)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    err_word = int(step.dev_err.item())
+
+    # ---- the decode call (split-K kernel + combine) timed alone, per layer, same stream
+    reps = max(3, min(20, args.steps))
+    evs = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            for l in range(wl.L):
+                mla.mla_cache_append(wl.caches[l], wl.c_new[l], wl.kpe_new[l], wl.slot_new, step.dev_err)
+                mla.mla_q_absorb(wl.q_nope[l], wl.w_uk[l], step.q_lat)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                mla.mla_decode_absorbed(wl.caches[l], step.q_lat, wl.q_pe[l], wl.block_table, wl.seq_lens_dev,
+                                        step.workspace, step.o_lat, step.lse[l], step.dev_err,
+                                        num_splits=args.num_splits)
+                b.record(stream)
+                evs.append((a, b))
+                mla.mla_out_unabsorb(step.o_lat, wl.w_uv[l], step.o[l])
+    torch.cuda.synchronize()
+    dec_ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
+    host_in = [(pin(wl.c_new[l]), pin(wl.kpe_new[l]), pin(wl.q_nope[l]), pin(wl.q_pe[l])) for l in range(wl.L)]
+    host_out = torch.empty(step.o.shape, dtype=step.o.dtype, pin_memory=True)
+    h2d = sum(sum(t.numel() * t.element_size() for t in x) for x in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+    e2e_steps = max(3, min(args.steps, 50))
+    done = torch.cuda.Event()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            for l, (c, k, qn, qp) in enumerate(host_in):
+                wl.c_new[l].copy_(c, non_blocking=True)
+                wl.kpe_new[l].copy_(k, non_blocking=True)
+                wl.q_nope[l].copy_(qn, non_blocking=True)
+                wl.q_pe[l].copy_(qp, non_blocking=True)
+            graph.replay()
+            host_out.copy_(step.o, non_blocking=True)
+            done.record(stream)
+            done.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    tokens_per_step = wl.B * world
+    beta = BETA[(cfg["latent"], cfg["kpe"])]
+    cache_bytes_launch = sum(seq_lens) * beta
+    peak, peak_kind = hbm_peak()
+    achieved = cache_bytes_launch / (dec_ms * 1e-3) / 1e9
+    weight_bytes = 2 * cfg["heads"] * 128 * 512 * 2
+    step_bytes = layers * (cache_bytes_launch + weight_bytes)
+    out = {
+        "metric": METRIC,
+        "value": tokens_per_step / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8 codes / fp32 math" if cfg["latent"] != "bf16" else "bf16 / fp32 math",
+        "data": "synthetic (seeded; DeepSeek-V2-Lite shapes, random-init weights)",
+        "config": {"workload": args.config, "description": cfg["desc"], "layers": layers, "heads": cfg["heads"],
+                   "batch_per_gpu": wl.B, "context": (seq_lens[0] if len(set(seq_lens)) == 1 else
+                                                      "log-uniform, mean %d" % (sum(seq_lens) // len(seq_lens))),
+                   "latent_fmt": cfg["latent"], "kpe_fmt": cfg["kpe"], "page_tokens": 64,
+                   "num_splits": args.num_splits or "auto",
+                   "l2": "no flush: each step reads %.0f MB of cache, > 129 MB L2" % (step_bytes / 1e6),
+                   "parallelism": "replicas by sequence (dp%d)" % world, "cuda_graph": True},
+        "cache_gbs": achieved,
+        "step_gbs": step_bytes / (ms * 1e-3) / 1e9,
+        "hbm_frac_of_peak": achieved / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic(args.config),
+                     "kernel": "mla_decode_absorbed (split-K decode + LSE combine)",
+                     "bytes_per_launch": cache_bytes_launch, "launch_ms": dec_ms,
+                     "peak_source": "%s hbm_gbs (MEASURED_PEAKS.json)" % peak_kind if peak_kind == "measured"
+                     else "fallback 6.8 TB/s"},
+        "e2e": {"value": tokens_per_step / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * layers * 5,
+        "device_error_word": err_word,
+        "clocks": clk,
+        "setup_s": round(setup_s, 1),
+    }
+    return out, seq_lens
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="v2lite_int8", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (testing only)")
+    ap.add_argument("--num-splits", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    cfg = CONFIGS[args.config]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        seq_lens = seq_lens_for(cfg, SEED)
+        if args.layers:
+            cfg = dict(cfg, layers=args.layers)
+        steps = max(1, args.steps)
+        cb = cpu_baseline(cfg, seq_lens, steps=steps, warmup=max(1, min(args.warmup, 3)))
+        value = cb["value"] * world
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+                "steps": steps, "warmup": args.warmup, "ms_per_step": cb["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention / fp32 quantization",
+                "data": "synthetic (seeded; DeepSeek-V2-Lite shapes, random-init weights)",
+                "config": {"workload": args.config, "description": cfg["desc"]},
+                "cpu_baseline": cb, "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                            "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    out, seq_lens = run_ours(args, cfg, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            c = dict(cfg, layers=args.layers or cfg["layers"])
+            out["cpu_baseline"] = cpu_baseline(c, seq_lens)
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,220 @@
+/*
+ * mla.h - C ABI of the absorbed Multi-head Latent Attention (MLA) decode
+ * library for NVIDIA GB300 (sm_103a).
+ *
+ * What it computes.  A decode step of MLA attention runs directly against a
+ * cache that keeps, per token and layer, one 512-dim compressed latent
+ * ("compressed_kv") and one 64-dim RoPE key ("k_pe"), and never the per-head
+ * K/V.  Sources (page title, section):
+ *   [CN] "DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化 — 完整实验报告"
+ *        §1.1 (compressed_kv = kv_a_proj(h); K, V = kv_b_proj(compressed)),
+ *        §3.1 (cache the 576-dim latent), §3.2 (per-group INT8 in 32 blocks,
+ *        asymmetric INT4 in 32 blocks, k_pe INT8 in 8 blocks).
+ *   [EN] "Absorbed MLA Cache Optimization on DeepSeek-V2-Lite — Technical
+ *        Report" §1.3 (expanded K is nope 128 + rope 64, V is 128), §2.1
+ *        (store(layer, compressed_kv, k_pe) quantizes on write; get()
+ *        dequantizes and projects at compute time).
+ *   [TU] "DeepSeek的MLA技术：极致压缩KV Cache的创新方案" (juejin tutorial),
+ *        "步骤2" (K_i = C^KV W_i^upK, V_i = C^KV W_i^upV), "KV Cache的实现"
+ *        (append the latent every step), "量化压缩" (scale = absmax / 127).
+ * Per sequence b and head h, with c_hat / kpe_hat the dequantized cache:
+ *   q_lat[h] = q_nope[h] @ W_UK[h]                         (mla_q_absorb)
+ *   s[t]     = (q_lat[h] . c_hat[t] + q_pe[h] . kpe_hat[t]) * softmax_scale
+ *   o_lat[h] = sum_t softmax(s)[t] c_hat[t];  lse[h] = log sum_t exp(s[t])
+ *                                                          (mla_decode_absorbed)
+ *   o[h]     = o_lat[h] @ W_UV[h]                          (mla_out_unabsorb)
+ * Moving W_UK onto the query and W_UV onto the output is the algebraic
+ * identity q.(W c) = (q W).c; it lets every cached byte be read once for all
+ * heads.
+ *
+ * Conventions for every call.
+ *   - Ownership: the caller allocates and frees all memory (device memory
+ *     unless stated).  The library never allocates, frees or synchronizes;
+ *     it keeps no state between calls apart from a per-device attribute
+ *     cache.  Calls are thread-safe and re-entrant.
+ *   - Execution: every call enqueues its kernels on `stream` (NULL = the
+ *     legacy default stream) and returns without waiting.
+ *   - Layout: arrays are row-major and contiguous with the shapes given.
+ *     bf16 values are passed as their 16-bit patterns (uint16_t).
+ *   - Errors: arguments are checked on the host before any launch; a bad
+ *     argument returns MLA_ERR_INVALID_ARG (or MLA_ERR_UNSUPPORTED for a
+ *     valid but unimplemented shape) and launches nothing.  A failed launch
+ *     returns MLA_ERR_CUDA.  Data-dependent faults found on the device (a
+ *     slot, page id or sequence length out of range) never trap: the kernel
+ *     skips the affected work and ORs a MLA_DEVERR_* bit into *dev_err when
+ *     dev_err is not NULL.  The caller reads dev_err after the stream
+ *     completes; a non-zero value means MLA_ERR_DEVICE_BOUNDS.
+ *   - Heads: H is a multiple of 16 and at most 128.  Dimensions are fixed at
+ *     the DeepSeek-V2 values: kv_lora_rank 512, rope 64, qk_nope 128, v 128.
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                       /* cudaStream_t is struct CUstream_st* */
+typedef struct CUstream_st* mla_stream_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,
+  MLA_ERR_UNSUPPORTED = 2,
+  MLA_ERR_CUDA = 3,
+  MLA_ERR_DEVICE_BOUNDS = 4
+} mla_status;
+
+typedef enum {
+  MLA_FMT_BF16 = 0,        /* values stored as bf16, no scale */
+  MLA_FMT_INT8_SYM = 1,    /* int8 code, fp32 scale per (token, group) */
+  MLA_FMT_INT4_ASYM = 2    /* 4-bit code, fp32 scale and zero per (token, group) */
+} mla_fmt;
+
+/* Bits ORed into *dev_err. */
+#define MLA_DEVERR_SLOT    1  /* append: slot not in [0, num_pages*64) and not -1 */
+#define MLA_DEVERR_PAGE    2  /* decode: block_table entry not in [0, num_pages)   */
+#define MLA_DEVERR_SEQLEN  4  /* decode: seq_len < 0 or > max_pages*64            */
+#define MLA_DEVERR_TIMEOUT 8  /* a bounded wait inside a kernel gave up           */
+
+#define MLA_KV_LORA_RANK 512
+#define MLA_ROPE_DIM 64
+#define MLA_QK_NOPE_DIM 128
+#define MLA_V_DIM 128
+#define MLA_PAGE_TOKENS 64
+#define MLA_LATENT_GROUP 16      /* 512 channels = 32 groups ([CN] §3.2 "32块") */
+#define MLA_KPE_GROUP 8          /* 64 channels = 8 groups ([CN] §3.2 "8块")   */
+
+/*
+ * One layer's paged latent cache.  The pool holds num_pages pages of 64
+ * tokens; a token's physical slot is page * 64 + offset.  Which pages belong
+ * to which sequence is the caller's business (block tables below).
+ *   latent_fmt: any mla_fmt.  kpe_fmt: MLA_FMT_BF16 or MLA_FMT_INT8_SYM.
+ *   pool: device memory of mla_cache_pool_bytes() bytes, 256-byte aligned,
+ *         owned by the caller.
+ */
+typedef struct {
+  int32_t num_pages;
+  int32_t latent_fmt;
+  int32_t kpe_fmt;
+  int32_t reserved;        /* must be 0 */
+  void* pool;
+} mla_cache_layer;
+
+/*
+ * Byte layout of one page (structure of arrays; every field starts on a
+ * 256-byte boundary so that one bulk copy can fetch it).  Offsets are from
+ * the page start; -1 marks a field the format does not have.
+ *   codes      [64 tokens][codes_row_bytes]: bf16 values (1024 B), int8
+ *              codes (512 B), or 4-bit codes two per byte, low nibble = even
+ *              channel (256 B).
+ *   scale      fp32 [32 groups][64 tokens]   (int8 / int4 latent)
+ *   zero       fp32 [32 groups][64 tokens]   (int4 latent; integer-valued)
+ *   kpe        [64 tokens][kpe_row_bytes]: bf16 (128 B) or int8 codes (64 B)
+ *   kpe_scale  fp32 [8 groups][64 tokens]    (int8 k_pe)
+ * page_bytes = 64 x (1152, 736 or 608) for bf16/bf16, int8/int8, int4/int8.
+ */
+typedef struct {
+  int64_t page_bytes;
+  int64_t codes_off, codes_row_bytes;
+  int64_t scale_off, zero_off;
+  int64_t kpe_off, kpe_row_bytes;
+  int64_t kpe_scale_off;
+} mla_page_layout;
+
+/* Fills *out for the cache's formats.  MLA_ERR_INVALID_ARG on a bad format. */
+mla_status mla_cache_page_layout(const mla_cache_layer* cache, mla_page_layout* out);
+
+/* num_pages * page_bytes, or 0 for an invalid descriptor. */
+size_t mla_cache_pool_bytes(const mla_cache_layer* cache);
+
+/*
+ * mla_cache_append - quantize-on-write of n new tokens into the paged cache.
+ * [EN] §2.1 store(): compressed_kv [seq, 512] is quantized, k_pe [seq, 64]
+ * stored; [CN] §3.2 for the formats.  Quantization rules, all IEEE fp32 with
+ * round-half-even and no fused multiply-add:
+ *   INT8_SYM  (groups of 16 latent channels, or 8 k_pe channels):
+ *       s = max|x| / 127;  q = clamp(rint(x / s), -127, 127);  s = 0 -> q = 0
+ *   INT4_ASYM (groups of 16): s = (max - min) / 15;  z = rint(-min / s);
+ *       q = clamp(rint(x / s) + z, 0, 15); if s == 0: s = |min|, z = rint(-min/s)
+ *       (or s = z = 0 when min == 0) and q = 0.
+ *   BF16: the input bits are copied.
+ *   c_new   bf16 [n][512]     kpe_new bf16 [n][64]
+ *   slot    int32 [n]: physical slot (page * 64 + offset) of each token;
+ *           -1 skips the token silently; any other value outside
+ *           [0, num_pages * 64) skips it and sets MLA_DEVERR_SLOT.
+ *   Two tokens with the same slot in one call race; the result is one of them.
+ *   n == 0 is a no-op.  dev_err may be NULL.
+ */
+mla_status mla_cache_append(const mla_cache_layer* cache, const uint16_t* c_new,
+                            const uint16_t* kpe_new, const int32_t* slot, int32_t n,
+                            int32_t* dev_err, mla_stream_t stream);
+
+/*
+ * mla_q_absorb - q_lat[b][h] = q_nope[b][h] @ W_UK[h]   (the query side of
+ * weight absorption; [TU] "步骤2" K_i = C^KV W_i^upK with W_UK[h] = (W_i^upK)^T).
+ *   q_nope bf16 [B][H][128]   W_UK bf16 [H][128][512]   q_lat fp32 [B][H][512]
+ *   fp32 accumulation of exact bf16 products.  B == 0 is a no-op.
+ */
+mla_status mla_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_lat,
+                        int32_t batch, int32_t heads, mla_stream_t stream);
+
+/*
+ * mla_decode_workspace_bytes - bytes of device workspace mla_decode_absorbed
+ * needs for this batch, head count and num_splits (0 = automatic).  The
+ * workspace holds the split-K partials (per split: running max, running sum
+ * and the unnormalised 512-wide latent output, fp32, per head).
+ */
+size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_splits);
+
+/*
+ * mla_decode_absorbed - absorbed attention of one decode query per sequence
+ * against its cached latents ([EN] §2.1 get(): attention computed from the
+ * latent; flash-decode split over context chunks with a log-sum-exp
+ * combine).  Dequantization is fused into the tile loads: x_hat = q * s for
+ * INT8, (q - z) * s for INT4.
+ *   q_lat       fp32 [B][H][512]   (from mla_q_absorb)
+ *   q_pe        bf16 [B][H][64]
+ *   block_table int32 [B][max_pages]: page id of each sequence's logical page
+ *   seq_lens    int32 [B]: tokens attended (positions 0..len-1, the newly
+ *               appended token included).  0 gives o_lat = 0 and lse = -inf.
+ *   softmax_scale: typically 1 / sqrt(128 + 64).
+ *   num_splits: CTAs the context work is divided over (0 = one per SM).
+ *               Work is split evenly over all sequences' 32-token chunks.
+ *   workspace:  device, >= mla_decode_workspace_bytes(B, H, num_splits)
+ *               bytes, 256-byte aligned; contents are scratch.
+ *   o_lat fp32 [B][H][512]      lse fp32 [B][H] (natural log; may be NULL)
+ *   A page id outside [0, num_pages) contributes nothing and sets
+ *   MLA_DEVERR_PAGE; seq_len outside [0, max_pages*64] is treated as 0 and
+ *   sets MLA_DEVERR_SEQLEN.  B == 0 is a no-op.  B <= 4096.
+ */
+mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
+                               const uint16_t* q_pe, const int32_t* block_table,
+                               int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                               int32_t heads, float softmax_scale, int32_t num_splits,
+                               void* workspace, size_t workspace_bytes, float* o_lat,
+                               float* lse, int32_t* dev_err, mla_stream_t stream);
+
+/*
+ * mla_out_unabsorb - o[b][h] = o_lat[b][h] @ W_UV[h]   (the output side of
+ * weight absorption; [TU] "步骤2" V_i = C^KV W_i^upV with W_UV[h] = W_i^upV).
+ *   o_lat fp32 [B][H][512]   W_UV bf16 [H][512][128]   o fp32 [B][H][128]
+ *   B == 0 is a no-op.
+ */
+mla_status mla_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o,
+                            int32_t batch, int32_t heads, mla_stream_t stream);
+
+/* Static string for a status code. */
+const char* mla_status_string(mla_status status);
+
+/* ABI version (major * 100 + minor). */
+int32_t mla_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H */

@@ -1,0 +1,157 @@
+// Host side of the C ABI declared in include/mla.h: argument checks, layout
+// arithmetic and dispatch to the kernel launchers.  Nothing here allocates.
+#include <math.h>
+
+#include "mla_internal.cuh"
+
+namespace mla {
+
+int device_sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+mla_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+static bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+static bool heads_ok(int H) { return H >= 16 && H <= 128 && H % 16 == 0; }
+
+static bool cache_ok(const mla_cache_layer* c, PageLayout* L) {
+  if (!c || c->num_pages <= 0 || c->reserved != 0 || !c->pool) return false;
+  if (!aligned(c->pool, 256)) return false;
+  return compute_layout(c->latent_fmt, c->kpe_fmt, L);
+}
+
+static int decode_grid(int num_splits) {
+  if (num_splits > 0) return num_splits;
+  int sms = device_sm_count();
+  return sms > 0 ? sms : 1;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+int32_t mla_abi_version(void) { return 100; }
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "ok";
+    case MLA_ERR_INVALID_ARG: return "invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "unsupported shape or format";
+    case MLA_ERR_CUDA: return "CUDA launch error";
+    case MLA_ERR_DEVICE_BOUNDS: return "device-side bounds error";
+  }
+  return "unknown status";
+}
+
+mla_status mla_cache_page_layout(const mla_cache_layer* cache, mla_page_layout* out) {
+  if (!cache || !out) return MLA_ERR_INVALID_ARG;
+  PageLayout L;
+  if (!compute_layout(cache->latent_fmt, cache->kpe_fmt, &L)) return MLA_ERR_INVALID_ARG;
+  out->page_bytes = L.page_bytes;
+  out->codes_off = L.codes_off;
+  out->codes_row_bytes = L.codes_row;
+  out->scale_off = L.scale_off;
+  out->zero_off = L.zero_off;
+  out->kpe_off = L.kpe_off;
+  out->kpe_row_bytes = L.kpe_row;
+  out->kpe_scale_off = L.kpe_scale_off;
+  return MLA_OK;
+}
+
+size_t mla_cache_pool_bytes(const mla_cache_layer* cache) {
+  if (!cache || cache->num_pages <= 0) return 0;
+  PageLayout L;
+  if (!compute_layout(cache->latent_fmt, cache->kpe_fmt, &L)) return 0;
+  return (size_t)L.page_bytes * (size_t)cache->num_pages;
+}
+
+mla_status mla_cache_append(const mla_cache_layer* cache, const uint16_t* c_new,
+                            const uint16_t* kpe_new, const int32_t* slot, int32_t n,
+                            int32_t* dev_err, mla_stream_t stream) {
+  PageLayout L;
+  if (!cache_ok(cache, &L) || n < 0) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  if (!c_new || !kpe_new || !slot) return MLA_ERR_INVALID_ARG;
+  if (!aligned(c_new, 16) || !aligned(kpe_new, 16) || !aligned(slot, 4)) return MLA_ERR_INVALID_ARG;
+  if (dev_err && !aligned(dev_err, 4)) return MLA_ERR_INVALID_ARG;
+  return launch_append(cache, L, c_new, kpe_new, slot, n, dev_err, (cudaStream_t)stream);
+}
+
+mla_status mla_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_lat, int32_t batch,
+                        int32_t heads, mla_stream_t stream) {
+  if (batch < 0 || !heads_ok(heads)) return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (!q_nope || !w_uk || !q_lat) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q_nope, 16) || !aligned(w_uk, 16) || !aligned(q_lat, 16)) return MLA_ERR_INVALID_ARG;
+  return launch_q_absorb(q_nope, w_uk, q_lat, batch, heads, (cudaStream_t)stream);
+}
+
+mla_status mla_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o, int32_t batch,
+                            int32_t heads, mla_stream_t stream) {
+  if (batch < 0 || !heads_ok(heads)) return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (!o_lat || !w_uv || !o) return MLA_ERR_INVALID_ARG;
+  if (!aligned(o_lat, 16) || !aligned(w_uv, 16) || !aligned(o, 16)) return MLA_ERR_INVALID_ARG;
+  return launch_out_unabsorb(o_lat, w_uv, o, batch, heads, (cudaStream_t)stream);
+}
+
+size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_splits) {
+  if (batch < 0 || batch > kMaxBatch || !heads_ok(heads) || num_splits < 0) return 0;
+  return (size_t)workspace_bytes(batch, heads, decode_grid(num_splits));
+}
+
+mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
+                               const uint16_t* q_pe, const int32_t* block_table,
+                               int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                               int32_t heads, float softmax_scale, int32_t num_splits,
+                               void* workspace, size_t workspace_bytes_, float* o_lat,
+                               float* lse, int32_t* dev_err, mla_stream_t stream) {
+  PageLayout L;
+  if (!cache_ok(cache, &L)) return MLA_ERR_INVALID_ARG;
+  if (batch < 0 || batch > kMaxBatch || !heads_ok(heads) || num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (max_pages <= 0 || (int64_t)max_pages * kPage > (int64_t)INT32_MAX) return MLA_ERR_INVALID_ARG;
+  if (!q_lat || !q_pe || !block_table || !seq_lens || !workspace || !o_lat) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q_lat, 16) || !aligned(q_pe, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
+      !aligned(workspace, 256) || !aligned(o_lat, 16) || (lse && !aligned(lse, 4)) ||
+      (dev_err && !aligned(dev_err, 4)))
+    return MLA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  int G = decode_grid(num_splits);
+  if ((int64_t)workspace_bytes_ < workspace_bytes(batch, heads, G)) return MLA_ERR_INVALID_ARG;
+  DecodeParams p;
+  p.pool = (const uint8_t*)cache->pool;
+  p.L = L;
+  p.latent_fmt = cache->latent_fmt;
+  p.kpe_fmt = cache->kpe_fmt;
+  p.num_pages = cache->num_pages;
+  p.q_lat = q_lat;
+  p.q_pe = q_pe;
+  p.block_table = block_table;
+  p.max_pages = max_pages;
+  p.seq_lens = seq_lens;
+  p.B = batch;
+  p.H = heads;
+  p.G = G;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.ws = carve_workspace(workspace, batch, heads, G);
+  p.o_lat = o_lat;
+  p.lse = lse;
+  p.dev_err = dev_err;
+  return launch_decode(p, (cudaStream_t)stream);
+}
+
+}  // extern "C"

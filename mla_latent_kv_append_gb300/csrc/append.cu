@@ -1,0 +1,187 @@
+// mla_cache_append: quantize-on-write of new tokens into the paged cache.
+//
+// English report "Absorbed MLA Cache Optimization on DeepSeek-V2-Lite —
+// Technical Report" §2.1 (store() quantizes compressed_kv [seq, 512] and
+// keeps k_pe [seq, 64]); Chinese report "DeepSeek-V2-Lite MLA 吸收式 KV 缓存优化"
+// §3.2 (per-channel INT8 in 32 blocks, asymmetric INT4 in 32 blocks, k_pe
+// INT8 in 8 blocks); juejin tutorial "量化压缩" (scale = absmax / 127).
+//
+// One warp per token.  Lane g owns latent group g (16 channels = 32 bytes of
+// bf16 input), so a group's absmax / min / max needs no shuffles; lanes 0..7
+// own the eight 8-channel k_pe groups.  The warp reads the token's 1152 input
+// bytes in two coalesced sweeps and writes its codes row contiguously.
+//
+// Bit-exactness: every step is an IEEE fp32 operation with round-to-nearest
+// (__fdiv_rn, __fsub_rn, __fadd_rn) or round-half-even to integer (rintf),
+// never a fused multiply-add, in the same order as the plain definition, so
+// codes, scales and zero-points equal those of any correct fp32
+// implementation bit for bit.  Denormals are kept (no flush-to-zero).
+#include "mla_internal.cuh"
+
+namespace mla {
+
+namespace {
+
+__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float* x) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = bf16lo(w[i]);
+    x[2 * i + 1] = bf16hi(w[i]);
+  }
+}
+
+// Symmetric INT8 of n values; returns the scale, writes int8 codes.
+template <int N>
+__device__ __forceinline__ float quant_sym8(const float* x, int8_t* q) {
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) a = fmaxf(a, fabsf(x[i]));
+  const float s = __fdiv_rn(a, 127.f);
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    float r = 0.f;
+    if (s > 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -127.f), 127.f);
+    q[i] = (int8_t)(int)r;
+  }
+  return s;
+}
+
+// Asymmetric INT4 of 16 values; returns scale, zero (fp32) and codes 0..15.
+__device__ __forceinline__ void quant_asym4(const float* x, float& s_out, float& z_out, uint8_t* q) {
+  float mn = x[0], mx = x[0];
+#pragma unroll
+  for (int i = 1; i < 16; ++i) {
+    mn = fminf(mn, x[i]);
+    mx = fmaxf(mx, x[i]);
+  }
+  float s = __fdiv_rn(__fsub_rn(mx, mn), 15.f);
+  if (s == 0.f) s = fabsf(mn);
+  float z = 0.f;
+  if (s > 0.f) z = rintf(__fdiv_rn(-mn, s));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float r = 0.f;
+    if (s > 0.f) r = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(x[i], s)), z), 0.f), 15.f);
+    q[i] = (uint8_t)(int)r;
+  }
+  s_out = s;
+  z_out = z;
+}
+
+template <int LF, int KF>
+__global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool, PageLayout L, int64_t num_slots,
+                                                     const uint16_t* __restrict__ c_new,
+                                                     const uint16_t* __restrict__ kpe_new,
+                                                     const int32_t* __restrict__ slot, int n,
+                                                     int32_t* dev_err) {
+  const int lane = threadIdx.x & 31;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += warps) {
+    const int32_t s = slot[i];
+    if (s == -1) continue;
+    if (s < 0 || (int64_t)s >= num_slots) {
+      if (lane == 0) set_err(dev_err, MLA_DEVERR_SLOT);
+      continue;
+    }
+    const int64_t page = s >> 6;
+    const int tok = s & 63;
+    uint8_t* pg = pool + page * L.page_bytes;
+
+    // ---- latent: lane g = group g (channels 16g .. 16g+15)
+    const uint4* src = reinterpret_cast<const uint4*>(c_new + (size_t)i * kDc) + 2 * lane;
+    const uint4 v0 = src[0], v1 = src[1];
+    if (LF == MLA_FMT_BF16) {
+      uint4* dst = reinterpret_cast<uint4*>(pg + L.codes_off + (int64_t)tok * L.codes_row) + 2 * lane;
+      dst[0] = v0;
+      dst[1] = v1;
+    } else {
+      float x[16];
+      unpack16(v0, v1, x);
+      float* scale = reinterpret_cast<float*>(pg + L.scale_off);
+      if (LF == MLA_FMT_INT8_SYM) {
+        int8_t q[16];
+        scale[lane * kPage + tok] = quant_sym8<16>(x, q);
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          w[j] = (uint32_t)(uint8_t)q[4 * j] | ((uint32_t)(uint8_t)q[4 * j + 1] << 8) |
+                 ((uint32_t)(uint8_t)q[4 * j + 2] << 16) | ((uint32_t)(uint8_t)q[4 * j + 3] << 24);
+        *reinterpret_cast<uint4*>(pg + L.codes_off + (int64_t)tok * L.codes_row + 16 * lane) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+        uint8_t q[16];
+        float sc, zp;
+        quant_asym4(x, sc, zp, q);
+        scale[lane * kPage + tok] = sc;
+        reinterpret_cast<float*>(pg + L.zero_off)[lane * kPage + tok] = zp;
+        uint32_t w[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          uint32_t v = 0;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) v |= (uint32_t)q[8 * j + k] << (4 * k);  // low nibble = even channel
+          w[j] = v;
+        }
+        *reinterpret_cast<uint2*>(pg + L.codes_off + (int64_t)tok * L.codes_row + 8 * lane) = make_uint2(w[0], w[1]);
+      }
+    }
+
+    // ---- k_pe: lanes 0..7, group = lane (channels 8g .. 8g+7)
+    if (lane < kNKG) {
+      const uint4 k = reinterpret_cast<const uint4*>(kpe_new + (size_t)i * kDr)[lane];
+      if (KF == MLA_FMT_BF16) {
+        reinterpret_cast<uint4*>(pg + L.kpe_off + (int64_t)tok * L.kpe_row)[lane] = k;
+      } else {
+        float x[8];
+        const uint32_t w[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x[2 * j] = bf16lo(w[j]);
+          x[2 * j + 1] = bf16hi(w[j]);
+        }
+        int8_t q[8];
+        reinterpret_cast<float*>(pg + L.kpe_scale_off)[lane * kPage + tok] = quant_sym8<8>(x, q);
+        const uint32_t lo = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) |
+                            ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
+        const uint32_t hi = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) |
+                            ((uint32_t)(uint8_t)q[6] << 16) | ((uint32_t)(uint8_t)q[7] << 24);
+        *reinterpret_cast<uint2*>(pg + L.kpe_off + (int64_t)tok * L.kpe_row + 8 * lane) = make_uint2(lo, hi);
+      }
+    }
+  }
+}
+
+template <int LF, int KF>
+mla_status launch_t(const mla_cache_layer* cache, const PageLayout& L, const uint16_t* c_new,
+                    const uint16_t* kpe_new, const int32_t* slot, int n, int32_t* dev_err,
+                    cudaStream_t stream) {
+  const int warps_per_block = 8;
+  int sms = device_sm_count();
+  int64_t want = ((int64_t)n + warps_per_block - 1) / warps_per_block;
+  int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 16;
+  int grid = (int)(want < cap ? want : cap);
+  append_kernel<LF, KF><<<grid, 32 * warps_per_block, 0, stream>>>(
+      (uint8_t*)cache->pool, L, (int64_t)cache->num_pages * kPage, c_new, kpe_new, slot, n, dev_err);
+  return launch_status();
+}
+
+}  // namespace
+
+mla_status launch_append(const mla_cache_layer* cache, const PageLayout& L, const uint16_t* c_new,
+                         const uint16_t* kpe_new, const int32_t* slot, int n, int32_t* dev_err,
+                         cudaStream_t stream) {
+  const int lf = cache->latent_fmt, kf = cache->kpe_fmt;
+#define MLA_APPEND_CASE(A, K) \
+  if (lf == A && kf == K) return launch_t<A, K>(cache, L, c_new, kpe_new, slot, n, dev_err, stream);
+  MLA_APPEND_CASE(MLA_FMT_BF16, MLA_FMT_BF16)
+  MLA_APPEND_CASE(MLA_FMT_BF16, MLA_FMT_INT8_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT8_SYM, MLA_FMT_BF16)
+  MLA_APPEND_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT8_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_BF16)
+  MLA_APPEND_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT8_SYM)
+#undef MLA_APPEND_CASE
+  return MLA_ERR_UNSUPPORTED;
+}
+
+}  // namespace mla

@@ -1,0 +1,393 @@
+// mla_decode_absorbed: split-K flash-decode of absorbed MLA attention over the
+// paged latent cache, followed by the log-sum-exp combine.
+//
+// What is computed (English report "Absorbed MLA Cache Optimization on
+// DeepSeek-V2-Lite — Technical Report" §2.1 get(): attention runs from the
+// cached latent; juejin tutorial "步骤2" for K_i = C^KV W_i^upK, V_i = C^KV
+// W_i^upV with the up-projections absorbed into q_lat and o_lat):
+//   s[h,t] = (q_lat[h] . c_hat[t] + q_pe[h] . kpe_hat[t]) * softmax_scale
+//   o_lat[h] = sum_t exp(s - max) c_hat[t] / sum_t exp(s - max)
+//
+// Work partition: the context of every sequence is cut into 32-token chunks;
+// the C chunks of the whole batch are divided into G contiguous ranges, one
+// per CTA along grid x (G = num SMs by default), so ragged batches stay
+// balanced.  blockIdx.y selects a tile of 16 heads.  A CTA keeps the online
+// softmax state (running max m, running sum l, unnormalised o) of the
+// sequence it is in and writes it as a partial to slot (x + b) when the
+// sequence or its range ends.  The combine kernel merges the partials of
+// each sequence.  Scores are kept in the log2 domain (scaled by log2 e).
+//
+// This translation unit holds the partition, the combine and the reference
+// decode kernel (fp32 CUDA cores, dequantized chunk in shared memory).
+#include <math.h>
+
+#include "mla_internal.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kHT = 16;          // heads per CTA
+constexpr int kThreads = 256;
+constexpr int kCS = kDc + 1;     // padded row stride of the latent chunk (floats)
+constexpr int kKS = kDr + 1;     // padded row stride of the k_pe chunk
+
+__device__ __forceinline__ int checked_len(const DecodeParams& p, int b, bool report) {
+  int len = p.seq_lens[b];
+  if (len < 0 || (int64_t)len > (int64_t)p.max_pages * kPage) {
+    if (report) set_err(p.dev_err, MLA_DEVERR_SEQLEN);
+    len = 0;
+  }
+  return len;
+}
+
+// Exclusive prefix sum of chunk counts into cum[0..B] (warp 0 of the CTA).
+__device__ void chunk_prefix(const DecodeParams& p, int32_t* cum, bool report) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    int carry = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      int v = 0;
+      if (b < p.B) v = (checked_len(p, b, report) + kChunk - 1) / kChunk;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += t;
+      }
+      if (b < p.B) cum[b + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) cum[0] = 0;
+  }
+}
+
+// Largest b with cum[b] <= c (c < cum[B]).
+__device__ __forceinline__ int seq_of_chunk(const int32_t* cum, int B, int64_t c) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= c) lo = mid; else hi = mid - 1;
+  }
+  while (lo + 1 < B && cum[lo + 1] <= c) ++lo;  // skip empty sequences
+  return lo;
+}
+
+template <int LF, int KF>
+__global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
+  extern __shared__ __align__(16) float smem[];
+  float* s_qlat = smem;                       // [16][512]
+  float* s_qpe = s_qlat + kHT * kDc;          // [16][64]
+  float* s_c = s_qpe + kHT * kDr;             // [32][513]
+  float* s_k = s_c + kChunk * kCS;            // [32][65]
+  float* s_p = s_k + kChunk * kKS;            // [16][32]
+  float* s_alpha = s_p + kHT * kChunk;        // [16]
+  float* s_m = s_alpha + kHT;                 // [16]
+  float* s_l = s_m + kHT;                     // [16]
+  int32_t* s_valid = reinterpret_cast<int32_t*>(s_l + kHT);   // [32]
+  int32_t* s_page = s_valid + kChunk;                         // [32]
+  int32_t* cum = s_page + kChunk;                             // [B + 1]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int x = blockIdx.x, G = gridDim.x, h0 = blockIdx.y * kHT;
+  const bool lead = (blockIdx.x == 0 && blockIdx.y == 0);
+
+  chunk_prefix(p, cum, lead);
+  __syncthreads();
+  if (lead)
+    for (int i = tid; i <= p.B; i += kThreads) p.ws.cum[i] = cum[i];
+
+  const int64_t C = cum[p.B];
+  int64_t c = range_lo(C, x, G);
+  const int64_t c_end = range_lo(C, x + 1, G);
+  const uint8_t* pool = p.pool;
+  const int64_t pb = p.L.page_bytes;
+
+  while (c < c_end) {
+    const int b = seq_of_chunk(cum, p.B, c);
+    const int64_t seg_end = c_end < (int64_t)cum[b + 1] ? c_end : (int64_t)cum[b + 1];
+    const int len = checked_len(p, b, false);
+    const int slot = x + b;
+
+    __syncthreads();
+    for (int i = tid; i < kHT * kDc; i += kThreads)
+      s_qlat[i] = p.q_lat[((size_t)b * p.H + h0 + i / kDc) * kDc + i % kDc];
+    for (int i = tid; i < kHT * kDr; i += kThreads)
+      s_qpe[i] = bf16f(p.q_pe[((size_t)b * p.H + h0 + i / kDr) * kDr + i % kDr]);
+    if (tid < kHT) {
+      s_m[tid] = -INFINITY;
+      s_l[tid] = 0.f;
+    }
+    float o0[kHT], o1[kHT];
+#pragma unroll
+    for (int h = 0; h < kHT; ++h) o0[h] = o1[h] = 0.f;
+
+    for (int64_t ch = c - cum[b]; ch < seg_end - cum[b]; ++ch) {
+      const int t0 = (int)ch * kChunk;
+      if (tid < kChunk) {
+        const int t = t0 + tid;
+        int valid = t < len;
+        int page = 0;
+        if (valid) {
+          page = p.block_table[(size_t)b * p.max_pages + (t >> 6)];
+          if (page < 0 || page >= p.num_pages) {
+            set_err(p.dev_err, MLA_DEVERR_PAGE);
+            valid = 0;
+          }
+        }
+        s_valid[tid] = valid;
+        s_page[tid] = page;
+      }
+      __syncthreads();
+
+      // ---- dequantize the chunk into shared memory (x_hat exactly as defined)
+      if (LF == MLA_FMT_BF16) {
+        for (int i = tid; i < kChunk * (kDc / 2); i += kThreads) {
+          const int t = i / (kDc / 2), pr = i % (kDc / 2);
+          float a = 0.f, bb = 0.f;
+          if (s_valid[t]) {
+            const uint32_t w = reinterpret_cast<const uint32_t*>(
+                pool + s_page[t] * pb + p.L.codes_off + (int64_t)((t0 + t) & 63) * p.L.codes_row)[pr];
+            a = bf16lo(w);
+            bb = bf16hi(w);
+          }
+          s_c[t * kCS + 2 * pr] = a;
+          s_c[t * kCS + 2 * pr + 1] = bb;
+        }
+      } else if (LF == MLA_FMT_INT8_SYM) {
+        for (int i = tid; i < kChunk * (kDc / 4); i += kThreads) {
+          const int t = i / (kDc / 4), wi = i % (kDc / 4);
+          float v[4] = {0.f, 0.f, 0.f, 0.f};
+          if (s_valid[t]) {
+            const uint8_t* pg = pool + s_page[t] * pb;
+            const int off = (t0 + t) & 63;
+            const uint32_t w = reinterpret_cast<const uint32_t*>(pg + p.L.codes_off + (int64_t)off * p.L.codes_row)[wi];
+            const float s = reinterpret_cast<const float*>(pg + p.L.scale_off)[(wi >> 2) * kPage + off];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), s);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) s_c[t * kCS + 4 * wi + j] = v[j];
+        }
+      } else {
+        for (int i = tid; i < kChunk * (kDc / 8); i += kThreads) {
+          const int t = i / (kDc / 8), wi = i % (kDc / 8);
+          float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (s_valid[t]) {
+            const uint8_t* pg = pool + s_page[t] * pb;
+            const int off = (t0 + t) & 63;
+            const uint32_t w = reinterpret_cast<const uint32_t*>(pg + p.L.codes_off + (int64_t)off * p.L.codes_row)[wi];
+            const int g = wi >> 1;
+            const float s = reinterpret_cast<const float*>(pg + p.L.scale_off)[g * kPage + off];
+            const float z = reinterpret_cast<const float*>(pg + p.L.zero_off)[g * kPage + off];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(__fsub_rn((float)((w >> (4 * j)) & 15u), z), s);
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) s_c[t * kCS + 8 * wi + j] = v[j];
+        }
+      }
+      if (KF == MLA_FMT_BF16) {
+        for (int i = tid; i < kChunk * (kDr / 2); i += kThreads) {
+          const int t = i / (kDr / 2), pr = i % (kDr / 2);
+          float a = 0.f, bb = 0.f;
+          if (s_valid[t]) {
+            const uint32_t w = reinterpret_cast<const uint32_t*>(
+                pool + s_page[t] * pb + p.L.kpe_off + (int64_t)((t0 + t) & 63) * p.L.kpe_row)[pr];
+            a = bf16lo(w);
+            bb = bf16hi(w);
+          }
+          s_k[t * kKS + 2 * pr] = a;
+          s_k[t * kKS + 2 * pr + 1] = bb;
+        }
+      } else {
+        for (int i = tid; i < kChunk * (kDr / 4); i += kThreads) {
+          const int t = i / (kDr / 4), wi = i % (kDr / 4);
+          float v[4] = {0.f, 0.f, 0.f, 0.f};
+          if (s_valid[t]) {
+            const uint8_t* pg = pool + s_page[t] * pb;
+            const int off = (t0 + t) & 63;
+            const uint32_t w = reinterpret_cast<const uint32_t*>(pg + p.L.kpe_off + (int64_t)off * p.L.kpe_row)[wi];
+            const float s = reinterpret_cast<const float*>(pg + p.L.kpe_scale_off)[(wi >> 1) * kPage + off];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), s);
+          }
+#pragma unroll
+          for (int j = 0; j < 4; ++j) s_k[t * kKS + 4 * wi + j] = v[j];
+        }
+      }
+      __syncthreads();
+
+      // ---- scores: thread -> head tid/16, tokens 2*(tid%16) and +1
+      {
+        const int h = tid >> 4, tp = (tid & 15) * 2;
+        const float* q = s_qlat + h * kDc;
+        const float* r0 = s_c + tp * kCS;
+        const float* r1 = r0 + kCS;
+        float a0 = 0.f, a1 = 0.f;
+        for (int i = 0; i < kDc; ++i) {
+          a0 = fmaf(q[i], r0[i], a0);
+          a1 = fmaf(q[i], r1[i], a1);
+        }
+        const float* qp = s_qpe + h * kDr;
+        const float* k0 = s_k + tp * kKS;
+        const float* k1 = k0 + kKS;
+        for (int i = 0; i < kDr; ++i) {
+          a0 = fmaf(qp[i], k0[i], a0);
+          a1 = fmaf(qp[i], k1[i], a1);
+        }
+        s_p[h * kChunk + tp] = s_valid[tp] ? a0 * p.scale_log2 : -INFINITY;
+        s_p[h * kChunk + tp + 1] = s_valid[tp + 1] ? a1 * p.scale_log2 : -INFINITY;
+      }
+      __syncthreads();
+
+      // ---- online softmax: warp w owns heads 2w, 2w+1; lane = token
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int h = 2 * warp + r;
+        const float v = s_p[h * kChunk + lane];
+        float mx = v;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_old = s_m[h];
+        const float m_new = fmaxf(m_old, mx);
+        float alpha = 1.f, pv = 0.f;
+        if (m_new != -INFINITY) {
+          alpha = exp2f(m_old - m_new);
+          pv = exp2f(v - m_new);
+        }
+        float sum = pv;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        s_p[h * kChunk + lane] = pv;
+        __syncwarp();
+        if (lane == 0) {
+          s_m[h] = m_new;
+          s_l[h] = s_l[h] * alpha + sum;
+          s_alpha[h] = alpha;
+        }
+      }
+      __syncthreads();
+
+      // ---- P V: thread owns channels tid and tid + 256 for all 16 heads
+#pragma unroll
+      for (int h = 0; h < kHT; ++h) {
+        o0[h] *= s_alpha[h];
+        o1[h] *= s_alpha[h];
+      }
+      for (int t = 0; t < kChunk; ++t) {
+        const float v0 = s_c[t * kCS + tid], v1 = s_c[t * kCS + tid + kThreads];
+#pragma unroll
+        for (int h = 0; h < kHT; ++h) {
+          const float pv = s_p[h * kChunk + t];
+          o0[h] = fmaf(pv, v0, o0[h]);
+          o1[h] = fmaf(pv, v1, o1[h]);
+        }
+      }
+    }
+
+    // ---- partial of (sequence b, this CTA) -> slot x + b
+    __syncthreads();
+    if (tid < kHT) {
+      p.ws.m[(size_t)slot * p.H + h0 + tid] = s_m[tid];
+      p.ws.l[(size_t)slot * p.H + h0 + tid] = s_l[tid];
+    }
+#pragma unroll
+    for (int h = 0; h < kHT; ++h) {
+      float* dst = p.ws.o + ((size_t)slot * p.H + h0 + h) * kDc;
+      dst[tid] = o0[h];
+      dst[tid + kThreads] = o1[h];
+    }
+    c = seg_end;
+  }
+}
+
+// Largest x in [0, G) with range_lo(C, x, G) <= c.
+__device__ __forceinline__ int owner_of_chunk(int64_t C, int G, int64_t c) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (range_lo(C, mid, G) <= c) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// grid (B, H), block 128: merge the partials of sequence b, head h.
+__global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int32_t* cum = p.ws.cum;
+  const int64_t C = cum[p.B];
+  const int64_t cs = cum[b], ce = cum[b + 1];
+  float4* out = reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc) + tid;
+  if (cs == ce) {
+    *out = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
+    return;
+  }
+  const int G = p.G;
+  const int x0 = owner_of_chunk(C, G, cs), x1 = owner_of_chunk(C, G, ce - 1);
+  float M = -INFINITY;
+  for (int x = x0; x <= x1; ++x)
+    if (range_lo(C, x, G) < range_lo(C, x + 1, G)) M = fmaxf(M, p.ws.m[(size_t)(x + b) * p.H + h]);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    for (int x = x0; x <= x1; ++x) {
+      if (range_lo(C, x, G) >= range_lo(C, x + 1, G)) continue;
+      const size_t si = (size_t)(x + b) * p.H + h;
+      const float m = p.ws.m[si];
+      if (m == -INFINITY) continue;
+      const float w = exp2f(m - M);
+      L = fmaf(w, p.ws.l[si], L);
+      const float4 v = reinterpret_cast<const float4*>(p.ws.o + si * kDc)[tid];
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+  }
+  if (L > 0.f) {
+    const float inv = 1.f / L;
+    *out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = (M + log2f(L)) * 0.69314718055994531f;
+  } else {
+    *out = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
+  }
+}
+
+template <int LF, int KF>
+mla_status launch_ref_t(const DecodeParams& p, cudaStream_t stream) {
+  const size_t smem = sizeof(float) * (kHT * kDc + kHT * kDr + kChunk * kCS + kChunk * kKS + kHT * kChunk + 3 * kHT) +
+                      sizeof(int32_t) * (2 * kChunk + p.B + 1);
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    if (cudaFuncSetAttribute(decode_ref_kernel<LF, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             200 * 1024) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  decode_ref_kernel<LF, KF><<<dim3(p.G, p.H / kHT), kThreads, smem, stream>>>(p);
+  if (launch_status() != MLA_OK) return MLA_ERR_CUDA;
+  combine_kernel<<<dim3(p.B, p.H), 128, 0, stream>>>(p);
+  return launch_status();
+}
+
+}  // namespace
+
+mla_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
+#define MLA_DECODE_CASE(A, K) \
+  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_ref_t<A, K>(p, stream);
+  MLA_DECODE_CASE(MLA_FMT_BF16, MLA_FMT_BF16)
+  MLA_DECODE_CASE(MLA_FMT_BF16, MLA_FMT_INT8_SYM)
+  MLA_DECODE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_BF16)
+  MLA_DECODE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT8_SYM)
+  MLA_DECODE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_BF16)
+  MLA_DECODE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT8_SYM)
+#undef MLA_DECODE_CASE
+  return MLA_ERR_UNSUPPORTED;
+}
+
+}  // namespace mla

@@ -1,0 +1,135 @@
+// Internal helpers shared by the library's translation units (device code and
+// host-side launch plumbing).  Not part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+
+namespace mla {
+
+constexpr int kDc = MLA_KV_LORA_RANK;      // 512 latent channels
+constexpr int kDr = MLA_ROPE_DIM;          // 64 rope channels
+constexpr int kDn = MLA_QK_NOPE_DIM;       // 128
+constexpr int kDv = MLA_V_DIM;             // 128
+constexpr int kPage = MLA_PAGE_TOKENS;     // 64 tokens per page
+constexpr int kLG = MLA_LATENT_GROUP;      // 16
+constexpr int kKG = MLA_KPE_GROUP;         // 8
+constexpr int kNLG = kDc / kLG;            // 32 latent groups
+constexpr int kNKG = kDr / kKG;            // 8 k_pe groups
+constexpr int kChunk = 32;                 // decode work unit: 32 tokens
+constexpr int kMaxBatch = 4096;
+
+// Byte layout of one page; see mla_page_layout in mla.h.
+struct PageLayout {
+  int64_t page_bytes;
+  int64_t codes_off, codes_row;
+  int64_t scale_off, zero_off;
+  int64_t kpe_off, kpe_row;
+  int64_t kpe_scale_off;
+};
+
+__host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, PageLayout* L) {
+  int64_t row;
+  switch (latent_fmt) {
+    case MLA_FMT_BF16: row = 2 * kDc; break;
+    case MLA_FMT_INT8_SYM: row = kDc; break;
+    case MLA_FMT_INT4_ASYM: row = kDc / 2; break;
+    default: return false;
+  }
+  if (kpe_fmt != MLA_FMT_BF16 && kpe_fmt != MLA_FMT_INT8_SYM) return false;
+  int64_t off = 0;
+  L->codes_off = off;
+  L->codes_row = row;
+  off += kPage * row;
+  L->scale_off = L->zero_off = -1;
+  if (latent_fmt != MLA_FMT_BF16) { L->scale_off = off; off += (int64_t)kNLG * kPage * 4; }
+  if (latent_fmt == MLA_FMT_INT4_ASYM) { L->zero_off = off; off += (int64_t)kNLG * kPage * 4; }
+  L->kpe_off = off;
+  L->kpe_row = kpe_fmt == MLA_FMT_BF16 ? 2 * kDr : kDr;
+  off += kPage * L->kpe_row;
+  L->kpe_scale_off = -1;
+  if (kpe_fmt == MLA_FMT_INT8_SYM) { L->kpe_scale_off = off; off += (int64_t)kNKG * kPage * 4; }
+  L->page_bytes = off;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 bit helpers (exact widening; rounding narrowing is RNE)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16f(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+__device__ __forceinline__ void set_err(int32_t* dev_err, int bit) {
+  if (dev_err) atomicOr(dev_err, bit);
+}
+
+// Split-K partial workspace: [cum: B+1 int32 | m: slots*H | l: slots*H | o: slots*H*512]
+struct Workspace {
+  int32_t* cum;
+  float* m;
+  float* l;
+  float* o;
+};
+
+__host__ __device__ inline int64_t align256(int64_t x) { return (x + 255) & ~(int64_t)255; }
+
+__host__ __device__ inline int64_t workspace_bytes(int B, int H, int G) {
+  int64_t slots = (int64_t)G + B;
+  return align256((int64_t)(B + 1) * 4) + 2 * align256(slots * H * 4) + slots * H * kDc * 4;
+}
+
+__host__ __device__ inline Workspace carve_workspace(void* base, int B, int H, int G) {
+  char* p = (char*)base;
+  int64_t slots = (int64_t)G + B;
+  Workspace w;
+  w.cum = (int32_t*)p;
+  p += align256((int64_t)(B + 1) * 4);
+  w.m = (float*)p;
+  p += align256(slots * H * 4);
+  w.l = (float*)p;
+  p += align256(slots * H * 4);
+  w.o = (float*)p;
+  return w;
+}
+
+// Context partition: the total C chunks (32 tokens each) of all sequences are
+// cut into G contiguous ranges, range x = [C*x/G, C*(x+1)/G).  Partials of
+// sequence b computed by CTA x go to slot x + b, which is unique because two
+// sequences share at most a boundary CTA.
+__host__ __device__ inline int64_t range_lo(int64_t C, int x, int G) { return C * x / G; }
+
+// Host side launch helpers (api.cu)
+int device_sm_count();
+mla_status launch_status();
+
+// Launchers implemented in the kernel translation units.
+mla_status launch_append(const mla_cache_layer* cache, const PageLayout& L, const uint16_t* c_new,
+                         const uint16_t* kpe_new, const int32_t* slot, int n, int32_t* dev_err,
+                         cudaStream_t stream);
+mla_status launch_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_lat, int B, int H,
+                           cudaStream_t stream);
+mla_status launch_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o, int B, int H,
+                               cudaStream_t stream);
+struct DecodeParams {
+  const uint8_t* pool;
+  PageLayout L;
+  int latent_fmt, kpe_fmt;
+  int num_pages;
+  const float* q_lat;
+  const uint16_t* q_pe;
+  const int32_t* block_table;
+  int max_pages;
+  const int32_t* seq_lens;
+  int B, H, G;
+  float scale_log2;       // softmax_scale * log2(e)
+  Workspace ws;
+  float* o_lat;
+  float* lse;
+  int32_t* dev_err;
+};
+mla_status launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+}  // namespace mla

@@ -61,7 +61,7 @@ def quantize_sym_int8(x, group):
     q = np.rint(g / safe[..., None])
     q = np.clip(q, -127, 127)
     q = np.where(live[..., None], q, F32(0))
-    return q.astype(np.int8).reshape(x.shape[0], -1), s.astype(np.float32)
+    return q.astype(np.int8).reshape(x.shape), s.astype(np.float32)
 
 
 def dequantize_sym_int8(codes, scale, group):
@@ -96,7 +96,7 @@ def quantize_asym_int4(x, group=16):
     r = np.rint(g / safe[..., None]).astype(np.float32)
     q = np.clip(r + z[..., None], 0, 15)
     q = np.where(live[..., None], q, F32(0))
-    return q.astype(np.uint8).reshape(x.shape[0], -1), s, z
+    return q.astype(np.uint8).reshape(x.shape), s, z
 
 
 def dequantize_asym_int4(codes, scale, zero, group=16):
@@ -140,7 +140,7 @@ def quantize_sym_int4(x, group=16):
     safe = np.where(live, s, F32(1)).astype(np.float32)
     q = np.clip(np.rint(g / safe[..., None]), -7, 7)
     q = np.where(live[..., None], q, F32(0))
-    return q.astype(np.int8).reshape(x.shape[0], -1), s
+    return q.astype(np.int8).reshape(x.shape), s
 
 
 def relative_error(x, x_hat):

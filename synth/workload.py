@@ -1,0 +1,124 @@
+"""GPU-resident synthetic decode workloads (tests, bench, smoke check).
+
+A workload is L layers of paged latent caches for a batch of sequences with
+given context lengths, plus per-layer weights and decode queries, all drawn
+from the seeded generator.  The first T-1 tokens of every sequence are written
+into the caches by the library's own quantize-on-write call; the decode step
+appends token T-1 and attends over all T.  Physical pages are a seeded
+permutation, so block tables are scattered as in a real pool.
+
+Host twins of every tensor come from ``synth`` (NumPy) for the oracle.
+"""
+
+import numpy as np
+import torch
+
+import synth
+import synth.device as sd
+import mla_latent_kv_append_gb300 as mla
+
+
+class Workload:
+    def __init__(self, layers, heads, seq_lens, latent_fmt, kpe_fmt, seed, device="cuda", fill=True,
+                 fill_chunk=65536):
+        self.L, self.H = int(layers), int(heads)
+        self.seq_lens = [int(t) for t in seq_lens]
+        self.B = len(self.seq_lens)
+        self.latent_fmt, self.kpe_fmt, self.seed, self.device = latent_fmt, kpe_fmt, seed, device
+        pages = [(t + 63) // 64 for t in self.seq_lens]
+        self.max_pages = max(1, max(pages) if pages else 1)
+        self.num_pages = max(1, sum(pages))
+        perm = synth.page_permutation(seed, self.num_pages)
+        bt = np.full((self.B, self.max_pages), -1, np.int32)
+        k = 0
+        for b, n in enumerate(pages):
+            bt[b, :n] = perm[k:k + n]
+            k += n
+        self.block_table_host = bt
+        self.block_table = torch.from_numpy(bt).to(device)
+        self.seq_lens_dev = torch.tensor(self.seq_lens, dtype=torch.int32, device=device)
+        self.caches = [mla.CacheLayer(self.num_pages, latent_fmt, kpe_fmt, device=device) for _ in range(self.L)]
+        self.rope = sd.RopeTables(max(1, max(self.seq_lens) if self.seq_lens else 1), device)
+        self.w_uk = [sd.w_uk(seed, l, self.H, device) for l in range(self.L)]
+        self.w_uv = [sd.w_uv(seed, l, self.H, device) for l in range(self.L)]
+        self.q_nope = [sd.q_nope(seed, l, self.B, self.H, device) for l in range(self.L)]
+        self.q_pe = [sd.q_pe(seed, l, self.B, self.H, device) for l in range(self.L)]
+        # the decode step's new token per sequence (position T-1; skipped for T == 0)
+        self.slot_new = torch.tensor([self.slot_of(b, t - 1) if t > 0 else -1 for b, t in enumerate(self.seq_lens)],
+                                     dtype=torch.int32, device=device)
+        self.c_new, self.kpe_new = [], []
+        for l in range(self.L):
+            st = sd.LayerStats(seed, l, device)
+            c = torch.zeros((self.B, synth.D_C), dtype=torch.bfloat16, device=device)
+            kk = torch.zeros((self.B, synth.D_R), dtype=torch.bfloat16, device=device)
+            for b, t in enumerate(self.seq_lens):
+                if t > 0:
+                    sd.latent_into(c[b:b + 1], seed, l, b, t - 1, st, kind=synth.KIND_NEW_LATENT)
+                    sd.kpe_into(kk[b:b + 1], seed, l, b, t - 1, self.rope, kind=synth.KIND_NEW_KPE)
+            self.c_new.append(c)
+            self.kpe_new.append(kk)
+        if fill:
+            self.fill(fill_chunk)
+
+    def slot_of(self, b, t):
+        return int(self.block_table_host[b, t // 64]) * 64 + t % 64
+
+    def slots(self, b, t0, t1):
+        t = np.arange(t0, t1)
+        return (self.block_table_host[b, t // 64].astype(np.int64) * 64 + t % 64).astype(np.int32)
+
+    def fill(self, chunk=65536):
+        """Write the T-1 context tokens of every sequence into every layer."""
+        dev = self.device
+        for l in range(self.L):
+            st = sd.LayerStats(self.seed, l, dev)
+            for b, T in enumerate(self.seq_lens):
+                for t0 in range(0, max(0, T - 1), chunk):
+                    t1 = min(T - 1, t0 + chunk)
+                    n = t1 - t0
+                    c = torch.empty((n, synth.D_C), dtype=torch.bfloat16, device=dev)
+                    k = torch.empty((n, synth.D_R), dtype=torch.bfloat16, device=dev)
+                    sd.latent_into(c, self.seed, l, b, t0, st)
+                    sd.kpe_into(k, self.seed, l, b, t0, self.rope)
+                    slot = torch.from_numpy(self.slots(b, t0, t1)).to(dev)
+                    mla.mla_cache_append(self.caches[l], c, k, slot)
+
+    # ---- host twins for the oracle -------------------------------------------------
+    def host_sequence(self, layer, b):
+        """bf16 bits of all T tokens of sequence b (context + appended token)."""
+        T = self.seq_lens[b]
+        cos, sin = synth.rope_tables(max(1, T))
+        return synth.sequence_bf16(self.seed, layer, b, T, cos, sin, stats=synth.channel_stats(self.seed, layer))
+
+    def host_query(self, layer):
+        return (synth.q_nope_bf16(self.seed, layer, self.B, self.H), synth.q_pe_bf16(self.seed, layer, self.B, self.H),
+                synth.w_uk_bf16(self.seed, layer, self.H), synth.w_uv_bf16(self.seed, layer, self.H))
+
+
+class DecodeStep:
+    """Buffers and the per-layer call sequence of one decode step:
+    append -> absorb -> decode (+combine) -> unabsorb, for every layer."""
+
+    def __init__(self, wl, num_splits=0, with_lse=True):
+        dev = wl.device
+        self.wl, self.num_splits = wl, num_splits
+        self.q_lat = torch.empty((wl.B, wl.H, synth.D_C), dtype=torch.float32, device=dev)
+        self.o_lat = torch.empty((wl.B, wl.H, synth.D_C), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((wl.L, wl.B, wl.H), dtype=torch.float32, device=dev) if with_lse else None
+        self.o = torch.empty((wl.L, wl.B, wl.H, synth.D_V), dtype=torch.float32, device=dev)
+        nbytes = mla.mla_decode_workspace_bytes(wl.B, wl.H, num_splits)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(self, keep_o_lat=None):
+        wl = self.wl
+        for l in range(wl.L):
+            mla.mla_cache_append(wl.caches[l], wl.c_new[l], wl.kpe_new[l], wl.slot_new, self.dev_err)
+            mla.mla_q_absorb(wl.q_nope[l], wl.w_uk[l], self.q_lat)
+            mla.mla_decode_absorbed(wl.caches[l], self.q_lat, wl.q_pe[l], wl.block_table, wl.seq_lens_dev,
+                                    self.workspace, self.o_lat, None if self.lse is None else self.lse[l],
+                                    self.dev_err, num_splits=self.num_splits)
+            if keep_o_lat is not None:
+                keep_o_lat[l].copy_(self.o_lat)
+            mla.mla_out_unabsorb(self.o_lat, wl.w_uv[l], self.o[l])
+        return self.o

@@ -1,0 +1,90 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/mla.h declares, computes layouts and sizes, and rejects bad arguments
+on the host before any launch (no kernel runs in these tests)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    try:
+        __graft_entry__.build()
+    except RuntimeError as e:  # pragma: no cover - needs nvcc
+        pytest.skip("cannot build: %s" % e)
+    import mla_latent_kv_append_gb300 as mla
+    return mla
+
+
+def declared_functions():
+    src = open(HEADER, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+    assert lib.abi_version() == 100
+
+
+def test_layouts_match_the_accounting(lib):
+    from oracle import accounting as acc
+    for lf in (0, 1, 2):
+        for kf in (0, 1):
+            L = lib.mla_cache_page_layout(lf, kf)
+            assert L.page_bytes == 64 * acc.layer_bytes(lf, kf, metadata=True)
+            for off in (L.codes_off, L.scale_off, L.zero_off, L.kpe_off, L.kpe_scale_off):
+                assert off == -1 or off % 256 == 0
+    assert lib.mla_cache_pool_bytes(10, 1, 1) == 10 * 64 * 736
+    assert lib.mla_cache_pool_bytes(0, 1, 1) == 0
+    assert lib.mla_cache_pool_bytes(4, 3, 1) == 0
+    assert lib.mla_cache_pool_bytes(4, 1, 2) == 0     # INT4 k_pe is not a cache format
+
+
+def test_workspace_size(lib):
+    # explicit split count: no device query needed
+    G, B, H = 10, 3, 16
+    slots = G + B
+    align = lambda x: (x + 255) // 256 * 256
+    expect = align((B + 1) * 4) + 2 * align(slots * H * 4) + slots * H * 512 * 4
+    assert lib.mla_decode_workspace_bytes(B, H, G) == expect
+    assert lib.mla_decode_workspace_bytes(B, 24, G) == 0
+    assert lib.mla_decode_workspace_bytes(5000, 16, G) == 0
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    raw = lib.lib
+    fake = ctypes.c_void_p(0x10000)          # never dereferenced: checks fail first
+    cs = lib._CacheLayer(4, 1, 1, 0, 0x100000)
+    # n < 0
+    assert raw.mla_cache_append(ctypes.byref(cs), fake, fake, fake, -1, None, None) == 1
+    # misaligned c_new
+    assert raw.mla_cache_append(ctypes.byref(cs), ctypes.c_void_p(0x10002), fake, fake, 4, None, None) == 1
+    # bad pool alignment
+    bad = lib._CacheLayer(4, 1, 1, 0, 0x100010)
+    assert raw.mla_cache_append(ctypes.byref(bad), fake, fake, fake, 4, None, None) == 1
+    # heads not a multiple of 16
+    assert raw.mla_q_absorb(fake, fake, fake, 2, 24, None) == 1
+    assert raw.mla_out_unabsorb(fake, fake, fake, 2, 8, None) == 1
+    # n == 0 / batch == 0 are no-ops that launch nothing
+    assert raw.mla_cache_append(ctypes.byref(cs), None, None, None, 0, None, None) == 0
+    assert raw.mla_q_absorb(None, None, None, 0, 16, None) == 0
+    # decode: workspace too small, bad softmax scale, batch too large
+    args = lambda ws_bytes, scale, B: (ctypes.byref(cs), fake, fake, fake, 4, fake, B, 16, scale, 3,
+                                       ctypes.c_void_p(0x200000), ws_bytes, fake, None, None, None)
+    assert raw.mla_decode_absorbed(*args(16, 0.07, 2)) == 1
+    assert raw.mla_decode_absorbed(*args(1 << 30, 0.0, 2)) == 1
+    assert raw.mla_decode_absorbed(*args(1 << 30, 0.07, 5000)) == 1
+    assert raw.mla_decode_absorbed(*args(1 << 30, 0.07, 0)) == 0
+    assert raw.mla_status_string(4) == b"device-side bounds error"

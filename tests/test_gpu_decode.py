@@ -1,0 +1,94 @@
+"""mla_decode_absorbed (with the full per-layer step: append -> absorb ->
+decode -> unabsorb) on the GPU against the oracle: max relative error 2e-3
+per row of o_lat and o, lse within 2e-3 absolute, on the same codes."""
+
+import numpy as np
+import pytest
+import torch
+
+import mla_latent_kv_append_gb300 as mla
+from oracle import attention as A
+from synth.workload import DecodeStep, Workload
+from tests._helpers import ALL_FORMATS, ATTN_TOL, FMT_NAME, OracleCache
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_check(wl, num_splits=0, layers=None, seqs=None, tol=ATTN_TOL):
+    step = DecodeStep(wl, num_splits=num_splits)
+    keep = torch.empty((wl.L, wl.B, wl.H, 512), dtype=torch.float32, device="cuda")
+    o = step.run(keep_o_lat=keep)
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0
+    oc = OracleCache(wl)
+    o_h, ol_h, lse_h = o.cpu().numpy(), keep.cpu().numpy(), step.lse.cpu().numpy()
+    worst = 0.0
+    for l in (layers if layers is not None else range(wl.L)):
+        for b in (seqs if seqs is not None else range(wl.B)):
+            _, ol_ref, lse_ref, o_ref = oc.decode(l, b)
+            if wl.seq_lens[b] == 0:
+                assert np.all(ol_h[l, b] == 0) and np.all(o_h[l, b] == 0) and np.all(np.isneginf(lse_h[l, b]))
+                continue
+            e1 = A.max_rel_error(ol_h[l, b], ol_ref)
+            e2 = A.max_rel_error(o_h[l, b], o_ref)
+            e3 = float(np.max(np.abs(lse_h[l, b] - lse_ref)))
+            worst = max(worst, e1, e2)
+            assert e1 < tol and e2 < tol and e3 < tol, (l, b, e1, e2, e3)
+    return o_h, worst
+
+
+@pytest.mark.parametrize("lf,kf", ALL_FORMATS, ids=["%s-%s" % (FMT_NAME[a], FMT_NAME[b]) for a, b in ALL_FORMATS])
+def test_tiny_config(lf, kf):
+    """1 layer, 16 heads, batch 1, context 256 (paged, 64-token pages)."""
+    wl = Workload(1, 16, [256], lf, kf, seed=0x4D4C41)
+    run_and_check(wl)
+
+
+@pytest.mark.parametrize("lf", [mla.FMT_BF16, mla.FMT_INT8_SYM, mla.FMT_INT4_ASYM])
+def test_ragged_batch_edges(lf):
+    """Context lengths around page and chunk boundaries, plus an empty sequence."""
+    lens = [1, 31, 32, 33, 63, 64, 65, 100, 0, 257, 129]
+    wl = Workload(1, 16, lens, lf, mla.FMT_INT8_SYM, seed=77)
+    run_and_check(wl)
+
+
+def test_split_invariance_and_counts():
+    lens = [700, 5, 1300, 64, 2049]
+    wl = Workload(2, 16, lens, mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, seed=78)
+    outs = []
+    for ns in (1, 2, 3, 7, 40, 0, 400):
+        o, _ = run_and_check(wl, num_splits=ns, layers=[1])
+        outs.append(o)
+    for o in outs[1:]:
+        assert A.max_rel_error(o, outs[0]) < 1e-5
+
+
+def test_64_heads_mixed_lengths():
+    wl = Workload(1, 64, [1000, 37, 2500], mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, seed=79)
+    run_and_check(wl)
+
+
+def test_int4_longer_context():
+    wl = Workload(1, 16, [4096, 3000], mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM, seed=80)
+    run_and_check(wl)
+
+
+def test_bad_page_and_bad_length_are_flagged_not_faulted():
+    wl = Workload(1, 16, [200, 100], mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, seed=81)
+    step = DecodeStep(wl)
+    step.run()
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0
+    # corrupt one block-table entry of sequence 0, and make sequence 1 too long
+    bt = wl.block_table.clone()
+    bt[0, 1] = wl.num_pages + 5
+    lens = wl.seq_lens_dev.clone()
+    lens[1] = wl.max_pages * 64 + 1
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_decode_absorbed(wl.caches[0], step.q_lat, wl.q_pe[0], bt, lens, step.workspace, step.o_lat,
+                            step.lse[0], err)
+    torch.cuda.synchronize()
+    assert err.item() == mla.DEVERR_PAGE | mla.DEVERR_SEQLEN
+    ol = step.o_lat.cpu().numpy()
+    assert np.all(np.isfinite(ol))
+    assert np.all(ol[1] == 0) and np.all(np.isneginf(step.lse[0, 1].cpu().numpy()))
