@@ -105,20 +105,34 @@ typedef struct {
 } mla_cache_layer;
 
 /*
- * Byte layout of one page (structure of arrays; every field starts on a
- * 256-byte boundary so that one bulk copy can fetch it).  Offsets are from
- * the page start; -1 marks a field the format does not have.
- *   codes      [64 tokens][codes_row_bytes]: bf16 values (1024 B), int8
- *              codes (512 B), or 4-bit codes two per byte, low nibble = even
- *              channel (256 B).
- *   scale      fp32 [32 groups][64 tokens]   (int8 / int4 latent)
- *   zero       fp32 [32 groups][64 tokens]   (int4 latent; integer-valued)
- *   kpe        [64 tokens][kpe_row_bytes]: bf16 (128 B) or int8 codes (64 B)
- *   kpe_scale  fp32 [8 groups][64 tokens]    (int8 k_pe)
- * page_bytes = 64 x (1152, 736 or 608) for bf16/bf16, int8/int8, int4/int8.
+ * Byte layout of one page.  A page of 64 tokens is two contiguous blocks of
+ * 32 tokens (token t of a page lives in block t / 32 as block token
+ * u = t % 32), so that one bulk copy moves a whole 32-token work unit.
+ * Inside a block, structure of arrays; offsets are from the block start,
+ * every field starts on a 256-byte boundary, -1 marks a field the format
+ * does not have:
+ *   codes      [32][codes_row_bytes]: bf16 values (1024 B), int8 codes
+ *              (512 B) or 4-bit codes (256 B).  The row is a sequence of
+ *              16-byte chunks; logical chunk c of block token u is stored at
+ *              chunk position (c & ~7) | ((c ^ u) & 7).  An int8 chunk is one
+ *              16-channel group in channel order; a bf16 chunk is 8 channels.
+ *              An int4 chunk c holds groups A = 2c and B = 2c + 1; its 32-bit
+ *              word j (j = 0..3) packs, from the least significant nibble,
+ *              A[4j], A[4j+2], B[4j], B[4j+2], A[4j+1], A[4j+3], B[4j+1],
+ *              B[4j+3] (X[i] = code of channel i of group X).
+ *   scale      fp32 [32 groups][32 block tokens]   (int8 / int4 latent)
+ *   zero       fp32 [32 groups][32 block tokens]   (int4 latent; integer-valued)
+ *   kpe        [32][kpe_row_bytes]: bf16 (128 B = 8 chunks of 8 channels,
+ *              chunk c of token u at position c ^ (u & 7)) or int8 (64 B =
+ *              4 chunks of two 8-channel groups, chunk c at c ^ ((u >> 1) & 3))
+ *   kpe_scale  fp32 [8 groups][32 block tokens]    (int8 k_pe)
+ * page_bytes = 2 * block_bytes = 64 x (1152, 736 or 608) bytes for
+ * bf16/bf16, int8/int8 and int4/int8.  The swizzles spread the rows of eight
+ * consecutive tokens over all shared-memory banks when a block is copied
+ * verbatim into shared memory.
  */
 typedef struct {
-  int64_t page_bytes;
+  int64_t page_bytes, block_bytes;
   int64_t codes_off, codes_row_bytes;
   int64_t scale_off, zero_off;
   int64_t kpe_off, kpe_row_bytes;
@@ -209,6 +223,10 @@ mla_status mla_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o,
 
 /* Static string for a status code. */
 const char* mla_status_string(mla_status status);
+
+/* Text of the CUDA error behind the calling thread's most recent
+ * MLA_ERR_CUDA ("no error" if none); a static string, not to be freed. */
+const char* mla_last_cuda_error(void);
 
 /* ABI version (major * 100 + minor). */
 int32_t mla_abi_version(void);

@@ -38,8 +38,9 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error", 4: 
 
 
 class MlaError(RuntimeError):
-    def __init__(self, fn, status):
-        super().__init__("%s failed: %s (status %d)" % (fn, STATUS.get(status, "?"), status))
+    def __init__(self, fn, status, detail=""):
+        super().__init__("%s failed: %s (status %d)%s" % (fn, STATUS.get(status, "?"), status,
+                                                         ": " + detail if detail else ""))
         self.status = status
 
 
@@ -49,14 +50,15 @@ class _CacheLayer(ctypes.Structure):
 
 
 class PageLayout(ctypes.Structure):
-    _fields_ = [("page_bytes", ctypes.c_int64), ("codes_off", ctypes.c_int64), ("codes_row_bytes", ctypes.c_int64),
+    _fields_ = [("page_bytes", ctypes.c_int64), ("block_bytes", ctypes.c_int64), ("codes_off", ctypes.c_int64),
+                ("codes_row_bytes", ctypes.c_int64),
                 ("scale_off", ctypes.c_int64), ("zero_off", ctypes.c_int64), ("kpe_off", ctypes.c_int64),
                 ("kpe_row_bytes", ctypes.c_int64), ("kpe_scale_off", ctypes.c_int64)]
 
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError("libmla_gb300.so is not built: run `python -m mla_latent_kv_append_gb300.build` "
+        raise ImportError("libmla_gb300.so is not built: run `python mla_latent_kv_append_gb300/build.py` "
                           "(or __graft_entry__.build()) on a machine with nvcc")
     lib = ctypes.CDLL(LIB_PATH)
     P, I32, SZ, F32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
@@ -64,6 +66,7 @@ def _load():
     sig = {
         "mla_abi_version": (I32, []),
         "mla_status_string": (ctypes.c_char_p, [I32]),
+        "mla_last_cuda_error": (ctypes.c_char_p, []),
         "mla_cache_page_layout": (I32, [CP, ctypes.POINTER(PageLayout)]),
         "mla_cache_pool_bytes": (SZ, [CP]),
         "mla_cache_append": (I32, [CP, P, P, P, I32, P, P]),
@@ -93,7 +96,8 @@ def _stream(stream=None):
 
 def _check(fn, status):
     if status != 0:
-        raise MlaError(fn, status)
+        detail = lib.mla_last_cuda_error().decode() if status == 3 else ""
+        raise MlaError(fn, status, detail)
 
 
 def _need(t, dtype, shape, name):

@@ -1,6 +1,6 @@
 """Build the CUDA shared libraries in-tree with nvcc (sm_103a only).
 
-    python -m mla_latent_kv_append_gb300.build          # library + synth generator
+    python mla_latent_kv_append_gb300/build.py          # library + synth generator
 
 Translation units compile in parallel, then link into
 ``mla_latent_kv_append_gb300/libmla_gb300.so`` and ``synth/libmla_synth.so``.

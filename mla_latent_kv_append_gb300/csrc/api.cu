@@ -17,9 +17,15 @@ int device_sm_count() {
   return n;
 }
 
-mla_status launch_status() {
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+static thread_local const char* g_last_cuda_error = "no error";
+
+mla_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MLA_OK;
+  g_last_cuda_error = cudaGetErrorString(e);
+  return MLA_ERR_CUDA;
 }
+
+mla_status launch_status() { return cuda_status(cudaGetLastError()); }
 
 static bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
@@ -45,6 +51,8 @@ extern "C" {
 
 int32_t mla_abi_version(void) { return 100; }
 
+const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
+
 const char* mla_status_string(mla_status s) {
   switch (s) {
     case MLA_OK: return "ok";
@@ -61,6 +69,7 @@ mla_status mla_cache_page_layout(const mla_cache_layer* cache, mla_page_layout* 
   PageLayout L;
   if (!compute_layout(cache->latent_fmt, cache->kpe_fmt, &L)) return MLA_ERR_INVALID_ARG;
   out->page_bytes = L.page_bytes;
+  out->block_bytes = L.block_bytes;
   out->codes_off = L.codes_off;
   out->codes_row_bytes = L.codes_row;
   out->scale_off = L.scale_off;

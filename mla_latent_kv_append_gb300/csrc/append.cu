@@ -9,7 +9,9 @@
 // One warp per token.  Lane g owns latent group g (16 channels = 32 bytes of
 // bf16 input), so a group's absmax / min / max needs no shuffles; lanes 0..7
 // own the eight 8-channel k_pe groups.  The warp reads the token's 1152 input
-// bytes in two coalesced sweeps and writes its codes row contiguously.
+// bytes in two coalesced sweeps and writes its code row (512 contiguous bytes
+// for INT8) in the page's chunk order: 16-byte chunks swizzled by token, INT4
+// nibbles of two groups interleaved per chunk (see mla_internal.cuh).
 //
 // Bit-exactness: every step is an IEEE fp32 operation with round-to-nearest
 // (__fdiv_rn, __fsub_rn, __fadd_rn) or round-half-even to integer (rintf),
@@ -85,53 +87,59 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
       continue;
     }
     const int64_t page = s >> 6;
-    const int tok = s & 63;
-    uint8_t* pg = pool + page * L.page_bytes;
+    const int t = s & 31;                       // token within its 32-token block
+    uint8_t* blk = pool + page * L.page_bytes + ((s >> 5) & 1) * L.block_bytes;
 
     // ---- latent: lane g = group g (channels 16g .. 16g+15)
     const uint4* src = reinterpret_cast<const uint4*>(c_new + (size_t)i * kDc) + 2 * lane;
     const uint4 v0 = src[0], v1 = src[1];
+    uint8_t* row = blk + L.codes_off + (int64_t)t * L.codes_row;
     if (LF == MLA_FMT_BF16) {
-      uint4* dst = reinterpret_cast<uint4*>(pg + L.codes_off + (int64_t)tok * L.codes_row) + 2 * lane;
-      dst[0] = v0;
-      dst[1] = v1;
+      reinterpret_cast<uint4*>(row)[latent_chunk_pos(2 * lane, t)] = v0;
+      reinterpret_cast<uint4*>(row)[latent_chunk_pos(2 * lane + 1, t)] = v1;
     } else {
       float x[16];
       unpack16(v0, v1, x);
-      float* scale = reinterpret_cast<float*>(pg + L.scale_off);
+      float* scale = reinterpret_cast<float*>(blk + L.scale_off);
       if (LF == MLA_FMT_INT8_SYM) {
         int8_t q[16];
-        scale[lane * kPage + tok] = quant_sym8<16>(x, q);
+        scale[lane * kBlockTokens + t] = quant_sym8<16>(x, q);
         uint32_t w[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           w[j] = (uint32_t)(uint8_t)q[4 * j] | ((uint32_t)(uint8_t)q[4 * j + 1] << 8) |
                  ((uint32_t)(uint8_t)q[4 * j + 2] << 16) | ((uint32_t)(uint8_t)q[4 * j + 3] << 24);
-        *reinterpret_cast<uint4*>(pg + L.codes_off + (int64_t)tok * L.codes_row + 16 * lane) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        reinterpret_cast<uint4*>(row)[latent_chunk_pos(lane, t)] = make_uint4(w[0], w[1], w[2], w[3]);
       } else {
         uint8_t q[16];
         float sc, zp;
         quant_asym4(x, sc, zp, q);
-        scale[lane * kPage + tok] = sc;
-        reinterpret_cast<float*>(pg + L.zero_off)[lane * kPage + tok] = zp;
-        uint32_t w[2];
+        scale[lane * kBlockTokens + t] = sc;
+        reinterpret_cast<float*>(blk + L.zero_off)[lane * kBlockTokens + t] = zp;
+        // this lane's nibbles of the shared chunk (groups 2c and 2c+1), then
+        // merge with the partner lane's
+        uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < 4; ++j) {
           uint32_t v = 0;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) v |= (uint32_t)q[8 * j + k] << (4 * k);  // low nibble = even channel
-          w[j] = v;
+          for (int k = 0; k < 8; ++k) {
+            const int ch = int4_nibble_channel(j, k);
+            if ((ch >> 4) == (lane & 1)) v |= (uint32_t)q[ch & 15] << (4 * k);
+          }
+          w[j] = v | __shfl_xor_sync(0xffffffffu, v, 1);
         }
-        *reinterpret_cast<uint2*>(pg + L.codes_off + (int64_t)tok * L.codes_row + 8 * lane) = make_uint2(w[0], w[1]);
+        if ((lane & 1) == 0)
+          reinterpret_cast<uint4*>(row)[latent_chunk_pos(lane >> 1, t)] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
 
     // ---- k_pe: lanes 0..7, group = lane (channels 8g .. 8g+7)
     if (lane < kNKG) {
       const uint4 k = reinterpret_cast<const uint4*>(kpe_new + (size_t)i * kDr)[lane];
+      uint8_t* krow = blk + L.kpe_off + (int64_t)t * L.kpe_row;
       if (KF == MLA_FMT_BF16) {
-        reinterpret_cast<uint4*>(pg + L.kpe_off + (int64_t)tok * L.kpe_row)[lane] = k;
+        reinterpret_cast<uint4*>(krow)[kpe_chunk_pos(lane, t, true)] = k;
       } else {
         float x[8];
         const uint32_t w[4] = {k.x, k.y, k.z, k.w};
@@ -141,12 +149,13 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
           x[2 * j + 1] = bf16hi(w[j]);
         }
         int8_t q[8];
-        reinterpret_cast<float*>(pg + L.kpe_scale_off)[lane * kPage + tok] = quant_sym8<8>(x, q);
+        reinterpret_cast<float*>(blk + L.kpe_scale_off)[lane * kBlockTokens + t] = quant_sym8<8>(x, q);
         const uint32_t lo = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) |
                             ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
         const uint32_t hi = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) |
                             ((uint32_t)(uint8_t)q[6] << 16) | ((uint32_t)(uint8_t)q[7] << 24);
-        *reinterpret_cast<uint2*>(pg + L.kpe_off + (int64_t)tok * L.kpe_row + 8 * lane) = make_uint2(lo, hi);
+        *reinterpret_cast<uint2*>(krow + kpe_chunk_pos(lane >> 1, t, false) * 16 + (lane & 1) * 8) =
+            make_uint2(lo, hi);
       }
     }
   }

@@ -20,6 +20,7 @@
 // This translation unit holds the partition, the combine and the reference
 // decode kernel (fp32 CUDA cores, dequantized chunk in shared memory).
 #include <math.h>
+#include <stdlib.h>
 
 #include "mla_internal.cuh"
 
@@ -140,14 +141,17 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
       }
       __syncthreads();
 
-      // ---- dequantize the chunk into shared memory (x_hat exactly as defined)
+      // ---- dequantize the chunk into shared memory (x_hat exactly as defined).
+      // A chunk is one 32-token block of a page; t is the token in the block.
+      const int64_t blk_off = (int64_t)((t0 >> 5) & 1) * p.L.block_bytes;
       if (LF == MLA_FMT_BF16) {
         for (int i = tid; i < kChunk * (kDc / 2); i += kThreads) {
           const int t = i / (kDc / 2), pr = i % (kDc / 2);
           float a = 0.f, bb = 0.f;
           if (s_valid[t]) {
             const uint32_t w = reinterpret_cast<const uint32_t*>(
-                pool + s_page[t] * pb + p.L.codes_off + (int64_t)((t0 + t) & 63) * p.L.codes_row)[pr];
+                pool + s_page[t] * pb + blk_off + p.L.codes_off + (int64_t)t * p.L.codes_row)[
+                latent_chunk_pos(pr >> 2, t) * 4 + (pr & 3)];
             a = bf16lo(w);
             bb = bf16hi(w);
           }
@@ -159,10 +163,10 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
           const int t = i / (kDc / 4), wi = i % (kDc / 4);
           float v[4] = {0.f, 0.f, 0.f, 0.f};
           if (s_valid[t]) {
-            const uint8_t* pg = pool + s_page[t] * pb;
-            const int off = (t0 + t) & 63;
-            const uint32_t w = reinterpret_cast<const uint32_t*>(pg + p.L.codes_off + (int64_t)off * p.L.codes_row)[wi];
-            const float s = reinterpret_cast<const float*>(pg + p.L.scale_off)[(wi >> 2) * kPage + off];
+            const uint8_t* blk = pool + s_page[t] * pb + blk_off;
+            const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.codes_off + (int64_t)t * p.L.codes_row)[
+                latent_chunk_pos(wi >> 2, t) * 4 + (wi & 3)];
+            const float s = reinterpret_cast<const float*>(blk + p.L.scale_off)[(wi >> 2) * kBlockTokens + t];
 #pragma unroll
             for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), s);
           }
@@ -171,20 +175,23 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
         }
       } else {
         for (int i = tid; i < kChunk * (kDc / 8); i += kThreads) {
-          const int t = i / (kDc / 8), wi = i % (kDc / 8);
+          const int t = i / (kDc / 8), pw = i % (kDc / 8);
+          const int c = latent_chunk_pos(pw >> 2, t), j = pw & 3;   // logical chunk of this stored word
           float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
           if (s_valid[t]) {
-            const uint8_t* pg = pool + s_page[t] * pb;
-            const int off = (t0 + t) & 63;
-            const uint32_t w = reinterpret_cast<const uint32_t*>(pg + p.L.codes_off + (int64_t)off * p.L.codes_row)[wi];
-            const int g = wi >> 1;
-            const float s = reinterpret_cast<const float*>(pg + p.L.scale_off)[g * kPage + off];
-            const float z = reinterpret_cast<const float*>(pg + p.L.zero_off)[g * kPage + off];
+            const uint8_t* blk = pool + s_page[t] * pb + blk_off;
+            const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.codes_off + (int64_t)t * p.L.codes_row)[pw];
+            const float* sc = reinterpret_cast<const float*>(blk + p.L.scale_off);
+            const float* zp = reinterpret_cast<const float*>(blk + p.L.zero_off);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(__fsub_rn((float)((w >> (4 * j)) & 15u), z), s);
+            for (int k = 0; k < 8; ++k) {
+              const int g = 2 * c + (int4_nibble_channel(j, k) >> 4);
+              v[k] = __fmul_rn(__fsub_rn((float)((w >> (4 * k)) & 15u), zp[g * kBlockTokens + t]),
+                               sc[g * kBlockTokens + t]);
+            }
           }
 #pragma unroll
-          for (int j = 0; j < 8; ++j) s_c[t * kCS + 8 * wi + j] = v[j];
+          for (int k = 0; k < 8; ++k) s_c[t * kCS + 32 * c + int4_nibble_channel(j, k)] = v[k];
         }
       }
       if (KF == MLA_FMT_BF16) {
@@ -193,7 +200,8 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
           float a = 0.f, bb = 0.f;
           if (s_valid[t]) {
             const uint32_t w = reinterpret_cast<const uint32_t*>(
-                pool + s_page[t] * pb + p.L.kpe_off + (int64_t)((t0 + t) & 63) * p.L.kpe_row)[pr];
+                pool + s_page[t] * pb + blk_off + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[
+                kpe_chunk_pos(pr >> 2, t, true) * 4 + (pr & 3)];
             a = bf16lo(w);
             bb = bf16hi(w);
           }
@@ -205,10 +213,10 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
           const int t = i / (kDr / 4), wi = i % (kDr / 4);
           float v[4] = {0.f, 0.f, 0.f, 0.f};
           if (s_valid[t]) {
-            const uint8_t* pg = pool + s_page[t] * pb;
-            const int off = (t0 + t) & 63;
-            const uint32_t w = reinterpret_cast<const uint32_t*>(pg + p.L.kpe_off + (int64_t)off * p.L.kpe_row)[wi];
-            const float s = reinterpret_cast<const float*>(pg + p.L.kpe_scale_off)[(wi >> 1) * kPage + off];
+            const uint8_t* blk = pool + s_page[t] * pb + blk_off;
+            const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[
+                kpe_chunk_pos(wi >> 2, t, false) * 4 + (wi & 3)];
+            const float s = reinterpret_cast<const float*>(blk + p.L.kpe_scale_off)[(wi >> 1) * kBlockTokens + t];
 #pragma unroll
             for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), s);
           }
@@ -364,20 +372,16 @@ mla_status launch_ref_t(const DecodeParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !configured[dev]) {
-    if (cudaFuncSetAttribute(decode_ref_kernel<LF, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             200 * 1024) != cudaSuccess)
-      return MLA_ERR_CUDA;
+    const mla_status st = cuda_status(
+        cudaFuncSetAttribute(decode_ref_kernel<LF, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+    if (st != MLA_OK) return st;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
   decode_ref_kernel<LF, KF><<<dim3(p.G, p.H / kHT), kThreads, smem, stream>>>(p);
-  if (launch_status() != MLA_OK) return MLA_ERR_CUDA;
-  combine_kernel<<<dim3(p.B, p.H), 128, 0, stream>>>(p);
   return launch_status();
 }
 
-}  // namespace
-
-mla_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
+mla_status launch_decode_ref(const DecodeParams& p, cudaStream_t stream) {
 #define MLA_DECODE_CASE(A, K) \
   if (p.latent_fmt == A && p.kpe_fmt == K) return launch_ref_t<A, K>(p, stream);
   MLA_DECODE_CASE(MLA_FMT_BF16, MLA_FMT_BF16)
@@ -388,6 +392,17 @@ mla_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
   MLA_DECODE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT8_SYM)
 #undef MLA_DECODE_CASE
   return MLA_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+mla_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
+  static const bool force_ref = getenv("MLA_DEBUG_REFERENCE_DECODE") != nullptr;
+  mla_status st = force_ref ? MLA_ERR_UNSUPPORTED : launch_decode_mma(p, stream);
+  if (st == MLA_ERR_UNSUPPORTED) st = launch_decode_ref(p, stream);
+  if (st != MLA_OK) return st;
+  combine_kernel<<<dim3(p.B, p.H), 128, 0, stream>>>(p);
+  return launch_status();
 }
 
 }  // namespace mla

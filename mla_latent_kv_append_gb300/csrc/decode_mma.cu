@@ -1,0 +1,811 @@
+// Tensor-core split-K decode kernel for mla_decode_absorbed (sm_103a).
+//
+// Computes, for a tile of 16 heads and the 32-token chunks of the CTA's share
+// of the batch (same partition and partial-slot scheme as decode.cu), the
+// online-softmax partials of
+//   s[h,t] = (q_lat[h] . c_hat[t] + q_pe[h] . kpe_hat[t]) * softmax_scale
+//   o[h]   = sum_t exp(s - m) c_hat[t]
+// (English report "Absorbed MLA Cache Optimization on DeepSeek-V2-Lite —
+// Technical Report" §2.1: attention straight from the cached latent; juejin
+// tutorial "步骤2" for the absorbed up-projections).
+//
+// Structure (one CTA per SM, 8 warps):
+//  * Thread 0 streams 32-token blocks (one contiguous bulk copy each,
+//    cp.async.bulk into a ring of shared-memory stages, mbarrier-signalled).
+//    A stage is refilled as soon as every warp has passed the score-exchange
+//    barrier of the chunk it held, which orders all reads of it before the
+//    refill; no separate producer warp is needed, which leaves each thread
+//    the registers of two warps per scheduler.
+//  * Consumer warp w owns latent groups 4w..4w+3 (64 channels) and k_pe
+//    group w.  Each code byte is read from shared memory once (ldmatrix) and
+//    turned into exact fp16 integers; the same registers serve QK^T and,
+//    after dequantization and a movmatrix transpose, PV.
+//  * QK^T per 16-channel group: mma.m16n8k16 (M = 16 heads, N = 8 tokens,
+//    K = the group's 16 channels) of q_lat split into fp16 hi + lo against
+//    the exact integer codes (INT4: the -z * sum(q_lat) zero-point term
+//    enters through the MMA's C operand), then one fp32 FMA per element
+//    applies the group's per-token scale.  This keeps every product exact, which the
+//    2e-3 bound needs: scores here have a spread of ~10, so a rounding of the
+//    latent or the query to 11 bits would already cost ~1e-3.
+//  * The partial scores of the 8 warps are summed through shared memory by
+//    256 threads (16 per head row), which also run the online softmax (max /
+//    sum with warp shuffles over the row's 16 threads) and publish P in fp16.
+//  * PV: o[16 heads][the warp's 64 channels] += (P scaled per token by the
+//    group's scale) x (the same exact codes, transposed with movmatrix).
+//  * bf16 latent: q_lat is split into bf16 hi + lo against the exact bf16
+//    values, one accumulator over all groups, P split into bf16 hi + lo.
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "mla_internal.cuh"
+
+namespace mla {
+
+namespace {
+
+constexpr int kCW = 8;                         // warps (all consume; thread 0 also loads)
+constexpr int kThreads = kCW * 32;
+constexpr int kHT = 16;                        // heads per CTA
+constexpr int kPStride = 40;                   // row stride (16-bit elements) of the P tile: 80 B, conflict-free ldmatrix
+
+template <int LF, int KF>
+struct Fmt {
+  static constexpr bool kLatBf16 = LF == MLA_FMT_BF16;
+  static constexpr bool kLatInt4 = LF == MLA_FMT_INT4_ASYM;
+  static constexpr bool kKpeBf16 = KF == MLA_FMT_BF16;
+  static constexpr int kRow = kLatBf16 ? 1024 : (LF == MLA_FMT_INT8_SYM ? 512 : 256);
+  static constexpr int kKRow = kKpeBf16 ? 128 : 64;
+  static constexpr int kScaleOff = kBlockTokens * kRow;
+  static constexpr int kZeroOff = kScaleOff + (kLatBf16 ? 0 : kNLG * kBlockTokens * 4);
+  static constexpr int kKpeOff = kZeroOff + (kLatInt4 ? kNLG * kBlockTokens * 4 : 0);
+  static constexpr int kKScaleOff = kKpeOff + kBlockTokens * kKRow;
+  static constexpr int kBlock = kKScaleOff + (kKpeBf16 ? 0 : kNKG * kBlockTokens * 4);
+  static constexpr int kStages = kBlock <= 24 * 1024 ? 6 : (kBlock <= 40 * 1024 ? 4 : 3);
+  static constexpr int kXPartBytes = kCW * 4 * 32 * 16;    // partial scores [warp][ntile][lane] float4
+  static constexpr int kPBytes = 2 * kHT * kPStride * 2;   // P tile (hi, lo)
+  static constexpr int kFixed = kStages * kBlock + kXPartBytes + kPBytes + (kHT + kCW) * 4 + kStages * 8 + kStages * 4;
+};
+
+// ---------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false after ~10 s without
+// completion; the caller records MLA_DEVERR_TIMEOUT and stops.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done = 0;
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 255) == 0) {
+      const uint64_t now = global_ns();
+      if (it == 0) t0 = now;
+      else if (now - t0 > 10000000000ull) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(kCW * 32) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movt(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+  return d;
+}
+
+// d = a * b + c, fp16 inputs, fp32 accumulate (c and d may alias)
+__device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1, const float* c) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
+}
+
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1, const float* c) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+        "f"(c[3]));
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+__device__ __forceinline__ uint32_t pack_f16(float a, float b) { return h2_bits(__floats2half2_rn(a, b)); }
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo_f(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// fp32 pair -> (hi, lo) split in fp16 (hi = rn(x), lo = rn(x - hi)); x already scaled into range
+__device__ __forceinline__ void split_f16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(a, b);
+  const float2 hf = __half22float2(h);
+  hi = h2_bits(h);
+  lo = pack_f16(a - hf.x, b - hf.y);
+}
+
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(a, b);
+  lo = pack_bf16(a - bf16_lo_f(hi), b - bf16_hi_f(hi));
+}
+
+// 4 int8 codes (one 32-bit word) -> two f16x2 holding the codes exactly:
+// the bytes become 1024 + (code + 128) by bit placement, then 1152 is
+// subtracted in fp16 (exact: integers below 2048)
+__device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& r0, uint32_t& r1) {
+  const __half2 bias = __floats2half2_rn(1152.f, 1152.f);
+  const uint32_t x = w ^ 0x80808080u;
+  r0 = h2_bits(__hsub2(bits_h2(__byte_perm(x, 0x64646464u, 0x4140)), bias));
+  r1 = h2_bits(__hsub2(bits_h2(__byte_perm(x, 0x64646464u, 0x4342)), bias));
+}
+
+// one int4 word (layout in mla_internal.cuh) -> group A regs (a0, a1) and
+// group B regs (b0, b1), each f16x2 holding code - zero exactly: the nibbles
+// become 1024 + code (or 1024 + 16 code) by bit placement; za / zb hold
+// 1024 + z and ca / cb hold -64 - z of the two groups (f16x2, exact for
+// |z| < 960), and one exact fp16 subtract or fma removes both offsets
+__device__ __forceinline__ void i4x8_to_f16(uint32_t w, uint32_t za, uint32_t ca, uint32_t zb, uint32_t cb,
+                                            uint32_t& a0, uint32_t& a1, uint32_t& b0, uint32_t& b1) {
+  const __half2 k16 = __floats2half2_rn(0.0625f, 0.0625f);
+  a0 = h2_bits(__hsub2(bits_h2((w & 0x000F000Fu) | 0x64006400u), bits_h2(za)));
+  a1 = h2_bits(__hfma2(bits_h2((w & 0x00F000F0u) | 0x64006400u), k16, bits_h2(ca)));
+  const uint32_t v = w >> 8;
+  b0 = h2_bits(__hsub2(bits_h2((v & 0x000F000Fu) | 0x64006400u), bits_h2(zb)));
+  b1 = h2_bits(__hfma2(bits_h2((v & 0x00F000F0u) | 0x64006400u), k16, bits_h2(cb)));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  return v;
+}
+
+__device__ __forceinline__ int checked_len(const DecodeParams& p, int b, bool report) {
+  int len = p.seq_lens[b];
+  if (len < 0 || (int64_t)len > (int64_t)p.max_pages * kPage) {
+    if (report) set_err(p.dev_err, MLA_DEVERR_SEQLEN);
+    len = 0;
+  }
+  return len;
+}
+
+__device__ __forceinline__ int seq_of_chunk(const int32_t* cum, int B, int64_t c) {
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= c) lo = mid; else hi = mid - 1;
+  }
+  while (lo + 1 < B && cum[lo + 1] <= c) ++lo;
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp query state for one (sequence, head tile)
+// ---------------------------------------------------------------------------
+struct QueryRaw {            // this thread's fp32 query values, before range scaling
+  float4 x[4][2];            // q_lat: [group][row r / r+8], the 4 channels this thread feeds
+  float kx[2][4];            // q_pe: [row][4 channels]
+};
+
+struct Query {
+  uint32_t hi[4][4], lo[4][4];   // A fragments of q_lat (hi + lo split) for the warp's 4 groups
+  uint32_t ka[4];                // A fragment of q_pe for the warp's k_pe group / chunk
+};
+
+// Loads this thread's share of q_lat / q_pe and returns its largest magnitude.
+template <int LF, int KF>
+__device__ __forceinline__ float load_query_raw(const DecodeParams& p, int b, int h0, int w, int lane, QueryRaw& q) {
+  using F = Fmt<LF, KF>;
+  const int r = lane >> 2, j = lane & 3;
+  const float* ql0 = p.q_lat + ((size_t)b * p.H + h0 + r) * kDc;
+  const float* ql1 = ql0 + 8 * kDc;
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int gg = 4 * w + g;
+    if (F::kLatBf16) {
+      // standard layout: channels 2j, 2j+1 and 8+2j, 8+2j+1 of the group
+      const float2 a0 = *reinterpret_cast<const float2*>(ql0 + 16 * gg + 2 * j);
+      const float2 a1 = *reinterpret_cast<const float2*>(ql0 + 16 * gg + 8 + 2 * j);
+      const float2 b0 = *reinterpret_cast<const float2*>(ql1 + 16 * gg + 2 * j);
+      const float2 b1 = *reinterpret_cast<const float2*>(ql1 + 16 * gg + 8 + 2 * j);
+      q.x[g][0] = make_float4(a0.x, a0.y, a1.x, a1.y);
+      q.x[g][1] = make_float4(b0.x, b0.y, b1.x, b1.y);
+    } else {
+      // permuted layout: thread j feeds channels 4j .. 4j+3 of the group
+      q.x[g][0] = *reinterpret_cast<const float4*>(ql0 + 16 * gg + 4 * j);
+      q.x[g][1] = *reinterpret_cast<const float4*>(ql1 + 16 * gg + 4 * j);
+    }
+  }
+  const uint16_t* qp0 = p.q_pe + ((size_t)b * p.H + h0 + r) * kDr;
+  const uint16_t* qp1 = qp0 + 8 * kDr;
+  if (F::kKpeBf16) {
+    // warps 0..3: k16 chunk w (channels 16w..16w+15), standard layout
+    const bool act = w < 4;
+    const int c0 = 16 * (w & 3);
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const uint16_t* qp = rr ? qp1 : qp0;
+      q.kx[rr][0] = act ? bf16f(qp[c0 + 2 * j]) : 0.f;
+      q.kx[rr][1] = act ? bf16f(qp[c0 + 2 * j + 1]) : 0.f;
+      q.kx[rr][2] = act ? bf16f(qp[c0 + 8 + 2 * j]) : 0.f;
+      q.kx[rr][3] = act ? bf16f(qp[c0 + 8 + 2 * j + 1]) : 0.f;
+    }
+  } else {
+    // warp w: k_pe group w inside 16-channel chunk w/2; thread j feeds channels
+    // 4j..4j+3 of the chunk, which belong to the group only when j/2 == w%2
+    const bool act = (j >> 1) == (w & 1);
+    const int c0 = 16 * (w >> 1) + 4 * j;
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const uint16_t* qp = rr ? qp1 : qp0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) q.kx[rr][e] = act ? bf16f(qp[c0 + e]) : 0.f;
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+      amax = fmaxf(amax, fmaxf(fmaxf(fabsf(q.x[g][rr].x), fabsf(q.x[g][rr].y)),
+                               fmaxf(fabsf(q.x[g][rr].z), fabsf(q.x[g][rr].w))));
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(q.kx[rr][e]));
+  return amax;
+}
+
+// Scales by 2^e (exact) and splits into the MMA A fragments.
+template <int LF, int KF>
+__device__ __forceinline__ void finish_query(const QueryRaw& raw, float up, Query& q) {
+  using F = Fmt<LF, KF>;
+#pragma unroll
+  for (int g = 0; g < 4; ++g)
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const float4 v = raw.x[g][rr];
+      uint32_t h01, l01, h23, l23;
+      if (F::kLatBf16) {
+        split_bf16(v.x, v.y, h01, l01);
+        split_bf16(v.z, v.w, h23, l23);
+      } else {
+        split_f16(v.x * up, v.y * up, h01, l01);
+        split_f16(v.z * up, v.w * up, h23, l23);
+      }
+      // A fragment: reg0 = row r (k 0..7 half), reg1 = row r+8, reg2 = row r (k 8..15), reg3 = row r+8
+      q.hi[g][rr] = h01;
+      q.hi[g][rr + 2] = h23;
+      q.lo[g][rr] = l01;
+      q.lo[g][rr + 2] = l23;
+    }
+  if (F::kKpeBf16) {
+    q.ka[0] = pack_bf16(raw.kx[0][0] * up, raw.kx[0][1] * up);
+    q.ka[1] = pack_bf16(raw.kx[1][0] * up, raw.kx[1][1] * up);
+    q.ka[2] = pack_bf16(raw.kx[0][2] * up, raw.kx[0][3] * up);
+    q.ka[3] = pack_bf16(raw.kx[1][2] * up, raw.kx[1][3] * up);
+  } else {
+    q.ka[0] = pack_f16(raw.kx[0][0] * up, raw.kx[0][1] * up);
+    q.ka[1] = pack_f16(raw.kx[1][0] * up, raw.kx[1][1] * up);
+    q.ka[2] = pack_f16(raw.kx[0][2] * up, raw.kx[0][3] * up);
+    q.ka[3] = pack_f16(raw.kx[1][2] * up, raw.kx[1][3] * up);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int LF, int KF>
+__global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p) {
+  using F = Fmt<LF, KF>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stages = smem;
+  float4* xpart = reinterpret_cast<float4*>(smem + F::kStages * F::kBlock);      // [8 warps][4 ntiles][32 lanes]
+  uint16_t* ptab = reinterpret_cast<uint16_t*>(xpart + kCW * 4 * 32);            // [2][16][kPStride]
+  float* alpha_s = reinterpret_cast<float*>(ptab + 2 * kHT * kPStride);          // [16]
+  float* amax_s = alpha_s + kHT;                                                  // [8]
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(amax_s + kCW);
+  int32_t* meta = reinterpret_cast<int32_t*>(full_bar + F::kStages);
+  int32_t* cum = meta + F::kStages;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int x = blockIdx.x, G = gridDim.x, h0 = blockIdx.y * kHT;
+  const bool lead = (blockIdx.x == 0 && blockIdx.y == 0);
+
+  // ---- chunk prefix sums (warp 0) and barrier init (thread 32)
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < p.B; base += 32) {
+      const int b = base + lane;
+      int v = 0;
+      if (b < p.B) v = (checked_len(p, b, lead) + kChunk - 1) / kChunk;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += t;
+      }
+      if (b < p.B) cum[b + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) cum[0] = 0;
+  } else if (tid == 32) {
+    for (int s = 0; s < F::kStages; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  if (lead)
+    for (int i = tid; i <= p.B; i += kThreads) p.ws.cum[i] = cum[i];
+
+  const int64_t C = cum[p.B];
+  const int64_t c_lo = range_lo(C, x, G), c_hi = range_lo(C, x + 1, G);
+  if (c_lo >= c_hi) return;
+
+  // ---- loader state (thread 0 only).  plan() looks up the next chunk's page
+  // early (its global load then overlaps the QK^T work); commit(s) starts the
+  // copy into stage s.  Invalid pages and chunks past the end of the range
+  // complete the stage's phase with no data.
+  int64_t ld_c = c_lo;
+  int ld_b = 0, ld_len = 0, pl_page = -1, pl_t0 = 0;
+  bool pl_ready = false;
+  if (tid == 0) {
+    ld_b = seq_of_chunk(cum, p.B, c_lo);
+    ld_len = checked_len(p, ld_b, false);
+  }
+  auto plan = [&]() {
+    if (pl_ready || ld_c >= c_hi) return;
+    while (cum[ld_b + 1] <= ld_c) ld_len = checked_len(p, ++ld_b, false);
+    pl_t0 = (int)(ld_c - cum[ld_b]) * kChunk;
+    pl_page = p.block_table[(size_t)ld_b * p.max_pages + (pl_t0 >> 6)];
+    pl_ready = true;
+  };
+  auto commit = [&](int s) {
+    plan();
+    if (!pl_ready) return;
+    int nv = ld_len - pl_t0 < kChunk ? ld_len - pl_t0 : kChunk;
+    if (pl_page < 0 || pl_page >= p.num_pages) {
+      set_err(p.dev_err, MLA_DEVERR_PAGE);
+      nv = 0;
+    }
+    meta[s] = nv;
+    const uint32_t fb = smem_u32(&full_bar[s]);
+    if (nv > 0) {
+      mbar_expect_tx(fb, F::kBlock);
+      bulk_g2s(smem_u32(stages + s * F::kBlock),
+               p.pool + (int64_t)pl_page * p.L.page_bytes + ((pl_t0 >> 5) & 1) * p.L.block_bytes, F::kBlock, fb);
+    } else {
+      mbar_arrive(fb);
+    }
+    pl_ready = false;
+    ++ld_c;
+  };
+  if (tid == 0)
+    for (int s = 0; s < F::kStages; ++s) commit(s);
+
+  // =========================== compute ===========================
+  // Warp w: latent groups 4w..4w+3.  Reduction / softmax role: thread T owns
+  // row hr = T / 16 and tokens 2 (T % 16), +1 of each chunk.
+  const int w = warp, r = lane >> 2, j = lane & 3;
+  const int hr = tid >> 4, tp = tid & 15;
+  const int rd_n = tp >> 2, rd_lane = 4 * (hr & 7) + (tp & 3), rd_half = hr >> 3;
+  Query q;
+  float cw = 0.f;                  // softmax_scale * log2 e * 2^-e
+  float o[4][2][4];
+  float m_row = -INFINITY, l_row = 0.f;
+  int b = -1;
+  int i = 0;
+  bool dead = false;
+
+  auto flush = [&](int bb) {
+    const size_t slot = (size_t)x + bb;
+    if (tp == 0) {
+      p.ws.m[slot * p.H + h0 + hr] = m_row;
+      p.ws.l[slot * p.H + h0 + hr] = l_row;
+    }
+    float* o0 = p.ws.o + (slot * p.H + h0 + r) * kDc;
+    float* o1 = o0 + 8 * kDc;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int base = 16 * (4 * w + g);
+      if (F::kLatBf16) {
+        *reinterpret_cast<float2*>(o0 + base + 2 * j) = make_float2(o[g][0][0], o[g][0][1]);
+        *reinterpret_cast<float2*>(o0 + base + 8 + 2 * j) = make_float2(o[g][1][0], o[g][1][1]);
+        *reinterpret_cast<float2*>(o1 + base + 2 * j) = make_float2(o[g][0][2], o[g][0][3]);
+        *reinterpret_cast<float2*>(o1 + base + 8 + 2 * j) = make_float2(o[g][1][2], o[g][1][3]);
+      } else {
+        *reinterpret_cast<float4*>(o0 + base + 4 * j) = make_float4(o[g][0][0], o[g][0][1], o[g][1][0], o[g][1][1]);
+        *reinterpret_cast<float4*>(o1 + base + 4 * j) = make_float4(o[g][0][2], o[g][0][3], o[g][1][2], o[g][1][3]);
+      }
+    }
+  };
+
+  for (int64_t c = c_lo; c < c_hi && !dead; ++c, ++i) {
+    // ---- sequence boundary: flush the previous partial, load the new query
+    {
+      int nb = b < 0 ? seq_of_chunk(cum, p.B, c) : b;
+      while (cum[nb + 1] <= c) ++nb;
+      if (nb != b) {
+        if (b >= 0) flush(b);
+        b = nb;
+        QueryRaw raw;
+        const float am = warp_max(load_query_raw<LF, KF>(p, b, h0, w, lane, raw));
+        if (lane == 0) amax_s[w] = am;
+        consumer_sync();
+        float amx = 0.f;
+#pragma unroll
+        for (int k = 0; k < kCW; ++k) amx = fmaxf(amx, amax_s[k]);
+        int ex = 0;
+        if (!F::kLatBf16 && amx > 0.f && isfinite(amx)) {
+          ex = 14 - ilogbf(amx);
+          ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
+        }
+        finish_query<LF, KF>(raw, __int_as_float((127 + ex) << 23), q);
+        cw = p.scale_log2 * __int_as_float((127 - ex) << 23);
+        m_row = -INFINITY;
+        l_row = 0.f;
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
+      }
+    }
+    const int s = i % F::kStages;
+    if (tid == 0) plan();
+    if (!mbar_wait(smem_u32(&full_bar[s]), (i / F::kStages) & 1)) {
+      set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+      dead = true;
+      break;
+    }
+    const int nv = meta[s];
+    if (nv == 0) {
+      consumer_sync();                 // every warp has read meta[s]
+      if (tid == 0) commit(s);
+      continue;
+    }
+    const bool partial = nv < kChunk;
+    const uint8_t* st = stages + s * F::kBlock;
+    const uint32_t st_a = smem_u32(st);
+    const float* sc = reinterpret_cast<const float*>(st + F::kScaleOff);
+
+    // ---- B operands: exact codes (or code - zero) of the warp's 4 groups, 4 token tiles
+    uint32_t bq[4][4][2];      // [group][ntile][reg]
+    if (F::kLatBf16) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int ch = 2 * (4 * w + g);
+        uint32_t t0, t1, t2, t3;
+        ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(ch, lane) * 16, t0, t1, t2, t3);
+        bq[g][0][0] = t0; bq[g][1][0] = t1; bq[g][2][0] = t2; bq[g][3][0] = t3;
+        ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(ch + 1, lane) * 16, t0, t1, t2, t3);
+        bq[g][0][1] = t0; bq[g][1][1] = t1; bq[g][2][1] = t2; bq[g][3][1] = t3;
+      }
+      if (partial) {       // PV reads these values: zero the tokens past the end
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+          if (8 * n + r >= nv)
+#pragma unroll
+            for (int g = 0; g < 4; ++g) bq[g][n][0] = bq[g][n][1] = 0u;
+      }
+    } else if (F::kLatInt4) {
+      const float* zp = reinterpret_cast<const float*>(st + F::kZeroOff);
+      const __half2 k960 = __floats2half2_rn(960.f, 960.f);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t t[4];
+        ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(2 * w + cc, lane) * 16, t[0], t[1], t[2], t[3]);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          // zero-points of this thread's B token (8n + r) for groups A and B of the chunk
+          float za = zp[(4 * w + 2 * cc) * kBlockTokens + 8 * n + r];
+          float zb = zp[(4 * w + 2 * cc + 1) * kBlockTokens + 8 * n + r];
+          if (partial && 8 * n + r >= nv) za = zb = 0.f;
+          const uint32_t ba = pack_f16(za + 1024.f, za + 1024.f), bb = pack_f16(zb + 1024.f, zb + 1024.f);
+          const uint32_t ca = h2_bits(__hsub2(k960, bits_h2(ba))), cb = h2_bits(__hsub2(k960, bits_h2(bb)));
+          i4x8_to_f16(t[n], ba, ca, bb, cb, bq[2 * cc][n][0], bq[2 * cc][n][1], bq[2 * cc + 1][n][0],
+                      bq[2 * cc + 1][n][1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        uint32_t t[4];
+        ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(4 * w + g, lane) * 16, t[0], t[1], t[2], t[3]);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) i8x4_to_f16(t[n], bq[g][n][0], bq[g][n][1]);
+      }
+    }
+    // k_pe B operands
+    uint32_t bk[4][2];
+    const bool kact = F::kKpeBf16 ? (w < 4) : true;
+    if (F::kKpeBf16) {
+      if (kact) {
+        uint32_t t[4];
+        ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(2 * w, lane, true) * 16, t[0], t[1], t[2], t[3]);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) bk[n][0] = t[n];
+        ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(2 * w + 1, lane, true) * 16, t[0], t[1], t[2],
+                t[3]);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) bk[n][1] = t[n];
+      }
+    } else {
+      uint32_t t[4];
+      ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(w >> 1, lane, false) * 16, t[0], t[1], t[2], t[3]);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) i8x4_to_f16(t[n], bk[n][0], bk[n][1]);
+    }
+
+    // ---- QK^T partial scores of this warp's channels: acc[ntile][c-reg]
+    float acc[4][4];
+    uint32_t s2h[4][4];        // fp16 scale pairs of the C-fragment tokens (8n + 2j, +1), for PV
+#pragma unroll
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+    if (F::kLatBf16) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          mma_bf16(acc[n], q.hi[g], bq[g][n][0], bq[g][n][1], acc[n]);
+          mma_bf16(acc[n], q.lo[g], bq[g][n][0], bq[g][n][1], acc[n]);
+        }
+    } else {
+      const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          float2 s2 = *reinterpret_cast<const float2*>(sc + (4 * w + g) * kBlockTokens + 8 * n + 2 * j);
+          if (partial) {
+            if (8 * n + 2 * j >= nv) s2.x = 0.f;
+            if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
+          }
+          float d[4];
+          mma_f16(d, q.hi[g], bq[g][n][0], bq[g][n][1], zero4);
+          mma_f16(d, q.lo[g], bq[g][n][0], bq[g][n][1], d);
+          acc[n][0] = fmaf(d[0], s2.x, acc[n][0]);
+          acc[n][1] = fmaf(d[1], s2.y, acc[n][1]);
+          acc[n][2] = fmaf(d[2], s2.x, acc[n][2]);
+          acc[n][3] = fmaf(d[3], s2.y, acc[n][3]);
+          s2h[g][n] = pack_f16(s2.x, s2.y);
+        }
+    }
+    if (F::kKpeBf16) {
+      if (kact) {
+#pragma unroll
+        for (int n = 0; n < 4; ++n) mma_bf16(acc[n], q.ka, bk[n][0], bk[n][1], acc[n]);
+      }
+    } else {
+      const float* ks = reinterpret_cast<const float*>(st + F::kKScaleOff);
+      const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const float2 s2 = *reinterpret_cast<const float2*>(ks + w * kBlockTokens + 8 * n + 2 * j);
+        float d[4];
+        mma_f16(d, q.ka, bk[n][0], bk[n][1], zero4);
+        acc[n][0] = fmaf(d[0], s2.x, acc[n][0]);
+        acc[n][1] = fmaf(d[1], s2.y, acc[n][1]);
+        acc[n][2] = fmaf(d[2], s2.x, acc[n][2]);
+        acc[n][3] = fmaf(d[3], s2.y, acc[n][3]);
+      }
+    }
+
+    // ---- publish the partial scores; after the barrier every read of the
+    // stage is done, so thread 0 refills it
+#pragma unroll
+    for (int n = 0; n < 4; ++n) xpart[(w * 4 + n) * 32 + lane] = make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
+    consumer_sync();
+    if (tid == 0) commit(s);
+
+    // ---- reduction + online softmax: thread owns row hr, tokens 2tp, 2tp+1
+    {
+      float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int ww = 0; ww < kCW; ++ww) {
+        const float2 v = reinterpret_cast<const float2*>(&xpart[(ww * 4 + rd_n) * 32 + rd_lane])[rd_half];
+        sum.x += v.x;
+        sum.y += v.y;
+      }
+      float x0 = sum.x * cw, x1 = sum.y * cw;
+      if (partial) {
+        if (2 * tp >= nv) x0 = -INFINITY;
+        if (2 * tp + 1 >= nv) x1 = -INFINITY;
+      }
+      float mx = fmaxf(x0, x1);
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m_row, mx);
+      const float al = mn == -INFINITY ? 1.f : ex2(m_row - mn);
+      const float sub = mn == -INFINITY ? 0.f : mn;
+      const float p0 = ex2(x0 - sub), p1 = ex2(x1 - sub);
+      float ps = p0 + p1;
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+      l_row = l_row * al + ps;
+      m_row = mn;
+      uint32_t* prow = reinterpret_cast<uint32_t*>(ptab + hr * kPStride) + tp;
+      if (F::kLatBf16) {
+        uint32_t phi, plo;
+        split_bf16(p0, p1, phi, plo);
+        prow[0] = phi;
+        prow[kHT * kPStride / 2] = plo;
+      } else {
+        prow[0] = pack_f16(p0, p1);
+      }
+      if (tp == 0) alpha_s[hr] = al;
+    }
+    consumer_sync();
+
+    // ---- rescale o, load P as A fragments
+    {
+      const float al0 = alpha_s[r], al1 = alpha_s[r + 8];
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            o[g][e][0] *= al0;
+            o[g][e][1] *= al0;
+            o[g][e][2] *= al1;
+            o[g][e][3] *= al1;
+          }
+      }
+    }
+    uint32_t pa[2][2][4];      // [hi/lo][k step][reg]
+    {
+      const uint32_t pbase = smem_u32(ptab) + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kPStride * 2 + 8 * (lane >> 4) * 2;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        ldsm_x4(pbase + 32 * ks, pa[0][ks][0], pa[0][ks][1], pa[0][ks][2], pa[0][ks][3]);
+        if (F::kLatBf16)
+          ldsm_x4(pbase + kHT * kPStride * 2 + 32 * ks, pa[1][ks][0], pa[1][ks][1], pa[1][ks][2], pa[1][ks][3]);
+      }
+    }
+
+    // ---- P V
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t vt[4][2];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        vt[n][0] = movt(bq[g][n][0]);
+        vt[n][1] = movt(bq[g][n][1]);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        if (F::kLatBf16) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            mma_bf16(o[g][e], pa[0][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
+            mma_bf16(o[g][e], pa[1][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
+          }
+        } else {
+          // A = P scaled per token by the group's scale (columns = tokens)
+          uint32_t ag[4];
+          ag[0] = h2_bits(__hmul2(bits_h2(pa[0][ks][0]), bits_h2(s2h[g][2 * ks])));
+          ag[1] = h2_bits(__hmul2(bits_h2(pa[0][ks][1]), bits_h2(s2h[g][2 * ks])));
+          ag[2] = h2_bits(__hmul2(bits_h2(pa[0][ks][2]), bits_h2(s2h[g][2 * ks + 1])));
+          ag[3] = h2_bits(__hmul2(bits_h2(pa[0][ks][3]), bits_h2(s2h[g][2 * ks + 1])));
+#pragma unroll
+          for (int e = 0; e < 2; ++e) mma_f16(o[g][e], ag, vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
+        }
+      }
+    }
+  }
+  if (b >= 0 && !dead) flush(b);
+}
+
+// Largest dynamic shared memory a block may opt into on the current device.
+size_t smem_max() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cached[dev]) return (size_t)cached[dev];
+  int v = 0;
+  cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (dev >= 0 && dev < 64) cached[dev] = v;
+  return (size_t)v;
+}
+
+template <int LF, int KF>
+mla_status launch_t(const DecodeParams& p, cudaStream_t stream) {
+  using F = Fmt<LF, KF>;
+  if (p.L.block_bytes != F::kBlock || p.H % kHT) return MLA_ERR_UNSUPPORTED;
+  const size_t smem = F::kFixed + sizeof(int32_t) * (p.B + 1);
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    const mla_status st = cuda_status(cudaFuncSetAttribute(
+        decode_mma_kernel<LF, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max()));
+    if (st != MLA_OK) return st;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  if (smem > smem_max()) return MLA_ERR_UNSUPPORTED;
+  decode_mma_kernel<LF, KF><<<dim3(p.G, p.H / kHT), kThreads, smem, stream>>>(p);
+  return launch_status();
+}
+
+}  // namespace
+
+mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
+#define MLA_MMA_CASE(A, K) \
+  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_t<A, K>(p, stream);
+  MLA_MMA_CASE(MLA_FMT_BF16, MLA_FMT_BF16)
+  MLA_MMA_CASE(MLA_FMT_BF16, MLA_FMT_INT8_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT8_SYM, MLA_FMT_BF16)
+  MLA_MMA_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT8_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_BF16)
+  MLA_MMA_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT8_SYM)
+#undef MLA_MMA_CASE
+  return MLA_ERR_UNSUPPORTED;
+}
+
+}  // namespace mla

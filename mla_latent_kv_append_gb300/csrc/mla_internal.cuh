@@ -21,9 +21,12 @@ constexpr int kNKG = kDr / kKG;            // 8 k_pe groups
 constexpr int kChunk = 32;                 // decode work unit: 32 tokens
 constexpr int kMaxBatch = 4096;
 
-// Byte layout of one page; see mla_page_layout in mla.h.
+// Byte layout of one page; see mla_page_layout in mla.h.  A page is two
+// contiguous blocks of 32 tokens; offsets are within a block.
+constexpr int kBlockTokens = 32;
+
 struct PageLayout {
-  int64_t page_bytes;
+  int64_t page_bytes, block_bytes;
   int64_t codes_off, codes_row;
   int64_t scale_off, zero_off;
   int64_t kpe_off, kpe_row;
@@ -42,17 +45,37 @@ __host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, Page
   int64_t off = 0;
   L->codes_off = off;
   L->codes_row = row;
-  off += kPage * row;
+  off += kBlockTokens * row;
   L->scale_off = L->zero_off = -1;
-  if (latent_fmt != MLA_FMT_BF16) { L->scale_off = off; off += (int64_t)kNLG * kPage * 4; }
-  if (latent_fmt == MLA_FMT_INT4_ASYM) { L->zero_off = off; off += (int64_t)kNLG * kPage * 4; }
+  if (latent_fmt != MLA_FMT_BF16) { L->scale_off = off; off += (int64_t)kNLG * kBlockTokens * 4; }
+  if (latent_fmt == MLA_FMT_INT4_ASYM) { L->zero_off = off; off += (int64_t)kNLG * kBlockTokens * 4; }
   L->kpe_off = off;
   L->kpe_row = kpe_fmt == MLA_FMT_BF16 ? 2 * kDr : kDr;
-  off += kPage * L->kpe_row;
+  off += kBlockTokens * L->kpe_row;
   L->kpe_scale_off = -1;
-  if (kpe_fmt == MLA_FMT_INT8_SYM) { L->kpe_scale_off = off; off += (int64_t)kNKG * kPage * 4; }
-  L->page_bytes = off;
+  if (kpe_fmt == MLA_FMT_INT8_SYM) { L->kpe_scale_off = off; off += (int64_t)kNKG * kBlockTokens * 4; }
+  L->block_bytes = off;
+  L->page_bytes = 2 * off;
   return true;
+}
+
+// Stored position of 16-byte chunk c of a latent code row of token t (t =
+// token index within its 32-token block): the low three bits of the chunk
+// index are XORed with t, so that eight consecutive tokens' copies of one
+// logical chunk fall in eight different shared-memory bank groups.
+__host__ __device__ __forceinline__ int latent_chunk_pos(int c, int t) { return (c & ~7) | ((c ^ t) & 7); }
+// Same for the k_pe row: 8 chunks (bf16) or 4 chunks (int8) per token.
+__host__ __device__ __forceinline__ int kpe_chunk_pos(int c, int t, bool bf16) {
+  return bf16 ? (c ^ (t & 7)) : (c ^ ((t >> 1) & 3));
+}
+// INT4 chunk c holds latent groups A = 2c and B = 2c + 1 (16 channels each).
+// Its 32-bit word j (j = 0..3) packs, from the least significant nibble:
+// A[4j], A[4j+2], B[4j], B[4j+2], A[4j+1], A[4j+3], B[4j+1], B[4j+3].
+// Returns (group_in_chunk * 16 + channel_in_group) of nibble k of word j.
+__host__ __device__ __forceinline__ int int4_nibble_channel(int j, int k) {
+  const int grp = (k >> 1) & 1;                       // nibbles 2,3,6,7 -> group B
+  const int idx = 4 * j + ((k & 1) ? 2 : 0) + (k >> 2);
+  return grp * 16 + idx;
 }
 
 // ---------------------------------------------------------------------------
@@ -104,6 +127,7 @@ __host__ __device__ inline int64_t range_lo(int64_t C, int x, int G) { return C 
 // Host side launch helpers (api.cu)
 int device_sm_count();
 mla_status launch_status();
+mla_status cuda_status(cudaError_t e);   // records the error string on failure
 
 // Launchers implemented in the kernel translation units.
 mla_status launch_append(const mla_cache_layer* cache, const PageLayout& L, const uint16_t* c_new,
@@ -131,5 +155,6 @@ struct DecodeParams {
   int32_t* dev_err;
 };
 mla_status launch_decode(const DecodeParams& p, cudaStream_t stream);
+mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream);   // decode kernel only
 
 }  // namespace mla

@@ -15,36 +15,64 @@ FMT_NAME = {F_BF16: "bf16", F_INT8: "int8", F_INT4: "int4"}
 ATTN_TOL = 2e-3          # max relative error of attention outputs (per row, inf-norm)
 
 
+def _int4_channel(j, k):
+    """Channel (0..31 within a chunk) of nibble k of word j, as mla.h documents."""
+    grp = (k >> 1) & 1
+    return grp * 16 + 4 * j + (2 if k & 1 else 0) + (k >> 2)
+
+
 def read_tokens(pool_np, layout, latent_fmt, kpe_fmt, slots):
-    """Stored fields of the tokens at `slots` (numpy int array)."""
+    """Stored fields of the tokens at `slots` (numpy int array), decoded from
+    the byte layout that include/mla.h documents (32-token blocks, swizzled
+    16-byte chunks, interleaved INT4 nibbles)."""
     slots = np.asarray(slots, np.int64)
-    page, off = slots // 64, slots % 64
-    base = page * layout.page_bytes
+    n = len(slots)
+    page, tok = slots // 64, slots % 64
+    u = tok % 32
+    base = page * layout.page_bytes + (tok // 32) * layout.block_bytes
     out = {}
-    rows = pool_np[(base + layout.codes_off + off * layout.codes_row_bytes)[:, None]
-                   + np.arange(layout.codes_row_bytes)[None, :]]
+
+    def gather(off, nbytes):
+        return pool_np[(base + off)[:, None] + np.arange(nbytes)[None, :]]
+
+    def fp32_field(off, groups):
+        idx = (base + off)[:, None, None] + ((np.arange(groups)[None, :] * 32 + u[:, None]) * 4)[..., None] \
+            + np.arange(4)
+        return pool_np[idx].reshape(n, groups, 4).copy().view(np.float32)[..., 0]
+
+    row = layout.codes_row_bytes
+    nchunk = row // 16
+    phys = gather(layout.codes_off + u * row, row).reshape(n, nchunk, 16)
+    c = np.arange(nchunk)[None, :]
+    pos = (c & ~7) | ((c ^ u[:, None]) & 7)
+    logical = np.take_along_axis(phys, pos[..., None], axis=1)           # [n, nchunk, 16]
     if latent_fmt == F_BF16:
-        out["c_bits"] = rows.copy().view(np.uint16)
+        out["c_bits"] = logical.reshape(n, row).copy().view(np.uint16)
     else:
-        gi = np.arange(32)[None, :] * 64 + off[:, None]
-        scale = pool_np[(base + layout.scale_off)[:, None, None] + (gi * 4)[..., None] + np.arange(4)]
-        out["c_scale"] = scale.reshape(len(slots), 32, 4).copy().view(np.float32)[..., 0]
+        out["c_scale"] = fp32_field(layout.scale_off, 32)
         if latent_fmt == F_INT8:
-            out["c_codes"] = rows.view(np.int8).copy()
+            out["c_codes"] = logical.reshape(n, row).view(np.int8).copy()
         else:
-            lo, hi = rows & 15, rows >> 4
-            out["c_codes"] = np.stack([lo, hi], axis=2).reshape(len(slots), 512).astype(np.uint8)
-            zero = pool_np[(base + layout.zero_off)[:, None, None] + (gi * 4)[..., None] + np.arange(4)]
-            out["c_zero"] = zero.reshape(len(slots), 32, 4).copy().view(np.float32)[..., 0]
-    krows = pool_np[(base + layout.kpe_off + off * layout.kpe_row_bytes)[:, None]
-                    + np.arange(layout.kpe_row_bytes)[None, :]]
+            words = logical.reshape(n, nchunk, 4, 4).astype(np.uint32)
+            words = words[..., 0] | (words[..., 1] << 8) | (words[..., 2] << 16) | (words[..., 3] << 24)
+            codes = np.zeros((n, 512), np.uint8)
+            for j in range(4):
+                for k in range(8):
+                    ch = np.arange(nchunk) * 32 + _int4_channel(j, k)
+                    codes[:, ch] = (words[:, :, j] >> (4 * k)) & 15
+            out["c_codes"] = codes
+            out["c_zero"] = fp32_field(layout.zero_off, 32)
+    krow = layout.kpe_row_bytes
+    kch = krow // 16
+    kphys = gather(layout.kpe_off + u * krow, krow).reshape(n, kch, 16)
+    c = np.arange(kch)[None, :]
+    kpos = (c ^ (u[:, None] & 7)) if kpe_fmt == F_BF16 else (c ^ ((u[:, None] >> 1) & 3))
+    klog = np.take_along_axis(kphys, kpos[..., None], axis=1).reshape(n, krow)
     if kpe_fmt == F_BF16:
-        out["kpe_bits"] = krows.copy().view(np.uint16)
+        out["kpe_bits"] = klog.copy().view(np.uint16)
     else:
-        out["kpe_codes"] = krows.view(np.int8).copy()
-        gi = np.arange(8)[None, :] * 64 + off[:, None]
-        ks = pool_np[(base + layout.kpe_scale_off)[:, None, None] + (gi * 4)[..., None] + np.arange(4)]
-        out["kpe_scale"] = ks.reshape(len(slots), 8, 4).copy().view(np.float32)[..., 0]
+        out["kpe_codes"] = klog.view(np.int8).copy()
+        out["kpe_scale"] = fp32_field(layout.kpe_scale_off, 8)
     return out
 
 

@@ -59,8 +59,11 @@ def test_split_invariance_and_counts():
     for ns in (1, 2, 3, 7, 40, 0, 400):
         o, _ = run_and_check(wl, num_splits=ns, layers=[1])
         outs.append(o)
+    # every split count is within 2e-3 of the oracle (run_and_check); between
+    # split counts the results differ only by the fp16 rounding of P and of
+    # the scaled P, taken relative to different running maxima (~2^-11)
     for o in outs[1:]:
-        assert A.max_rel_error(o, outs[0]) < 1e-5
+        assert A.max_rel_error(o, outs[0]) < 1e-3
 
 
 def test_64_heads_mixed_lengths():
