@@ -130,15 +130,18 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "r"(addr));
 }
 
+// Register-only instructions are not volatile so that the compiler may
+// interleave independent MMA chains; shared-memory reads (ldmatrix) stay
+// volatile to keep them after the barrier waits that guard them.
 __device__ __forceinline__ uint32_t movt(uint32_t a) {
   uint32_t d;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
+  asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(d) : "r"(a));
   return d;
 }
 
 // d = a * b + c, fp16 inputs, fp32 accumulate (c and d may alias)
 __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1, const float* c) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%10,%11,%12,%13};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -147,7 +150,7 @@ __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0
 }
 
 __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1, const float* c) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%10,%11,%12,%13};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -619,7 +622,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
     } else {
       const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
+      for (int g = 0; g < 4; ++g) {
+        // four independent hi MMAs, then the lo MMAs that depend on them
+        float d[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) mma_f16(d[n], q.hi[g], bq[g][n][0], bq[g][n][1], zero4);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) mma_f16(d[n], q.lo[g], bq[g][n][0], bq[g][n][1], d[n]);
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
           float2 s2 = *reinterpret_cast<const float2*>(sc + (4 * w + g) * kBlockTokens + 8 * n + 2 * j);
@@ -627,15 +636,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
             if (8 * n + 2 * j >= nv) s2.x = 0.f;
             if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
           }
-          float d[4];
-          mma_f16(d, q.hi[g], bq[g][n][0], bq[g][n][1], zero4);
-          mma_f16(d, q.lo[g], bq[g][n][0], bq[g][n][1], d);
-          acc[n][0] = fmaf(d[0], s2.x, acc[n][0]);
-          acc[n][1] = fmaf(d[1], s2.y, acc[n][1]);
-          acc[n][2] = fmaf(d[2], s2.x, acc[n][2]);
-          acc[n][3] = fmaf(d[3], s2.y, acc[n][3]);
+          acc[n][0] = fmaf(d[n][0], s2.x, acc[n][0]);
+          acc[n][1] = fmaf(d[n][1], s2.y, acc[n][1]);
+          acc[n][2] = fmaf(d[n][2], s2.x, acc[n][2]);
+          acc[n][3] = fmaf(d[n][3], s2.y, acc[n][3]);
           s2h[g][n] = pack_f16(s2.x, s2.y);
         }
+      }
     }
     if (F::kKpeBf16) {
       if (kact) {
