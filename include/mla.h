@@ -213,6 +213,34 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
                                float* lse, int32_t* dev_err, mla_stream_t stream);
 
 /*
+ * mla_decode_absorbed_noalloc - the same decode as mla_decode_absorbed for
+ * callers that cannot allocate device memory: a plugin handed only its input
+ * and output buffers, code running during CUDA-graph capture (cudaMalloc is
+ * not capturable there), or a serving loop that forbids allocation after
+ * start-up.  The source pages have no counterpart; this is a deployment
+ * variant of the call above.
+ *   Arguments and results are those of mla_decode_absorbed, without the
+ *   workspace: the split-K partials go to a scratch array of
+ *   MLA_NOALLOC_SCRATCH_BYTES compiled into the library, which every device
+ *   that loads the library holds until the process exits.  It calls no
+ *   allocator (no cudaMalloc, cudaFree or allocating library routine).
+ *   Returns MLA_ERR_INVALID_ARG when mla_decode_workspace_bytes(batch, heads,
+ *   num_splits) exceeds MLA_NOALLOC_SCRATCH_BYTES (e.g. 64 heads at batch 64
+ *   with one split per SM fits; pass a smaller num_splits otherwise).
+ *   The first call on a device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.  All calls share the array and it keeps the last call's
+ *   contents (nothing in it needs to start at zero), so calls that overlap
+ *   on the GPU - on different streams or from different host threads - race.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+mla_status mla_decode_absorbed_noalloc(const mla_cache_layer* cache, const float* q_lat,
+                                       const uint16_t* q_pe, const int32_t* block_table,
+                                       int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                                       int32_t heads, float softmax_scale, int32_t num_splits,
+                                       float* o_lat, float* lse, int32_t* dev_err, mla_stream_t stream);
+
+/*
  * mla_out_unabsorb - o[b][h] = o_lat[b][h] @ W_UV[h]   (the output side of
  * weight absorption; [TU] "步骤2" V_i = C^KV W_i^upV with W_UV[h] = W_i^upV).
  *   o_lat fp32 [B][H][512]   W_UV bf16 [H][512][128]   o fp32 [B][H][128]

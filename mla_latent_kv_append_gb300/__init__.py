@@ -17,7 +17,8 @@ Names follow the C ABI:
     mla_out_unabsorb(o_lat, w_uv, o)
 
 plus ``CacheLayer`` (one layer's pool and formats), ``mla_cache_page_layout``,
-``mla_cache_pool_bytes`` and ``mla_decode_workspace_bytes``.
+``mla_cache_pool_bytes``, ``mla_decode_workspace_bytes`` and
+``mla_decode_absorbed_noalloc`` (the decode for callers that cannot allocate).
 """
 
 import ctypes
@@ -74,6 +75,7 @@ def _load():
         "mla_decode_workspace_bytes": (SZ, [I32, I32, I32]),
         "mla_decode_absorbed": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, SZ, P, P, P, P]),
         "mla_out_unabsorb": (I32, [P, P, P, I32, I32, P]),
+        "mla_decode_absorbed_noalloc": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -183,6 +185,26 @@ def mla_decode_absorbed(cache, q_lat, q_pe, block_table, seq_lens, workspace, o_
         ctypes.byref(cs), _ptr(q_lat), _ptr(q_pe), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H,
         scale, int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o_lat),
         _ptr(lse), _ptr(dev_err), _stream(stream)))
+
+
+def mla_decode_absorbed_noalloc(cache, q_lat, q_pe, block_table, seq_lens, o_lat, lse=None, dev_err=None,
+                                softmax_scale=None, num_splits=0, stream=None):
+    """mla_decode_absorbed without a workspace argument: for callers that
+    cannot allocate device memory (see include/mla.h).  Concurrent calls on
+    different streams share the library's scratch array and race."""
+    B, H = q_lat.shape[0], q_lat.shape[1]
+    _need(q_lat, torch.float32, (B, H, KV_LORA_RANK), "q_lat")
+    _need(q_pe, torch.bfloat16, (B, H, ROPE_DIM), "q_pe")
+    _need(block_table, torch.int32, (B, block_table.shape[1]), "block_table")
+    _need(seq_lens, torch.int32, (B,), "seq_lens")
+    _need(o_lat, torch.float32, (B, H, KV_LORA_RANK), "o_lat")
+    if lse is not None:
+        _need(lse, torch.float32, (B, H), "lse")
+    scale = DEFAULT_SOFTMAX_SCALE if softmax_scale is None else float(softmax_scale)
+    cs = cache.c_struct()
+    _check("mla_decode_absorbed_noalloc", lib.mla_decode_absorbed_noalloc(
+        ctypes.byref(cs), _ptr(q_lat), _ptr(q_pe), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H,
+        scale, int(num_splits), _ptr(o_lat), _ptr(lse), _ptr(dev_err), _stream(stream)))
 
 
 def abi_version():
