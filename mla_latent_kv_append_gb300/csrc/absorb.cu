@@ -116,12 +116,13 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t* __restric
 }
 
 // ---------------------------------------------------------------------------
-// out_unabsorb: grid (H, 128 / 32), block 128.  Warp w takes K rows
-// 128w .. 128w+127 for all 32 columns; the 4 partial tiles are summed in
+// out_unabsorb: grid (H, 128 / 16), block 128.  Warp w takes K rows
+// 128w .. 128w+127 for the CTA's 16 columns; all of the warp's A values are
+// loaded up front (independent loads), and the 4 partial tiles are summed in
 // shared memory.
 // ---------------------------------------------------------------------------
-constexpr int kUnN = 32;             // columns per CTA
-constexpr int kUnWS = kUnN + 8;      // W tile row stride (bf16): 80 B
+constexpr int kUnN = 16;             // columns per CTA
+constexpr int kUnWS = kUnN + 8;      // W tile row stride (bf16): 48 B, conflict-free ldmatrix
 
 __global__ void __launch_bounds__(128) out_unabsorb_kernel(const float* __restrict__ o_lat,
                                                            const uint16_t* __restrict__ w_uv,
@@ -132,46 +133,40 @@ __global__ void __launch_bounds__(128) out_unabsorb_kernel(const float* __restri
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, j = lane & 3;
   const uint16_t* wsrc = w_uv + (size_t)h * kDc * kDv + v0;
   for (int i = tid; i < kDc * (kUnN / 8); i += 128) {
-    const int k = i >> 2, c = i & 3;
+    const int k = i >> 1, c = i & 1;
     *reinterpret_cast<uint4*>(ws + k * kUnWS + 8 * c) = *reinterpret_cast<const uint4*>(wsrc + (size_t)k * kDv + 8 * c);
   }
   const uint32_t b_base = smem_addr(ws) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kUnWS + 8 * (lane >> 4)) * 2;
   for (int b0 = 0; b0 < B; b0 += 16) {
-    __syncthreads();
-    const float* a0p = o_lat + ((size_t)(b0 + r) * H + h) * kDc;
-    const float* a1p = o_lat + ((size_t)(b0 + r + 8) * H + h) * kDc;
+    const float* a0p = o_lat + ((size_t)(b0 + r) * H + h) * kDc + 128 * warp;
+    const float* a1p = o_lat + ((size_t)(b0 + r + 8) * H + h) * kDc + 128 * warp;
     const bool ok0 = b0 + r < B, ok1 = b0 + r + 8 < B;
-    float acc[4][4];
+    float2 xa[8][4];
+    const float2 z = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-#pragma unroll 2
     for (int ks = 0; ks < 8; ++ks) {
-      const int k = 128 * warp + 16 * ks;
-      const float2 z = make_float2(0.f, 0.f);
-      const float2 x00 = ok0 ? *reinterpret_cast<const float2*>(a0p + k + 2 * j) : z;
-      const float2 x10 = ok1 ? *reinterpret_cast<const float2*>(a1p + k + 2 * j) : z;
-      const float2 x01 = ok0 ? *reinterpret_cast<const float2*>(a0p + k + 8 + 2 * j) : z;
-      const float2 x11 = ok1 ? *reinterpret_cast<const float2*>(a1p + k + 8 + 2 * j) : z;
+      xa[ks][0] = ok0 ? *reinterpret_cast<const float2*>(a0p + 16 * ks + 2 * j) : z;
+      xa[ks][1] = ok1 ? *reinterpret_cast<const float2*>(a1p + 16 * ks + 2 * j) : z;
+      xa[ks][2] = ok0 ? *reinterpret_cast<const float2*>(a0p + 16 * ks + 8 + 2 * j) : z;
+      xa[ks][3] = ok1 ? *reinterpret_cast<const float2*>(a1p + 16 * ks + 8 + 2 * j) : z;
+    }
+    __syncthreads();     // W tile in place; previous tile's partials consumed
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
       uint32_t a[3][4];
-      split3(x00.x, x00.y, a[0][0], a[1][0], a[2][0]);
-      split3(x10.x, x10.y, a[0][1], a[1][1], a[2][1]);
-      split3(x01.x, x01.y, a[0][2], a[1][2], a[2][2]);
-      split3(x11.x, x11.y, a[0][3], a[1][3], a[2][3]);
-      uint32_t bf[2][4];
-      ldsm_x4_t(b_base + k * kUnWS * 2, bf[0]);            // columns 0..15
-      ldsm_x4_t(b_base + k * kUnWS * 2 + 32, bf[1]);       // columns 16..31
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split3(xa[ks][e].x, xa[ks][e].y, a[0][e], a[1][e], a[2][e]);
+      uint32_t bf[4];
+      ldsm_x4_t(b_base + (128 * warp + 16 * ks) * kUnWS * 2, bf);
 #pragma unroll
       for (int part3 = 0; part3 < 3; ++part3) {
-        mma_bf16(acc[0], a[part3], bf[0][0], bf[0][1]);
-        mma_bf16(acc[1], a[part3], bf[0][2], bf[0][3]);
-        mma_bf16(acc[2], a[part3], bf[1][0], bf[1][1]);
-        mma_bf16(acc[3], a[part3], bf[1][2], bf[1][3]);
+        mma_bf16(acc[0], a[part3], bf[0], bf[1]);
+        mma_bf16(acc[1], a[part3], bf[2], bf[3]);
       }
     }
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
+    for (int nt = 0; nt < 2; ++nt) {
       part[warp][r][8 * nt + 2 * j] = acc[nt][0];
       part[warp][r][8 * nt + 2 * j + 1] = acc[nt][1];
       part[warp][r + 8][8 * nt + 2 * j] = acc[nt][2];

@@ -99,8 +99,10 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
     for (int i = tid; i <= p.B; i += kThreads) p.ws.cum[i] = cum[i];
 
   const int64_t C = cum[p.B];
-  int64_t c = range_lo(C, x, G);
-  const int64_t c_end = range_lo(C, x + 1, G);
+  const int Ge = (int64_t)G < C ? G : (int)C;          // no empty ranges
+  if (x >= Ge) return;
+  const int64_t c_lo = range_lo(C, x, Ge), c_end = range_lo(C, x + 1, Ge);
+  int64_t c = c_lo;
   const uint8_t* pool = p.pool;
   const int64_t pb = p.L.page_bytes;
 
@@ -296,6 +298,10 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
 
     // ---- partial of (sequence b, this CTA) -> slot x + b
     __syncthreads();
+    if (tid == 0 && blockIdx.y == 0) {
+      if (c_lo <= cum[b]) p.ws.span[2 * b] = x;
+      if (c_end >= cum[b + 1]) p.ws.span[2 * b + 1] = x;
+    }
     if (tid < kHT) {
       p.ws.m[(size_t)slot * p.H + h0 + tid] = s_m[tid];
       p.ws.l[(size_t)slot * p.H + h0 + tid] = s_l[tid];
@@ -310,44 +316,66 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
   }
 }
 
-// Largest x in [0, G) with range_lo(C, x, G) <= c.
-__device__ __forceinline__ int owner_of_chunk(int64_t C, int G, int64_t c) {
-  int lo = 0, hi = G - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (range_lo(C, mid, G) <= c) lo = mid; else hi = mid - 1;
+// grid (B, H), block 128: merge the partials of sequence b, head h.  CTAs
+// span[2b] .. span[2b+1] wrote slots x + b.  The slots' maxima and sums are
+// read in parallel (one slot per thread), the block reduces them, and each
+// thread then accumulates 4 channels over all slots with independent loads.
+constexpr int kCombSlots = 1024;     // weights cached in shared memory
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = is_max ? fmaxf(v, o) : v + o;
   }
-  return lo;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  v = red[0];
+#pragma unroll
+  for (int k = 1; k < 4; ++k) v = is_max ? fmaxf(v, red[k]) : v + red[k];
+  return v;
 }
 
-// grid (B, H), block 128: merge the partials of sequence b, head h.
 __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
+  __shared__ float sw[kCombSlots];
+  __shared__ float red[4];
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int32_t* cum = p.ws.cum;
-  const int64_t C = cum[p.B];
-  const int64_t cs = cum[b], ce = cum[b + 1];
   float4* out = reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc) + tid;
-  if (cs == ce) {
+  if (cum[b] == cum[b + 1]) {
     *out = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
     return;
   }
-  const int G = p.G;
-  const int x0 = owner_of_chunk(C, G, cs), x1 = owner_of_chunk(C, G, ce - 1);
-  float M = -INFINITY;
-  for (int x = x0; x <= x1; ++x)
-    if (range_lo(C, x, G) < range_lo(C, x + 1, G)) M = fmaxf(M, p.ws.m[(size_t)(x + b) * p.H + h]);
-  float L = 0.f;
+  const int x0 = p.ws.span[2 * b], S = p.ws.span[2 * b + 1] - x0 + 1;
+  const float* mp = p.ws.m + (size_t)(x0 + b) * p.H + h;
+  const float* lp = p.ws.l + (size_t)(x0 + b) * p.H + h;
+  float mloc = -INFINITY;
+  for (int t = tid; t < S; t += 128) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
+  const float M = block_reduce(mloc, true, red);
+  float lloc = 0.f;
+  for (int t = tid; t < S; t += 128) {
+    const float m = mp[(size_t)t * p.H];
+    const float w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
+    if (t < kCombSlots) sw[t] = w;
+    if (w != 0.f) lloc = fmaf(w, lp[(size_t)t * p.H], lloc);
+  }
+  const float L = block_reduce(lloc, false, red);   // also orders the sw writes before the reads below
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int x = x0; x <= x1; ++x) {
-      if (range_lo(C, x, G) >= range_lo(C, x + 1, G)) continue;
-      const size_t si = (size_t)(x + b) * p.H + h;
-      const float m = p.ws.m[si];
-      if (m == -INFINITY) continue;
-      const float w = exp2f(m - M);
-      L = fmaf(w, p.ws.l[si], L);
-      const float4 v = reinterpret_cast<const float4*>(p.ws.o + si * kDc)[tid];
+  const float4* o4 = reinterpret_cast<const float4*>(p.ws.o + ((size_t)(x0 + b) * p.H + h) * kDc) + tid;
+#pragma unroll 4
+  for (int t = 0; t < S; ++t) {
+    float w;
+    if (t < kCombSlots) {
+      w = sw[t];
+    } else {
+      const float m = mp[(size_t)t * p.H];
+      w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
+    }
+    if (w != 0.f) {
+      const float4 v = o4[(size_t)t * p.H * (kDc / 4)];
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);

@@ -405,8 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
     for (int i = tid; i <= p.B; i += kThreads) p.ws.cum[i] = cum[i];
 
   const int64_t C = cum[p.B];
-  const int64_t c_lo = range_lo(C, x, G), c_hi = range_lo(C, x + 1, G);
-  if (c_lo >= c_hi) return;
+  const int Ge = (int64_t)G < C ? G : (int)C;          // no empty ranges
+  if (x >= Ge) return;
+  const int64_t c_lo = range_lo(C, x, Ge), c_hi = range_lo(C, x + 1, Ge);
 
   // ---- loader state (thread 0 only).  plan() looks up the next chunk's page
   // early (its global load then overlaps the QK^T work); commit(s) starts the
@@ -465,6 +466,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
 
   auto flush = [&](int bb) {
     const size_t slot = (size_t)x + bb;
+    if (tid == 0 && blockIdx.y == 0) {
+      if (c_lo <= cum[bb]) p.ws.span[2 * bb] = x;            // holds the sequence's first chunk
+      if (c_hi >= cum[bb + 1]) p.ws.span[2 * bb + 1] = x;    // holds its last chunk
+    }
     if (tp == 0) {
       p.ws.m[slot * p.H + h0 + hr] = m_row;
       p.ws.l[slot * p.H + h0 + hr] = l_row;

@@ -89,9 +89,12 @@ __device__ __forceinline__ void set_err(int32_t* dev_err, int bit) {
   if (dev_err) atomicOr(dev_err, bit);
 }
 
-// Split-K partial workspace: [cum: B+1 int32 | m: slots*H | l: slots*H | o: slots*H*512]
+// Split-K partial workspace:
+//   [cum: B+1 int32 | span: 2B int32 | m: slots*H | l: slots*H | o: slots*H*512]
+// span[2b], span[2b+1] = first and last CTA (grid x) that worked on sequence b.
 struct Workspace {
   int32_t* cum;
+  int32_t* span;
   float* m;
   float* l;
   float* o;
@@ -101,7 +104,8 @@ __host__ __device__ inline int64_t align256(int64_t x) { return (x + 255) & ~(in
 
 __host__ __device__ inline int64_t workspace_bytes(int B, int H, int G) {
   int64_t slots = (int64_t)G + B;
-  return align256((int64_t)(B + 1) * 4) + 2 * align256(slots * H * 4) + slots * H * kDc * 4;
+  return align256((int64_t)(B + 1) * 4) + align256((int64_t)2 * B * 4) + 2 * align256(slots * H * 4) +
+         slots * H * kDc * 4;
 }
 
 __host__ __device__ inline Workspace carve_workspace(void* base, int B, int H, int G) {
@@ -110,6 +114,8 @@ __host__ __device__ inline Workspace carve_workspace(void* base, int B, int H, i
   Workspace w;
   w.cum = (int32_t*)p;
   p += align256((int64_t)(B + 1) * 4);
+  w.span = (int32_t*)p;
+  p += align256((int64_t)2 * B * 4);
   w.m = (float*)p;
   p += align256(slots * H * 4);
   w.l = (float*)p;
@@ -119,9 +125,11 @@ __host__ __device__ inline Workspace carve_workspace(void* base, int B, int H, i
 }
 
 // Context partition: the total C chunks (32 tokens each) of all sequences are
-// cut into G contiguous ranges, range x = [C*x/G, C*(x+1)/G).  Partials of
-// sequence b computed by CTA x go to slot x + b, which is unique because two
-// sequences share at most a boundary CTA.
+// cut into Ge = min(G, C) contiguous, non-empty ranges, range x =
+// [C*x/Ge, C*(x+1)/Ge); CTAs x >= Ge have no work.  Partials of sequence b
+// computed by CTA x go to slot x + b, which is unique because two sequences
+// share at most a boundary CTA.  The CTAs that hold a sequence's first and
+// last chunk record themselves in span[], so the combine needs no division.
 __host__ __device__ inline int64_t range_lo(int64_t C, int x, int G) { return C * x / G; }
 
 // Host side launch helpers (api.cu)
