@@ -30,6 +30,8 @@
 //  * The partial scores of the 8 warps are summed through shared memory by
 //    256 threads (16 per head row), which also run the online softmax (max /
 //    sum with warp shuffles over the row's 16 threads) and publish P in fp16.
+//    This runs one chunk behind the QK^T work (software pipeline, one
+//    barrier per chunk), so the two overlap.
 //  * PV: o[16 heads][the warp's 64 channels] += (P scaled per token by the
 //    group's scale) x (the same exact codes, transposed with movmatrix).
 //  * bf16 latent: q_lat is split into bf16 hi + lo against the exact bf16
@@ -47,6 +49,7 @@ constexpr int kCW = 8;                         // warps (all consume; thread 0 a
 constexpr int kThreads = kCW * 32;
 constexpr int kHT = 16;                        // heads per CTA
 constexpr int kPStride = 40;                   // row stride (16-bit elements) of the P tile: 80 B, conflict-free ldmatrix
+constexpr int kXStride = 20;                   // row stride (float2) of a warp's partial-score tile: 160 B, conflict-free
 
 template <int LF, int KF>
 struct Fmt {
@@ -61,9 +64,9 @@ struct Fmt {
   static constexpr int kKScaleOff = kKpeOff + kBlockTokens * kKRow;
   static constexpr int kBlock = kKScaleOff + (kKpeBf16 ? 0 : kNKG * kBlockTokens * 4);
   static constexpr int kStages = kBlock <= 24 * 1024 ? 6 : (kBlock <= 40 * 1024 ? 4 : 3);
-  static constexpr int kXPartBytes = kCW * 4 * 32 * 16;    // partial scores [warp][ntile][lane] float4
-  static constexpr int kPBytes = 2 * kHT * kPStride * 2;   // P tile (hi, lo)
-  static constexpr int kFixed = kStages * kBlock + kXPartBytes + kPBytes + (kHT + kCW) * 4 + kStages * 8 + kStages * 4;
+  static constexpr int kXPartBytes = 2 * kCW * kHT * kXStride * 8;   // partial scores [buf][warp][row][pair]
+  static constexpr int kPBytes = 4 * kHT * kPStride * 2;              // P tiles [buf][hi, lo]
+  static constexpr int kFixed = kStages * kBlock + kXPartBytes + kPBytes + (2 * kHT + kCW) * 4 + kStages * 8 + kStages * 4;
 };
 
 // ---------------------------------------------------------------------------
@@ -363,15 +366,20 @@ __device__ __forceinline__ void finish_query(const QueryRaw& raw, float up, Quer
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+// Per-chunk pipeline with one barrier per chunk: iteration k computes the
+// partial scores of chunk k (QK^T, step A) while the reduction threads run the
+// softmax of chunk k-1 (step B); after the barrier every warp accumulates
+// PV of chunk k-1 (step C) from the code registers it kept from A(k-1).  The
+// score-exchange and P tiles are double-buffered by chunk parity.
 template <int LF, int KF>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p) {
   using F = Fmt<LF, KF>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  float4* xpart = reinterpret_cast<float4*>(smem + F::kStages * F::kBlock);      // [8 warps][4 ntiles][32 lanes]
-  uint16_t* ptab = reinterpret_cast<uint16_t*>(xpart + kCW * 4 * 32);            // [2][16][kPStride]
-  float* alpha_s = reinterpret_cast<float*>(ptab + 2 * kHT * kPStride);          // [16]
-  float* amax_s = alpha_s + kHT;                                                  // [8]
+  float2* xpart = reinterpret_cast<float2*>(smem + F::kStages * F::kBlock);   // [2][8 warps][16 rows][kXStride]
+  uint16_t* ptab = reinterpret_cast<uint16_t*>(xpart + 2 * kCW * kHT * kXStride);  // [2 buf][hi, lo][16][kPStride]
+  float* alpha_s = reinterpret_cast<float*>(ptab + 4 * kHT * kPStride);        // [2][16]
+  float* amax_s = alpha_s + 2 * kHT;                                           // [8]
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(amax_s + kCW);
   int32_t* meta = reinterpret_cast<int32_t*>(full_bar + F::kStages);
   int32_t* cum = meta + F::kStages;
@@ -411,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
 
   // ---- loader state (thread 0 only).  plan() looks up the next chunk's page
   // early (its global load then overlaps the QK^T work); commit(s) starts the
-  // copy into stage s.  Invalid pages and chunks past the end of the range
-  // complete the stage's phase with no data.
+  // copy into stage s.  Invalid pages complete the stage's phase with no data
+  // (nv = 0).
   int64_t ld_c = c_lo;
   int ld_b = 0, ld_len = 0, pl_page = -1, pl_t0 = 0;
   bool pl_ready = false;
@@ -455,13 +463,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
   // row hr = T / 16 and tokens 2 (T % 16), +1 of each chunk.
   const int w = warp, r = lane >> 2, j = lane & 3;
   const int hr = tid >> 4, tp = tid & 15;
-  const int rd_n = tp >> 2, rd_lane = 4 * (hr & 7) + (tp & 3), rd_half = hr >> 3;
   Query q;
   float cw = 0.f;                  // softmax_scale * log2 e * 2^-e
   float o[4][2][4];
   float m_row = -INFINITY, l_row = 0.f;
-  int b = -1;
-  int i = 0;
+  uint32_t bq[4][4][2], bq_prev[4][4][2];     // exact codes: [group][ntile][reg]
+  uint32_t s2h[4][4], s2h_prev[4][4];         // fp16 scale pairs of the C-fragment tokens
+  int nv_prev = 0;
+  bool pending = false;
+  int b = -1, s = 0;
+  uint32_t phase = 0;
+  int64_t i = 0;
   bool dead = false;
 
   auto flush = [&](int bb) {
@@ -491,12 +503,121 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
     }
   };
 
-  for (int64_t c = c_lo; c < c_hi && !dead; ++c, ++i) {
-    // ---- sequence boundary: flush the previous partial, load the new query
+  // Step B: sum the 8 warps' partial scores of the chunk in buffer `buf`,
+  // online softmax of row hr, publish P and the rescale factor.
+  auto softmax_step = [&](int buf, int nv) {
+    const float2* xp = xpart + (size_t)buf * kCW * kHT * kXStride + hr * kXStride + tp;
+    float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int ww = 0; ww < kCW; ++ww) {
+      const float2 v = xp[ww * kHT * kXStride];
+      sum.x += v.x;
+      sum.y += v.y;
+    }
+    float x0 = sum.x * cw, x1 = sum.y * cw;
+    if (nv < kChunk) {
+      if (2 * tp >= nv) x0 = -INFINITY;
+      if (2 * tp + 1 >= nv) x1 = -INFINITY;
+    }
+    float mx = fmaxf(x0, x1);
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float mn = fmaxf(m_row, mx);
+    const float al = mn == -INFINITY ? 1.f : ex2(m_row - mn);
+    const float sub = mn == -INFINITY ? 0.f : mn;
+    const float p0 = ex2(x0 - sub), p1 = ex2(x1 - sub);
+    float ps = p0 + p1;
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    l_row = l_row * al + ps;
+    m_row = mn;
+    uint32_t* prow = reinterpret_cast<uint32_t*>(ptab + ((2 * buf) * kHT + hr) * kPStride) + tp;
+    if (F::kLatBf16) {
+      uint32_t phi, plo;
+      split_bf16(p0, p1, phi, plo);
+      prow[0] = phi;
+      prow[kHT * kPStride / 2] = plo;
+    } else {
+      prow[0] = pack_f16(p0, p1);
+    }
+    if (tp == 0) alpha_s[buf * kHT + hr] = al;
+  };
+
+  // Step C: rescale o and accumulate P V of the chunk in buffer `buf`, whose
+  // codes and scales this thread holds in bqv / s2v.
+  auto pv_step = [&](int buf, const uint32_t (&bqv)[4][4][2], const uint32_t (&s2v)[4][4]) {
+    {
+      const float al0 = alpha_s[buf * kHT + r], al1 = alpha_s[buf * kHT + r + 8];
+      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            o[g][e][0] *= al0;
+            o[g][e][1] *= al0;
+            o[g][e][2] *= al1;
+            o[g][e][3] *= al1;
+          }
+      }
+    }
+    uint32_t pa[2][2][4];      // [hi/lo][k step][reg]
+    {
+      const uint32_t pbase = smem_u32(ptab) + (2 * buf) * kHT * kPStride * 2 +
+                             ((lane & 7) + 8 * ((lane >> 3) & 1)) * kPStride * 2 + 8 * (lane >> 4) * 2;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        ldsm_x4(pbase + 32 * ks, pa[0][ks][0], pa[0][ks][1], pa[0][ks][2], pa[0][ks][3]);
+        if (F::kLatBf16)
+          ldsm_x4(pbase + kHT * kPStride * 2 + 32 * ks, pa[1][ks][0], pa[1][ks][1], pa[1][ks][2], pa[1][ks][3]);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t vt[4][2];
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        vt[n][0] = movt(bqv[g][n][0]);
+        vt[n][1] = movt(bqv[g][n][1]);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        if (F::kLatBf16) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            mma_bf16(o[g][e], pa[0][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
+            mma_bf16(o[g][e], pa[1][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
+          }
+        } else {
+          // A = P scaled per token (column) by the group's scale
+          uint32_t ag[4];
+          ag[0] = h2_bits(__hmul2(bits_h2(pa[0][ks][0]), bits_h2(s2v[g][2 * ks])));
+          ag[1] = h2_bits(__hmul2(bits_h2(pa[0][ks][1]), bits_h2(s2v[g][2 * ks])));
+          ag[2] = h2_bits(__hmul2(bits_h2(pa[0][ks][2]), bits_h2(s2v[g][2 * ks + 1])));
+          ag[3] = h2_bits(__hmul2(bits_h2(pa[0][ks][3]), bits_h2(s2v[g][2 * ks + 1])));
+#pragma unroll
+          for (int e = 0; e < 2; ++e) mma_f16(o[g][e], ag, vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
+        }
+      }
+    }
+  };
+
+  auto drain = [&]() {
+    if (!pending) return;
+    const int buf = (int)((i - 1) & 1);
+    softmax_step(buf, nv_prev);
+    consumer_sync();
+    pv_step(buf, bq_prev, s2h_prev);
+    pending = false;
+  };
+
+  for (int64_t c = c_lo; c < c_hi; ++c, ++i) {
+    // ---- sequence boundary: finish the previous chunk, flush the partial,
+    // load the new query
     {
       int nb = b < 0 ? seq_of_chunk(cum, p.B, c) : b;
       while (cum[nb + 1] <= c) ++nb;
       if (nb != b) {
+        drain();
         if (b >= 0) flush(b);
         b = nb;
         QueryRaw raw;
@@ -523,26 +644,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
             for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
       }
     }
-    const int s = i % F::kStages;
     if (tid == 0) plan();
-    if (!mbar_wait(smem_u32(&full_bar[s]), (i / F::kStages) & 1)) {
+    if (!mbar_wait(smem_u32(&full_bar[s]), phase)) {
       set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
       dead = true;
       break;
     }
     const int nv = meta[s];
-    if (nv == 0) {
-      consumer_sync();                 // every warp has read meta[s]
-      if (tid == 0) commit(s);
-      continue;
-    }
-    const bool partial = nv < kChunk;
+    const bool partial = nv < kChunk;     // includes nv == 0 (no data: everything is masked)
     const uint8_t* st = stages + s * F::kBlock;
     const uint32_t st_a = smem_u32(st);
     const float* sc = reinterpret_cast<const float*>(st + F::kScaleOff);
 
-    // ---- B operands: exact codes (or code - zero) of the warp's 4 groups, 4 token tiles
-    uint32_t bq[4][4][2];      // [group][ntile][reg]
+    // ---- step A: B operands (exact codes, or code - zero) and QK^T of chunk i
     if (F::kLatBf16) {
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
@@ -588,7 +702,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
         for (int n = 0; n < 4; ++n) i8x4_to_f16(t[n], bq[g][n][0], bq[g][n][1]);
       }
     }
-    // k_pe B operands
     uint32_t bk[4][2];
     const bool kact = F::kKpeBf16 ? (w < 4) : true;
     if (F::kKpeBf16) {
@@ -609,26 +722,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
       for (int n = 0; n < 4; ++n) i8x4_to_f16(t[n], bk[n][0], bk[n][1]);
     }
 
-    // ---- QK^T partial scores of this warp's channels: acc[ntile][c-reg]
     float acc[4][4];
-    uint32_t s2h[4][4];        // fp16 scale pairs of the C-fragment tokens (8n + 2j, +1), for PV
 #pragma unroll
     for (int n = 0; n < 4; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
     if (F::kLatBf16) {
 #pragma unroll
-      for (int g = 0; g < 4; ++g)
+      for (int g = 0; g < 4; ++g) {
 #pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          mma_bf16(acc[n], q.hi[g], bq[g][n][0], bq[g][n][1], acc[n]);
-          mma_bf16(acc[n], q.lo[g], bq[g][n][0], bq[g][n][1], acc[n]);
-        }
+        for (int n = 0; n < 4; ++n) mma_bf16(acc[n], q.hi[g], bq[g][n][0], bq[g][n][1], acc[n]);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) mma_bf16(acc[n], q.lo[g], bq[g][n][0], bq[g][n][1], acc[n]);
+      }
     } else {
       const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        // four independent hi MMAs, then the lo MMAs that depend on them
         float d[4][4];
 #pragma unroll
         for (int n = 0; n < 4; ++n) mma_f16(d[n], q.hi[g], bq[g][n][0], bq[g][n][1], zero4);
@@ -668,110 +778,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
         acc[n][3] = fmaf(d[3], s2.y, acc[n][3]);
       }
     }
-
-    // ---- publish the partial scores; after the barrier every read of the
-    // stage is done, so thread 0 refills it
-#pragma unroll
-    for (int n = 0; n < 4; ++n) xpart[(w * 4 + n) * 32 + lane] = make_float4(acc[n][0], acc[n][1], acc[n][2], acc[n][3]);
-    consumer_sync();
-    if (tid == 0) commit(s);
-
-    // ---- reduction + online softmax: thread owns row hr, tokens 2tp, 2tp+1
     {
-      float2 sum = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int ww = 0; ww < kCW; ++ww) {
-        const float2 v = reinterpret_cast<const float2*>(&xpart[(ww * 4 + rd_n) * 32 + rd_lane])[rd_half];
-        sum.x += v.x;
-        sum.y += v.y;
-      }
-      float x0 = sum.x * cw, x1 = sum.y * cw;
-      if (partial) {
-        if (2 * tp >= nv) x0 = -INFINITY;
-        if (2 * tp + 1 >= nv) x1 = -INFINITY;
-      }
-      float mx = fmaxf(x0, x1);
-#pragma unroll
-      for (int off = 1; off < 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float mn = fmaxf(m_row, mx);
-      const float al = mn == -INFINITY ? 1.f : ex2(m_row - mn);
-      const float sub = mn == -INFINITY ? 0.f : mn;
-      const float p0 = ex2(x0 - sub), p1 = ex2(x1 - sub);
-      float ps = p0 + p1;
-#pragma unroll
-      for (int off = 1; off < 16; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-      l_row = l_row * al + ps;
-      m_row = mn;
-      uint32_t* prow = reinterpret_cast<uint32_t*>(ptab + hr * kPStride) + tp;
-      if (F::kLatBf16) {
-        uint32_t phi, plo;
-        split_bf16(p0, p1, phi, plo);
-        prow[0] = phi;
-        prow[kHT * kPStride / 2] = plo;
-      } else {
-        prow[0] = pack_f16(p0, p1);
-      }
-      if (tp == 0) alpha_s[hr] = al;
-    }
-    consumer_sync();
-
-    // ---- rescale o, load P as A fragments
-    {
-      const float al0 = alpha_s[r], al1 = alpha_s[r + 8];
-      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            o[g][e][0] *= al0;
-            o[g][e][1] *= al0;
-            o[g][e][2] *= al1;
-            o[g][e][3] *= al1;
-          }
-      }
-    }
-    uint32_t pa[2][2][4];      // [hi/lo][k step][reg]
-    {
-      const uint32_t pbase = smem_u32(ptab) + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kPStride * 2 + 8 * (lane >> 4) * 2;
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        ldsm_x4(pbase + 32 * ks, pa[0][ks][0], pa[0][ks][1], pa[0][ks][2], pa[0][ks][3]);
-        if (F::kLatBf16)
-          ldsm_x4(pbase + kHT * kPStride * 2 + 32 * ks, pa[1][ks][0], pa[1][ks][1], pa[1][ks][2], pa[1][ks][3]);
-      }
-    }
-
-    // ---- P V
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      uint32_t vt[4][2];
+      float2* xw = xpart + (((size_t)(i & 1) * kCW + w) * kHT + r) * kXStride + j;
 #pragma unroll
       for (int n = 0; n < 4; ++n) {
-        vt[n][0] = movt(bq[g][n][0]);
-        vt[n][1] = movt(bq[g][n][1]);
-      }
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        if (F::kLatBf16) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            mma_bf16(o[g][e], pa[0][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
-            mma_bf16(o[g][e], pa[1][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
-          }
-        } else {
-          // A = P scaled per token by the group's scale (columns = tokens)
-          uint32_t ag[4];
-          ag[0] = h2_bits(__hmul2(bits_h2(pa[0][ks][0]), bits_h2(s2h[g][2 * ks])));
-          ag[1] = h2_bits(__hmul2(bits_h2(pa[0][ks][1]), bits_h2(s2h[g][2 * ks])));
-          ag[2] = h2_bits(__hmul2(bits_h2(pa[0][ks][2]), bits_h2(s2h[g][2 * ks + 1])));
-          ag[3] = h2_bits(__hmul2(bits_h2(pa[0][ks][3]), bits_h2(s2h[g][2 * ks + 1])));
-#pragma unroll
-          for (int e = 0; e < 2; ++e) mma_f16(o[g][e], ag, vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
-        }
+        xw[4 * n] = make_float2(acc[n][0], acc[n][1]);
+        xw[8 * kXStride + 4 * n] = make_float2(acc[n][2], acc[n][3]);
       }
     }
+
+    // ---- step B for chunk i - 1, one barrier, refill, step C for chunk i - 1
+    if (pending) softmax_step((int)((i - 1) & 1), nv_prev);
+    consumer_sync();
+    if (tid == 0) commit(s);
+    if (pending) pv_step((int)((i - 1) & 1), bq_prev, s2h_prev);
+
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        bq_prev[g][n][0] = bq[g][n][0];
+        bq_prev[g][n][1] = bq[g][n][1];
+        s2h_prev[g][n] = s2h[g][n];
+      }
+    nv_prev = nv;
+    pending = true;
+    if (++s == F::kStages) {
+      s = 0;
+      phase ^= 1u;
+    }
   }
-  if (b >= 0 && !dead) flush(b);
+  if (!dead) {
+    drain();
+    if (b >= 0) flush(b);
+  }
 }
 
 // Largest dynamic shared memory a block may opt into on the current device.
