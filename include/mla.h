@@ -203,7 +203,9 @@ size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_spli
  *   o_lat fp32 [B][H][512]      lse fp32 [B][H] (natural log; may be NULL)
  *   A page id outside [0, num_pages) contributes nothing and sets
  *   MLA_DEVERR_PAGE; seq_len outside [0, max_pages*64] is treated as 0 and
- *   sets MLA_DEVERR_SEQLEN.  B == 0 is a no-op.  B <= 4096.
+ *   sets MLA_DEVERR_SEQLEN.  B == 0 is a no-op.  B <= 4096, and
+ *   B * max_pages * 2 (the batch's 32-token chunk capacity) < 2^31, else
+ *   MLA_ERR_INVALID_ARG.
  */
 mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
                                const uint16_t* q_pe, const int32_t* block_table,

@@ -133,6 +133,8 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
   if (batch < 0 || batch > kMaxBatch || !heads_ok(heads) || num_splits < 0) return MLA_ERR_INVALID_ARG;
   if (batch == 0) return MLA_OK;
   if (max_pages <= 0 || (int64_t)max_pages * kPage > (int64_t)INT32_MAX) return MLA_ERR_INVALID_ARG;
+  // every 32-token chunk of the batch gets a 32-bit index
+  if ((int64_t)batch * max_pages * (kPage / kChunk) > (int64_t)INT32_MAX) return MLA_ERR_INVALID_ARG;
   if (!q_lat || !q_pe || !block_table || !seq_lens || !workspace || !o_lat) return MLA_ERR_INVALID_ARG;
   if (!aligned(q_lat, 16) || !aligned(q_pe, 16) || !aligned(block_table, 4) || !aligned(seq_lens, 4) ||
       !aligned(workspace, 256) || !aligned(o_lat, 16) || (lse && !aligned(lse, 4)) ||

@@ -22,9 +22,8 @@
 //    after dequantization and a movmatrix transpose, PV.
 //  * QK^T per 16-channel group: mma.m16n8k16 (M = 16 heads, N = 8 tokens,
 //    K = the group's 16 channels) of q_lat split into fp16 hi + lo against
-//    the exact integer codes (INT4: the -z * sum(q_lat) zero-point term
-//    enters through the MMA's C operand), then one fp32 FMA per element
-//    applies the group's per-token scale.  This keeps every product exact, which the
+//    the exact integer codes (INT4: code - zero, formed exactly in fp16),
+//    then one fp32 FMA per element applies the group's per-token scale.  This keeps every product exact, which the
 //    2e-3 bound needs: scores here have a spread of ~10, so a rounding of the
 //    latent or the query to 11 bits would already cost ~1e-3.
 //  * The partial scores of the 8 warps are summed through shared memory by
@@ -206,17 +205,17 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& r0, uint32_t& 
 
 // one int4 word (layout in mla_internal.cuh) -> group A regs (a0, a1) and
 // group B regs (b0, b1), each f16x2 holding code - zero exactly: the nibbles
-// become 1024 + code (or 1024 + 16 code) by bit placement; za / zb hold
-// 1024 + z and ca / cb hold -64 - z of the two groups (f16x2, exact for
-// |z| < 960), and one exact fp16 subtract or fma removes both offsets
-__device__ __forceinline__ void i4x8_to_f16(uint32_t w, uint32_t za, uint32_t ca, uint32_t zb, uint32_t cb,
-                                            uint32_t& a0, uint32_t& a1, uint32_t& b0, uint32_t& b1) {
+// become 1024 + code (or 1024 + 16 code) by bit placement; zo = (1024 + zA,
+// 1024 + zB) and zc = (-64 - zA, -64 - zB) (f16x2, exact for |z| < 960), and
+// one exact fp16 subtract or fma with the broadcast half removes both offsets
+__device__ __forceinline__ void i4x8_to_f16(uint32_t w, __half2 zo, __half2 zc, uint32_t& a0, uint32_t& a1,
+                                            uint32_t& b0, uint32_t& b1) {
   const __half2 k16 = __floats2half2_rn(0.0625f, 0.0625f);
-  a0 = h2_bits(__hsub2(bits_h2((w & 0x000F000Fu) | 0x64006400u), bits_h2(za)));
-  a1 = h2_bits(__hfma2(bits_h2((w & 0x00F000F0u) | 0x64006400u), k16, bits_h2(ca)));
+  a0 = h2_bits(__hsub2(bits_h2((w & 0x000F000Fu) | 0x64006400u), __low2half2(zo)));
+  a1 = h2_bits(__hfma2(bits_h2((w & 0x00F000F0u) | 0x64006400u), k16, __low2half2(zc)));
   const uint32_t v = w >> 8;
-  b0 = h2_bits(__hsub2(bits_h2((v & 0x000F000Fu) | 0x64006400u), bits_h2(zb)));
-  b1 = h2_bits(__hfma2(bits_h2((v & 0x00F000F0u) | 0x64006400u), k16, bits_h2(cb)));
+  b0 = h2_bits(__hsub2(bits_h2((v & 0x000F000Fu) | 0x64006400u), __high2half2(zo)));
+  b1 = h2_bits(__hfma2(bits_h2((v & 0x00F000F0u) | 0x64006400u), k16, __high2half2(zc)));
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -240,7 +239,7 @@ __device__ __forceinline__ int checked_len(const DecodeParams& p, int b, bool re
   return len;
 }
 
-__device__ __forceinline__ int seq_of_chunk(const int32_t* cum, int B, int64_t c) {
+__device__ __forceinline__ int seq_of_chunk(const int32_t* cum, int B, int c) {
   int lo = 0, hi = B - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -256,6 +255,11 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* cum, int B, int64_t c
 struct QueryRaw {            // this thread's fp32 query values, before range scaling
   float4 x[4][2];            // q_lat: [group][row r / r+8], the 4 channels this thread feeds
   float kx[2][4];            // q_pe: [row][4 channels]
+};
+
+struct ChunkRegs {           // one chunk's B operands, kept from QK^T for PV
+  uint32_t bq[4][4][2];      // exact codes (or code - zero): [group][ntile][reg]
+  uint32_t s2h[4][4];        // fp16 scale pairs of the C-fragment tokens: [group][ntile]
 };
 
 struct Query {
@@ -412,16 +416,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
   if (lead)
     for (int i = tid; i <= p.B; i += kThreads) p.ws.cum[i] = cum[i];
 
-  const int64_t C = cum[p.B];
-  const int Ge = (int64_t)G < C ? G : (int)C;          // no empty ranges
+  // chunk indices fit in 32 bits: the host checks B x max_pages x 2 < 2^31
+  const int C = cum[p.B];
+  const int Ge = G < C ? G : C;          // no empty ranges
   if (x >= Ge) return;
-  const int64_t c_lo = range_lo(C, x, Ge), c_hi = range_lo(C, x + 1, Ge);
+  const int c_lo = (int)range_lo(C, x, Ge), c_hi = (int)range_lo(C, x + 1, Ge);
 
   // ---- loader state (thread 0 only).  plan() looks up the next chunk's page
   // early (its global load then overlaps the QK^T work); commit(s) starts the
   // copy into stage s.  Invalid pages complete the stage's phase with no data
   // (nv = 0).
-  int64_t ld_c = c_lo;
+  int ld_c = c_lo;
   int ld_b = 0, ld_len = 0, pl_page = -1, pl_t0 = 0;
   bool pl_ready = false;
   if (tid == 0) {
@@ -431,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
   auto plan = [&]() {
     if (pl_ready || ld_c >= c_hi) return;
     while (cum[ld_b + 1] <= ld_c) ld_len = checked_len(p, ++ld_b, false);
-    pl_t0 = (int)(ld_c - cum[ld_b]) * kChunk;
+    pl_t0 = (ld_c - cum[ld_b]) * kChunk;
     pl_page = p.block_table[(size_t)ld_b * p.max_pages + (pl_t0 >> 6)];
     pl_ready = true;
   };
@@ -467,13 +472,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
   float cw = 0.f;                  // softmax_scale * log2 e * 2^-e
   float o[4][2][4];
   float m_row = -INFINITY, l_row = 0.f;
-  uint32_t bq[4][4][2], bq_prev[4][4][2];     // exact codes: [group][ntile][reg]
-  uint32_t s2h[4][4], s2h_prev[4][4];         // fp16 scale pairs of the C-fragment tokens
+  // Register sets of two consecutive chunks (the loop is unrolled by two and
+  // alternates them, so the set of chunk i-1 is never copied)
+  ChunkRegs ra, rb;
   int nv_prev = 0;
   bool pending = false;
   int b = -1, s = 0;
   uint32_t phase = 0;
-  int64_t i = 0;
+  int i = 0;
   bool dead = false;
 
   auto flush = [&](int bb) {
@@ -601,23 +607,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
     }
   };
 
-  auto drain = [&]() {
+  auto drain = [&](const ChunkRegs& prev) {
     if (!pending) return;
     const int buf = (int)((i - 1) & 1);
     softmax_step(buf, nv_prev);
     consumer_sync();
-    pv_step(buf, bq_prev, s2h_prev);
+    pv_step(buf, prev.bq, prev.s2h);
     pending = false;
   };
 
-  for (int64_t c = c_lo; c < c_hi; ++c, ++i) {
+  // One chunk: QK^T of chunk c into `cur`, softmax and PV of the previous
+  // chunk from `prev`.  Returns false when a wait timed out.
+  auto chunk_step = [&](int c, ChunkRegs& cur, const ChunkRegs& prev) -> bool {
+    uint32_t (&bq)[4][4][2] = cur.bq;
+    uint32_t (&s2h)[4][4] = cur.s2h;
     // ---- sequence boundary: finish the previous chunk, flush the partial,
     // load the new query
     {
       int nb = b < 0 ? seq_of_chunk(cum, p.B, c) : b;
       while (cum[nb + 1] <= c) ++nb;
       if (nb != b) {
-        drain();
+        drain(prev);
         if (b >= 0) flush(b);
         b = nb;
         QueryRaw raw;
@@ -647,8 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
     if (tid == 0) plan();
     if (!mbar_wait(smem_u32(&full_bar[s]), phase)) {
       set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
-      dead = true;
-      break;
+      return false;
     }
     const int nv = meta[s];
     const bool partial = nv < kChunk;     // includes nv == 0 (no data: everything is masked)
@@ -676,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
       }
     } else if (F::kLatInt4) {
       const float* zp = reinterpret_cast<const float*>(st + F::kZeroOff);
-      const __half2 k960 = __floats2half2_rn(960.f, 960.f);
+      const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f), km64 = __floats2half2_rn(-64.f, -64.f);
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t t[4];
@@ -687,10 +696,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
           float za = zp[(4 * w + 2 * cc) * kBlockTokens + 8 * n + r];
           float zb = zp[(4 * w + 2 * cc + 1) * kBlockTokens + 8 * n + r];
           if (partial && 8 * n + r >= nv) za = zb = 0.f;
-          const uint32_t ba = pack_f16(za + 1024.f, za + 1024.f), bb = pack_f16(zb + 1024.f, zb + 1024.f);
-          const uint32_t ca = h2_bits(__hsub2(k960, bits_h2(ba))), cb = h2_bits(__hsub2(k960, bits_h2(bb)));
-          i4x8_to_f16(t[n], ba, ca, bb, cb, bq[2 * cc][n][0], bq[2 * cc][n][1], bq[2 * cc + 1][n][0],
-                      bq[2 * cc + 1][n][1]);
+          const __half2 zz = __floats2half2_rn(za, zb);            // exact (integer zero-points)
+          i4x8_to_f16(t[n], __hadd2(zz, k1024), __hsub2(km64, zz), bq[2 * cc][n][0], bq[2 * cc][n][1],
+                      bq[2 * cc + 1][n][0], bq[2 * cc + 1][n][1]);
         }
       }
     } else {
@@ -791,25 +799,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
     if (pending) softmax_step((int)((i - 1) & 1), nv_prev);
     consumer_sync();
     if (tid == 0) commit(s);
-    if (pending) pv_step((int)((i - 1) & 1), bq_prev, s2h_prev);
-
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        bq_prev[g][n][0] = bq[g][n][0];
-        bq_prev[g][n][1] = bq[g][n][1];
-        s2h_prev[g][n] = s2h[g][n];
-      }
+    if (pending) pv_step((int)((i - 1) & 1), prev.bq, prev.s2h);
     nv_prev = nv;
     pending = true;
+    ++i;
     if (++s == F::kStages) {
       s = 0;
       phase ^= 1u;
     }
+    return true;
+  };
+
+  bool last_in_a = false;
+  for (int c = c_lo; c < c_hi; c += 2) {
+    if (!chunk_step(c, ra, rb)) { dead = true; break; }
+    last_in_a = true;
+    if (c + 1 >= c_hi) break;
+    if (!chunk_step(c + 1, rb, ra)) { dead = true; break; }
+    last_in_a = false;
   }
   if (!dead) {
-    drain();
+    if (last_in_a) drain(ra);
+    else drain(rb);
     if (b >= 0) flush(b);
   }
 }

@@ -87,4 +87,8 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert raw.mla_decode_absorbed(*args(1 << 30, 0.0, 2)) == 1
     assert raw.mla_decode_absorbed(*args(1 << 30, 0.07, 5000)) == 1
     assert raw.mla_decode_absorbed(*args(1 << 30, 0.07, 0)) == 0
+    # decode: the batch's chunk capacity B * max_pages * 2 must stay below 2^31
+    big = (ctypes.byref(cs), fake, fake, fake, 1 << 18, fake, 4096, 16, 0.07, 3, ctypes.c_void_p(0x200000), 1 << 40,
+           fake, None, None, None)
+    assert raw.mla_decode_absorbed(*big) == 1
     assert raw.mla_status_string(4) == b"device-side bounds error"
