@@ -42,12 +42,15 @@ CONFIGS = {
                          desc="V2-Lite shapes, batch 1, context 1,048,576, asymmetric INT4 latent + INT8 k_pe"),
     "long_bf16_256k": dict(layers=27, heads=16, batch=1, ctx=262144, latent="bf16", kpe="bf16",
                            desc="V2-Lite shapes, batch 1, context 262,144, bf16 latent + bf16 k_pe"),
-    "mixed_h64_int8": dict(layers=1, heads=64, batch=64, ctx="loguniform", latent="int8", kpe="int8",
-                           desc="64 heads, batch 64, context log-uniform in [1K, 64K], INT8 latent + k_pe"),
-    "mixed_h64_int4": dict(layers=1, heads=64, batch=64, ctx="loguniform", latent="int4", kpe="int8",
-                           desc="64 heads, batch 64, context log-uniform in [1K, 64K], INT4 latent + INT8 k_pe"),
-    "mixed_h64_bf16": dict(layers=1, heads=64, batch=64, ctx="loguniform", latent="bf16", kpe="bf16",
-                           desc="64 heads, batch 64, context log-uniform in [1K, 64K], bf16 latent + k_pe"),
+    "mixed_h64_int8": dict(layers=1, heads=64, batch=64, ctx="loguniform", latent="int8", kpe="int8", prefill=8192,
+                           desc="mixed serving step: prefill append of 8192 tokens + decode of batch 64 with "
+                                "context log-uniform in [1K, 64K], 64 heads, INT8 latent + k_pe"),
+    "mixed_h64_int4": dict(layers=1, heads=64, batch=64, ctx="loguniform", latent="int4", kpe="int8", prefill=8192,
+                           desc="mixed serving step: prefill append of 8192 tokens + decode of batch 64 with "
+                                "context log-uniform in [1K, 64K], 64 heads, INT4 latent + INT8 k_pe"),
+    "mixed_h64_bf16": dict(layers=1, heads=64, batch=64, ctx="loguniform", latent="bf16", kpe="bf16", prefill=8192,
+                           desc="mixed serving step: prefill append of 8192 tokens + decode of batch 64 with "
+                                "context log-uniform in [1K, 64K], 64 heads, bf16 latent + k_pe"),
     "tiny": dict(layers=1, heads=16, batch=1, ctx=256, latent="int8", kpe="int8",
                  desc="1 layer, 16 heads, batch 1, context 256"),
 }
@@ -160,6 +163,7 @@ def _oracle_worker(conn, cfg, seq_lens, tasks, seed):
     from oracle import quant as Q
     lf, kf = FMT[cfg["latent"]], FMT[cfg["kpe"]]
     H, B = cfg["heads"], len(seq_lens)
+    P = cfg.get("prefill", 0)
     state = []
     for (l, b) in tasks:                     # untimed: the cache as the step finds it
         T = seq_lens[b]
@@ -170,14 +174,22 @@ def _oracle_worker(conn, cfg, seq_lens, tasks, seed):
         q = [synth.bf16_to_f32(a) for a in (synth.q_nope_bf16(seed, l, B, H)[b:b + 1],
                                              synth.q_pe_bf16(seed, l, B, H)[b:b + 1],
                                              synth.w_uk_bf16(seed, l, H), synth.w_uv_bf16(seed, l, H))]
-        state.append((stored, c[T - 1:], k[T - 1:], q))
+        pre = None
+        if P:                                # the prefill tokens this layer appends every step
+            pcos, psin = synth.rope_tables(P)
+            st = synth.channel_stats(seed, l)
+            pre = (synth.bf16_to_f32(synth.latent_bf16(seed, l, B, 0, P, stats=st)),
+                   synth.bf16_to_f32(synth.kpe_bf16(seed, l, B, 0, P, pcos, psin)))
+        state.append((stored, c[T - 1:], k[T - 1:], q, pre))
     conn.send("ready")
     while True:
         msg = conn.recv()
         if msg == "stop":
             break
         t0 = time.perf_counter()
-        for stored, c_new, k_new, (qn, qp, wuk, wuv) in state:
+        for stored, c_new, k_new, (qn, qp, wuk, wuv), pre in state:
+            if pre is not None:
+                Q.quantize_token_rows(pre[0], pre[1], lf, kf)        # prefill append
             new = Q.quantize_token_rows(c_new, k_new, lf, kf)      # append the new token
             c_hat = np.concatenate([_dequant_latent(Q, stored, lf), new["c_hat"]])
             kpe_hat = np.concatenate([_dequant_kpe(Q, stored, kf), new["kpe_hat"]])
@@ -250,9 +262,11 @@ def cpu_baseline(cfg, seq_lens, min_seconds=8.0, steps=None, warmup=1):
     r.close()
     total = sum(times)
     return {"value": len(times) / total, "unit": "tokens/s", "cores": r.n, "kind": "oracle",
-            "sample": "sequence 0 through all %d layers per step (context %d), layers spread over %d "
+            "sample": "sequence 0 through all %d layers per step (context %d)%s, layers spread over %d "
                       "spawned single-BLAS-thread processes; %d steps, %.1f s" % (
-                          cfg["layers"], seq_lens[0], r.n, len(times), total),
+                          cfg["layers"], seq_lens[0],
+                          (" plus the %d-token prefill append" % cfg["prefill"]) if cfg.get("prefill") else "",
+                          r.n, len(times), total),
             "ms_per_step": 1000 * total / len(times), "steps": len(times)}
 
 
@@ -270,7 +284,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     seq_lens = seq_lens_for(cfg, seed)
     layers = args.layers or cfg["layers"]
     t_setup = time.time()
-    wl = Workload(layers, cfg["heads"], seq_lens, FMT[cfg["latent"]], FMT[cfg["kpe"]], seed, device=dev)
+    wl = Workload(layers, cfg["heads"], seq_lens, FMT[cfg["latent"]], FMT[cfg["kpe"]], seed, device=dev,
+                  prefill=cfg.get("prefill", 0))
     step = DecodeStep(wl, num_splits=args.num_splits)
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -333,11 +348,43 @@ def run_ours(args, cfg, rank, world, local_rank):
     torch.cuda.synchronize()
     dec_ms = a.elapsed_time(b) / (reps * wl.L)
 
+    # ---- the prefill append (mixed serving step) timed alone: one graph of R
+    # appends, each from its own input copy into its own pages of a scratch
+    # pool, so that the R x (inputs + pages) working set exceeds L2
+    pre = None
+    if wl.prefill:
+        import numpy as np
+        R, P, pp = 16, wl.prefill, wl.prefill_pages
+        tcache = mla.CacheLayer(R * pp, wl.latent_fmt, wl.kpe_fmt, device=dev)
+        t = np.arange(P)
+        sets = [(wl.c_pre[0].clone(), wl.kpe_pre[0].clone(),
+                 torch.from_numpy(((t // 64 + r * pp) * 64 + t % 64).astype(np.int32)).to(dev)) for r in range(R)]
+        pgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pgraph, stream=stream):
+            for c_in, k_in, sl in sets:
+                mla.mla_cache_append(tcache, c_in, k_in, sl, step.dev_err)
+        with torch.cuda.stream(stream):
+            pgraph.replay()
+            a.record(stream)
+            for _ in range(reps):
+                pgraph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        pre_ms = a.elapsed_time(b) / (reps * R)
+        del sets, tcache
+        beta_w = BETA[(cfg["latent"], cfg["kpe"])]
+        pre_bytes = wl.prefill * ((512 + 64) * 2 + 4 + beta_w)     # bf16 rows + slot in, cache bytes out
+        peak0, _ = hbm_peak()
+        pre = {"bound": "hbm", "tokens": wl.prefill, "bytes_per_launch": pre_bytes, "launch_ms": pre_ms,
+               "achieved": pre_bytes / (pre_ms * 1e-3) / 1e9, "peak": peak0, "unit": "GB/s",
+               "frac": pre_bytes / (pre_ms * 1e-3) / 1e9 / peak0}
+
     # ---- end to end through the public API with host buffers
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
     host_in = [(pin(wl.c_new[l]), pin(wl.kpe_new[l]), pin(wl.q_nope[l]), pin(wl.q_pe[l])) for l in range(wl.L)]
+    host_pre = [(pin(wl.c_pre[l]), pin(wl.kpe_pre[l])) for l in range(wl.L)] if wl.prefill else []
     host_out = torch.empty(step.o.shape, dtype=step.o.dtype, pin_memory=True)
-    h2d = sum(sum(t.numel() * t.element_size() for t in x) for x in host_in)
+    h2d = sum(sum(t.numel() * t.element_size() for t in x) for x in host_in + host_pre)
     d2h = host_out.numel() * host_out.element_size()
     e2e_steps = max(3, min(args.steps, 50))
     done = torch.cuda.Event()
@@ -351,6 +398,9 @@ def run_ours(args, cfg, rank, world, local_rank):
                 wl.kpe_new[l].copy_(k, non_blocking=True)
                 wl.q_nope[l].copy_(qn, non_blocking=True)
                 wl.q_pe[l].copy_(qp, non_blocking=True)
+            for l, (c, k) in enumerate(host_pre):
+                wl.c_pre[l].copy_(c, non_blocking=True)
+                wl.kpe_pre[l].copy_(k, non_blocking=True)
             graph.replay()
             host_out.copy_(step.o, non_blocking=True)
             done.record(stream)
@@ -400,9 +450,10 @@ def run_ours(args, cfg, rank, world, local_rank):
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": tokens_per_step / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * layers * 5,
+        "gpu_launches": args.steps * layers * (6 if wl.prefill else 5),
         "device_error_word": err_word,
         "clocks": clk,
+        "prefill_append": pre,
         "setup_s": round(setup_s, 1),
     }
     return out, seq_lens

@@ -72,6 +72,8 @@ constexpr int kAbAS = kDn + 8;       // A tile row stride (bf16): 272 B
 __global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t* __restrict__ q_nope,
                                                        const uint16_t* __restrict__ w_uk,
                                                        float* __restrict__ q_lat, int B, int H) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ __align__(16) uint16_t ws[kDn * kAbWS];
   __shared__ __align__(16) uint16_t as[16 * kAbAS];
   const int h = blockIdx.x, n0 = blockIdx.y * kAbN;
@@ -127,6 +129,8 @@ constexpr int kUnWS = kUnN + 8;      // W tile row stride (bf16): 48 B, conflict
 __global__ void __launch_bounds__(128) out_unabsorb_kernel(const float* __restrict__ o_lat,
                                                            const uint16_t* __restrict__ w_uv,
                                                            float* __restrict__ o, int B, int H) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ __align__(16) uint16_t ws[kDc * kUnWS];
   __shared__ float part[4][16][kUnN];
   const int h = blockIdx.x, v0 = blockIdx.y * kUnN;
@@ -185,14 +189,12 @@ __global__ void __launch_bounds__(128) out_unabsorb_kernel(const float* __restri
 
 mla_status launch_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_lat, int B, int H,
                            cudaStream_t stream) {
-  q_absorb_kernel<<<dim3(H, kDc / kAbN), 128, 0, stream>>>(q_nope, w_uk, q_lat, B, H);
-  return launch_status();
+  return cuda_status(launch_pdl(q_absorb_kernel, dim3(H, kDc / kAbN), dim3(128), 0, stream, q_nope, w_uk, q_lat, B, H));
 }
 
 mla_status launch_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o, int B, int H,
                                cudaStream_t stream) {
-  out_unabsorb_kernel<<<dim3(H, kDv / kUnN), 128, 0, stream>>>(o_lat, w_uv, o, B, H);
-  return launch_status();
+  return cuda_status(launch_pdl(out_unabsorb_kernel, dim3(H, kDv / kUnN), dim3(128), 0, stream, o_lat, w_uv, o, B, H));
 }
 
 }  // namespace mla

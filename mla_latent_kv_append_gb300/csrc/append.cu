@@ -13,11 +13,19 @@
 // for INT8) in the page's chunk order: 16-byte chunks swizzled by token, INT4
 // nibbles of two groups interleaved per chunk (see mla_internal.cuh).
 //
-// Bit-exactness: every step is an IEEE fp32 operation with round-to-nearest
-// (__fdiv_rn, __fsub_rn, __fadd_rn) or round-half-even to integer (rintf),
-// never a fused multiply-add, in the same order as the plain definition, so
-// codes, scales and zero-points equal those of any correct fp32
-// implementation bit for bit.  Denormals are kept (no flush-to-zero).
+// Bit-exactness: every step yields the IEEE fp32 round-to-nearest result of
+// the plain definition's operation (x / s, max - min, ...), in the same order,
+// followed by round-half-even to integer (rintf), so codes, scales and
+// zero-points equal those of any correct fp32 implementation bit for bit.
+// Denormals are kept (no flush-to-zero).  The per-element quotients x / s of
+// a group share one divisor and use Markstein's FMA division (P. Markstein,
+// "IA-64 and Elementary Functions", 2000): with y = RN(1/s), q0 = RN(x y) and
+// one correction q1 = RN(q0 + RN(x - s q0) y), q1 is within an ulp of x / s,
+// so the residual x - s q1 is exact in one FMA and q2 = RN(q1 + (x - s q1) y)
+// is the correctly rounded quotient RN(x / s).  The theorem needs no
+// overflow or underflow on the way, so a divisor outside [2^-100, 2^100]
+// takes the plain IEEE division instead (quotients here are at most 127 for
+// INT8 and 15 * 2^24 for INT4, so none overflows).
 #include "mla_internal.cuh"
 
 namespace mla {
@@ -33,6 +41,23 @@ __device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float* 
   }
 }
 
+// RN(x[i] / s) for N values sharing the divisor s > 0 (see the header).
+template <int N>
+__device__ __forceinline__ void div_rn_shared(const float* x, float s, float* out) {
+  if (s >= 0x1p-100f && s <= 0x1p100f) {
+    const float y = __frcp_rn(s);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const float q0 = __fmul_rn(x[i], y);
+      const float q1 = __fmaf_rn(__fmaf_rn(-q0, s, x[i]), y, q0);
+      out[i] = __fmaf_rn(__fmaf_rn(-q1, s, x[i]), y, q1);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) out[i] = __fdiv_rn(x[i], s);
+  }
+}
+
 // Symmetric INT8 of n values; returns the scale, writes int8 codes.
 template <int N>
 __device__ __forceinline__ float quant_sym8(const float* x, int8_t* q) {
@@ -40,10 +65,11 @@ __device__ __forceinline__ float quant_sym8(const float* x, int8_t* q) {
 #pragma unroll
   for (int i = 0; i < N; ++i) a = fmaxf(a, fabsf(x[i]));
   const float s = __fdiv_rn(a, 127.f);
+  float d[N];
+  if (s > 0.f) div_rn_shared<N>(x, s, d);
 #pragma unroll
   for (int i = 0; i < N; ++i) {
-    float r = 0.f;
-    if (s > 0.f) r = fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -127.f), 127.f);
+    const float r = s > 0.f ? fminf(fmaxf(rintf(d[i]), -127.f), 127.f) : 0.f;
     q[i] = (int8_t)(int)r;
   }
   return s;
@@ -60,11 +86,14 @@ __device__ __forceinline__ void quant_asym4(const float* x, float& s_out, float&
   float s = __fdiv_rn(__fsub_rn(mx, mn), 15.f);
   if (s == 0.f) s = fabsf(mn);
   float z = 0.f;
-  if (s > 0.f) z = rintf(__fdiv_rn(-mn, s));
+  float d[16];
+  if (s > 0.f) {
+    z = rintf(__fdiv_rn(-mn, s));
+    div_rn_shared<16>(x, s, d);
+  }
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    float r = 0.f;
-    if (s > 0.f) r = fminf(fmaxf(__fadd_rn(rintf(__fdiv_rn(x[i], s)), z), 0.f), 15.f);
+    const float r = s > 0.f ? fminf(fmaxf(__fadd_rn(rintf(d[i]), z), 0.f), 15.f) : 0.f;
     q[i] = (uint8_t)(int)r;
   }
   s_out = s;
@@ -77,6 +106,8 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
                                                      const uint16_t* __restrict__ kpe_new,
                                                      const int32_t* __restrict__ slot, int n,
                                                      int32_t* dev_err) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   for (int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; i < n; i += warps) {
@@ -116,17 +147,16 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
         quant_asym4(x, sc, zp, q);
         scale[lane * kBlockTokens + t] = sc;
         reinterpret_cast<float*>(blk + L.zero_off)[lane * kBlockTokens + t] = zp;
-        // this lane's nibbles of the shared chunk (groups 2c and 2c+1), then
-        // merge with the partner lane's
+        // this lane's nibbles of the shared chunk (groups 2c and 2c+1): the
+        // group's channels 4j, 4j+2, 4j+1, 4j+3 sit at nibbles 0, 1, 4, 5 of
+        // word j for the chunk's first group and 2, 3, 6, 7 for the second
+        // (int4_nibble_channel); then merge with the partner lane's
         uint32_t w[4];
+        const int sh = 8 * (lane & 1);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          uint32_t v = 0;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const int ch = int4_nibble_channel(j, k);
-            if ((ch >> 4) == (lane & 1)) v |= (uint32_t)q[ch & 15] << (4 * k);
-          }
+          const uint32_t v = ((uint32_t)q[4 * j] | ((uint32_t)q[4 * j + 2] << 4) | ((uint32_t)q[4 * j + 1] << 16) |
+                              ((uint32_t)q[4 * j + 3] << 20)) << sh;
           w[j] = v | __shfl_xor_sync(0xffffffffu, v, 1);
         }
         if ((lane & 1) == 0)
@@ -170,9 +200,9 @@ mla_status launch_t(const mla_cache_layer* cache, const PageLayout& L, const uin
   int64_t want = ((int64_t)n + warps_per_block - 1) / warps_per_block;
   int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 16;
   int grid = (int)(want < cap ? want : cap);
-  append_kernel<LF, KF><<<grid, 32 * warps_per_block, 0, stream>>>(
-      (uint8_t*)cache->pool, L, (int64_t)cache->num_pages * kPage, c_new, kpe_new, slot, n, dev_err);
-  return launch_status();
+  return cuda_status(launch_pdl(append_kernel<LF, KF>, dim3(grid), dim3(32 * warps_per_block), 0, stream,
+                                (uint8_t*)cache->pool, L, (int64_t)cache->num_pages * kPage, c_new, kpe_new, slot,
+                                n, dev_err));
 }
 
 }  // namespace

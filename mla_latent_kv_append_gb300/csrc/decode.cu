@@ -76,6 +76,8 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* cum, int B, int64_t c
 
 template <int LF, int KF>
 __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ __align__(16) float smem[];
   float* s_qlat = smem;                       // [16][512]
   float* s_qpe = s_qlat + kHT * kDc;          // [16][64]
@@ -339,6 +341,8 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
 }
 
 __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ float sw[kCombSlots];
   __shared__ float red[4];
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
@@ -405,8 +409,7 @@ mla_status launch_ref_t(const DecodeParams& p, cudaStream_t stream) {
     if (st != MLA_OK) return st;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  decode_ref_kernel<LF, KF><<<dim3(p.G, p.H / kHT), kThreads, smem, stream>>>(p);
-  return launch_status();
+  return cuda_status(launch_pdl(decode_ref_kernel<LF, KF>, dim3(p.G, p.H / kHT), dim3(kThreads), smem, stream, p));
 }
 
 mla_status launch_decode_ref(const DecodeParams& p, cudaStream_t stream) {
@@ -429,8 +432,7 @@ mla_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
   mla_status st = force_ref ? MLA_ERR_UNSUPPORTED : launch_decode_mma(p, stream);
   if (st == MLA_ERR_UNSUPPORTED) st = launch_decode_ref(p, stream);
   if (st != MLA_OK) return st;
-  combine_kernel<<<dim3(p.B, p.H), 128, 0, stream>>>(p);
-  return launch_status();
+  return cuda_status(launch_pdl(combine_kernel, dim3(p.B, p.H), dim3(128), 0, stream, p));
 }
 
 }  // namespace mla

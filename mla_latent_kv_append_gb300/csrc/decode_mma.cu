@@ -378,6 +378,8 @@ __device__ __forceinline__ void finish_query(const QueryRaw& raw, float up, Quer
 template <int LF, int KF>
 __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p) {
   using F = Fmt<LF, KF>;
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   float2* xpart = reinterpret_cast<float2*>(smem + F::kStages * F::kBlock);   // [2][8 warps][16 rows][kXStride]
@@ -852,8 +854,7 @@ mla_status launch_t(const DecodeParams& p, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
   if (smem > smem_max()) return MLA_ERR_UNSUPPORTED;
-  decode_mma_kernel<LF, KF><<<dim3(p.G, p.H / kHT), kThreads, smem, stream>>>(p);
-  return launch_status();
+  return cuda_status(launch_pdl(decode_mma_kernel<LF, KF>, dim3(p.G, p.H / kHT), dim3(kThreads), smem, stream, p));
 }
 
 }  // namespace

@@ -132,6 +132,34 @@ __host__ __device__ inline Workspace carve_workspace(void* base, int B, int H, i
 // last chunk record themselves in span[], so the combine needs no division.
 __host__ __device__ inline int64_t range_lo(int64_t C, int x, int G) { return C * x / G; }
 
+// Programmatic dependent launch.  Every kernel of the library lets the next
+// kernel in the stream begin launching as soon as all of its own blocks are
+// running (pdl_launch_dependents), and waits for the previous kernel to
+// complete and its memory to be visible (pdl_wait) before its first global
+// memory access, in every block.  Results are ordered exactly as in plain
+// stream order; the next grid's launch and block scheduling overlap this
+// grid's tail.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Host side launch helpers (api.cu)
 int device_sm_count();
 mla_status launch_status();

@@ -7,6 +7,11 @@ into the caches by the library's own quantize-on-write call; the decode step
 appends token T-1 and attends over all T.  Physical pages are a seeded
 permutation, so block tables are scattered as in a real pool.
 
+A workload may also carry a prefill: P tokens of one further sequence
+(index B, positions 0..P-1) that every step appends to every layer before the
+decode step, into spare pages of the same pools (the mixed serving step:
+prefill quantize-on-write plus batched decode).
+
 Host twins of every tensor come from ``synth`` (NumPy) for the oracle.
 """
 
@@ -20,7 +25,7 @@ import mla_latent_kv_append_gb300 as mla
 
 class Workload:
     def __init__(self, layers, heads, seq_lens, latent_fmt, kpe_fmt, seed, device="cuda", fill=True,
-                 fill_chunk=65536):
+                 fill_chunk=65536, prefill=0):
         self.L, self.H = int(layers), int(heads)
         self.seq_lens = [int(t) for t in seq_lens]
         self.B = len(self.seq_lens)
@@ -28,6 +33,8 @@ class Workload:
         pages = [(t + 63) // 64 for t in self.seq_lens]
         self.max_pages = max(1, max(pages) if pages else 1)
         self.num_pages = max(1, sum(pages))
+        self.prefill = int(prefill)
+        self.prefill_pages = (self.prefill + 63) // 64
         perm = synth.page_permutation(seed, self.num_pages)
         bt = np.full((self.B, self.max_pages), -1, np.int32)
         k = 0
@@ -37,8 +44,9 @@ class Workload:
         self.block_table_host = bt
         self.block_table = torch.from_numpy(bt).to(device)
         self.seq_lens_dev = torch.tensor(self.seq_lens, dtype=torch.int32, device=device)
-        self.caches = [mla.CacheLayer(self.num_pages, latent_fmt, kpe_fmt, device=device) for _ in range(self.L)]
-        self.rope = sd.RopeTables(max(1, max(self.seq_lens) if self.seq_lens else 1), device)
+        self.caches = [mla.CacheLayer(self.num_pages + self.prefill_pages, latent_fmt, kpe_fmt, device=device)
+                       for _ in range(self.L)]
+        self.rope = sd.RopeTables(max(1, self.prefill, max(self.seq_lens) if self.seq_lens else 1), device)
         self.w_uk = [sd.w_uk(seed, l, self.H, device) for l in range(self.L)]
         self.w_uv = [sd.w_uv(seed, l, self.H, device) for l in range(self.L)]
         self.q_nope = [sd.q_nope(seed, l, self.B, self.H, device) for l in range(self.L)]
@@ -57,6 +65,21 @@ class Workload:
                     sd.kpe_into(kk[b:b + 1], seed, l, b, t - 1, self.rope, kind=synth.KIND_NEW_KPE)
             self.c_new.append(c)
             self.kpe_new.append(kk)
+        # prefill: sequence B's P tokens, in a seeded order of the spare pages
+        self.c_pre, self.kpe_pre, self.slot_pre_host = [], [], None
+        if self.prefill:
+            spare = self.num_pages + synth.page_permutation(seed + 1, self.prefill_pages).astype(np.int64)
+            t = np.arange(self.prefill)
+            self.slot_pre_host = (spare[t // 64] * 64 + t % 64).astype(np.int32)
+            self.slot_pre = torch.from_numpy(self.slot_pre_host).to(device)
+            for l in range(self.L):
+                st = sd.LayerStats(seed, l, device)
+                c = torch.empty((self.prefill, synth.D_C), dtype=torch.bfloat16, device=device)
+                kk = torch.empty((self.prefill, synth.D_R), dtype=torch.bfloat16, device=device)
+                sd.latent_into(c, seed, l, self.B, 0, st)
+                sd.kpe_into(kk, seed, l, self.B, 0, self.rope)
+                self.c_pre.append(c)
+                self.kpe_pre.append(kk)
         if fill:
             self.fill(fill_chunk)
 
@@ -90,6 +113,13 @@ class Workload:
         cos, sin = synth.rope_tables(max(1, T))
         return synth.sequence_bf16(self.seed, layer, b, T, cos, sin, stats=synth.channel_stats(self.seed, layer))
 
+    def host_prefill(self, layer):
+        """bf16 bits of the prefill tokens (sequence B, positions 0..P-1)."""
+        cos, sin = synth.rope_tables(max(1, self.prefill))
+        stats = synth.channel_stats(self.seed, layer)
+        return (synth.latent_bf16(self.seed, layer, self.B, 0, self.prefill, stats=stats),
+                synth.kpe_bf16(self.seed, layer, self.B, 0, self.prefill, cos, sin))
+
     def host_query(self, layer):
         return (synth.q_nope_bf16(self.seed, layer, self.B, self.H), synth.q_pe_bf16(self.seed, layer, self.B, self.H),
                 synth.w_uk_bf16(self.seed, layer, self.H), synth.w_uv_bf16(self.seed, layer, self.H))
@@ -97,7 +127,8 @@ class Workload:
 
 class DecodeStep:
     """Buffers and the per-layer call sequence of one decode step:
-    append -> absorb -> decode (+combine) -> unabsorb, for every layer."""
+    [prefill append ->] append -> absorb -> decode (+combine) -> unabsorb,
+    for every layer."""
 
     def __init__(self, wl, num_splits=0, with_lse=True):
         dev = wl.device
@@ -113,6 +144,8 @@ class DecodeStep:
     def run(self, keep_o_lat=None):
         wl = self.wl
         for l in range(wl.L):
+            if wl.prefill:
+                mla.mla_cache_append(wl.caches[l], wl.c_pre[l], wl.kpe_pre[l], wl.slot_pre, self.dev_err)
             mla.mla_cache_append(wl.caches[l], wl.c_new[l], wl.kpe_new[l], wl.slot_new, self.dev_err)
             mla.mla_q_absorb(wl.q_nope[l], wl.w_uk[l], self.q_lat)
             mla.mla_decode_absorbed(wl.caches[l], self.q_lat, wl.q_pe[l], wl.block_table, wl.seq_lens_dev,

@@ -99,3 +99,50 @@ def test_prefill_sized_append(lf):
     torch.cuda.synchronize()
     got = read_tokens(cache.pool.cpu().numpy(), cache.layout, lf, mla.FMT_INT8_SYM, slots)
     assert_fields_match(got, c, k, lf, mla.FMT_INT8_SYM)
+
+
+def near_tie_rows(n_rows, lf, seed=123):
+    """Latent rows whose per-group quotients x / s sit at or within a few fp32
+    ulps of half-integers (the cases where a division that is not correctly
+    rounded would change a code).  Each group holds its extreme values, so
+    the scale is known on the host."""
+    rng = np.random.default_rng(seed)
+    b16 = lambda v: np.float32(synth.bf16_to_f32(synth.bf16_rne(np.array([v], np.float32)))[0])
+    rows = np.zeros((n_rows, 512), np.float32)
+    for i in range(n_rows):
+        for g in range(32):
+            if lf == mla.FMT_INT8_SYM:
+                a = b16(abs(rng.standard_normal()) * 2.0 ** rng.integers(-20, 20)) or np.float32(1)
+                s = np.float32(a / np.float32(127))
+                vals, lo, hi = [a], -a, a
+            else:
+                mn = b16(rng.standard_normal() * 2.0 ** rng.integers(-10, 10))
+                mx = b16(mn + abs(rng.standard_normal()) * 2.0 ** rng.integers(-8, 8))
+                if mx <= mn:
+                    mx = b16(mn + abs(mn) * 0.05 + 1e-3)
+                s = np.float32(np.float32(mx - mn) / np.float32(15))
+                vals, lo, hi = [mn, mx], mn, mx
+            k0 = int(np.floor(lo / np.float64(s)))
+            tries = 0
+            while len(vals) < 16 and tries < 200:
+                tries += 1
+                k = rng.integers(k0, k0 + 255 if lf == mla.FMT_INT8_SYM else k0 + 16)
+                x = b16((k + 0.5) * np.float64(s))
+                if lo <= x <= hi:
+                    vals.append(x)
+            vals += [lo] * (16 - len(vals))
+            rows[i, 16 * g:16 * g + 16] = rng.permutation(np.array(vals, np.float32))
+    return synth.bf16_rne(rows)
+
+
+@pytest.mark.parametrize("lf", [mla.FMT_INT8_SYM, mla.FMT_INT4_ASYM])
+def test_near_tie_quotients_bit_exact(lf):
+    n = 256
+    c = near_tie_rows(n, lf)
+    k = c[:, :64].copy()
+    slots = np.arange(n, dtype=np.int32)
+    cache = mla.CacheLayer(n // 64, lf, mla.FMT_INT8_SYM)
+    mla.mla_cache_append(cache, to_dev(c), to_dev(k), torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    got = read_tokens(cache.pool.cpu().numpy(), cache.layout, lf, mla.FMT_INT8_SYM, slots)
+    assert_fields_match(got, c, k, lf, mla.FMT_INT8_SYM)

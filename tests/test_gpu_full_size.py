@@ -8,7 +8,8 @@ INT8 workload and the 64-head mixed-length workloads; for the 32K, 256K and
 oracle works through each sequence in 32K-token ranges in spawned host
 processes and merges the ranges with its log-sum-exp combine.  Stored codes,
 scales and zero-points are compared bit for bit on sampled token windows
-(first, last, and random ones) of the compared layers.
+(first, last, and random ones) of the compared layers; the mixed serving
+step's 8192-token prefill append is compared in full.
 """
 
 import gc
@@ -74,7 +75,7 @@ def test_full_size_parity(pool, name, layers):
     layers = list(range(L)) if layers is None else [l for l in layers if l < L]
     gc.collect()
     torch.cuda.empty_cache()                      # the previous workload's cache pools
-    wl = Workload(L, H, seq_lens, lf, kf, seed)
+    wl = Workload(L, H, seq_lens, lf, kf, seed, prefill=cfg.get("prefill", 0))
     step = DecodeStep(wl)                         # automatic split count, as timed by the bench
     keep = torch.empty((L, wl.B, H, synth.D_C), dtype=torch.float32, device="cuda")
     o = step.run(keep_o_lat=keep)
@@ -92,3 +93,8 @@ def test_full_size_parity(pool, name, layers):
         assert e1 < ATTN_TOL and e2 < ATTN_TOL and e3 < ATTN_TOL, (name, l, b, e1, e2, e3)
     print("%s: %d (layer, sequence) pairs compared, worst max-rel error %.2e" % (name, len(ref), worst))
     check_stored_windows(wl, layers[:1] + layers[-1:], np.random.default_rng(len(name)))
+    if wl.prefill:                    # the serving step's prefill append, every token
+        for l in layers[:1] + layers[-1:]:
+            c, k = wl.host_prefill(l)
+            got = read_tokens(wl.caches[l].pool.cpu().numpy(), wl.caches[l].layout, lf, kf, wl.slot_pre_host)
+            assert_fields_match(got, c, k, lf, kf)
