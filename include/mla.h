@@ -251,6 +251,24 @@ mla_status mla_decode_absorbed_noalloc(const mla_cache_layer* cache, const float
 mla_status mla_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o,
                             int32_t batch, int32_t heads, mla_stream_t stream);
 
+/*
+ * mla_lse_merge - attention over the union of disjoint context parts of the
+ * same sequences, from the parts' own results: the exchange step of a
+ * context-sharded decode (each GPU runs mla_decode_absorbed over its own
+ * pages of a sequence; the (o_lat, lse) pairs are gathered and merged here).
+ * With M = max_r lse_r and w_r = exp(lse_r - M):
+ *   o_lat = sum_r w_r o_r / sum_r w_r,   lse = M + ln sum_r w_r
+ * which is exactly the softmax attention of [EN] §2.1 over the union.
+ *   o_parts  fp32 [R][B][H][512]   lse_parts fp32 [R][B][H]  (natural log;
+ *            -inf marks an empty part, weight 0)
+ *   o_lat    fp32 [B][H][512]      lse fp32 [B][H] (may be NULL)
+ *   All parts empty gives o_lat = 0 and lse = -inf.  1 <= R <= 4096,
+ *   B <= 4096, H as for the decode; B == 0 is a no-op.  Arrays 16-byte
+ *   aligned; o_lat must not overlap o_parts.
+ */
+mla_status mla_lse_merge(const float* o_parts, const float* lse_parts, int32_t parts, int32_t batch,
+                         int32_t heads, float* o_lat, float* lse, mla_stream_t stream);
+
 /* Static string for a status code. */
 const char* mla_status_string(mla_status status);
 

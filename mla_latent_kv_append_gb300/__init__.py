@@ -17,8 +17,10 @@ Names follow the C ABI:
     mla_out_unabsorb(o_lat, w_uv, o)
 
 plus ``CacheLayer`` (one layer's pool and formats), ``mla_cache_page_layout``,
-``mla_cache_pool_bytes``, ``mla_decode_workspace_bytes`` and
-``mla_decode_absorbed_noalloc`` (the decode for callers that cannot allocate).
+``mla_cache_pool_bytes``, ``mla_decode_workspace_bytes``,
+``mla_decode_absorbed_noalloc`` (the decode for callers that cannot allocate)
+and ``mla_lse_merge`` (merges per-part results of a context-sharded decode;
+the host side of that exchange is in ``sharded``).
 """
 
 import ctypes
@@ -76,6 +78,7 @@ def _load():
         "mla_decode_absorbed": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, SZ, P, P, P, P]),
         "mla_out_unabsorb": (I32, [P, P, P, I32, I32, P]),
         "mla_decode_absorbed_noalloc": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, P, P, P]),
+        "mla_lse_merge": (I32, [P, P, I32, I32, I32, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -205,6 +208,19 @@ def mla_decode_absorbed_noalloc(cache, q_lat, q_pe, block_table, seq_lens, o_lat
     _check("mla_decode_absorbed_noalloc", lib.mla_decode_absorbed_noalloc(
         ctypes.byref(cs), _ptr(q_lat), _ptr(q_pe), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H,
         scale, int(num_splits), _ptr(o_lat), _ptr(lse), _ptr(dev_err), _stream(stream)))
+
+
+def mla_lse_merge(o_parts, lse_parts, o_lat, lse=None, stream=None):
+    """Merge R per-part results (o_lat, lse) of the same sequences over
+    disjoint context parts into the result over their union."""
+    R, B, H = o_parts.shape[0], o_parts.shape[1], o_parts.shape[2]
+    _need(o_parts, torch.float32, (R, B, H, KV_LORA_RANK), "o_parts")
+    _need(lse_parts, torch.float32, (R, B, H), "lse_parts")
+    _need(o_lat, torch.float32, (B, H, KV_LORA_RANK), "o_lat")
+    if lse is not None:
+        _need(lse, torch.float32, (B, H), "lse")
+    _check("mla_lse_merge", lib.mla_lse_merge(_ptr(o_parts), _ptr(lse_parts), R, B, H, _ptr(o_lat), _ptr(lse),
+                                              _stream(stream)))
 
 
 def abi_version():

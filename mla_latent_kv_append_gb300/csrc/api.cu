@@ -49,7 +49,7 @@ using namespace mla;
 
 extern "C" {
 
-int32_t mla_abi_version(void) { return 100; }
+int32_t mla_abi_version(void) { return 101; }
 
 const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
 
@@ -115,6 +115,21 @@ mla_status mla_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o, 
   if (!o_lat || !w_uv || !o) return MLA_ERR_INVALID_ARG;
   if (!aligned(o_lat, 16) || !aligned(w_uv, 16) || !aligned(o, 16)) return MLA_ERR_INVALID_ARG;
   return launch_out_unabsorb(o_lat, w_uv, o, batch, heads, (cudaStream_t)stream);
+}
+
+mla_status mla_lse_merge(const float* o_parts, const float* lse_parts, int32_t parts, int32_t batch,
+                         int32_t heads, float* o_lat, float* lse, mla_stream_t stream) {
+  if (parts < 1 || parts > kMaxMergeParts || batch < 0 || batch > kMaxBatch || !heads_ok(heads))
+    return MLA_ERR_INVALID_ARG;
+  if (batch == 0) return MLA_OK;
+  if (!o_parts || !lse_parts || !o_lat) return MLA_ERR_INVALID_ARG;
+  if (!aligned(o_parts, 16) || !aligned(lse_parts, 4) || !aligned(o_lat, 16) || (lse && !aligned(lse, 4)))
+    return MLA_ERR_INVALID_ARG;
+  const char* a = (const char*)o_parts;
+  const char* e = a + (size_t)parts * batch * heads * kDc * sizeof(float);
+  const char* o = (const char*)o_lat;
+  if (o < e && a < o + (size_t)batch * heads * kDc * sizeof(float)) return MLA_ERR_INVALID_ARG;
+  return launch_lse_merge(o_parts, lse_parts, parts, batch, heads, o_lat, lse, (cudaStream_t)stream);
 }
 
 size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_splits) {

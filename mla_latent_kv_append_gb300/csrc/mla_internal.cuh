@@ -20,6 +20,7 @@ constexpr int kNLG = kDc / kLG;            // 32 latent groups
 constexpr int kNKG = kDr / kKG;            // 8 k_pe groups
 constexpr int kChunk = 32;                 // decode work unit: 32 tokens
 constexpr int kMaxBatch = 4096;
+constexpr int kMaxMergeParts = 4096;         // mla_lse_merge: most parts per call
 
 // Byte layout of one page; see mla_page_layout in mla.h.  A page is two
 // contiguous blocks of 32 tokens; offsets are within a block.
@@ -173,6 +174,8 @@ mla_status launch_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* 
                            cudaStream_t stream);
 mla_status launch_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o, int B, int H,
                                cudaStream_t stream);
+mla_status launch_lse_merge(const float* o_parts, const float* lse_parts, int R, int B, int H, float* o_lat,
+                            float* lse, cudaStream_t stream);
 struct DecodeParams {
   const uint8_t* pool;
   PageLayout L;

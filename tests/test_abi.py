@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
-    assert lib.abi_version() == 100
+    assert lib.abi_version() == 101
 
 
 def test_layouts_match_the_accounting(lib):
@@ -91,4 +91,10 @@ def test_invalid_arguments_rejected_on_host(lib):
     big = (ctypes.byref(cs), fake, fake, fake, 1 << 18, fake, 4096, 16, 0.07, 3, ctypes.c_void_p(0x200000), 1 << 40,
            fake, None, None, None)
     assert raw.mla_decode_absorbed(*big) == 1
+    # merge: part count out of range, output overlapping the parts
+    a16 = ctypes.c_void_p(0x10000)
+    assert raw.mla_lse_merge(a16, a16, 0, 2, 16, ctypes.c_void_p(0x900000), None, None) == 1
+    assert raw.mla_lse_merge(a16, a16, 5000, 2, 16, ctypes.c_void_p(0x900000), None, None) == 1
+    assert raw.mla_lse_merge(a16, a16, 2, 2, 16, ctypes.c_void_p(0x10000 + 4096), None, None) == 1
+    assert raw.mla_lse_merge(a16, a16, 2, 0, 16, a16, None, None) == 0
     assert raw.mla_status_string(4) == b"device-side bounds error"
