@@ -24,7 +24,7 @@ Parity status: pinned (every printed figure is reproduced as an exact integer
 or to the printed rounding, in tests/test_oracle_accounting.py).
 """
 
-FMT_BF16, FMT_INT8, FMT_INT4 = 0, 1, 2
+FMT_BF16, FMT_INT8, FMT_INT4, FMT_INT4_SYM = 0, 1, 2, 3
 
 KV_LORA_RANK = 512
 ROPE_DIM = 64
@@ -54,7 +54,7 @@ def _elem_bytes(fmt, n):
         return 2 * n
     if fmt == FMT_INT8:
         return n
-    if fmt == FMT_INT4:
+    if fmt in (FMT_INT4, FMT_INT4_SYM):
         return n // 2
     raise ValueError(fmt)
 
@@ -64,9 +64,9 @@ def layer_bytes(latent_fmt, kpe_fmt, metadata=False):
 
     metadata=False gives the pages' code-only figure; metadata=True adds one
     fp32 scale per group (and one fp32 zero-point per latent group for
-    asymmetric INT4), which is what the cache here actually stores.
-    kpe_fmt may be FMT_INT4 only for the code-only figure (the Chinese
-    report's 7.6 KB scheme), which the cache does not implement.
+    asymmetric INT4), which is what the cache here actually stores.  4-bit
+    k_pe is symmetric (FMT_INT4_SYM; FMT_INT4 gives the same code-only
+    figure), as in the Chinese report's "k_pe 对称 INT4 (8块)" row.
     """
     b = _elem_bytes(latent_fmt, KV_LORA_RANK) + _elem_bytes(kpe_fmt, ROPE_DIM)
     if metadata:
@@ -76,7 +76,9 @@ def layer_bytes(latent_fmt, kpe_fmt, metadata=False):
             b += 4 * lg
         elif latent_fmt == FMT_INT4:
             b += 8 * lg
-        if kpe_fmt in (FMT_INT8, FMT_INT4):
+        elif latent_fmt == FMT_INT4_SYM:
+            b += 4 * lg
+        if kpe_fmt in (FMT_INT8, FMT_INT4, FMT_INT4_SYM):
             b += 4 * kg
     return b
 

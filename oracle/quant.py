@@ -25,6 +25,11 @@ Readings taken where the pages are open (each is listed in the design doc):
   q = clamp(rint(x / s) + z, 0, 15).  x_hat = (q - z) * s.  When s comes out
   0: if min == 0 then s = z = q = 0; otherwise s = |min|, z = rint(-min / s)
   (= -1 or +1) and q = 0, which reconstructs the constant group exactly.
+* Symmetric INT4 (the report's "对称 INT4 (32块)" latent row and "k_pe 对称
+  INT4 (8块)" row): s = absmax / 7, q = clamp(rint(x / s), -7, 7), the
+  INT8 rule with 7 levels a side; x_hat = q * s.  Used as a cache format
+  for the latent and for k_pe (the report's 7.6 KB scheme pairs asymmetric
+  INT4 latent codes with 4-bit k_pe).
 * All arithmetic is IEEE fp32 with round-half-even (NumPy float32 ops and
   ``np.rint``); no fused multiply-add.
 
@@ -132,7 +137,11 @@ def quantize_per_token_int8(x):
 
 def quantize_sym_int4(x, group=16):
     """Symmetric INT4, s = absmax / 7, codes in [-7, 7]: Chinese report §3.2
-    "对称 INT4 (32块)" (the row the asymmetric scheme is said to beat)."""
+    rows "对称 INT4 (32块)" (group 16 on the latent; the row the asymmetric
+    scheme is said to beat) and "k_pe 对称 INT4 (8块)" (group 8 on k_pe).
+
+    Returns (codes int8 in [-7, 7] [rows, channels], scale float32 [rows, groups]).
+    """
     g = _groups(x, group)
     a = np.max(np.abs(g), axis=2)
     s = (a / F32(7)).astype(np.float32)
@@ -141,6 +150,11 @@ def quantize_sym_int4(x, group=16):
     q = np.clip(np.rint(g / safe[..., None]), -7, 7)
     q = np.where(live[..., None], q, F32(0))
     return q.astype(np.int8).reshape(x.shape), s
+
+
+def dequantize_sym_int4(codes, scale, group):
+    """x_hat = float(code) * scale in fp32 (same as the INT8 rule)."""
+    return dequantize_sym_int8(codes, scale, group)
 
 
 def relative_error(x, x_hat):
@@ -159,7 +173,7 @@ def relative_error(x, x_hat):
 # Whole-token helpers used by tests: latent (512) + k_pe (64) in one call.
 # ---------------------------------------------------------------------------
 
-FMT_BF16, FMT_INT8, FMT_INT4 = 0, 1, 2
+FMT_BF16, FMT_INT8, FMT_INT4, FMT_INT4_SYM = 0, 1, 2, 3
 LATENT_GROUP, KPE_GROUP = 16, 8
 
 
@@ -179,6 +193,9 @@ def quantize_token_rows(c, kpe, latent_fmt, kpe_fmt):
         q, s, z = quantize_asym_int4(c, LATENT_GROUP)
         out.update(c_codes=q, c_scale=s, c_zero=z,
                    c_hat=dequantize_asym_int4(q, s, z, LATENT_GROUP))
+    elif latent_fmt == FMT_INT4_SYM:
+        q, s = quantize_sym_int4(c, LATENT_GROUP)
+        out.update(c_codes=q, c_scale=s, c_hat=dequantize_sym_int4(q, s, LATENT_GROUP))
     else:
         raise ValueError("latent_fmt")
     if kpe_fmt == FMT_BF16:
@@ -186,6 +203,9 @@ def quantize_token_rows(c, kpe, latent_fmt, kpe_fmt):
     elif kpe_fmt == FMT_INT8:
         q, s = quantize_sym_int8(kpe, KPE_GROUP)
         out.update(kpe_codes=q, kpe_scale=s, kpe_hat=dequantize_sym_int8(q, s, KPE_GROUP))
+    elif kpe_fmt == FMT_INT4_SYM:
+        q, s = quantize_sym_int4(kpe, KPE_GROUP)
+        out.update(kpe_codes=q, kpe_scale=s, kpe_hat=dequantize_sym_int4(q, s, KPE_GROUP))
     else:
         raise ValueError("kpe_fmt")
     return out

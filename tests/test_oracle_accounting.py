@@ -68,6 +68,16 @@ def test_metadata_overhead_reported_on_top():
     assert acc.token_bytes(608) == 16416 and r1(acc.kib(16416)) == 16.0
 
 
+def test_symmetric_int4_formats_metadata():
+    # the 7.6 KB scheme as stored: asymmetric INT4 latent (scale + zero) and
+    # symmetric INT4 k_pe (scale only): 288 B of codes + 288 B of metadata
+    I4S = acc.FMT_INT4_SYM
+    assert acc.layer_bytes(I4, I4S) == 288
+    assert acc.layer_bytes(I4, I4S, metadata=True) == 256 + 32 + 8 * 32 + 4 * 8 == 576
+    assert acc.layer_bytes(I4S, I8, metadata=True) == 256 + 64 + 4 * 32 + 4 * 8 == 480
+    assert acc.layer_bytes(I4S, I4S, metadata=True) == 256 + 32 + 4 * 32 + 4 * 8 == 448
+
+
 def test_capacity_in_10gb():
     # CN §4.1: INT8 69万 tokens, INT4 138万 tokens; EN §4.3: 39K / 690K / 620K / 1.24M.
     cap = lambda per_layer: acc.capacity_tokens(acc.token_bytes(per_layer))

@@ -36,6 +36,14 @@ def _int4_zero_sign(x, group=16):
     return q, s, (-z).astype(np.float32)
 
 
+def _sym_int4_over_8(x, group=16):
+    g = Q._groups(x, group)
+    s = (np.max(np.abs(g), axis=2) / F32(8)).astype(np.float32)
+    safe = np.where(s > 0, s, F32(1)).astype(np.float32)
+    q = np.clip(np.rint(g / safe[..., None]), -7, 7)
+    return q.astype(np.int8).reshape(x.shape[0], -1), s
+
+
 def _decode_no_rope(q_lat, q_pe, c_hat, kpe_hat, softmax_scale=A.DEFAULT_SOFTMAX_SCALE):
     return A.__dict__["_orig_decode"](q_lat, np.zeros_like(np.asarray(q_pe, np.float64)), c_hat, kpe_hat,
                                       softmax_scale)
@@ -62,6 +70,8 @@ CASES = [
      TQ.test_int8_scale_is_absmax_over_127),
     ("int4 zero-point sign flipped", Q, "quantize_asym_int4", _int4_zero_sign,
      TQ.test_int4_scale_zero_and_endpoints),
+    ("sym int4 scale absmax/8", Q, "quantize_sym_int4", _sym_int4_over_8,
+     TQ.test_sym_int4_scale_absmax_over_7_ties_and_zero_group),
     ("decode drops the q_pe.k_pe term", A, "absorbed_decode", _decode_no_rope,
      lambda: TA.test_absorbed_equals_expanded(Q.FMT_INT8, Q.FMT_INT8)),
     ("absorb uses the wrong head's W_UK", A, "absorb_q", _absorb_wrong_head,

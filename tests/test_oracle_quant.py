@@ -167,6 +167,54 @@ def test_int4_round_trip_bound():
     assert np.all(err <= 0.5 * sg + 8 * ulp32(ag))
 
 
+# ----------------------------------------------------------- symmetric INT4 --
+
+@pytest.mark.parametrize("group", [16, 8])
+def test_sym_int4_codes_are_nearest_levels_brute_force(group):
+    x = np.concatenate([synth_latent(64)[:, :128], RNG.standard_normal((64, 128)).astype(np.float32) * 3])
+    q, s = Q.quantize_sym_int4(x, group)
+    assert q.dtype == np.int8 and q.min() >= -7 and q.max() <= 7
+    sg = np.repeat(s, group, axis=1)
+    ratio = (x / sg).astype(np.float64)
+    levels = np.arange(-7, 8, dtype=np.float64)
+    d = np.abs(ratio[..., None] - levels)
+    best = d.min(axis=-1)
+    assert np.all(np.abs(ratio - q.astype(np.float64)) == best)
+    tie = np.sum(d == best[..., None], axis=-1) > 1
+    assert np.all(q[tie] % 2 == 0)
+
+
+def test_sym_int4_scale_absmax_over_7_ties_and_zero_group():
+    x = synth_kpe(32)
+    q, s = Q.quantize_sym_int4(x, 8)
+    a = np.abs(x).reshape(32, 8, 8).max(axis=2).astype(np.float64)
+    assert np.all(np.abs(s.astype(np.float64) * 7 - a) <= 2 * ulp32(a))
+    assert np.all(np.abs(q.reshape(32, 8, 8).astype(np.int32)).max(axis=2) == 7)
+    # absmax 7 -> s = 1: 2.5 -> 2, 3.5 -> 4, -0.5 -> 0, 6.5 -> 6 (half even); a zero group stays zero
+    row = np.array([[7, 2.5, 3.5, -0.5, 6.5, -6.5, 1.5, 0, 0, 0, 0, 0, 0, 0, 0, 0]], np.float32)
+    q, s = Q.quantize_sym_int4(row, 8)
+    assert s[0].tolist() == [1.0, 0.0]
+    assert q[0].tolist() == [7, 2, 4, 0, 6, -6, 2, 0] + [0] * 8
+
+
+def test_sym_int4_round_trip_bound():
+    x = np.concatenate([synth_latent(128), synth_kpe(128)[:, :64].repeat(8, axis=1)])
+    for group in (16, 8):
+        q, s = Q.quantize_sym_int4(x, group)
+        x_hat = Q.dequantize_sym_int4(q, s, group)
+        sg = np.repeat(s, group, axis=1).astype(np.float64)
+        ag = np.repeat(np.abs(x).reshape(x.shape[0], -1, group).max(axis=2), group, axis=1)
+        assert np.all(np.abs(x.astype(np.float64) - x_hat) <= 0.5 * sg + 4 * ulp32(ag))
+
+
+def test_token_rows_sym_int4_fields():
+    c, k = synth_latent(16), synth_kpe(16)
+    d = Q.quantize_token_rows(c, k, Q.FMT_INT4_SYM, Q.FMT_INT4_SYM)
+    assert d["c_codes"].shape == (16, 512) and d["c_scale"].shape == (16, 32) and "c_zero" not in d
+    assert d["kpe_codes"].shape == (16, 64) and d["kpe_scale"].shape == (16, 8)
+    assert np.array_equal(d["c_hat"], Q.dequantize_sym_int4(*Q.quantize_sym_int4(c, 16), 16))
+
+
 # ------------------------------------------------- the pages' error ordering --
 
 def test_error_ordering_per_group_per_token_per_tensor():
