@@ -38,6 +38,12 @@ CONFIGS = {
                              "INT8 latent (32 groups) + INT8 k_pe, 64-token pages"),
     "v2lite_int4_32k": dict(layers=27, heads=16, batch=32, ctx=32768, latent="int4", kpe="int8",
                             desc="V2-Lite shapes, batch 32, context 32768, asymmetric INT4 latent + INT8 k_pe"),
+    "v2lite_int4_kpe4_32k": dict(layers=27, heads=16, batch=32, ctx=32768, latent="int4", kpe="int4sym",
+                                 desc="V2-Lite shapes, batch 32, context 32768, asymmetric INT4 latent + "
+                                      "symmetric INT4 k_pe (the 7.6 KB-per-token scheme; 576 B per token-layer "
+                                      "with scales and zero-points)"),
+    "v2lite_int4sym_32k": dict(layers=27, heads=16, batch=32, ctx=32768, latent="int4sym", kpe="int8",
+                               desc="V2-Lite shapes, batch 32, context 32768, symmetric INT4 latent + INT8 k_pe"),
     "long_int4_1m": dict(layers=27, heads=16, batch=1, ctx=1048576, latent="int4", kpe="int8",
                          desc="V2-Lite shapes, batch 1, context 1,048,576, asymmetric INT4 latent + INT8 k_pe"),
     "long_bf16_256k": dict(layers=27, heads=16, batch=1, ctx=262144, latent="bf16", kpe="bf16",
@@ -54,9 +60,18 @@ CONFIGS = {
     "tiny": dict(layers=1, heads=16, batch=1, ctx=256, latent="int8", kpe="int8",
                  desc="1 layer, 16 heads, batch 1, context 256"),
 }
-FMT = {"bf16": 0, "int8": 1, "int4": 2}
-BETA = {("bf16", "bf16"): 1152, ("int8", "int8"): 736, ("int4", "int8"): 608, ("int8", "bf16"): 800,
-        ("int4", "bf16"): 672, ("bf16", "int8"): 1088}
+FMT = {"bf16": 0, "int8": 1, "int4": 2, "int4sym": 3}
+def _beta(latent, kpe):
+    """Stored bytes per token and layer (codes + fp32 scales / zero-points),
+    as laid out in include/mla.h: 32 latent groups of 16, 8 k_pe groups of 8."""
+    code = {"bf16": 1024, "int8": 512, "int4": 256, "int4sym": 256}[latent]
+    meta = {"bf16": 0, "int8": 128, "int4": 256, "int4sym": 128}[latent]
+    kcode = {"bf16": 128, "int8": 64, "int4sym": 32}[kpe]
+    kmeta = 0 if kpe == "bf16" else 32
+    return code + meta + kcode + kmeta
+
+
+BETA = {(a, b): _beta(a, b) for a in ("bf16", "int8", "int4", "int4sym") for b in ("bf16", "int8", "int4sym")}
 METRIC = "decode tokens/s & achieved HBM GB/s (% of GB300 peak) for absorbed MLA decode"
 SEED = 0x4D4C41
 FALLBACK_HBM_GBS = 6800.0
@@ -202,12 +217,16 @@ def _dequant_latent(Q, stored, lf):
         return Q.dequantize_sym_int8(stored["c_codes"], stored["c_scale"], 16)
     if lf == 2:
         return Q.dequantize_asym_int4(stored["c_codes"], stored["c_scale"], stored["c_zero"], 16)
+    if lf == 3:
+        return Q.dequantize_sym_int4(stored["c_codes"], stored["c_scale"], 16)
     return stored["c_hat"]                      # bf16 cache: the values themselves
 
 
 def _dequant_kpe(Q, stored, kf):
     if kf == 1:
         return Q.dequantize_sym_int8(stored["kpe_codes"], stored["kpe_scale"], 8)
+    if kf == 3:
+        return Q.dequantize_sym_int4(stored["kpe_codes"], stored["kpe_scale"], 8)
     return stored["kpe_hat"]
 
 
@@ -430,7 +449,8 @@ def run_ours(args, cfg, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int8 codes / fp32 math" if cfg["latent"] != "bf16" else "bf16 / fp32 math",
+        "dtype": "f16 MMA on exact integer codes, f32 accumulate" if cfg["latent"] != "bf16"
+                 else "bf16 MMA, f32 accumulate",
         "data": "synthetic (seeded; DeepSeek-V2-Lite shapes, random-init weights)",
         "config": {"workload": args.config, "description": cfg["desc"], "layers": layers, "heads": cfg["heads"],
                    "batch_per_gpu": wl.B, "context": (seq_lens[0] if len(set(seq_lens)) == 1 else

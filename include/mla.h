@@ -71,7 +71,8 @@ typedef enum {
 typedef enum {
   MLA_FMT_BF16 = 0,        /* values stored as bf16, no scale */
   MLA_FMT_INT8_SYM = 1,    /* int8 code, fp32 scale per (token, group) */
-  MLA_FMT_INT4_ASYM = 2    /* 4-bit code, fp32 scale and zero per (token, group) */
+  MLA_FMT_INT4_ASYM = 2,   /* 4-bit code, fp32 scale and zero per (token, group) */
+  MLA_FMT_INT4_SYM = 3     /* 4-bit code in [-7, 7], fp32 scale per (token, group) */
 } mla_fmt;
 
 /* Bits ORed into *dev_err. */
@@ -92,7 +93,8 @@ typedef enum {
  * One layer's paged latent cache.  The pool holds num_pages pages of 64
  * tokens; a token's physical slot is page * 64 + offset.  Which pages belong
  * to which sequence is the caller's business (block tables below).
- *   latent_fmt: any mla_fmt.  kpe_fmt: MLA_FMT_BF16 or MLA_FMT_INT8_SYM.
+ *   latent_fmt: any mla_fmt.  kpe_fmt: MLA_FMT_BF16, MLA_FMT_INT8_SYM or
+ *   MLA_FMT_INT4_SYM.
  *   pool: device memory of mla_cache_pool_bytes() bytes, 256-byte aligned,
  *         owned by the caller.
  */
@@ -116,20 +118,27 @@ typedef struct {
  *              16-byte chunks; logical chunk c of block token u is stored at
  *              chunk position (c & ~7) | ((c ^ u) & 7).  An int8 chunk is one
  *              16-channel group in channel order; a bf16 chunk is 8 channels.
- *              An int4 chunk c holds groups A = 2c and B = 2c + 1; its 32-bit
+ *              A 4-bit chunk c holds groups A = 2c and B = 2c + 1; its 32-bit
  *              word j (j = 0..3) packs, from the least significant nibble,
  *              A[4j], A[4j+2], B[4j], B[4j+2], A[4j+1], A[4j+3], B[4j+1],
- *              B[4j+3] (X[i] = code of channel i of group X).
- *   scale      fp32 [32 groups][32 block tokens]   (int8 / int4 latent)
- *   zero       fp32 [32 groups][32 block tokens]   (int4 latent; integer-valued)
+ *              B[4j+3] (X[i] = nibble of channel i of group X).  A nibble is
+ *              the code (INT4_ASYM, 0..15) or the code + 8 (INT4_SYM, 1..15).
+ *   scale      fp32 [32 groups][32 block tokens]   (int8 / 4-bit latent)
+ *   zero       fp32 [32 groups][32 block tokens]   (INT4_ASYM latent; integer-valued)
  *   kpe        [32][kpe_row_bytes]: bf16 (128 B = 8 chunks of 8 channels,
- *              chunk c of token u at position c ^ (u & 7)) or int8 (64 B =
+ *              chunk c of token u at position c ^ (u & 7)), int8 (64 B =
  *              4 chunks of two 8-channel groups, chunk c at c ^ ((u >> 1) & 3))
- *   kpe_scale  fp32 [8 groups][32 block tokens]    (int8 k_pe)
- * page_bytes = 2 * block_bytes = 64 x (1152, 736 or 608) bytes for
- * bf16/bf16, int8/int8 and int4/int8.  The swizzles spread the rows of eight
- * consecutive tokens over all shared-memory banks when a block is copied
- * verbatim into shared memory.
+ *              or INT4_SYM (32 B = 2 chunks of 32 channels, chunk c at
+ *              c ^ ((u >> 2) & 1); chunk c packs its halves A = channels
+ *              32c .. 32c+15 and B = 32c+16 .. 32c+31 like a 4-bit latent
+ *              chunk, nibble = code + 8)
+ *   kpe_scale  fp32 [8 groups][32 block tokens]    (int8 / INT4_SYM k_pe)
+ * page_bytes = 2 * block_bytes = 64 x (1152, 736, 608 or 576) bytes for
+ * bf16/bf16, int8/int8, int4/int8 and int4/int4-sym (the last is [CN]
+ * §4.1's 7.6 KB-per-token scheme: 288 B of codes per layer plus scales and
+ * zero-points).  The swizzles spread the rows of eight consecutive tokens
+ * over all shared-memory banks when a block is copied verbatim into shared
+ * memory.
  */
 typedef struct {
   int64_t page_bytes, block_bytes;
@@ -155,6 +164,9 @@ size_t mla_cache_pool_bytes(const mla_cache_layer* cache);
  *   INT4_ASYM (groups of 16): s = (max - min) / 15;  z = rint(-min / s);
  *       q = clamp(rint(x / s) + z, 0, 15); if s == 0: s = |min|, z = rint(-min/s)
  *       (or s = z = 0 when min == 0) and q = 0.
+ *   INT4_SYM  (groups of 16 latent channels, or 8 k_pe channels; [CN] §3.2
+ *       "对称 INT4" rows): s = max|x| / 7;  q = clamp(rint(x / s), -7, 7);
+ *       s = 0 -> q = 0.
  *   BF16: the input bits are copied.
  *   c_new   bf16 [n][512]     kpe_new bf16 [n][64]
  *   slot    int32 [n]: physical slot (page * 64 + offset) of each token;
@@ -189,7 +201,7 @@ size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_spli
  * against its cached latents ([EN] §2.1 get(): attention computed from the
  * latent; flash-decode split over context chunks with a log-sum-exp
  * combine).  Dequantization is fused into the tile loads: x_hat = q * s for
- * INT8, (q - z) * s for INT4.
+ * INT8 and INT4_SYM, (q - z) * s for INT4_ASYM.
  *   q_lat       fp32 [B][H][512]   (from mla_q_absorb)
  *   q_pe        bf16 [B][H][64]
  *   block_table int32 [B][max_pages]: page id of each sequence's logical page

@@ -32,7 +32,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmla_gb300.so")
 
-FMT_BF16, FMT_INT8_SYM, FMT_INT4_ASYM = 0, 1, 2
+FMT_BF16, FMT_INT8_SYM, FMT_INT4_ASYM, FMT_INT4_SYM = 0, 1, 2, 3
 DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 KV_LORA_RANK, ROPE_DIM, QK_NOPE_DIM, V_DIM, PAGE_TOKENS = 512, 64, 128, 128, 64
 DEFAULT_SOFTMAX_SCALE = 1.0 / math.sqrt(QK_NOPE_DIM + ROPE_DIM)

@@ -58,21 +58,33 @@ __device__ __forceinline__ void div_rn_shared(const float* x, float s, float* ou
   }
 }
 
-// Symmetric INT8 of n values; returns the scale, writes int8 codes.
-template <int N>
-__device__ __forceinline__ float quant_sym8(const float* x, int8_t* q) {
+// Symmetric quantization of N values with levels -QMAX .. QMAX (127 for
+// INT8, 7 for INT4_SYM); returns the scale, writes the codes.
+template <int N, int QMAX>
+__device__ __forceinline__ float quant_sym(const float* x, int8_t* q) {
   float a = 0.f;
 #pragma unroll
   for (int i = 0; i < N; ++i) a = fmaxf(a, fabsf(x[i]));
-  const float s = __fdiv_rn(a, 127.f);
+  const float s = __fdiv_rn(a, (float)QMAX);
   float d[N];
   if (s > 0.f) div_rn_shared<N>(x, s, d);
 #pragma unroll
   for (int i = 0; i < N; ++i) {
-    const float r = s > 0.f ? fminf(fmaxf(rintf(d[i]), -127.f), 127.f) : 0.f;
+    const float r = s > 0.f ? fminf(fmaxf(rintf(d[i]), (float)-QMAX), (float)QMAX) : 0.f;
     q[i] = (int8_t)(int)r;
   }
   return s;
+}
+
+// Nibbles of one 16-channel half (or group) of a 4-bit chunk, placed in the
+// chunk's four words: channels 4j, 4j+2, 4j+1, 4j+3 at nibbles 0, 1, 4, 5 of
+// word j for the first half and 2, 3, 6, 7 for the second (half = 1), see
+// int4_nibble_channel.  q[i] is the nibble value of channel i of the half.
+__device__ __forceinline__ void int4_half_words(const uint8_t* q, int half, uint32_t* w) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    w[j] = ((uint32_t)q[4 * j] | ((uint32_t)q[4 * j + 2] << 4) | ((uint32_t)q[4 * j + 1] << 16) |
+            ((uint32_t)q[4 * j + 3] << 20)) << (8 * half);
 }
 
 // Asymmetric INT4 of 16 values; returns scale, zero (fp32) and codes 0..15.
@@ -134,7 +146,7 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
       float* scale = reinterpret_cast<float*>(blk + L.scale_off);
       if (LF == MLA_FMT_INT8_SYM) {
         int8_t q[16];
-        scale[lane * kBlockTokens + t] = quant_sym8<16>(x, q);
+        scale[lane * kBlockTokens + t] = quant_sym<16, 127>(x, q);
         uint32_t w[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -143,33 +155,73 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
         reinterpret_cast<uint4*>(row)[latent_chunk_pos(lane, t)] = make_uint4(w[0], w[1], w[2], w[3]);
       } else {
         uint8_t q[16];
-        float sc, zp;
-        quant_asym4(x, sc, zp, q);
-        scale[lane * kBlockTokens + t] = sc;
-        reinterpret_cast<float*>(blk + L.zero_off)[lane * kBlockTokens + t] = zp;
-        // this lane's nibbles of the shared chunk (groups 2c and 2c+1): the
-        // group's channels 4j, 4j+2, 4j+1, 4j+3 sit at nibbles 0, 1, 4, 5 of
-        // word j for the chunk's first group and 2, 3, 6, 7 for the second
-        // (int4_nibble_channel); then merge with the partner lane's
-        uint32_t w[4];
-        const int sh = 8 * (lane & 1);
+        if (LF == MLA_FMT_INT4_ASYM) {
+          float sc, zp;
+          quant_asym4(x, sc, zp, q);
+          scale[lane * kBlockTokens + t] = sc;
+          reinterpret_cast<float*>(blk + L.zero_off)[lane * kBlockTokens + t] = zp;
+        } else {
+          int8_t qs[16];
+          scale[lane * kBlockTokens + t] = quant_sym<16, 7>(x, qs);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t v = ((uint32_t)q[4 * j] | ((uint32_t)q[4 * j + 2] << 4) | ((uint32_t)q[4 * j + 1] << 16) |
-                              ((uint32_t)q[4 * j + 3] << 20)) << sh;
-          w[j] = v | __shfl_xor_sync(0xffffffffu, v, 1);
+          for (int i = 0; i < 16; ++i) q[i] = (uint8_t)(qs[i] + 8);
         }
+        // this lane's nibbles of the shared chunk (groups 2c and 2c+1), then
+        // merge with the partner lane's
+        uint32_t w[4];
+        int4_half_words(q, lane & 1, w);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) w[j] |= __shfl_xor_sync(0xffffffffu, w[j], 1);
         if ((lane & 1) == 0)
           reinterpret_cast<uint4*>(row)[latent_chunk_pos(lane >> 1, t)] = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
 
-    // ---- k_pe: lanes 0..7, group = lane (channels 8g .. 8g+7)
-    if (lane < kNKG) {
+    // ---- k_pe: lanes 0..7, group = lane (channels 8g .. 8g+7).  For 4-bit
+    // k_pe the eight lanes all take part in the shuffles (lanes 8.. idle).
+    if (KF == MLA_FMT_INT4_SYM) {
+      uint4 k = make_uint4(0u, 0u, 0u, 0u);
+      if (lane < kNKG) k = reinterpret_cast<const uint4*>(kpe_new + (size_t)i * kDr)[lane];
+      float x[8];
+      const uint32_t kw[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        x[2 * j] = bf16lo(kw[j]);
+        x[2 * j + 1] = bf16hi(kw[j]);
+      }
+      int8_t qs[8];
+      const float sc = quant_sym<8, 7>(x, qs);
+      // lane g: chunk g / 4, half (g / 2) % 2, channels 8 (g % 2) .. +7 of
+      // the half; the half's channel i = 8 (g % 2) + i
+      uint8_t q[16];
+#pragma unroll
+      for (int i2 = 0; i2 < 16; ++i2) q[i2] = 0;
+      if (lane & 1) {
+#pragma unroll
+        for (int i2 = 0; i2 < 8; ++i2) q[8 + i2] = (uint8_t)(qs[i2] + 8);
+      } else {
+#pragma unroll
+        for (int i2 = 0; i2 < 8; ++i2) q[i2] = (uint8_t)(qs[i2] + 8);
+      }
+      uint32_t w[4];
+      int4_half_words(q, (lane >> 1) & 1, w);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        w[j] |= __shfl_xor_sync(0xffffffffu, w[j], 1);
+        w[j] |= __shfl_xor_sync(0xffffffffu, w[j], 2);
+      }
+      if (lane < kNKG) {
+        reinterpret_cast<float*>(blk + L.kpe_scale_off)[lane * kBlockTokens + t] = sc;
+        if ((lane & 3) == 0) {
+          uint8_t* krow = blk + L.kpe_off + (int64_t)t * L.kpe_row;
+          reinterpret_cast<uint4*>(krow)[kpe_chunk_pos(lane >> 2, t, KF)] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    } else if (lane < kNKG) {
       const uint4 k = reinterpret_cast<const uint4*>(kpe_new + (size_t)i * kDr)[lane];
       uint8_t* krow = blk + L.kpe_off + (int64_t)t * L.kpe_row;
       if (KF == MLA_FMT_BF16) {
-        reinterpret_cast<uint4*>(krow)[kpe_chunk_pos(lane, t, true)] = k;
+        reinterpret_cast<uint4*>(krow)[kpe_chunk_pos(lane, t, KF)] = k;
       } else {
         float x[8];
         const uint32_t w[4] = {k.x, k.y, k.z, k.w};
@@ -179,12 +231,12 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
           x[2 * j + 1] = bf16hi(w[j]);
         }
         int8_t q[8];
-        reinterpret_cast<float*>(blk + L.kpe_scale_off)[lane * kBlockTokens + t] = quant_sym8<8>(x, q);
+        reinterpret_cast<float*>(blk + L.kpe_scale_off)[lane * kBlockTokens + t] = quant_sym<8, 127>(x, q);
         const uint32_t lo = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) |
                             ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
         const uint32_t hi = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) |
                             ((uint32_t)(uint8_t)q[6] << 16) | ((uint32_t)(uint8_t)q[7] << 24);
-        *reinterpret_cast<uint2*>(krow + kpe_chunk_pos(lane >> 1, t, false) * 16 + (lane & 1) * 8) =
+        *reinterpret_cast<uint2*>(krow + kpe_chunk_pos(lane >> 1, t, KF) * 16 + (lane & 1) * 8) =
             make_uint2(lo, hi);
       }
     }
@@ -219,6 +271,12 @@ mla_status launch_append(const mla_cache_layer* cache, const PageLayout& L, cons
   MLA_APPEND_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT8_SYM)
   MLA_APPEND_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_BF16)
   MLA_APPEND_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT8_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT4_SYM, MLA_FMT_BF16)
+  MLA_APPEND_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT8_SYM)
+  MLA_APPEND_CASE(MLA_FMT_BF16, MLA_FMT_INT4_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT4_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT4_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT4_SYM)
 #undef MLA_APPEND_CASE
   return MLA_ERR_UNSUPPORTED;
 }

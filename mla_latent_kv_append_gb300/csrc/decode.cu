@@ -190,8 +190,8 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const int g = 2 * c + (int4_nibble_channel(j, k) >> 4);
-              v[k] = __fmul_rn(__fsub_rn((float)((w >> (4 * k)) & 15u), zp[g * kBlockTokens + t]),
-                               sc[g * kBlockTokens + t]);
+              const float zero = LF == MLA_FMT_INT4_SYM ? 8.f : zp[g * kBlockTokens + t];
+              v[k] = __fmul_rn(__fsub_rn((float)((w >> (4 * k)) & 15u), zero), sc[g * kBlockTokens + t]);
             }
           }
 #pragma unroll
@@ -205,12 +205,30 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
           if (s_valid[t]) {
             const uint32_t w = reinterpret_cast<const uint32_t*>(
                 pool + s_page[t] * pb + blk_off + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[
-                kpe_chunk_pos(pr >> 2, t, true) * 4 + (pr & 3)];
+                kpe_chunk_pos(pr >> 2, t, KF) * 4 + (pr & 3)];
             a = bf16lo(w);
             bb = bf16hi(w);
           }
           s_k[t * kKS + 2 * pr] = a;
           s_k[t * kKS + 2 * pr + 1] = bb;
+        }
+      } else if (KF == MLA_FMT_INT4_SYM) {
+        for (int i = tid; i < kChunk * (kDr / 8); i += kThreads) {
+          const int t = i / (kDr / 8), pw = i % (kDr / 8);
+          const int c = kpe_chunk_pos(pw >> 2, t, KF), j = pw & 3;   // logical chunk of this stored word
+          float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          if (s_valid[t]) {
+            const uint8_t* blk = pool + s_page[t] * pb + blk_off;
+            const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[pw];
+            const float* sc = reinterpret_cast<const float*>(blk + p.L.kpe_scale_off);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int ch = 32 * c + int4_nibble_channel(j, k);
+              v[k] = __fmul_rn(__fsub_rn((float)((w >> (4 * k)) & 15u), 8.f), sc[(ch >> 3) * kBlockTokens + t]);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) s_k[t * kKS + 32 * c + int4_nibble_channel(j, k)] = v[k];
         }
       } else {
         for (int i = tid; i < kChunk * (kDr / 4); i += kThreads) {
@@ -219,7 +237,7 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
           if (s_valid[t]) {
             const uint8_t* blk = pool + s_page[t] * pb + blk_off;
             const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[
-                kpe_chunk_pos(wi >> 2, t, false) * 4 + (wi & 3)];
+                kpe_chunk_pos(wi >> 2, t, KF) * 4 + (wi & 3)];
             const float s = reinterpret_cast<const float*>(blk + p.L.kpe_scale_off)[(wi >> 1) * kBlockTokens + t];
 #pragma unroll
             for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), s);
@@ -421,6 +439,12 @@ mla_status launch_decode_ref(const DecodeParams& p, cudaStream_t stream) {
   MLA_DECODE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT8_SYM)
   MLA_DECODE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_BF16)
   MLA_DECODE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT8_SYM)
+  MLA_DECODE_CASE(MLA_FMT_INT4_SYM, MLA_FMT_BF16)
+  MLA_DECODE_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT8_SYM)
+  MLA_DECODE_CASE(MLA_FMT_BF16, MLA_FMT_INT4_SYM)
+  MLA_DECODE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT4_SYM)
+  MLA_DECODE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT4_SYM)
+  MLA_DECODE_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT4_SYM)
 #undef MLA_DECODE_CASE
   return MLA_ERR_UNSUPPORTED;
 }

@@ -53,13 +53,15 @@ constexpr int kXStride = 20;                   // row stride (float2) of a warp'
 template <int LF, int KF>
 struct Fmt {
   static constexpr bool kLatBf16 = LF == MLA_FMT_BF16;
-  static constexpr bool kLatInt4 = LF == MLA_FMT_INT4_ASYM;
+  static constexpr bool kLatInt4 = LF == MLA_FMT_INT4_ASYM || LF == MLA_FMT_INT4_SYM;
+  static constexpr bool kLatSym4 = LF == MLA_FMT_INT4_SYM;       // zero-point fixed at 8 (nibble = code + 8)
   static constexpr bool kKpeBf16 = KF == MLA_FMT_BF16;
+  static constexpr bool kKpeInt4 = KF == MLA_FMT_INT4_SYM;
   static constexpr int kRow = kLatBf16 ? 1024 : (LF == MLA_FMT_INT8_SYM ? 512 : 256);
-  static constexpr int kKRow = kKpeBf16 ? 128 : 64;
+  static constexpr int kKRow = kKpeBf16 ? 128 : (kKpeInt4 ? 32 : 64);
   static constexpr int kScaleOff = kBlockTokens * kRow;
   static constexpr int kZeroOff = kScaleOff + (kLatBf16 ? 0 : kNLG * kBlockTokens * 4);
-  static constexpr int kKpeOff = kZeroOff + (kLatInt4 ? kNLG * kBlockTokens * 4 : 0);
+  static constexpr int kKpeOff = kZeroOff + (LF == MLA_FMT_INT4_ASYM ? kNLG * kBlockTokens * 4 : 0);
   static constexpr int kKScaleOff = kKpeOff + kBlockTokens * kKRow;
   static constexpr int kBlock = kKScaleOff + (kKpeBf16 ? 0 : kNKG * kBlockTokens * 4);
   static constexpr int kStages = kBlock <= 24 * 1024 ? 6 : (kBlock <= 40 * 1024 ? 4 : 3);
@@ -694,11 +696,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
         ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(2 * w + cc, lane) * 16, t[0], t[1], t[2], t[3]);
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          // zero-points of this thread's B token (8n + r) for groups A and B of the chunk
-          float za = zp[(4 * w + 2 * cc) * kBlockTokens + 8 * n + r];
-          float zb = zp[(4 * w + 2 * cc + 1) * kBlockTokens + 8 * n + r];
-          if (partial && 8 * n + r >= nv) za = zb = 0.f;
-          const __half2 zz = __floats2half2_rn(za, zb);            // exact (integer zero-points)
+          __half2 zz;
+          if (F::kLatSym4) {
+            zz = __floats2half2_rn(8.f, 8.f);                         // nibble = code + 8
+          } else {
+            // zero-points of this thread's B token (8n + r) for groups A and B of the chunk
+            float za = zp[(4 * w + 2 * cc) * kBlockTokens + 8 * n + r];
+            float zb = zp[(4 * w + 2 * cc + 1) * kBlockTokens + 8 * n + r];
+            if (partial && 8 * n + r >= nv) za = zb = 0.f;
+            zz = __floats2half2_rn(za, zb);                            // exact (integer zero-points)
+          }
           i4x8_to_f16(t[n], __hadd2(zz, k1024), __hsub2(km64, zz), bq[2 * cc][n][0], bq[2 * cc][n][1],
                       bq[2 * cc + 1][n][0], bq[2 * cc + 1][n][1]);
         }
@@ -717,17 +724,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
     if (F::kKpeBf16) {
       if (kact) {
         uint32_t t[4];
-        ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(2 * w, lane, true) * 16, t[0], t[1], t[2], t[3]);
+        ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(2 * w, lane, KF) * 16, t[0], t[1], t[2], t[3]);
 #pragma unroll
         for (int n = 0; n < 4; ++n) bk[n][0] = t[n];
-        ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(2 * w + 1, lane, true) * 16, t[0], t[1], t[2],
+        ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(2 * w + 1, lane, KF) * 16, t[0], t[1], t[2],
                 t[3]);
 #pragma unroll
         for (int n = 0; n < 4; ++n) bk[n][1] = t[n];
       }
+    } else if (F::kKpeInt4) {
+      // warp w: k_pe group w = channels 8w .. 8w+7, in 32-channel chunk w / 4,
+      // 16-channel half (w / 2) % 2; the MMA takes the half's 16 channels
+      // (its A fragment is zero outside the group, as for INT8 k_pe)
+      uint32_t t[4];
+      ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(w >> 2, lane, KF) * 16, t[0], t[1], t[2], t[3]);
+      const __half2 zo = __floats2half2_rn(1032.f, 1032.f), zc = __floats2half2_rn(-72.f, -72.f);
+      const bool hb = (w >> 1) & 1;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        uint32_t a0, a1, b0, b1;
+        i4x8_to_f16(t[n], zo, zc, a0, a1, b0, b1);
+        bk[n][0] = hb ? b0 : a0;
+        bk[n][1] = hb ? b1 : a1;
+      }
     } else {
       uint32_t t[4];
-      ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(w >> 1, lane, false) * 16, t[0], t[1], t[2], t[3]);
+      ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(w >> 1, lane, KF) * 16, t[0], t[1], t[2], t[3]);
 #pragma unroll
       for (int n = 0; n < 4; ++n) i8x4_to_f16(t[n], bk[n][0], bk[n][1]);
     }
@@ -868,6 +890,12 @@ mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
   MLA_MMA_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT8_SYM)
   MLA_MMA_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_BF16)
   MLA_MMA_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT8_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT4_SYM, MLA_FMT_BF16)
+  MLA_MMA_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT8_SYM)
+  MLA_MMA_CASE(MLA_FMT_BF16, MLA_FMT_INT4_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT4_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT4_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT4_SYM)
 #undef MLA_MMA_CASE
   return MLA_ERR_UNSUPPORTED;
 }

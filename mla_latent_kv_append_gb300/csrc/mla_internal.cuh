@@ -39,10 +39,11 @@ __host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, Page
   switch (latent_fmt) {
     case MLA_FMT_BF16: row = 2 * kDc; break;
     case MLA_FMT_INT8_SYM: row = kDc; break;
-    case MLA_FMT_INT4_ASYM: row = kDc / 2; break;
+    case MLA_FMT_INT4_ASYM:
+    case MLA_FMT_INT4_SYM: row = kDc / 2; break;
     default: return false;
   }
-  if (kpe_fmt != MLA_FMT_BF16 && kpe_fmt != MLA_FMT_INT8_SYM) return false;
+  if (kpe_fmt != MLA_FMT_BF16 && kpe_fmt != MLA_FMT_INT8_SYM && kpe_fmt != MLA_FMT_INT4_SYM) return false;
   int64_t off = 0;
   L->codes_off = off;
   L->codes_row = row;
@@ -51,10 +52,10 @@ __host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, Page
   if (latent_fmt != MLA_FMT_BF16) { L->scale_off = off; off += (int64_t)kNLG * kBlockTokens * 4; }
   if (latent_fmt == MLA_FMT_INT4_ASYM) { L->zero_off = off; off += (int64_t)kNLG * kBlockTokens * 4; }
   L->kpe_off = off;
-  L->kpe_row = kpe_fmt == MLA_FMT_BF16 ? 2 * kDr : kDr;
+  L->kpe_row = kpe_fmt == MLA_FMT_BF16 ? 2 * kDr : (kpe_fmt == MLA_FMT_INT8_SYM ? kDr : kDr / 2);
   off += kBlockTokens * L->kpe_row;
   L->kpe_scale_off = -1;
-  if (kpe_fmt == MLA_FMT_INT8_SYM) { L->kpe_scale_off = off; off += (int64_t)kNKG * kBlockTokens * 4; }
+  if (kpe_fmt != MLA_FMT_BF16) { L->kpe_scale_off = off; off += (int64_t)kNKG * kBlockTokens * 4; }
   L->block_bytes = off;
   L->page_bytes = 2 * off;
   return true;
@@ -65,9 +66,10 @@ __host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, Page
 // index are XORed with t, so that eight consecutive tokens' copies of one
 // logical chunk fall in eight different shared-memory bank groups.
 __host__ __device__ __forceinline__ int latent_chunk_pos(int c, int t) { return (c & ~7) | ((c ^ t) & 7); }
-// Same for the k_pe row: 8 chunks (bf16) or 4 chunks (int8) per token.
-__host__ __device__ __forceinline__ int kpe_chunk_pos(int c, int t, bool bf16) {
-  return bf16 ? (c ^ (t & 7)) : (c ^ ((t >> 1) & 3));
+// Same for the k_pe row: 8 chunks (bf16), 4 chunks (int8) or 2 chunks
+// (4-bit) per token.
+__host__ __device__ __forceinline__ int kpe_chunk_pos(int c, int t, int kpe_fmt) {
+  return kpe_fmt == MLA_FMT_BF16 ? (c ^ (t & 7)) : (kpe_fmt == MLA_FMT_INT8_SYM ? (c ^ ((t >> 1) & 3)) : (c ^ ((t >> 2) & 1)));
 }
 // INT4 chunk c holds latent groups A = 2c and B = 2c + 1 (16 channels each).
 // Its 32-bit word j (j = 0..3) packs, from the least significant nibble:

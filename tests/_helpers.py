@@ -7,10 +7,9 @@ import synth
 from oracle import attention as A
 from oracle import quant as Q
 
-F_BF16, F_INT8, F_INT4 = 0, 1, 2
-ALL_FORMATS = [(F_BF16, F_BF16), (F_BF16, F_INT8), (F_INT8, F_BF16), (F_INT8, F_INT8), (F_INT4, F_BF16),
-               (F_INT4, F_INT8)]
-FMT_NAME = {F_BF16: "bf16", F_INT8: "int8", F_INT4: "int4"}
+F_BF16, F_INT8, F_INT4, F_INT4S = 0, 1, 2, 3
+ALL_FORMATS = [(lf, kf) for lf in (F_BF16, F_INT8, F_INT4, F_INT4S) for kf in (F_BF16, F_INT8, F_INT4S)]
+FMT_NAME = {F_BF16: "bf16", F_INT8: "int8", F_INT4: "int4", F_INT4S: "int4sym"}
 
 ATTN_TOL = 2e-3          # max relative error of attention outputs (per row, inf-norm)
 
@@ -24,7 +23,8 @@ def _int4_channel(j, k):
 def read_tokens(pool_np, layout, latent_fmt, kpe_fmt, slots):
     """Stored fields of the tokens at `slots` (numpy int array), decoded from
     the byte layout that include/mla.h documents (32-token blocks, swizzled
-    16-byte chunks, interleaved INT4 nibbles)."""
+    16-byte chunks, interleaved 4-bit nibbles, symmetric 4-bit codes stored
+    as code + 8)."""
     slots = np.asarray(slots, np.int64)
     n = len(slots)
     page, tok = slots // 64, slots % 64
@@ -53,27 +53,45 @@ def read_tokens(pool_np, layout, latent_fmt, kpe_fmt, slots):
         if latent_fmt == F_INT8:
             out["c_codes"] = logical.reshape(n, row).view(np.int8).copy()
         else:
-            words = logical.reshape(n, nchunk, 4, 4).astype(np.uint32)
-            words = words[..., 0] | (words[..., 1] << 8) | (words[..., 2] << 16) | (words[..., 3] << 24)
-            codes = np.zeros((n, 512), np.uint8)
-            for j in range(4):
-                for k in range(8):
-                    ch = np.arange(nchunk) * 32 + _int4_channel(j, k)
-                    codes[:, ch] = (words[:, :, j] >> (4 * k)) & 15
-            out["c_codes"] = codes
-            out["c_zero"] = fp32_field(layout.zero_off, 32)
+            codes = _nibbles(logical, n, nchunk)
+            if latent_fmt == F_INT4:
+                out["c_codes"] = codes
+                out["c_zero"] = fp32_field(layout.zero_off, 32)
+            else:
+                out["c_codes"] = (codes.astype(np.int16) - 8).astype(np.int8)
     krow = layout.kpe_row_bytes
     kch = krow // 16
     kphys = gather(layout.kpe_off + u * krow, krow).reshape(n, kch, 16)
     c = np.arange(kch)[None, :]
-    kpos = (c ^ (u[:, None] & 7)) if kpe_fmt == F_BF16 else (c ^ ((u[:, None] >> 1) & 3))
-    klog = np.take_along_axis(kphys, kpos[..., None], axis=1).reshape(n, krow)
     if kpe_fmt == F_BF16:
-        out["kpe_bits"] = klog.copy().view(np.uint16)
+        kpos = c ^ (u[:, None] & 7)
+    elif kpe_fmt == F_INT8:
+        kpos = c ^ ((u[:, None] >> 1) & 3)
     else:
-        out["kpe_codes"] = klog.view(np.int8).copy()
+        kpos = c ^ ((u[:, None] >> 2) & 1)
+    klog = np.take_along_axis(kphys, kpos[..., None], axis=1)
+    if kpe_fmt == F_BF16:
+        out["kpe_bits"] = klog.reshape(n, krow).copy().view(np.uint16)
+    elif kpe_fmt == F_INT8:
+        out["kpe_codes"] = klog.reshape(n, krow).view(np.int8).copy()
+        out["kpe_scale"] = fp32_field(layout.kpe_scale_off, 8)
+    else:
+        out["kpe_codes"] = (_nibbles(klog, n, kch, channels=64).astype(np.int16) - 8).astype(np.int8)
         out["kpe_scale"] = fp32_field(layout.kpe_scale_off, 8)
     return out
+
+
+def _nibbles(logical, n, nchunk, channels=512):
+    """4-bit values of [n, nchunk, 16] logical chunk bytes (the documented
+    word / nibble order) -> uint8 [n, channels]."""
+    words = logical.reshape(n, nchunk, 4, 4).astype(np.uint32)
+    words = words[..., 0] | (words[..., 1] << 8) | (words[..., 2] << 16) | (words[..., 3] << 24)
+    codes = np.zeros((n, channels), np.uint8)
+    for j in range(4):
+        for k in range(8):
+            ch = np.arange(nchunk) * 32 + _int4_channel(j, k)
+            codes[:, ch] = (words[:, :, j] >> (4 * k)) & 15
+    return codes
 
 
 def assert_fields_match(got, c_bits, k_bits, latent_fmt, kpe_fmt):
@@ -82,7 +100,7 @@ def assert_fields_match(got, c_bits, k_bits, latent_fmt, kpe_fmt):
     if latent_fmt == F_BF16:
         assert np.array_equal(got["c_bits"], c_bits)
     else:
-        assert np.array_equal(got["c_codes"], exp["c_codes"]), "latent codes differ"
+        assert np.array_equal(got["c_codes"].astype(np.int16), exp["c_codes"].astype(np.int16)), "latent codes differ"
         assert np.array_equal(got["c_scale"].view(np.uint32), exp["c_scale"].view(np.uint32)), "scales differ"
         if latent_fmt == F_INT4:
             assert np.array_equal(got["c_zero"].view(np.uint32), exp["c_zero"].view(np.uint32)), "zeros differ"

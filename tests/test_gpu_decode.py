@@ -44,11 +44,16 @@ def test_tiny_config(lf, kf):
     run_and_check(wl)
 
 
-@pytest.mark.parametrize("lf", [mla.FMT_BF16, mla.FMT_INT8_SYM, mla.FMT_INT4_ASYM])
-def test_ragged_batch_edges(lf):
+RAGGED_FORMATS = [(mla.FMT_BF16, mla.FMT_INT8_SYM), (mla.FMT_INT8_SYM, mla.FMT_INT8_SYM),
+                  (mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM), (mla.FMT_INT4_SYM, mla.FMT_INT8_SYM),
+                  (mla.FMT_INT4_ASYM, mla.FMT_INT4_SYM)]
+
+
+@pytest.mark.parametrize("lf,kf", RAGGED_FORMATS, ids=["%s-%s" % (FMT_NAME[a], FMT_NAME[b]) for a, b in RAGGED_FORMATS])
+def test_ragged_batch_edges(lf, kf):
     """Context lengths around page and chunk boundaries, plus an empty sequence."""
     lens = [1, 31, 32, 33, 63, 64, 65, 100, 0, 257, 129]
-    wl = Workload(1, 16, lens, lf, mla.FMT_INT8_SYM, seed=77)
+    wl = Workload(1, 16, lens, lf, kf, seed=77)
     run_and_check(wl)
 
 
