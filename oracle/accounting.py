@@ -25,6 +25,8 @@ or to the printed rounding, in tests/test_oracle_accounting.py).
 """
 
 FMT_BF16, FMT_INT8, FMT_INT4, FMT_INT4_SYM = 0, 1, 2, 3
+FMT_INT8_G8, FMT_INT8_G32, FMT_INT8_G64, FMT_INT8_TOKEN = 4, 5, 6, 7
+INT8_GROUP = {FMT_INT8: 16, FMT_INT8_G8: 8, FMT_INT8_G32: 32, FMT_INT8_G64: 64, FMT_INT8_TOKEN: 512}
 
 KV_LORA_RANK = 512
 ROPE_DIM = 64
@@ -52,7 +54,7 @@ def mla_theoretical_token_bytes(layers=V2_LITE_LAYERS):
 def _elem_bytes(fmt, n):
     if fmt == FMT_BF16:
         return 2 * n
-    if fmt == FMT_INT8:
+    if fmt in INT8_GROUP:
         return n
     if fmt in (FMT_INT4, FMT_INT4_SYM):
         return n // 2
@@ -72,8 +74,8 @@ def layer_bytes(latent_fmt, kpe_fmt, metadata=False):
     if metadata:
         lg = KV_LORA_RANK // LATENT_GROUP
         kg = ROPE_DIM // KPE_GROUP
-        if latent_fmt == FMT_INT8:
-            b += 4 * lg
+        if latent_fmt in INT8_GROUP:
+            b += 4 * (KV_LORA_RANK // INT8_GROUP[latent_fmt])
         elif latent_fmt == FMT_INT4:
             b += 8 * lg
         elif latent_fmt == FMT_INT4_SYM:

@@ -25,6 +25,10 @@ Readings taken where the pages are open (each is listed in the design doc):
   q = clamp(rint(x / s) + z, 0, 15).  x_hat = (q - z) * s.  When s comes out
   0: if min == 0 then s = z = q = 0; otherwise s = |min|, z = rint(-min / s)
   (= -1 or +1) and q = 0, which reconstructs the constant group exactly.
+* The block count of INT8 is a format choice: the English report's §5.1
+  compares 8, 32 and 64 blocks (groups of 64, 16 and 8 channels) and the
+  Chinese report's §3.2 a per-token row (one block of 512); each is a cache
+  format here (same rule, group size 8 / 16 / 32 / 64 / 512).
 * Symmetric INT4 (the report's "对称 INT4 (32块)" latent row and "k_pe 对称
   INT4 (8块)" row): s = absmax / 7, q = clamp(rint(x / s), -7, 7), the
   INT8 rule with 7 levels a side; x_hat = q * s.  Used as a cache format
@@ -174,7 +178,11 @@ def relative_error(x, x_hat):
 # ---------------------------------------------------------------------------
 
 FMT_BF16, FMT_INT8, FMT_INT4, FMT_INT4_SYM = 0, 1, 2, 3
+FMT_INT8_G8, FMT_INT8_G32, FMT_INT8_G64, FMT_INT8_TOKEN = 4, 5, 6, 7
 LATENT_GROUP, KPE_GROUP = 16, 8
+# symmetric INT8 latent formats -> channels per group (English report §5.1
+# block-count sweep: 64, 16, 8 blocks; Chinese report §3.2 per-token row)
+INT8_GROUP = {FMT_INT8: 16, FMT_INT8_G8: 8, FMT_INT8_G32: 32, FMT_INT8_G64: 64, FMT_INT8_TOKEN: 512}
 
 
 def quantize_token_rows(c, kpe, latent_fmt, kpe_fmt):
@@ -186,9 +194,10 @@ def quantize_token_rows(c, kpe, latent_fmt, kpe_fmt):
     out = {}
     if latent_fmt == FMT_BF16:
         out["c_hat"] = c.copy()
-    elif latent_fmt == FMT_INT8:
-        q, s = quantize_sym_int8(c, LATENT_GROUP)
-        out.update(c_codes=q, c_scale=s, c_hat=dequantize_sym_int8(q, s, LATENT_GROUP))
+    elif latent_fmt in INT8_GROUP:
+        g = INT8_GROUP[latent_fmt]
+        q, s = quantize_sym_int8(c, g)
+        out.update(c_codes=q, c_scale=s, c_hat=dequantize_sym_int8(q, s, g))
     elif latent_fmt == FMT_INT4:
         q, s, z = quantize_asym_int4(c, LATENT_GROUP)
         out.update(c_codes=q, c_scale=s, c_zero=z,

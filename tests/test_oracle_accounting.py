@@ -78,6 +78,17 @@ def test_symmetric_int4_formats_metadata():
     assert acc.layer_bytes(I4S, I4S, metadata=True) == 256 + 32 + 4 * 32 + 4 * 8 == 448
 
 
+def test_int8_block_count_formats_metadata():
+    # EN §5.1 sweep (8 / 32 / 64 blocks) and CN §3.2 per-token: same 512 B of
+    # codes, one fp32 scale per block
+    assert acc.layer_bytes(acc.FMT_INT8_G64, I8, metadata=True) == 512 + 4 * 8 + 96 == 640
+    assert acc.layer_bytes(acc.FMT_INT8_G32, I8, metadata=True) == 512 + 4 * 16 + 96 == 672
+    assert acc.layer_bytes(I8, I8, metadata=True) == 736
+    assert acc.layer_bytes(acc.FMT_INT8_G8, I8, metadata=True) == 512 + 4 * 64 + 96 == 864
+    assert acc.layer_bytes(acc.FMT_INT8_TOKEN, I8, metadata=True) == 512 + 4 + 96 == 612
+    assert acc.layer_bytes(acc.FMT_INT8_G8, I8) == acc.layer_bytes(I8, I8) == 576
+
+
 def test_capacity_in_10gb():
     # CN §4.1: INT8 69万 tokens, INT4 138万 tokens; EN §4.3: 39K / 690K / 620K / 1.24M.
     cap = lambda per_layer: acc.capacity_tokens(acc.token_bytes(per_layer))

@@ -32,9 +32,10 @@ def synth_kpe(T=512, layer=0, seed=7):
 
 # --------------------------------------------------------------- INT8 --------
 
-@pytest.mark.parametrize("group", [16, 8])
+@pytest.mark.parametrize("group", [16, 8, 32, 64, 512])
 def test_int8_codes_are_nearest_levels_brute_force(group):
-    x = np.concatenate([synth_latent(64)[:, :128], RNG.standard_normal((64, 128)).astype(np.float32) * 3])
+    w = max(128, group)
+    x = np.concatenate([synth_latent(64)[:, :w], RNG.standard_normal((64, w)).astype(np.float32) * 3])
     q, s = Q.quantize_sym_int8(x, group)
     assert q.dtype == np.int8 and s.dtype == np.float32
     sg = np.repeat(s, group, axis=1)
@@ -195,6 +196,19 @@ def test_sym_int4_scale_absmax_over_7_ties_and_zero_group():
     q, s = Q.quantize_sym_int4(row, 8)
     assert s[0].tolist() == [1.0, 0.0]
     assert q[0].tolist() == [7, 2, 4, 0, 6, -6, 2, 0] + [0] * 8
+
+
+def test_token_rows_int8_block_count_formats():
+    c, k = synth_latent(16), synth_kpe(16)
+    for fmt, g in ((Q.FMT_INT8_G8, 8), (Q.FMT_INT8_G32, 32), (Q.FMT_INT8_G64, 64), (Q.FMT_INT8_TOKEN, 512)):
+        d = Q.quantize_token_rows(c, k, fmt, Q.FMT_INT8)
+        q, s = Q.quantize_sym_int8(c, g)
+        assert d["c_scale"].shape == (16, 512 // g)
+        assert np.array_equal(d["c_codes"], q) and np.array_equal(d["c_scale"], s)
+    # one block per token is the report's per-token row
+    q1, s1 = Q.quantize_per_token_int8(c)
+    d = Q.quantize_token_rows(c, k, Q.FMT_INT8_TOKEN, Q.FMT_INT8)
+    assert np.array_equal(d["c_codes"], q1) and np.array_equal(d["c_scale"][:, 0], s1[:, 0])
 
 
 def test_sym_int4_round_trip_bound():
