@@ -44,6 +44,17 @@ CONFIGS = {
                                       "with scales and zero-points)"),
     "v2lite_int4sym_32k": dict(layers=27, heads=16, batch=32, ctx=32768, latent="int4sym", kpe="int8",
                                desc="V2-Lite shapes, batch 32, context 32768, symmetric INT4 latent + INT8 k_pe"),
+    # the English report's block-count sweep (8 / 32 / 64 blocks) and the
+    # per-token row, on the V2-Lite INT8 workload
+    "v2lite_int8_8blocks": dict(layers=27, heads=16, batch=8, ctx=4096, latent="int8g64", kpe="int8",
+                                desc="V2-Lite INT8 workload with 8 blocks of 64 latent channels"),
+    "v2lite_int8_16blocks": dict(layers=27, heads=16, batch=8, ctx=4096, latent="int8g32", kpe="int8",
+                                 desc="V2-Lite INT8 workload with 16 blocks of 32 latent channels"),
+    "v2lite_int8_64blocks": dict(layers=27, heads=16, batch=8, ctx=4096, latent="int8g8", kpe="int8",
+                                 desc="V2-Lite INT8 workload with 64 blocks of 8 latent channels "
+                                      "(fp32 CUDA-core decode)"),
+    "v2lite_int8_per_token": dict(layers=27, heads=16, batch=8, ctx=4096, latent="int8tok", kpe="int8",
+                                  desc="V2-Lite INT8 workload with one scale per token (per-token INT8)"),
     "long_int4_1m": dict(layers=27, heads=16, batch=1, ctx=1048576, latent="int4", kpe="int8",
                          desc="V2-Lite shapes, batch 1, context 1,048,576, asymmetric INT4 latent + INT8 k_pe"),
     "long_bf16_256k": dict(layers=27, heads=16, batch=1, ctx=262144, latent="bf16", kpe="bf16",
@@ -60,18 +71,20 @@ CONFIGS = {
     "tiny": dict(layers=1, heads=16, batch=1, ctx=256, latent="int8", kpe="int8",
                  desc="1 layer, 16 heads, batch 1, context 256"),
 }
-FMT = {"bf16": 0, "int8": 1, "int4": 2, "int4sym": 3}
+FMT = {"bf16": 0, "int8": 1, "int4": 2, "int4sym": 3, "int8g8": 4, "int8g32": 5, "int8g64": 6, "int8tok": 7}
 def _beta(latent, kpe):
     """Stored bytes per token and layer (codes + fp32 scales / zero-points),
     as laid out in include/mla.h: 32 latent groups of 16, 8 k_pe groups of 8."""
-    code = {"bf16": 1024, "int8": 512, "int4": 256, "int4sym": 256}[latent]
-    meta = {"bf16": 0, "int8": 128, "int4": 256, "int4sym": 128}[latent]
+    code = {"bf16": 1024, "int4": 256, "int4sym": 256}.get(latent, 512)
+    groups = {"int8g8": 64, "int8g32": 16, "int8g64": 8, "int8tok": 1}.get(latent, 32)
+    meta = {"bf16": 0, "int4": 8 * groups}.get(latent, 4 * groups)
     kcode = {"bf16": 128, "int8": 64, "int4sym": 32}[kpe]
     kmeta = 0 if kpe == "bf16" else 32
     return code + meta + kcode + kmeta
 
 
 BETA = {(a, b): _beta(a, b) for a in ("bf16", "int8", "int4", "int4sym") for b in ("bf16", "int8", "int4sym")}
+BETA.update({(a, "int8"): _beta(a, "int8") for a in ("int8g8", "int8g32", "int8g64", "int8tok")})
 METRIC = "decode tokens/s & achieved HBM GB/s (% of GB300 peak) for absorbed MLA decode"
 SEED = 0x4D4C41
 FALLBACK_HBM_GBS = 6800.0

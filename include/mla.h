@@ -72,7 +72,13 @@ typedef enum {
   MLA_FMT_BF16 = 0,        /* values stored as bf16, no scale */
   MLA_FMT_INT8_SYM = 1,    /* int8 code, fp32 scale per (token, group) */
   MLA_FMT_INT4_ASYM = 2,   /* 4-bit code, fp32 scale and zero per (token, group) */
-  MLA_FMT_INT4_SYM = 3     /* 4-bit code in [-7, 7], fp32 scale per (token, group) */
+  MLA_FMT_INT4_SYM = 3,    /* 4-bit code in [-7, 7], fp32 scale per (token, group) */
+  /* INT8_SYM latent with another block count ([EN] §5.1 sweep of 8 / 32 /
+   * 64 blocks, [CN] §3.2 per-token row); latent only, with INT8 k_pe */
+  MLA_FMT_INT8_G8 = 4,     /* 64 blocks of 8 channels */
+  MLA_FMT_INT8_G32 = 5,    /* 16 blocks of 32 channels */
+  MLA_FMT_INT8_G64 = 6,    /* 8 blocks of 64 channels */
+  MLA_FMT_INT8_TOKEN = 7   /* one block of 512 channels (per-token scale) */
 } mla_fmt;
 
 /* Bits ORed into *dev_err. */
@@ -94,7 +100,8 @@ typedef enum {
  * tokens; a token's physical slot is page * 64 + offset.  Which pages belong
  * to which sequence is the caller's business (block tables below).
  *   latent_fmt: any mla_fmt.  kpe_fmt: MLA_FMT_BF16, MLA_FMT_INT8_SYM or
- *   MLA_FMT_INT4_SYM.
+ *   MLA_FMT_INT4_SYM; the INT8_G* / INT8_TOKEN latent formats take
+ *   MLA_FMT_INT8_SYM k_pe only.
  *   pool: device memory of mla_cache_pool_bytes() bytes, 256-byte aligned,
  *         owned by the caller.
  */
@@ -111,7 +118,7 @@ typedef struct {
  * 32 tokens (token t of a page lives in block t / 32 as block token
  * u = t % 32), so that one bulk copy moves a whole 32-token work unit.
  * Inside a block, structure of arrays; offsets are from the block start,
- * every field starts on a 256-byte boundary, -1 marks a field the format
+ * every field starts on a 128-byte boundary, -1 marks a field the format
  * does not have:
  *   codes      [32][codes_row_bytes]: bf16 values (1024 B), int8 codes
  *              (512 B) or 4-bit codes (256 B).  The row is a sequence of
@@ -123,7 +130,8 @@ typedef struct {
  *              A[4j], A[4j+2], B[4j], B[4j+2], A[4j+1], A[4j+3], B[4j+1],
  *              B[4j+3] (X[i] = nibble of channel i of group X).  A nibble is
  *              the code (INT4_ASYM, 0..15) or the code + 8 (INT4_SYM, 1..15).
- *   scale      fp32 [32 groups][32 block tokens]   (int8 / 4-bit latent)
+ *   scale      fp32 [G groups][32 block tokens]    (int8 / 4-bit latent; G = 32,
+ *              or 64 / 16 / 8 / 1 for INT8_G8 / G32 / G64 / TOKEN)
  *   zero       fp32 [32 groups][32 block tokens]   (INT4_ASYM latent; integer-valued)
  *   kpe        [32][kpe_row_bytes]: bf16 (128 B = 8 chunks of 8 channels,
  *              chunk c of token u at position c ^ (u & 7)), int8 (64 B =
@@ -159,7 +167,8 @@ size_t mla_cache_pool_bytes(const mla_cache_layer* cache);
  * [EN] §2.1 store(): compressed_kv [seq, 512] is quantized, k_pe [seq, 64]
  * stored; [CN] §3.2 for the formats.  Quantization rules, all IEEE fp32 with
  * round-half-even and no fused multiply-add:
- *   INT8_SYM  (groups of 16 latent channels, or 8 k_pe channels):
+ *   INT8_SYM  (groups of 16 latent channels - 8, 32, 64 or 512 for the
+ *             INT8_G8 / G32 / G64 / TOKEN formats - or 8 k_pe channels):
  *       s = max|x| / 127;  q = clamp(rint(x / s), -127, 127);  s = 0 -> q = 0
  *   INT4_ASYM (groups of 16): s = (max - min) / 15;  z = rint(-min / s);
  *       q = clamp(rint(x / s) + z, 0, 15); if s == 0: s = |min|, z = rint(-min/s)

@@ -33,6 +33,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmla_gb300.so")
 
 FMT_BF16, FMT_INT8_SYM, FMT_INT4_ASYM, FMT_INT4_SYM = 0, 1, 2, 3
+FMT_INT8_G8, FMT_INT8_G32, FMT_INT8_G64, FMT_INT8_TOKEN = 4, 5, 6, 7    # INT8 latent, other block counts
 DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 KV_LORA_RANK, ROPE_DIM, QK_NOPE_DIM, V_DIM, PAGE_TOKENS = 512, 64, 128, 128, 64
 DEFAULT_SOFTMAX_SCALE = 1.0 / math.sqrt(QK_NOPE_DIM + ROPE_DIM)

@@ -58,13 +58,19 @@ __device__ __forceinline__ void div_rn_shared(const float* x, float s, float* ou
   }
 }
 
-// Symmetric quantization of N values with levels -QMAX .. QMAX (127 for
-// INT8, 7 for INT4_SYM); returns the scale, writes the codes.
-template <int N, int QMAX>
-__device__ __forceinline__ float quant_sym(const float* x, int8_t* q) {
+template <int N>
+__device__ __forceinline__ float absmax(const float* x) {
   float a = 0.f;
 #pragma unroll
   for (int i = 0; i < N; ++i) a = fmaxf(a, fabsf(x[i]));
+  return a;
+}
+
+// Symmetric quantization of N values with levels -QMAX .. QMAX (127 for
+// INT8, 7 for INT4_SYM) given their group's absmax a (which may span more
+// than these N values); returns the scale, writes the codes.
+template <int N, int QMAX>
+__device__ __forceinline__ float quant_sym_a(const float* x, float a, int8_t* q) {
   const float s = __fdiv_rn(a, (float)QMAX);
   float d[N];
   if (s > 0.f) div_rn_shared<N>(x, s, d);
@@ -74,6 +80,11 @@ __device__ __forceinline__ float quant_sym(const float* x, int8_t* q) {
     q[i] = (int8_t)(int)r;
   }
   return s;
+}
+
+template <int N, int QMAX>
+__device__ __forceinline__ float quant_sym(const float* x, int8_t* q) {
+  return quant_sym_a<N, QMAX>(x, absmax<N>(x), q);
 }
 
 // Nibbles of one 16-channel half (or group) of a 4-bit chunk, placed in the
@@ -144,9 +155,22 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
       float x[16];
       unpack16(v0, v1, x);
       float* scale = reinterpret_cast<float*>(blk + L.scale_off);
-      if (LF == MLA_FMT_INT8_SYM) {
+      if (is_int8_latent(LF)) {
+        // lane = 16-channel chunk; a group of GS channels spans GS / 16
+        // lanes (absmax by shuffles, every lane then derives the same
+        // scale) or, for GS = 8, half a lane
+        constexpr int GS = latent_group_size(LF);
         int8_t q[16];
-        scale[lane * kBlockTokens + t] = quant_sym<16, 127>(x, q);
+        if (GS == 8) {
+          scale[(2 * lane) * kBlockTokens + t] = quant_sym<8, 127>(x, q);
+          scale[(2 * lane + 1) * kBlockTokens + t] = quant_sym<8, 127>(x + 8, q + 8);
+        } else {
+          float a = absmax<16>(x);
+#pragma unroll
+          for (int o = 1; o < GS / 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+          const float sc = quant_sym_a<16, 127>(x, a, q);
+          if (lane % (GS / 16) == 0) scale[(lane / (GS / 16)) * kBlockTokens + t] = sc;
+        }
         uint32_t w[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -277,6 +301,10 @@ mla_status launch_append(const mla_cache_layer* cache, const PageLayout& L, cons
   MLA_APPEND_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT4_SYM)
   MLA_APPEND_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT4_SYM)
   MLA_APPEND_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT4_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT8_G8, MLA_FMT_INT8_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT8_G32, MLA_FMT_INT8_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT8_G64, MLA_FMT_INT8_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM)
 #undef MLA_APPEND_CASE
   return MLA_ERR_UNSUPPORTED;
 }

@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
           s_c[t * kCS + 2 * pr] = a;
           s_c[t * kCS + 2 * pr + 1] = bb;
         }
-      } else if (LF == MLA_FMT_INT8_SYM) {
+      } else if (is_int8_latent(LF)) {
         for (int i = tid; i < kChunk * (kDc / 4); i += kThreads) {
           const int t = i / (kDc / 4), wi = i % (kDc / 4);
           float v[4] = {0.f, 0.f, 0.f, 0.f};
@@ -170,7 +170,8 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
             const uint8_t* blk = pool + s_page[t] * pb + blk_off;
             const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.codes_off + (int64_t)t * p.L.codes_row)[
                 latent_chunk_pos(wi >> 2, t) * 4 + (wi & 3)];
-            const float s = reinterpret_cast<const float*>(blk + p.L.scale_off)[(wi >> 2) * kBlockTokens + t];
+            const float s = reinterpret_cast<const float*>(blk + p.L.scale_off)[
+                (4 * wi / latent_group_size(LF)) * kBlockTokens + t];
 #pragma unroll
             for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), s);
           }
@@ -445,6 +446,10 @@ mla_status launch_decode_ref(const DecodeParams& p, cudaStream_t stream) {
   MLA_DECODE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT4_SYM)
   MLA_DECODE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT4_SYM)
   MLA_DECODE_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT4_SYM)
+  MLA_DECODE_CASE(MLA_FMT_INT8_G8, MLA_FMT_INT8_SYM)
+  MLA_DECODE_CASE(MLA_FMT_INT8_G32, MLA_FMT_INT8_SYM)
+  MLA_DECODE_CASE(MLA_FMT_INT8_G64, MLA_FMT_INT8_SYM)
+  MLA_DECODE_CASE(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM)
 #undef MLA_DECODE_CASE
   return MLA_ERR_UNSUPPORTED;
 }

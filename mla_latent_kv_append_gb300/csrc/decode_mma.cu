@@ -57,10 +57,13 @@ struct Fmt {
   static constexpr bool kLatSym4 = LF == MLA_FMT_INT4_SYM;       // zero-point fixed at 8 (nibble = code + 8)
   static constexpr bool kKpeBf16 = KF == MLA_FMT_BF16;
   static constexpr bool kKpeInt4 = KF == MLA_FMT_INT4_SYM;
-  static constexpr int kRow = kLatBf16 ? 1024 : (LF == MLA_FMT_INT8_SYM ? 512 : 256);
+  static constexpr int kRow = kLatBf16 ? 1024 : (is_int8_latent(LF) ? 512 : 256);
   static constexpr int kKRow = kKpeBf16 ? 128 : (kKpeInt4 ? 32 : 64);
+  static constexpr int kGS = latent_group_size(LF);             // channels per scale group
+  static constexpr int kSPG = kGS / 16;                          // 16-channel MMA steps per scale group
+  static_assert(kGS % 16 == 0, "scale groups of whole 16-channel MMA steps");
   static constexpr int kScaleOff = kBlockTokens * kRow;
-  static constexpr int kZeroOff = kScaleOff + (kLatBf16 ? 0 : kNLG * kBlockTokens * 4);
+  static constexpr int kZeroOff = kScaleOff + (kLatBf16 ? 0 : (kDc / kGS) * kBlockTokens * 4);
   static constexpr int kKpeOff = kZeroOff + (LF == MLA_FMT_INT4_ASYM ? kNLG * kBlockTokens * 4 : 0);
   static constexpr int kKScaleOff = kKpeOff + kBlockTokens * kKRow;
   static constexpr int kBlock = kKScaleOff + (kKpeBf16 ? 0 : kNKG * kBlockTokens * 4);
@@ -768,26 +771,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
         for (int n = 0; n < 4; ++n) mma_bf16(acc[n], q.lo[g], bq[g][n][0], bq[g][n][1], acc[n]);
       }
     } else {
+      // the MMA steps of one scale group accumulate together (exact codes,
+      // fp32 accumulator), then one FMA per element applies the scale
       const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+      float d[4][4];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
-        float d[4][4];
+        const bool first = g % F::kSPG == 0, last = (g + 1) % F::kSPG == 0 || g == 3;
 #pragma unroll
-        for (int n = 0; n < 4; ++n) mma_f16(d[n], q.hi[g], bq[g][n][0], bq[g][n][1], zero4);
+        for (int n = 0; n < 4; ++n) mma_f16(d[n], q.hi[g], bq[g][n][0], bq[g][n][1], first ? zero4 : d[n]);
 #pragma unroll
         for (int n = 0; n < 4; ++n) mma_f16(d[n], q.lo[g], bq[g][n][0], bq[g][n][1], d[n]);
+        if (last) {
+          const int si = (4 * w + g) / F::kSPG;
 #pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          float2 s2 = *reinterpret_cast<const float2*>(sc + (4 * w + g) * kBlockTokens + 8 * n + 2 * j);
-          if (partial) {
-            if (8 * n + 2 * j >= nv) s2.x = 0.f;
-            if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
+          for (int n = 0; n < 4; ++n) {
+            float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
+            if (partial) {
+              if (8 * n + 2 * j >= nv) s2.x = 0.f;
+              if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
+            }
+            acc[n][0] = fmaf(d[n][0], s2.x, acc[n][0]);
+            acc[n][1] = fmaf(d[n][1], s2.y, acc[n][1]);
+            acc[n][2] = fmaf(d[n][2], s2.x, acc[n][2]);
+            acc[n][3] = fmaf(d[n][3], s2.y, acc[n][3]);
+            const uint32_t sh = pack_f16(s2.x, s2.y);
+#pragma unroll
+            for (int g2 = 0; g2 < 4; ++g2)
+              if (g2 <= g && g2 > g - F::kSPG) s2h[g2][n] = sh;
           }
-          acc[n][0] = fmaf(d[n][0], s2.x, acc[n][0]);
-          acc[n][1] = fmaf(d[n][1], s2.y, acc[n][1]);
-          acc[n][2] = fmaf(d[n][2], s2.x, acc[n][2]);
-          acc[n][3] = fmaf(d[n][3], s2.y, acc[n][3]);
-          s2h[g][n] = pack_f16(s2.x, s2.y);
         }
       }
     }
@@ -896,6 +908,9 @@ mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
   MLA_MMA_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT4_SYM)
   MLA_MMA_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT4_SYM)
   MLA_MMA_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT4_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT8_G32, MLA_FMT_INT8_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT8_G64, MLA_FMT_INT8_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM)
 #undef MLA_MMA_CASE
   return MLA_ERR_UNSUPPORTED;
 }

@@ -34,10 +34,29 @@ struct PageLayout {
   int64_t kpe_scale_off;
 };
 
+// Channels per scale group of a quantized latent format (16 unless one of
+// the INT8 block-count variants).
+__host__ __device__ constexpr int latent_group_size(int latent_fmt) {
+  return latent_fmt == MLA_FMT_INT8_G8 ? 8
+         : latent_fmt == MLA_FMT_INT8_G32 ? 32
+         : latent_fmt == MLA_FMT_INT8_G64 ? 64
+         : latent_fmt == MLA_FMT_INT8_TOKEN ? kDc : kLG;
+}
+__host__ __device__ constexpr bool is_int8_latent(int latent_fmt) {
+  return latent_fmt == MLA_FMT_INT8_SYM || (latent_fmt >= MLA_FMT_INT8_G8 && latent_fmt <= MLA_FMT_INT8_TOKEN);
+}
+
 __host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, PageLayout* L) {
   int64_t row;
   switch (latent_fmt) {
     case MLA_FMT_BF16: row = 2 * kDc; break;
+    case MLA_FMT_INT8_G8:
+    case MLA_FMT_INT8_G32:
+    case MLA_FMT_INT8_G64:
+    case MLA_FMT_INT8_TOKEN:
+      if (kpe_fmt != MLA_FMT_INT8_SYM) return false;
+      row = kDc;
+      break;
     case MLA_FMT_INT8_SYM: row = kDc; break;
     case MLA_FMT_INT4_ASYM:
     case MLA_FMT_INT4_SYM: row = kDc / 2; break;
@@ -49,7 +68,10 @@ __host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, Page
   L->codes_row = row;
   off += kBlockTokens * row;
   L->scale_off = L->zero_off = -1;
-  if (latent_fmt != MLA_FMT_BF16) { L->scale_off = off; off += (int64_t)kNLG * kBlockTokens * 4; }
+  if (latent_fmt != MLA_FMT_BF16) {
+    L->scale_off = off;
+    off += (int64_t)(kDc / latent_group_size(latent_fmt)) * kBlockTokens * 4;
+  }
   if (latent_fmt == MLA_FMT_INT4_ASYM) { L->zero_off = off; off += (int64_t)kNLG * kBlockTokens * 4; }
   L->kpe_off = off;
   L->kpe_row = kpe_fmt == MLA_FMT_BF16 ? 2 * kDr : (kpe_fmt == MLA_FMT_INT8_SYM ? kDr : kDr / 2);

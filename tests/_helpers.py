@@ -8,8 +8,12 @@ from oracle import attention as A
 from oracle import quant as Q
 
 F_BF16, F_INT8, F_INT4, F_INT4S = 0, 1, 2, 3
-ALL_FORMATS = [(lf, kf) for lf in (F_BF16, F_INT8, F_INT4, F_INT4S) for kf in (F_BF16, F_INT8, F_INT4S)]
-FMT_NAME = {F_BF16: "bf16", F_INT8: "int8", F_INT4: "int4", F_INT4S: "int4sym"}
+F_I8G8, F_I8G32, F_I8G64, F_I8TOK = 4, 5, 6, 7
+INT8_GROUP = {F_INT8: 16, F_I8G8: 8, F_I8G32: 32, F_I8G64: 64, F_I8TOK: 512}
+ALL_FORMATS = ([(lf, kf) for lf in (F_BF16, F_INT8, F_INT4, F_INT4S) for kf in (F_BF16, F_INT8, F_INT4S)] +
+               [(lf, F_INT8) for lf in (F_I8G8, F_I8G32, F_I8G64, F_I8TOK)])
+FMT_NAME = {F_BF16: "bf16", F_INT8: "int8", F_INT4: "int4", F_INT4S: "int4sym", F_I8G8: "int8g8",
+            F_I8G32: "int8g32", F_I8G64: "int8g64", F_I8TOK: "int8tok"}
 
 ATTN_TOL = 2e-3          # max relative error of attention outputs (per row, inf-norm)
 
@@ -49,8 +53,8 @@ def read_tokens(pool_np, layout, latent_fmt, kpe_fmt, slots):
     if latent_fmt == F_BF16:
         out["c_bits"] = logical.reshape(n, row).copy().view(np.uint16)
     else:
-        out["c_scale"] = fp32_field(layout.scale_off, 32)
-        if latent_fmt == F_INT8:
+        out["c_scale"] = fp32_field(layout.scale_off, 512 // INT8_GROUP.get(latent_fmt, 16))
+        if latent_fmt in INT8_GROUP:
             out["c_codes"] = logical.reshape(n, row).view(np.int8).copy()
         else:
             codes = _nibbles(logical, n, nchunk)

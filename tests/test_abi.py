@@ -40,17 +40,21 @@ def test_exports_every_declared_symbol(lib):
 
 def test_layouts_match_the_accounting(lib):
     from oracle import accounting as acc
-    for lf in (0, 1, 2, 3):
-        for kf in (0, 1, 3):
-            L = lib.mla_cache_page_layout(lf, kf)
-            assert L.page_bytes == 64 * acc.layer_bytes(lf, kf, metadata=True)
-            for off in (L.codes_off, L.scale_off, L.zero_off, L.kpe_off, L.kpe_scale_off):
-                assert off == -1 or off % 256 == 0
-            assert (L.zero_off == -1) == (lf != 2)
+    pairs = [(lf, kf) for lf in (0, 1, 2, 3) for kf in (0, 1, 3)] + [(lf, 1) for lf in (4, 5, 6, 7)]
+    for lf, kf in pairs:
+        L = lib.mla_cache_page_layout(lf, kf)
+        assert L.page_bytes == 64 * acc.layer_bytes(lf, kf, metadata=True)
+        for off in (L.codes_off, L.scale_off, L.zero_off, L.kpe_off, L.kpe_scale_off):
+            assert off == -1 or off % 128 == 0
+        assert (L.zero_off == -1) == (lf != 2)
+    for lf in (4, 5, 6, 7):                           # other block counts: INT8 k_pe only
+        for kf in (0, 3):
+            with pytest.raises(lib.MlaError):
+                lib.mla_cache_page_layout(lf, kf)
     assert lib.mla_cache_pool_bytes(10, 1, 1) == 10 * 64 * 736
     assert lib.mla_cache_pool_bytes(10, 2, 3) == 10 * 64 * 576   # the 7.6 KB-per-token scheme, with metadata
     assert lib.mla_cache_pool_bytes(0, 1, 1) == 0
-    assert lib.mla_cache_pool_bytes(4, 4, 1) == 0
+    assert lib.mla_cache_pool_bytes(4, 8, 1) == 0
     assert lib.mla_cache_pool_bytes(4, 1, 2) == 0     # asymmetric INT4 k_pe is not a cache format
 
 

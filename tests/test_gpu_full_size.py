@@ -32,6 +32,8 @@ CASES = [
     ("v2lite_int8", None),
     ("v2lite_int4_32k", SAMPLED),
     ("v2lite_int4_kpe4_32k", (0, 26)),
+    ("v2lite_int8_per_token", (0, 13, 26)),
+    ("v2lite_int8_64blocks", (0, 26)),
     ("long_int4_1m", SAMPLED),
     ("long_bf16_256k", SAMPLED),
     ("mixed_h64_int8", None),
