@@ -128,7 +128,9 @@ class Workload:
 class DecodeStep:
     """Buffers and the per-layer call sequence of one decode step:
     [prefill append ->] append -> absorb -> decode (+combine) -> unabsorb,
-    for every layer."""
+    for every layer.  The appends and the absorb of a layer depend only on
+    the layer's inputs, so the appends run on a side stream beside the
+    absorb and the decode waits for both."""
 
     def __init__(self, wl, num_splits=0, with_lse=True):
         dev = wl.device
@@ -140,14 +142,19 @@ class DecodeStep:
         nbytes = mla.mla_decode_workspace_bytes(wl.B, wl.H, num_splits)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.side = torch.cuda.Stream(device=dev)
 
     def run(self, keep_o_lat=None):
         wl = self.wl
+        main = torch.cuda.current_stream(self.q_lat.device)
         for l in range(wl.L):
-            if wl.prefill:
-                mla.mla_cache_append(wl.caches[l], wl.c_pre[l], wl.kpe_pre[l], wl.slot_pre, self.dev_err)
-            mla.mla_cache_append(wl.caches[l], wl.c_new[l], wl.kpe_new[l], wl.slot_new, self.dev_err)
+            self.side.wait_stream(main)
+            with torch.cuda.stream(self.side):
+                if wl.prefill:
+                    mla.mla_cache_append(wl.caches[l], wl.c_pre[l], wl.kpe_pre[l], wl.slot_pre, self.dev_err)
+                mla.mla_cache_append(wl.caches[l], wl.c_new[l], wl.kpe_new[l], wl.slot_new, self.dev_err)
             mla.mla_q_absorb(wl.q_nope[l], wl.w_uk[l], self.q_lat)
+            main.wait_stream(self.side)
             mla.mla_decode_absorbed(wl.caches[l], self.q_lat, wl.q_pe[l], wl.block_table, wl.seq_lens_dev,
                                     self.workspace, self.o_lat, None if self.lse is None else self.lse[l],
                                     self.dev_err, num_splits=self.num_splits)
