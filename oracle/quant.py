@@ -13,7 +13,7 @@ Sources (page title, section):
   section "量化压缩": scale = absmax / 127, code = round(x / scale),
   x_hat = code * scale.
 
-Readings taken where the pages are open (each is listed in the design doc):
+Readings taken where the pages are open:
 
 * "32 blocks" of the 512-dim latent are 32 groups of 16 consecutive channels
   with one scale per (token, group): a scale computed across future tokens is
