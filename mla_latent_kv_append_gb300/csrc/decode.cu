@@ -340,7 +340,9 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
 // grid (B, H), block 128: merge the partials of sequence b, head h.  CTAs
 // span[2b] .. span[2b+1] wrote slots x + b.  The slots' maxima and sums are
 // read in parallel (one slot per thread), the block reduces them, and each
-// thread then accumulates 4 channels over all slots with independent loads.
+// thread then accumulates 4 channels over all slots with independent loads:
+// every slot in the span was written (o finite, weight 0 for an empty one),
+// so the loads are unconditional and eight of them are in flight at a time.
 constexpr int kCombSlots = 1024;     // weights cached in shared memory
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
@@ -388,7 +390,8 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   const float L = block_reduce(lloc, false, red);   // also orders the sw writes before the reads below
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* o4 = reinterpret_cast<const float4*>(p.ws.o + ((size_t)(x0 + b) * p.H + h) * kDc) + tid;
-#pragma unroll 4
+  const size_t ostride = (size_t)p.H * (kDc / 4);
+#pragma unroll 8
   for (int t = 0; t < S; ++t) {
     float w;
     if (t < kCombSlots) {
@@ -397,13 +400,11 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
       const float m = mp[(size_t)t * p.H];
       w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
     }
-    if (w != 0.f) {
-      const float4 v = o4[(size_t)t * p.H * (kDc / 4)];
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
-    }
+    const float4 v = __ldcg(o4 + (size_t)t * ostride);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
   }
   if (L > 0.f) {
     const float inv = 1.f / L;

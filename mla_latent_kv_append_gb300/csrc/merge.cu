@@ -72,12 +72,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const float* __res
     l += w;
   }
   l = block_sum(l, red);                        // also orders the wts writes before the reads below
+  // an empty part (weight 0) may hold any values, even non-finite ones:
+  // its loads are skipped by a select, not a branch, so that up to eight
+  // loads are in flight at a time
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* src = reinterpret_cast<const float4*>(o_parts + row * kDc) + tid;
+#pragma unroll 8
   for (int r = 0; r < R; ++r) {
     const float w = wts[r];
-    if (w == 0.f) continue;
-    const float4 v = src[r * stride * (kDc / 4)];
+    float4 v = __ldcg(src + r * stride * (kDc / 4));
+    if (w == 0.f) v = make_float4(0.f, 0.f, 0.f, 0.f);
     acc.x = fmaf(w, v.x, acc.x);
     acc.y = fmaf(w, v.y, acc.y);
     acc.z = fmaf(w, v.z, acc.z);
