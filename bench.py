@@ -51,8 +51,7 @@ CONFIGS = {
     "v2lite_int8_16blocks": dict(layers=27, heads=16, batch=8, ctx=4096, latent="int8g32", kpe="int8",
                                  desc="V2-Lite INT8 workload with 16 blocks of 32 latent channels"),
     "v2lite_int8_64blocks": dict(layers=27, heads=16, batch=8, ctx=4096, latent="int8g8", kpe="int8",
-                                 desc="V2-Lite INT8 workload with 64 blocks of 8 latent channels "
-                                      "(fp32 CUDA-core decode)"),
+                                 desc="V2-Lite INT8 workload with 64 blocks of 8 latent channels"),
     "v2lite_int8_per_token": dict(layers=27, heads=16, batch=8, ctx=4096, latent="int8tok", kpe="int8",
                                   desc="V2-Lite INT8 workload with one scale per token (per-token INT8)"),
     "long_int4_1m": dict(layers=27, heads=16, batch=1, ctx=1048576, latent="int4", kpe="int8",

@@ -123,8 +123,9 @@ typedef struct {
  *   codes      [32][codes_row_bytes]: bf16 values (1024 B), int8 codes
  *              (512 B) or 4-bit codes (256 B).  The row is a sequence of
  *              16-byte chunks; logical chunk c of block token u is stored at
- *              chunk position (c & ~7) | ((c ^ u) & 7).  An int8 chunk is one
- *              16-channel group in channel order; a bf16 chunk is 8 channels.
+ *              chunk position (c & ~7) | ((c ^ u) & 7).  An int8 chunk is 16
+ *              channels in channel order (INT8_G8: its 32-bit word j holds
+ *              channels 2j, 2j+1, 8+2j, 8+2j+1); a bf16 chunk is 8 channels.
  *              A 4-bit chunk c holds groups A = 2c and B = 2c + 1; its 32-bit
  *              word j (j = 0..3) packs, from the least significant nibble,
  *              A[4j], A[4j+2], B[4j], B[4j+2], A[4j+1], A[4j+3], B[4j+1],

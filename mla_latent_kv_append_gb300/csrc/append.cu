@@ -171,11 +171,15 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
           const float sc = quant_sym_a<16, 127>(x, a, q);
           if (lane % (GS / 16) == 0) scale[(lane / (GS / 16)) * kBlockTokens + t] = sc;
         }
+        // byte order of the chunk: channels in order, except for 8-channel
+        // groups, where word j holds channels 2j, 2j+1, 8+2j, 8+2j+1
         uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          w[j] = (uint32_t)(uint8_t)q[4 * j] | ((uint32_t)(uint8_t)q[4 * j + 1] << 8) |
-                 ((uint32_t)(uint8_t)q[4 * j + 2] << 16) | ((uint32_t)(uint8_t)q[4 * j + 3] << 24);
+        for (int j = 0; j < 4; ++j) {
+          const int c0 = GS == 8 ? 2 * j : 4 * j, c2 = GS == 8 ? 8 + 2 * j : 4 * j + 2;
+          w[j] = (uint32_t)(uint8_t)q[c0] | ((uint32_t)(uint8_t)q[c0 + 1] << 8) |
+                 ((uint32_t)(uint8_t)q[c2] << 16) | ((uint32_t)(uint8_t)q[c2 + 1] << 24);
+        }
         reinterpret_cast<uint4*>(row)[latent_chunk_pos(lane, t)] = make_uint4(w[0], w[1], w[2], w[3]);
       } else {
         uint8_t q[16];

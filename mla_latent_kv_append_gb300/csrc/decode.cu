@@ -166,17 +166,23 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
         for (int i = tid; i < kChunk * (kDc / 4); i += kThreads) {
           const int t = i / (kDc / 4), wi = i % (kDc / 4);
           float v[4] = {0.f, 0.f, 0.f, 0.f};
+          // channel of byte j of word wi (8-channel groups store 2jj, 2jj+1,
+          // 8+2jj, 8+2jj+1 in word jj of a 16-channel chunk)
+          int ch[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            ch[j] = latent_group_size(LF) == 8 ? 16 * (wi >> 2) + 2 * (wi & 3) + (j & 1) + 8 * (j >> 1) : 4 * wi + j;
           if (s_valid[t]) {
             const uint8_t* blk = pool + s_page[t] * pb + blk_off;
             const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.codes_off + (int64_t)t * p.L.codes_row)[
                 latent_chunk_pos(wi >> 2, t) * 4 + (wi & 3)];
-            const float s = reinterpret_cast<const float*>(blk + p.L.scale_off)[
-                (4 * wi / latent_group_size(LF)) * kBlockTokens + t];
+            const float* sc = reinterpret_cast<const float*>(blk + p.L.scale_off);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), s);
+            for (int j = 0; j < 4; ++j)
+              v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), sc[(ch[j] / latent_group_size(LF)) * kBlockTokens + t]);
           }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) s_c[t * kCS + 4 * wi + j] = v[j];
+          for (int j = 0; j < 4; ++j) s_c[t * kCS + ch[j]] = v[j];
         }
       } else {
         for (int i = tid; i < kChunk * (kDc / 8); i += kThreads) {

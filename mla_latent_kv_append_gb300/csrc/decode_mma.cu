@@ -60,8 +60,12 @@ struct Fmt {
   static constexpr int kRow = kLatBf16 ? 1024 : (is_int8_latent(LF) ? 512 : 256);
   static constexpr int kKRow = kKpeBf16 ? 128 : (kKpeInt4 ? 32 : 64);
   static constexpr int kGS = latent_group_size(LF);             // channels per scale group
-  static constexpr int kSPG = kGS / 16;                          // 16-channel MMA steps per scale group
-  static_assert(kGS % 16 == 0, "scale groups of whole 16-channel MMA steps");
+  static constexpr bool kLatG8 = kGS == 8;                       // two scale groups per 16-channel MMA step
+  static constexpr int kSPG = kLatG8 ? 1 : kGS / 16;             // 16-channel MMA steps per scale group
+  // operand layout: standard m16n8k16 fragments (thread j holds channels 2j,
+  // 2j+1 and 8+2j, 8+2j+1) for bf16 and 8-channel groups, else permuted
+  // (thread j holds channels 4j .. 4j+3)
+  static constexpr bool kStdLayout = kLatBf16 || kLatG8;
   static constexpr int kScaleOff = kBlockTokens * kRow;
   static constexpr int kZeroOff = kScaleOff + (kLatBf16 ? 0 : (kDc / kGS) * kBlockTokens * 4);
   static constexpr int kKpeOff = kZeroOff + (LF == MLA_FMT_INT4_ASYM ? kNLG * kBlockTokens * 4 : 0);
@@ -154,6 +158,13 @@ __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
         "f"(c[3]));
+}
+
+// d = a * b + c for m16n8k8 (two A registers, one B register)
+__device__ __forceinline__ void mma_f16_k8(float* d, uint32_t a0, uint32_t a1, uint32_t b0, const float* c) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%8,%9,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
 
 __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1, const float* c) {
@@ -282,8 +293,8 @@ __device__ __forceinline__ float load_query_raw(const DecodeParams& p, int b, in
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     const int gg = 4 * w + g;
-    if (F::kLatBf16) {
-      // standard layout: channels 2j, 2j+1 and 8+2j, 8+2j+1 of the group
+    if (F::kStdLayout) {
+      // standard layout: channels 2j, 2j+1 and 8+2j, 8+2j+1 of the 16 channels
       const float2 a0 = *reinterpret_cast<const float2*>(ql0 + 16 * gg + 2 * j);
       const float2 a1 = *reinterpret_cast<const float2*>(ql0 + 16 * gg + 8 + 2 * j);
       const float2 b0 = *reinterpret_cast<const float2*>(ql1 + 16 * gg + 2 * j);
@@ -504,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const int base = 16 * (4 * w + g);
-      if (F::kLatBf16) {
+      if (F::kStdLayout) {
         *reinterpret_cast<float2*>(o0 + base + 2 * j) = make_float2(o[g][0][0], o[g][0][1]);
         *reinterpret_cast<float2*>(o0 + base + 8 + 2 * j) = make_float2(o[g][1][0], o[g][1][1]);
         *reinterpret_cast<float2*>(o1 + base + 2 * j) = make_float2(o[g][0][2], o[g][0][3]);
@@ -600,6 +611,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
             mma_bf16(o[g][e], pa[0][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
             mma_bf16(o[g][e], pa[1][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
           }
+        } else if (F::kLatG8) {
+          // the operands already carry their 8-channel group's scale
+#pragma unroll
+          for (int e = 0; e < 2; ++e) mma_f16(o[g][e], pa[0][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
         } else {
           // A = P scaled per token (column) by the group's scale
           uint32_t ag[4];
@@ -770,6 +785,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
 #pragma unroll
         for (int n = 0; n < 4; ++n) mma_bf16(acc[n], q.lo[g], bq[g][n][0], bq[g][n][1], acc[n]);
       }
+    } else if (F::kLatG8) {
+      // two 8-channel scale groups per 16-channel step: one m16n8k8 MMA per
+      // group (standard layout: A registers 0 / 1 and B register 0 carry
+      // channels 0-7 of the step, A registers 2 / 3 and B register 1
+      // channels 8-15) and one scale FMA per element; then each operand
+      // register is scaled by its own group's scale for PV (fp16, one
+      // rounding, as the P-side scaling of the other formats)
+      const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int si = 2 * (4 * w + g) + hh;
+          float d[4][4];
+#pragma unroll
+          for (int n = 0; n < 4; ++n) mma_f16_k8(d[n], q.hi[g][2 * hh], q.hi[g][2 * hh + 1], bq[g][n][hh], zero4);
+#pragma unroll
+          for (int n = 0; n < 4; ++n) mma_f16_k8(d[n], q.lo[g][2 * hh], q.lo[g][2 * hh + 1], bq[g][n][hh], d[n]);
+#pragma unroll
+          for (int n = 0; n < 4; ++n) {
+            float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
+            float sv = sc[si * kBlockTokens + 8 * n + r];
+            if (partial) {
+              if (8 * n + 2 * j >= nv) s2.x = 0.f;
+              if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
+              if (8 * n + r >= nv) sv = 0.f;
+            }
+            acc[n][0] = fmaf(d[n][0], s2.x, acc[n][0]);
+            acc[n][1] = fmaf(d[n][1], s2.y, acc[n][1]);
+            acc[n][2] = fmaf(d[n][2], s2.x, acc[n][2]);
+            acc[n][3] = fmaf(d[n][3], s2.y, acc[n][3]);
+            bq[g][n][hh] = h2_bits(__hmul2(bits_h2(bq[g][n][hh]), __float2half2_rn(sv)));
+          }
+        }
+      }
     } else {
       // the MMA steps of one scale group accumulate together (exact codes,
       // fp32 accumulator), then one FMA per element applies the scale
@@ -908,6 +958,7 @@ mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
   MLA_MMA_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT4_SYM)
   MLA_MMA_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT4_SYM)
   MLA_MMA_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT4_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT8_G8, MLA_FMT_INT8_SYM)
   MLA_MMA_CASE(MLA_FMT_INT8_G32, MLA_FMT_INT8_SYM)
   MLA_MMA_CASE(MLA_FMT_INT8_G64, MLA_FMT_INT8_SYM)
   MLA_MMA_CASE(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM)

@@ -55,7 +55,14 @@ def read_tokens(pool_np, layout, latent_fmt, kpe_fmt, slots):
     else:
         out["c_scale"] = fp32_field(layout.scale_off, 512 // INT8_GROUP.get(latent_fmt, 16))
         if latent_fmt in INT8_GROUP:
-            out["c_codes"] = logical.reshape(n, row).view(np.int8).copy()
+            codes = logical.reshape(n, row).view(np.int8).copy()
+            if latent_fmt == F_I8G8:         # word j of a chunk: channels 2j, 2j+1, 8+2j, 8+2j+1
+                perm = np.array([0, 1, 8, 9, 2, 3, 10, 11, 4, 5, 12, 13, 6, 7, 14, 15])
+                fixed = np.empty_like(codes)
+                for c in range(row // 16):
+                    fixed[:, 16 * c + perm] = codes[:, 16 * c:16 * c + 16]
+                codes = fixed
+            out["c_codes"] = codes
         else:
             codes = _nibbles(logical, n, nchunk)
             if latent_fmt == F_INT4:
