@@ -343,13 +343,16 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
   }
 }
 
-// grid (B, H), block 128: merge the partials of sequence b, head h.  CTAs
+// grid (B, H), block 256: merge the partials of sequence b, head h.  CTAs
 // span[2b] .. span[2b+1] wrote slots x + b.  The slots' maxima and sums are
-// read in parallel (one slot per thread), the block reduces them, and each
-// thread then accumulates 4 channels over all slots with independent loads:
-// every slot in the span was written (o finite, weight 0 for an empty one),
-// so the loads are unconditional and eight of them are in flight at a time.
+// read in parallel (one slot per thread), the block reduces them; then each
+// half of the block accumulates 4 channels per thread over every other slot
+// (a long context spreads one sequence over every SM, so there can be ~150
+// slots) and the halves are summed through shared memory.  Every slot in
+// the span was written (o finite, weight 0 for an empty one), so the loads
+// are unconditional and eight of them are in flight at a time.
 constexpr int kCombSlots = 1024;     // weights cached in shared memory
+constexpr int kCombThreads = 256;
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
 #pragma unroll
@@ -363,20 +366,22 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
   __syncthreads();
   v = red[0];
 #pragma unroll
-  for (int k = 1; k < 4; ++k) v = is_max ? fmaxf(v, red[k]) : v + red[k];
+  for (int k = 1; k < kCombThreads / 32; ++k) v = is_max ? fmaxf(v, red[k]) : v + red[k];
   return v;
 }
 
-__global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams p) {
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float sw[kCombSlots];
-  __shared__ float red[4];
+  __shared__ float red[kCombThreads / 32];
+  __shared__ float4 half1[kDc / 4];
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  const int quad = tid & (kDc / 4 - 1), part = tid / (kDc / 4);
   const int32_t* cum = p.ws.cum;
-  float4* out = reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc) + tid;
+  float4* out = reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc) + quad;
   if (cum[b] == cum[b + 1]) {
-    *out = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (part == 0) *out = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
     return;
   }
@@ -384,10 +389,10 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   const float* mp = p.ws.m + (size_t)(x0 + b) * p.H + h;
   const float* lp = p.ws.l + (size_t)(x0 + b) * p.H + h;
   float mloc = -INFINITY;
-  for (int t = tid; t < S; t += 128) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
+  for (int t = tid; t < S; t += kCombThreads) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
   const float M = block_reduce(mloc, true, red);
   float lloc = 0.f;
-  for (int t = tid; t < S; t += 128) {
+  for (int t = tid; t < S; t += kCombThreads) {
     const float m = mp[(size_t)t * p.H];
     const float w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
     if (t < kCombSlots) sw[t] = w;
@@ -395,10 +400,10 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
   }
   const float L = block_reduce(lloc, false, red);   // also orders the sw writes before the reads below
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* o4 = reinterpret_cast<const float4*>(p.ws.o + ((size_t)(x0 + b) * p.H + h) * kDc) + tid;
+  const float4* o4 = reinterpret_cast<const float4*>(p.ws.o + ((size_t)(x0 + b) * p.H + h) * kDc) + quad;
   const size_t ostride = (size_t)p.H * (kDc / 4);
 #pragma unroll 8
-  for (int t = 0; t < S; ++t) {
+  for (int t = part; t < S; t += 2) {
     float w;
     if (t < kCombSlots) {
       w = sw[t];
@@ -412,6 +417,14 @@ __global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
     acc.z = fmaf(w, v.z, acc.z);
     acc.w = fmaf(w, v.w, acc.w);
   }
+  if (part == 1) half1[quad] = acc;
+  __syncthreads();
+  if (part == 1) return;
+  const float4 a1 = half1[quad];
+  acc.x += a1.x;
+  acc.y += a1.y;
+  acc.z += a1.z;
+  acc.w += a1.w;
   if (L > 0.f) {
     const float inv = 1.f / L;
     *out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -468,7 +481,7 @@ mla_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
   mla_status st = force_ref ? MLA_ERR_UNSUPPORTED : launch_decode_mma(p, stream);
   if (st == MLA_ERR_UNSUPPORTED) st = launch_decode_ref(p, stream);
   if (st != MLA_OK) return st;
-  return cuda_status(launch_pdl(combine_kernel, dim3(p.B, p.H), dim3(128), 0, stream, p));
+  return cuda_status(launch_pdl(combine_kernel, dim3(p.B, p.H), dim3(kCombThreads), 0, stream, p));
 }
 
 }  // namespace mla
