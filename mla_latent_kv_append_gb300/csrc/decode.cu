@@ -343,16 +343,17 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
   }
 }
 
-// grid (B, H), block 256: merge the partials of sequence b, head h.  CTAs
+// grid (B, H), block 512: merge the partials of sequence b, head h.  CTAs
 // span[2b] .. span[2b+1] wrote slots x + b.  The slots' maxima and sums are
 // read in parallel (one slot per thread), the block reduces them; then each
-// half of the block accumulates 4 channels per thread over every other slot
-// (a long context spreads one sequence over every SM, so there can be ~150
-// slots) and the halves are summed through shared memory.  Every slot in
+// quarter of the block accumulates 4 channels per thread over every fourth
+// slot (a long context spreads one sequence over every SM, so there can be
+// ~150 slots) and the quarters are summed through shared memory.  Every slot in
 // the span was written (o finite, weight 0 for an empty one), so the loads
 // are unconditional and eight of them are in flight at a time.
 constexpr int kCombSlots = 1024;     // weights cached in shared memory
-constexpr int kCombThreads = 256;
+constexpr int kCombThreads = 512;
+constexpr int kCombParts = kCombThreads / (kDc / 4);
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
 #pragma unroll
@@ -375,7 +376,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams p) {
   pdl_wait();
   __shared__ float sw[kCombSlots];
   __shared__ float red[kCombThreads / 32];
-  __shared__ float4 half1[kDc / 4];
+  __shared__ float4 parts[kCombParts - 1][kDc / 4];
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int quad = tid & (kDc / 4 - 1), part = tid / (kDc / 4);
   const int32_t* cum = p.ws.cum;
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams p) {
   const float4* o4 = reinterpret_cast<const float4*>(p.ws.o + ((size_t)(x0 + b) * p.H + h) * kDc) + quad;
   const size_t ostride = (size_t)p.H * (kDc / 4);
 #pragma unroll 8
-  for (int t = part; t < S; t += 2) {
+  for (int t = part; t < S; t += kCombParts) {
     float w;
     if (t < kCombSlots) {
       w = sw[t];
@@ -417,14 +418,17 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams p) {
     acc.z = fmaf(w, v.z, acc.z);
     acc.w = fmaf(w, v.w, acc.w);
   }
-  if (part == 1) half1[quad] = acc;
+  if (part > 0) parts[part - 1][quad] = acc;
   __syncthreads();
-  if (part == 1) return;
-  const float4 a1 = half1[quad];
-  acc.x += a1.x;
-  acc.y += a1.y;
-  acc.z += a1.z;
-  acc.w += a1.w;
+  if (part > 0) return;
+#pragma unroll
+  for (int k = 0; k < kCombParts - 1; ++k) {
+    const float4 a1 = parts[k][quad];
+    acc.x += a1.x;
+    acc.y += a1.y;
+    acc.z += a1.z;
+    acc.w += a1.w;
+  }
   if (L > 0.f) {
     const float inv = 1.f / L;
     *out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
