@@ -343,16 +343,16 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
   }
 }
 
-// grid (B, H), block 512: merge the partials of sequence b, head h.  CTAs
+// grid (B, H), block 1024: merge the partials of sequence b, head h.  CTAs
 // span[2b] .. span[2b+1] wrote slots x + b.  The slots' maxima and sums are
 // read in parallel (one slot per thread), the block reduces them; then each
-// quarter of the block accumulates 4 channels per thread over every fourth
+// eighth of the block accumulates 4 channels per thread over every eighth
 // slot (a long context spreads one sequence over every SM, so there can be
-// ~150 slots) and the quarters are summed through shared memory.  Every slot in
+// ~150 slots) and the eighths are summed through shared memory.  Every slot in
 // the span was written (o finite, weight 0 for an empty one), so the loads
 // are unconditional and eight of them are in flight at a time.
 constexpr int kCombSlots = 1024;     // weights cached in shared memory
-constexpr int kCombThreads = 512;
+constexpr int kCombThreads = 1024;
 constexpr int kCombParts = kCombThreads / (kDc / 4);
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
