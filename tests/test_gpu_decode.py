@@ -100,3 +100,19 @@ def test_bad_page_and_bad_length_are_flagged_not_faulted():
     ol = step.o_lat.cpu().numpy()
     assert np.all(np.isfinite(ol))
     assert np.all(ol[1] == 0) and np.all(np.isneginf(step.lse[0, 1].cpu().numpy()))
+
+
+def test_most_heads():
+    """128 heads (eight head tiles), the largest head count the ABI takes."""
+    wl = Workload(1, 128, [300, 65, 1], mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, seed=82)
+    run_and_check(wl)
+
+
+def test_largest_batch():
+    """B = 4096 (the ABI's limit) short sequences: the chunk prefix sums fill
+    the shared-memory reserve; sampled sequences against the oracle."""
+    rng = np.random.default_rng(83)
+    lens = [int(t) for t in rng.integers(0, 80, 4096)]
+    wl = Workload(1, 16, lens, mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM, seed=83)
+    seqs = sorted(set([0, 4095] + [int(b) for b in rng.integers(0, 4096, 48)]))
+    run_and_check(wl, seqs=seqs)
