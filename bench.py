@@ -415,11 +415,11 @@ def run_ours(args, cfg, rank, world, local_rank):
                "frac": pre_bytes / (pre_ms * 1e-3) / 1e9 / peak0}
 
     # ---- end to end through the public API with host buffers
-    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t.cpu())
-    host_in = [(pin(wl.c_new[l]), pin(wl.kpe_new[l]), pin(wl.q_nope[l]), pin(wl.q_pe[l])) for l in range(wl.L)]
-    host_pre = [(pin(wl.c_pre[l]), pin(wl.kpe_pre[l])) for l in range(wl.L)] if wl.prefill else []
+    # every step's inputs of all layers live in one device buffer
+    # (wl.step_inputs): one pinned host buffer, one copy in, one copy out
+    host_in = torch.empty(wl.step_inputs.shape, dtype=torch.uint8, pin_memory=True).copy_(wl.step_inputs.cpu())
     host_out = torch.empty(step.o.shape, dtype=step.o.dtype, pin_memory=True)
-    h2d = sum(sum(t.numel() * t.element_size() for t in x) for x in host_in + host_pre)
+    h2d = host_in.numel()
     d2h = host_out.numel() * host_out.element_size()
     e2e_steps = max(3, min(args.steps, 50))
     done = torch.cuda.Event()
@@ -428,14 +428,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         for _ in range(e2e_steps):
-            for l, (c, k, qn, qp) in enumerate(host_in):
-                wl.c_new[l].copy_(c, non_blocking=True)
-                wl.kpe_new[l].copy_(k, non_blocking=True)
-                wl.q_nope[l].copy_(qn, non_blocking=True)
-                wl.q_pe[l].copy_(qp, non_blocking=True)
-            for l, (c, k) in enumerate(host_pre):
-                wl.c_pre[l].copy_(c, non_blocking=True)
-                wl.kpe_pre[l].copy_(k, non_blocking=True)
+            wl.step_inputs.copy_(host_in, non_blocking=True)
             graph.replay()
             host_out.copy_(step.o, non_blocking=True)
             done.record(stream)

@@ -80,8 +80,29 @@ class Workload:
                 sd.kpe_into(kk, seed, l, self.B, 0, self.rope)
                 self.c_pre.append(c)
                 self.kpe_pre.append(kk)
+        self._pack_step_inputs()
         if fill:
             self.fill(fill_chunk)
+
+    def _pack_step_inputs(self):
+        """Place every per-step input (new tokens, queries, prefill tokens of
+        all layers) in one device buffer, so that a host copy of a step's
+        inputs is a single transfer; the per-layer tensors become views."""
+        groups = [self.c_new, self.kpe_new, self.q_nope, self.q_pe, self.c_pre, self.kpe_pre]
+        total = 0
+        for lst in groups:
+            for t in lst:
+                total = (total + 255) // 256 * 256 + t.numel() * t.element_size()
+        self.step_inputs = torch.empty(max(1, total), dtype=torch.uint8, device=self.device)
+        off = 0
+        for lst in groups:
+            for i, t in enumerate(lst):
+                off = (off + 255) // 256 * 256
+                n = t.numel() * t.element_size()
+                v = self.step_inputs[off:off + n].view(t.dtype).view(t.shape)
+                v.copy_(t)
+                lst[i] = v
+                off += n
 
     def slot_of(self, b, t):
         return int(self.block_table_host[b, t // 64]) * 64 + t % 64
