@@ -9,30 +9,30 @@
 // Technical Report" §2.1: attention straight from the cached latent; juejin
 // tutorial "步骤2" for the absorbed up-projections).
 //
-// Structure (one CTA per SM, 8 warps):
-//  * Thread 0 streams 32-token blocks (one contiguous bulk copy each,
-//    cp.async.bulk into a ring of shared-memory stages, mbarrier-signalled).
-//    A stage is refilled as soon as every warp has passed the score-exchange
-//    barrier of the chunk it held, which orders all reads of it before the
-//    refill; no separate producer warp is needed, which leaves each thread
-//    the registers of two warps per scheduler.
-//  * Consumer warp w owns latent groups 4w..4w+3 (64 channels) and k_pe
-//    group w.  Each code byte is read from shared memory once (ldmatrix) and
-//    turned into exact fp16 integers; the same registers serve QK^T and,
-//    after dequantization and a movmatrix transpose, PV.
+// Structure (one CTA per SM, 12 warps, warp-specialized):
+//  * Compute warps 0..7: warp w owns latent groups 4w..4w+3 (64 channels)
+//    and k_pe group w.  Each code byte is read from shared memory once
+//    (ldmatrix) and turned into exact fp16 integers; the same registers serve
+//    QK^T and, after a movmatrix transpose, PV.
 //  * QK^T per 16-channel group: mma.m16n8k16 (M = 16 heads, N = 8 tokens,
 //    K = the group's 16 channels) of q_lat split into fp16 hi + lo against
 //    the exact integer codes (INT4: code - zero, formed exactly in fp16),
-//    then one fp32 FMA per element applies the group's per-token scale.  This keeps every product exact, which the
-//    2e-3 bound needs: scores here have a spread of ~10, so a rounding of the
-//    latent or the query to 11 bits would already cost ~1e-3.
-//  * The partial scores of the 8 warps are summed through shared memory by
-//    256 threads (16 per head row), which also run the online softmax (max /
-//    sum with warp shuffles over the row's 16 threads) and publish P in fp16.
-//    This runs one chunk behind the QK^T work (software pipeline, one
-//    barrier per chunk), so the two overlap.
+//    then one fp32 FMA per element applies the group's per-token scale.
+//    This keeps every product exact, which the 2e-3 bound needs: scores here
+//    have a spread of ~10, so a rounding of the latent or the query to 11
+//    bits would already cost ~1e-3.
+//  * Softmax warpgroup (warps 8..11, 128 threads, 8 per head row): sums the
+//    8 compute warps' partial scores of a chunk through shared memory, runs
+//    the online softmax (max / sum by shuffles over the row's 8 threads) and
+//    publishes P in fp16 (bf16 hi + lo for a bf16 latent) with the rescale
+//    factor.  Its first thread is the loader: it streams 32-token blocks
+//    (one contiguous cp.async.bulk each, mbarrier-signalled) into a ring of
+//    shared-memory stages and refills a stage once every compute warp has
+//    handed in the chunk it held.
 //  * PV: o[16 heads][the warp's 64 channels] += (P scaled per token by the
-//    group's scale) x (the same exact codes, transposed with movmatrix).
+//    group's scale) x (the same exact codes, transposed with movmatrix),
+//    one chunk behind QK^T, so a compute warp's QK^T of chunk i overlaps
+//    the softmax of chunk i - 1.
 //  * bf16 latent: q_lat is split into bf16 hi + lo against the exact bf16
 //    values, one accumulator over all groups, P split into bf16 hi + lo.
 #include <cuda_fp16.h>
@@ -44,7 +44,7 @@ namespace mla {
 
 namespace {
 
-constexpr int kCW = 8;                         // warps (all consume; thread 0 also loads)
+constexpr int kCW = 8;                         // compute warps
 constexpr int kThreads = kCW * 32;
 constexpr int kHT = 16;                        // heads per CTA
 constexpr int kPStride = 40;                   // row stride (16-bit elements) of the P tile: 80 B, conflict-free ldmatrix
@@ -129,10 +129,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
-}
-
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;\n" ::"n"(kCW * 32) : "memory");
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -310,16 +306,15 @@ __device__ __forceinline__ float load_query_raw(const DecodeParams& p, int b, in
   const uint16_t* qp0 = p.q_pe + ((size_t)b * p.H + h0 + r) * kDr;
   const uint16_t* qp1 = qp0 + 8 * kDr;
   if (F::kKpeBf16) {
-    // warps 0..3: k16 chunk w (channels 16w..16w+15), standard layout
-    const bool act = w < 4;
+    // warp w: k16 chunk w % 4 (channels 16(w%4) .. +15), standard layout
     const int c0 = 16 * (w & 3);
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const uint16_t* qp = rr ? qp1 : qp0;
-      q.kx[rr][0] = act ? bf16f(qp[c0 + 2 * j]) : 0.f;
-      q.kx[rr][1] = act ? bf16f(qp[c0 + 2 * j + 1]) : 0.f;
-      q.kx[rr][2] = act ? bf16f(qp[c0 + 8 + 2 * j]) : 0.f;
-      q.kx[rr][3] = act ? bf16f(qp[c0 + 8 + 2 * j + 1]) : 0.f;
+      q.kx[rr][0] = bf16f(qp[c0 + 2 * j]);
+      q.kx[rr][1] = bf16f(qp[c0 + 2 * j + 1]);
+      q.kx[rr][2] = bf16f(qp[c0 + 8 + 2 * j]);
+      q.kx[rr][3] = bf16f(qp[c0 + 8 + 2 * j + 1]);
     }
   } else {
     // warp w: k_pe group w inside 16-channel chunk w/2; thread j feeds channels
@@ -383,16 +378,297 @@ __device__ __forceinline__ void finish_query(const QueryRaw& raw, float up, Quer
   }
 }
 
+// Step A of one chunk for warp w (latent groups 4w .. 4w+3): B operands
+// (exact codes, or code - zero) into bq, the fp16 PV scale pairs into s2h,
+// and the warp's partial scores (QK^T over its channels plus its k_pe part)
+// into acc [ntile][C fragment].  st: the chunk's block in shared memory;
+// nv: its valid tokens.
+template <int LF, int KF>
+__device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int lane, const Query& q,
+                                         uint32_t (&bq)[4][4][2], uint32_t (&s2h)[4][4], float (&acc)[4][4]) {
+  using F = Fmt<LF, KF>;
+  const int r = lane >> 2, j = lane & 3;
+  const bool partial = nv < kChunk;     // includes nv == 0 (no data: everything is masked)
+  const uint32_t st_a = smem_u32(st);
+  const float* sc = reinterpret_cast<const float*>(st + F::kScaleOff);
+  // ---- step A: B operands (exact codes, or code - zero) and QK^T of chunk i
+  if (F::kLatBf16) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int ch = 2 * (4 * w + g);
+      uint32_t t0, t1, t2, t3;
+      ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(ch, lane) * 16, t0, t1, t2, t3);
+      bq[g][0][0] = t0; bq[g][1][0] = t1; bq[g][2][0] = t2; bq[g][3][0] = t3;
+      ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(ch + 1, lane) * 16, t0, t1, t2, t3);
+      bq[g][0][1] = t0; bq[g][1][1] = t1; bq[g][2][1] = t2; bq[g][3][1] = t3;
+    }
+    if (partial) {       // PV reads these values: zero the tokens past the end
+#pragma unroll
+      for (int n = 0; n < 4; ++n)
+        if (8 * n + r >= nv)
+#pragma unroll
+          for (int g = 0; g < 4; ++g) bq[g][n][0] = bq[g][n][1] = 0u;
+    }
+  } else if (F::kLatInt4) {
+    const float* zp = reinterpret_cast<const float*>(st + F::kZeroOff);
+    const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f), km64 = __floats2half2_rn(-64.f, -64.f);
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t t[4];
+      ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(2 * w + cc, lane) * 16, t[0], t[1], t[2], t[3]);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        __half2 zz;
+        if (F::kLatSym4) {
+          zz = __floats2half2_rn(8.f, 8.f);                         // nibble = code + 8
+        } else {
+          // zero-points of this thread's B token (8n + r) for groups A and B of the chunk
+          float za = zp[(4 * w + 2 * cc) * kBlockTokens + 8 * n + r];
+          float zb = zp[(4 * w + 2 * cc + 1) * kBlockTokens + 8 * n + r];
+          if (partial && 8 * n + r >= nv) za = zb = 0.f;
+          zz = __floats2half2_rn(za, zb);                            // exact (integer zero-points)
+        }
+        i4x8_to_f16(t[n], __hadd2(zz, k1024), __hsub2(km64, zz), bq[2 * cc][n][0], bq[2 * cc][n][1],
+                    bq[2 * cc + 1][n][0], bq[2 * cc + 1][n][1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint32_t t[4];
+      ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(4 * w + g, lane) * 16, t[0], t[1], t[2], t[3]);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) i8x4_to_f16(t[n], bq[g][n][0], bq[g][n][1]);
+    }
+  }
+  // bf16 k_pe: warp w takes 16-channel chunk w % 4 and n-tiles 2 (w / 4),
+  // 2 (w / 4) + 1 (bk[0..1]); quantized k_pe: group w, all four n-tiles
+  uint32_t bk[4][2];
+  if (F::kKpeBf16) {
+    const int nh = w >> 2, kc = w & 3;
+    uint32_t t[4], u[4];
+    ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(2 * kc, lane, KF) * 16, t[0], t[1], t[2], t[3]);
+    ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(2 * kc + 1, lane, KF) * 16, u[0], u[1], u[2], u[3]);
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+      bk[n][0] = nh ? t[n + 2] : t[n];
+      bk[n][1] = nh ? u[n + 2] : u[n];
+    }
+  } else if (F::kKpeInt4) {
+    // warp w: k_pe group w = channels 8w .. 8w+7, in 32-channel chunk w / 4,
+    // 16-channel half (w / 2) % 2; the MMA takes the half's 16 channels
+    // (its A fragment is zero outside the group, as for INT8 k_pe)
+    uint32_t t[4];
+    ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(w >> 2, lane, KF) * 16, t[0], t[1], t[2], t[3]);
+    const __half2 zo = __floats2half2_rn(1032.f, 1032.f), zc = __floats2half2_rn(-72.f, -72.f);
+    const bool hb = (w >> 1) & 1;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      uint32_t a0, a1, b0, b1;
+      i4x8_to_f16(t[n], zo, zc, a0, a1, b0, b1);
+      bk[n][0] = hb ? b0 : a0;
+      bk[n][1] = hb ? b1 : a1;
+    }
+  } else {
+    uint32_t t[4];
+    ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(w >> 1, lane, KF) * 16, t[0], t[1], t[2], t[3]);
+#pragma unroll
+    for (int n = 0; n < 4; ++n) i8x4_to_f16(t[n], bk[n][0], bk[n][1]);
+  }
+
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
+  if (F::kLatBf16) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+#pragma unroll
+      for (int n = 0; n < 4; ++n) mma_bf16(acc[n], q.hi[g], bq[g][n][0], bq[g][n][1], acc[n]);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) mma_bf16(acc[n], q.lo[g], bq[g][n][0], bq[g][n][1], acc[n]);
+    }
+  } else if (F::kLatG8) {
+    // two 8-channel scale groups per 16-channel step: one m16n8k8 MMA per
+    // group (standard layout: A registers 0 / 1 and B register 0 carry
+    // channels 0-7 of the step, A registers 2 / 3 and B register 1
+    // channels 8-15) and one scale FMA per element; then each operand
+    // register is scaled by its own group's scale for PV (fp16, one
+    // rounding, as the P-side scaling of the other formats)
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int si = 2 * (4 * w + g) + hh;
+        float d[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) mma_f16_k8(d[n], q.hi[g][2 * hh], q.hi[g][2 * hh + 1], bq[g][n][hh], zero4);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) mma_f16_k8(d[n], q.lo[g][2 * hh], q.lo[g][2 * hh + 1], bq[g][n][hh], d[n]);
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
+          float sv = sc[si * kBlockTokens + 8 * n + r];
+          if (partial) {
+            if (8 * n + 2 * j >= nv) s2.x = 0.f;
+            if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
+            if (8 * n + r >= nv) sv = 0.f;
+          }
+          acc[n][0] = fmaf(d[n][0], s2.x, acc[n][0]);
+          acc[n][1] = fmaf(d[n][1], s2.y, acc[n][1]);
+          acc[n][2] = fmaf(d[n][2], s2.x, acc[n][2]);
+          acc[n][3] = fmaf(d[n][3], s2.y, acc[n][3]);
+          bq[g][n][hh] = h2_bits(__hmul2(bits_h2(bq[g][n][hh]), __float2half2_rn(sv)));
+        }
+      }
+    }
+  } else {
+    // the MMA steps of one scale group accumulate together (exact codes,
+    // fp32 accumulator), then one FMA per element applies the scale
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    float d[4][4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const bool first = g % F::kSPG == 0, last = (g + 1) % F::kSPG == 0 || g == 3;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) mma_f16(d[n], q.hi[g], bq[g][n][0], bq[g][n][1], first ? zero4 : d[n]);
+#pragma unroll
+      for (int n = 0; n < 4; ++n) mma_f16(d[n], q.lo[g], bq[g][n][0], bq[g][n][1], d[n]);
+      if (last) {
+        const int si = (4 * w + g) / F::kSPG;
+#pragma unroll
+        for (int n = 0; n < 4; ++n) {
+          float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
+          if (partial) {
+            if (8 * n + 2 * j >= nv) s2.x = 0.f;
+            if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
+          }
+          acc[n][0] = fmaf(d[n][0], s2.x, acc[n][0]);
+          acc[n][1] = fmaf(d[n][1], s2.y, acc[n][1]);
+          acc[n][2] = fmaf(d[n][2], s2.x, acc[n][2]);
+          acc[n][3] = fmaf(d[n][3], s2.y, acc[n][3]);
+          const uint32_t sh = pack_f16(s2.x, s2.y);
+#pragma unroll
+          for (int g2 = 0; g2 < 4; ++g2)
+            if (g2 <= g && g2 > g - F::kSPG) s2h[g2][n] = sh;
+        }
+      }
+    }
+  }
+  if (F::kKpeBf16) {
+    if (w >> 2) {
+      mma_bf16(acc[2], q.ka, bk[0][0], bk[0][1], acc[2]);
+      mma_bf16(acc[3], q.ka, bk[1][0], bk[1][1], acc[3]);
+    } else {
+      mma_bf16(acc[0], q.ka, bk[0][0], bk[0][1], acc[0]);
+      mma_bf16(acc[1], q.ka, bk[1][0], bk[1][1], acc[1]);
+    }
+  } else {
+    const float* ks = reinterpret_cast<const float*>(st + F::kKScaleOff);
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      const float2 s2 = *reinterpret_cast<const float2*>(ks + w * kBlockTokens + 8 * n + 2 * j);
+      float d[4];
+      mma_f16(d, q.ka, bk[n][0], bk[n][1], zero4);
+      acc[n][0] = fmaf(d[0], s2.x, acc[n][0]);
+      acc[n][1] = fmaf(d[1], s2.y, acc[n][1]);
+      acc[n][2] = fmaf(d[2], s2.x, acc[n][2]);
+      acc[n][3] = fmaf(d[3], s2.y, acc[n][3]);
+    }
+  }
+}
+
+// Step C of one chunk for warp w: rescale o by the chunk's alpha and add
+// P V with the operands bqv / scales s2v kept from its step A.  alpha_s:
+// [2][16]; ptab: the P tiles [2 buf][hi, lo][16][kPStride].
+template <int LF, int KF>
+__device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha_s, const uint16_t* ptab, int buf,
+                                         const uint32_t (&bqv)[4][4][2], const uint32_t (&s2v)[4][4], int lane) {
+  using F = Fmt<LF, KF>;
+  const int r = lane >> 2;
+    {
+    const float al0 = alpha_s[buf * kHT + r], al1 = alpha_s[buf * kHT + r + 8];
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          o[g][e][0] *= al0;
+          o[g][e][1] *= al0;
+          o[g][e][2] *= al1;
+          o[g][e][3] *= al1;
+        }
+    }
+  }
+  uint32_t pa[2][2][4];      // [hi/lo][k step][reg]
+  {
+    const uint32_t pbase = smem_u32(ptab) + (2 * buf) * kHT * kPStride * 2 +
+                           ((lane & 7) + 8 * ((lane >> 3) & 1)) * kPStride * 2 + 8 * (lane >> 4) * 2;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      ldsm_x4(pbase + 32 * ks, pa[0][ks][0], pa[0][ks][1], pa[0][ks][2], pa[0][ks][3]);
+      if (F::kLatBf16)
+        ldsm_x4(pbase + kHT * kPStride * 2 + 32 * ks, pa[1][ks][0], pa[1][ks][1], pa[1][ks][2], pa[1][ks][3]);
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    uint32_t vt[4][2];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      vt[n][0] = movt(bqv[g][n][0]);
+      vt[n][1] = movt(bqv[g][n][1]);
+    }
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      if (F::kLatBf16) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          mma_bf16(o[g][e], pa[0][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
+          mma_bf16(o[g][e], pa[1][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
+        }
+      } else if (F::kLatG8) {
+        // the operands already carry their 8-channel group's scale
+#pragma unroll
+        for (int e = 0; e < 2; ++e) mma_f16(o[g][e], pa[0][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
+      } else {
+        // A = P scaled per token (column) by the group's scale
+        uint32_t ag[4];
+        ag[0] = h2_bits(__hmul2(bits_h2(pa[0][ks][0]), bits_h2(s2v[g][2 * ks])));
+        ag[1] = h2_bits(__hmul2(bits_h2(pa[0][ks][1]), bits_h2(s2v[g][2 * ks])));
+        ag[2] = h2_bits(__hmul2(bits_h2(pa[0][ks][2]), bits_h2(s2v[g][2 * ks + 1])));
+        ag[3] = h2_bits(__hmul2(bits_h2(pa[0][ks][3]), bits_h2(s2v[g][2 * ks + 1])));
+#pragma unroll
+        for (int e = 0; e < 2; ++e) mma_f16(o[g][e], ag, vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-// Per-chunk pipeline with one barrier per chunk: iteration k computes the
-// partial scores of chunk k (QK^T, step A) while the reduction threads run the
-// softmax of chunk k-1 (step B); after the barrier every warp accumulates
-// PV of chunk k-1 (step C) from the code registers it kept from A(k-1).  The
-// score-exchange and P tiles are double-buffered by chunk parity.
+// Warps 0..7 compute QK^T (step A) and PV (step C) of their latent groups;
+// warpgroup 2 (warps 8..11) runs the online softmax (step B) of every chunk
+// and the loader.  Hand-offs go through mbarriers with bounded waits:
+//   bx[i & 1]: the 256 compute threads have written chunk i's partial
+//              scores (and thread 0 its valid-token count and score scale);
+//              the stage of chunk i is free again;
+//   bp[i & 1]: the 128 softmax threads have written chunk i's P and alpha.
+// A compute warp therefore runs A(i), arrives on bx, waits for bp of chunk
+// i - 1 and runs C(i - 1), while the softmax warpgroup works on chunk i - 1
+// or i.  Registers move to the compute warps with setmaxnreg (232 each;
+// 40 for the softmax warpgroup; the 384-thread block launches with 168).
+constexpr int kWsThreads = kThreads + 128;
+constexpr int kWsExtra = 5 * 8 + 4 * 4;     // bx[2], bp[2], qa; nvq[2], cwq[2]
+
+__device__ __forceinline__ void ws_regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory"); }
+__device__ __forceinline__ void ws_regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory"); }
+
 template <int LF, int KF>
-__global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams p) {
   using F = Fmt<LF, KF>;
   pdl_launch_dependents();
   pdl_wait();
@@ -403,14 +679,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
   float* alpha_s = reinterpret_cast<float*>(ptab + 4 * kHT * kPStride);        // [2][16]
   float* amax_s = alpha_s + 2 * kHT;                                           // [8]
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(amax_s + kCW);
-  int32_t* meta = reinterpret_cast<int32_t*>(full_bar + F::kStages);
-  int32_t* cum = meta + F::kStages;
+  uint64_t* bx = full_bar + F::kStages;                                        // [2]
+  uint64_t* bp = bx + 2;                                                       // [2]
+  uint64_t* qa = bp + 2;                                                       // [1]
+  int32_t* meta = reinterpret_cast<int32_t*>(qa + 1);
+  int32_t* nvq = meta + F::kStages;                                            // [2]
+  float* cwq = reinterpret_cast<float*>(nvq + 2);                              // [2]
+  int32_t* cum = reinterpret_cast<int32_t*>(cwq + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int x = blockIdx.x, G = gridDim.x, h0 = blockIdx.y * kHT;
   const bool lead = (blockIdx.x == 0 && blockIdx.y == 0);
 
-  // ---- chunk prefix sums (warp 0) and barrier init (thread 32)
   if (warp == 0) {
     int carry = 0;
     for (int base = 0; base < p.B; base += 32) {
@@ -428,87 +708,159 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
     if (lane == 0) cum[0] = 0;
   } else if (tid == 32) {
     for (int s = 0; s < F::kStages; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(smem_u32(&bx[k]), kThreads);
+      mbar_init(smem_u32(&bp[k]), 128);
+    }
+    mbar_init(smem_u32(qa), kThreads);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
   if (lead)
-    for (int i = tid; i <= p.B; i += kThreads) p.ws.cum[i] = cum[i];
+    for (int i = tid; i <= p.B; i += kWsThreads) p.ws.cum[i] = cum[i];
 
-  // chunk indices fit in 32 bits: the host checks B x max_pages x 2 < 2^31
   const int C = cum[p.B];
-  const int Ge = G < C ? G : C;          // no empty ranges
+  const int Ge = G < C ? G : C;
   if (x >= Ge) return;
   const int c_lo = (int)range_lo(C, x, Ge), c_hi = (int)range_lo(C, x + 1, Ge);
 
-  // ---- loader state (thread 0 only).  plan() looks up the next chunk's page
-  // early (its global load then overlaps the QK^T work); commit(s) starts the
-  // copy into stage s.  Invalid pages complete the stage's phase with no data
-  // (nv = 0).
-  int ld_c = c_lo;
-  int ld_b = 0, ld_len = 0, pl_page = -1, pl_t0 = 0;
-  bool pl_ready = false;
-  if (tid == 0) {
-    ld_b = seq_of_chunk(cum, p.B, c_lo);
-    ld_len = checked_len(p, ld_b, false);
-  }
-  auto plan = [&]() {
-    if (pl_ready || ld_c >= c_hi) return;
-    while (cum[ld_b + 1] <= ld_c) ld_len = checked_len(p, ++ld_b, false);
-    pl_t0 = (ld_c - cum[ld_b]) * kChunk;
-    pl_page = p.block_table[(size_t)ld_b * p.max_pages + (pl_t0 >> 6)];
-    pl_ready = true;
-  };
-  auto commit = [&](int s) {
-    plan();
-    if (!pl_ready) return;
-    int nv = ld_len - pl_t0 < kChunk ? ld_len - pl_t0 : kChunk;
-    if (pl_page < 0 || pl_page >= p.num_pages) {
-      set_err(p.dev_err, MLA_DEVERR_PAGE);
-      nv = 0;
+  if (warp >= kCW) {
+    // ======================= softmax / loader warpgroup =======================
+    ws_regs_dec();
+    const int t = tid - kThreads;              // 0..127: row hr, tokens 4 tq .. 4 tq + 3
+    const int hr = t >> 3, tq = t & 7;
+    int ld_c = c_lo, ld_b = 0, ld_len = 0, pl_page = -1, pl_t0 = 0;
+    bool pl_ready = false;
+    if (t == 0) {
+      ld_b = seq_of_chunk(cum, p.B, c_lo);
+      ld_len = checked_len(p, ld_b, false);
     }
-    meta[s] = nv;
-    const uint32_t fb = smem_u32(&full_bar[s]);
-    if (nv > 0) {
-      mbar_expect_tx(fb, F::kBlock);
-      bulk_g2s(smem_u32(stages + s * F::kBlock),
-               p.pool + (int64_t)pl_page * p.L.page_bytes + ((pl_t0 >> 5) & 1) * p.L.block_bytes, F::kBlock, fb);
-    } else {
-      mbar_arrive(fb);
-    }
-    pl_ready = false;
-    ++ld_c;
-  };
-  if (tid == 0)
-    for (int s = 0; s < F::kStages; ++s) commit(s);
+    auto plan = [&]() {
+      if (pl_ready || ld_c >= c_hi) return;
+      while (cum[ld_b + 1] <= ld_c) ld_len = checked_len(p, ++ld_b, false);
+      pl_t0 = (ld_c - cum[ld_b]) * kChunk;
+      pl_page = p.block_table[(size_t)ld_b * p.max_pages + (pl_t0 >> 6)];
+      pl_ready = true;
+    };
+    auto commit = [&](int s) {
+      plan();
+      if (!pl_ready) return;
+      int nv = ld_len - pl_t0 < kChunk ? ld_len - pl_t0 : kChunk;
+      if (pl_page < 0 || pl_page >= p.num_pages) {
+        set_err(p.dev_err, MLA_DEVERR_PAGE);
+        nv = 0;
+      }
+      meta[s] = nv;
+      const uint32_t fb = smem_u32(&full_bar[s]);
+      if (nv > 0) {
+        mbar_expect_tx(fb, F::kBlock);
+        bulk_g2s(smem_u32(stages + s * F::kBlock),
+                 p.pool + (int64_t)pl_page * p.L.page_bytes + ((pl_t0 >> 5) & 1) * p.L.block_bytes, F::kBlock, fb);
+      } else {
+        mbar_arrive(fb);
+      }
+      pl_ready = false;
+      ++ld_c;
+    };
+    if (t == 0)
+      for (int s = 0; s < F::kStages; ++s) commit(s);
 
-  // =========================== compute ===========================
-  // Warp w: latent groups 4w..4w+3.  Reduction / softmax role: thread T owns
-  // row hr = T / 16 and tokens 2 (T % 16), +1 of each chunk.
+    float m_row = -INFINITY, l_row = 0.f;
+    int b = -1, s = 0;
+    bool dead = false;
+    auto flush_ml = [&](int bb) {
+      if (tq == 0) {
+        const size_t slot = (size_t)x + bb;
+        p.ws.m[slot * p.H + h0 + hr] = m_row;
+        p.ws.l[slot * p.H + h0 + hr] = l_row;
+      }
+    };
+    for (int c = c_lo, i = 0; c < c_hi; ++c, ++i) {
+      int nb = b < 0 ? seq_of_chunk(cum, p.B, c) : b;
+      while (cum[nb + 1] <= c) ++nb;
+      if (nb != b) {
+        if (b >= 0) flush_ml(b);
+        b = nb;
+        m_row = -INFINITY;
+        l_row = 0.f;
+      }
+      if (t == 0) plan();
+      if (!mbar_wait(smem_u32(&bx[i & 1]), (uint32_t)((i >> 1) & 1))) {
+        set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+        dead = true;
+        break;
+      }
+      if (t == 0) commit(s);                   // every compute warp is past chunk i's stage
+      const int buf = i & 1, nv = nvq[buf];
+      const float cw = cwq[buf];
+      // sum the 8 warps' partial scores of 4 tokens of row hr
+      const float4* xp = reinterpret_cast<const float4*>(xpart + ((size_t)buf * kCW * kHT + hr) * kXStride) + tq;
+      float4 sm = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int ww = 0; ww < kCW; ++ww) {
+        const float4 v = xp[ww * kHT * kXStride / 2];
+        sm.x += v.x;
+        sm.y += v.y;
+        sm.z += v.z;
+        sm.w += v.w;
+      }
+      float xv[4] = {sm.x * cw, sm.y * cw, sm.z * cw, sm.w * cw};
+      if (nv < kChunk) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (4 * tq + k >= nv) xv[k] = -INFINITY;
+      }
+      float mx = fmaxf(fmaxf(xv[0], xv[1]), fmaxf(xv[2], xv[3]));
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m_row, mx);
+      const float al = mn == -INFINITY ? 1.f : ex2(m_row - mn);
+      const float sub = mn == -INFINITY ? 0.f : mn;
+      float pv[4], ps = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        pv[k] = ex2(xv[k] - sub);
+        ps += pv[k];
+      }
+#pragma unroll
+      for (int off = 1; off < 8; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+      l_row = l_row * al + ps;
+      m_row = mn;
+      uint2* prow = reinterpret_cast<uint2*>(ptab + ((2 * buf) * kHT + hr) * kPStride) + tq;
+      if (F::kLatBf16) {
+        uint32_t h0w, l0w, h1w, l1w;
+        split_bf16(pv[0], pv[1], h0w, l0w);
+        split_bf16(pv[2], pv[3], h1w, l1w);
+        prow[0] = make_uint2(h0w, h1w);
+        prow[kHT * kPStride / 4] = make_uint2(l0w, l1w);
+      } else {
+        prow[0] = make_uint2(pack_f16(pv[0], pv[1]), pack_f16(pv[2], pv[3]));
+      }
+      if (tq == 0) alpha_s[buf * kHT + hr] = al;
+      mbar_arrive(smem_u32(&bp[buf]));
+      if (++s == F::kStages) s = 0;
+    }
+    if (!dead && b >= 0) flush_ml(b);
+    return;
+  }
+
+  // ============================= compute warps =============================
+  ws_regs_inc();
   const int w = warp, r = lane >> 2, j = lane & 3;
-  const int hr = tid >> 4, tp = tid & 15;
   Query q;
-  float cw = 0.f;                  // softmax_scale * log2 e * 2^-e
+  float cw = 0.f;
   float o[4][2][4];
-  float m_row = -INFINITY, l_row = 0.f;
-  // Register sets of two consecutive chunks (the loop is unrolled by two and
-  // alternates them, so the set of chunk i-1 is never copied)
   ChunkRegs ra, rb;
-  int nv_prev = 0;
   bool pending = false;
-  int b = -1, s = 0;
-  uint32_t phase = 0;
-  int i = 0;
+  int b = -1, s = 0, i = 0;
+  uint32_t phase = 0, qphase = 0;
   bool dead = false;
 
-  auto flush = [&](int bb) {
+  auto flush_o = [&](int bb) {
     const size_t slot = (size_t)x + bb;
     if (tid == 0 && blockIdx.y == 0) {
-      if (c_lo <= cum[bb]) p.ws.span[2 * bb] = x;            // holds the sequence's first chunk
-      if (c_hi >= cum[bb + 1]) p.ws.span[2 * bb + 1] = x;    // holds its last chunk
-    }
-    if (tp == 0) {
-      p.ws.m[slot * p.H + h0 + hr] = m_row;
-      p.ws.l[slot * p.H + h0 + hr] = l_row;
+      if (c_lo <= cum[bb]) p.ws.span[2 * bb] = x;
+      if (c_hi >= cum[bb + 1]) p.ws.span[2 * bb + 1] = x;
     }
     float* o0 = p.ws.o + (slot * p.H + h0 + r) * kDc;
     float* o1 = o0 + 8 * kDc;
@@ -526,352 +878,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
       }
     }
   };
-
-  // Step B: sum the 8 warps' partial scores of the chunk in buffer `buf`,
-  // online softmax of row hr, publish P and the rescale factor.
-  auto softmax_step = [&](int buf, int nv) {
-    const float2* xp = xpart + (size_t)buf * kCW * kHT * kXStride + hr * kXStride + tp;
-    float2 sum = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int ww = 0; ww < kCW; ++ww) {
-      const float2 v = xp[ww * kHT * kXStride];
-      sum.x += v.x;
-      sum.y += v.y;
+  // C of the previous chunk: wait for its P, then accumulate
+  auto finish_prev = [&](const ChunkRegs& prev) -> bool {
+    if (!pending) return true;
+    const int pi = i - 1;
+    if (!mbar_wait(smem_u32(&bp[pi & 1]), (uint32_t)((pi >> 1) & 1))) {
+      set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+      return false;
     }
-    float x0 = sum.x * cw, x1 = sum.y * cw;
-    if (nv < kChunk) {
-      if (2 * tp >= nv) x0 = -INFINITY;
-      if (2 * tp + 1 >= nv) x1 = -INFINITY;
-    }
-    float mx = fmaxf(x0, x1);
-#pragma unroll
-    for (int off = 1; off < 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    const float mn = fmaxf(m_row, mx);
-    const float al = mn == -INFINITY ? 1.f : ex2(m_row - mn);
-    const float sub = mn == -INFINITY ? 0.f : mn;
-    const float p0 = ex2(x0 - sub), p1 = ex2(x1 - sub);
-    float ps = p0 + p1;
-#pragma unroll
-    for (int off = 1; off < 16; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-    l_row = l_row * al + ps;
-    m_row = mn;
-    uint32_t* prow = reinterpret_cast<uint32_t*>(ptab + ((2 * buf) * kHT + hr) * kPStride) + tp;
-    if (F::kLatBf16) {
-      uint32_t phi, plo;
-      split_bf16(p0, p1, phi, plo);
-      prow[0] = phi;
-      prow[kHT * kPStride / 2] = plo;
-    } else {
-      prow[0] = pack_f16(p0, p1);
-    }
-    if (tp == 0) alpha_s[buf * kHT + hr] = al;
-  };
-
-  // Step C: rescale o and accumulate P V of the chunk in buffer `buf`, whose
-  // codes and scales this thread holds in bqv / s2v.
-  auto pv_step = [&](int buf, const uint32_t (&bqv)[4][4][2], const uint32_t (&s2v)[4][4]) {
-    {
-      const float al0 = alpha_s[buf * kHT + r], al1 = alpha_s[buf * kHT + r + 8];
-      if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            o[g][e][0] *= al0;
-            o[g][e][1] *= al0;
-            o[g][e][2] *= al1;
-            o[g][e][3] *= al1;
-          }
-      }
-    }
-    uint32_t pa[2][2][4];      // [hi/lo][k step][reg]
-    {
-      const uint32_t pbase = smem_u32(ptab) + (2 * buf) * kHT * kPStride * 2 +
-                             ((lane & 7) + 8 * ((lane >> 3) & 1)) * kPStride * 2 + 8 * (lane >> 4) * 2;
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        ldsm_x4(pbase + 32 * ks, pa[0][ks][0], pa[0][ks][1], pa[0][ks][2], pa[0][ks][3]);
-        if (F::kLatBf16)
-          ldsm_x4(pbase + kHT * kPStride * 2 + 32 * ks, pa[1][ks][0], pa[1][ks][1], pa[1][ks][2], pa[1][ks][3]);
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      uint32_t vt[4][2];
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        vt[n][0] = movt(bqv[g][n][0]);
-        vt[n][1] = movt(bqv[g][n][1]);
-      }
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        if (F::kLatBf16) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            mma_bf16(o[g][e], pa[0][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
-            mma_bf16(o[g][e], pa[1][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
-          }
-        } else if (F::kLatG8) {
-          // the operands already carry their 8-channel group's scale
-#pragma unroll
-          for (int e = 0; e < 2; ++e) mma_f16(o[g][e], pa[0][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
-        } else {
-          // A = P scaled per token (column) by the group's scale
-          uint32_t ag[4];
-          ag[0] = h2_bits(__hmul2(bits_h2(pa[0][ks][0]), bits_h2(s2v[g][2 * ks])));
-          ag[1] = h2_bits(__hmul2(bits_h2(pa[0][ks][1]), bits_h2(s2v[g][2 * ks])));
-          ag[2] = h2_bits(__hmul2(bits_h2(pa[0][ks][2]), bits_h2(s2v[g][2 * ks + 1])));
-          ag[3] = h2_bits(__hmul2(bits_h2(pa[0][ks][3]), bits_h2(s2v[g][2 * ks + 1])));
-#pragma unroll
-          for (int e = 0; e < 2; ++e) mma_f16(o[g][e], ag, vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
-        }
-      }
-    }
-  };
-
-  auto drain = [&](const ChunkRegs& prev) {
-    if (!pending) return;
-    const int buf = (int)((i - 1) & 1);
-    softmax_step(buf, nv_prev);
-    consumer_sync();
-    pv_step(buf, prev.bq, prev.s2h);
+    pv_chunk<LF, KF>(o, alpha_s, ptab, pi & 1, prev.bq, prev.s2h, lane);
     pending = false;
+    return true;
   };
 
-  // One chunk: QK^T of chunk c into `cur`, softmax and PV of the previous
-  // chunk from `prev`.  Returns false when a wait timed out.
-  auto chunk_step = [&](int c, ChunkRegs& cur, const ChunkRegs& prev) -> bool {
-    uint32_t (&bq)[4][4][2] = cur.bq;
-    uint32_t (&s2h)[4][4] = cur.s2h;
-    // ---- sequence boundary: finish the previous chunk, flush the partial,
-    // load the new query
-    {
-      int nb = b < 0 ? seq_of_chunk(cum, p.B, c) : b;
-      while (cum[nb + 1] <= c) ++nb;
-      if (nb != b) {
-        drain(prev);
-        if (b >= 0) flush(b);
-        b = nb;
-        QueryRaw raw;
-        const float am = warp_max(load_query_raw<LF, KF>(p, b, h0, w, lane, raw));
-        if (lane == 0) amax_s[w] = am;
-        consumer_sync();
-        float amx = 0.f;
-#pragma unroll
-        for (int k = 0; k < kCW; ++k) amx = fmaxf(amx, amax_s[k]);
-        int ex = 0;
-        if (!F::kLatBf16 && amx > 0.f && isfinite(amx)) {
-          ex = 14 - ilogbf(amx);
-          ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
-        }
-        finish_query<LF, KF>(raw, __int_as_float((127 + ex) << 23), q);
-        cw = p.scale_log2 * __int_as_float((127 - ex) << 23);
-        m_row = -INFINITY;
-        l_row = 0.f;
-#pragma unroll
-        for (int g = 0; g < 4; ++g)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-#pragma unroll
-            for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
+  auto chunk_step = [&](int c, ChunkRegs& cur, ChunkRegs& prev) -> bool {
+    int nb = b < 0 ? seq_of_chunk(cum, p.B, c) : b;
+    while (cum[nb + 1] <= c) ++nb;
+    if (nb != b) {
+      if (!finish_prev(prev)) return false;
+      if (b >= 0) flush_o(b);
+      b = nb;
+      QueryRaw raw;
+      const float am = warp_max(load_query_raw<LF, KF>(p, b, h0, w, lane, raw));
+      if (lane == 0) amax_s[w] = am;
+      mbar_arrive(smem_u32(qa));
+      if (!mbar_wait(smem_u32(qa), qphase)) {
+        set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+        return false;
       }
+      qphase ^= 1u;
+      float amx = 0.f;
+#pragma unroll
+      for (int k = 0; k < kCW; ++k) amx = fmaxf(amx, amax_s[k]);
+      int ex = 0;
+      if (!F::kLatBf16 && amx > 0.f && isfinite(amx)) {
+        ex = 14 - ilogbf(amx);
+        ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
+      }
+      finish_query<LF, KF>(raw, __int_as_float((127 + ex) << 23), q);
+      cw = p.scale_log2 * __int_as_float((127 - ex) << 23);
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
     }
-    if (tid == 0) plan();
     if (!mbar_wait(smem_u32(&full_bar[s]), phase)) {
       set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
       return false;
     }
     const int nv = meta[s];
-    const bool partial = nv < kChunk;     // includes nv == 0 (no data: everything is masked)
-    const uint8_t* st = stages + s * F::kBlock;
-    const uint32_t st_a = smem_u32(st);
-    const float* sc = reinterpret_cast<const float*>(st + F::kScaleOff);
-
-    // ---- step A: B operands (exact codes, or code - zero) and QK^T of chunk i
-    if (F::kLatBf16) {
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const int ch = 2 * (4 * w + g);
-        uint32_t t0, t1, t2, t3;
-        ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(ch, lane) * 16, t0, t1, t2, t3);
-        bq[g][0][0] = t0; bq[g][1][0] = t1; bq[g][2][0] = t2; bq[g][3][0] = t3;
-        ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(ch + 1, lane) * 16, t0, t1, t2, t3);
-        bq[g][0][1] = t0; bq[g][1][1] = t1; bq[g][2][1] = t2; bq[g][3][1] = t3;
-      }
-      if (partial) {       // PV reads these values: zero the tokens past the end
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-          if (8 * n + r >= nv)
-#pragma unroll
-            for (int g = 0; g < 4; ++g) bq[g][n][0] = bq[g][n][1] = 0u;
-      }
-    } else if (F::kLatInt4) {
-      const float* zp = reinterpret_cast<const float*>(st + F::kZeroOff);
-      const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f), km64 = __floats2half2_rn(-64.f, -64.f);
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t t[4];
-        ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(2 * w + cc, lane) * 16, t[0], t[1], t[2], t[3]);
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          __half2 zz;
-          if (F::kLatSym4) {
-            zz = __floats2half2_rn(8.f, 8.f);                         // nibble = code + 8
-          } else {
-            // zero-points of this thread's B token (8n + r) for groups A and B of the chunk
-            float za = zp[(4 * w + 2 * cc) * kBlockTokens + 8 * n + r];
-            float zb = zp[(4 * w + 2 * cc + 1) * kBlockTokens + 8 * n + r];
-            if (partial && 8 * n + r >= nv) za = zb = 0.f;
-            zz = __floats2half2_rn(za, zb);                            // exact (integer zero-points)
-          }
-          i4x8_to_f16(t[n], __hadd2(zz, k1024), __hsub2(km64, zz), bq[2 * cc][n][0], bq[2 * cc][n][1],
-                      bq[2 * cc + 1][n][0], bq[2 * cc + 1][n][1]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        uint32_t t[4];
-        ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(4 * w + g, lane) * 16, t[0], t[1], t[2], t[3]);
-#pragma unroll
-        for (int n = 0; n < 4; ++n) i8x4_to_f16(t[n], bq[g][n][0], bq[g][n][1]);
-      }
-    }
-    uint32_t bk[4][2];
-    const bool kact = F::kKpeBf16 ? (w < 4) : true;
-    if (F::kKpeBf16) {
-      if (kact) {
-        uint32_t t[4];
-        ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(2 * w, lane, KF) * 16, t[0], t[1], t[2], t[3]);
-#pragma unroll
-        for (int n = 0; n < 4; ++n) bk[n][0] = t[n];
-        ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(2 * w + 1, lane, KF) * 16, t[0], t[1], t[2],
-                t[3]);
-#pragma unroll
-        for (int n = 0; n < 4; ++n) bk[n][1] = t[n];
-      }
-    } else if (F::kKpeInt4) {
-      // warp w: k_pe group w = channels 8w .. 8w+7, in 32-channel chunk w / 4,
-      // 16-channel half (w / 2) % 2; the MMA takes the half's 16 channels
-      // (its A fragment is zero outside the group, as for INT8 k_pe)
-      uint32_t t[4];
-      ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(w >> 2, lane, KF) * 16, t[0], t[1], t[2], t[3]);
-      const __half2 zo = __floats2half2_rn(1032.f, 1032.f), zc = __floats2half2_rn(-72.f, -72.f);
-      const bool hb = (w >> 1) & 1;
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        uint32_t a0, a1, b0, b1;
-        i4x8_to_f16(t[n], zo, zc, a0, a1, b0, b1);
-        bk[n][0] = hb ? b0 : a0;
-        bk[n][1] = hb ? b1 : a1;
-      }
-    } else {
-      uint32_t t[4];
-      ldsm_x4(st_a + F::kKpeOff + lane * F::kKRow + kpe_chunk_pos(w >> 1, lane, KF) * 16, t[0], t[1], t[2], t[3]);
-#pragma unroll
-      for (int n = 0; n < 4; ++n) i8x4_to_f16(t[n], bk[n][0], bk[n][1]);
-    }
-
     float acc[4][4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[n][e] = 0.f;
-    if (F::kLatBf16) {
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-#pragma unroll
-        for (int n = 0; n < 4; ++n) mma_bf16(acc[n], q.hi[g], bq[g][n][0], bq[g][n][1], acc[n]);
-#pragma unroll
-        for (int n = 0; n < 4; ++n) mma_bf16(acc[n], q.lo[g], bq[g][n][0], bq[g][n][1], acc[n]);
-      }
-    } else if (F::kLatG8) {
-      // two 8-channel scale groups per 16-channel step: one m16n8k8 MMA per
-      // group (standard layout: A registers 0 / 1 and B register 0 carry
-      // channels 0-7 of the step, A registers 2 / 3 and B register 1
-      // channels 8-15) and one scale FMA per element; then each operand
-      // register is scaled by its own group's scale for PV (fp16, one
-      // rounding, as the P-side scaling of the other formats)
-      const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int si = 2 * (4 * w + g) + hh;
-          float d[4][4];
-#pragma unroll
-          for (int n = 0; n < 4; ++n) mma_f16_k8(d[n], q.hi[g][2 * hh], q.hi[g][2 * hh + 1], bq[g][n][hh], zero4);
-#pragma unroll
-          for (int n = 0; n < 4; ++n) mma_f16_k8(d[n], q.lo[g][2 * hh], q.lo[g][2 * hh + 1], bq[g][n][hh], d[n]);
-#pragma unroll
-          for (int n = 0; n < 4; ++n) {
-            float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
-            float sv = sc[si * kBlockTokens + 8 * n + r];
-            if (partial) {
-              if (8 * n + 2 * j >= nv) s2.x = 0.f;
-              if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
-              if (8 * n + r >= nv) sv = 0.f;
-            }
-            acc[n][0] = fmaf(d[n][0], s2.x, acc[n][0]);
-            acc[n][1] = fmaf(d[n][1], s2.y, acc[n][1]);
-            acc[n][2] = fmaf(d[n][2], s2.x, acc[n][2]);
-            acc[n][3] = fmaf(d[n][3], s2.y, acc[n][3]);
-            bq[g][n][hh] = h2_bits(__hmul2(bits_h2(bq[g][n][hh]), __float2half2_rn(sv)));
-          }
-        }
-      }
-    } else {
-      // the MMA steps of one scale group accumulate together (exact codes,
-      // fp32 accumulator), then one FMA per element applies the scale
-      const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-      float d[4][4];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const bool first = g % F::kSPG == 0, last = (g + 1) % F::kSPG == 0 || g == 3;
-#pragma unroll
-        for (int n = 0; n < 4; ++n) mma_f16(d[n], q.hi[g], bq[g][n][0], bq[g][n][1], first ? zero4 : d[n]);
-#pragma unroll
-        for (int n = 0; n < 4; ++n) mma_f16(d[n], q.lo[g], bq[g][n][0], bq[g][n][1], d[n]);
-        if (last) {
-          const int si = (4 * w + g) / F::kSPG;
-#pragma unroll
-          for (int n = 0; n < 4; ++n) {
-            float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
-            if (partial) {
-              if (8 * n + 2 * j >= nv) s2.x = 0.f;
-              if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
-            }
-            acc[n][0] = fmaf(d[n][0], s2.x, acc[n][0]);
-            acc[n][1] = fmaf(d[n][1], s2.y, acc[n][1]);
-            acc[n][2] = fmaf(d[n][2], s2.x, acc[n][2]);
-            acc[n][3] = fmaf(d[n][3], s2.y, acc[n][3]);
-            const uint32_t sh = pack_f16(s2.x, s2.y);
-#pragma unroll
-            for (int g2 = 0; g2 < 4; ++g2)
-              if (g2 <= g && g2 > g - F::kSPG) s2h[g2][n] = sh;
-          }
-        }
-      }
-    }
-    if (F::kKpeBf16) {
-      if (kact) {
-#pragma unroll
-        for (int n = 0; n < 4; ++n) mma_bf16(acc[n], q.ka, bk[n][0], bk[n][1], acc[n]);
-      }
-    } else {
-      const float* ks = reinterpret_cast<const float*>(st + F::kKScaleOff);
-      const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        const float2 s2 = *reinterpret_cast<const float2*>(ks + w * kBlockTokens + 8 * n + 2 * j);
-        float d[4];
-        mma_f16(d, q.ka, bk[n][0], bk[n][1], zero4);
-        acc[n][0] = fmaf(d[0], s2.x, acc[n][0]);
-        acc[n][1] = fmaf(d[1], s2.y, acc[n][1]);
-        acc[n][2] = fmaf(d[2], s2.x, acc[n][2]);
-        acc[n][3] = fmaf(d[3], s2.y, acc[n][3]);
-      }
-    }
+    qk_chunk<LF, KF>(stages + s * F::kBlock, nv, w, lane, q, cur.bq, cur.s2h, acc);
     {
       float2* xw = xpart + (((size_t)(i & 1) * kCW + w) * kHT + r) * kXStride + j;
 #pragma unroll
@@ -880,13 +939,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
         xw[8 * kXStride + 4 * n] = make_float2(acc[n][2], acc[n][3]);
       }
     }
-
-    // ---- step B for chunk i - 1, one barrier, refill, step C for chunk i - 1
-    if (pending) softmax_step((int)((i - 1) & 1), nv_prev);
-    consumer_sync();
-    if (tid == 0) commit(s);
-    if (pending) pv_step((int)((i - 1) & 1), prev.bq, prev.s2h);
-    nv_prev = nv;
+    if (tid == 0) {
+      nvq[i & 1] = nv;
+      cwq[i & 1] = cw;
+    }
+    mbar_arrive(smem_u32(&bx[i & 1]));
+    if (!finish_prev(prev)) return false;
     pending = true;
     ++i;
     if (++s == F::kStages) {
@@ -905,9 +963,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(DecodeParams p)
     last_in_a = false;
   }
   if (!dead) {
-    if (last_in_a) drain(ra);
-    else drain(rb);
-    if (b >= 0) flush(b);
+    const bool ok = last_in_a ? finish_prev(ra) : finish_prev(rb);
+    if (ok && b >= 0) flush_o(b);
   }
 }
 
@@ -937,8 +994,9 @@ mla_status launch_t(const DecodeParams& p, cudaStream_t stream) {
     if (st != MLA_OK) return st;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
-  if (smem > smem_max()) return MLA_ERR_UNSUPPORTED;
-  return cuda_status(launch_pdl(decode_mma_kernel<LF, KF>, dim3(p.G, p.H / kHT), dim3(kThreads), smem, stream, p));
+  if (smem + kWsExtra > smem_max()) return MLA_ERR_UNSUPPORTED;
+  return cuda_status(launch_pdl(decode_mma_kernel<LF, KF>, dim3(p.G, p.H / kHT), dim3(kWsThreads), smem + kWsExtra,
+                                stream, p));
 }
 
 }  // namespace
