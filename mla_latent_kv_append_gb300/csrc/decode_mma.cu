@@ -172,6 +172,17 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
         "f"(c[3]));
 }
 
+// acc[0..1] += d[0..1] * s and acc[2..3] += d[2..3] * s (C-fragment rows r and
+// r + 8 of one n-tile against its two tokens' scales) as two packed f32x2 FMAs
+__device__ __forceinline__ void scale_acc(float* acc, const float* d, float2 s) {
+  const float2 a = __ffma2_rn(make_float2(d[0], d[1]), s, make_float2(acc[0], acc[1]));
+  const float2 b = __ffma2_rn(make_float2(d[2], d[3]), s, make_float2(acc[2], acc[3]));
+  acc[0] = a.x;
+  acc[1] = a.y;
+  acc[2] = b.x;
+  acc[3] = b.y;
+}
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
@@ -515,10 +526,7 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
             if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
             if (8 * n + r >= nv) sv = 0.f;
           }
-          acc[n][0] = fmaf(d[n][0], s2.x, acc[n][0]);
-          acc[n][1] = fmaf(d[n][1], s2.y, acc[n][1]);
-          acc[n][2] = fmaf(d[n][2], s2.x, acc[n][2]);
-          acc[n][3] = fmaf(d[n][3], s2.y, acc[n][3]);
+          scale_acc(acc[n], d[n], s2);
           bq[g][n][hh] = h2_bits(__hmul2(bits_h2(bq[g][n][hh]), __float2half2_rn(sv)));
         }
       }
@@ -544,10 +552,7 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
             if (8 * n + 2 * j >= nv) s2.x = 0.f;
             if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
           }
-          acc[n][0] = fmaf(d[n][0], s2.x, acc[n][0]);
-          acc[n][1] = fmaf(d[n][1], s2.y, acc[n][1]);
-          acc[n][2] = fmaf(d[n][2], s2.x, acc[n][2]);
-          acc[n][3] = fmaf(d[n][3], s2.y, acc[n][3]);
+          scale_acc(acc[n], d[n], s2);
           const uint32_t sh = pack_f16(s2.x, s2.y);
 #pragma unroll
           for (int g2 = 0; g2 < 4; ++g2)
@@ -572,10 +577,7 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
       const float2 s2 = *reinterpret_cast<const float2*>(ks + w * kBlockTokens + 8 * n + 2 * j);
       float d[4];
       mma_f16(d, q.ka, bk[n][0], bk[n][1], zero4);
-      acc[n][0] = fmaf(d[0], s2.x, acc[n][0]);
-      acc[n][1] = fmaf(d[1], s2.y, acc[n][1]);
-      acc[n][2] = fmaf(d[2], s2.x, acc[n][2]);
-      acc[n][3] = fmaf(d[3], s2.y, acc[n][3]);
+      scale_acc(acc[n], d, s2);
     }
   }
 }
@@ -595,10 +597,12 @@ __device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha
       for (int g = 0; g < 4; ++g)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          o[g][e][0] *= al0;
-          o[g][e][1] *= al0;
-          o[g][e][2] *= al1;
-          o[g][e][3] *= al1;
+          const float2 a = __fmul2_rn(make_float2(o[g][e][0], o[g][e][1]), make_float2(al0, al0));
+          const float2 b = __fmul2_rn(make_float2(o[g][e][2], o[g][e][3]), make_float2(al1, al1));
+          o[g][e][0] = a.x;
+          o[g][e][1] = a.y;
+          o[g][e][2] = b.x;
+          o[g][e][3] = b.y;
         }
     }
   }
@@ -795,15 +799,14 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       const float cw = cwq[buf];
       // sum the 8 warps' partial scores of 4 tokens of row hr
       const float4* xp = reinterpret_cast<const float4*>(xpart + ((size_t)buf * kCW * kHT + hr) * kXStride) + tq;
-      float4 sm = make_float4(0.f, 0.f, 0.f, 0.f);
+      float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int ww = 0; ww < kCW; ++ww) {
         const float4 v = xp[ww * kHT * kXStride / 2];
-        sm.x += v.x;
-        sm.y += v.y;
-        sm.z += v.z;
-        sm.w += v.w;
+        s01 = __fadd2_rn(s01, make_float2(v.x, v.y));
+        s23 = __fadd2_rn(s23, make_float2(v.z, v.w));
       }
+      const float4 sm = make_float4(s01.x, s01.y, s23.x, s23.y);
       float xv[4] = {sm.x * cw, sm.y * cw, sm.z * cw, sm.w * cw};
       if (nv < kChunk) {
 #pragma unroll
