@@ -400,6 +400,17 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
   using F = Fmt<LF, KF>;
   const int r = lane >> 2, j = lane & 3;
   const bool partial = nv < kChunk;     // includes nv == 0 (no data: everything is masked)
+  // Tokens past nv hold stale or unwritten bytes.  Their scores need no mask
+  // here (the softmax replaces them with -inf by selection), but everything
+  // PV multiplies with their zero P must be finite: their scales and
+  // zero-points are masked bitwise.  mc[n]: the C-fragment token pair
+  // (8n + 2j, 8n + 2j + 1), as f16x2 lanes; mb[n]: the B-operand token 8n + r.
+  uint32_t mc[4], mb[4];
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    mc[n] = partial ? (8 * n + 2 * j < nv ? 0x0000FFFFu : 0u) | (8 * n + 2 * j + 1 < nv ? 0xFFFF0000u : 0u) : ~0u;
+    mb[n] = partial ? (8 * n + r < nv ? ~0u : 0u) : ~0u;
+  }
   const uint32_t st_a = smem_u32(st);
   const float* sc = reinterpret_cast<const float*>(st + F::kScaleOff);
   // ---- step A: B operands (exact codes, or code - zero) and QK^T of chunk i
@@ -434,10 +445,9 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
           zz = __floats2half2_rn(8.f, 8.f);                         // nibble = code + 8
         } else {
           // zero-points of this thread's B token (8n + r) for groups A and B of the chunk
-          float za = zp[(4 * w + 2 * cc) * kBlockTokens + 8 * n + r];
-          float zb = zp[(4 * w + 2 * cc + 1) * kBlockTokens + 8 * n + r];
-          if (partial && 8 * n + r >= nv) za = zb = 0.f;
-          zz = __floats2half2_rn(za, zb);                            // exact (integer zero-points)
+          const float za = zp[(4 * w + 2 * cc) * kBlockTokens + 8 * n + r];
+          const float zb = zp[(4 * w + 2 * cc + 1) * kBlockTokens + 8 * n + r];
+          zz = bits_h2(h2_bits(__floats2half2_rn(za, zb)) & mb[n]);   // exact (integer zero-points)
         }
         i4x8_to_f16(t[n], __hadd2(zz, k1024), __hsub2(km64, zz), bq[2 * cc][n][0], bq[2 * cc][n][1],
                     bq[2 * cc + 1][n][0], bq[2 * cc + 1][n][1]);
@@ -519,15 +529,10 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
         for (int n = 0; n < 4; ++n) mma_f16_k8(d[n], q.lo[g][2 * hh], q.lo[g][2 * hh + 1], bq[g][n][hh], d[n]);
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
-          float sv = sc[si * kBlockTokens + 8 * n + r];
-          if (partial) {
-            if (8 * n + 2 * j >= nv) s2.x = 0.f;
-            if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
-            if (8 * n + r >= nv) sv = 0.f;
-          }
+          const float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
+          const float sv = sc[si * kBlockTokens + 8 * n + r];
           scale_acc(acc[n], d[n], s2);
-          bq[g][n][hh] = h2_bits(__hmul2(bits_h2(bq[g][n][hh]), __float2half2_rn(sv)));
+          bq[g][n][hh] = h2_bits(__hmul2(bits_h2(bq[g][n][hh]), __float2half2_rn(sv))) & mb[n];
         }
       }
     }
@@ -547,13 +552,9 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
         const int si = (4 * w + g) / F::kSPG;
 #pragma unroll
         for (int n = 0; n < 4; ++n) {
-          float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
-          if (partial) {
-            if (8 * n + 2 * j >= nv) s2.x = 0.f;
-            if (8 * n + 2 * j + 1 >= nv) s2.y = 0.f;
-          }
+          const float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
           scale_acc(acc[n], d[n], s2);
-          const uint32_t sh = pack_f16(s2.x, s2.y);
+          const uint32_t sh = pack_f16(s2.x, s2.y) & mc[n];
 #pragma unroll
           for (int g2 = 0; g2 < 4; ++g2)
             if (g2 <= g && g2 > g - F::kSPG) s2h[g2][n] = sh;

@@ -116,3 +116,23 @@ def test_largest_batch():
     wl = Workload(1, 16, lens, mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM, seed=83)
     seqs = sorted(set([0, 4095] + [int(b) for b in rng.integers(0, 4096, 48)]))
     run_and_check(wl, seqs=seqs)
+
+
+POISON_FORMATS = [(mla.FMT_BF16, mla.FMT_BF16), (mla.FMT_INT8_SYM, mla.FMT_INT8_SYM),
+                  (mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM), (mla.FMT_INT4_SYM, mla.FMT_INT4_SYM),
+                  (mla.FMT_INT8_G8, mla.FMT_INT8_SYM), (mla.FMT_INT8_G32, mla.FMT_INT8_SYM),
+                  (mla.FMT_INT8_G64, mla.FMT_INT8_SYM), (mla.FMT_INT8_TOKEN, mla.FMT_INT8_SYM),
+                  (mla.FMT_INT4_ASYM, mla.FMT_BF16)]
+
+
+@pytest.mark.parametrize("lf,kf", POISON_FORMATS, ids=["%s-%s" % (FMT_NAME[a], FMT_NAME[b]) for a, b in POISON_FORMATS])
+def test_poisoned_page_tails(lf, kf):
+    """Every pool byte starts as 0xFF (NaN scales and zero-points, extreme
+    codes), so the slots past each sequence's end hold garbage: the decode
+    must read only the first seq_len tokens and stay finite."""
+    lens = [1, 31, 33, 64, 65, 100, 129, 250]
+    wl = Workload(1, 16, lens, lf, kf, seed=84, fill=False)
+    for c in wl.caches:
+        c.pool.fill_(0xFF)
+    wl.fill()
+    run_and_check(wl)
