@@ -87,6 +87,7 @@ BETA.update({(a, "int8"): _beta(a, "int8") for a in ("int8g8", "int8g32", "int8g
 METRIC = "decode tokens/s & achieved HBM GB/s (% of GB300 peak) for absorbed MLA decode"
 SEED = 0x4D4C41
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def seq_lens_for(cfg, seed):
@@ -102,6 +103,24 @@ def hbm_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense 16-bit tensor peak (TFLOP/s) for a kernel timed alone: the burst
+    cuBLAS figure of MEASURED_PEAKS.json (fp16 and bf16 run at one rate)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def prefill_flops(P, H, ctx_before=0):
+    """Useful absorbed-attention flops of a P-token chunk: each of the
+    sum_i (ctx_before + i + 1) (query, key) pairs per head costs a 576-wide
+    score dot product and a 512-wide P V update (2 flops per multiply-add)."""
+    pairs = P * ctx_before + P * (P + 1) // 2
+    return pairs * H * 2 * (576 + 512)
 
 
 def decode_source_hash():
@@ -311,7 +330,7 @@ def cpu_baseline(cfg, seq_lens, min_seconds=8.0, steps=None, warmup=1):
 def run_ours(args, cfg, rank, world, local_rank):
     import torch
     import mla_latent_kv_append_gb300 as mla
-    from synth.workload import DecodeStep, Workload
+    from synth.workload import DecodeStep, PrefillStep, Workload
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -414,6 +433,49 @@ def run_ours(args, cfg, rank, world, local_rank):
                "achieved": pre_bytes / (pre_ms * 1e-3) / 1e9, "peak": peak0, "unit": "GB/s",
                "frac": pre_bytes / (pre_ms * 1e-3) / 1e9 / peak0}
 
+    # ---- the prefill chunk's causal attention (mixed serving step): absorb
+    # the P queries, mla_prefill_absorbed over the chunk, unabsorb; the
+    # attention call is also timed alone.  Its cache pages (a few MB) stay in
+    # L2: this part is bound by the tensor pipe, not by HBM.
+    pattn = None
+    if wl.prefill:
+        pstep = PrefillStep(wl)
+        with torch.cuda.stream(stream):
+            pstep.run()
+        torch.cuda.synchronize()
+        fgraph, agraph = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(fgraph, stream=stream):
+            pstep.run()
+        with torch.cuda.graph(agraph, stream=stream):
+            mla.mla_prefill_absorbed(wl.caches[0], pstep.q_lat, wl.q_pe_pre[0], wl.prefill_block_table, 0,
+                                     pstep.workspace, pstep.o_lat, pstep.lse[0], pstep.dev_err)
+        preps = 3
+        with torch.cuda.stream(stream):
+            fgraph.replay()
+            a.record(stream)
+            for _ in range(preps):
+                fgraph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        full_ms = a.elapsed_time(b) / (preps * wl.L)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for _ in range(preps):
+                agraph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        attn_ms = a.elapsed_time(b) / preps
+        flops = prefill_flops(wl.prefill, wl.H)
+        tpk, tpk_kind = tensor_peak()
+        achieved_t = flops / (attn_ms * 1e-3) / 1e12
+        pattn = {"bound": "tensor", "tokens": wl.prefill, "heads": wl.H, "flops_per_launch": flops,
+                 "launch_ms": attn_ms, "achieved": achieved_t, "peak": tpk, "unit": "TFLOP/s",
+                 "frac": achieved_t / tpk, "peak_source": "%s bf16_tflops (MEASURED_PEAKS.json)" % tpk_kind,
+                 "ms_with_absorb_unabsorb": full_ms, "device_error_word": int(pstep.dev_err.item()),
+                 "kernel": "mla_prefill_absorbed (split-K decode kernels over the causal prefixes + combine)"}
+        del pstep, fgraph, agraph
+        torch.cuda.empty_cache()
+
     # ---- end to end through the public API with host buffers
     # every step's inputs of all layers live in one device buffer
     # (wl.step_inputs): one pinned host buffer, one copy in, one copy out
@@ -483,6 +545,7 @@ def run_ours(args, cfg, rank, world, local_rank):
         "device_error_word": err_word,
         "clocks": clk,
         "prefill_append": pre,
+        "prefill_attention": pattn,
         "setup_s": round(setup_s, 1),
     }
     return out, seq_lens

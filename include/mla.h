@@ -265,6 +265,37 @@ mla_status mla_decode_absorbed_noalloc(const mla_cache_layer* cache, const float
                                        float* o_lat, float* lse, int32_t* dev_err, mla_stream_t stream);
 
 /*
+ * mla_prefill_workspace_bytes - bytes of device workspace mla_prefill_absorbed
+ * needs for a chunk of n query tokens and this head count (0 for invalid
+ * arguments).  Bounded in n: queries are processed in slices of 2048.
+ */
+size_t mla_prefill_workspace_bytes(int32_t n, int32_t heads);
+
+/*
+ * mla_prefill_absorbed - causal absorbed attention of a prefill chunk: the
+ * queries of n tokens of one sequence that were just appended to the cache
+ * (chunked prefill when ctx_before > 0).  Query i sits at position
+ * ctx_before + i and attends to the cached positions 0 .. ctx_before + i,
+ * its own token included; per query this is the decode of [EN] §2.1 over
+ * that prefix, computed by the same split-K kernels with the queries as the
+ * batch.
+ *   q_lat       fp32 [n][H][512]  (mla_q_absorb with batch = n)
+ *   q_pe        bf16 [n][H][64]
+ *   block_table int32 [max_pages]: the sequence's page ids; positions up to
+ *               ctx_before + n - 1 must have been appended.
+ *   workspace:  device, >= mla_prefill_workspace_bytes(n, H) bytes,
+ *               256-byte aligned; contents are scratch.
+ *   o_lat fp32 [n][H][512]      lse fp32 [n][H] (natural log; may be NULL)
+ *   n == 0 is a no-op.  ctx_before >= 0 and ctx_before + n <= max_pages * 64,
+ *   else MLA_ERR_INVALID_ARG.  A page id outside [0, num_pages) contributes
+ *   nothing and sets MLA_DEVERR_PAGE.
+ */
+mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat, const uint16_t* q_pe,
+                                const int32_t* block_table, int32_t max_pages, int32_t ctx_before, int32_t n,
+                                int32_t heads, float softmax_scale, void* workspace, size_t workspace_bytes,
+                                float* o_lat, float* lse, int32_t* dev_err, mla_stream_t stream);
+
+/*
  * mla_out_unabsorb - o[b][h] = o_lat[b][h] @ W_UV[h]   (the output side of
  * weight absorption; [TU] "步骤2" V_i = C^KV W_i^upV with W_UV[h] = W_i^upV).
  *   o_lat fp32 [B][H][512]   W_UV bf16 [H][512][128]   o fp32 [B][H][128]

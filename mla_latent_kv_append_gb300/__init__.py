@@ -18,8 +18,9 @@ Names follow the C ABI:
 
 plus ``CacheLayer`` (one layer's pool and formats), ``mla_cache_page_layout``,
 ``mla_cache_pool_bytes``, ``mla_decode_workspace_bytes``,
-``mla_decode_absorbed_noalloc`` (the decode for callers that cannot allocate)
-and ``mla_lse_merge`` (merges per-part results of a context-sharded decode;
+``mla_decode_absorbed_noalloc`` (the decode for callers that cannot allocate),
+``mla_prefill_absorbed`` / ``mla_prefill_workspace_bytes`` (causal attention
+of a prefill chunk) and ``mla_lse_merge`` (merges per-part results of a context-sharded decode;
 the host side of that exchange is in ``sharded``).
 """
 
@@ -80,6 +81,8 @@ def _load():
         "mla_out_unabsorb": (I32, [P, P, P, I32, I32, P]),
         "mla_decode_absorbed_noalloc": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, P, P, P]),
         "mla_lse_merge": (I32, [P, P, I32, I32, I32, P, P, P]),
+        "mla_prefill_workspace_bytes": (SZ, [I32, I32]),
+        "mla_prefill_absorbed": (I32, [CP, P, P, P, I32, I32, I32, I32, F32, P, SZ, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -209,6 +212,30 @@ def mla_decode_absorbed_noalloc(cache, q_lat, q_pe, block_table, seq_lens, o_lat
     _check("mla_decode_absorbed_noalloc", lib.mla_decode_absorbed_noalloc(
         ctypes.byref(cs), _ptr(q_lat), _ptr(q_pe), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H,
         scale, int(num_splits), _ptr(o_lat), _ptr(lse), _ptr(dev_err), _stream(stream)))
+
+
+def mla_prefill_workspace_bytes(n, heads):
+    return int(lib.mla_prefill_workspace_bytes(int(n), int(heads)))
+
+
+def mla_prefill_absorbed(cache, q_lat, q_pe, block_table, ctx_before, workspace, o_lat, lse=None, dev_err=None,
+                         softmax_scale=None, stream=None):
+    """Causal attention of n just-appended query tokens of one sequence:
+    query i (position ctx_before + i) attends to positions 0 .. ctx_before + i.
+    block_table is the sequence's int32 page list [max_pages]."""
+    n, H = q_lat.shape[0], q_lat.shape[1]
+    _need(q_lat, torch.float32, (n, H, KV_LORA_RANK), "q_lat")
+    _need(q_pe, torch.bfloat16, (n, H, ROPE_DIM), "q_pe")
+    _need(block_table, torch.int32, (block_table.shape[0],), "block_table")
+    _need(o_lat, torch.float32, (n, H, KV_LORA_RANK), "o_lat")
+    if lse is not None:
+        _need(lse, torch.float32, (n, H), "lse")
+    scale = DEFAULT_SOFTMAX_SCALE if softmax_scale is None else float(softmax_scale)
+    cs = cache.c_struct()
+    _check("mla_prefill_absorbed", lib.mla_prefill_absorbed(
+        ctypes.byref(cs), _ptr(q_lat), _ptr(q_pe), _ptr(block_table), block_table.shape[0], int(ctx_before), n, H,
+        scale, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o_lat), _ptr(lse),
+        _ptr(dev_err), _stream(stream)))
 
 
 def mla_lse_merge(o_parts, lse_parts, o_lat, lse=None, stream=None):

@@ -49,7 +49,7 @@ using namespace mla;
 
 extern "C" {
 
-int32_t mla_abi_version(void) { return 101; }
+int32_t mla_abi_version(void) { return 102; }
 
 const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
 
@@ -168,6 +168,7 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
   p.q_pe = q_pe;
   p.block_table = block_table;
   p.max_pages = max_pages;
+  p.bt_stride = max_pages;
   p.seq_lens = seq_lens;
   p.B = batch;
   p.H = heads;

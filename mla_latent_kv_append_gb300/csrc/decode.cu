@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
         int valid = t < len;
         int page = 0;
         if (valid) {
-          page = p.block_table[(size_t)b * p.max_pages + (t >> 6)];
+          page = p.block_table[(size_t)b * p.bt_stride + (t >> 6)];
           if (page < 0 || page >= p.num_pages) {
             set_err(p.dev_err, MLA_DEVERR_PAGE);
             valid = 0;

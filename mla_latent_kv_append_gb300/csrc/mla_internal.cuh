@@ -209,6 +209,7 @@ struct DecodeParams {
   const uint16_t* q_pe;
   const int32_t* block_table;
   int max_pages;
+  int bt_stride;          // block-table row stride: max_pages, or 0 when every row is row 0 (prefill)
   const int32_t* seq_lens;
   int B, H, G;
   float scale_log2;       // softmax_scale * log2(e)

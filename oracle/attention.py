@@ -29,9 +29,15 @@ is W_UK[h]^T and W_i^upV (d_c x d_v) is W_UV[h].
 
 An empty context (T = 0) gives o_lat = 0, o = 0 and lse = -inf.
 
+The prefill chunk (queries of tokens just appended, attending causally to
+the positions up to their own) is the same absorbed attention per query
+over its prefix; its expanded twin is the textbook masked score matrix.
+
 Parity status: pinned (the tutorial's worked example for the row-vector
 convention, absorbed == expanded, closed forms for T = 1 and for equal
-scores, brute-force exp/sum on tiny inputs, split invariance).
+scores, brute-force exp/sum on tiny inputs, split invariance; for the
+prefill: absorbed == the expanded masked matrix, the first query's closed
+form, causality under changes to later tokens, and a hand-computed chunk).
 """
 
 import numpy as np
@@ -115,6 +121,51 @@ def expanded_decode(q_nope, q_pe, w_uk, w_uv, c_hat, kpe_hat,
         outs.append((e @ v) / e.sum())
         lses.append(m + np.log(e.sum()))
     return np.stack(outs), np.array(lses)
+
+
+# ---------------------------------------------------------------------------
+# Causal attention of a prefill chunk.
+# ---------------------------------------------------------------------------
+
+def absorbed_prefill(q_lat, q_pe, c_hat, kpe_hat, ctx_before, softmax_scale=DEFAULT_SOFTMAX_SCALE):
+    """Queries of n tokens appended at positions ctx_before .. ctx_before+n-1
+    of one sequence; query i attends to the cached positions 0 ..
+    ctx_before + i (causal, its own token included), each one an absorbed
+    decode over that prefix.  q_lat [n, H, 512], q_pe [n, H, 64]; c_hat /
+    kpe_hat hold at least ctx_before + n tokens.  Returns (o_lat [n, H, 512],
+    lse [n, H])."""
+    n = np.asarray(q_lat).shape[0]
+    outs, lses = [], []
+    for i in range(n):
+        t = ctx_before + i + 1
+        o, l = absorbed_decode(q_lat[i], q_pe[i], c_hat[:t], kpe_hat[:t], softmax_scale)
+        outs.append(o)
+        lses.append(l)
+    return np.stack(outs), np.stack(lses)
+
+
+def expanded_prefill(q_nope, q_pe, w_uk, w_uv, c_hat, kpe_hat, ctx_before, softmax_scale=DEFAULT_SOFTMAX_SCALE):
+    """Textbook masked attention of the same chunk on re-expanded K/V: per
+    head, the [n, T] score matrix of [q_nope, q_pe] against [c_hat W_UK^T,
+    kpe_hat], entries with key position > ctx_before + row set to -inf, a
+    row softmax, times V = c_hat W_UV.  Returns (o [n, H, 128], lse [n, H])."""
+    q_nope, q_pe, w_uk, w_uv = map(_f64, (q_nope, q_pe, w_uk, w_uv))
+    c_hat, kpe_hat = _f64(c_hat), _f64(kpe_hat)
+    n, H = q_nope.shape[0], q_nope.shape[1]
+    T = ctx_before + n
+    c_hat, kpe_hat = c_hat[:T], kpe_hat[:T]
+    allowed = np.arange(T)[None, :] <= (ctx_before + np.arange(n))[:, None]     # [n, T]
+    outs, lses = [], []
+    for h in range(H):
+        k = np.concatenate([c_hat @ w_uk[h].T, kpe_hat], axis=1)               # [T, 192]
+        v = c_hat @ w_uv[h]                                                     # [T, 128]
+        q = np.concatenate([q_nope[:, h], q_pe[:, h]], axis=1)                  # [n, 192]
+        s = np.where(allowed, (q @ k.T) * softmax_scale, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        outs.append((e @ v) / e.sum(axis=1, keepdims=True))
+        lses.append(m[:, 0] + np.log(e.sum(axis=1)))
+    return np.stack(outs, axis=1), np.stack(lses, axis=1)
 
 
 # ---------------------------------------------------------------------------

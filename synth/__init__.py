@@ -15,7 +15,9 @@ the workload description):
   per layer whose mu and sigma are multiplied by 20;
 * k_pe[t] = RoPE(z, position t): pairs (i, i + 32), base 10000, rotation
   done in fp32 with tabulated fp32 cos / sin;
-* q_nope, q_pe = bf16(z); W_UK, W_UV = bf16(z / sqrt(512)) (variance 1/512).
+* q_nope, q_pe = bf16(z); W_UK, W_UV = bf16(z / sqrt(512)) (variance 1/512);
+  the queries of a prefill chunk come from their own streams, indexed like
+  the decode queries with the token's index in the chunk in place of b.
 
 z is an approximately standard normal variate built from a counter-based
 generator: h = mix64(key + i * GOLDEN) with the splitmix64 finaliser
@@ -38,6 +40,7 @@ KIND_MUL = 0xD1B54A32D192ED03
 
 KIND_LATENT, KIND_KPE, KIND_QNOPE, KIND_QPE, KIND_WUK, KIND_WUV, KIND_STATS = 1, 2, 3, 4, 5, 6, 7
 KIND_NEW_LATENT, KIND_NEW_KPE = 8, 9
+KIND_PRE_QNOPE, KIND_PRE_QPE = 10, 11          # queries of a prefill chunk
 
 D_C, D_R, D_NOPE, D_V = 512, 64, 128, 128
 ROPE_BASE = 10000.0
@@ -176,6 +179,25 @@ def q_nope_bf16(seed, layer, B, H):
 
 def q_pe_bf16(seed, layer, B, H):
     return normal3_bf16(seed, layer, KIND_QPE, B, H, D_R, UNIT_SCALE)
+
+
+def normal_rows_bf16(seed, layer, kind, rows, d1, d2, mul):
+    """Rows `rows` (any subset, any order) of the [*, d1, d2] grid of
+    normal3_bf16: the same values, without generating the other rows."""
+    i0 = np.asarray(rows, dtype=_U64)[:, None, None]
+    i1 = np.arange(d1, dtype=_U64)[None, :, None]
+    i2 = np.arange(d2, dtype=_U64)[None, None, :]
+    z = normal_from_hash(hash_at(stream_key(seed, layer, kind), ((i0 << _U64(10) | i1) << _U64(10)) | i2))
+    return bf16_rne(z * np.float32(mul))
+
+
+def prefill_q_nope_bf16(seed, layer, rows, H):
+    """q_nope of the prefill chunk's query tokens `rows` (index within the chunk)."""
+    return normal_rows_bf16(seed, layer, KIND_PRE_QNOPE, rows, H, D_NOPE, UNIT_SCALE)
+
+
+def prefill_q_pe_bf16(seed, layer, rows, H):
+    return normal_rows_bf16(seed, layer, KIND_PRE_QPE, rows, H, D_R, UNIT_SCALE)
 
 
 def w_uk_bf16(seed, layer, H):

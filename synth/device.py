@@ -95,6 +95,18 @@ def q_pe(seed, layer, B, H, device="cuda"):
     return t
 
 
+def prefill_q_nope(seed, layer, n, H, device="cuda"):
+    t = torch.empty((n, H, synth.D_NOPE), dtype=torch.bfloat16, device=device)
+    normal3_into(t, seed, layer, synth.KIND_PRE_QNOPE, synth.UNIT_SCALE)
+    return t
+
+
+def prefill_q_pe(seed, layer, n, H, device="cuda"):
+    t = torch.empty((n, H, synth.D_R), dtype=torch.bfloat16, device=device)
+    normal3_into(t, seed, layer, synth.KIND_PRE_QPE, synth.UNIT_SCALE)
+    return t
+
+
 def w_uk(seed, layer, H, device="cuda"):
     t = torch.empty((H, synth.D_NOPE, synth.D_C), dtype=torch.bfloat16, device=device)
     normal3_into(t, seed, layer, synth.KIND_WUK, synth.WEIGHT_SCALE)

@@ -72,6 +72,10 @@ class Workload:
             t = np.arange(self.prefill)
             self.slot_pre_host = (spare[t // 64] * 64 + t % 64).astype(np.int32)
             self.slot_pre = torch.from_numpy(self.slot_pre_host).to(device)
+            # the sequence's page list, and its chunk queries (prefill attention)
+            self.prefill_block_table = torch.from_numpy(spare.astype(np.int32)).to(device)
+            self.q_nope_pre = [sd.prefill_q_nope(seed, l, self.prefill, self.H, device) for l in range(self.L)]
+            self.q_pe_pre = [sd.prefill_q_pe(seed, l, self.prefill, self.H, device) for l in range(self.L)]
             for l in range(self.L):
                 st = sd.LayerStats(seed, l, device)
                 c = torch.empty((self.prefill, synth.D_C), dtype=torch.bfloat16, device=device)
@@ -179,6 +183,35 @@ class DecodeStep:
             mla.mla_decode_absorbed(wl.caches[l], self.q_lat, wl.q_pe[l], wl.block_table, wl.seq_lens_dev,
                                     self.workspace, self.o_lat, None if self.lse is None else self.lse[l],
                                     self.dev_err, num_splits=self.num_splits)
+            if keep_o_lat is not None:
+                keep_o_lat[l].copy_(self.o_lat)
+            mla.mla_out_unabsorb(self.o_lat, wl.w_uv[l], self.o[l])
+        return self.o
+
+
+class PrefillStep:
+    """Causal attention of the workload's prefill chunk (sequence B, positions
+    0 .. P-1) in every layer: absorb the P queries, mla_prefill_absorbed over
+    the chunk's own pages (nothing cached before it), unabsorb.  The chunk's
+    tokens must already be in the cache (a DecodeStep run appends them)."""
+
+    def __init__(self, wl):
+        dev = wl.device
+        P, H = wl.prefill, wl.H
+        self.wl = wl
+        self.q_lat = torch.empty((P, H, synth.D_C), dtype=torch.float32, device=dev)
+        self.o_lat = torch.empty((P, H, synth.D_C), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((wl.L, P, H), dtype=torch.float32, device=dev)
+        self.o = torch.empty((wl.L, P, H, synth.D_V), dtype=torch.float32, device=dev)
+        self.workspace = torch.empty(mla.mla_prefill_workspace_bytes(P, H), dtype=torch.uint8, device=dev)
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def run(self, keep_o_lat=None):
+        wl = self.wl
+        for l in range(wl.L):
+            mla.mla_q_absorb(wl.q_nope_pre[l], wl.w_uk[l], self.q_lat)
+            mla.mla_prefill_absorbed(wl.caches[l], self.q_lat, wl.q_pe_pre[l], wl.prefill_block_table, 0,
+                                     self.workspace, self.o_lat, self.lse[l], self.dev_err)
             if keep_o_lat is not None:
                 keep_o_lat[l].copy_(self.o_lat)
             mla.mla_out_unabsorb(self.o_lat, wl.w_uv[l], self.o[l])

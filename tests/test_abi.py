@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
-    assert lib.abi_version() == 101
+    assert lib.abi_version() == 102
 
 
 def test_layouts_match_the_accounting(lib):
@@ -103,4 +103,21 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert raw.mla_lse_merge(a16, a16, 5000, 2, 16, ctypes.c_void_p(0x900000), None, None) == 1
     assert raw.mla_lse_merge(a16, a16, 2, 2, 16, ctypes.c_void_p(0x10000 + 4096), None, None) == 1
     assert raw.mla_lse_merge(a16, a16, 2, 0, 16, a16, None, None) == 0
+    # prefill: n < 0, ctx_before < 0, bad heads, chunk past the block table,
+    # workspace too small, bad softmax scale, misaligned q_lat; n == 0 is a no-op
+    ws = ctypes.c_void_p(0x200000)
+    pre = lambda q, bt_pages, ctx, n, H, scale, ws_bytes: (ctypes.byref(cs), q, fake, fake, bt_pages, ctx, n, H, scale,
+                                                           ws, ws_bytes, fake, None, None, None)
+    assert raw.mla_prefill_absorbed(*pre(fake, 4, 0, -1, 16, 0.07, 1 << 40)) == 1
+    assert raw.mla_prefill_absorbed(*pre(fake, 4, -1, 8, 16, 0.07, 1 << 40)) == 1
+    assert raw.mla_prefill_absorbed(*pre(fake, 4, 0, 8, 24, 0.07, 1 << 40)) == 1
+    assert raw.mla_prefill_absorbed(*pre(fake, 4, 250, 7, 16, 0.07, 1 << 40)) == 1     # 257 > 4 pages * 64
+    assert raw.mla_prefill_absorbed(*pre(fake, 4, 0, 8, 16, 0.07, 64)) == 1
+    assert raw.mla_prefill_absorbed(*pre(fake, 4, 0, 8, 16, float("nan"), 1 << 40)) == 1
+    assert raw.mla_prefill_absorbed(*pre(ctypes.c_void_p(0x10004), 4, 0, 8, 16, 0.07, 1 << 40)) == 1
+    assert raw.mla_prefill_absorbed(*pre(None, 4, 0, 0, 16, 0.07, 0)) == 0
+    assert raw.mla_prefill_workspace_bytes(-1, 16) == 0
+    assert raw.mla_prefill_workspace_bytes(8, 24) == 0
+    assert raw.mla_prefill_workspace_bytes(100, 16) <= raw.mla_prefill_workspace_bytes(5000, 16)
+    assert raw.mla_prefill_workspace_bytes(5000, 16) == raw.mla_prefill_workspace_bytes(50000, 16)
     assert raw.mla_status_string(4) == b"device-side bounds error"

@@ -32,3 +32,13 @@ def test_reference_arm_prints_the_contract_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["config"]["workload"] == "tiny"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_prefill_flop_count():
+    """Useful flops of a prefill chunk: (query, key) pairs of the causal
+    triangle (plus ctx_before keys per query) x heads x 2 x (576 + 512)."""
+    import bench
+    assert bench.prefill_flops(1, 1) == 2 * 1088
+    assert bench.prefill_flops(2, 1) == 3 * 2 * 1088
+    assert bench.prefill_flops(2, 4, ctx_before=1) == 5 * 4 * 2 * 1088
+    assert bench.prefill_flops(8192, 64) == 8192 * 8193 // 2 * 64 * 2176

@@ -33,3 +33,7 @@ def test_queries_and_weights_match_host():
     assert np.array_equal(bits(sd.q_pe(seed, layer, 5, 64)), synth.q_pe_bf16(seed, layer, 5, 64))
     assert np.array_equal(bits(sd.w_uk(seed, layer, 16)), synth.w_uk_bf16(seed, layer, 16))
     assert np.array_equal(bits(sd.w_uv(seed, layer, 16)), synth.w_uv_bf16(seed, layer, 16))
+    rows = [0, 3, 299]
+    assert np.array_equal(bits(sd.prefill_q_nope(seed, layer, 300, 16))[rows],
+                          synth.prefill_q_nope_bf16(seed, layer, rows, 16))
+    assert np.array_equal(bits(sd.prefill_q_pe(seed, layer, 300, 64))[rows], synth.prefill_q_pe_bf16(seed, layer, rows, 64))

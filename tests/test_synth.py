@@ -48,3 +48,14 @@ def test_rope_preserves_pair_norms():
     key = synth.stream_key(1, 0, synth.KIND_KPE)
     raw = synth.normal_from_hash(synth.hash_at(key, synth.token_index(0, np.arange(1), np.arange(64))))
     assert np.array_equal(z[0], synth.bf16_to_f32(synth.bf16_rne(raw[0])))
+
+
+def test_row_subset_matches_full_grid():
+    """normal_rows_bf16 gives exactly the selected rows of normal3_bf16."""
+    full = synth.normal3_bf16(4, 2, synth.KIND_PRE_QNOPE, 40, 16, synth.D_NOPE, synth.UNIT_SCALE)
+    rows = [39, 0, 17, 17, 5]
+    assert np.array_equal(synth.prefill_q_nope_bf16(4, 2, rows, 16), full[rows])
+    pe = synth.normal3_bf16(4, 2, synth.KIND_PRE_QPE, 40, 16, synth.D_R, synth.UNIT_SCALE)
+    assert np.array_equal(synth.prefill_q_pe_bf16(4, 2, rows, 16), pe[rows])
+    # the prefill queries are streams of their own, not the decode queries
+    assert not np.array_equal(full[:5], synth.q_nope_bf16(4, 2, 5, 16))
