@@ -74,6 +74,143 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* cum, int B, int64_t c
   return lo;
 }
 
+// Dequantizes tokens t0 .. t0 + 31 of sequence b (one 32-token block of a
+// page) into s_c [32][kCS] and s_k [32][kKS], exactly as the oracle defines
+// x_hat; tokens at or past len, or on a page id outside the pool (reported),
+// read as 0.  s_valid, s_page: [32] scratch.  All NT threads of the block
+// take part; the caller synchronizes before reading s_c / s_k.
+template <int LF, int KF, int NT>
+__device__ void dequant_chunk(const DecodeParams& p, int b, int t0, int len, float* s_c, float* s_k,
+                              int32_t* s_valid, int32_t* s_page) {
+  const int tid = threadIdx.x;
+  const uint8_t* pool = p.pool;
+  const int64_t pb = p.L.page_bytes;
+  if (tid < kChunk) {
+    const int t = t0 + tid;
+    int valid = t < len;
+    int page = 0;
+    if (valid) {
+      page = p.block_table[(size_t)b * p.bt_stride + (t >> 6)];
+      if (page < 0 || page >= p.num_pages) {
+        set_err(p.dev_err, MLA_DEVERR_PAGE);
+        valid = 0;
+      }
+    }
+    s_valid[tid] = valid;
+    s_page[tid] = page;
+  }
+  __syncthreads();
+
+  // ---- dequantize the chunk into shared memory (x_hat exactly as defined).
+  // A chunk is one 32-token block of a page; t is the token in the block.
+  const int64_t blk_off = (int64_t)((t0 >> 5) & 1) * p.L.block_bytes;
+  if (LF == MLA_FMT_BF16) {
+    for (int i = tid; i < kChunk * (kDc / 2); i += NT) {
+      const int t = i / (kDc / 2), pr = i % (kDc / 2);
+      float a = 0.f, bb = 0.f;
+      if (s_valid[t]) {
+        const uint32_t w = reinterpret_cast<const uint32_t*>(
+            pool + s_page[t] * pb + blk_off + p.L.codes_off + (int64_t)t * p.L.codes_row)[
+            latent_chunk_pos(pr >> 2, t) * 4 + (pr & 3)];
+        a = bf16lo(w);
+        bb = bf16hi(w);
+      }
+      s_c[t * kCS + 2 * pr] = a;
+      s_c[t * kCS + 2 * pr + 1] = bb;
+    }
+  } else if (is_int8_latent(LF)) {
+    for (int i = tid; i < kChunk * (kDc / 4); i += NT) {
+      const int t = i / (kDc / 4), wi = i % (kDc / 4);
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      // channel of byte j of word wi (8-channel groups store 2jj, 2jj+1,
+      // 8+2jj, 8+2jj+1 in word jj of a 16-channel chunk)
+      int ch[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ch[j] = latent_group_size(LF) == 8 ? 16 * (wi >> 2) + 2 * (wi & 3) + (j & 1) + 8 * (j >> 1) : 4 * wi + j;
+      if (s_valid[t]) {
+        const uint8_t* blk = pool + s_page[t] * pb + blk_off;
+        const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.codes_off + (int64_t)t * p.L.codes_row)[
+            latent_chunk_pos(wi >> 2, t) * 4 + (wi & 3)];
+        const float* sc = reinterpret_cast<const float*>(blk + p.L.scale_off);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), sc[(ch[j] / latent_group_size(LF)) * kBlockTokens + t]);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s_c[t * kCS + ch[j]] = v[j];
+    }
+  } else {
+    for (int i = tid; i < kChunk * (kDc / 8); i += NT) {
+      const int t = i / (kDc / 8), pw = i % (kDc / 8);
+      const int c = latent_chunk_pos(pw >> 2, t), j = pw & 3;   // logical chunk of this stored word
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (s_valid[t]) {
+        const uint8_t* blk = pool + s_page[t] * pb + blk_off;
+        const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.codes_off + (int64_t)t * p.L.codes_row)[pw];
+        const float* sc = reinterpret_cast<const float*>(blk + p.L.scale_off);
+        const float* zp = reinterpret_cast<const float*>(blk + p.L.zero_off);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int g = 2 * c + (int4_nibble_channel(j, k) >> 4);
+          const float zero = LF == MLA_FMT_INT4_SYM ? 8.f : zp[g * kBlockTokens + t];
+          v[k] = __fmul_rn(__fsub_rn((float)((w >> (4 * k)) & 15u), zero), sc[g * kBlockTokens + t]);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s_c[t * kCS + 32 * c + int4_nibble_channel(j, k)] = v[k];
+    }
+  }
+  if (KF == MLA_FMT_BF16) {
+    for (int i = tid; i < kChunk * (kDr / 2); i += NT) {
+      const int t = i / (kDr / 2), pr = i % (kDr / 2);
+      float a = 0.f, bb = 0.f;
+      if (s_valid[t]) {
+        const uint32_t w = reinterpret_cast<const uint32_t*>(
+            pool + s_page[t] * pb + blk_off + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[
+            kpe_chunk_pos(pr >> 2, t, KF) * 4 + (pr & 3)];
+        a = bf16lo(w);
+        bb = bf16hi(w);
+      }
+      s_k[t * kKS + 2 * pr] = a;
+      s_k[t * kKS + 2 * pr + 1] = bb;
+    }
+  } else if (KF == MLA_FMT_INT4_SYM) {
+    for (int i = tid; i < kChunk * (kDr / 8); i += NT) {
+      const int t = i / (kDr / 8), pw = i % (kDr / 8);
+      const int c = kpe_chunk_pos(pw >> 2, t, KF), j = pw & 3;   // logical chunk of this stored word
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (s_valid[t]) {
+        const uint8_t* blk = pool + s_page[t] * pb + blk_off;
+        const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[pw];
+        const float* sc = reinterpret_cast<const float*>(blk + p.L.kpe_scale_off);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int ch = 32 * c + int4_nibble_channel(j, k);
+          v[k] = __fmul_rn(__fsub_rn((float)((w >> (4 * k)) & 15u), 8.f), sc[(ch >> 3) * kBlockTokens + t]);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s_k[t * kKS + 32 * c + int4_nibble_channel(j, k)] = v[k];
+    }
+  } else {
+    for (int i = tid; i < kChunk * (kDr / 4); i += NT) {
+      const int t = i / (kDr / 4), wi = i % (kDr / 4);
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (s_valid[t]) {
+        const uint8_t* blk = pool + s_page[t] * pb + blk_off;
+        const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[
+            kpe_chunk_pos(wi >> 2, t, KF) * 4 + (wi & 3)];
+        const float s = reinterpret_cast<const float*>(blk + p.L.kpe_scale_off)[(wi >> 1) * kBlockTokens + t];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), s);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s_k[t * kKS + 4 * wi + j] = v[j];
+    }
+  }
+}
+
 template <int LF, int KF>
 __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
   pdl_launch_dependents();
@@ -105,8 +242,6 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
   if (x >= Ge) return;
   const int64_t c_lo = range_lo(C, x, Ge), c_end = range_lo(C, x + 1, Ge);
   int64_t c = c_lo;
-  const uint8_t* pool = p.pool;
-  const int64_t pb = p.L.page_bytes;
 
   while (c < c_end) {
     const int b = seq_of_chunk(cum, p.B, c);
@@ -129,130 +264,7 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
 
     for (int64_t ch = c - cum[b]; ch < seg_end - cum[b]; ++ch) {
       const int t0 = (int)ch * kChunk;
-      if (tid < kChunk) {
-        const int t = t0 + tid;
-        int valid = t < len;
-        int page = 0;
-        if (valid) {
-          page = p.block_table[(size_t)b * p.bt_stride + (t >> 6)];
-          if (page < 0 || page >= p.num_pages) {
-            set_err(p.dev_err, MLA_DEVERR_PAGE);
-            valid = 0;
-          }
-        }
-        s_valid[tid] = valid;
-        s_page[tid] = page;
-      }
-      __syncthreads();
-
-      // ---- dequantize the chunk into shared memory (x_hat exactly as defined).
-      // A chunk is one 32-token block of a page; t is the token in the block.
-      const int64_t blk_off = (int64_t)((t0 >> 5) & 1) * p.L.block_bytes;
-      if (LF == MLA_FMT_BF16) {
-        for (int i = tid; i < kChunk * (kDc / 2); i += kThreads) {
-          const int t = i / (kDc / 2), pr = i % (kDc / 2);
-          float a = 0.f, bb = 0.f;
-          if (s_valid[t]) {
-            const uint32_t w = reinterpret_cast<const uint32_t*>(
-                pool + s_page[t] * pb + blk_off + p.L.codes_off + (int64_t)t * p.L.codes_row)[
-                latent_chunk_pos(pr >> 2, t) * 4 + (pr & 3)];
-            a = bf16lo(w);
-            bb = bf16hi(w);
-          }
-          s_c[t * kCS + 2 * pr] = a;
-          s_c[t * kCS + 2 * pr + 1] = bb;
-        }
-      } else if (is_int8_latent(LF)) {
-        for (int i = tid; i < kChunk * (kDc / 4); i += kThreads) {
-          const int t = i / (kDc / 4), wi = i % (kDc / 4);
-          float v[4] = {0.f, 0.f, 0.f, 0.f};
-          // channel of byte j of word wi (8-channel groups store 2jj, 2jj+1,
-          // 8+2jj, 8+2jj+1 in word jj of a 16-channel chunk)
-          int ch[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            ch[j] = latent_group_size(LF) == 8 ? 16 * (wi >> 2) + 2 * (wi & 3) + (j & 1) + 8 * (j >> 1) : 4 * wi + j;
-          if (s_valid[t]) {
-            const uint8_t* blk = pool + s_page[t] * pb + blk_off;
-            const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.codes_off + (int64_t)t * p.L.codes_row)[
-                latent_chunk_pos(wi >> 2, t) * 4 + (wi & 3)];
-            const float* sc = reinterpret_cast<const float*>(blk + p.L.scale_off);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), sc[(ch[j] / latent_group_size(LF)) * kBlockTokens + t]);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) s_c[t * kCS + ch[j]] = v[j];
-        }
-      } else {
-        for (int i = tid; i < kChunk * (kDc / 8); i += kThreads) {
-          const int t = i / (kDc / 8), pw = i % (kDc / 8);
-          const int c = latent_chunk_pos(pw >> 2, t), j = pw & 3;   // logical chunk of this stored word
-          float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (s_valid[t]) {
-            const uint8_t* blk = pool + s_page[t] * pb + blk_off;
-            const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.codes_off + (int64_t)t * p.L.codes_row)[pw];
-            const float* sc = reinterpret_cast<const float*>(blk + p.L.scale_off);
-            const float* zp = reinterpret_cast<const float*>(blk + p.L.zero_off);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int g = 2 * c + (int4_nibble_channel(j, k) >> 4);
-              const float zero = LF == MLA_FMT_INT4_SYM ? 8.f : zp[g * kBlockTokens + t];
-              v[k] = __fmul_rn(__fsub_rn((float)((w >> (4 * k)) & 15u), zero), sc[g * kBlockTokens + t]);
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) s_c[t * kCS + 32 * c + int4_nibble_channel(j, k)] = v[k];
-        }
-      }
-      if (KF == MLA_FMT_BF16) {
-        for (int i = tid; i < kChunk * (kDr / 2); i += kThreads) {
-          const int t = i / (kDr / 2), pr = i % (kDr / 2);
-          float a = 0.f, bb = 0.f;
-          if (s_valid[t]) {
-            const uint32_t w = reinterpret_cast<const uint32_t*>(
-                pool + s_page[t] * pb + blk_off + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[
-                kpe_chunk_pos(pr >> 2, t, KF) * 4 + (pr & 3)];
-            a = bf16lo(w);
-            bb = bf16hi(w);
-          }
-          s_k[t * kKS + 2 * pr] = a;
-          s_k[t * kKS + 2 * pr + 1] = bb;
-        }
-      } else if (KF == MLA_FMT_INT4_SYM) {
-        for (int i = tid; i < kChunk * (kDr / 8); i += kThreads) {
-          const int t = i / (kDr / 8), pw = i % (kDr / 8);
-          const int c = kpe_chunk_pos(pw >> 2, t, KF), j = pw & 3;   // logical chunk of this stored word
-          float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          if (s_valid[t]) {
-            const uint8_t* blk = pool + s_page[t] * pb + blk_off;
-            const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[pw];
-            const float* sc = reinterpret_cast<const float*>(blk + p.L.kpe_scale_off);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int ch = 32 * c + int4_nibble_channel(j, k);
-              v[k] = __fmul_rn(__fsub_rn((float)((w >> (4 * k)) & 15u), 8.f), sc[(ch >> 3) * kBlockTokens + t]);
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) s_k[t * kKS + 32 * c + int4_nibble_channel(j, k)] = v[k];
-        }
-      } else {
-        for (int i = tid; i < kChunk * (kDr / 4); i += kThreads) {
-          const int t = i / (kDr / 4), wi = i % (kDr / 4);
-          float v[4] = {0.f, 0.f, 0.f, 0.f};
-          if (s_valid[t]) {
-            const uint8_t* blk = pool + s_page[t] * pb + blk_off;
-            const uint32_t w = reinterpret_cast<const uint32_t*>(blk + p.L.kpe_off + (int64_t)t * p.L.kpe_row)[
-                kpe_chunk_pos(wi >> 2, t, KF) * 4 + (wi & 3)];
-            const float s = reinterpret_cast<const float*>(blk + p.L.kpe_scale_off)[(wi >> 1) * kBlockTokens + t];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), s);
-          }
-#pragma unroll
-          for (int j = 0; j < 4; ++j) s_k[t * kKS + 4 * wi + j] = v[j];
-        }
-      }
+      dequant_chunk<LF, KF, kThreads>(p, b, t0, len, s_c, s_k, s_valid, s_page);
       __syncthreads();
 
       // ---- scores: thread -> head tid/16, tokens 2*(tid%16) and +1
@@ -371,9 +383,79 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
   return v;
 }
 
-__global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams p) {
+// Sequences shorter than kExactLen tokens skip the split partials: the
+// combine recomputes their attention from the cache in fp32.  Over so few
+// tokens the split kernel's fp16 products P * s (fp16 P, fp16 group scale)
+// do not average out; with a peaked softmax they reach the 2e-3 bound, while
+// over 256 and more tokens they stay near 3e-4.
+constexpr int kExactLen = 256;
+constexpr int kShortSmemBytes =
+    (int)sizeof(float) * (kChunk * kCS + kChunk * kKS + kDc + kDr + kChunk + kDc) + (int)sizeof(int32_t) * 2 * kChunk;
+
+// Attention of (sequence b, head h) over its len < kExactLen tokens, in
+// fp32, straight from the cache: per 32-token block, dequantize into shared
+// memory, one warp per token for the scores (log2 domain), then an online
+// softmax in which thread (c, half) accumulates channel c over the tokens of
+// parity half.  sm: kShortSmemBytes of shared memory.
+template <int LF, int KF>
+__device__ __noinline__ void short_exact(const DecodeParams& p, int b, int h, int len, float* sm) {
+  float* s_c = sm;                       // [32][kCS]
+  float* s_k = s_c + kChunk * kCS;       // [32][kKS]
+  float* s_q = s_k + kChunk * kKS;       // [512]
+  float* s_qp = s_q + kDc;               // [64]
+  float* s_s = s_qp + kDr;               // [32] scores
+  float* s_o = s_s + kChunk;             // [512] the odd tokens' sums
+  int32_t* s_valid = reinterpret_cast<int32_t*>(s_o + kDc);   // [32]
+  int32_t* s_page = s_valid + kChunk;                          // [32]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t row = (size_t)b * p.H + h;
+  for (int i = tid; i < kDc; i += kCombThreads) s_q[i] = p.q_lat[row * kDc + i];
+  for (int i = tid; i < kDr; i += kCombThreads) s_qp[i] = bf16f(p.q_pe[row * kDr + i]);
+  const int c = tid & (kDc - 1), half = tid / kDc;
+  float m = -INFINITY, l = 0.f, o = 0.f;
+  for (int t0 = 0; t0 < len; t0 += kChunk) {
+    __syncthreads();                     // the previous block's readers are done; s_q, s_qp in place
+    dequant_chunk<LF, KF, kCombThreads>(p, b, t0, len, s_c, s_k, s_valid, s_page);
+    __syncthreads();
+    {
+      const float* cr = s_c + warp * kCS;
+      const float* kr = s_k + warp * kKS;
+      float a = 0.f;
+      for (int i = lane; i < kDc; i += 32) a = fmaf(s_q[i], cr[i], a);
+      for (int i = lane; i < kDr; i += 32) a = fmaf(s_qp[i], kr[i], a);
+#pragma unroll
+      for (int off = 16; off; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+      if (lane == 0) s_s[warp] = (t0 + warp < len && s_valid[warp]) ? a * p.scale_log2 : -INFINITY;
+    }
+    __syncthreads();
+    float mx = -INFINITY;
+    for (int t = 0; t < kChunk; ++t) mx = fmaxf(mx, s_s[t]);
+    const float mn = fmaxf(m, mx);
+    if (mn == -INFINITY) continue;       // nothing valid yet
+    const float al = exp2f(m - mn);
+    float lsum = 0.f, acc = 0.f;
+    for (int t = 0; t < kChunk; ++t) {
+      const float w = exp2f(s_s[t] - mn);
+      lsum += w;
+      if ((t & 1) == half) acc = fmaf(w, s_c[t * kCS + c], acc);
+    }
+    l = l * al + lsum;
+    o = o * al + acc;
+    m = mn;
+  }
+  __syncthreads();
+  if (half) s_o[c] = o;
+  __syncthreads();
+  if (half) return;
+  p.o_lat[row * kDc + c] = l > 0.f ? (o + s_o[c]) / l : 0.f;
+  if (p.lse && c == 0) p.lse[row] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+}
+
+template <int LF, int KF>
+__global__ void __launch_bounds__(kCombThreads, 2) combine_kernel(DecodeParams p) {
   pdl_launch_dependents();
   pdl_wait();
+  extern __shared__ __align__(16) float short_smem[];
   __shared__ float sw[kCombSlots];
   __shared__ float red[kCombThreads / 32];
   __shared__ float4 parts[kCombParts - 1][kDc / 4];
@@ -384,6 +466,11 @@ __global__ void __launch_bounds__(kCombThreads) combine_kernel(DecodeParams p) {
   if (cum[b] == cum[b + 1]) {
     if (part == 0) *out = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
+    return;
+  }
+  const int len = checked_len(p, b, false);
+  if (len < kExactLen) {
+    short_exact<LF, KF>(p, b, h, len, short_smem);
     return;
   }
   const int x0 = p.ws.span[2 * b], S = p.ws.span[2 * b + 1] - x0 + 1;
@@ -480,12 +567,54 @@ mla_status launch_decode_ref(const DecodeParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+namespace {
+
+template <int LF, int KF>
+mla_status launch_combine_t(const DecodeParams& p, cudaStream_t stream) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    const mla_status st = cuda_status(
+        cudaFuncSetAttribute(combine_kernel<LF, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, kShortSmemBytes));
+    if (st != MLA_OK) return st;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  return cuda_status(
+      launch_pdl(combine_kernel<LF, KF>, dim3(p.B, p.H), dim3(kCombThreads), kShortSmemBytes, stream, p));
+}
+
+mla_status launch_combine(const DecodeParams& p, cudaStream_t stream) {
+#define MLA_COMBINE_CASE(A, K) \
+  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_combine_t<A, K>(p, stream);
+  MLA_COMBINE_CASE(MLA_FMT_BF16, MLA_FMT_BF16)
+  MLA_COMBINE_CASE(MLA_FMT_BF16, MLA_FMT_INT8_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_BF16)
+  MLA_COMBINE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT8_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_BF16)
+  MLA_COMBINE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT8_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT4_SYM, MLA_FMT_BF16)
+  MLA_COMBINE_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT8_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_BF16, MLA_FMT_INT4_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT4_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT4_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT4_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT8_G8, MLA_FMT_INT8_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT8_G32, MLA_FMT_INT8_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT8_G64, MLA_FMT_INT8_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM)
+#undef MLA_COMBINE_CASE
+  return MLA_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
 mla_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
   static const bool force_ref = getenv("MLA_DEBUG_REFERENCE_DECODE") != nullptr;
   mla_status st = force_ref ? MLA_ERR_UNSUPPORTED : launch_decode_mma(p, stream);
   if (st == MLA_ERR_UNSUPPORTED) st = launch_decode_ref(p, stream);
   if (st != MLA_OK) return st;
-  return cuda_status(launch_pdl(combine_kernel, dim3(p.B, p.H), dim3(kCombThreads), 0, stream, p));
+  return launch_combine(p, stream);
 }
 
 }  // namespace mla

@@ -34,11 +34,8 @@
 //    one chunk behind QK^T, so a compute warp's QK^T of chunk i overlaps
 //    the softmax of chunk i - 1.  P * s is one fp16 product of fp16 P and
 //    fp16 s; over long contexts its roundings average out (~3e-4 of the
-//    output), but a sequence of a few dozen tokens with a peaked softmax can
-//    reach the 2e-3 bound.  A CTA whose chunks touch a sequence shorter than
-//    kExactPvLen therefore runs a second instance of the loop (kept out of
-//    line) that carries P * s as an fp16 (hi, lo) pair: two MMAs per step,
-//    P's own rounding the only one left.
+//    output).  Sequences shorter than 256 tokens, where they need not, are
+//    recomputed exactly by the combine kernel (decode.cu).
 //  * bf16 latent: q_lat is split into bf16 hi + lo against the exact bf16
 //    values, one accumulator over all groups, P split into bf16 hi + lo.
 #include <cuda_fp16.h>
@@ -55,10 +52,6 @@ constexpr int kThreads = kCW * 32;
 constexpr int kHT = 16;                        // heads per CTA
 constexpr int kPStride = 40;                   // row stride (16-bit elements) of the P tile: 80 B, conflict-free ldmatrix
 constexpr int kXStride = 20;                   // row stride (float2) of a warp's partial-score tile: 160 B, conflict-free
-// A CTA whose chunks touch a sequence shorter than this takes the exact PV
-// scaling (see pv_chunk): few tokens share the softmax weight there, so the
-// fp16 roundings of P * s do not average out.
-constexpr int kExactPvLen = 256;
 
 template <int LF, int KF>
 struct Fmt {
@@ -84,12 +77,7 @@ struct Fmt {
   static constexpr int kStages = kBlock <= 24 * 1024 ? 6 : (kBlock <= 40 * 1024 ? 4 : 3);
   static constexpr int kXPartBytes = 2 * kCW * kHT * kXStride * 8;   // partial scores [buf][warp][row][pair]
   static constexpr int kPBytes = 4 * kHT * kPStride * 2;              // P tiles [buf][hi, lo]
-  // fp16 (hi, lo) scale pairs of the exact PV path: [warp][buf][group][ntile][j]
-  // (bf16 has no scales; 8-channel blocks scale the operands instead)
-  static constexpr bool kExactPv = !kLatBf16 && !kLatG8;
-  static constexpr int kPvsBytes = kExactPv ? kCW * 2 * 64 * 8 : 0;
-  static constexpr int kFixed = kStages * kBlock + kXPartBytes + kPBytes + kPvsBytes + (2 * kHT + kCW) * 4 +
-                                kStages * 8 + kStages * 4;
+  static constexpr int kFixed = kStages * kBlock + kXPartBytes + kPBytes + (2 * kHT + kCW) * 4 + kStages * 8 + kStages * 4;
 };
 
 // ---------------------------------------------------------------------------
@@ -208,18 +196,6 @@ __device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cas
 __device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
 __device__ __forceinline__ uint32_t pack_f16(float a, float b) { return h2_bits(__floats2half2_rn(a, b)); }
-
-// A = P * s for PV as an fp16 pair: hi = P * s_hi rounded once; lo = the
-// exact residual of that product (a fused multiply-add of two 11-bit
-// significands is exact) plus P * s_lo, rounded once.  s = (s_hi, s_lo) holds
-// the fp32 scale to 22 bits, so hi + lo carries P * s with P's own rounding
-// only.
-__device__ __forceinline__ void scaled_split(uint32_t p, uint2 s, uint32_t& hi, uint32_t& lo) {
-  const __half2 ph = bits_h2(p), sh = bits_h2(s.x), sl = bits_h2(s.y);
-  const __half2 h = __hmul2(ph, sh);
-  hi = h2_bits(h);
-  lo = h2_bits(__hfma2(ph, sl, __hfma2(ph, sh, __hneg2(h))));
-}
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   uint32_t r;
@@ -414,13 +390,10 @@ __device__ __forceinline__ void finish_query(const QueryRaw& raw, float up, Quer
 // (exact codes, or code - zero) into bq, the fp16 PV scale pairs into s2h,
 // and the warp's partial scores (QK^T over its channels plus its k_pe part)
 // into acc [ntile][C fragment].  st: the chunk's block in shared memory;
-// nv: its valid tokens.  kEx: the PV scale pairs go to pvs (the warp's
-// [group][ntile][j] tile for this chunk) as fp16 (hi, lo) splits instead of
-// s2h.
-template <int LF, int KF, bool kEx>
+// nv: its valid tokens.
+template <int LF, int KF>
 __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int lane, const Query& q,
-                                         uint32_t (&bq)[4][4][2], uint32_t (&s2h)[4][4], float (&acc)[4][4],
-                                         uint2* pvs) {
+                                         uint32_t (&bq)[4][4][2], uint32_t (&s2h)[4][4], float (&acc)[4][4]) {
   using F = Fmt<LF, KF>;
   const int r = lane >> 2, j = lane & 3;
   const bool partial = nv < kChunk;     // includes nv == 0 (no data: everything is masked)
@@ -579,19 +552,9 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
           const float2 s2 = *reinterpret_cast<const float2*>(sc + si * kBlockTokens + 8 * n + 2 * j);
           scale_acc(acc[n], d[n], s2);
           const uint32_t sh = pack_f16(s2.x, s2.y) & mc[n];
-          if (kEx) {
-            if (r == 0) {
-              const float2 hb = __half22float2(bits_h2(sh));
-              const uint2 e = make_uint2(sh, pack_f16(s2.x - hb.x, s2.y - hb.y) & mc[n]);
 #pragma unroll
-              for (int g2 = 0; g2 < 4; ++g2)
-                if (g2 <= g && g2 > g - F::kSPG) pvs[(4 * g2 + n) * 4 + j] = e;
-            }
-          } else {
-#pragma unroll
-            for (int g2 = 0; g2 < 4; ++g2)
-              if (g2 <= g && g2 > g - F::kSPG) s2h[g2][n] = sh;
-          }
+          for (int g2 = 0; g2 < 4; ++g2)
+            if (g2 <= g && g2 > g - F::kSPG) s2h[g2][n] = sh;
         }
       }
     }
@@ -619,16 +582,12 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
 
 // Step C of one chunk for warp w: rescale o by the chunk's alpha and add
 // P V with the operands bqv / scales s2v kept from its step A.  alpha_s:
-// [2][16]; ptab: the P tiles [2 buf][hi, lo][16][kPStride].  kEx: P * s goes
-// in as an fp16 (hi, lo) pair built from the split scales step A left in pvs
-// (two MMAs per step), not as one fp16 product of fp16 P and fp16 s.
-template <int LF, int KF, bool kEx>
+// [2][16]; ptab: the P tiles [2 buf][hi, lo][16][kPStride].
+template <int LF, int KF>
 __device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha_s, const uint16_t* ptab, int buf,
-                                         const uint32_t (&bqv)[4][4][2], const uint32_t (&s2v)[4][4], int lane,
-                                         const uint2* pvs) {
+                                         const uint32_t (&bqv)[4][4][2], const uint32_t (&s2v)[4][4], int lane) {
   using F = Fmt<LF, KF>;
-  const int r = lane >> 2, j = lane & 3;
-  if (kEx) __syncwarp();        // the pvs entries were written by the warp's r == 0 lanes
+  const int r = lane >> 2;
     {
     const float al0 = alpha_s[buf * kHT + r], al1 = alpha_s[buf * kHT + r + 8];
     if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
@@ -676,18 +635,6 @@ __device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha
         // the operands already carry their 8-channel group's scale
 #pragma unroll
         for (int e = 0; e < 2; ++e) mma_f16(o[g][e], pa[0][ks], vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
-      } else if (kEx) {
-        const uint2 e0 = pvs[(4 * g + 2 * ks) * 4 + j], e1 = pvs[(4 * g + 2 * ks + 1) * 4 + j];
-        uint32_t ah[4], al[4];
-        scaled_split(pa[0][ks][0], e0, ah[0], al[0]);
-        scaled_split(pa[0][ks][1], e0, ah[1], al[1]);
-        scaled_split(pa[0][ks][2], e1, ah[2], al[2]);
-        scaled_split(pa[0][ks][3], e1, ah[3], al[3]);
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          mma_f16(o[g][e], ah, vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
-          mma_f16(o[g][e], al, vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
-        }
       } else {
         // A = P scaled per token (column) by the group's scale
         uint32_t ag[4];
@@ -722,175 +669,25 @@ constexpr int kWsExtra = 5 * 8 + 4 * 4;     // bx[2], bp[2], qa; nvq[2], cwq[2]
 __device__ __forceinline__ void ws_regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory"); }
 __device__ __forceinline__ void ws_regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory"); }
 
-// The kernel's shared-memory carve (F = Fmt<LF, KF> in scope): stages,
-// partial scores [2][8 warps][16 rows][kXStride], P tiles [2 buf][hi, lo]
-// [16][kPStride], exact-PV scale pairs [warp][buf][64], alpha [2][16], query
-// amax [8], the stage barriers, bx[2], bp[2], qa, per-stage valid counts,
-// nv[2], score scale [2], chunk prefix sums.  Spelled out wherever it is
-// needed, so that every pointer visibly derives from the shared array.
-#define MLA_DECODE_SMEM_CARVE \
-  extern __shared__ __align__(1024) uint8_t smem[]; \
-  uint8_t* stages = smem; \
-  float2* xpart = reinterpret_cast<float2*>(smem + F::kStages * F::kBlock); \
-  uint16_t* ptab = reinterpret_cast<uint16_t*>(xpart + 2 * kCW * kHT * kXStride); \
-  uint2* pvs = reinterpret_cast<uint2*>(ptab + 4 * kHT * kPStride); \
-  float* alpha_s = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(pvs) + F::kPvsBytes); \
-  float* amax_s = alpha_s + 2 * kHT; \
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(amax_s + kCW); \
-  uint64_t* bx = full_bar + F::kStages; \
-  uint64_t* bp = bx + 2; \
-  uint64_t* qa = bp + 2; \
-  int32_t* meta = reinterpret_cast<int32_t*>(qa + 1); \
-  int32_t* nvq = meta + F::kStages; \
-  float* cwq = reinterpret_cast<float*>(nvq + 2); \
-  int32_t* cum = reinterpret_cast<int32_t*>(cwq + 2); \
-  (void)0
-
-// The compute warps' loop over the CTA's chunks [c_lo, c_hi): QK^T of chunk
-// i, hand-in of its partial scores, PV of chunk i - 1.  kEx selects the exact
-// PV scaling.
-template <int LF, int KF, bool kEx>
-__device__ __forceinline__ void compute_loop(const DecodeParams& p, int c_lo, int c_hi) {
-  using F = Fmt<LF, KF>;
-  MLA_DECODE_SMEM_CARVE;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int x = blockIdx.x, h0 = blockIdx.y * kHT;
-  const int w = warp, r = lane >> 2, j = lane & 3;
-  Query q;
-  float cw = 0.f;
-  float o[4][2][4];
-  ChunkRegs ra, rb;
-  bool pending = false;
-  int b = -1, s = 0, i = 0;
-  uint32_t phase = 0, qphase = 0;
-  bool dead = false;
-
-  auto flush_o = [&](int bb) {
-    const size_t slot = (size_t)x + bb;
-    if (tid == 0 && blockIdx.y == 0) {
-      if (c_lo <= cum[bb]) p.ws.span[2 * bb] = x;
-      if (c_hi >= cum[bb + 1]) p.ws.span[2 * bb + 1] = x;
-    }
-    float* o0 = p.ws.o + (slot * p.H + h0 + r) * kDc;
-    float* o1 = o0 + 8 * kDc;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const int base = 16 * (4 * w + g);
-      if (F::kStdLayout) {
-        *reinterpret_cast<float2*>(o0 + base + 2 * j) = make_float2(o[g][0][0], o[g][0][1]);
-        *reinterpret_cast<float2*>(o0 + base + 8 + 2 * j) = make_float2(o[g][1][0], o[g][1][1]);
-        *reinterpret_cast<float2*>(o1 + base + 2 * j) = make_float2(o[g][0][2], o[g][0][3]);
-        *reinterpret_cast<float2*>(o1 + base + 8 + 2 * j) = make_float2(o[g][1][2], o[g][1][3]);
-      } else {
-        *reinterpret_cast<float4*>(o0 + base + 4 * j) = make_float4(o[g][0][0], o[g][0][1], o[g][1][0], o[g][1][1]);
-        *reinterpret_cast<float4*>(o1 + base + 4 * j) = make_float4(o[g][0][2], o[g][0][3], o[g][1][2], o[g][1][3]);
-      }
-    }
-  };
-  // C of the previous chunk: wait for its P, then accumulate
-  auto finish_prev = [&](const ChunkRegs& prev) -> bool {
-    if (!pending) return true;
-    const int pi = i - 1;
-    if (!mbar_wait(smem_u32(&bp[pi & 1]), (uint32_t)((pi >> 1) & 1))) {
-      set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
-      return false;
-    }
-    pv_chunk<LF, KF, kEx>(o, alpha_s, ptab, pi & 1, prev.bq, prev.s2h, lane, pvs + (2 * w + (pi & 1)) * 64);
-    pending = false;
-    return true;
-  };
-
-  auto chunk_step = [&](int c, ChunkRegs& cur, ChunkRegs& prev) -> bool {
-    int nb = b < 0 ? seq_of_chunk(cum, p.B, c) : b;
-    while (cum[nb + 1] <= c) ++nb;
-    if (nb != b) {
-      if (!finish_prev(prev)) return false;
-      if (b >= 0) flush_o(b);
-      b = nb;
-      QueryRaw raw;
-      const float am = warp_max(load_query_raw<LF, KF>(p, b, h0, w, lane, raw));
-      if (lane == 0) amax_s[w] = am;
-      mbar_arrive(smem_u32(qa));
-      if (!mbar_wait(smem_u32(qa), qphase)) {
-        set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
-        return false;
-      }
-      qphase ^= 1u;
-      float amx = 0.f;
-#pragma unroll
-      for (int k = 0; k < kCW; ++k) amx = fmaxf(amx, amax_s[k]);
-      int ex = 0;
-      if (!F::kLatBf16 && amx > 0.f && isfinite(amx)) {
-        ex = 14 - ilogbf(amx);
-        ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
-      }
-      finish_query<LF, KF>(raw, __int_as_float((127 + ex) << 23), q);
-      cw = p.scale_log2 * __int_as_float((127 - ex) << 23);
-#pragma unroll
-      for (int g = 0; g < 4; ++g)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
-    }
-    if (!mbar_wait(smem_u32(&full_bar[s]), phase)) {
-      set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
-      return false;
-    }
-    const int nv = meta[s];
-    float acc[4][4];
-    qk_chunk<LF, KF, kEx>(stages + s * F::kBlock, nv, w, lane, q, cur.bq, cur.s2h, acc,
-                           pvs + (2 * w + (i & 1)) * 64);
-    {
-      float2* xw = xpart + (((size_t)(i & 1) * kCW + w) * kHT + r) * kXStride + j;
-#pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        xw[4 * n] = make_float2(acc[n][0], acc[n][1]);
-        xw[8 * kXStride + 4 * n] = make_float2(acc[n][2], acc[n][3]);
-      }
-    }
-    if (tid == 0) {
-      nvq[i & 1] = nv;
-      cwq[i & 1] = cw;
-    }
-    mbar_arrive(smem_u32(&bx[i & 1]));
-    if (!finish_prev(prev)) return false;
-    pending = true;
-    ++i;
-    if (++s == F::kStages) {
-      s = 0;
-      phase ^= 1u;
-    }
-    return true;
-  };
-
-  bool last_in_a = false;
-  for (int c = c_lo; c < c_hi; c += 2) {
-    if (!chunk_step(c, ra, rb)) { dead = true; break; }
-    last_in_a = true;
-    if (c + 1 >= c_hi) break;
-    if (!chunk_step(c + 1, rb, ra)) { dead = true; break; }
-    last_in_a = false;
-  }
-  if (!dead) {
-    const bool ok = last_in_a ? finish_prev(ra) : finish_prev(rb);
-    if (ok && b >= 0) flush_o(b);
-  }
-}
-
-// The exact-scaling instance out of line: it runs only in CTAs that touch a
-// short sequence, and keeps the common loop's code and registers as they are.
-template <int LF, int KF>
-__device__ __noinline__ void compute_loop_exact(DecodeParams p, int c_lo, int c_hi) {
-  compute_loop<LF, KF, true>(p, c_lo, c_hi);
-}
-
 template <int LF, int KF>
 __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams p) {
   using F = Fmt<LF, KF>;
   pdl_launch_dependents();
   pdl_wait();
-  MLA_DECODE_SMEM_CARVE;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stages = smem;
+  float2* xpart = reinterpret_cast<float2*>(smem + F::kStages * F::kBlock);   // [2][8 warps][16 rows][kXStride]
+  uint16_t* ptab = reinterpret_cast<uint16_t*>(xpart + 2 * kCW * kHT * kXStride);  // [2 buf][hi, lo][16][kPStride]
+  float* alpha_s = reinterpret_cast<float*>(ptab + 4 * kHT * kPStride);        // [2][16]
+  float* amax_s = alpha_s + 2 * kHT;                                           // [8]
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(amax_s + kCW);
+  uint64_t* bx = full_bar + F::kStages;                                        // [2]
+  uint64_t* bp = bx + 2;                                                       // [2]
+  uint64_t* qa = bp + 2;                                                       // [1]
+  int32_t* meta = reinterpret_cast<int32_t*>(qa + 1);
+  int32_t* nvq = meta + F::kStages;                                            // [2]
+  float* cwq = reinterpret_cast<float*>(nvq + 2);                              // [2]
+  int32_t* cum = reinterpret_cast<int32_t*>(cwq + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int x = blockIdx.x, G = gridDim.x, h0 = blockIdx.y * kHT;
@@ -1050,23 +847,126 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
 
   // ============================= compute warps =============================
   ws_regs_inc();
-  // A CTA whose chunks touch a short sequence (fewer than kExactPvLen
-  // tokens) runs the exact PV scaling over its whole range: one uniform
-  // branch per CTA between two instances of the loop below.
-  bool has_short = false;
-  if (F::kExactPv) {
-    const int b_lo = seq_of_chunk(cum, p.B, c_lo), b_hi = seq_of_chunk(cum, p.B, c_hi - 1);
-    bool mine = false;
-    for (int bb = b_lo + (threadIdx.x & 31); bb <= b_hi; bb += 32) {
-      const int len = checked_len(p, bb, false);
-      mine |= len > 0 && len < kExactPvLen;
+  const int w = warp, r = lane >> 2, j = lane & 3;
+  Query q;
+  float cw = 0.f;
+  float o[4][2][4];
+  ChunkRegs ra, rb;
+  bool pending = false;
+  int b = -1, s = 0, i = 0;
+  uint32_t phase = 0, qphase = 0;
+  bool dead = false;
+
+  auto flush_o = [&](int bb) {
+    const size_t slot = (size_t)x + bb;
+    if (tid == 0 && blockIdx.y == 0) {
+      if (c_lo <= cum[bb]) p.ws.span[2 * bb] = x;
+      if (c_hi >= cum[bb + 1]) p.ws.span[2 * bb + 1] = x;
     }
-    has_short = __any_sync(0xffffffffu, mine);
+    float* o0 = p.ws.o + (slot * p.H + h0 + r) * kDc;
+    float* o1 = o0 + 8 * kDc;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int base = 16 * (4 * w + g);
+      if (F::kStdLayout) {
+        *reinterpret_cast<float2*>(o0 + base + 2 * j) = make_float2(o[g][0][0], o[g][0][1]);
+        *reinterpret_cast<float2*>(o0 + base + 8 + 2 * j) = make_float2(o[g][1][0], o[g][1][1]);
+        *reinterpret_cast<float2*>(o1 + base + 2 * j) = make_float2(o[g][0][2], o[g][0][3]);
+        *reinterpret_cast<float2*>(o1 + base + 8 + 2 * j) = make_float2(o[g][1][2], o[g][1][3]);
+      } else {
+        *reinterpret_cast<float4*>(o0 + base + 4 * j) = make_float4(o[g][0][0], o[g][0][1], o[g][1][0], o[g][1][1]);
+        *reinterpret_cast<float4*>(o1 + base + 4 * j) = make_float4(o[g][0][2], o[g][0][3], o[g][1][2], o[g][1][3]);
+      }
+    }
+  };
+  // C of the previous chunk: wait for its P, then accumulate
+  auto finish_prev = [&](const ChunkRegs& prev) -> bool {
+    if (!pending) return true;
+    const int pi = i - 1;
+    if (!mbar_wait(smem_u32(&bp[pi & 1]), (uint32_t)((pi >> 1) & 1))) {
+      set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+      return false;
+    }
+    pv_chunk<LF, KF>(o, alpha_s, ptab, pi & 1, prev.bq, prev.s2h, lane);
+    pending = false;
+    return true;
+  };
+
+  auto chunk_step = [&](int c, ChunkRegs& cur, ChunkRegs& prev) -> bool {
+    int nb = b < 0 ? seq_of_chunk(cum, p.B, c) : b;
+    while (cum[nb + 1] <= c) ++nb;
+    if (nb != b) {
+      if (!finish_prev(prev)) return false;
+      if (b >= 0) flush_o(b);
+      b = nb;
+      QueryRaw raw;
+      const float am = warp_max(load_query_raw<LF, KF>(p, b, h0, w, lane, raw));
+      if (lane == 0) amax_s[w] = am;
+      mbar_arrive(smem_u32(qa));
+      if (!mbar_wait(smem_u32(qa), qphase)) {
+        set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+        return false;
+      }
+      qphase ^= 1u;
+      float amx = 0.f;
+#pragma unroll
+      for (int k = 0; k < kCW; ++k) amx = fmaxf(amx, amax_s[k]);
+      int ex = 0;
+      if (!F::kLatBf16 && amx > 0.f && isfinite(amx)) {
+        ex = 14 - ilogbf(amx);
+        ex = ex < -100 ? -100 : (ex > 100 ? 100 : ex);
+      }
+      finish_query<LF, KF>(raw, __int_as_float((127 + ex) << 23), q);
+      cw = p.scale_log2 * __int_as_float((127 - ex) << 23);
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
+    }
+    if (!mbar_wait(smem_u32(&full_bar[s]), phase)) {
+      set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+      return false;
+    }
+    const int nv = meta[s];
+    float acc[4][4];
+    qk_chunk<LF, KF>(stages + s * F::kBlock, nv, w, lane, q, cur.bq, cur.s2h, acc);
+    {
+      float2* xw = xpart + (((size_t)(i & 1) * kCW + w) * kHT + r) * kXStride + j;
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        xw[4 * n] = make_float2(acc[n][0], acc[n][1]);
+        xw[8 * kXStride + 4 * n] = make_float2(acc[n][2], acc[n][3]);
+      }
+    }
+    if (tid == 0) {
+      nvq[i & 1] = nv;
+      cwq[i & 1] = cw;
+    }
+    mbar_arrive(smem_u32(&bx[i & 1]));
+    if (!finish_prev(prev)) return false;
+    pending = true;
+    ++i;
+    if (++s == F::kStages) {
+      s = 0;
+      phase ^= 1u;
+    }
+    return true;
+  };
+
+  bool last_in_a = false;
+  for (int c = c_lo; c < c_hi; c += 2) {
+    if (!chunk_step(c, ra, rb)) { dead = true; break; }
+    last_in_a = true;
+    if (c + 1 >= c_hi) break;
+    if (!chunk_step(c + 1, rb, ra)) { dead = true; break; }
+    last_in_a = false;
   }
-  if (has_short)
-    compute_loop_exact<LF, KF>(p, c_lo, c_hi);
-  else
-    compute_loop<LF, KF, false>(p, c_lo, c_hi);
+  if (!dead) {
+    const bool ok = last_in_a ? finish_prev(ra) : finish_prev(rb);
+    if (ok && b >= 0) flush_o(b);
+  }
 }
 
 // Largest dynamic shared memory a block may opt into on the current device.
