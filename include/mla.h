@@ -194,6 +194,9 @@ mla_status mla_cache_append(const mla_cache_layer* cache, const uint16_t* c_new,
  * weight absorption; [TU] "步骤2" K_i = C^KV W_i^upK with W_UK[h] = (W_i^upK)^T).
  *   q_nope bf16 [B][H][128]   W_UK bf16 [H][128][512]   q_lat fp32 [B][H][512]
  *   fp32 accumulation of exact bf16 products.  B == 0 is a no-op.
+ *   W_UK is read while the previous kernel of the stream may still run (the
+ *   launch overlaps it): no kernel that triggers an early launch of its
+ *   dependents may write W_UK right before this call.
  */
 mla_status mla_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_lat,
                         int32_t batch, int32_t heads, mla_stream_t stream);
@@ -299,7 +302,8 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
  * mla_out_unabsorb - o[b][h] = o_lat[b][h] @ W_UV[h]   (the output side of
  * weight absorption; [TU] "步骤2" V_i = C^KV W_i^upV with W_UV[h] = W_i^upV).
  *   o_lat fp32 [B][H][512]   W_UV bf16 [H][512][128]   o fp32 [B][H][128]
- *   B == 0 is a no-op.
+ *   B == 0 is a no-op.  W_UV is read while the previous kernel of the stream
+ *   may still run, as W_UK in mla_q_absorb.
  */
 mla_status mla_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o,
                             int32_t batch, int32_t heads, mla_stream_t stream);

@@ -73,17 +73,19 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t* __restric
                                                        const uint16_t* __restrict__ w_uk,
                                                        float* __restrict__ q_lat, int B, int H) {
   pdl_launch_dependents();
-  pdl_wait();
   __shared__ __align__(16) uint16_t ws[kDn * kAbWS];
   __shared__ __align__(16) uint16_t as[16 * kAbAS];
   const int h = blockIdx.x, n0 = blockIdx.y * kAbN;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, j = lane & 3;
-  // W_UK[h][k][n0 .. n0+63]: 128 rows x 8 chunks of 16 B
+  // W_UK[h][k][n0 .. n0+63]: 128 rows x 8 chunks of 16 B.  No kernel of the
+  // library writes the weights, so their fetch starts before the wait for
+  // the previous kernel and overlaps its tail.
   const uint16_t* wsrc = w_uk + (size_t)h * kDn * kDc + n0;
   for (int i = tid; i < kDn * (kAbN / 8); i += 128) {
     const int k = i >> 3, c = i & 7;
     *reinterpret_cast<uint4*>(ws + k * kAbWS + 8 * c) = *reinterpret_cast<const uint4*>(wsrc + (size_t)k * kDc + 8 * c);
   }
+  pdl_wait();
   const uint32_t a_base = smem_addr(as) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kAbAS + 8 * (lane >> 4)) * 2;
   const uint32_t b_base =
       smem_addr(ws) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kAbWS + 16 * warp + 8 * (lane >> 4)) * 2;
@@ -130,16 +132,18 @@ __global__ void __launch_bounds__(128) out_unabsorb_kernel(const float* __restri
                                                            const uint16_t* __restrict__ w_uv,
                                                            float* __restrict__ o, int B, int H) {
   pdl_launch_dependents();
-  pdl_wait();
   __shared__ __align__(16) uint16_t ws[kDc * kUnWS];
   __shared__ float part[4][16][kUnN];
   const int h = blockIdx.x, v0 = blockIdx.y * kUnN;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, j = lane & 3;
+  // the weight tile before the wait for the previous kernel (no kernel of
+  // the library writes the weights): its fetch overlaps that kernel's tail
   const uint16_t* wsrc = w_uv + (size_t)h * kDc * kDv + v0;
   for (int i = tid; i < kDc * (kUnN / 8); i += 128) {
     const int k = i >> 1, c = i & 1;
     *reinterpret_cast<uint4*>(ws + k * kUnWS + 8 * c) = *reinterpret_cast<const uint4*>(wsrc + (size_t)k * kDv + 8 * c);
   }
+  pdl_wait();
   const uint32_t b_base = smem_addr(ws) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kUnWS + 8 * (lane >> 4)) * 2;
   for (int b0 = 0; b0 < B; b0 += 16) {
     const float* a0p = o_lat + ((size_t)(b0 + r) * H + h) * kDc + 128 * warp;

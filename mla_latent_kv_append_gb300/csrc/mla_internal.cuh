@@ -161,9 +161,11 @@ __host__ __device__ inline int64_t range_lo(int64_t C, int x, int G) { return C 
 // kernel in the stream begin launching as soon as all of its own blocks are
 // running (pdl_launch_dependents), and waits for the previous kernel to
 // complete and its memory to be visible (pdl_wait) before its first global
-// memory access, in every block.  Results are ordered exactly as in plain
-// stream order; the next grid's launch and block scheduling overlap this
-// grid's tail.
+// memory access, in every block; the one exception is the projection
+// weights, which no kernel of the library writes: the absorb and unabsorb
+// kernels fetch their weight tile before the wait.  Results are ordered as
+// in plain stream order; the next grid's launch and block scheduling overlap
+// this grid's tail.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
