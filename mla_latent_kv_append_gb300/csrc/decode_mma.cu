@@ -673,7 +673,6 @@ template <int LF, int KF>
 __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams p) {
   using F = Fmt<LF, KF>;
   pdl_launch_dependents();
-  pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   float2* xpart = reinterpret_cast<float2*>(smem + F::kStages * F::kBlock);   // [2][8 warps][16 rows][kXStride]
@@ -718,6 +717,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
+  // Up to here only the sequence lengths were read: a call's input, or the
+  // prefill's per-row lengths, whose kernel does not let dependents launch
+  // early.  The chunk prefix sums thus overlap the previous kernel's tail;
+  // the workspace, queries and cache wait for it.
+  pdl_wait();
   if (lead)
     for (int i = tid; i <= p.B; i += kWsThreads) p.ws.cum[i] = cum[i];
 
