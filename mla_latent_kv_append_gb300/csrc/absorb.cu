@@ -62,7 +62,7 @@ __device__ __forceinline__ void split3(float a, float b, uint32_t& p0, uint32_t&
 }
 
 // ---------------------------------------------------------------------------
-// q_absorb: grid (H, 512 / 64), block 128.  Warp w computes columns
+// q_absorb: grid (H, 512 / 64, batch splits), block 128.  Warp w computes columns
 // n0 + 16w .. +15 of a 16-row tile; K = 128 in 8 k-steps.
 // ---------------------------------------------------------------------------
 constexpr int kAbN = 64;             // columns per CTA
@@ -89,7 +89,10 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t* __restric
   const uint32_t a_base = smem_addr(as) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kAbAS + 8 * (lane >> 4)) * 2;
   const uint32_t b_base =
       smem_addr(ws) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kAbWS + 16 * warp + 8 * (lane >> 4)) * 2;
-  for (int b0 = 0; b0 < B; b0 += 16) {
+  const int tiles = (B + 15) / 16;
+  const int t_lo = (int)((int64_t)tiles * blockIdx.z / gridDim.z);
+  const int t_hi = (int)((int64_t)tiles * (blockIdx.z + 1) / gridDim.z);
+  for (int b0 = 16 * t_lo; b0 < 16 * t_hi; b0 += 16) {
     __syncthreads();   // previous tile's readers are done (and the W tile is in place)
     for (int i = tid; i < 16 * (kDn / 8); i += 128) {
       const int m = i >> 4, c = i & 15;
@@ -120,7 +123,7 @@ __global__ void __launch_bounds__(128) q_absorb_kernel(const uint16_t* __restric
 }
 
 // ---------------------------------------------------------------------------
-// out_unabsorb: grid (H, 128 / 16), block 128.  Warp w takes K rows
+// out_unabsorb: grid (H, 128 / 16, batch splits), block 128.  Warp w takes K rows
 // 128w .. 128w+127 for the CTA's 16 columns; all of the warp's A values are
 // loaded up front (independent loads), and the 4 partial tiles are summed in
 // shared memory.
@@ -145,7 +148,10 @@ __global__ void __launch_bounds__(128) out_unabsorb_kernel(const float* __restri
   }
   pdl_wait();
   const uint32_t b_base = smem_addr(ws) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kUnWS + 8 * (lane >> 4)) * 2;
-  for (int b0 = 0; b0 < B; b0 += 16) {
+  const int tiles = (B + 15) / 16;
+  const int t_lo = (int)((int64_t)tiles * blockIdx.z / gridDim.z);
+  const int t_hi = (int)((int64_t)tiles * (blockIdx.z + 1) / gridDim.z);
+  for (int b0 = 16 * t_lo; b0 < 16 * t_hi; b0 += 16) {
     const float* a0p = o_lat + ((size_t)(b0 + r) * H + h) * kDc + 128 * warp;
     const float* a1p = o_lat + ((size_t)(b0 + r + 8) * H + h) * kDc + 128 * warp;
     const bool ok0 = b0 + r < B, ok1 = b0 + r + 8 < B;
@@ -191,14 +197,24 @@ __global__ void __launch_bounds__(128) out_unabsorb_kernel(const float* __restri
 
 }  // namespace
 
+// Large batches (a prefill chunk's queries) split their 16-row tiles over
+// grid z, so that more CTAs stream them; each CTA still takes 8 or more
+// tiles per weight tile it loads.
+static int batch_splits(int B) {
+  const int tiles = (B + 15) / 16, z = tiles / 8;
+  return z < 1 ? 1 : (z > 32 ? 32 : z);
+}
+
 mla_status launch_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_lat, int B, int H,
                            cudaStream_t stream) {
-  return cuda_status(launch_pdl(q_absorb_kernel, dim3(H, kDc / kAbN), dim3(128), 0, stream, q_nope, w_uk, q_lat, B, H));
+  return cuda_status(launch_pdl(q_absorb_kernel, dim3(H, kDc / kAbN, batch_splits(B)), dim3(128), 0, stream, q_nope,
+                                w_uk, q_lat, B, H));
 }
 
 mla_status launch_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o, int B, int H,
                                cudaStream_t stream) {
-  return cuda_status(launch_pdl(out_unabsorb_kernel, dim3(H, kDv / kUnN), dim3(128), 0, stream, o_lat, w_uv, o, B, H));
+  return cuda_status(launch_pdl(out_unabsorb_kernel, dim3(H, kDv / kUnN, batch_splits(B)), dim3(128), 0, stream, o_lat,
+                                w_uv, o, B, H));
 }
 
 }  // namespace mla

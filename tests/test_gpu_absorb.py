@@ -55,3 +55,28 @@ def test_zero_batch_is_noop():
                          torch.zeros((16, 512, 128), dtype=torch.bfloat16, device="cuda"),
                          torch.empty((0, 16, 128), dtype=torch.float32, device="cuda"))
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("B", [1000, 4100])
+def test_large_batches_split_over_the_grid(B):
+    """Prefill-sized batches: the 16-row tiles are split over several CTAs
+    per weight tile (a ragged last tile included); sampled rows of both
+    projections against the oracle."""
+    seed, layer, H = 7, 0, 16
+    rng = np.random.default_rng(B)
+    rows = sorted(set([0, 15, 16, B - 17, B - 1] + [int(r) for r in rng.integers(0, B, 20)]))
+    qn = sd.q_nope(seed, layer, B, H)
+    wuk = sd.w_uk(seed, layer, H)
+    q_lat = torch.empty((B, H, 512), dtype=torch.float32, device="cuda")
+    mla.mla_q_absorb(qn, wuk, q_lat)
+    wuv = sd.w_uv(seed, layer, H)
+    o = torch.empty((B, H, 128), dtype=torch.float32, device="cuda")
+    mla.mla_out_unabsorb(q_lat, wuv, o)
+    torch.cuda.synchronize()
+    qn_h = synth.bf16_to_f32(synth.q_nope_bf16(seed, layer, B, H))
+    wuk_h = synth.bf16_to_f32(synth.w_uk_bf16(seed, layer, H))
+    wuv_h = synth.bf16_to_f32(synth.w_uv_bf16(seed, layer, H))
+    ql, oo = q_lat.cpu().numpy(), o.cpu().numpy()
+    for b in rows:
+        assert A.max_rel_error(ql[b], A.absorb_q(qn_h[b], wuk_h)) < TOL
+        assert A.max_rel_error(oo[b], A.unabsorb_o(ql[b], wuv_h)) < TOL
