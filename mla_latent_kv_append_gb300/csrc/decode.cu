@@ -390,13 +390,14 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
 // over 256 and more tokens they stay near 3e-4.
 constexpr int kExactLen = 256;
 constexpr int kShortSmemBytes =
-    (int)sizeof(float) * (kChunk * kCS + kChunk * kKS + kDc + kDr + kChunk + kDc) + (int)sizeof(int32_t) * 2 * kChunk;
+    (int)sizeof(float) * (kChunk * kCS + kChunk * kKS + kDc + kDr + 2 * kChunk + kDc + 2) +
+    (int)sizeof(int32_t) * 2 * kChunk;
 
 // Attention of (sequence b, head h) over its len < kExactLen tokens, in
 // fp32, straight from the cache: per 32-token block, dequantize into shared
-// memory, one warp per token for the scores (log2 domain), then an online
-// softmax in which thread (c, half) accumulates channel c over the tokens of
-// parity half.  sm: kShortSmemBytes of shared memory.
+// memory, one warp per token for the scores (log2 domain), warp 0 turns them
+// into the block's weights, then thread (c, half) accumulates channel c over
+// the tokens of parity half.  sm: kShortSmemBytes of shared memory.
 template <int LF, int KF>
 __device__ __noinline__ void short_exact(const DecodeParams& p, int b, int h, int len, float* sm) {
   float* s_c = sm;                       // [32][kCS]
@@ -404,8 +405,10 @@ __device__ __noinline__ void short_exact(const DecodeParams& p, int b, int h, in
   float* s_q = s_k + kChunk * kKS;       // [512]
   float* s_qp = s_q + kDc;               // [64]
   float* s_s = s_qp + kDr;               // [32] scores
-  float* s_o = s_s + kChunk;             // [512] the odd tokens' sums
-  int32_t* s_valid = reinterpret_cast<int32_t*>(s_o + kDc);   // [32]
+  float* s_w = s_s + kChunk;             // [32] weights exp2(score - running max)
+  float* s_o = s_w + kChunk;             // [512] the odd tokens' sums
+  float* s_stat = s_o + kDc;             // [2] the block's new running max and weight sum
+  int32_t* s_valid = reinterpret_cast<int32_t*>(s_stat + 2);  // [32]
   int32_t* s_page = s_valid + kChunk;                          // [32]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t row = (size_t)b * p.H + h;
@@ -428,18 +431,29 @@ __device__ __noinline__ void short_exact(const DecodeParams& p, int b, int h, in
       if (lane == 0) s_s[warp] = (t0 + warp < len && s_valid[warp]) ? a * p.scale_log2 : -INFINITY;
     }
     __syncthreads();
-    float mx = -INFINITY;
-    for (int t = 0; t < kChunk; ++t) mx = fmaxf(mx, s_s[t]);
-    const float mn = fmaxf(m, mx);
+    if (warp == 0) {
+      const float sv = s_s[lane];
+      float mx = sv;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m, mx);
+      const float w = mn == -INFINITY ? 0.f : exp2f(sv - mn);
+      float ws = w;
+#pragma unroll
+      for (int off = 16; off; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+      s_w[lane] = w;
+      if (lane == 0) {
+        s_stat[0] = mn;
+        s_stat[1] = ws;
+      }
+    }
+    __syncthreads();
+    const float mn = s_stat[0];
     if (mn == -INFINITY) continue;       // nothing valid yet
     const float al = exp2f(m - mn);
-    float lsum = 0.f, acc = 0.f;
-    for (int t = 0; t < kChunk; ++t) {
-      const float w = exp2f(s_s[t] - mn);
-      lsum += w;
-      if ((t & 1) == half) acc = fmaf(w, s_c[t * kCS + c], acc);
-    }
-    l = l * al + lsum;
+    float acc = 0.f;
+    for (int t = half; t < kChunk; t += 2) acc = fmaf(s_w[t], s_c[t * kCS + c], acc);
+    l = l * al + s_stat[1];
     o = o * al + acc;
     m = mn;
   }
@@ -476,6 +490,15 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_kernel(DecodeParams p
   const int x0 = p.ws.span[2 * b], S = p.ws.span[2 * b + 1] - x0 + 1;
   const float* mp = p.ws.m + (size_t)(x0 + b) * p.H + h;
   const float* lp = p.ws.l + (size_t)(x0 + b) * p.H + h;
+  if (S == 1) {                          // one CTA held the whole sequence: normalise its partial
+    if (part > 0) return;
+    const float m = *mp, l = *lp;
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws.o + ((size_t)(x0 + b) * p.H + h) * kDc) + quad);
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    *out = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+    if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    return;
+  }
   float mloc = -INFINITY;
   for (int t = tid; t < S; t += kCombThreads) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
   const float M = block_reduce(mloc, true, red);
