@@ -231,6 +231,9 @@ size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_spli
  *   sets MLA_DEVERR_SEQLEN.  B == 0 is a no-op.  B <= 4096, and
  *   B * max_pages * 2 (the batch's 32-token chunk capacity) < 2^31, else
  *   MLA_ERR_INVALID_ARG.
+ *   seq_lens is read while the previous kernel of the stream may still run
+ *   (the launch overlaps it): no kernel that triggers an early launch of its
+ *   dependents may write seq_lens right before this call.
  */
 mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
                                const uint16_t* q_pe, const int32_t* block_table,
