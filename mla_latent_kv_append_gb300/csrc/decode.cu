@@ -389,80 +389,118 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
 // do not average out; with a peaked softmax they reach the 2e-3 bound, while
 // over 256 and more tokens they stay near 3e-4.
 constexpr int kExactLen = 256;
+constexpr int kShortHeads = 8;             // heads per block of the exact path
+constexpr int kQS = kDc + kDr;             // a head's query row: q_lat, then q_pe
 constexpr int kShortSmemBytes =
-    (int)sizeof(float) * (kChunk * kCS + kChunk * kKS + kDc + kDr + 2 * kChunk + kDc + 2) +
+    (int)sizeof(float) * (kChunk * kCS + kChunk * kKS + kShortHeads * kQS + kChunk * kShortHeads + 3 * kShortHeads) +
     (int)sizeof(int32_t) * 2 * kChunk;
 
-// Attention of (sequence b, head h) over its len < kExactLen tokens, in
-// fp32, straight from the cache: per 32-token block, dequantize into shared
-// memory, one warp per token for the scores (log2 domain), warp 0 turns them
-// into the block's weights, then thread (c, half) accumulates channel c over
-// the tokens of parity half.  sm: kShortSmemBytes of shared memory.
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Attention of sequence b, heads h0 .. h0 + 7, over its len < kExactLen
+// tokens, in fp32, straight from the cache.  Per 32-token block: dequantize
+// into shared memory once for the eight heads; four warps per head score
+// eight tokens each (lanes over channels, log2 domain); warp j runs head j's
+// online softmax over the block and overwrites the scores with the weights;
+// then thread (c, half) accumulates channel c of heads 4 half .. 4 half + 3
+// over the block's tokens.  sm: kShortSmemBytes of shared memory.  Inlined:
+// as a call it left spill code on the combine's common path.
 template <int LF, int KF>
-__device__ __noinline__ void short_exact(const DecodeParams& p, int b, int h, int len, float* sm) {
-  float* s_c = sm;                       // [32][kCS]
-  float* s_k = s_c + kChunk * kCS;       // [32][kKS]
-  float* s_q = s_k + kChunk * kKS;       // [512]
-  float* s_qp = s_q + kDc;               // [64]
-  float* s_s = s_qp + kDr;               // [32] scores
-  float* s_w = s_s + kChunk;             // [32] weights exp2(score - running max)
-  float* s_o = s_w + kChunk;             // [512] the odd tokens' sums
-  float* s_stat = s_o + kDc;             // [2] the block's new running max and weight sum
-  int32_t* s_valid = reinterpret_cast<int32_t*>(s_stat + 2);  // [32]
-  int32_t* s_page = s_valid + kChunk;                          // [32]
+__device__ __forceinline__ void short_exact(const DecodeParams& p, int b, int h0, int len, float* sm) {
+  float* s_c = sm;                                 // [32][kCS]
+  float* s_k = s_c + kChunk * kCS;                 // [32][kKS]
+  float* s_q = s_k + kChunk * kKS;                 // [8][kQS]
+  float* s_w = s_q + kShortHeads * kQS;            // [32 tokens][8 heads] scores, then weights
+  float* s_al = s_w + kChunk * kShortHeads;        // [8] the block's rescale factor per head
+  float* s_ml = s_al + kShortHeads;                // [8][2] final running max and weight sum
+  int32_t* s_valid = reinterpret_cast<int32_t*>(s_ml + 2 * kShortHeads);  // [32]
+  int32_t* s_page = s_valid + kChunk;                                      // [32]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const size_t row = (size_t)b * p.H + h;
-  for (int i = tid; i < kDc; i += kCombThreads) s_q[i] = p.q_lat[row * kDc + i];
-  for (int i = tid; i < kDr; i += kCombThreads) s_qp[i] = bf16f(p.q_pe[row * kDr + i]);
-  const int c = tid & (kDc - 1), half = tid / kDc;
-  float m = -INFINITY, l = 0.f, o = 0.f;
+  const size_t row0 = (size_t)b * p.H + h0;
+  for (int i = tid; i < kShortHeads * kDc; i += kCombThreads) s_q[(i / kDc) * kQS + i % kDc] = p.q_lat[row0 * kDc + i];
+  for (int i = tid; i < kShortHeads * kDr; i += kCombThreads)
+    s_q[(i / kDr) * kQS + kDc + i % kDr] = bf16f(p.q_pe[row0 * kDr + i]);
+  const int sh = warp >> 2, st0 = (warp & 3) * 8;  // scoring: head sh, tokens st0 .. st0 + 7
+  const float* qrow = s_q + sh * kQS;
+  const int c = tid & (kDc - 1), hb = (tid / kDc) * 4;
+  float m = -INFINITY, l = 0.f;                    // warps 0..7: head `warp`'s running max and weight sum
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int t0 = 0; t0 < len; t0 += kChunk) {
-    __syncthreads();                     // the previous block's readers are done; s_q, s_qp in place
+    __syncthreads();                               // the previous block's readers are done; s_q in place
     dequant_chunk<LF, KF, kCombThreads>(p, b, t0, len, s_c, s_k, s_valid, s_page);
     __syncthreads();
-    {
-      const float* cr = s_c + warp * kCS;
-      const float* kr = s_k + warp * kKS;
-      float a = 0.f;
-      for (int i = lane; i < kDc; i += 32) a = fmaf(s_q[i], cr[i], a);
-      for (int i = lane; i < kDr; i += 32) a = fmaf(s_qp[i], kr[i], a);
+    for (int u = 0; u < 8; u += 2) {
+      const int ta = st0 + u;
+      const float* ca = s_c + ta * kCS;
+      const float* ka = s_k + ta * kKS;
+      float a = 0.f, a2 = 0.f;
+#pragma unroll 4
+      for (int i = lane; i < kDc; i += 32) {
+        const float q = qrow[i];
+        a = fmaf(q, ca[i], a);
+        a2 = fmaf(q, ca[kCS + i], a2);
+      }
 #pragma unroll
-      for (int off = 16; off; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-      if (lane == 0) s_s[warp] = (t0 + warp < len && s_valid[warp]) ? a * p.scale_log2 : -INFINITY;
-    }
-    __syncthreads();
-    if (warp == 0) {
-      const float sv = s_s[lane];
-      float mx = sv;
-#pragma unroll
-      for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float mn = fmaxf(m, mx);
-      const float w = mn == -INFINITY ? 0.f : exp2f(sv - mn);
-      float ws = w;
-#pragma unroll
-      for (int off = 16; off; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
-      s_w[lane] = w;
+      for (int i = lane; i < kDr; i += 32) {
+        const float q = qrow[kDc + i];
+        a = fmaf(q, ka[i], a);
+        a2 = fmaf(q, ka[kKS + i], a2);
+      }
+      a = warp_sum(a);
+      a2 = warp_sum(a2);
       if (lane == 0) {
-        s_stat[0] = mn;
-        s_stat[1] = ws;
+        s_w[ta * kShortHeads + sh] = (t0 + ta < len && s_valid[ta]) ? a * p.scale_log2 : -INFINITY;
+        s_w[(ta + 1) * kShortHeads + sh] = (t0 + ta + 1 < len && s_valid[ta + 1]) ? a2 * p.scale_log2 : -INFINITY;
       }
     }
     __syncthreads();
-    const float mn = s_stat[0];
-    if (mn == -INFINITY) continue;       // nothing valid yet
-    const float al = exp2f(m - mn);
-    float acc = 0.f;
-    for (int t = half; t < kChunk; t += 2) acc = fmaf(s_w[t], s_c[t * kCS + c], acc);
-    l = l * al + s_stat[1];
-    o = o * al + acc;
-    m = mn;
+    if (warp < kShortHeads) {
+      const float sv = s_w[lane * kShortHeads + warp];
+      const float mn = fmaxf(m, warp_max(sv));
+      const float w = mn == -INFINITY ? 0.f : exp2f(sv - mn);
+      const float al = mn == -INFINITY ? 1.f : exp2f(m - mn);
+      s_w[lane * kShortHeads + warp] = w;
+      if (lane == 0) s_al[warp] = al;
+      l = fmaf(l, al, warp_sum(w));
+      m = mn;
+    }
+    __syncthreads();
+    const float4 al = *reinterpret_cast<const float4*>(s_al + hb);
+    acc[0] *= al.x;
+    acc[1] *= al.y;
+    acc[2] *= al.z;
+    acc[3] *= al.w;
+#pragma unroll 8
+    for (int t = 0; t < kChunk; ++t) {
+      const float v = s_c[t * kCS + c];
+      const float4 w = *reinterpret_cast<const float4*>(s_w + t * kShortHeads + hb);
+      acc[0] = fmaf(w.x, v, acc[0]);
+      acc[1] = fmaf(w.y, v, acc[1]);
+      acc[2] = fmaf(w.z, v, acc[2]);
+      acc[3] = fmaf(w.w, v, acc[3]);
+    }
+  }
+  if (warp < kShortHeads && lane == 0) {
+    s_ml[2 * warp] = m;
+    s_ml[2 * warp + 1] = l;
+    if (p.lse) p.lse[row0 + warp] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
   }
   __syncthreads();
-  if (half) s_o[c] = o;
-  __syncthreads();
-  if (half) return;
-  p.o_lat[row * kDc + c] = l > 0.f ? (o + s_o[c]) / l : 0.f;
-  if (p.lse && c == 0) p.lse[row] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float lj = s_ml[2 * (hb + j) + 1];
+    p.o_lat[(row0 + hb + j) * kDc + c] = lj > 0.f ? acc[j] / lj : 0.f;
+  }
 }
 
 template <int LF, int KF>
@@ -483,8 +521,8 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_kernel(DecodeParams p
     return;
   }
   const int len = checked_len(p, b, false);
-  if (len < kExactLen) {
-    short_exact<LF, KF>(p, b, h, len, short_smem);
+  if (len < kExactLen) {                 // the block of every eighth head takes eight heads
+    if (h % kShortHeads == 0) short_exact<LF, KF>(p, b, h, len, short_smem);
     return;
   }
   const int x0 = p.ws.span[2 * b], S = p.ws.span[2 * b + 1] - x0 + 1;
