@@ -366,6 +366,7 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
 constexpr int kCombSlots = 1024;     // weights cached in shared memory
 constexpr int kCombThreads = 1024;
 constexpr int kCombParts = kCombThreads / (kDc / 4);
+constexpr int kCombGroupHeads = 8;   // heads per block of the grouped grid
 
 __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
 #pragma unroll
@@ -587,6 +588,148 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_kernel(DecodeParams p
   }
 }
 
+// The same merge in two other grids, for the shapes where one block per
+// (sequence, head) fits badly (chosen in launch_combine_t from the batch and
+// the split count; G / B is the average number of slots per sequence):
+//  * grid (B, H / 8), for many sequences with few slots each (G < 8 B): block
+//    (b, g) merges heads 8 g .. 8 g + 7, 128 threads per head, each thread
+//    summing every slot for its four channels; no block-wide reduction;
+//  * grid (B, H, C), C = 2, 4 or 8, for few sequences with very many slots
+//    (G >= 32 B): block (b, h, z) merges channels [512 z / C, 512 (z + 1) / C)
+//    with 8 C parts of ~19 slots each, after the block-wide max and sum.
+// Sequences shorter than kExactLen tokens go to short_exact as in
+// combine_kernel (in the sliced grid from the z = 0 block of every eighth
+// head).  Its shared arrays live in the dynamic buffer, so this kernel adds
+// no static shared memory to the exact path's.
+template <int LF, int KF>
+__global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(DecodeParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  extern __shared__ __align__(16) float short_smem[];
+  __shared__ float red[kCombThreads / 32];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const bool grouped = gridDim.y != (unsigned)p.H;
+  // per-group grid: head h0 + tid / 128, channel quad tid % 128; per-head
+  // grid: head blockIdx.y, the slice's quads split over 8 C parts
+  const int h0 = grouped ? blockIdx.y * kCombGroupHeads : blockIdx.y;
+  const int C = gridDim.z, z = blockIdx.z;
+  const int qs_shift = 7 - (31 - __clz(C));          // quads per slice: 128 / C (C a power of two)
+  const int ql = tid & ((1 << qs_shift) - 1);
+  const int part = grouped ? 0 : tid >> qs_shift, nparts = kCombThreads >> qs_shift;
+  const int h = grouped ? h0 + (tid >> 7) : h0;
+  const int quad = grouped ? (tid & 127) : (z << qs_shift) + ql;
+  const bool writes_lse = p.lse && (grouped ? (tid & 127) == 0 : (z == 0 && tid == 0));
+  const size_t row = (size_t)b * p.H + h;
+  const int32_t* cum = p.ws.cum;
+  float4* out = reinterpret_cast<float4*>(p.o_lat + row * kDc) + quad;
+  if (cum[b] == cum[b + 1]) {
+    if (part == 0) *out = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (writes_lse) p.lse[row] = -INFINITY;
+    return;
+  }
+  const int len = checked_len(p, b, false);
+  if (len < kExactLen) {                 // eight heads per block
+    if (grouped || (h0 % kShortHeads == 0 && z == 0)) short_exact<LF, KF>(p, b, h0, len, short_smem);
+    return;
+  }
+  const int x0 = p.ws.span[2 * b], S = p.ws.span[2 * b + 1] - x0 + 1;
+  const float* mp = p.ws.m + (size_t)(x0 + b) * p.H + h;
+  const float* lp = p.ws.l + (size_t)(x0 + b) * p.H + h;
+  const float4* o4 = reinterpret_cast<const float4*>(p.ws.o + ((size_t)(x0 + b) * p.H + h) * kDc) + quad;
+  const size_t ostride = (size_t)p.H * (kDc / 4);
+  if (S == 1) {                          // one CTA held the whole sequence: normalise its partial
+    if (part > 0) return;
+    const float m = *mp, l = *lp;
+    const float4 v = __ldcg(o4);
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    *out = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
+    if (writes_lse) p.lse[row] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    return;
+  }
+  float M, L;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (grouped) {
+    M = -INFINITY;
+#pragma unroll 8
+    for (int t = 0; t < S; ++t) M = fmaxf(M, mp[(size_t)t * p.H]);
+    L = 0.f;
+#pragma unroll 4
+    for (int t = 0; t < S; ++t) {
+      const float m = mp[(size_t)t * p.H], l = lp[(size_t)t * p.H];
+      const float4 v = __ldcg(o4 + (size_t)t * ostride);
+      const float w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
+      L = fmaf(w, l, L);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+  } else {
+    float* sw = short_smem;                                        // [kCombSlots]
+    float4* parts = reinterpret_cast<float4*>(short_smem + kCombSlots);   // [kCombThreads]
+    float mloc = -INFINITY;
+    for (int t = tid; t < S; t += kCombThreads) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
+    M = block_reduce(mloc, true, red);
+    float lloc = 0.f;
+    for (int t = tid; t < S; t += kCombThreads) {
+      const float m = mp[(size_t)t * p.H];
+      const float w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
+      if (t < kCombSlots) sw[t] = w;
+      if (w != 0.f) lloc = fmaf(w, lp[(size_t)t * p.H], lloc);
+    }
+    L = block_reduce(lloc, false, red);   // also orders the sw writes before the reads below
+#pragma unroll 8
+    for (int t = part; t < S; t += nparts) {
+      float w;
+      if (t < kCombSlots) {
+        w = sw[t];
+      } else {
+        const float m = mp[(size_t)t * p.H];
+        w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
+      }
+      const float4 v = __ldcg(o4 + (size_t)t * ostride);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    // parts 0..7 first fold in parts 8, 16, ... of their column, then part 0
+    // adds parts 1..7
+    parts[tid] = acc;
+    __syncthreads();
+    if (nparts > 8) {
+      if (part < 8) {
+        for (int k = part + 8; k < nparts; k += 8) {
+          const float4 a1 = parts[(k << qs_shift) + ql];
+          acc.x += a1.x;
+          acc.y += a1.y;
+          acc.z += a1.z;
+          acc.w += a1.w;
+        }
+        parts[tid] = acc;
+      }
+      __syncthreads();
+    }
+    if (part > 0) return;
+#pragma unroll
+    for (int k = 1; k < 8; ++k) {         // nparts >= 8
+      const float4 a1 = parts[(k << qs_shift) + ql];
+      acc.x += a1.x;
+      acc.y += a1.y;
+      acc.z += a1.z;
+      acc.w += a1.w;
+    }
+  }
+  if (L > 0.f) {
+    const float inv = 1.f / L;
+    *out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (writes_lse) p.lse[row] = (M + log2f(L)) * 0.69314718055994531f;
+  } else {
+    *out = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (writes_lse) p.lse[row] = -INFINITY;
+  }
+}
+
 template <int LF, int KF>
 mla_status launch_ref_t(const DecodeParams& p, cudaStream_t stream) {
   const size_t smem = sizeof(float) * (kHT * kDc + kHT * kDr + kChunk * kCS + kChunk * kKS + kHT * kChunk + 3 * kHT) +
@@ -641,6 +784,22 @@ mla_status launch_combine_t(const DecodeParams& p, cudaStream_t stream) {
     if (st != MLA_OK) return st;
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
+  static int configured_g[64] = {0};
+  if (dev < 0 || dev >= 64 || !configured_g[dev]) {
+    const mla_status st = cuda_status(cudaFuncSetAttribute(
+        combine_grouped_kernel<LF, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, kShortSmemBytes));
+    if (st != MLA_OK) return st;
+    if (dev >= 0 && dev < 64) configured_g[dev] = 1;
+  }
+  // G / B: the average number of partial slots per sequence
+  if (p.G < 8 * p.B)
+    return cuda_status(launch_pdl(combine_grouped_kernel<LF, KF>, dim3(p.B, p.H / kCombGroupHeads, 1),
+                                  dim3(kCombThreads), kShortSmemBytes, stream, p));
+  int c = 1;                             // channel slices: ~19 slots or more per part
+  while (c < 8 && (int64_t)2 * c * 16 * p.B <= p.G) c *= 2;
+  if (c > 1)
+    return cuda_status(launch_pdl(combine_grouped_kernel<LF, KF>, dim3(p.B, p.H, c), dim3(kCombThreads),
+                                  kShortSmemBytes, stream, p));
   return cuda_status(
       launch_pdl(combine_kernel<LF, KF>, dim3(p.B, p.H), dim3(kCombThreads), kShortSmemBytes, stream, p));
 }

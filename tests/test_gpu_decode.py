@@ -71,6 +71,19 @@ def test_split_invariance_and_counts():
         assert A.max_rel_error(o, outs[0]) < 1e-3
 
 
+@pytest.mark.parametrize("ns", [16, 64, 128, 512], ids=["grouped", "per-head", "sliced-2", "sliced-8"])
+def test_combine_grids(ns):
+    """The combine's three grids, chosen from the batch (4) and the split
+    count: eight heads per block (G < 8 B), one head per block
+    (8 B <= G < 32 B), and one head's channels sliced over 2 or 8 blocks
+    (G >= 32 B).  The batch holds an empty sequence, a short one (recomputed
+    exactly) and long ones spread over up to ~250 slots; 32 heads (four head
+    groups)."""
+    lens = [3000, 0, 150, 4100]
+    wl = Workload(1, 32, lens, mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, seed=81)
+    run_and_check(wl, num_splits=ns)
+
+
 def test_64_heads_mixed_lengths():
     wl = Workload(1, 64, [1000, 37, 2500], mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, seed=79)
     run_and_check(wl)
