@@ -33,7 +33,15 @@
  *     it keeps no state between calls apart from a per-device attribute
  *     cache.  Calls are thread-safe and re-entrant.
  *   - Execution: every call enqueues its kernels on `stream` (NULL = the
- *     legacy default stream) and returns without waiting.
+ *     legacy default stream) and returns without waiting.  The kernels use
+ *     programmatic dependent launch: each may start while the previous
+ *     kernels of the stream still run, and waits for them (griddepcontrol.wait,
+ *     which also makes their stores visible) before touching data a kernel
+ *     may have produced.  The few arrays read before that wait are named
+ *     below ("read during the launch overlap"): no kernel enqueued on the
+ *     stream since its last full ordering point (a host synchronisation, a
+ *     cudaStreamWaitEvent, a memory copy) may write them, whether or not
+ *     that kernel triggers its dependents early.
  *   - Layout: arrays are row-major and contiguous with the shapes given.
  *     bf16 values are passed as their 16-bit patterns (uint16_t).
  *   - Errors: arguments are checked on the host before any launch; a bad
@@ -194,9 +202,7 @@ mla_status mla_cache_append(const mla_cache_layer* cache, const uint16_t* c_new,
  * weight absorption; [TU] "步骤2" K_i = C^KV W_i^upK with W_UK[h] = (W_i^upK)^T).
  *   q_nope bf16 [B][H][128]   W_UK bf16 [H][128][512]   q_lat fp32 [B][H][512]
  *   fp32 accumulation of exact bf16 products.  B == 0 is a no-op.
- *   W_UK is read while the previous kernel of the stream may still run (the
- *   launch overlaps it): no kernel that triggers an early launch of its
- *   dependents may write W_UK right before this call.
+ *   W_UK is read during the launch overlap (see Execution above).
  */
 mla_status mla_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_lat,
                         int32_t batch, int32_t heads, mla_stream_t stream);
@@ -231,9 +237,7 @@ size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_spli
  *   sets MLA_DEVERR_SEQLEN.  B == 0 is a no-op.  B <= 4096, and
  *   B * max_pages * 2 (the batch's 32-token chunk capacity) < 2^31, else
  *   MLA_ERR_INVALID_ARG.
- *   seq_lens is read while the previous kernel of the stream may still run
- *   (the launch overlaps it): no kernel that triggers an early launch of its
- *   dependents may write seq_lens right before this call.
+ *   seq_lens is read during the launch overlap (see Execution above).
  */
 mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
                                const uint16_t* q_pe, const int32_t* block_table,
@@ -305,8 +309,8 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
  * mla_out_unabsorb - o[b][h] = o_lat[b][h] @ W_UV[h]   (the output side of
  * weight absorption; [TU] "步骤2" V_i = C^KV W_i^upV with W_UV[h] = W_i^upV).
  *   o_lat fp32 [B][H][512]   W_UV bf16 [H][512][128]   o fp32 [B][H][128]
- *   B == 0 is a no-op.  W_UV is read while the previous kernel of the stream
- *   may still run, as W_UK in mla_q_absorb.
+ *   B == 0 is a no-op.  W_UV is read during the launch overlap (see
+ *   Execution above).
  */
 mla_status mla_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o,
                             int32_t batch, int32_t heads, mla_stream_t stream);

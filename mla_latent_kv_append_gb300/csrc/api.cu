@@ -169,6 +169,7 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
   p.block_table = block_table;
   p.max_pages = max_pages;
   p.bt_stride = max_pages;
+  p.lens_after_wait = 0;
   p.seq_lens = seq_lens;
   p.B = batch;
   p.H = heads;

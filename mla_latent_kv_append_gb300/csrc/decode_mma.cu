@@ -692,6 +692,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   const int x = blockIdx.x, G = gridDim.x, h0 = blockIdx.y * kHT;
   const bool lead = (blockIdx.x == 0 && blockIdx.y == 0);
 
+  if (p.lens_after_wait) pdl_wait();     // the lengths come from the kernel just before
   if (warp == 0) {
     int carry = 0;
     for (int base = 0; base < p.B; base += 32) {
@@ -717,10 +718,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
-  // Up to here only the sequence lengths were read: a call's input, or the
-  // prefill's per-row lengths, whose kernel does not let dependents launch
-  // early.  The chunk prefix sums thus overlap the previous kernel's tail;
-  // the workspace, queries and cache wait for it.
+  // Up to here only the sequence lengths were read, a call's input that no
+  // kernel in flight may write (the API's rule): the chunk prefix sums thus
+  // overlap the previous kernel's tail; the workspace, queries and cache wait
+  // for it.  The prefill's per-row lengths were waited for above: only
+  // griddepcontrol.wait makes the lengths kernel's stores visible.
   pdl_wait();
   if (lead)
     for (int i = tid; i <= p.B; i += kWsThreads) p.ws.cum[i] = cum[i];

@@ -161,11 +161,14 @@ __host__ __device__ inline int64_t range_lo(int64_t C, int x, int G) { return C 
 // kernel in the stream begin launching as soon as all of its own blocks are
 // running (pdl_launch_dependents), and waits for the previous kernel to
 // complete and its memory to be visible (pdl_wait) before its first global
-// memory access, in every block; the one exception is the projection
-// weights, which no kernel of the library writes: the absorb and unabsorb
-// kernels fetch their weight tile before the wait.  Results are ordered as
-// in plain stream order; the next grid's launch and block scheduling overlap
-// this grid's tail.
+// memory access, in every block.  The exceptions are call inputs that no
+// kernel of the library writes and that the API forbids any kernel in flight
+// to write: the absorb and unabsorb kernels fetch their weight tile, and the
+// decode kernel reads the sequence lengths, before the wait (not the
+// prefill's per-row lengths, which a kernel writes just before).  Only the
+// wait makes a previous kernel's stores visible, triggered early or not.
+// Results are ordered as in plain stream order; the next grid's launch and
+// block scheduling overlap this grid's tail.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -213,6 +216,8 @@ struct DecodeParams {
   int max_pages;
   int bt_stride;          // block-table row stride: max_pages, or 0 when every row is row 0 (prefill)
   const int32_t* seq_lens;
+  int lens_after_wait;    // 1: seq_lens is written by the kernel launched just before (the
+                          // prefill's lengths): read it only after waiting on that kernel
   int B, H, G;
   float scale_log2;       // softmax_scale * log2(e)
   Workspace ws;

@@ -78,7 +78,9 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
   for (int i0 = 0; i0 < n; i0 += kSlice) {
     const int s = n - i0 < kSlice ? n - i0 : kSlice;
     // a plain launch: it starts after the previous slice's combine has
-    // finished with the lengths and the split-K workspace
+    // finished with the lengths and the split-K workspace.  Its stores are
+    // visible to the decode kernel only once that kernel has waited on it
+    // (lens_after_wait)
     causal_lengths_kernel<<<(s + 255) / 256, 256, 0, st>>>(lens, s, ctx_before + i0);
     const mla_status ls = launch_status();
     if (ls != MLA_OK) return ls;
@@ -94,6 +96,7 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
     p.max_pages = max_pages;
     p.bt_stride = 0;
     p.seq_lens = lens;
+    p.lens_after_wait = 1;
     p.B = s;
     p.H = heads;
     p.G = G;
