@@ -516,12 +516,14 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_kernel(DecodeParams p
   const int quad = tid & (kDc / 4 - 1), part = tid / (kDc / 4);
   const int32_t* cum = p.ws.cum;
   float4* out = reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc) + quad;
+  // a length out of range ran as 0 in the split kernel; it is reported here,
+  // after the wait, so that no earlier kernel's write to dev_err can land later
+  const int len = checked_len(p, b, tid == 0);
   if (cum[b] == cum[b + 1]) {
     if (part == 0) *out = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
     return;
   }
-  const int len = checked_len(p, b, false);
   if (len < kExactLen) {                 // the block of every eighth head takes eight heads
     if (h % kShortHeads == 0) short_exact<LF, KF>(p, b, h, len, short_smem);
     return;
@@ -622,6 +624,7 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
   const size_t row = (size_t)b * p.H + h;
   const int32_t* cum = p.ws.cum;
   float4* out = reinterpret_cast<float4*>(p.o_lat + row * kDc) + quad;
+  if (tid == 0) checked_len(p, b, true);            // reports, after the wait, as in combine_kernel
   if (cum[b] == cum[b + 1]) {
     if (part == 0) *out = make_float4(0.f, 0.f, 0.f, 0.f);
     if (writes_lse) p.lse[row] = -INFINITY;

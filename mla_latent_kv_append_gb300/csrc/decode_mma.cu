@@ -698,7 +698,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
     for (int base = 0; base < p.B; base += 32) {
       const int b = base + lane;
       int v = 0;
-      if (b < p.B) v = (checked_len(p, b, lead) + kChunk - 1) / kChunk;
+      // a length out of range counts as 0; the combine, after its wait,
+      // reports it (dev_err may be written by a kernel still in flight here)
+      if (b < p.B) v = (checked_len(p, b, false) + kChunk - 1) / kChunk;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int t = __shfl_up_sync(0xffffffffu, v, off);
