@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
         // scale) or, for GS = 8, half a lane
         constexpr int GS = latent_group_size(LF);
         int8_t q[16];
-        if (GS == 8) {
+        if constexpr (GS == 8) {
           scale[(2 * lane) * kBlockTokens + t] = quant_sym<8, 127>(x, q);
           scale[(2 * lane + 1) * kBlockTokens + t] = quant_sym<8, 127>(x + 8, q + 8);
         } else {
