@@ -18,6 +18,7 @@ layers spread over the host cores).
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import multiprocessing as mp
@@ -123,12 +124,20 @@ def prefill_flops(P, H, ctx_before=0):
     return pairs * H * 2 * (576 + 512)
 
 
+def code_text(src):
+    """Source text without comments and whitespace: what the compiler sees."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return re.sub(r"\s+", "", src)
+
+
 def decode_source_hash():
+    """Hash of the decode path's code (comments and whitespace ignored)."""
     h = hashlib.sha256()
     for name in ("decode.cu", "decode_mma.cu", "mla_internal.cuh"):
         p = os.path.join(ROOT, "mla_latent_kv_append_gb300", "csrc", name)
         if os.path.exists(p):
-            h.update(open(p, "rb").read())
+            h.update(code_text(open(p, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

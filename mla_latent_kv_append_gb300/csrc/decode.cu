@@ -14,11 +14,15 @@
 // balanced.  blockIdx.y selects a tile of 16 heads.  A CTA keeps the online
 // softmax state (running max m, running sum l, unnormalised o) of the
 // sequence it is in and writes it as a partial to slot (x + b) when the
-// sequence or its range ends.  The combine kernel merges the partials of
-// each sequence.  Scores are kept in the log2 domain (scaled by log2 e).
+// sequence or its range ends.  A combine kernel merges the partials of
+// each sequence (combine_kernel, or combine_grouped_kernel for batches with
+// few or very many partials per sequence); sequences shorter than 256
+// tokens are recomputed exactly in fp32 there instead.  Scores are kept in
+// the log2 domain (scaled by log2 e).
 //
-// This translation unit holds the partition, the combine and the reference
-// decode kernel (fp32 CUDA cores, dequantized chunk in shared memory).
+// This translation unit holds the partition, the combine kernels with the
+// exact short-sequence path, and the reference decode kernel (fp32 CUDA
+// cores, dequantized chunk in shared memory).
 #include <math.h>
 #include <stdlib.h>
 
@@ -355,7 +359,8 @@ __global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
   }
 }
 
-// grid (B, H), block 1024: merge the partials of sequence b, head h.  CTAs
+// combine_kernel: grid (B, H), block 1024: merge the partials of sequence b,
+// head h (the grid for ~8 to ~32 slots per sequence).  CTAs
 // span[2b] .. span[2b+1] wrote slots x + b.  The slots' maxima and sums are
 // read in parallel (one slot per thread), the block reduces them; then each
 // eighth of the block accumulates 4 channels per thread over every eighth
