@@ -43,18 +43,22 @@ def _stale(target, deps):
 def _compile(src, obj, deps):
     if not _stale(obj, [src] + deps):
         return obj, ""
-    cmd = [nvcc()] + ARCH + FLAGS + ["-c", src, "-o", obj]
+    tmp = obj + ".tmp%d" % os.getpid()
+    cmd = [nvcc()] + ARCH + FLAGS + ["-c", src, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))
+    os.replace(tmp, obj)        # an interrupted compile leaves no object that looks current
     return obj, r.stdout + r.stderr
 
 
 def _link(objs, out):
-    cmd = [nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", out] + objs
+    tmp = out + ".tmp%d" % os.getpid()
+    cmd = [nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed for %s:\n%s\n%s" % (out, r.stdout, r.stderr))
+    os.replace(tmp, out)        # readers see the old library or the new one, never a partial file
 
 
 def build_target(srcs, headers, out, tag, verbose=False):
