@@ -42,3 +42,22 @@ def test_prefill_flop_count():
     assert bench.prefill_flops(2, 1) == 3 * 2 * 1088
     assert bench.prefill_flops(2, 4, ctx_before=1) == 5 * 4 * 2 * 1088
     assert bench.prefill_flops(8192, 64) == 8192 * 8193 // 2 * 64 * 2176
+
+
+def test_traffic_record_follows_the_code_not_its_comments():
+    """The committed ncu traffic is tied to a hash of the decode path's code:
+    comments and whitespace do not change it, any code token does."""
+    a = "int f(int x) {  // doubles\n  return 2 * x; /* plain */ }\n"
+    b = "int f(int x)\n{\n    return 2*x;   // twice, reworded\n}\n"
+    c = "int f(int x) { return 3 * x; }\n"
+    assert bench.code_text(a) == bench.code_text(b)
+    assert bench.code_text(a) != bench.code_text(c)
+    rec = json.load(open(os.path.join(bench.ROOT, "profiles", "decode_traffic.json")))
+    for name, e in rec.items():
+        if name.startswith("_"):
+            continue
+        assert e["bytes_per_launch"] > 0
+        if e["source_hash"] == bench.decode_source_hash():
+            assert bench.ncu_traffic(name) == e["bytes_per_launch"]
+        else:
+            assert bench.ncu_traffic(name) is None
