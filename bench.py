@@ -529,10 +529,12 @@ def run_ours(args, cfg, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 MMA on exact integer codes, f32 accumulate" if cfg["latent"] != "bf16"
-                 else "bf16 MMA, f32 accumulate",
+        "dtype": "f16" if cfg["latent"] != "bf16" else "bf16",
         "data": "synthetic (seeded; DeepSeek-V2-Lite shapes, random-init weights)",
-        "config": {"workload": args.config, "description": cfg["desc"], "layers": layers, "heads": cfg["heads"],
+        "config": {"workload": args.config, "description": cfg["desc"],
+                   "arithmetic": "f16 MMA on exact integer codes, f32 accumulate" if cfg["latent"] != "bf16"
+                   else "bf16 MMA, f32 accumulate",
+                   "layers": layers, "heads": cfg["heads"],
                    "batch_per_gpu": wl.B, "context": (seq_lens[0] if len(set(seq_lens)) == 1 else
                                                       "log-uniform, mean %d" % (sum(seq_lens) // len(seq_lens))),
                    "latent_fmt": cfg["latent"], "kpe_fmt": cfg["kpe"], "page_tokens": 64,
@@ -590,9 +592,10 @@ def main():
         value = cb["value"] * world
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
                 "steps": steps, "warmup": args.warmup, "ms_per_step": cb["ms_per_step"], "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention / fp32 quantization",
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic (seeded; DeepSeek-V2-Lite shapes, random-init weights)",
-                "config": {"workload": args.config, "description": cfg["desc"]},
+                "config": {"workload": args.config, "description": cfg["desc"],
+                           "arithmetic": "f64 attention / fp32 quantization"},
                 "cpu_baseline": cb, "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                                             "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
