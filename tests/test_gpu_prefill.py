@@ -94,7 +94,9 @@ def check(ch, rows=None):
 
 FORMATS = [(mla.FMT_INT8_SYM, mla.FMT_INT8_SYM), (mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM), (mla.FMT_BF16, mla.FMT_BF16),
            (mla.FMT_INT4_SYM, mla.FMT_INT4_SYM), (mla.FMT_INT8_G8, mla.FMT_INT8_SYM),
-           (mla.FMT_INT8_TOKEN, mla.FMT_INT8_SYM)]
+           (mla.FMT_INT8_TOKEN, mla.FMT_INT8_SYM), (mla.FMT_INT8_G32, mla.FMT_INT8_SYM),
+           (mla.FMT_INT8_G64, mla.FMT_INT8_SYM), (mla.FMT_INT4_ASYM, mla.FMT_INT4_SYM),
+           (mla.FMT_BF16, mla.FMT_INT8_SYM)]
 
 
 @pytest.mark.parametrize("lf,kf", FORMATS, ids=["%s-%s" % (FMT_NAME[a], FMT_NAME[b]) for a, b in FORMATS])
