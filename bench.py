@@ -310,6 +310,24 @@ class OracleRunner:
             p.join(timeout=10)
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
 def cpu_baseline(cfg, seq_lens, min_seconds=8.0, steps=None, warmup=1):
     r = OracleRunner(cfg, seq_lens, SEED)
     for _ in range(warmup):
@@ -325,6 +343,7 @@ def cpu_baseline(cfg, seq_lens, min_seconds=8.0, steps=None, warmup=1):
     r.close()
     total = sum(times)
     return {"value": len(times) / total, "unit": "tokens/s", "cores": r.n, "kind": "oracle",
+            "workers": r.n, "host_cores": os.cpu_count(), "cpu_model": cpu_model(),
             "sample": "sequence 0 through all %d layers per step (context %d)%s, layers spread over %d "
                       "spawned single-BLAS-thread processes; %d steps, %.1f s" % (
                           cfg["layers"], seq_lens[0],
@@ -567,7 +586,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="v2lite_int8", choices=sorted(CONFIGS))
+    ap.add_argument("--config", default="v2lite_int4_32k", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (testing only)")
     ap.add_argument("--num-splits", type=int, default=0)

@@ -227,8 +227,11 @@ size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_spli
  *   seq_lens    int32 [B]: tokens attended (positions 0..len-1, the newly
  *               appended token included).  0 gives o_lat = 0 and lse = -inf.
  *   softmax_scale: typically 1 / sqrt(128 + 64).
- *   num_splits: CTAs the context work is divided over (0 = one per SM).
- *               Work is split evenly over all sequences' 32-token chunks.
+ *   num_splits: ranges the context work is divided into, 1 .. 65535
+ *               (0 = automatic: SMs / (H / 16), so that the H / 16 head
+ *               tiles of every range run side by side, one CTA per SM, and
+ *               read the range's pages once between them).  Work is split
+ *               evenly over all sequences' 32-token chunks.
  *   workspace:  device, >= mla_decode_workspace_bytes(B, H, num_splits)
  *               bytes, 256-byte aligned; contents are scratch.
  *   o_lat fp32 [B][H][512]      lse fp32 [B][H] (natural log; may be NULL)
@@ -267,7 +270,8 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
  *   allocator (no cudaMalloc, cudaFree or allocating library routine).
  *   Returns MLA_ERR_INVALID_ARG when mla_decode_workspace_bytes(batch, heads,
  *   num_splits) exceeds MLA_NOALLOC_SCRATCH_BYTES (e.g. 64 heads at batch 64
- *   with one split per SM fits; pass a smaller num_splits otherwise).
+ *   with the automatic split count fits; pass a smaller num_splits
+ *   otherwise).
  *   The first call on a device looks up the array's device address (with
  *   that device current) and caches it; make that first call before any
  *   stream capture.  All calls share the array and it keeps the last call's
@@ -346,6 +350,20 @@ const char* mla_status_string(mla_status status);
 /* Text of the CUDA error behind the calling thread's most recent
  * MLA_ERR_CUDA ("no error" if none); a static string, not to be freed. */
 const char* mla_last_cuda_error(void);
+
+/*
+ * mla_set_wait_limit_ns - bound, in nanoseconds, on every wait inside the
+ * decode kernels (stage arrivals, the hand-offs between the block's warp
+ * roles) of the decode and prefill calls this process launches afterwards;
+ * returns the previous bound, or -1 (nothing changed) for ns < 0.  The
+ * default is 10 s.  A test and diagnostic hook, not part of the pages'
+ * method: a wait that runs out sets MLA_DEVERR_TIMEOUT in *dev_err, and its
+ * block writes empty partials (weight 0) for the rest of its share of the
+ * context and leaves once its own bulk copies have landed.  Nothing traps
+ * and the outputs stay finite, but they miss that share of the context.
+ * With ns = 0 a wait gives up as soon as its second poll fails.
+ */
+int64_t mla_set_wait_limit_ns(int64_t ns);
 
 /* ABI version (major * 100 + minor). */
 int32_t mla_abi_version(void);

@@ -83,6 +83,7 @@ def _load():
         "mla_lse_merge": (I32, [P, P, I32, I32, I32, P, P, P]),
         "mla_prefill_workspace_bytes": (SZ, [I32, I32]),
         "mla_prefill_absorbed": (I32, [CP, P, P, P, I32, I32, I32, I32, F32, P, SZ, P, P, P, P]),
+        "mla_set_wait_limit_ns": (ctypes.c_int64, [ctypes.c_int64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -249,6 +250,15 @@ def mla_lse_merge(o_parts, lse_parts, o_lat, lse=None, stream=None):
         _need(lse, torch.float32, (B, H), "lse")
     _check("mla_lse_merge", lib.mla_lse_merge(_ptr(o_parts), _ptr(lse_parts), R, B, H, _ptr(o_lat), _ptr(lse),
                                               _stream(stream)))
+
+
+def mla_set_wait_limit_ns(ns):
+    """Bound (ns) on every wait inside the decode kernels launched afterwards;
+    returns the previous bound.  A test and diagnostic hook (default 10 s)."""
+    prev = int(lib.mla_set_wait_limit_ns(int(ns)))
+    if prev < 0:
+        raise ValueError("wait limit must be >= 0")
+    return prev
 
 
 def abi_version():

@@ -2,6 +2,8 @@
 // arithmetic and dispatch to the kernel launchers.  Nothing here allocates.
 #include <math.h>
 
+#include <atomic>
+
 #include "mla_internal.cuh"
 
 namespace mla {
@@ -16,6 +18,10 @@ int device_sm_count() {
   if (dev >= 0 && dev < 64) cached[dev] = n;
   return n;
 }
+
+static std::atomic<int64_t> g_wait_limit_ns{10000000000ll};
+
+uint64_t wait_limit_ns() { return (uint64_t)g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 static thread_local const char* g_last_cuda_error = "no error";
 
@@ -37,10 +43,14 @@ static bool cache_ok(const mla_cache_layer* c, PageLayout* L) {
   return compute_layout(c->latent_fmt, c->kpe_fmt, L);
 }
 
-static int decode_grid(int num_splits) {
+// Context splits of a decode call: the caller's count, else one CTA per SM
+// over all head tiles (the H / 16 CTAs of a split run side by side and read
+// the split's pages once between them, through L2).
+static int decode_grid(int num_splits, int heads) {
   if (num_splits > 0) return num_splits;
-  int sms = device_sm_count();
-  return sms > 0 ? sms : 1;
+  const int sms = device_sm_count();
+  const int g = sms / (heads / 16);
+  return g > 0 ? g : 1;
 }
 
 }  // namespace mla
@@ -49,9 +59,14 @@ using namespace mla;
 
 extern "C" {
 
-int32_t mla_abi_version(void) { return 102; }
+int32_t mla_abi_version(void) { return 103; }
 
 const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
+
+int64_t mla_set_wait_limit_ns(int64_t ns) {
+  if (ns < 0) return -1;
+  return g_wait_limit_ns.exchange(ns);
+}
 
 const char* mla_status_string(mla_status s) {
   switch (s) {
@@ -133,8 +148,8 @@ mla_status mla_lse_merge(const float* o_parts, const float* lse_parts, int32_t p
 }
 
 size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_splits) {
-  if (batch < 0 || batch > kMaxBatch || !heads_ok(heads) || num_splits < 0) return 0;
-  return (size_t)workspace_bytes(batch, heads, decode_grid(num_splits));
+  if (batch < 0 || batch > kMaxBatch || !heads_ok(heads) || num_splits < 0 || num_splits > kMaxSplits) return 0;
+  return (size_t)workspace_bytes(batch, heads, decode_grid(num_splits, heads));
 }
 
 mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
@@ -145,7 +160,8 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
                                float* lse, int32_t* dev_err, mla_stream_t stream) {
   PageLayout L;
   if (!cache_ok(cache, &L)) return MLA_ERR_INVALID_ARG;
-  if (batch < 0 || batch > kMaxBatch || !heads_ok(heads) || num_splits < 0) return MLA_ERR_INVALID_ARG;
+  if (batch < 0 || batch > kMaxBatch || !heads_ok(heads) || num_splits < 0 || num_splits > kMaxSplits)
+    return MLA_ERR_INVALID_ARG;
   if (batch == 0) return MLA_OK;
   if (max_pages <= 0 || (int64_t)max_pages * kPage > (int64_t)INT32_MAX) return MLA_ERR_INVALID_ARG;
   // every 32-token chunk of the batch gets a 32-bit index
@@ -156,7 +172,7 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
       (dev_err && !aligned(dev_err, 4)))
     return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
-  int G = decode_grid(num_splits);
+  int G = decode_grid(num_splits, heads);
   if ((int64_t)workspace_bytes_ < workspace_bytes(batch, heads, G)) return MLA_ERR_INVALID_ARG;
   DecodeParams p;
   p.pool = (const uint8_t*)cache->pool;
@@ -175,6 +191,7 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
   p.H = heads;
   p.G = G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.wait_ns = wait_limit_ns();
   p.ws = carve_workspace(workspace, batch, heads, G);
   p.o_lat = o_lat;
   p.lse = lse;

@@ -20,11 +20,9 @@
 // tokens are recomputed exactly in fp32 there instead.  Scores are kept in
 // the log2 domain (scaled by log2 e).
 //
-// This translation unit holds the partition, the combine kernels with the
-// exact short-sequence path, and the reference decode kernel (fp32 CUDA
-// cores, dequantized chunk in shared memory).
+// This translation unit holds the combine kernels with the exact
+// short-sequence path (fp32 CUDA cores, dequantized block in shared memory).
 #include <math.h>
-#include <stdlib.h>
 
 #include "mla_internal.cuh"
 
@@ -32,8 +30,6 @@ namespace mla {
 
 namespace {
 
-constexpr int kHT = 16;          // heads per CTA
-constexpr int kThreads = 256;
 constexpr int kCS = kDc + 1;     // padded row stride of the latent chunk (floats)
 constexpr int kKS = kDr + 1;     // padded row stride of the k_pe chunk
 
@@ -44,38 +40,6 @@ __device__ __forceinline__ int checked_len(const DecodeParams& p, int b, bool re
     len = 0;
   }
   return len;
-}
-
-// Exclusive prefix sum of chunk counts into cum[0..B] (warp 0 of the CTA).
-__device__ void chunk_prefix(const DecodeParams& p, int32_t* cum, bool report) {
-  const int lane = threadIdx.x & 31;
-  if (threadIdx.x < 32) {
-    int carry = 0;
-    for (int base = 0; base < p.B; base += 32) {
-      const int b = base + lane;
-      int v = 0;
-      if (b < p.B) v = (checked_len(p, b, report) + kChunk - 1) / kChunk;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, v, off);
-        if (lane >= off) v += t;
-      }
-      if (b < p.B) cum[b + 1] = carry + v;
-      carry += __shfl_sync(0xffffffffu, v, 31);
-    }
-    if (lane == 0) cum[0] = 0;
-  }
-}
-
-// Largest b with cum[b] <= c (c < cum[B]).
-__device__ __forceinline__ int seq_of_chunk(const int32_t* cum, int B, int64_t c) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cum[mid] <= c) lo = mid; else hi = mid - 1;
-  }
-  while (lo + 1 < B && cum[lo + 1] <= c) ++lo;  // skip empty sequences
-  return lo;
 }
 
 // Dequantizes tokens t0 .. t0 + 31 of sequence b (one 32-token block of a
@@ -212,150 +176,6 @@ __device__ void dequant_chunk(const DecodeParams& p, int b, int t0, int len, flo
 #pragma unroll
       for (int j = 0; j < 4; ++j) s_k[t * kKS + 4 * wi + j] = v[j];
     }
-  }
-}
-
-template <int LF, int KF>
-__global__ void __launch_bounds__(kThreads) decode_ref_kernel(DecodeParams p) {
-  pdl_launch_dependents();
-  pdl_wait();
-  extern __shared__ __align__(16) float smem[];
-  float* s_qlat = smem;                       // [16][512]
-  float* s_qpe = s_qlat + kHT * kDc;          // [16][64]
-  float* s_c = s_qpe + kHT * kDr;             // [32][513]
-  float* s_k = s_c + kChunk * kCS;            // [32][65]
-  float* s_p = s_k + kChunk * kKS;            // [16][32]
-  float* s_alpha = s_p + kHT * kChunk;        // [16]
-  float* s_m = s_alpha + kHT;                 // [16]
-  float* s_l = s_m + kHT;                     // [16]
-  int32_t* s_valid = reinterpret_cast<int32_t*>(s_l + kHT);   // [32]
-  int32_t* s_page = s_valid + kChunk;                         // [32]
-  int32_t* cum = s_page + kChunk;                             // [B + 1]
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int x = blockIdx.x, G = gridDim.x, h0 = blockIdx.y * kHT;
-  const bool lead = (blockIdx.x == 0 && blockIdx.y == 0);
-
-  chunk_prefix(p, cum, lead);
-  __syncthreads();
-  if (lead)
-    for (int i = tid; i <= p.B; i += kThreads) p.ws.cum[i] = cum[i];
-
-  const int64_t C = cum[p.B];
-  const int Ge = (int64_t)G < C ? G : (int)C;          // no empty ranges
-  if (x >= Ge) return;
-  const int64_t c_lo = range_lo(C, x, Ge), c_end = range_lo(C, x + 1, Ge);
-  int64_t c = c_lo;
-
-  while (c < c_end) {
-    const int b = seq_of_chunk(cum, p.B, c);
-    const int64_t seg_end = c_end < (int64_t)cum[b + 1] ? c_end : (int64_t)cum[b + 1];
-    const int len = checked_len(p, b, false);
-    const int slot = x + b;
-
-    __syncthreads();
-    for (int i = tid; i < kHT * kDc; i += kThreads)
-      s_qlat[i] = p.q_lat[((size_t)b * p.H + h0 + i / kDc) * kDc + i % kDc];
-    for (int i = tid; i < kHT * kDr; i += kThreads)
-      s_qpe[i] = bf16f(p.q_pe[((size_t)b * p.H + h0 + i / kDr) * kDr + i % kDr]);
-    if (tid < kHT) {
-      s_m[tid] = -INFINITY;
-      s_l[tid] = 0.f;
-    }
-    float o0[kHT], o1[kHT];
-#pragma unroll
-    for (int h = 0; h < kHT; ++h) o0[h] = o1[h] = 0.f;
-
-    for (int64_t ch = c - cum[b]; ch < seg_end - cum[b]; ++ch) {
-      const int t0 = (int)ch * kChunk;
-      dequant_chunk<LF, KF, kThreads>(p, b, t0, len, s_c, s_k, s_valid, s_page);
-      __syncthreads();
-
-      // ---- scores: thread -> head tid/16, tokens 2*(tid%16) and +1
-      {
-        const int h = tid >> 4, tp = (tid & 15) * 2;
-        const float* q = s_qlat + h * kDc;
-        const float* r0 = s_c + tp * kCS;
-        const float* r1 = r0 + kCS;
-        float a0 = 0.f, a1 = 0.f;
-        for (int i = 0; i < kDc; ++i) {
-          a0 = fmaf(q[i], r0[i], a0);
-          a1 = fmaf(q[i], r1[i], a1);
-        }
-        const float* qp = s_qpe + h * kDr;
-        const float* k0 = s_k + tp * kKS;
-        const float* k1 = k0 + kKS;
-        for (int i = 0; i < kDr; ++i) {
-          a0 = fmaf(qp[i], k0[i], a0);
-          a1 = fmaf(qp[i], k1[i], a1);
-        }
-        s_p[h * kChunk + tp] = s_valid[tp] ? a0 * p.scale_log2 : -INFINITY;
-        s_p[h * kChunk + tp + 1] = s_valid[tp + 1] ? a1 * p.scale_log2 : -INFINITY;
-      }
-      __syncthreads();
-
-      // ---- online softmax: warp w owns heads 2w, 2w+1; lane = token
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int h = 2 * warp + r;
-        const float v = s_p[h * kChunk + lane];
-        float mx = v;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        const float m_old = s_m[h];
-        const float m_new = fmaxf(m_old, mx);
-        float alpha = 1.f, pv = 0.f;
-        if (m_new != -INFINITY) {
-          alpha = exp2f(m_old - m_new);
-          pv = exp2f(v - m_new);
-        }
-        float sum = pv;
-#pragma unroll
-        for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-        s_p[h * kChunk + lane] = pv;
-        __syncwarp();
-        if (lane == 0) {
-          s_m[h] = m_new;
-          s_l[h] = s_l[h] * alpha + sum;
-          s_alpha[h] = alpha;
-        }
-      }
-      __syncthreads();
-
-      // ---- P V: thread owns channels tid and tid + 256 for all 16 heads
-#pragma unroll
-      for (int h = 0; h < kHT; ++h) {
-        o0[h] *= s_alpha[h];
-        o1[h] *= s_alpha[h];
-      }
-      for (int t = 0; t < kChunk; ++t) {
-        const float v0 = s_c[t * kCS + tid], v1 = s_c[t * kCS + tid + kThreads];
-#pragma unroll
-        for (int h = 0; h < kHT; ++h) {
-          const float pv = s_p[h * kChunk + t];
-          o0[h] = fmaf(pv, v0, o0[h]);
-          o1[h] = fmaf(pv, v1, o1[h]);
-        }
-      }
-    }
-
-    // ---- partial of (sequence b, this CTA) -> slot x + b
-    __syncthreads();
-    if (tid == 0 && blockIdx.y == 0) {
-      if (c_lo <= cum[b]) p.ws.span[2 * b] = x;
-      if (c_end >= cum[b + 1]) p.ws.span[2 * b + 1] = x;
-    }
-    if (tid < kHT) {
-      p.ws.m[(size_t)slot * p.H + h0 + tid] = s_m[tid];
-      p.ws.l[(size_t)slot * p.H + h0 + tid] = s_l[tid];
-    }
-#pragma unroll
-    for (int h = 0; h < kHT; ++h) {
-      float* dst = p.ws.o + ((size_t)slot * p.H + h0 + h) * kDc;
-      dst[tid] = o0[h];
-      dst[tid + kThreads] = o1[h];
-    }
-    c = seg_end;
   }
 }
 
@@ -738,45 +558,6 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
   }
 }
 
-template <int LF, int KF>
-mla_status launch_ref_t(const DecodeParams& p, cudaStream_t stream) {
-  const size_t smem = sizeof(float) * (kHT * kDc + kHT * kDr + kChunk * kCS + kChunk * kKS + kHT * kChunk + 3 * kHT) +
-                      sizeof(int32_t) * (2 * kChunk + p.B + 1);
-  static int configured[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    const mla_status st = cuda_status(
-        cudaFuncSetAttribute(decode_ref_kernel<LF, KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
-    if (st != MLA_OK) return st;
-    if (dev >= 0 && dev < 64) configured[dev] = 1;
-  }
-  return cuda_status(launch_pdl(decode_ref_kernel<LF, KF>, dim3(p.G, p.H / kHT), dim3(kThreads), smem, stream, p));
-}
-
-mla_status launch_decode_ref(const DecodeParams& p, cudaStream_t stream) {
-#define MLA_DECODE_CASE(A, K) \
-  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_ref_t<A, K>(p, stream);
-  MLA_DECODE_CASE(MLA_FMT_BF16, MLA_FMT_BF16)
-  MLA_DECODE_CASE(MLA_FMT_BF16, MLA_FMT_INT8_SYM)
-  MLA_DECODE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_BF16)
-  MLA_DECODE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT8_SYM)
-  MLA_DECODE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_BF16)
-  MLA_DECODE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT8_SYM)
-  MLA_DECODE_CASE(MLA_FMT_INT4_SYM, MLA_FMT_BF16)
-  MLA_DECODE_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT8_SYM)
-  MLA_DECODE_CASE(MLA_FMT_BF16, MLA_FMT_INT4_SYM)
-  MLA_DECODE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_INT4_SYM)
-  MLA_DECODE_CASE(MLA_FMT_INT4_ASYM, MLA_FMT_INT4_SYM)
-  MLA_DECODE_CASE(MLA_FMT_INT4_SYM, MLA_FMT_INT4_SYM)
-  MLA_DECODE_CASE(MLA_FMT_INT8_G8, MLA_FMT_INT8_SYM)
-  MLA_DECODE_CASE(MLA_FMT_INT8_G32, MLA_FMT_INT8_SYM)
-  MLA_DECODE_CASE(MLA_FMT_INT8_G64, MLA_FMT_INT8_SYM)
-  MLA_DECODE_CASE(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM)
-#undef MLA_DECODE_CASE
-  return MLA_ERR_UNSUPPORTED;
-}
-
 }  // namespace
 
 namespace {
@@ -838,9 +619,7 @@ mla_status launch_combine(const DecodeParams& p, cudaStream_t stream) {
 }  // namespace
 
 mla_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
-  static const bool force_ref = getenv("MLA_DEBUG_REFERENCE_DECODE") != nullptr;
-  mla_status st = force_ref ? MLA_ERR_UNSUPPORTED : launch_decode_mma(p, stream);
-  if (st == MLA_ERR_UNSUPPORTED) st = launch_decode_ref(p, stream);
+  const mla_status st = launch_decode_mma(p, stream);
   if (st != MLA_OK) return st;
   return launch_combine(p, stream);
 }

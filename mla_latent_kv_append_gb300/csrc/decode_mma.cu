@@ -107,9 +107,11 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Bounded wait on an mbarrier phase.  Returns false after ~10 s without
-// completion; the caller records MLA_DEVERR_TIMEOUT and stops.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Bounded wait on an mbarrier phase.  Returns false once limit_ns have
+// passed without completion (checked every 256 polls, or at every poll when
+// the limit is 0); the caller records MLA_DEVERR_TIMEOUT and gives up its
+// work.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   uint32_t done = 0;
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
@@ -119,13 +121,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         : "r"(bar), "r"(parity)
         : "memory");
     if (done) return true;
-    if ((it & 255) == 0) {
-      const uint64_t now = global_ns();
-      if (it == 0) t0 = now;
-      else if (now - t0 > 10000000000ull) return false;
-    }
+    if (it == 0) t0 = global_ns();
+    else if (((it & 255) == 0 || limit_ns == 0) && global_ns() - t0 > limit_ns) return false;
   }
 }
+
+// Limit of the loader's final wait for its own bulk copies: those land within
+// microseconds unless the memory system itself is stuck.
+constexpr uint64_t kDrainLimitNs = 10000000000ull;
 
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
@@ -689,7 +692,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   int32_t* cum = reinterpret_cast<int32_t*>(cwq + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int x = blockIdx.x, G = gridDim.x, h0 = blockIdx.y * kHT;
+  // grid (H / 16, G): the head tiles of one split are neighbours in launch
+  // order, so they run side by side and share the split's pages through L2
+  const int x = blockIdx.y, G = gridDim.y, h0 = blockIdx.x * kHT;
   const bool lead = (blockIdx.x == 0 && blockIdx.y == 0);
 
   if (p.lens_after_wait) pdl_wait();     // the lengths come from the kernel just before
@@ -795,7 +800,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
         l_row = 0.f;
       }
       if (t == 0) plan();
-      if (!mbar_wait(smem_u32(&bx[i & 1]), (uint32_t)((i >> 1) & 1))) {
+      if (!mbar_wait(smem_u32(&bx[i & 1]), (uint32_t)((i >> 1) & 1), p.wait_ns)) {
         set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
         dead = true;
         break;
@@ -849,7 +854,26 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       mbar_arrive(smem_u32(&bp[buf]));
       if (++s == F::kStages) s = 0;
     }
-    if (!dead && b >= 0) flush_ml(b);
+    if (!dead) {
+      if (b >= 0) flush_ml(b);
+    } else {
+      // gave up: empty partials (weight 0) for the sequence in hand and every
+      // later one of the range, so that the combine reads finite values
+      m_row = -INFINITY;
+      l_row = 0.f;
+      for (int bb = b >= 0 ? b : seq_of_chunk(cum, p.B, c_lo); bb < p.B && cum[bb] < c_hi; ++bb)
+        if (cum[bb] < cum[bb + 1]) flush_ml(bb);
+    }
+    if (t == 0) {
+      // the loader leaves only once every bulk copy it issued has landed, so
+      // that no copy writes into the shared memory of a block that has exited
+      const int issued = ld_c - c_lo;
+      for (int k = issued > F::kStages ? issued - F::kStages : 0; k < issued; ++k)
+        if (!mbar_wait(smem_u32(&full_bar[k % F::kStages]), (uint32_t)((k / F::kStages) & 1), kDrainLimitNs)) {
+          set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+          break;
+        }
+    }
     return;
   }
 
@@ -867,7 +891,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
 
   auto flush_o = [&](int bb) {
     const size_t slot = (size_t)x + bb;
-    if (tid == 0 && blockIdx.y == 0) {
+    if (tid == 0 && blockIdx.x == 0) {
       if (c_lo <= cum[bb]) p.ws.span[2 * bb] = x;
       if (c_hi >= cum[bb + 1]) p.ws.span[2 * bb + 1] = x;
     }
@@ -891,7 +915,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   auto finish_prev = [&](const ChunkRegs& prev) -> bool {
     if (!pending) return true;
     const int pi = i - 1;
-    if (!mbar_wait(smem_u32(&bp[pi & 1]), (uint32_t)((pi >> 1) & 1))) {
+    if (!mbar_wait(smem_u32(&bp[pi & 1]), (uint32_t)((pi >> 1) & 1), p.wait_ns)) {
       set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
       return false;
     }
@@ -911,7 +935,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       const float am = warp_max(load_query_raw<LF, KF>(p, b, h0, w, lane, raw));
       if (lane == 0) amax_s[w] = am;
       mbar_arrive(smem_u32(qa));
-      if (!mbar_wait(smem_u32(qa), qphase)) {
+      if (!mbar_wait(smem_u32(qa), qphase, p.wait_ns)) {
         set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
         return false;
       }
@@ -933,7 +957,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
 #pragma unroll
           for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
     }
-    if (!mbar_wait(smem_u32(&full_bar[s]), phase)) {
+    if (!mbar_wait(smem_u32(&full_bar[s]), phase, p.wait_ns)) {
       set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
       return false;
     }
@@ -974,6 +998,19 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   if (!dead) {
     const bool ok = last_in_a ? finish_prev(ra) : finish_prev(rb);
     if (ok && b >= 0) flush_o(b);
+    dead = !ok;
+  }
+  if (dead) {
+    // gave up: empty partials (o = 0) and the span entries for the sequence
+    // in hand and every later one of the range
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
+    for (int bb = b >= 0 ? b : seq_of_chunk(cum, p.B, c_lo); bb < p.B && cum[bb] < c_hi; ++bb)
+      if (cum[bb] < cum[bb + 1]) flush_o(bb);
   }
 }
 
@@ -1004,7 +1041,7 @@ mla_status launch_t(const DecodeParams& p, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) configured[dev] = 1;
   }
   if (smem + kWsExtra > smem_max()) return MLA_ERR_UNSUPPORTED;
-  return cuda_status(launch_pdl(decode_mma_kernel<LF, KF>, dim3(p.G, p.H / kHT), dim3(kWsThreads), smem + kWsExtra,
+  return cuda_status(launch_pdl(decode_mma_kernel<LF, KF>, dim3(p.H / kHT, p.G), dim3(kWsThreads), smem + kWsExtra,
                                 stream, p));
 }
 

@@ -20,6 +20,7 @@ constexpr int kNLG = kDc / kLG;            // 32 latent groups
 constexpr int kNKG = kDr / kKG;            // 8 k_pe groups
 constexpr int kChunk = 32;                 // decode work unit: 32 tokens
 constexpr int kMaxBatch = 4096;
+constexpr int kMaxSplits = 65535;          // decode grid dimension y
 constexpr int kMaxMergeParts = 4096;         // mla_lse_merge: most parts per call
 
 // Byte layout of one page; see mla_page_layout in mla.h.  A page is two
@@ -116,7 +117,7 @@ __device__ __forceinline__ void set_err(int32_t* dev_err, int bit) {
 
 // Split-K partial workspace:
 //   [cum: B+1 int32 | span: 2B int32 | m: slots*H | l: slots*H | o: slots*H*512]
-// span[2b], span[2b+1] = first and last CTA (grid x) that worked on sequence b.
+// span[2b], span[2b+1] = first and last split (CTA column) that worked on sequence b.
 struct Workspace {
   int32_t* cum;
   int32_t* span;
@@ -192,6 +193,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // Host side launch helpers (api.cu)
 int device_sm_count();
+uint64_t wait_limit_ns();                // set by mla_set_wait_limit_ns
 mla_status launch_status();
 mla_status cuda_status(cudaError_t e);   // records the error string on failure
 
@@ -220,6 +222,7 @@ struct DecodeParams {
                           // prefill's lengths): read it only after waiting on that kernel
   int B, H, G;
   float scale_log2;       // softmax_scale * log2(e)
+  uint64_t wait_ns;       // bound on every wait inside the decode kernel (wait_limit_ns())
   Workspace ws;
   float* o_lat;
   float* lse;

@@ -101,6 +101,7 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
     p.H = heads;
     p.G = G;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.wait_ns = wait_limit_ns();
     p.ws = carve_workspace(split_ws, s, heads, G);
     p.o_lat = o_lat + (size_t)i0 * heads * kDc;
     p.lse = lse ? lse + (size_t)i0 * heads : nullptr;

@@ -13,6 +13,8 @@ The functions here hold the host-side plan and exchange; the decode and the
 merge are the library's kernels.
 """
 
+import contextlib
+
 import torch
 import torch.distributed as dist
 
@@ -66,11 +68,16 @@ def sharded_decode(cache, q_lat, q_pe, block_table, seq_lens, workspace, o_lat, 
                    softmax_scale=None, num_splits=0, stream=None):
     """Decode over this rank's pages (block_table / seq_lens are already the
     local view, e.g. from local_block_table), then exchange and merge, so
-    every rank ends with the attention over the whole context in o_lat / lse."""
-    part_o = torch.empty_like(o_lat)
-    part_l = torch.empty_like(lse)
-    mla.mla_decode_absorbed(cache, q_lat, q_pe, block_table, seq_lens, workspace, part_o, part_l, dev_err,
-                            softmax_scale=softmax_scale, num_splits=num_splits, stream=stream)
-    o_parts, l_parts = gather_partials(part_o, part_l, group)
-    mla.mla_lse_merge(o_parts, l_parts, o_lat, lse, stream=stream)
+    every rank ends with the attention over the whole context in o_lat / lse.
+
+    With ``stream`` given, every step runs on it: the collective of the
+    all-gather is ordered against torch's current stream, so the body makes
+    ``stream`` current for the decode, the gather and the merge alike."""
+    with torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext():
+        part_o = torch.empty_like(o_lat)
+        part_l = torch.empty_like(lse)
+        mla.mla_decode_absorbed(cache, q_lat, q_pe, block_table, seq_lens, workspace, part_o, part_l, dev_err,
+                                softmax_scale=softmax_scale, num_splits=num_splits)
+        o_parts, l_parts = gather_partials(part_o, part_l, group)
+        mla.mla_lse_merge(o_parts, l_parts, o_lat, lse)
     return o_lat

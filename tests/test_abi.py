@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
-    assert lib.abi_version() == 102
+    assert lib.abi_version() == 103
 
 
 def test_layouts_match_the_accounting(lib):
@@ -121,3 +121,17 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert raw.mla_prefill_workspace_bytes(100, 16) <= raw.mla_prefill_workspace_bytes(5000, 16)
     assert raw.mla_prefill_workspace_bytes(5000, 16) == raw.mla_prefill_workspace_bytes(50000, 16)
     assert raw.mla_status_string(4) == b"device-side bounds error"
+
+
+def test_wait_limit_hook(lib):
+    """The wait-limit hook only sets a host-side value: set, read back,
+    reject a negative limit, restore."""
+    prev = lib.mla_set_wait_limit_ns(12345)
+    try:
+        assert lib.mla_set_wait_limit_ns(777) == 12345
+        with pytest.raises(ValueError):
+            lib.mla_set_wait_limit_ns(-1)
+        assert lib.mla_set_wait_limit_ns(777) == 777
+    finally:
+        lib.mla_set_wait_limit_ns(prev)
+    assert prev == 10 ** 10

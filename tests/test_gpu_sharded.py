@@ -70,3 +70,42 @@ def test_merge_empty_parts_and_single_part():
     assert np.all(got[1] == 0) and np.all(np.isneginf(got_lse[1]))
     assert A.max_rel_error(one.cpu().numpy()[[0, 2]], on[0][[0, 2]]) < 1e-6
     assert np.max(np.abs(one_lse.cpu().numpy()[[0, 2]] - ln[0][[0, 2]])) < 1e-6
+
+
+def test_sharded_decode_on_a_side_stream():
+    """sharded_decode with a stream that is not torch's current one, in a
+    one-rank NCCL group: the decode, the all-gather and the merge must all be
+    ordered on that stream, and the result equals the plain decode."""
+    import datetime
+    import os
+    import socket
+
+    import torch.distributed as dist
+
+    wl = Workload(1, 16, [5000, 300], mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, seed=91)
+    step = DecodeStep(wl)
+    step.run()
+    torch.cuda.synchronize()
+    ref_o, ref_lse = step.o_lat.clone(), step.lse[0].clone()
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
+    dist.init_process_group("nccl", init_method="tcp://127.0.0.1:%d" % port, rank=0, world_size=1,
+                            timeout=datetime.timedelta(seconds=120))
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        o_lat = torch.full_like(ref_o, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        for _ in range(3):
+            sharded.sharded_decode(wl.caches[0], step.q_lat, wl.q_pe[0], wl.block_table, wl.seq_lens_dev,
+                                   step.workspace, o_lat, lse, dev_err=step.dev_err, stream=side)
+        side.synchronize()
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    assert step.dev_err.item() == 0
+    # one part: the merge of a single part reproduces it up to the lse rounding
+    assert A.max_rel_error(o_lat.cpu().numpy(), ref_o.cpu().numpy()) < 1e-5
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse.cpu().numpy())) < 1e-5

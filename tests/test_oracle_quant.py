@@ -269,3 +269,20 @@ def test_error_kpe_int8_below_latent_int8():
     e_lat = Q.relative_error(x, Q.dequantize_sym_int8(*Q.quantize_sym_int8(x, 16), 16))[0]
     e_kpe = Q.relative_error(k, Q.dequantize_sym_int8(*Q.quantize_sym_int8(k, 8), 8))[0]
     assert e_kpe < e_lat
+
+
+def test_relative_error_literal_values():
+    """The error metric behind the ordering checks, pinned by hand-computed
+    values: mean |x - x_hat| / mean |x| and max |x - x_hat| / mean |x|."""
+    # e = [0.5, 0]; mean|x| = 1.5 -> mean 0.25 / 1.5 = 1/6, max 0.5 / 1.5 = 1/3
+    m, mx = Q.relative_error([1.0, 2.0], [1.5, 2.0])
+    assert m == pytest.approx(1 / 6, rel=1e-15) and mx == pytest.approx(1 / 3, rel=1e-15)
+    # signs do not matter; a denominator of max|x| (= 3) would give 1/6, not 1/4
+    m, mx = Q.relative_error([-1.0, -3.0], [-1.0, -2.0])
+    assert m == pytest.approx(0.25, rel=1e-15) and mx == pytest.approx(0.5, rel=1e-15)
+    # the mean runs over every element of a 2-D tensor: e = [0, 0, 0, 2],
+    # mean|x| = 10 / 4 -> mean 0.5 / 2.5 = 0.2, max 2 / 2.5 = 0.8
+    m, mx = Q.relative_error([[1.0, 2.0], [3.0, 4.0]], [[1.0, 2.0], [3.0, 2.0]])
+    assert m == pytest.approx(0.2, rel=1e-15) and mx == pytest.approx(0.8, rel=1e-15)
+    # no error at all
+    assert Q.relative_error([0.5, -7.0, 3.0], [0.5, -7.0, 3.0]) == (0.0, 0.0)
