@@ -210,8 +210,9 @@ mla_status mla_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_l
 /*
  * mla_decode_workspace_bytes - bytes of device workspace mla_decode_absorbed
  * needs for this batch, head count and num_splits (0 = automatic).  The
- * workspace holds the split-K partials (per split: running max, running sum
- * and the unnormalised 512-wide latent output, fp32, per head).
+ * workspace holds the split-K partials (per split and head, fp32: running
+ * max, running sum, the weight of the fp16 P V products and the
+ * unnormalised 512-wide latent output).
  */
 size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_splits);
 
@@ -239,9 +240,13 @@ size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_spli
  *   the scores use exact products (q_lat split into two fp16 parts against
  *   the exact codes); P enters the P V products as fp16 times the fp16
  *   group scale, which costs ~2-6e-4 relative error over long contexts.
- *   Sequences shorter than 256 tokens are recomputed in fp32.  Every row
- *   is tested to a max relative error below 2e-3 (o_lat) and 2e-3
- *   absolute (lse).
+ *   Two kinds of rows are recomputed in fp32 from the cache instead:
+ *   sequences shorter than 256 tokens, and rows whose output is a small
+ *   residual of heavily weighted tokens (latents that cancel), detected
+ *   from the partials as sqrt(sum_t (w_t M_t)^2) > 3 |o_lat row|_inf, with
+ *   w_t the softmax weights and M_t a bound on |c_hat_t| from its scales.
+ *   Every row is tested to a max relative error below 2e-3 (o_lat) and
+ *   2e-3 absolute (lse).
  *   A page id outside [0, num_pages) contributes nothing and sets
  *   MLA_DEVERR_PAGE; seq_len outside [0, max_pages*64] is treated as 0 and
  *   sets MLA_DEVERR_SEQLEN.  B == 0 is a no-op.  B <= 4096, and

@@ -69,6 +69,12 @@ struct Fmt {
   // 2j+1 and 8+2j, 8+2j+1) for bf16 and 8-channel groups, else permuted
   // (thread j holds channels 4j .. 4j+3)
   static constexpr bool kStdLayout = kLatBf16 || kLatG8;
+  static constexpr int kNG = kDc / kGS;                          // scale groups per token
+  // quantized latents: the softmax warps also accumulate, per head row, the
+  // weight of the fp16 P V products (sum of (p_t M_t)^2, M_t a bound on the
+  // token's |c_hat|), from which the combine decides whether the row needs
+  // the exact fp32 recomputation
+  static constexpr bool kRisk = !kLatBf16;
   static constexpr int kScaleOff = kBlockTokens * kRow;
   static constexpr int kZeroOff = kScaleOff + (kLatBf16 ? 0 : (kDc / kGS) * kBlockTokens * 4);
   static constexpr int kKpeOff = kZeroOff + (LF == MLA_FMT_INT4_ASYM ? kNLG * kBlockTokens * 4 : 0);
@@ -124,6 +130,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     if (it == 0) t0 = global_ns();
     else if (((it & 255) == 0 || limit_ns == 0) && global_ns() - t0 > limit_ns) return false;
   }
+}
+
+// mbar_wait by every lane of a warp, with a warp-uniform answer: a lane
+// that gave up makes the whole warp give up, so that the warp leaves its
+// loops together (its mma.sync, ldmatrix and shuffles need all lanes).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, limit_ns));
 }
 
 // Limit of the loader's final wait for its own bulk copies: those land within
@@ -251,6 +264,26 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+// Bound on max_c |c_hat[u][c]| of token u of a staged block, from its scales
+// (and zero-points): |q| s <= 127 s (INT8), <= 8 s (4-bit symmetric, stored
+// as code + 8), |q - z| s <= max(|z|, |15 - z|) s (asymmetric INT4).
+template <int LF, int KF>
+__device__ __forceinline__ float latent_bound(const uint8_t* st, int u) {
+  using F = Fmt<LF, KF>;
+  const float* sc = reinterpret_cast<const float*>(st + F::kScaleOff);
+  float mb = 0.f;
+  if (LF == MLA_FMT_INT4_ASYM) {
+    const float* zp = reinterpret_cast<const float*>(st + F::kZeroOff);
+#pragma unroll 8
+    for (int g = 0; g < kNLG; ++g)
+      mb = fmaxf(mb, sc[g * kBlockTokens + u] * (fabsf(zp[g * kBlockTokens + u] - 7.5f) + 7.5f));
+    return mb;
+  }
+#pragma unroll 8
+  for (int g = 0; g < F::kNG; ++g) mb = fmaxf(mb, sc[g * kBlockTokens + u]);
+  return mb * (F::kLatInt4 ? 8.f : 127.f);
 }
 
 __device__ __forceinline__ int checked_len(const DecodeParams& p, int b, bool report) {
@@ -667,7 +700,7 @@ __device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha
 // or i.  Registers move to the compute warps with setmaxnreg (232 each;
 // 40 for the softmax warpgroup; the 384-thread block launches with 168).
 constexpr int kWsThreads = kThreads + 128;
-constexpr int kWsExtra = 5 * 8 + 4 * 4;     // bx[2], bp[2], qa; nvq[2], cwq[2]
+constexpr int kWsExtra = 7 * 8 + 4 * 4 + 64 * 4;   // bx[2], bp[2], qa, mready[2]; nvq[2], cwq[2]; mbuf[2][32]
 
 __device__ __forceinline__ void ws_regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory"); }
 __device__ __forceinline__ void ws_regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory"); }
@@ -686,10 +719,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   uint64_t* bx = full_bar + F::kStages;                                        // [2]
   uint64_t* bp = bx + 2;                                                       // [2]
   uint64_t* qa = bp + 2;                                                       // [1]
-  int32_t* meta = reinterpret_cast<int32_t*>(qa + 1);
+  uint64_t* mready = qa + 1;                                                   // [2]
+  int32_t* meta = reinterpret_cast<int32_t*>(mready + 2);
   int32_t* nvq = meta + F::kStages;                                            // [2]
   float* cwq = reinterpret_cast<float*>(nvq + 2);                              // [2]
-  int32_t* cum = reinterpret_cast<int32_t*>(cwq + 2);
+  float* mbuf = cwq + 2;                                                       // [2][32] token bounds M_t
+  int32_t* cum = reinterpret_cast<int32_t*>(mbuf + 64);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // grid (H / 16, G): the head tiles of one split are neighbours in launch
@@ -722,6 +757,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       mbar_init(smem_u32(&bp[k]), 128);
     }
     mbar_init(smem_u32(qa), kThreads);
+    mbar_init(smem_u32(&mready[0]), 1);
+    mbar_init(smem_u32(&mready[1]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -780,17 +817,42 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
     if (t == 0)
       for (int s = 0; s < F::kStages; ++s) commit(s);
 
-    float m_row = -INFINITY, l_row = 0.f;
+    float m_row = -INFINITY, l_row = 0.f, e2 = 0.f;
     int b = -1, s = 0;
     bool dead = false;
+    const int wsm = warp - kCW, nch = c_hi - c_lo;
     auto flush_ml = [&](int bb) {
+      float e = e2;
+      if (F::kRisk) {
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) e += __shfl_xor_sync(0xffffffffu, e, off);
+      }
       if (tq == 0) {
         const size_t slot = (size_t)x + bb;
         p.ws.m[slot * p.H + h0 + hr] = m_row;
         p.ws.l[slot * p.H + h0 + hr] = l_row;
+        p.ws.e2[slot * p.H + h0 + hr] = e;
       }
     };
-    for (int c = c_lo, i = 0; c < c_hi; ++c, ++i) {
+    // The bounds M_t of chunk k (relative index) go to mbuf[k & 1], written
+    // by softmax warp k % 4 one iteration ahead (lane = token; tokens past the
+    // chunk's end get 0), then mready[k & 1] completes.  The buffer is reused
+    // for chunk k + 2 only after bp of chunk k, i.e. once every softmax thread
+    // has read it; the loader refills a stage only after its bounds are taken.
+    auto produce_bound = [&](int k) -> bool {
+      const int sk = k % F::kStages;
+      if (!mbar_wait_warp(smem_u32(&full_bar[sk]), (uint32_t)((k / F::kStages) & 1), p.wait_ns)) return false;
+      const int nvk = meta[sk];
+      mbuf[(k & 1) * 32 + lane] = lane < nvk ? latent_bound<LF, KF>(stages + sk * F::kBlock, lane) : 0.f;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&mready[k & 1]));
+      return true;
+    };
+    if (F::kRisk && wsm < 2 && wsm < nch && !produce_bound(wsm)) {
+      set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+      dead = true;
+    }
+    for (int c = c_lo, i = 0; c < c_hi && !dead; ++c, ++i) {
       int nb = b < 0 ? seq_of_chunk(cum, p.B, c) : b;
       while (cum[nb + 1] <= c) ++nb;
       if (nb != b) {
@@ -798,14 +860,19 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
         b = nb;
         m_row = -INFINITY;
         l_row = 0.f;
+        e2 = 0.f;
       }
       if (t == 0) plan();
-      if (!mbar_wait(smem_u32(&bx[i & 1]), (uint32_t)((i >> 1) & 1), p.wait_ns)) {
+      if (!mbar_wait_warp(smem_u32(&bx[i & 1]), (uint32_t)((i >> 1) & 1), p.wait_ns) ||
+          (F::kRisk && !mbar_wait_warp(smem_u32(&mready[i & 1]), (uint32_t)((i >> 1) & 1), p.wait_ns))) {
         set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
         dead = true;
         break;
       }
-      if (t == 0) commit(s);                   // every compute warp is past chunk i's stage
+      // every compute warp is past chunk i's stage, and its bounds are taken
+      if (t == 0) commit(s);
+      float4 mb4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (F::kRisk) mb4 = *reinterpret_cast<const float4*>(mbuf + (i & 1) * 32 + 4 * tq);
       const int buf = i & 1, nv = nvq[buf];
       const float cw = cwq[buf];
       // sum the 8 warps' partial scores of 4 tokens of row hr
@@ -840,6 +907,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       for (int off = 1; off < 8; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
       l_row = l_row * al + ps;
       m_row = mn;
+      if (F::kRisk) {
+        const float a0 = pv[0] * mb4.x, a1 = pv[1] * mb4.y, a2 = pv[2] * mb4.z, a3 = pv[3] * mb4.w;
+        e2 = fmaf(e2 * al, al, fmaf(a0, a0, fmaf(a1, a1, fmaf(a2, a2, a3 * a3))));
+      }
       uint2* prow = reinterpret_cast<uint2*>(ptab + ((2 * buf) * kHT + hr) * kPStride) + tq;
       if (F::kLatBf16) {
         uint32_t h0w, l0w, h1w, l1w;
@@ -853,6 +924,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       if (tq == 0) alpha_s[buf * kHT + hr] = al;
       mbar_arrive(smem_u32(&bp[buf]));
       if (++s == F::kStages) s = 0;
+      if (F::kRisk && wsm == ((i + 2) & 3) && i + 2 < nch &&
+          (!mbar_wait_warp(smem_u32(&bp[buf]), (uint32_t)((i >> 1) & 1), p.wait_ns) || !produce_bound(i + 2))) {
+        set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+        dead = true;
+        break;
+      }
     }
     if (!dead) {
       if (b >= 0) flush_ml(b);
@@ -861,6 +938,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       // later one of the range, so that the combine reads finite values
       m_row = -INFINITY;
       l_row = 0.f;
+      e2 = 0.f;
       for (int bb = b >= 0 ? b : seq_of_chunk(cum, p.B, c_lo); bb < p.B && cum[bb] < c_hi; ++bb)
         if (cum[bb] < cum[bb + 1]) flush_ml(bb);
     }
@@ -915,7 +993,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   auto finish_prev = [&](const ChunkRegs& prev) -> bool {
     if (!pending) return true;
     const int pi = i - 1;
-    if (!mbar_wait(smem_u32(&bp[pi & 1]), (uint32_t)((pi >> 1) & 1), p.wait_ns)) {
+    if (!mbar_wait_warp(smem_u32(&bp[pi & 1]), (uint32_t)((pi >> 1) & 1), p.wait_ns)) {
       set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
       return false;
     }
@@ -935,7 +1013,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       const float am = warp_max(load_query_raw<LF, KF>(p, b, h0, w, lane, raw));
       if (lane == 0) amax_s[w] = am;
       mbar_arrive(smem_u32(qa));
-      if (!mbar_wait(smem_u32(qa), qphase, p.wait_ns)) {
+      if (!mbar_wait_warp(smem_u32(qa), qphase, p.wait_ns)) {
         set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
         return false;
       }
@@ -957,7 +1035,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
 #pragma unroll
           for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
     }
-    if (!mbar_wait(smem_u32(&full_bar[s]), phase, p.wait_ns)) {
+    if (!mbar_wait_warp(smem_u32(&full_bar[s]), phase, p.wait_ns)) {
       set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
       return false;
     }

@@ -116,13 +116,17 @@ __device__ __forceinline__ void set_err(int32_t* dev_err, int bit) {
 }
 
 // Split-K partial workspace:
-//   [cum: B+1 int32 | span: 2B int32 | m: slots*H | l: slots*H | o: slots*H*512]
+//   [cum: B+1 int32 | span: 2B int32 | m: slots*H | l: slots*H | e2: slots*H | o: slots*H*512]
 // span[2b], span[2b+1] = first and last split (CTA column) that worked on sequence b.
+// e2: per partial and head, sum_t (p_t M_t)^2 over its tokens (p_t in the
+// partial's scale, M_t a bound on |c_hat_t|): the weight of the split kernel's
+// fp16 P V products, which the combine compares with the merged output.
 struct Workspace {
   int32_t* cum;
   int32_t* span;
   float* m;
   float* l;
+  float* e2;
   float* o;
 };
 
@@ -130,7 +134,7 @@ __host__ __device__ inline int64_t align256(int64_t x) { return (x + 255) & ~(in
 
 __host__ __device__ inline int64_t workspace_bytes(int B, int H, int G) {
   int64_t slots = (int64_t)G + B;
-  return align256((int64_t)(B + 1) * 4) + align256((int64_t)2 * B * 4) + 2 * align256(slots * H * 4) +
+  return align256((int64_t)(B + 1) * 4) + align256((int64_t)2 * B * 4) + 3 * align256(slots * H * 4) +
          slots * H * kDc * 4;
 }
 
@@ -145,6 +149,8 @@ __host__ __device__ inline Workspace carve_workspace(void* base, int B, int H, i
   w.m = (float*)p;
   p += align256(slots * H * 4);
   w.l = (float*)p;
+  p += align256(slots * H * 4);
+  w.e2 = (float*)p;
   p += align256(slots * H * 4);
   w.o = (float*)p;
   return w;

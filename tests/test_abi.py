@@ -63,10 +63,13 @@ def test_workspace_size(lib):
     G, B, H = 10, 3, 16
     slots = G + B
     align = lambda x: (x + 255) // 256 * 256
-    expect = align((B + 1) * 4) + align(2 * B * 4) + 2 * align(slots * H * 4) + slots * H * 512 * 4
+    # chunk prefix sums, spans, then per slot and head: max, sum, the weight
+    # of the fp16 P V products, and the 512-wide unnormalised output
+    expect = align((B + 1) * 4) + align(2 * B * 4) + 3 * align(slots * H * 4) + slots * H * 512 * 4
     assert lib.mla_decode_workspace_bytes(B, H, G) == expect
     assert lib.mla_decode_workspace_bytes(B, 24, G) == 0
     assert lib.mla_decode_workspace_bytes(5000, 16, G) == 0
+    assert lib.mla_decode_workspace_bytes(B, H, 65536) == 0        # more splits than the grid allows
 
 
 def test_invalid_arguments_rejected_on_host(lib):
