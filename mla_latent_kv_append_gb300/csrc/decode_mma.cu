@@ -84,6 +84,10 @@ struct Fmt {
   static constexpr int kXPartBytes = 2 * kCW * kHT * kXStride * 8;   // partial scores [buf][warp][row][pair]
   static constexpr int kPBytes = 4 * kHT * kPStride * 2;              // P tiles [buf][hi, lo]
   static constexpr int kFixed = kStages * kBlock + kXPartBytes + kPBytes + (2 * kHT + kCW) * 4 + kStages * 8 + kStages * 4;
+  // shared-memory offsets that vector accesses rely on: stages and the P
+  // tiles (16 B), the bounds array after alpha / amax (float4 reads)
+  static_assert(kBlock % 128 == 0 && kXPartBytes % 16 == 0 && kPBytes % 16 == 0, "stage / tile alignment");
+  static_assert((kStages * kBlock + kXPartBytes + kPBytes + (2 * kHT + kCW) * 4) % 16 == 0, "bounds alignment");
 };
 
 // ---------------------------------------------------------------------------
@@ -691,10 +695,14 @@ __device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha
 // Warps 0..7 compute QK^T (step A) and PV (step C) of their latent groups;
 // warpgroup 2 (warps 8..11) runs the online softmax (step B) of every chunk
 // and the loader.  Hand-offs go through mbarriers with bounded waits:
-//   bx[i & 1]: the 256 compute threads have written chunk i's partial
-//              scores (and thread 0 its valid-token count and score scale);
-//              the stage of chunk i is free again;
-//   bp[i & 1]: the 128 softmax threads have written chunk i's P and alpha.
+//   bx[i & 1]: the 8 compute warps have written chunk i's partial scores
+//              (and thread 0 its valid-token count and score scale); the
+//              stage of chunk i is free again;
+//   bp[i & 1]: the 4 softmax warps have written chunk i's P and alpha;
+//   mready[i & 1]: the bounds M_t of chunk i's tokens are in mbuf;
+//   qa: the compute warps have posted their query magnitudes.
+// Each warp arrives once, from lane 0 after a __syncwarp that orders the
+// whole warp's stores before the arrival.
 // A compute warp therefore runs A(i), arrives on bx, waits for bp of chunk
 // i - 1 and runs C(i - 1), while the softmax warpgroup works on chunk i - 1
 // or i.  Registers move to the compute warps with setmaxnreg (232 each;
@@ -715,7 +723,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   uint16_t* ptab = reinterpret_cast<uint16_t*>(xpart + 2 * kCW * kHT * kXStride);  // [2 buf][hi, lo][16][kPStride]
   float* alpha_s = reinterpret_cast<float*>(ptab + 4 * kHT * kPStride);        // [2][16]
   float* amax_s = alpha_s + 2 * kHT;                                           // [8]
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(amax_s + kCW);
+  float* mbuf = amax_s + kCW;                      // [2][32] token bounds M_t (16-byte aligned: float4 reads)
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(mbuf + 64);
   uint64_t* bx = full_bar + F::kStages;                                        // [2]
   uint64_t* bp = bx + 2;                                                       // [2]
   uint64_t* qa = bp + 2;                                                       // [1]
@@ -723,8 +732,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   int32_t* meta = reinterpret_cast<int32_t*>(mready + 2);
   int32_t* nvq = meta + F::kStages;                                            // [2]
   float* cwq = reinterpret_cast<float*>(nvq + 2);                              // [2]
-  float* mbuf = cwq + 2;                                                       // [2][32] token bounds M_t
-  int32_t* cum = reinterpret_cast<int32_t*>(mbuf + 64);
+  int32_t* cum = reinterpret_cast<int32_t*>(cwq + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // grid (H / 16, G): the head tiles of one split are neighbours in launch
@@ -753,10 +761,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   } else if (tid == 32) {
     for (int s = 0; s < F::kStages; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
     for (int k = 0; k < 2; ++k) {
-      mbar_init(smem_u32(&bx[k]), kThreads);
-      mbar_init(smem_u32(&bp[k]), 128);
+      mbar_init(smem_u32(&bx[k]), kCW);      // one arrival per compute warp
+      mbar_init(smem_u32(&bp[k]), 4);        // one per softmax warp
     }
-    mbar_init(smem_u32(qa), kThreads);
+    mbar_init(smem_u32(qa), kCW);
     mbar_init(smem_u32(&mready[0]), 1);
     mbar_init(smem_u32(&mready[1]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -922,7 +930,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
         prow[0] = make_uint2(pack_f16(pv[0], pv[1]), pack_f16(pv[2], pv[3]));
       }
       if (tq == 0) alpha_s[buf * kHT + hr] = al;
-      mbar_arrive(smem_u32(&bp[buf]));
+      __syncwarp();                            // the warp's P and alpha stores, then one arrival
+      if (lane == 0) mbar_arrive(smem_u32(&bp[buf]));
       if (++s == F::kStages) s = 0;
       if (F::kRisk && wsm == ((i + 2) & 3) && i + 2 < nch &&
           (!mbar_wait_warp(smem_u32(&bp[buf]), (uint32_t)((i >> 1) & 1), p.wait_ns) || !produce_bound(i + 2))) {
@@ -1012,7 +1021,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       QueryRaw raw;
       const float am = warp_max(load_query_raw<LF, KF>(p, b, h0, w, lane, raw));
       if (lane == 0) amax_s[w] = am;
-      mbar_arrive(smem_u32(qa));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(qa));
       if (!mbar_wait_warp(smem_u32(qa), qphase, p.wait_ns)) {
         set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
         return false;
@@ -1054,7 +1064,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       nvq[i & 1] = nv;
       cwq[i & 1] = cw;
     }
-    mbar_arrive(smem_u32(&bx[i & 1]));
+    __syncwarp();                              // the warp's partial-score stores, then one arrival
+    if (lane == 0) mbar_arrive(smem_u32(&bx[i & 1]));
     if (!finish_prev(prev)) return false;
     pending = true;
     ++i;
