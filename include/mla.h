@@ -366,7 +366,8 @@ const char* mla_last_cuda_error(void);
  * block writes empty partials (weight 0) for the rest of its share of the
  * context and leaves once its own bulk copies have landed.  Nothing traps
  * and the outputs stay finite, but they miss that share of the context.
- * With ns = 0 a wait gives up as soon as its second poll fails.
+ * With ns = 0 a wait polls without suspending and gives up once the GPU's
+ * global timer has advanced (within about a microsecond) without completion.
  */
 int64_t mla_set_wait_limit_ns(int64_t ns);
 

@@ -119,17 +119,25 @@ __device__ __forceinline__ uint64_t global_ns() {
 
 // Bounded wait on an mbarrier phase.  Returns false once limit_ns have
 // passed without completion (checked every 256 polls, or at every poll when
-// the limit is 0); the caller records MLA_DEVERR_TIMEOUT and gives up its
-// work.
+// the limit is 0, which also polls without suspending); the caller records
+// MLA_DEVERR_TIMEOUT and gives up its work.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   uint32_t done = 0;
   uint64_t t0 = 0;
   for (uint32_t it = 0;; ++it) {
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if (limit_ns == 0) {     // no wait at all: the non-blocking probe (try_wait may suspend until completion)
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(done)
+          : "r"(bar), "r"(parity)
+          : "memory");
+    } else {
+      asm volatile(
+          "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(done)
+          : "r"(bar), "r"(parity)
+          : "memory");
+    }
     if (done) return true;
     if (it == 0) t0 = global_ns();
     else if (((it & 255) == 0 || limit_ns == 0) && global_ns() - t0 > limit_ns) return false;
