@@ -243,8 +243,9 @@ size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_spli
  *   Two kinds of rows are recomputed in fp32 from the cache instead:
  *   sequences shorter than 256 tokens, and rows whose output is a small
  *   residual of heavily weighted tokens (latents that cancel), detected
- *   from the partials as sqrt(sum_t (w_t M_t)^2) > 3 |o_lat row|_inf, with
- *   w_t the softmax weights and M_t a bound on |c_hat_t| from its scales.
+ *   from the partials as M sqrt(sum_t w_t^2) > 4 |o_lat row|_inf, with w_t
+ *   the softmax weights and M a bound on |c_hat| from the scales of the
+ *   tokens each split read.
  *   Every row is tested to a max relative error below 2e-3 (o_lat) and
  *   2e-3 absolute (lse).
  *   A page id outside [0, num_pages) contributes nothing and sets

@@ -220,16 +220,17 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
 //    scale) do not average out, and with a peaked softmax they would reach
 //    the 2e-3 bound;
 //  * rows whose split partials carry a large weight of fp16 products against
-//    the merged output: sqrt(sum_t (w_t M_t)^2) > kRiskRatio * |o|_inf, with
-//    w_t the normalised softmax weights and M_t a bound on |c_hat_t| (the
-//    split kernel accumulates the sum per partial).  Over natural data the
-//    ratio stays near 1 (the heavy tokens' latents make up the output);
-//    it grows when heavy tokens' latents cancel, where the fp16 roundings of
-//    their terms would dominate the small result.  The fast path's error is
-//    ~3e-4 times the ratio, so a threshold of 3 keeps rows that are not
-//    recomputed near 1e-3.
+//    the merged output: sqrt(sum_i M_i^2 sum_t w_t^2) > kRiskRatio * |o|_inf,
+//    with w_t the normalised softmax weights and M_i a bound on |c_hat| over
+//    the tokens that partial i's block read (from the scales; the split
+//    kernel stores M_i^2 sum_t p_t^2 per partial).  This bounds the spread
+//    of the fp16 roundings of the P V terms, sqrt(sum_t (w_t |c_hat_t|)^2),
+//    from above.  Over natural data the ratio stays below ~2.5 (the heavy
+//    tokens' latents make up the output); it grows when heavy tokens'
+//    latents cancel, where those roundings dominate the small result (the
+//    fast path's error is a few 1e-4 times the ratio).
 constexpr int kExactLen = 256;
-constexpr float kRiskRatio = 3.f;
+constexpr float kRiskRatio = 4.f;
 constexpr int kShortHeads = 8;             // heads per block of the short-sequence path
 constexpr int kQS = kDc + kDr;             // a head's query row: q_lat, then q_pe
 constexpr int kShortSmemBytes =
@@ -248,49 +249,42 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Attention of sequence b, heads h0 .. h0 + NH - 1 (NH = 8 or 1), over its
-// len tokens, in fp32, straight from the cache.  Per 32-token block:
-// dequantize into shared memory once for the NH heads; 32 / NH warps per
-// head score NH tokens each (lanes over channels, log2 domain); warp j runs
-// head j's online softmax over the block and overwrites the scores with the
-// weights; then thread (c, half) accumulates channel c of heads 4 half ..
-// 4 half + 3 (NH = 8) or thread c channel c of the one head (NH = 1) over
-// the block's tokens.  sm: kShortSmemBytes of shared memory.  Inlined: as a
-// call it left spill code on the combine's common path.
-template <int LF, int KF, int NH>
-__device__ __forceinline__ void exact_rows(const DecodeParams& p, int b, int h0, int len, float* sm) {
-  constexpr int kWPH = 32 / NH;                    // scoring warps per head
-  constexpr int kTPW = kChunk / kWPH;              // tokens per scoring warp and block (= NH)
-  constexpr int kHPT = NH >= 4 ? 4 : 1;            // heads per accumulating thread
+// Attention of sequence b, heads h0 .. h0 + 7, over its len tokens, in fp32,
+// straight from the cache; rows j with bit j of `rows` set are written (o_lat
+// and lse).  Per 32-token block: dequantize into shared memory once for the
+// eight heads; four warps per head score eight tokens each (lanes over
+// channels, log2 domain); warp j runs head j's online softmax over the block
+// and overwrites the scores with the weights; then thread (c, half)
+// accumulates channel c of heads 4 half .. 4 half + 3 over the block's
+// tokens.  sm: kShortSmemBytes of shared memory.  Each combine kernel has a
+// single call site (inlined: as a call it left spill code on the combine's
+// common path, and a second inlined copy slowed that path down).
+template <int LF, int KF>
+__device__ __forceinline__ void exact_rows(const DecodeParams& p, int b, int h0, int len, uint32_t rows, float* sm) {
   float* s_c = sm;                                 // [32][kCS]
   float* s_k = s_c + kChunk * kCS;                 // [32][kKS]
-  float* s_q = s_k + kChunk * kKS;                 // [NH][kQS]
-  float* s_w = s_q + NH * kQS;                     // [32 tokens][NH heads] scores, then weights
-  float* s_al = s_w + kChunk * NH;                 // [NH] the block's rescale factor per head
-  float* s_ml = s_al + NH;                         // [NH][2] final running max and weight sum
-  int32_t* s_valid = reinterpret_cast<int32_t*>(s_ml + 2 * NH);   // [32]
-  int32_t* s_page = s_valid + kChunk;                              // [32]
+  float* s_q = s_k + kChunk * kKS;                 // [8][kQS]
+  float* s_w = s_q + kShortHeads * kQS;            // [32 tokens][8 heads] scores, then weights
+  float* s_al = s_w + kChunk * kShortHeads;        // [8] the block's rescale factor per head
+  float* s_ml = s_al + kShortHeads;                // [8][2] final running max and weight sum
+  int32_t* s_valid = reinterpret_cast<int32_t*>(s_ml + 2 * kShortHeads);  // [32]
+  int32_t* s_page = s_valid + kChunk;                                      // [32]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t row0 = (size_t)b * p.H + h0;
-  for (int i = tid; i < NH * kDc; i += kCombThreads) s_q[(i / kDc) * kQS + i % kDc] = p.q_lat[row0 * kDc + i];
-  for (int i = tid; i < NH * kDr; i += kCombThreads)
+  for (int i = tid; i < kShortHeads * kDc; i += kCombThreads) s_q[(i / kDc) * kQS + i % kDc] = p.q_lat[row0 * kDc + i];
+  for (int i = tid; i < kShortHeads * kDr; i += kCombThreads)
     s_q[(i / kDr) * kQS + kDc + i % kDr] = bf16f(p.q_pe[row0 * kDr + i]);
-  const int sh = warp / kWPH, st0 = (warp % kWPH) * kTPW;   // scoring: head sh, tokens st0 .. st0 + kTPW - 1
+  const int sh = warp >> 2, st0 = (warp & 3) * 8;  // scoring: head sh, tokens st0 .. st0 + 7
   const float* qrow = s_q + sh * kQS;
-  const int c = tid & (kDc - 1), hb = NH >= 4 ? (tid / kDc) * kHPT : 0;
-  const bool accum = NH >= 4 || tid < kDc;
-  float m = -INFINITY, l = 0.f;                    // warps 0 .. NH - 1: head `warp`'s running max and weight sum
-  float acc[kHPT];
-#pragma unroll
-  for (int j = 0; j < kHPT; ++j) acc[j] = 0.f;
+  const int c = tid & (kDc - 1), hb = (tid / kDc) * 4;
+  float m = -INFINITY, l = 0.f;                    // warps 0..7: head `warp`'s running max and weight sum
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int t0 = 0; t0 < len; t0 += kChunk) {
     __syncthreads();                               // the previous block's readers are done; s_q in place
     dequant_chunk<LF, KF, kCombThreads>(p, b, t0, len, s_c, s_k, s_valid, s_page);
     __syncthreads();
-#pragma unroll
-    for (int u = 0; u < kTPW; u += 2) {
+    for (int u = 0; u < 8; u += 2) {
       const int ta = st0 + u;
-      const bool two = kTPW > 1;
       const float* ca = s_c + ta * kCS;
       const float* ka = s_k + ta * kKS;
       float a = 0.f, a2 = 0.f;
@@ -298,67 +292,148 @@ __device__ __forceinline__ void exact_rows(const DecodeParams& p, int b, int h0,
       for (int i = lane; i < kDc; i += 32) {
         const float q = qrow[i];
         a = fmaf(q, ca[i], a);
-        if (two) a2 = fmaf(q, ca[kCS + i], a2);
+        a2 = fmaf(q, ca[kCS + i], a2);
       }
 #pragma unroll
       for (int i = lane; i < kDr; i += 32) {
         const float q = qrow[kDc + i];
         a = fmaf(q, ka[i], a);
-        if (two) a2 = fmaf(q, ka[kKS + i], a2);
+        a2 = fmaf(q, ka[kKS + i], a2);
       }
       a = warp_sum(a);
-      if (two) a2 = warp_sum(a2);
+      a2 = warp_sum(a2);
       if (lane == 0) {
-        s_w[ta * NH + sh] = (t0 + ta < len && s_valid[ta]) ? a * p.scale_log2 : -INFINITY;
-        if (two) s_w[(ta + 1) * NH + sh] = (t0 + ta + 1 < len && s_valid[ta + 1]) ? a2 * p.scale_log2 : -INFINITY;
+        s_w[ta * kShortHeads + sh] = (t0 + ta < len && s_valid[ta]) ? a * p.scale_log2 : -INFINITY;
+        s_w[(ta + 1) * kShortHeads + sh] = (t0 + ta + 1 < len && s_valid[ta + 1]) ? a2 * p.scale_log2 : -INFINITY;
       }
     }
     __syncthreads();
-    if (warp < NH) {
-      const float sv = s_w[lane * NH + warp];
+    if (warp < kShortHeads) {
+      const float sv = s_w[lane * kShortHeads + warp];
       const float mn = fmaxf(m, warp_max(sv));
       const float w = mn == -INFINITY ? 0.f : exp2f(sv - mn);
       const float al = mn == -INFINITY ? 1.f : exp2f(m - mn);
-      s_w[lane * NH + warp] = w;
+      s_w[lane * kShortHeads + warp] = w;
       if (lane == 0) s_al[warp] = al;
       l = fmaf(l, al, warp_sum(w));
       m = mn;
     }
     __syncthreads();
-    if constexpr (kHPT == 4) {
-      const float4 al = *reinterpret_cast<const float4*>(s_al + hb);
-      acc[0] *= al.x;
-      acc[1] *= al.y;
-      acc[2] *= al.z;
-      acc[3] *= al.w;
+    const float4 al = *reinterpret_cast<const float4*>(s_al + hb);
+    acc[0] *= al.x;
+    acc[1] *= al.y;
+    acc[2] *= al.z;
+    acc[3] *= al.w;
 #pragma unroll 8
-      for (int t = 0; t < kChunk; ++t) {
-        const float v = s_c[t * kCS + c];
-        const float4 w = *reinterpret_cast<const float4*>(s_w + t * NH + hb);
-        acc[0] = fmaf(w.x, v, acc[0]);
-        acc[1] = fmaf(w.y, v, acc[1]);
-        acc[2] = fmaf(w.z, v, acc[2]);
-        acc[3] = fmaf(w.w, v, acc[3]);
-      }
-    } else if (accum) {
-      acc[0] *= s_al[0];
-#pragma unroll 8
-      for (int t = 0; t < kChunk; ++t) acc[0] = fmaf(s_w[t * NH], s_c[t * kCS + c], acc[0]);
+    for (int t = 0; t < kChunk; ++t) {
+      const float v = s_c[t * kCS + c];
+      const float4 w = *reinterpret_cast<const float4*>(s_w + t * kShortHeads + hb);
+      acc[0] = fmaf(w.x, v, acc[0]);
+      acc[1] = fmaf(w.y, v, acc[1]);
+      acc[2] = fmaf(w.z, v, acc[2]);
+      acc[3] = fmaf(w.w, v, acc[3]);
     }
   }
-  if (warp < NH && lane == 0) {
+  if (warp < kShortHeads && lane == 0) {
     s_ml[2 * warp] = m;
     s_ml[2 * warp + 1] = l;
-    if (p.lse) p.lse[row0 + warp] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    if (p.lse && ((rows >> warp) & 1)) p.lse[row0 + warp] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
   }
   __syncthreads();
-  if (accum) {
 #pragma unroll
-    for (int j = 0; j < kHPT; ++j) {
-      const float lj = s_ml[2 * (hb + j) + 1];
-      p.o_lat[(row0 + hb + j) * kDc + c] = lj > 0.f ? acc[j] / lj : 0.f;
+  for (int j = 0; j < 4; ++j) {
+    const float lj = s_ml[2 * (hb + j) + 1];
+    if ((rows >> (hb + j)) & 1) p.o_lat[(row0 + hb + j) * kDc + c] = lj > 0.f ? acc[j] / lj : 0.f;
+  }
+}
+
+// Merge of sequence b, head h in a 1024-thread block (combine_kernel's
+// grid): writes o_lat and lse and returns true, or returns false (in every
+// thread) when the row carries too much weight of fp16 P V products against
+// its merged output and must be recomputed exactly.
+template <int LF>
+__device__ __forceinline__ bool merge_head(const DecodeParams& p, int b, int h, float* sw, float* red,
+                                           float4 (*parts)[kDc / 4]) {
+  const int tid = threadIdx.x;
+  const int quad = tid & (kDc / 4 - 1), part = tid / (kDc / 4);
+  float4* out = reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc) + quad;
+  const int x0 = p.ws.span[2 * b], S = p.ws.span[2 * b + 1] - x0 + 1;
+  const float* mp = p.ws.m + (size_t)(x0 + b) * p.H + h;
+  const float* lp = p.ws.l + (size_t)(x0 + b) * p.H + h;
+  const float* ep = p.ws.e2 + (size_t)(x0 + b) * p.H + h;
+  const float4* o4 = reinterpret_cast<const float4*>(p.ws.o + ((size_t)(x0 + b) * p.H + h) * kDc) + quad;
+  float M, L, E2 = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (S == 1) {                          // one CTA held the whole sequence: normalise its partial
+    if (!kRiskFmt<LF> && part > 0) return true;
+    M = *mp;
+    L = *lp;
+    if (kRiskFmt<LF>) E2 = *ep;
+    if (part == 0) acc = __ldcg(o4);
+  } else {
+    float mloc = -INFINITY;
+    for (int t = tid; t < S; t += kCombThreads) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
+    M = block_reduce(mloc, true, red);
+    float lloc = 0.f, eloc = 0.f;
+    for (int t = tid; t < S; t += kCombThreads) {
+      const float m = mp[(size_t)t * p.H];
+      const float w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
+      if (t < kCombSlots) sw[t] = w;
+      if (w != 0.f) {
+        lloc = fmaf(w, lp[(size_t)t * p.H], lloc);
+        if (kRiskFmt<LF>) eloc = fmaf(w * w, ep[(size_t)t * p.H], eloc);
+      }
+    }
+    L = block_reduce(lloc, false, red);   // also orders the sw writes before the reads below
+    if (kRiskFmt<LF>) E2 = block_reduce(eloc, false, red);
+    const size_t ostride = (size_t)p.H * (kDc / 4);
+#pragma unroll 8
+    for (int t = part; t < S; t += kCombParts) {
+      float w;
+      if (t < kCombSlots) {
+        w = sw[t];
+      } else {
+        const float m = mp[(size_t)t * p.H];
+        w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
+      }
+      const float4 v = __ldcg(o4 + (size_t)t * ostride);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    if (part > 0) {
+      parts[part - 1][quad] = acc;
+      acc = make_float4(0.f, 0.f, 0.f, 0.f);   // the row maximum below is taken over part 0's sums
+    }
+    __syncthreads();
+    if (!kRiskFmt<LF> && part > 0) return true;
+    if (part == 0) {
+#pragma unroll
+      for (int k = 0; k < kCombParts - 1; ++k) {
+        const float4 a1 = parts[k][quad];
+        acc.x += a1.x;
+        acc.y += a1.y;
+        acc.z += a1.z;
+        acc.w += a1.w;
+      }
     }
   }
+  if (kRiskFmt<LF>) {                    // every thread takes part; parts > 0 hold 0
+    const float amax = block_reduce(fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w))),
+                                    true, red);
+    if (L > 0.f && sqrtf(E2) > kRiskRatio * amax) return false;
+    if (part > 0) return true;
+  }
+  if (L > 0.f) {
+    const float inv = 1.f / L;
+    *out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = (M + log2f(L)) * 0.69314718055994531f;
+  } else {
+    *out = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
+  }
+  return true;
 }
 
 template <int LF, int KF>
@@ -370,106 +445,21 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_kernel(DecodeParams p
   __shared__ float red[kCombThreads / 32];
   __shared__ float4 parts[kCombParts - 1][kDc / 4];
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
-  const int quad = tid & (kDc / 4 - 1), part = tid / (kDc / 4);
   const int32_t* cum = p.ws.cum;
-  float4* out = reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc) + quad;
   // a length out of range ran as 0 in the split kernel; it is reported here,
   // after the wait, so that no earlier kernel's write to dev_err can land later
   const int len = checked_len(p, b, tid == 0);
   if (cum[b] == cum[b + 1]) {
-    if (part == 0) *out = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid < kDc / 4) reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
     return;
   }
-  if (len < kExactLen) {                 // the block of every eighth head takes eight heads
-    if (h % kShortHeads == 0) exact_rows<LF, KF, kShortHeads>(p, b, h, len, short_smem);
-    return;
-  }
-  const int x0 = p.ws.span[2 * b], S = p.ws.span[2 * b + 1] - x0 + 1;
-  const float* mp = p.ws.m + (size_t)(x0 + b) * p.H + h;
-  const float* lp = p.ws.l + (size_t)(x0 + b) * p.H + h;
-  const float* ep = p.ws.e2 + (size_t)(x0 + b) * p.H + h;
-  if (S == 1) {                          // one CTA held the whole sequence: normalise its partial
-    if (!kRiskFmt<LF> && part > 0) return;
-    const float m = *mp, l = *lp;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (part == 0) v = __ldcg(reinterpret_cast<const float4*>(p.ws.o + ((size_t)(x0 + b) * p.H + h) * kDc) + quad);
-    if (kRiskFmt<LF>) {
-      const float vmax = block_reduce(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))), true, red);
-      if (l > 0.f && sqrtf(*ep) > kRiskRatio * vmax) {
-        exact_rows<LF, KF, 1>(p, b, h, len, short_smem);
-        return;
-      }
-      if (part > 0) return;
-    }
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    *out = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
-    if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
-    return;
-  }
-  float mloc = -INFINITY;
-  for (int t = tid; t < S; t += kCombThreads) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
-  const float M = block_reduce(mloc, true, red);
-  float lloc = 0.f, eloc = 0.f;
-  for (int t = tid; t < S; t += kCombThreads) {
-    const float m = mp[(size_t)t * p.H];
-    const float w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
-    if (t < kCombSlots) sw[t] = w;
-    if (w != 0.f) {
-      lloc = fmaf(w, lp[(size_t)t * p.H], lloc);
-      if (kRiskFmt<LF>) eloc = fmaf(w * w, ep[(size_t)t * p.H], eloc);
-    }
-  }
-  const float L = block_reduce(lloc, false, red);   // also orders the sw writes before the reads below
-  const float E2 = kRiskFmt<LF> ? block_reduce(eloc, false, red) : 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* o4 = reinterpret_cast<const float4*>(p.ws.o + ((size_t)(x0 + b) * p.H + h) * kDc) + quad;
-  const size_t ostride = (size_t)p.H * (kDc / 4);
-#pragma unroll 8
-  for (int t = part; t < S; t += kCombParts) {
-    float w;
-    if (t < kCombSlots) {
-      w = sw[t];
-    } else {
-      const float m = mp[(size_t)t * p.H];
-      w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
-    }
-    const float4 v = __ldcg(o4 + (size_t)t * ostride);
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
-  }
-  if (part > 0) parts[part - 1][quad] = acc;
-  __syncthreads();
-  if (!kRiskFmt<LF> && part > 0) return;
-  if (part == 0) {
-#pragma unroll
-    for (int k = 0; k < kCombParts - 1; ++k) {
-      const float4 a1 = parts[k][quad];
-      acc.x += a1.x;
-      acc.y += a1.y;
-      acc.z += a1.z;
-      acc.w += a1.w;
-    }
-  }
-  if (kRiskFmt<LF>) {                    // every thread takes part; parts > 0 contribute 0
-    const float a = part == 0 ? fmaxf(fmaxf(fabsf(acc.x), fabsf(acc.y)), fmaxf(fabsf(acc.z), fabsf(acc.w))) : 0.f;
-    const float amax = block_reduce(a, true, red);
-    if (L > 0.f && sqrtf(E2) > kRiskRatio * amax) {
-      exact_rows<LF, KF, 1>(p, b, h, len, short_smem);
-      return;
-    }
-    if (part > 0) return;
-  }
-  if (L > 0.f) {
-    const float inv = 1.f / L;
-    *out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-    if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = (M + log2f(L)) * 0.69314718055994531f;
-  } else {
-    *out = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
-  }
+  // Rows recomputed exactly: the eight heads of a short sequence (by the
+  // block of every eighth head), or this head when its merge asks for it
+  // (computed with its seven neighbours, written alone).  One call site.
+  const bool done = len < kExactLen ? h % kShortHeads != 0 : merge_head<LF>(p, b, h, sw, red, parts);
+  if (done) return;
+  exact_rows<LF, KF>(p, b, h - h % kShortHeads, len, len < kExactLen ? 0xffu : 1u << (h % kShortHeads), short_smem);
 }
 
 // The same merge in two other grids, for the shapes where one block per
@@ -514,10 +504,11 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
     return;
   }
   const int len = checked_len(p, b, false);
-  if (len < kExactLen) {                 // eight heads per block
-    if (grouped || (h0 % kShortHeads == 0 && z == 0)) exact_rows<LF, KF, kShortHeads>(p, b, h0, len, short_smem);
-    return;
-  }
+  // The merge proper: writes the block's rows and returns true, or returns
+  // false (in every thread; grouped grid, quantized latent) when one of its
+  // eight heads carries too much weight of fp16 P V products against its
+  // merged, unnormalised output, so that the eight are recomputed exactly.
+  auto merge = [&]() -> bool {
   const int x0 = p.ws.span[2 * b], S = p.ws.span[2 * b + 1] - x0 + 1;
   const float* mp = p.ws.m + (size_t)(x0 + b) * p.H + h;
   const float* lp = p.ws.l + (size_t)(x0 + b) * p.H + h;
@@ -527,7 +518,7 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
   // grouped grid, quantized latent: the block recomputes its eight heads
   // exactly when any of them carries too much weight of fp16 products
   // against its merged (unnormalised) output; every thread takes part
-  auto risky_block = [&](const float4& un, float lsum, float e2sum) -> bool {
+  auto risky = [&](const float4& un, float lsum, float e2sum) -> bool {
     float a = warp_max(fmaxf(fmaxf(fabsf(un.x), fabsf(un.y)), fmaxf(fabsf(un.z), fabsf(un.w))));
     if ((tid & 31) == 0) red[tid >> 5] = a;
     __syncthreads();
@@ -536,17 +527,14 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
     return __syncthreads_or(lsum > 0.f && sqrtf(e2sum) > kRiskRatio * a) != 0;
   };
   if (S == 1) {                          // one CTA held the whole sequence: normalise its partial
-    if (part > 0) return;
+    if (part > 0) return true;
     const float m = *mp, l = *lp;
     const float4 v = __ldcg(o4);
-    if (kRiskFmt<LF> && grouped && risky_block(v, l, *ep)) {
-      exact_rows<LF, KF, kShortHeads>(p, b, h0, len, short_smem);
-      return;
-    }
+    if (kRiskFmt<LF> && grouped && risky(v, l, *ep)) return false;
     const float inv = l > 0.f ? 1.f / l : 0.f;
     *out = make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv);
     if (writes_lse) p.lse[row] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
-    return;
+    return true;
   }
   float M, L;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -568,10 +556,7 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
       acc.z = fmaf(w, v.z, acc.z);
       acc.w = fmaf(w, v.w, acc.w);
     }
-    if (kRiskFmt<LF> && risky_block(acc, L, E2)) {
-      exact_rows<LF, KF, kShortHeads>(p, b, h0, len, short_smem);
-      return;
-    }
+    if (kRiskFmt<LF> && risky(acc, L, E2)) return false;
   } else {
     float* sw = short_smem;                                        // [kCombSlots]
     float4* parts = reinterpret_cast<float4*>(short_smem + kCombSlots);   // [kCombThreads]
@@ -618,7 +603,7 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
       }
       __syncthreads();
     }
-    if (part > 0) return;
+    if (part > 0) return true;
 #pragma unroll
     for (int k = 1; k < 8; ++k) {         // nparts >= 8
       const float4 a1 = parts[(k << qs_shift) + ql];
@@ -636,6 +621,14 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
     *out = make_float4(0.f, 0.f, 0.f, 0.f);
     if (writes_lse) p.lse[row] = -INFINITY;
   }
+  return true;
+  };
+  // Rows recomputed exactly (one call site): the eight heads of a short
+  // sequence (in the sliced grid by the z = 0 block of every eighth head), or
+  // the block's eight heads when its merge asks for it.
+  const bool done = len < kExactLen ? !(grouped || (h0 % kShortHeads == 0 && z == 0)) : merge();
+  if (done) return;
+  exact_rows<LF, KF>(p, b, h0, len, 0xffu, short_smem);
 }
 
 }  // namespace

@@ -72,9 +72,11 @@ struct Fmt {
   static constexpr int kNG = kDc / kGS;                          // scale groups per token
   // quantized latents: the softmax warps also accumulate, per head row, the
   // weight of the fp16 P V products (sum of (p_t M_t)^2, M_t a bound on the
-  // token's |c_hat|), from which the combine decides whether the row needs
-  // the exact fp32 recomputation
+  // token's |c_hat| from its scales, computed by the bounds warpgroup), from
+  // which the combine decides whether the row needs the exact fp32
+  // recomputation
   static constexpr bool kRisk = !kLatBf16;
+  static constexpr float kBoundFactor = LF == MLA_FMT_INT4_ASYM ? 1.f : (kLatInt4 ? 8.f : 127.f);
   static constexpr int kScaleOff = kBlockTokens * kRow;
   static constexpr int kZeroOff = kScaleOff + (kLatBf16 ? 0 : (kDc / kGS) * kBlockTokens * 4);
   static constexpr int kKpeOff = kZeroOff + (LF == MLA_FMT_INT4_ASYM ? kNLG * kBlockTokens * 4 : 0);
@@ -278,24 +280,26 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Bound on max_c |c_hat[u][c]| of token u of a staged block, from its scales
-// (and zero-points): |q| s <= 127 s (INT8), <= 8 s (4-bit symmetric, stored
-// as code + 8), |q - z| s <= max(|z|, |15 - z|) s (asymmetric INT4).
+// Bound on max_c |c_hat[u][c]| over the scale groups [g0, g1) of token u of
+// a staged block, from its scales (and zero-points): |q| s <= 127 s (INT8),
+// <= 8 s (4-bit symmetric, stored as code + 8), |q - z| s <= max(|z|,
+// |15 - z|) s (asymmetric INT4).  The factor (127 or 8) is applied by the
+// caller (Fmt::kBoundFactor).
 template <int LF, int KF>
-__device__ __forceinline__ float latent_bound(const uint8_t* st, int u) {
+__device__ __forceinline__ float latent_bound(const uint8_t* st, int u, int g0, int g1) {
   using F = Fmt<LF, KF>;
   const float* sc = reinterpret_cast<const float*>(st + F::kScaleOff);
   float mb = 0.f;
   if (LF == MLA_FMT_INT4_ASYM) {
     const float* zp = reinterpret_cast<const float*>(st + F::kZeroOff);
 #pragma unroll 8
-    for (int g = 0; g < kNLG; ++g)
+    for (int g = g0; g < g1; ++g)
       mb = fmaxf(mb, sc[g * kBlockTokens + u] * (fabsf(zp[g * kBlockTokens + u] - 7.5f) + 7.5f));
-    return mb;
-  }
+  } else {
 #pragma unroll 8
-  for (int g = 0; g < F::kNG; ++g) mb = fmaxf(mb, sc[g * kBlockTokens + u]);
-  return mb * (F::kLatInt4 ? 8.f : 127.f);
+    for (int g = g0; g < g1; ++g) mb = fmaxf(mb, sc[g * kBlockTokens + u]);
+  }
+  return mb;
 }
 
 __device__ __forceinline__ int checked_len(const DecodeParams& p, int b, bool report) {
@@ -702,24 +706,37 @@ __device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha
 // ---------------------------------------------------------------------------
 // Warps 0..7 compute QK^T (step A) and PV (step C) of their latent groups;
 // warpgroup 2 (warps 8..11) runs the online softmax (step B) of every chunk
-// and the loader.  Hand-offs go through mbarriers with bounded waits:
+// and the loader; warpgroup 3 (warps 12..15), for quantized latents, bounds
+// every staged token's |c_hat| from its scales, for the weight of the fp16
+// P V products the softmax accumulates (a role of its own so that this work
+// stays off the softmax's path).  Hand-offs go through mbarriers with
+// bounded waits:
 //   bx[i & 1]: the 8 compute warps have written chunk i's partial scores
 //              (and thread 0 its valid-token count and score scale); the
 //              stage of chunk i is free again;
 //   bp[i & 1]: the 4 softmax warps have written chunk i's P and alpha;
-//   mready[i & 1]: the bounds M_t of chunk i's tokens are in mbuf;
+//   bpart[i & 1]: the 4 bounds warps have posted chunk i's partial maxima;
+//   mready[i & 3]: the bounds M_t of chunk i's tokens are in mbuf;
+//   mfree[i & 3]: the 4 softmax warps have read them (the slot is free);
 //   qa: the compute warps have posted their query magnitudes.
 // Each warp arrives once, from lane 0 after a __syncwarp that orders the
 // whole warp's stores before the arrival.
 // A compute warp therefore runs A(i), arrives on bx, waits for bp of chunk
 // i - 1 and runs C(i - 1), while the softmax warpgroup works on chunk i - 1
-// or i.  Registers move to the compute warps with setmaxnreg (232 each;
-// 40 for the softmax warpgroup; the 384-thread block launches with 168).
-constexpr int kWsThreads = kThreads + 128;
-constexpr int kWsExtra = 7 * 8 + 4 * 4 + 64 * 4;   // bx[2], bp[2], qa, mready[2]; nvq[2], cwq[2]; mbuf[2][32]
+// or i.  Registers move to the compute warps with setmaxnreg: the 512-thread
+// block launches with 128 per thread (65,536), then 224 each for the 256
+// compute threads, 40 for the softmax warpgroup, 24 for the bounds one.
+constexpr int kWsThreads = kThreads + 256;
+constexpr int kRegsCompute = 224, kRegsSoftmax = 40, kRegsBounds = 24;
+static_assert(kThreads * kRegsCompute + 128 * kRegsSoftmax + 128 * kRegsBounds == 65536 &&
+                  65536 / kWsThreads == 128,
+              "the warpgroups' register shares must add up to the block's launch allocation");
+constexpr int kWsExtra = 15 * 8 + 4 * 4 + 384 * 4;   // bx[2], bp[2], qa, mready[4], mfree[4], bpart[2];
+                                                      // nvq[2], cwq[2]; mbuf[4][32], part[2][4][32]
 
 __device__ __forceinline__ void ws_regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory"); }
-__device__ __forceinline__ void ws_regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory"); }
+__device__ __forceinline__ void ws_regs_bounds() { asm volatile("setmaxnreg.dec.sync.aligned.u32 24;\n" ::: "memory"); }
+__device__ __forceinline__ void ws_regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory"); }
 
 template <int LF, int KF>
 __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams p) {
@@ -731,13 +748,16 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   uint16_t* ptab = reinterpret_cast<uint16_t*>(xpart + 2 * kCW * kHT * kXStride);  // [2 buf][hi, lo][16][kPStride]
   float* alpha_s = reinterpret_cast<float*>(ptab + 4 * kHT * kPStride);        // [2][16]
   float* amax_s = alpha_s + 2 * kHT;                                           // [8]
-  float* mbuf = amax_s + kCW;                      // [2][32] token bounds M_t (16-byte aligned: float4 reads)
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(mbuf + 64);
+  float* mbuf = amax_s + kCW;                      // [4][32] token bounds M_t, a ring of chunks (float4 reads)
+  float* part = mbuf + 128;                        // [2][4 bounds warps][32] partial maxima
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(part + 256);
   uint64_t* bx = full_bar + F::kStages;                                        // [2]
   uint64_t* bp = bx + 2;                                                       // [2]
   uint64_t* qa = bp + 2;                                                       // [1]
-  uint64_t* mready = qa + 1;                                                   // [2]
-  int32_t* meta = reinterpret_cast<int32_t*>(mready + 2);
+  uint64_t* mready = qa + 1;                                                   // [4]
+  uint64_t* mfree = mready + 4;                                                // [4]
+  uint64_t* bpart = mfree + 4;                                                 // [2]
+  int32_t* meta = reinterpret_cast<int32_t*>(bpart + 2);
   int32_t* nvq = meta + F::kStages;                                            // [2]
   float* cwq = reinterpret_cast<float*>(nvq + 2);                              // [2]
   int32_t* cum = reinterpret_cast<int32_t*>(cwq + 2);
@@ -773,8 +793,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       mbar_init(smem_u32(&bp[k]), 4);        // one per softmax warp
     }
     mbar_init(smem_u32(qa), kCW);
-    mbar_init(smem_u32(&mready[0]), 1);
-    mbar_init(smem_u32(&mready[1]), 1);
+    for (int k = 0; k < 4; ++k) {
+      mbar_init(smem_u32(&mready[k]), 1);   // the bounds warpgroup's first warp
+      mbar_init(smem_u32(&mfree[k]), 4);    // one arrival per softmax warp
+    }
+    for (int k = 0; k < 2; ++k) mbar_init(smem_u32(&bpart[k]), 4);   // one per bounds warp
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -792,6 +815,51 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   if (x >= Ge) return;
   const int c_lo = (int)range_lo(C, x, Ge), c_hi = (int)range_lo(C, x + 1, Ge);
 
+  const int nch = c_hi - c_lo;
+  if (warp >= kCW + 4) {
+    // ============================ bounds warpgroup ============================
+    // Chunk k (relative index): bounds warp wb takes a quarter of the scale
+    // groups, lane = token (tokens past the chunk's end get 0), posts its
+    // partial maxima to part[k & 1][wb] and arrives on bpart[k & 1]; every
+    // bounds warp then takes the max of the four, and the first writes M_t to
+    // mbuf[k & 3] (once the softmax warps have freed the slot, mfree) and
+    // arrives on mready[k & 3].  part[k & 1] is rewritten for chunk k + 2
+    // only after the wait on bpart of chunk k + 1, which every bounds warp
+    // arrives at after reading part[k & 1].  The loader refills a stage only
+    // after mready of its chunk, i.e. after every bounds warp has read it.
+    ws_regs_bounds();
+    if (!F::kRisk) return;
+    const int wb = warp - kCW - 4;
+    constexpr int kPer = (F::kNG + 3) / 4;
+    const int g0 = wb * kPer, g1 = g0 + kPer < F::kNG ? g0 + kPer : F::kNG;
+    for (int k = 0; k < nch; ++k) {
+      const int sk = k % F::kStages;
+      if (!mbar_wait_warp(smem_u32(&full_bar[sk]), (uint32_t)((k / F::kStages) & 1), p.wait_ns)) {
+        set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+        break;
+      }
+      part[(k & 1) * 128 + wb * 32 + lane] =
+          lane < meta[sk] ? latent_bound<LF, KF>(stages + sk * F::kBlock, lane, g0, g1) : 0.f;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bpart[k & 1]));
+      if (!mbar_wait_warp(smem_u32(&bpart[k & 1]), (uint32_t)((k >> 1) & 1), p.wait_ns)) {
+        set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+        break;
+      }
+      const float* pp = part + (k & 1) * 128 + lane;
+      const float m_all = fmaxf(fmaxf(pp[0], pp[32]), fmaxf(pp[64], pp[96])) * F::kBoundFactor;
+      if (wb == 0) {
+        if (k >= 4 && !mbar_wait_warp(smem_u32(&mfree[k & 3]), (uint32_t)(((k >> 2) - 1) & 1), p.wait_ns)) {
+          set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
+          break;
+        }
+        mbuf[(k & 3) * 32 + lane] = m_all;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&mready[k & 3]));
+      }
+    }
+    return;
+  }
   if (warp >= kCW) {
     // ======================= softmax / loader warpgroup =======================
     ws_regs_dec();
@@ -829,6 +897,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       }
       pl_ready = false;
       ++ld_c;
+      plan();     // the next chunk's page id: its load has a whole iteration to land
     };
     if (t == 0)
       for (int s = 0; s < F::kStages; ++s) commit(s);
@@ -836,7 +905,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
     float m_row = -INFINITY, l_row = 0.f, e2 = 0.f;
     int b = -1, s = 0;
     bool dead = false;
-    const int wsm = warp - kCW, nch = c_hi - c_lo;
+    // Flush of sequence bb's partial: m, l and, with a quantized latent,
+    // e2 = sum_t (p_t M_t)^2 over the row (M_t the bounds warpgroup's bound
+    // on |c_hat_t|), the weight of the fp16 P V products.
     auto flush_ml = [&](int bb) {
       float e = e2;
       if (F::kRisk) {
@@ -850,25 +921,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
         p.ws.e2[slot * p.H + h0 + hr] = e;
       }
     };
-    // The bounds M_t of chunk k (relative index) go to mbuf[k & 1], written
-    // by softmax warp k % 4 one iteration ahead (lane = token; tokens past the
-    // chunk's end get 0), then mready[k & 1] completes.  The buffer is reused
-    // for chunk k + 2 only after bp of chunk k, i.e. once every softmax thread
-    // has read it; the loader refills a stage only after its bounds are taken.
-    auto produce_bound = [&](int k) -> bool {
-      const int sk = k % F::kStages;
-      if (!mbar_wait_warp(smem_u32(&full_bar[sk]), (uint32_t)((k / F::kStages) & 1), p.wait_ns)) return false;
-      const int nvk = meta[sk];
-      mbuf[(k & 1) * 32 + lane] = lane < nvk ? latent_bound<LF, KF>(stages + sk * F::kBlock, lane) : 0.f;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&mready[k & 1]));
-      return true;
-    };
-    if (F::kRisk && wsm < 2 && wsm < nch && !produce_bound(wsm)) {
-      set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
-      dead = true;
-    }
-    for (int c = c_lo, i = 0; c < c_hi && !dead; ++c, ++i) {
+    for (int c = c_lo, i = 0; c < c_hi; ++c, ++i) {
       int nb = b < 0 ? seq_of_chunk(cum, p.B, c) : b;
       while (cum[nb + 1] <= c) ++nb;
       if (nb != b) {
@@ -880,15 +933,18 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       }
       if (t == 0) plan();
       if (!mbar_wait_warp(smem_u32(&bx[i & 1]), (uint32_t)((i >> 1) & 1), p.wait_ns) ||
-          (F::kRisk && !mbar_wait_warp(smem_u32(&mready[i & 1]), (uint32_t)((i >> 1) & 1), p.wait_ns))) {
+          (F::kRisk && !mbar_wait_warp(smem_u32(&mready[i & 3]), (uint32_t)((i >> 2) & 1), p.wait_ns))) {
         set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
         dead = true;
         break;
       }
-      // every compute warp is past chunk i's stage, and its bounds are taken
-      if (t == 0) commit(s);
       float4 mb4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (F::kRisk) mb4 = *reinterpret_cast<const float4*>(mbuf + (i & 1) * 32 + 4 * tq);
+      if (F::kRisk) {
+        mb4 = *reinterpret_cast<const float4*>(mbuf + (i & 3) * 32 + 4 * tq);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&mfree[i & 3]));
+      }
+      if (t == 0) commit(s);                   // every compute warp is past chunk i's stage
       const int buf = i & 1, nv = nvq[buf];
       const float cw = cwq[buf];
       // sum the 8 warps' partial scores of 4 tokens of row hr
@@ -941,16 +997,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       __syncwarp();                            // the warp's P and alpha stores, then one arrival
       if (lane == 0) mbar_arrive(smem_u32(&bp[buf]));
       if (++s == F::kStages) s = 0;
-      if (F::kRisk && wsm == ((i + 2) & 3) && i + 2 < nch &&
-          (!mbar_wait_warp(smem_u32(&bp[buf]), (uint32_t)((i >> 1) & 1), p.wait_ns) || !produce_bound(i + 2))) {
-        set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
-        dead = true;
-        break;
-      }
     }
-    if (!dead) {
-      if (b >= 0) flush_ml(b);
-    } else {
+    if (!dead && b >= 0) flush_ml(b);
+    if (dead) {
       // gave up: empty partials (weight 0) for the sequence in hand and every
       // later one of the range, so that the combine reads finite values
       m_row = -INFINITY;
