@@ -161,6 +161,29 @@ def dequantize_sym_int4(codes, scale, group):
     return dequantize_sym_int8(codes, scale, group)
 
 
+def latent_bound(scale, zero=None, levels=127):
+    """Per-token bound M_t on the dequantized latent: the largest magnitude a
+    code of the token can dequantize to, the maximum over its groups of
+    levels * s (symmetric formats: 127 levels a side for INT8, 7 for INT4)
+    or of s * (|z - 7.5| + 7.5) (asymmetric INT4, where q - z ranges over
+    -z .. 15 - z).  fp32, one rounding per product; the maximum skips NaN.
+
+    Not a quantity of the pages: the cache stores it beside the scales so
+    that the decode can weigh its fp16 P V roundings (the rows it recomputes
+    exactly).  For the symmetric formats it equals max_c |x_hat[c]|, since
+    each group's largest input maps to the extreme code.
+
+    scale, zero: float32 [rows, groups].  Returns float32 [rows].
+    """
+    s = np.asarray(scale, np.float32)
+    if zero is None:
+        per_group = s * F32(levels)
+    else:
+        z = np.asarray(zero, np.float32)
+        per_group = s * (np.abs(z - F32(7.5)) + F32(7.5))
+    return np.fmax.reduce(per_group.astype(np.float32), axis=1).astype(np.float32)
+
+
 def relative_error(x, x_hat):
     """Mean and max of |x - x_hat| / mean|x| over the tensor.
 
@@ -197,14 +220,15 @@ def quantize_token_rows(c, kpe, latent_fmt, kpe_fmt):
     elif latent_fmt in INT8_GROUP:
         g = INT8_GROUP[latent_fmt]
         q, s = quantize_sym_int8(c, g)
-        out.update(c_codes=q, c_scale=s, c_hat=dequantize_sym_int8(q, s, g))
+        out.update(c_codes=q, c_scale=s, c_hat=dequantize_sym_int8(q, s, g), c_bound=latent_bound(s))
     elif latent_fmt == FMT_INT4:
         q, s, z = quantize_asym_int4(c, LATENT_GROUP)
         out.update(c_codes=q, c_scale=s, c_zero=z,
-                   c_hat=dequantize_asym_int4(q, s, z, LATENT_GROUP))
+                   c_hat=dequantize_asym_int4(q, s, z, LATENT_GROUP), c_bound=latent_bound(s, z))
     elif latent_fmt == FMT_INT4_SYM:
         q, s = quantize_sym_int4(c, LATENT_GROUP)
-        out.update(c_codes=q, c_scale=s, c_hat=dequantize_sym_int4(q, s, LATENT_GROUP))
+        out.update(c_codes=q, c_scale=s, c_hat=dequantize_sym_int4(q, s, LATENT_GROUP),
+                   c_bound=latent_bound(s, levels=7))
     else:
         raise ValueError("latent_fmt")
     if kpe_fmt == FMT_BF16:

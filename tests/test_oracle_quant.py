@@ -286,3 +286,56 @@ def test_relative_error_literal_values():
     assert m == pytest.approx(0.2, rel=1e-15) and mx == pytest.approx(0.8, rel=1e-15)
     # no error at all
     assert Q.relative_error([0.5, -7.0, 3.0], [0.5, -7.0, 3.0]) == (0.0, 0.0)
+
+
+# ---------------------------------------------------------------------------
+# The stored per-token bound M_t (the decode's weight of its fp16 P V terms)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt", [Q.FMT_INT8, Q.FMT_INT8_G8, Q.FMT_INT8_G32, Q.FMT_INT8_G64, Q.FMT_INT8_TOKEN,
+                                 Q.FMT_INT4_SYM])
+def test_bound_is_the_largest_dequantized_magnitude_symmetric(fmt):
+    """Symmetric formats: every group's largest input maps to the extreme
+    code, so M_t is exactly max_c |x_hat[c]| (bit for bit), outliers or not."""
+    c = synth_latent(T=256)
+    c[7, 100:116] = 0.0                                   # an all-zero group
+    c[9] = 0.0                                            # an all-zero token: bound 0
+    d = Q.quantize_token_rows(c, synth_kpe(T=256), fmt, Q.FMT_INT8)
+    exp = np.max(np.abs(d["c_hat"]), axis=1).astype(np.float32)
+    assert np.array_equal(d["c_bound"].view(np.uint32), exp.view(np.uint32))
+    assert d["c_bound"][9] == 0.0
+
+
+def test_bound_asymmetric_int4_covers_both_ends():
+    """Asymmetric INT4: M_t = max_g s (|z - 7.5| + 7.5) >= max |x_hat|, equal
+    to it when a group's min and max map to codes 0 and 15, and never more
+    than one step s above it."""
+    c = synth_latent(T=256)
+    d = Q.quantize_token_rows(c, synth_kpe(T=256), Q.FMT_INT4, Q.FMT_INT8)
+    m = np.max(np.abs(d["c_hat"]), axis=1)
+    b = d["c_bound"].astype(np.float64)
+    assert np.all(b >= m * (1 - 2.0 ** -23))
+    assert np.all(b <= m + np.max(d["c_scale"], axis=1) * (1 + 2.0 ** -20))
+    # literal: one group [-3, 5, 0 ...]: s = 8/15, z = rint(3 / s) = rint(5.625) = 6;
+    # codes 0 (x = -3) and 15 (x = 5): x_hat = -6 s and 9 s; the bound is 9 s,
+    # the larger end, where |z| alone (6 s) would be wrong
+    x = np.zeros((1, 512), np.float32)
+    x[0, 0], x[0, 1] = -3.0, 5.0
+    q, s, z = Q.quantize_asym_int4(x)
+    assert z[0, 0] == 6.0 and s[0, 0] == np.float32(8.0) / np.float32(15.0)
+    bound = Q.latent_bound(s, z)
+    assert bound[0] == np.float32(s[0, 0] * np.float32(9.0))
+    assert bound[0] == np.max(np.abs(Q.dequantize_asym_int4(q, s, z)))
+    # a group with min > 0 has z < 0: the far end 15 - z dominates
+    y = np.zeros((1, 512), np.float32)
+    y[0, :16] = np.linspace(10.0, 11.0, 16, dtype=np.float32)
+    q, s, z = Q.quantize_asym_int4(y)
+    assert z[0, 0] < 0
+    assert Q.latent_bound(s, z)[0] == np.float32(s[0, 0] * (np.float32(15.0) - z[0, 0]))
+    # the bound takes the largest group, not the first
+    w = np.zeros((1, 512), np.float32)
+    w[0, 0:2] = [-1.0, 1.0]
+    w[0, 496:498] = [-4.0, 4.0]
+    q, s, z = Q.quantize_asym_int4(w)
+    assert Q.latent_bound(s, z)[0] == np.max(s * (np.abs(z - np.float32(7.5)) + np.float32(7.5)))
+    assert Q.latent_bound(s, z)[0] >= 4.0 * (1 - 2.0 ** -22)
