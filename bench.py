@@ -41,8 +41,8 @@ CONFIGS = {
                             desc="V2-Lite shapes, batch 32, context 32768, asymmetric INT4 latent + INT8 k_pe"),
     "v2lite_int4_kpe4_32k": dict(layers=27, heads=16, batch=32, ctx=32768, latent="int4", kpe="int4sym",
                                  desc="V2-Lite shapes, batch 32, context 32768, asymmetric INT4 latent + "
-                                      "symmetric INT4 k_pe (the 7.6 KB-per-token scheme; 576 B per token-layer "
-                                      "with scales and zero-points)"),
+                                      "symmetric INT4 k_pe (the 7.6 KB-per-token scheme; 580 B per token-layer "
+                                      "with scales, zero-points and the bound)"),
     "v2lite_int4sym_32k": dict(layers=27, heads=16, batch=32, ctx=32768, latent="int4sym", kpe="int8",
                                desc="V2-Lite shapes, batch 32, context 32768, symmetric INT4 latent + INT8 k_pe"),
     # the English report's block-count sweep (8 / 32 / 64 blocks) and the
@@ -73,11 +73,12 @@ CONFIGS = {
 }
 FMT = {"bf16": 0, "int8": 1, "int4": 2, "int4sym": 3, "int8g8": 4, "int8g32": 5, "int8g64": 6, "int8tok": 7}
 def _beta(latent, kpe):
-    """Stored bytes per token and layer (codes + fp32 scales / zero-points),
-    as laid out in include/mla.h: 32 latent groups of 16, 8 k_pe groups of 8."""
+    """Stored bytes per token and layer (codes + fp32 scales / zero-points +
+    the fp32 bound of a quantized latent), as laid out in include/mla.h:
+    32 latent groups of 16, 8 k_pe groups of 8."""
     code = {"bf16": 1024, "int4": 256, "int4sym": 256}.get(latent, 512)
     groups = {"int8g8": 64, "int8g32": 16, "int8g64": 8, "int8tok": 1}.get(latent, 32)
-    meta = {"bf16": 0, "int4": 8 * groups}.get(latent, 4 * groups)
+    meta = {"bf16": 0, "int4": 8 * groups + 4}.get(latent, 4 * groups + 4)
     kcode = {"bf16": 128, "int8": 64, "int4sym": 32}[kpe]
     kmeta = 0 if kpe == "bf16" else 32
     return code + meta + kcode + kmeta

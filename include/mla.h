@@ -150,10 +150,18 @@ typedef struct {
  *              32c .. 32c+15 and B = 32c+16 .. 32c+31 like a 4-bit latent
  *              chunk, nibble = code + 8)
  *   kpe_scale  fp32 [8 groups][32 block tokens]    (int8 / INT4_SYM k_pe)
- * page_bytes = 2 * block_bytes = 64 x (1152, 736, 608 or 576) bytes for
+ *   bound      fp32 [32 block tokens]              (int8 / 4-bit latent)
+ *              M_t, the largest magnitude a code of the token's latent can
+ *              dequantize to: 127 max_g s_g (INT8 formats), 7 max_g s_g
+ *              (INT4_SYM), max_g s_g (|z_g - 7.5| + 7.5) (INT4_ASYM), in
+ *              fp32 with one rounding per product.  For INT8 and INT4_SYM
+ *              it equals max_c |c_hat[c]|.  Written by mla_cache_append;
+ *              the decode reads it to find the rows it recomputes exactly
+ *              (see mla_decode_absorbed).
+ * page_bytes = 2 * block_bytes = 64 x (1152, 740, 612 or 580) bytes for
  * bf16/bf16, int8/int8, int4/int8 and int4/int4-sym (the last is [CN]
- * §4.1's 7.6 KB-per-token scheme: 288 B of codes per layer plus scales and
- * zero-points).  The swizzles spread the rows of eight consecutive tokens
+ * §4.1's 7.6 KB-per-token scheme: 288 B of codes per layer plus scales,
+ * zero-points and the bound).  The swizzles spread the rows of eight consecutive tokens
  * over all shared-memory banks when a block is copied verbatim into shared
  * memory.
  */
@@ -163,6 +171,7 @@ typedef struct {
   int64_t scale_off, zero_off;
   int64_t kpe_off, kpe_row_bytes;
   int64_t kpe_scale_off;
+  int64_t bound_off;
 } mla_page_layout;
 
 /* Fills *out for the cache's formats.  MLA_ERR_INVALID_ARG on a bad format. */
@@ -186,6 +195,7 @@ size_t mla_cache_pool_bytes(const mla_cache_layer* cache);
  *       "对称 INT4" rows): s = max|x| / 7;  q = clamp(rint(x / s), -7, 7);
  *       s = 0 -> q = 0.
  *   BF16: the input bits are copied.
+ *   A quantized latent also gets its bound M_t (see mla_page_layout).
  *   c_new   bf16 [n][512]     kpe_new bf16 [n][64]
  *   slot    int32 [n]: physical slot (page * 64 + offset) of each token;
  *           -1 skips the token silently; any other value outside
@@ -243,9 +253,9 @@ size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_spli
  *   Two kinds of rows are recomputed in fp32 from the cache instead:
  *   sequences shorter than 256 tokens, and rows whose output is a small
  *   residual of heavily weighted tokens (latents that cancel), detected
- *   from the partials as M sqrt(sum_t w_t^2) > 4 |o_lat row|_inf, with w_t
- *   the softmax weights and M a bound on |c_hat| from the scales of the
- *   tokens each split read.
+ *   from the partials as sqrt(sum_t (w_t M_t)^2) > 4 |o_lat row|_inf, with
+ *   w_t the softmax weights and M_t a bound on token t's |c_hat| from its
+ *   scales (and zero-points).
  *   Every row is tested to a max relative error below 2e-3 (o_lat) and
  *   2e-3 absolute (lse).
  *   A page id outside [0, num_pages) contributes nothing and sets

@@ -58,7 +58,8 @@ class PageLayout(ctypes.Structure):
     _fields_ = [("page_bytes", ctypes.c_int64), ("block_bytes", ctypes.c_int64), ("codes_off", ctypes.c_int64),
                 ("codes_row_bytes", ctypes.c_int64),
                 ("scale_off", ctypes.c_int64), ("zero_off", ctypes.c_int64), ("kpe_off", ctypes.c_int64),
-                ("kpe_row_bytes", ctypes.c_int64), ("kpe_scale_off", ctypes.c_int64)]
+                ("kpe_row_bytes", ctypes.c_int64), ("kpe_scale_off", ctypes.c_int64),
+                ("bound_off", ctypes.c_int64)]
 
 
 def _load():

@@ -59,7 +59,7 @@ using namespace mla;
 
 extern "C" {
 
-int32_t mla_abi_version(void) { return 103; }
+int32_t mla_abi_version(void) { return 104; }
 
 const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
 
@@ -92,6 +92,7 @@ mla_status mla_cache_page_layout(const mla_cache_layer* cache, mla_page_layout* 
   out->kpe_off = L.kpe_off;
   out->kpe_row_bytes = L.kpe_row;
   out->kpe_scale_off = L.kpe_scale_off;
+  out->bound_off = L.bound_off;
   return MLA_OK;
 }
 

@@ -11,12 +11,15 @@
 // own the eight 8-channel k_pe groups.  The warp reads the token's 1152 input
 // bytes in two coalesced sweeps and writes its code row (512 contiguous bytes
 // for INT8) in the page's chunk order: 16-byte chunks swizzled by token, INT4
-// nibbles of two groups interleaved per chunk (see mla_internal.cuh).
+// nibbles of two groups interleaved per chunk (see mla_internal.cuh).  A
+// quantized latent also gets its bound M_t (include/mla.h, mla_page_layout),
+// the warp maximum of the groups' largest reachable |c_hat|.
 //
 // Bit-exactness: every step yields the IEEE fp32 round-to-nearest result of
 // the plain definition's operation (x / s, max - min, ...), in the same order,
-// followed by round-half-even to integer (rintf), so codes, scales and
-// zero-points equal those of any correct fp32 implementation bit for bit.
+// followed by round-half-even to integer (rintf), so codes, scales,
+// zero-points and bounds equal those of any correct fp32 implementation bit
+// for bit.
 // Denormals are kept (no flush-to-zero).  The per-element quotients x / s of
 // a group share one divisor and use Markstein's FMA division (P. Markstein,
 // "IA-64 and Elementary Functions", 2000): with y = RN(1/s), q0 = RN(x y) and
@@ -155,6 +158,7 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
       float x[16];
       unpack16(v0, v1, x);
       float* scale = reinterpret_cast<float*>(blk + L.scale_off);
+      float mb;      // this lane's share of the bound M_t (before the level factor)
       if (is_int8_latent(LF)) {
         // lane = 16-channel chunk; a group of GS channels spans GS / 16
         // lanes (absmax by shuffles, every lane then derives the same
@@ -162,14 +166,17 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
         constexpr int GS = latent_group_size(LF);
         int8_t q[16];
         if constexpr (GS == 8) {
-          scale[(2 * lane) * kBlockTokens + t] = quant_sym<8, 127>(x, q);
-          scale[(2 * lane + 1) * kBlockTokens + t] = quant_sym<8, 127>(x + 8, q + 8);
+          const float s0 = quant_sym<8, 127>(x, q), s1 = quant_sym<8, 127>(x + 8, q + 8);
+          scale[(2 * lane) * kBlockTokens + t] = s0;
+          scale[(2 * lane + 1) * kBlockTokens + t] = s1;
+          mb = fmaxf(s0, s1);
         } else {
           float a = absmax<16>(x);
 #pragma unroll
           for (int o = 1; o < GS / 16; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
           const float sc = quant_sym_a<16, 127>(x, a, q);
           if (lane % (GS / 16) == 0) scale[(lane / (GS / 16)) * kBlockTokens + t] = sc;
+          mb = sc;
         }
         // byte order of the chunk: channels in order, except for 8-channel
         // groups, where word j holds channels 2j, 2j+1, 8+2j, 8+2j+1
@@ -188,9 +195,12 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
           quant_asym4(x, sc, zp, q);
           scale[lane * kBlockTokens + t] = sc;
           reinterpret_cast<float*>(blk + L.zero_off)[lane * kBlockTokens + t] = zp;
+          // |q - z| <= max(|z|, |15 - z|) = |z - 7.5| + 7.5 over q in 0..15
+          mb = __fmul_rn(sc, __fadd_rn(fabsf(__fsub_rn(zp, 7.5f)), 7.5f));
         } else {
           int8_t qs[16];
-          scale[lane * kBlockTokens + t] = quant_sym<16, 7>(x, qs);
+          mb = quant_sym<16, 7>(x, qs);
+          scale[lane * kBlockTokens + t] = mb;
 #pragma unroll
           for (int i = 0; i < 16; ++i) q[i] = (uint8_t)(qs[i] + 8);
         }
@@ -202,6 +212,14 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
         for (int j = 0; j < 4; ++j) w[j] |= __shfl_xor_sync(0xffffffffu, w[j], 1);
         if ((lane & 1) == 0)
           reinterpret_cast<uint4*>(row)[latent_chunk_pos(lane >> 1, t)] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      // the token's bound: the largest |c_hat| its codes can reach, the max
+      // over groups of (levels a side) x s (asymmetric: s (|z - 7.5| + 7.5))
+#pragma unroll
+      for (int o = 16; o; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+      if (lane == 0) {
+        const float lv = is_int8_latent(LF) ? 127.f : (LF == MLA_FMT_INT4_SYM ? 7.f : 1.f);
+        reinterpret_cast<float*>(blk + L.bound_off)[t] = LF == MLA_FMT_INT4_ASYM ? mb : __fmul_rn(lv, mb);
       }
     }
 

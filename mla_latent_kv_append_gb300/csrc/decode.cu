@@ -220,12 +220,13 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
 //    scale) do not average out, and with a peaked softmax they would reach
 //    the 2e-3 bound;
 //  * rows whose split partials carry a large weight of fp16 products against
-//    the merged output: sqrt(sum_i M_i^2 sum_t w_t^2) > kRiskRatio * |o|_inf,
-//    with w_t the normalised softmax weights and M_i a bound on |c_hat| over
-//    the tokens that partial i's block read (from the scales; the split
-//    kernel stores M_i^2 sum_t p_t^2 per partial).  This bounds the spread
+//    the merged output: sqrt(sum_t (w_t M_t)^2) > kRiskRatio * |o|_inf, with
+//    w_t the normalised softmax weights and M_t a bound on max_c |c_hat_t[c]|
+//    from token t's own scales (and zero-points).  The split kernel keeps
+//    sum_t (p_t M_t)^2 per partial (relative to the partial's running
+//    maximum) and the combine rescales and sums them.  This bounds the spread
 //    of the fp16 roundings of the P V terms, sqrt(sum_t (w_t |c_hat_t|)^2),
-//    from above.  Over natural data the ratio stays below ~2.5 (the heavy
+//    from above.  Over natural data the ratio stays near 1 (the heavy
 //    tokens' latents make up the output); it grows when heavy tokens'
 //    latents cancel, where those roundings dominate the small result (the
 //    fast path's error is a few 1e-4 times the ratio).

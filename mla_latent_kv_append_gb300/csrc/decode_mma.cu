@@ -71,17 +71,16 @@ struct Fmt {
   static constexpr bool kStdLayout = kLatBf16 || kLatG8;
   static constexpr int kNG = kDc / kGS;                          // scale groups per token
   // quantized latents: the softmax warps also accumulate, per head row, the
-  // weight of the fp16 P V products (sum of (p_t M_t)^2, M_t a bound on the
-  // token's |c_hat| from its scales, computed by the bounds warpgroup), from
-  // which the combine decides whether the row needs the exact fp32
-  // recomputation
+  // weight of the fp16 P V products (sum of (p_t M_t)^2, M_t the token's
+  // stored bound on |c_hat|), from which the combine decides whether the row
+  // needs the exact fp32 recomputation
   static constexpr bool kRisk = !kLatBf16;
-  static constexpr float kBoundFactor = LF == MLA_FMT_INT4_ASYM ? 1.f : (kLatInt4 ? 8.f : 127.f);
   static constexpr int kScaleOff = kBlockTokens * kRow;
   static constexpr int kZeroOff = kScaleOff + (kLatBf16 ? 0 : (kDc / kGS) * kBlockTokens * 4);
   static constexpr int kKpeOff = kZeroOff + (LF == MLA_FMT_INT4_ASYM ? kNLG * kBlockTokens * 4 : 0);
   static constexpr int kKScaleOff = kKpeOff + kBlockTokens * kKRow;
-  static constexpr int kBlock = kKScaleOff + (kKpeBf16 ? 0 : kNKG * kBlockTokens * 4);
+  static constexpr int kBoundOff = kKScaleOff + (kKpeBf16 ? 0 : kNKG * kBlockTokens * 4);
+  static constexpr int kBlock = kBoundOff + (kLatBf16 ? 0 : kBlockTokens * 4);
   static constexpr int kStages = kBlock <= 24 * 1024 ? 6 : (kBlock <= 40 * 1024 ? 4 : 3);
   static constexpr int kXPartBytes = 2 * kCW * kHT * kXStride * 8;   // partial scores [buf][warp][row][pair]
   static constexpr int kPBytes = 4 * kHT * kPStride * 2;              // P tiles [buf][hi, lo]
@@ -278,28 +277,6 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
-}
-
-// Bound on max_c |c_hat[u][c]| over the scale groups [g0, g1) of token u of
-// a staged block, from its scales (and zero-points): |q| s <= 127 s (INT8),
-// <= 8 s (4-bit symmetric, stored as code + 8), |q - z| s <= max(|z|,
-// |15 - z|) s (asymmetric INT4).  The factor (127 or 8) is applied by the
-// caller (Fmt::kBoundFactor).
-template <int LF, int KF>
-__device__ __forceinline__ float latent_bound(const uint8_t* st, int u, int g0, int g1) {
-  using F = Fmt<LF, KF>;
-  const float* sc = reinterpret_cast<const float*>(st + F::kScaleOff);
-  float mb = 0.f;
-  if (LF == MLA_FMT_INT4_ASYM) {
-    const float* zp = reinterpret_cast<const float*>(st + F::kZeroOff);
-#pragma unroll 8
-    for (int g = g0; g < g1; ++g)
-      mb = fmaxf(mb, sc[g * kBlockTokens + u] * (fabsf(zp[g * kBlockTokens + u] - 7.5f) + 7.5f));
-  } else {
-#pragma unroll 8
-    for (int g = g0; g < g1; ++g) mb = fmaxf(mb, sc[g * kBlockTokens + u]);
-  }
-  return mb;
 }
 
 __device__ __forceinline__ int checked_len(const DecodeParams& p, int b, bool report) {
@@ -706,37 +683,30 @@ __device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha
 // ---------------------------------------------------------------------------
 // Warps 0..7 compute QK^T (step A) and PV (step C) of their latent groups;
 // warpgroup 2 (warps 8..11) runs the online softmax (step B) of every chunk
-// and the loader; warpgroup 3 (warps 12..15), for quantized latents, bounds
-// every staged token's |c_hat| from its scales, for the weight of the fp16
-// P V products the softmax accumulates (a role of its own so that this work
-// stays off the softmax's path).  Hand-offs go through mbarriers with
-// bounded waits:
+// and the loader.  Hand-offs go through mbarriers with bounded waits:
 //   bx[i & 1]: the 8 compute warps have written chunk i's partial scores
-//              (and thread 0 its valid-token count and score scale); the
-//              stage of chunk i is free again;
-//   bp[i & 1]: the 4 softmax warps have written chunk i's P and alpha;
-//   bpart[i & 1]: the 4 bounds warps have posted chunk i's partial maxima;
-//   mready[i & 3]: the bounds M_t of chunk i's tokens are in mbuf;
-//   mfree[i & 3]: the 4 softmax warps have read them (the slot is free);
+//              (thread 0 also its valid-token count and score scale, warp 0
+//              its tokens' bounds M_t into mbuf[i & 1]); the stage of chunk
+//              i is free again;
+//   bp[i & 1]: the 4 softmax warps have written chunk i's P and alpha (and
+//              are done with mbuf[i & 1]);
 //   qa: the compute warps have posted their query magnitudes.
 // Each warp arrives once, from lane 0 after a __syncwarp that orders the
 // whole warp's stores before the arrival.
 // A compute warp therefore runs A(i), arrives on bx, waits for bp of chunk
 // i - 1 and runs C(i - 1), while the softmax warpgroup works on chunk i - 1
-// or i.  Registers move to the compute warps with setmaxnreg: the 512-thread
-// block launches with 128 per thread (65,536), then 224 each for the 256
-// compute threads, 40 for the softmax warpgroup, 24 for the bounds one.
-constexpr int kWsThreads = kThreads + 256;
-constexpr int kRegsCompute = 224, kRegsSoftmax = 40, kRegsBounds = 24;
-static_assert(kThreads * kRegsCompute + 128 * kRegsSoftmax + 128 * kRegsBounds == 65536 &&
-                  65536 / kWsThreads == 128,
+// or i.  Registers move to the compute warps with setmaxnreg: the 384-thread
+// block launches with 168 per thread (64,512), then 232 each for the 256
+// compute threads and 40 for the softmax warpgroup.
+constexpr int kWsThreads = kThreads + 128;
+constexpr int kRegsLaunch = 168, kRegsCompute = 232, kRegsSoftmax = 40;
+static_assert(kThreads * kRegsCompute + 128 * kRegsSoftmax == kWsThreads * kRegsLaunch &&
+                  kWsThreads * kRegsLaunch <= 65536 && kWsThreads * (kRegsLaunch + 8) > 65536,
               "the warpgroups' register shares must add up to the block's launch allocation");
-constexpr int kWsExtra = 15 * 8 + 4 * 4 + 384 * 4;   // bx[2], bp[2], qa, mready[4], mfree[4], bpart[2];
-                                                      // nvq[2], cwq[2]; mbuf[4][32], part[2][4][32]
+constexpr int kWsExtra = 5 * 8 + 4 * 4 + 64 * 4;   // bx[2], bp[2], qa; nvq[2], cwq[2]; mbuf[2][32]
 
 __device__ __forceinline__ void ws_regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n" ::: "memory"); }
-__device__ __forceinline__ void ws_regs_bounds() { asm volatile("setmaxnreg.dec.sync.aligned.u32 24;\n" ::: "memory"); }
-__device__ __forceinline__ void ws_regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 224;\n" ::: "memory"); }
+__device__ __forceinline__ void ws_regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 232;\n" ::: "memory"); }
 
 template <int LF, int KF>
 __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams p) {
@@ -748,16 +718,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   uint16_t* ptab = reinterpret_cast<uint16_t*>(xpart + 2 * kCW * kHT * kXStride);  // [2 buf][hi, lo][16][kPStride]
   float* alpha_s = reinterpret_cast<float*>(ptab + 4 * kHT * kPStride);        // [2][16]
   float* amax_s = alpha_s + 2 * kHT;                                           // [8]
-  float* mbuf = amax_s + kCW;                      // [4][32] token bounds M_t, a ring of chunks (float4 reads)
-  float* part = mbuf + 128;                        // [2][4 bounds warps][32] partial maxima
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(part + 256);
+  float* mbuf = amax_s + kCW;                      // [2][32] token bounds M_t of chunks i & 1 (float4 reads)
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(mbuf + 64);
   uint64_t* bx = full_bar + F::kStages;                                        // [2]
   uint64_t* bp = bx + 2;                                                       // [2]
   uint64_t* qa = bp + 2;                                                       // [1]
-  uint64_t* mready = qa + 1;                                                   // [4]
-  uint64_t* mfree = mready + 4;                                                // [4]
-  uint64_t* bpart = mfree + 4;                                                 // [2]
-  int32_t* meta = reinterpret_cast<int32_t*>(bpart + 2);
+  int32_t* meta = reinterpret_cast<int32_t*>(qa + 1);
   int32_t* nvq = meta + F::kStages;                                            // [2]
   float* cwq = reinterpret_cast<float*>(nvq + 2);                              // [2]
   int32_t* cum = reinterpret_cast<int32_t*>(cwq + 2);
@@ -793,11 +759,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       mbar_init(smem_u32(&bp[k]), 4);        // one per softmax warp
     }
     mbar_init(smem_u32(qa), kCW);
-    for (int k = 0; k < 4; ++k) {
-      mbar_init(smem_u32(&mready[k]), 1);   // the bounds warpgroup's first warp
-      mbar_init(smem_u32(&mfree[k]), 4);    // one arrival per softmax warp
-    }
-    for (int k = 0; k < 2; ++k) mbar_init(smem_u32(&bpart[k]), 4);   // one per bounds warp
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -816,50 +777,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   const int c_lo = (int)range_lo(C, x, Ge), c_hi = (int)range_lo(C, x + 1, Ge);
 
   const int nch = c_hi - c_lo;
-  if (warp >= kCW + 4) {
-    // ============================ bounds warpgroup ============================
-    // Chunk k (relative index): bounds warp wb takes a quarter of the scale
-    // groups, lane = token (tokens past the chunk's end get 0), posts its
-    // partial maxima to part[k & 1][wb] and arrives on bpart[k & 1]; every
-    // bounds warp then takes the max of the four, and the first writes M_t to
-    // mbuf[k & 3] (once the softmax warps have freed the slot, mfree) and
-    // arrives on mready[k & 3].  part[k & 1] is rewritten for chunk k + 2
-    // only after the wait on bpart of chunk k + 1, which every bounds warp
-    // arrives at after reading part[k & 1].  The loader refills a stage only
-    // after mready of its chunk, i.e. after every bounds warp has read it.
-    ws_regs_bounds();
-    if (!F::kRisk) return;
-    const int wb = warp - kCW - 4;
-    constexpr int kPer = (F::kNG + 3) / 4;
-    const int g0 = wb * kPer, g1 = g0 + kPer < F::kNG ? g0 + kPer : F::kNG;
-    for (int k = 0; k < nch; ++k) {
-      const int sk = k % F::kStages;
-      if (!mbar_wait_warp(smem_u32(&full_bar[sk]), (uint32_t)((k / F::kStages) & 1), p.wait_ns)) {
-        set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
-        break;
-      }
-      part[(k & 1) * 128 + wb * 32 + lane] =
-          lane < meta[sk] ? latent_bound<LF, KF>(stages + sk * F::kBlock, lane, g0, g1) : 0.f;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bpart[k & 1]));
-      if (!mbar_wait_warp(smem_u32(&bpart[k & 1]), (uint32_t)((k >> 1) & 1), p.wait_ns)) {
-        set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
-        break;
-      }
-      const float* pp = part + (k & 1) * 128 + lane;
-      const float m_all = fmaxf(fmaxf(pp[0], pp[32]), fmaxf(pp[64], pp[96])) * F::kBoundFactor;
-      if (wb == 0) {
-        if (k >= 4 && !mbar_wait_warp(smem_u32(&mfree[k & 3]), (uint32_t)(((k >> 2) - 1) & 1), p.wait_ns)) {
-          set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
-          break;
-        }
-        mbuf[(k & 3) * 32 + lane] = m_all;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&mready[k & 3]));
-      }
-    }
-    return;
-  }
   if (warp >= kCW) {
     // ======================= softmax / loader warpgroup =======================
     ws_regs_dec();
@@ -932,18 +849,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
         e2 = 0.f;
       }
       if (t == 0) plan();
-      if (!mbar_wait_warp(smem_u32(&bx[i & 1]), (uint32_t)((i >> 1) & 1), p.wait_ns) ||
-          (F::kRisk && !mbar_wait_warp(smem_u32(&mready[i & 3]), (uint32_t)((i >> 2) & 1), p.wait_ns))) {
+      if (!mbar_wait_warp(smem_u32(&bx[i & 1]), (uint32_t)((i >> 1) & 1), p.wait_ns)) {
         set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
         dead = true;
         break;
       }
       float4 mb4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (F::kRisk) {
-        mb4 = *reinterpret_cast<const float4*>(mbuf + (i & 3) * 32 + 4 * tq);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&mfree[i & 3]));
-      }
+      if (F::kRisk) mb4 = *reinterpret_cast<const float4*>(mbuf + (i & 1) * 32 + 4 * tq);
       if (t == 0) commit(s);                   // every compute warp is past chunk i's stage
       const int buf = i & 1, nv = nvq[buf];
       const float cw = cwq[buf];
@@ -1120,6 +1032,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
     if (tid == 0) {
       nvq[i & 1] = nv;
       cwq[i & 1] = cw;
+    }
+    if (F::kRisk && w == 0) {      // the tokens' stored bounds (0 past the chunk's end)
+      const float* bnd = reinterpret_cast<const float*>(stages + s * F::kBlock + F::kBoundOff);
+      mbuf[(i & 1) * 32 + lane] = lane < nv ? bnd[lane] : 0.f;
     }
     __syncwarp();                              // the warp's partial-score stores, then one arrival
     if (lane == 0) mbar_arrive(smem_u32(&bx[i & 1]));

@@ -33,6 +33,7 @@ struct PageLayout {
   int64_t scale_off, zero_off;
   int64_t kpe_off, kpe_row;
   int64_t kpe_scale_off;
+  int64_t bound_off;
 };
 
 // Channels per scale group of a quantized latent format (16 unless one of
@@ -79,6 +80,8 @@ __host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, Page
   off += kBlockTokens * L->kpe_row;
   L->kpe_scale_off = -1;
   if (kpe_fmt != MLA_FMT_BF16) { L->kpe_scale_off = off; off += (int64_t)kNKG * kBlockTokens * 4; }
+  L->bound_off = -1;
+  if (latent_fmt != MLA_FMT_BF16) { L->bound_off = off; off += kBlockTokens * 4; }
   L->block_bytes = off;
   L->page_bytes = 2 * off;
   return true;

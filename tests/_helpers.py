@@ -54,6 +54,7 @@ def read_tokens(pool_np, layout, latent_fmt, kpe_fmt, slots):
         out["c_bits"] = logical.reshape(n, row).copy().view(np.uint16)
     else:
         out["c_scale"] = fp32_field(layout.scale_off, 512 // INT8_GROUP.get(latent_fmt, 16))
+        out["c_bound"] = fp32_field(layout.bound_off, 1)[:, 0]
         if latent_fmt in INT8_GROUP:
             codes = logical.reshape(n, row).view(np.int8).copy()
             if latent_fmt == F_I8G8:         # word j of a chunk: channels 2j, 2j+1, 8+2j, 8+2j+1
@@ -113,6 +114,7 @@ def assert_fields_match(got, c_bits, k_bits, latent_fmt, kpe_fmt):
     else:
         assert np.array_equal(got["c_codes"].astype(np.int16), exp["c_codes"].astype(np.int16)), "latent codes differ"
         assert np.array_equal(got["c_scale"].view(np.uint32), exp["c_scale"].view(np.uint32)), "scales differ"
+        assert np.array_equal(got["c_bound"].view(np.uint32), exp["c_bound"].view(np.uint32)), "bounds differ"
         if latent_fmt == F_INT4:
             assert np.array_equal(got["c_zero"].view(np.uint32), exp["c_zero"].view(np.uint32)), "zeros differ"
     if kpe_fmt == F_BF16:

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
-    assert lib.abi_version() == 103
+    assert lib.abi_version() == 104
 
 
 def test_layouts_match_the_accounting(lib):
@@ -43,16 +43,19 @@ def test_layouts_match_the_accounting(lib):
     pairs = [(lf, kf) for lf in (0, 1, 2, 3) for kf in (0, 1, 3)] + [(lf, 1) for lf in (4, 5, 6, 7)]
     for lf, kf in pairs:
         L = lib.mla_cache_page_layout(lf, kf)
-        assert L.page_bytes == 64 * acc.layer_bytes(lf, kf, metadata=True)
-        for off in (L.codes_off, L.scale_off, L.zero_off, L.kpe_off, L.kpe_scale_off):
+        # the pages' bytes with metadata, plus the 4-byte bound of a quantized latent
+        assert L.page_bytes == 64 * (acc.layer_bytes(lf, kf, metadata=True) + (4 if lf != 0 else 0))
+        for off in (L.codes_off, L.scale_off, L.zero_off, L.kpe_off, L.kpe_scale_off, L.bound_off):
             assert off == -1 or off % 128 == 0
         assert (L.zero_off == -1) == (lf != 2)
+        assert (L.bound_off == -1) == (lf == 0)
+        assert L.bound_off == -1 or L.bound_off + 32 * 4 == L.block_bytes
     for lf in (4, 5, 6, 7):                           # other block counts: INT8 k_pe only
         for kf in (0, 3):
             with pytest.raises(lib.MlaError):
                 lib.mla_cache_page_layout(lf, kf)
-    assert lib.mla_cache_pool_bytes(10, 1, 1) == 10 * 64 * 736
-    assert lib.mla_cache_pool_bytes(10, 2, 3) == 10 * 64 * 576   # the 7.6 KB-per-token scheme, with metadata
+    assert lib.mla_cache_pool_bytes(10, 1, 1) == 10 * 64 * 740
+    assert lib.mla_cache_pool_bytes(10, 2, 3) == 10 * 64 * 580   # the 7.6 KB-per-token scheme, with metadata
     assert lib.mla_cache_pool_bytes(0, 1, 1) == 0
     assert lib.mla_cache_pool_bytes(4, 8, 1) == 0
     assert lib.mla_cache_pool_bytes(4, 1, 2) == 0     # asymmetric INT4 k_pe is not a cache format
