@@ -9,7 +9,8 @@ Sources (page title, section):
 * "Absorbed MLA Cache Optimization on DeepSeek-V2-Lite — Technical Report":
   §1.3 ((192+128) x 16 heads x 2 B = 10,240 B), §2.2 ((512+64)x2 = 1,152 B;
   512x1 + 64x2 = 640 B, 16.9 KB), §4.3 (39K / 340K / 690K / 620K / 1.24M
-  tokens in 10 GB; 8.4 KB for INT4 + k_pe INT8, 32x).
+  tokens in 10 GB; 8.4 KB for INT4 + k_pe INT8, 32x; row C, mixed precision
+  (outlier-protected), 18.2 KB, 14.8x, 580K tokens).
 
 Conventions the pages' numbers fix: "KB" is 1024 bytes (276,480 B is printed
 as 270 KB), "10 GB" is 10 x 2^30 bytes (39K, 690K, 620K, 1.24M and 1.38M all
@@ -26,6 +27,8 @@ or to the printed rounding, in tests/test_oracle_accounting.py).
 
 FMT_BF16, FMT_INT8, FMT_INT4, FMT_INT4_SYM = 0, 1, 2, 3
 FMT_INT8_G8, FMT_INT8_G32, FMT_INT8_G64, FMT_INT8_TOKEN = 4, 5, 6, 7
+FMT_INT8_OUTLIER = 8
+OUTLIER_CHANNELS = 25       # protected bf16 channels of FMT_INT8_OUTLIER
 INT8_GROUP = {FMT_INT8: 16, FMT_INT8_G8: 8, FMT_INT8_G32: 32, FMT_INT8_G64: 64, FMT_INT8_TOKEN: 512}
 
 KV_LORA_RANK = 512
@@ -56,6 +59,8 @@ def _elem_bytes(fmt, n):
         return 2 * n
     if fmt in INT8_GROUP:
         return n
+    if fmt == FMT_INT8_OUTLIER:           # int8 codes plus the protected channels in bf16
+        return n + 2 * OUTLIER_CHANNELS
     if fmt in (FMT_INT4, FMT_INT4_SYM):
         return n // 2
     raise ValueError(fmt)
@@ -76,6 +81,8 @@ def layer_bytes(latent_fmt, kpe_fmt, metadata=False):
         kg = ROPE_DIM // KPE_GROUP
         if latent_fmt in INT8_GROUP:
             b += 4 * (KV_LORA_RANK // INT8_GROUP[latent_fmt])
+        elif latent_fmt == FMT_INT8_OUTLIER:
+            b += 4 * lg
         elif latent_fmt == FMT_INT4:
             b += 8 * lg
         elif latent_fmt == FMT_INT4_SYM:

@@ -34,11 +34,27 @@ Readings taken where the pages are open:
   INT8 rule with 7 levels a side; x_hat = q * s.  Used as a cache format
   for the latent and for k_pe (the report's 7.6 KB scheme pairs asymmetric
   INT4 latent codes with 4-bit k_pe).
+* Outlier-protected mixed precision (the English report's §4.3 row "C:
+  Mixed precision (outlier-protected)", 18.2 KB per token, 14.8x, 580K
+  tokens in 10 GB; no mechanism is given): a fixed set of K = 25 latent
+  channels per layer (5 % of 512, rounded down) keeps its bf16 input
+  exactly; every other channel takes per-group symmetric INT8 (32 groups of
+  16) with the protected channels left out of their group's absmax (their
+  codes are 0); k_pe stays bf16, as in the row "B: latent8+kpe16" it
+  extends.  512 + 2 x 25 + 128 = 690 code bytes per layer reproduce all
+  three printed figures, which 24 or 26 channels do not (INT8 k_pe would
+  need 57 protected channels, 11 %, for the same bytes; the round 5 % with
+  row B's bf16 k_pe is the plainer reading).  The protected set comes from
+  calibration: the K channels with the largest max |x| over a sample of
+  rows (ties to the lower index).
 * All arithmetic is IEEE fp32 with round-half-even (NumPy float32 ops and
   ``np.rint``); no fused multiply-add.
 
 Parity status: pinned (round-trip bound, brute-force nearest level,
-hand-built half-way ties, degenerate groups, the pages' error ordering).
+hand-built half-way ties, degenerate groups, the pages' error ordering; the
+outlier-protected format by exact protected channels, brute-force levels of
+the rest, a literal group, brute-force channel selection and its error
+ordering against per-group INT8).
 """
 
 import numpy as np
@@ -161,6 +177,43 @@ def dequantize_sym_int4(codes, scale, group):
     return dequantize_sym_int8(codes, scale, group)
 
 
+OUTLIER_CHANNELS = 25
+
+
+def select_outlier_channels(sample, k=OUTLIER_CHANNELS):
+    """Calibration of the protected set: the k channels with the largest
+    max |x| over the sample rows [rows, 512], ties to the lower channel
+    index; returned in increasing order (int32 [k])."""
+    a = np.max(np.abs(np.asarray(sample, np.float32)), axis=0)
+    order = sorted(range(a.shape[0]), key=lambda c: (-float(a[c]), c))
+    return np.array(sorted(order[:k]), np.int32)
+
+
+def quantize_int8_outlier(x, outliers, group=16):
+    """Outlier-protected mixed precision (English report §4.3 row C, read as
+    above): per-group symmetric INT8 of the channels outside `outliers`,
+    whose absmax leaves the protected channels out; the protected channels
+    keep their (bf16) input values and get code 0.
+
+    Returns (codes int8 [rows, 512], scale float32 [rows, groups],
+    values float32 [rows, k] of the protected channels in `outliers` order).
+    """
+    x = np.asarray(x, np.float32)
+    o = np.asarray(outliers, np.int64)
+    inl = x.copy()
+    inl[:, o] = 0.0
+    q, s = quantize_sym_int8(inl, group)
+    return q, s, x[:, o].copy()
+
+
+def dequantize_int8_outlier(codes, scale, values, outliers, group=16):
+    """x_hat = code * scale on the INT8 channels, the stored value on the
+    protected ones."""
+    xh = dequantize_sym_int8(codes, scale, group)
+    xh[:, np.asarray(outliers, np.int64)] = np.asarray(values, np.float32)
+    return xh
+
+
 def latent_bound(scale, zero=None, levels=127):
     """Per-token bound M_t on the dequantized latent: the largest magnitude a
     code of the token can dequantize to, the maximum over its groups of
@@ -202,16 +255,18 @@ def relative_error(x, x_hat):
 
 FMT_BF16, FMT_INT8, FMT_INT4, FMT_INT4_SYM = 0, 1, 2, 3
 FMT_INT8_G8, FMT_INT8_G32, FMT_INT8_G64, FMT_INT8_TOKEN = 4, 5, 6, 7
+FMT_INT8_OUTLIER = 8
 LATENT_GROUP, KPE_GROUP = 16, 8
 # symmetric INT8 latent formats -> channels per group (English report §5.1
 # block-count sweep: 64, 16, 8 blocks; Chinese report §3.2 per-token row)
 INT8_GROUP = {FMT_INT8: 16, FMT_INT8_G8: 8, FMT_INT8_G32: 32, FMT_INT8_G64: 64, FMT_INT8_TOKEN: 512}
 
 
-def quantize_token_rows(c, kpe, latent_fmt, kpe_fmt):
+def quantize_token_rows(c, kpe, latent_fmt, kpe_fmt, outliers=None):
     """Quantize latent rows c [N, 512] and k_pe rows kpe [N, 64] as the cache
-    stores them.  Returns a dict of the stored fields plus the dequantized
-    fp32 values the attention reads ("c_hat", "kpe_hat")."""
+    stores them (`outliers`: the protected channels of FMT_INT8_OUTLIER).
+    Returns a dict of the stored fields plus the dequantized fp32 values the
+    attention reads ("c_hat", "kpe_hat")."""
     c = np.asarray(c, np.float32)
     kpe = np.asarray(kpe, np.float32)
     out = {}
@@ -229,6 +284,12 @@ def quantize_token_rows(c, kpe, latent_fmt, kpe_fmt):
         q, s = quantize_sym_int4(c, LATENT_GROUP)
         out.update(c_codes=q, c_scale=s, c_hat=dequantize_sym_int4(q, s, LATENT_GROUP),
                    c_bound=latent_bound(s, levels=7))
+    elif latent_fmt == FMT_INT8_OUTLIER:
+        q, s, v = quantize_int8_outlier(c, outliers, LATENT_GROUP)
+        vmax = np.fmax.reduce(np.abs(v), axis=1).astype(np.float32)
+        out.update(c_codes=q, c_scale=s, c_outlier=v,
+                   c_hat=dequantize_int8_outlier(q, s, v, outliers, LATENT_GROUP),
+                   c_bound=np.fmax(latent_bound(s), vmax).astype(np.float32))
     else:
         raise ValueError("latent_fmt")
     if kpe_fmt == FMT_BF16:

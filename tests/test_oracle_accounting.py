@@ -100,3 +100,20 @@ def test_capacity_in_10gb():
     # EN §4.3 prints 340K for the bf16 latent; the arithmetic gives 345,210
     # (a 1.5 % discrepancy on the page, recorded, not reproduced).
     assert cap(1152) == 345210
+
+
+def test_outlier_protected_row():
+    # EN §4.3 row C: 18.2 KB, 14.8x, 580K tokens in 10 GB.  Read as INT8
+    # latent + 25 protected bf16 channels + bf16 k_pe = 690 B per layer.
+    I8O = acc.FMT_INT8_OUTLIER
+    assert acc.layer_bytes(I8O, B16) == 512 + 2 * 25 + 128 == 690
+    t = acc.token_bytes(690)
+    assert r1(acc.kib(t)) == 18.2 and r1(acc.ratio(276480, t)) == 14.8
+    assert acc.capacity_tokens(t) == 576350 and round(acc.capacity_tokens(t), -4) == 580000
+    # 24 or 26 protected channels miss one of the three printed figures
+    for k in (24, 26):
+        tk = acc.token_bytes(512 + 2 * k + 128)
+        assert not (r1(acc.kib(tk)) == 18.2 and r1(acc.ratio(276480, tk)) == 14.8
+                    and round(acc.capacity_tokens(tk), -4) == 580000)
+    assert acc.layer_bytes(I8O, B16, metadata=True) == 690 + 4 * 32
+    assert acc.layer_bytes(I8O, I8, metadata=True) == 512 + 50 + 64 + 4 * 32 + 4 * 8

@@ -339,3 +339,79 @@ def test_bound_asymmetric_int4_covers_both_ends():
     q, s, z = Q.quantize_asym_int4(w)
     assert Q.latent_bound(s, z)[0] == np.max(s * (np.abs(z - np.float32(7.5)) + np.float32(7.5)))
     assert Q.latent_bound(s, z)[0] >= 4.0 * (1 - 2.0 ** -22)
+
+
+# ---------------------------------------------------------------------------
+# Outlier-protected mixed precision (English report §4.3 row C)
+# ---------------------------------------------------------------------------
+
+def test_select_outlier_channels_brute_force():
+    x = np.zeros((3, 512), np.float32)
+    big = [3, 40, 41, 200, 511]
+    for i, c in enumerate(big):
+        x[i % 3, c] = -(10.0 + i)                         # sign does not matter
+    x[1, 7] = x[2, 9] = 2.0                               # a tie: the lower index goes first
+    x[0, 100] = 1.5
+    got = Q.select_outlier_channels(x, k=7)
+    assert got.tolist() == sorted(big + [7, 9])
+    assert Q.select_outlier_channels(x, k=6).tolist() == sorted(big + [7])
+    # brute force on random data: the chosen set holds the k largest maxima
+    r = RNG.standard_normal((16, 512)).astype(np.float32)
+    sel = Q.select_outlier_channels(r)
+    a = np.max(np.abs(r), axis=0)
+    assert len(sel) == Q.OUTLIER_CHANNELS == 25 and np.all(np.diff(sel) > 0)
+    assert np.min(a[sel]) >= np.max(np.delete(a, sel))
+
+
+def test_outlier_format_literal_group():
+    """Group 0 holds a protected channel of 100 and inliers 1, -1, 0.25: the
+    scale comes from the inliers alone (1 / 127), the protected value is kept
+    exactly; plain per-group INT8 would quantize 1.0 to a single step of
+    100 / 127."""
+    x = np.zeros((1, 512), np.float32)
+    x[0, :4] = [100.0, 1.0, -1.0, 0.25]
+    q, s, v = Q.quantize_int8_outlier(x, [0] + list(range(400, 424)))
+    assert s[0, 0] == np.float32(1.0) / np.float32(127.0)
+    assert q[0, :4].tolist() == [0, 127, -127, 32]        # 0.25 * 127 = 31.75 -> 32
+    assert v[0, 0] == 100.0 and v.shape == (1, 25)
+    xh = Q.dequantize_int8_outlier(q, s, v, [0] + list(range(400, 424)))
+    assert xh[0, 0] == 100.0 and xh[0, 1] == np.float32(127) * s[0, 0]
+    q8, s8 = Q.quantize_sym_int8(x, 16)
+    assert q8[0, 1] == 1 and s8[0, 0] == np.float32(100.0) / np.float32(127.0)
+
+
+def test_outlier_format_exact_channels_and_nearest_levels():
+    c = synth_latent(T=64)
+    o = Q.select_outlier_channels(c)
+    d = Q.quantize_token_rows(c, synth_kpe(T=64), Q.FMT_INT8_OUTLIER, Q.FMT_BF16, outliers=o)
+    assert np.array_equal(d["c_hat"][:, o], c[:, o]) and np.all(d["c_codes"][:, o] == 0)
+    inl = np.setdiff1d(np.arange(512), o)
+    levels = np.arange(-127, 128, dtype=np.float64)
+    for t in range(0, 64, 9):
+        for g in range(32):
+            ch = [k for k in range(16 * g, 16 * g + 16) if k in set(inl.tolist())]
+            a = max((abs(float(c[t, k])) for k in ch), default=0.0)
+            s = np.float32(np.float32(a) / np.float32(127.0))
+            assert d["c_scale"][t, g] == s
+            for k in ch:
+                if s == 0:
+                    assert d["c_codes"][t, k] == 0
+                    continue
+                qf = np.float64(np.float32(c[t, k]) / s)       # the fp32 quotient, then nearest level
+                best = levels[np.argmin(np.abs(levels - qf))]
+                assert abs(d["c_codes"][t, k] - best) <= (1 if abs(abs(qf - best) - 0.5) < 1e-6 else 0)
+    exp = np.max(np.abs(d["c_hat"]), axis=1).astype(np.float32)
+    assert np.array_equal(d["c_bound"].view(np.uint32), exp.view(np.uint32))
+
+
+def test_error_outlier_protection_beats_per_group_int8():
+    """English report §4.3: row C (mixed, outlier-protected) 0.007 below row A
+    (per-group INT8) 0.011 - on the synthetic latent, whose outlier channels
+    the calibration finds."""
+    c = synth_latent(T=512, layer=3)
+    o = Q.select_outlier_channels(c[:128])                  # calibrated on a prefix
+    d = Q.quantize_token_rows(c, synth_kpe(T=512, layer=3), Q.FMT_INT8_OUTLIER, Q.FMT_BF16, outliers=o)
+    q8, s8 = Q.quantize_sym_int8(c, 16)
+    e_mixed = Q.relative_error(c, d["c_hat"])[0]
+    e_int8 = Q.relative_error(c, Q.dequantize_sym_int8(q8, s8, 16))[0]
+    assert e_mixed < 0.8 * e_int8
