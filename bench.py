@@ -55,6 +55,11 @@ CONFIGS = {
                                  desc="V2-Lite INT8 workload with 64 blocks of 8 latent channels"),
     "v2lite_int8_per_token": dict(layers=27, heads=16, batch=8, ctx=4096, latent="int8tok", kpe="int8",
                                   desc="V2-Lite INT8 workload with one scale per token (per-token INT8)"),
+    # the English report's §4.3 row C (outlier-protected mixed precision) on
+    # the V2-Lite INT8 workload: 25 protected bf16 channels per layer, bf16 k_pe
+    "v2lite_int8_outlier": dict(layers=27, heads=16, batch=8, ctx=4096, latent="int8out", kpe="bf16",
+                                desc="DeepSeek-V2-Lite shapes, batch 8, context 4096, INT8 latent with 25 "
+                                     "protected bf16 channels (calibrated per layer) + bf16 k_pe"),
     "long_int4_1m": dict(layers=27, heads=16, batch=1, ctx=1048576, latent="int4", kpe="int8",
                          desc="V2-Lite shapes, batch 1, context 1,048,576, asymmetric INT4 latent + INT8 k_pe"),
     "long_bf16_256k": dict(layers=27, heads=16, batch=1, ctx=262144, latent="bf16", kpe="bf16",
@@ -71,12 +76,14 @@ CONFIGS = {
     "tiny": dict(layers=1, heads=16, batch=1, ctx=256, latent="int8", kpe="int8",
                  desc="1 layer, 16 heads, batch 1, context 256"),
 }
-FMT = {"bf16": 0, "int8": 1, "int4": 2, "int4sym": 3, "int8g8": 4, "int8g32": 5, "int8g64": 6, "int8tok": 7}
+FMT = {"bf16": 0, "int8": 1, "int4": 2, "int4sym": 3, "int8g8": 4, "int8g32": 5, "int8g64": 6, "int8tok": 7,
+       "int8out": 8}
 def _beta(latent, kpe):
     """Stored bytes per token and layer (codes + fp32 scales / zero-points +
     the fp32 bound of a quantized latent), as laid out in include/mla.h:
     32 latent groups of 16, 8 k_pe groups of 8."""
-    code = {"bf16": 1024, "int4": 256, "int4sym": 256}.get(latent, 512)
+    # int8out: 512 codes + 25 protected bf16 values, their field padded to 52 B a token
+    code = {"bf16": 1024, "int4": 256, "int4sym": 256, "int8out": 512 + 52}.get(latent, 512)
     groups = {"int8g8": 64, "int8g32": 16, "int8g64": 8, "int8tok": 1}.get(latent, 32)
     meta = {"bf16": 0, "int4": 8 * groups + 4}.get(latent, 4 * groups + 4)
     kcode = {"bf16": 128, "int8": 64, "int4sym": 32}[kpe]
@@ -86,6 +93,7 @@ def _beta(latent, kpe):
 
 BETA = {(a, b): _beta(a, b) for a in ("bf16", "int8", "int4", "int4sym") for b in ("bf16", "int8", "int4sym")}
 BETA.update({(a, "int8"): _beta(a, "int8") for a in ("int8g8", "int8g32", "int8g64", "int8tok")})
+BETA.update({("int8out", b): _beta("int8out", b) for b in ("bf16", "int8")})
 METRIC = "decode tokens/s & achieved HBM GB/s (% of GB300 peak) for absorbed MLA decode"
 SEED = 0x4D4C41
 FALLBACK_HBM_GBS = 6800.0
@@ -230,7 +238,10 @@ def _oracle_worker(conn, cfg, seq_lens, tasks, seed):
         cos, sin = synth.rope_tables(max(1, T))
         c_bits, k_bits = synth.sequence_bf16(seed, l, b, T, cos, sin)
         c, k = synth.bf16_to_f32(c_bits), synth.bf16_to_f32(k_bits)
-        stored = Q.quantize_token_rows(c[:T - 1], k[:T - 1], lf, kf)
+        outl = None                          # the layer's protected channels (outlier format)
+        if lf == Q.FMT_INT8_OUTLIER:
+            outl = Q.select_outlier_channels(synth.bf16_to_f32(synth.calibration_latent_bf16(seed, l)))
+        stored = Q.quantize_token_rows(c[:T - 1], k[:T - 1], lf, kf, outliers=outl)
         q = [synth.bf16_to_f32(a) for a in (synth.q_nope_bf16(seed, l, B, H)[b:b + 1],
                                              synth.q_pe_bf16(seed, l, B, H)[b:b + 1],
                                              synth.w_uk_bf16(seed, l, H), synth.w_uv_bf16(seed, l, H))]
@@ -240,26 +251,28 @@ def _oracle_worker(conn, cfg, seq_lens, tasks, seed):
             st = synth.channel_stats(seed, l)
             pre = (synth.bf16_to_f32(synth.latent_bf16(seed, l, B, 0, P, stats=st)),
                    synth.bf16_to_f32(synth.kpe_bf16(seed, l, B, 0, P, pcos, psin)))
-        state.append((stored, c[T - 1:], k[T - 1:], q, pre))
+        state.append((stored, c[T - 1:], k[T - 1:], q, pre, outl))
     conn.send("ready")
     while True:
         msg = conn.recv()
         if msg == "stop":
             break
         t0 = time.perf_counter()
-        for stored, c_new, k_new, (qn, qp, wuk, wuv), pre in state:
+        for stored, c_new, k_new, (qn, qp, wuk, wuv), pre, outl in state:
             if pre is not None:
-                Q.quantize_token_rows(pre[0], pre[1], lf, kf)        # prefill append
-            new = Q.quantize_token_rows(c_new, k_new, lf, kf)      # append the new token
-            c_hat = np.concatenate([_dequant_latent(Q, stored, lf), new["c_hat"]])
+                Q.quantize_token_rows(pre[0], pre[1], lf, kf, outliers=outl)      # prefill append
+            new = Q.quantize_token_rows(c_new, k_new, lf, kf, outliers=outl)    # append the new token
+            c_hat = np.concatenate([_dequant_latent(Q, stored, lf, outl), new["c_hat"]])
             kpe_hat = np.concatenate([_dequant_kpe(Q, stored, kf), new["kpe_hat"]])
             A.absorbed_decode_full(qn[0], qp[0], wuk, wuv, c_hat, kpe_hat)
         conn.send(time.perf_counter() - t0)
 
 
-def _dequant_latent(Q, stored, lf):
+def _dequant_latent(Q, stored, lf, outl=None):
     if lf == 1:
         return Q.dequantize_sym_int8(stored["c_codes"], stored["c_scale"], 16)
+    if lf == Q.FMT_INT8_OUTLIER:
+        return Q.dequantize_int8_outlier(stored["c_codes"], stored["c_scale"], stored["c_outlier"], outl, 16)
     if lf == 2:
         return Q.dequantize_asym_int4(stored["c_codes"], stored["c_scale"], stored["c_zero"], 16)
     if lf == 3:

@@ -86,7 +86,15 @@ typedef enum {
   MLA_FMT_INT8_G8 = 4,     /* 64 blocks of 8 channels */
   MLA_FMT_INT8_G32 = 5,    /* 16 blocks of 32 channels */
   MLA_FMT_INT8_G64 = 6,    /* 8 blocks of 64 channels */
-  MLA_FMT_INT8_TOKEN = 7   /* one block of 512 channels (per-token scale) */
+  MLA_FMT_INT8_TOKEN = 7,  /* one block of 512 channels (per-token scale) */
+  /* outlier-protected mixed precision ([EN] §4.3 row "C: Mixed precision
+   * (outlier-protected)", 18.2 KB per token, 14.8x, 580K tokens in 10 GB;
+   * the page gives no mechanism, this is the reading): INT8_SYM latent
+   * (32 groups of 16) except MLA_OUTLIER_CHANNELS protected channels per
+   * layer, kept as their bf16 input and left out of their group's absmax
+   * (their codes are 0).  512 + 2 x 25 code bytes plus bf16 k_pe give the
+   * row's 690 B per layer.  k_pe: MLA_FMT_BF16 (the row) or INT8_SYM. */
+  MLA_FMT_INT8_OUTLIER = 8
 } mla_fmt;
 
 /* Bits ORed into *dev_err. */
@@ -102,6 +110,7 @@ typedef enum {
 #define MLA_PAGE_TOKENS 64
 #define MLA_LATENT_GROUP 16      /* 512 channels = 32 groups ([CN] §3.2 "32块") */
 #define MLA_KPE_GROUP 8          /* 64 channels = 8 groups ([CN] §3.2 "8块")   */
+#define MLA_OUTLIER_CHANNELS 25  /* protected channels of MLA_FMT_INT8_OUTLIER (5 % of 512) */
 
 /*
  * One layer's paged latent cache.  The pool holds num_pages pages of 64
@@ -109,9 +118,15 @@ typedef enum {
  * to which sequence is the caller's business (block tables below).
  *   latent_fmt: any mla_fmt.  kpe_fmt: MLA_FMT_BF16, MLA_FMT_INT8_SYM or
  *   MLA_FMT_INT4_SYM; the INT8_G* / INT8_TOKEN latent formats take
- *   MLA_FMT_INT8_SYM k_pe only.
+ *   MLA_FMT_INT8_SYM k_pe only, INT8_OUTLIER takes BF16 or INT8_SYM.
  *   pool: device memory of mla_cache_pool_bytes() bytes, 256-byte aligned,
  *         owned by the caller.
+ *   outlier_channels: INT8_OUTLIER only (NULL for every other format): HOST
+ *         memory holding the layer's MLA_OUTLIER_CHANNELS protected latent
+ *         channels, strictly increasing, in [0, 512) (for instance from
+ *         mla_select_outlier_channels); read during each call, by value.
+ *         Every call on a layer must pass the same set; a violation of
+ *         these rules is MLA_ERR_INVALID_ARG.
  */
 typedef struct {
   int32_t num_pages;
@@ -119,6 +134,7 @@ typedef struct {
   int32_t kpe_fmt;
   int32_t reserved;        /* must be 0 */
   void* pool;
+  const int32_t* outlier_channels;
 } mla_cache_layer;
 
 /*
@@ -142,6 +158,8 @@ typedef struct {
  *   scale      fp32 [G groups][32 block tokens]    (int8 / 4-bit latent; G = 32,
  *              or 64 / 16 / 8 / 1 for INT8_G8 / G32 / G64 / TOKEN)
  *   zero       fp32 [32 groups][32 block tokens]   (INT4_ASYM latent; integer-valued)
+ *   outlier    bf16 [25 protected channels][32 block tokens], in the order
+ *              of outlier_channels, padded to 1664 bytes (INT8_OUTLIER)
  *   kpe        [32][kpe_row_bytes]: bf16 (128 B = 8 chunks of 8 channels,
  *              chunk c of token u at position c ^ (u & 7)), int8 (64 B =
  *              4 chunks of two 8-channel groups, chunk c at c ^ ((u >> 1) & 3))
@@ -154,8 +172,9 @@ typedef struct {
  *              M_t, the largest magnitude a code of the token's latent can
  *              dequantize to: 127 max_g s_g (INT8 formats), 7 max_g s_g
  *              (INT4_SYM), max_g s_g (|z_g - 7.5| + 7.5) (INT4_ASYM), in
- *              fp32 with one rounding per product.  For INT8 and INT4_SYM
- *              it equals max_c |c_hat[c]|.  Written by mla_cache_append;
+ *              fp32 with one rounding per product; INT8_OUTLIER also takes
+ *              the protected values' magnitudes into the maximum.  For INT8
+ *              and INT4_SYM formats it equals max_c |c_hat[c]|.  Written by mla_cache_append;
  *              the decode reads it to find the rows it recomputes exactly
  *              (see mla_decode_absorbed).
  * page_bytes = 2 * block_bytes = 64 x (1152, 740, 612 or 580) bytes for
@@ -172,6 +191,7 @@ typedef struct {
   int64_t kpe_off, kpe_row_bytes;
   int64_t kpe_scale_off;
   int64_t bound_off;
+  int64_t outlier_off;
 } mla_page_layout;
 
 /* Fills *out for the cache's formats.  MLA_ERR_INVALID_ARG on a bad format. */
@@ -194,6 +214,9 @@ size_t mla_cache_pool_bytes(const mla_cache_layer* cache);
  *   INT4_SYM  (groups of 16 latent channels, or 8 k_pe channels; [CN] §3.2
  *       "对称 INT4" rows): s = max|x| / 7;  q = clamp(rint(x / s), -7, 7);
  *       s = 0 -> q = 0.
+ *   INT8_OUTLIER: the protected channels' input bits are stored, their
+ *       codes are 0, and the INT8_SYM rule runs on the other channels with
+ *       the protected ones counted as 0 in their group's max|x|.
  *   BF16: the input bits are copied.
  *   A quantized latent also gets its bound M_t (see mla_page_layout).
  *   c_new   bf16 [n][512]     kpe_new bf16 [n][64]
@@ -206,6 +229,18 @@ size_t mla_cache_pool_bytes(const mla_cache_layer* cache);
 mla_status mla_cache_append(const mla_cache_layer* cache, const uint16_t* c_new,
                             const uint16_t* kpe_new, const int32_t* slot, int32_t n,
                             int32_t* dev_err, mla_stream_t stream);
+
+/*
+ * mla_select_outlier_channels - calibration of MLA_FMT_INT8_OUTLIER's
+ * protected set ([EN] §4.3 row C, read as in mla_fmt): the
+ * MLA_OUTLIER_CHANNELS latent channels with the largest max |x| over n
+ * sample rows, ties to the lower channel index, written in increasing
+ * order.  NaN inputs are skipped by the maximum.
+ *   c_sample     device bf16 [n][512], 16-byte aligned; n >= 1
+ *   channels_out device int32 [MLA_OUTLIER_CHANNELS], 4-byte aligned
+ */
+mla_status mla_select_outlier_channels(const uint16_t* c_sample, int32_t n, int32_t* channels_out,
+                                       mla_stream_t stream);
 
 /*
  * mla_q_absorb - q_lat[b][h] = q_nope[b][h] @ W_UK[h]   (the query side of

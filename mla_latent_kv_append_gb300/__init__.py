@@ -16,7 +16,9 @@ Names follow the C ABI:
                         num_splits=0)
     mla_out_unabsorb(o_lat, w_uv, o)
 
-plus ``CacheLayer`` (one layer's pool and formats), ``mla_cache_page_layout``,
+plus ``CacheLayer`` (one layer's pool, formats and, for the outlier-protected
+format, its protected channels), ``mla_select_outlier_channels`` (their
+calibration), ``mla_cache_page_layout``,
 ``mla_cache_pool_bytes``, ``mla_decode_workspace_bytes``,
 ``mla_decode_absorbed_noalloc`` (the decode for callers that cannot allocate),
 ``mla_prefill_absorbed`` / ``mla_prefill_workspace_bytes`` (causal attention
@@ -35,6 +37,8 @@ LIB_PATH = os.path.join(_HERE, "libmla_gb300.so")
 
 FMT_BF16, FMT_INT8_SYM, FMT_INT4_ASYM, FMT_INT4_SYM = 0, 1, 2, 3
 FMT_INT8_G8, FMT_INT8_G32, FMT_INT8_G64, FMT_INT8_TOKEN = 4, 5, 6, 7    # INT8 latent, other block counts
+FMT_INT8_OUTLIER = 8        # INT8 latent with OUTLIER_CHANNELS protected bf16 channels
+OUTLIER_CHANNELS = 25
 DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 KV_LORA_RANK, ROPE_DIM, QK_NOPE_DIM, V_DIM, PAGE_TOKENS = 512, 64, 128, 128, 64
 DEFAULT_SOFTMAX_SCALE = 1.0 / math.sqrt(QK_NOPE_DIM + ROPE_DIM)
@@ -51,7 +55,8 @@ class MlaError(RuntimeError):
 
 class _CacheLayer(ctypes.Structure):
     _fields_ = [("num_pages", ctypes.c_int32), ("latent_fmt", ctypes.c_int32), ("kpe_fmt", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("pool", ctypes.c_void_p)]
+                ("reserved", ctypes.c_int32), ("pool", ctypes.c_void_p),
+                ("outlier_channels", ctypes.POINTER(ctypes.c_int32))]
 
 
 class PageLayout(ctypes.Structure):
@@ -59,7 +64,7 @@ class PageLayout(ctypes.Structure):
                 ("codes_row_bytes", ctypes.c_int64),
                 ("scale_off", ctypes.c_int64), ("zero_off", ctypes.c_int64), ("kpe_off", ctypes.c_int64),
                 ("kpe_row_bytes", ctypes.c_int64), ("kpe_scale_off", ctypes.c_int64),
-                ("bound_off", ctypes.c_int64)]
+                ("bound_off", ctypes.c_int64), ("outlier_off", ctypes.c_int64)]
 
 
 def _load():
@@ -85,6 +90,7 @@ def _load():
         "mla_prefill_workspace_bytes": (SZ, [I32, I32]),
         "mla_prefill_absorbed": (I32, [CP, P, P, P, I32, I32, I32, I32, F32, P, SZ, P, P, P, P]),
         "mla_set_wait_limit_ns": (ctypes.c_int64, [ctypes.c_int64]),
+        "mla_select_outlier_channels": (I32, [P, I32, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -118,10 +124,16 @@ def _need(t, dtype, shape, name):
 
 
 class CacheLayer:
-    """One layer's paged latent cache: a caller-owned pool tensor plus formats."""
+    """One layer's paged latent cache: a caller-owned pool tensor plus formats
+    (and, for FMT_INT8_OUTLIER, the layer's OUTLIER_CHANNELS protected
+    channels: a sequence of increasing ints in [0, 512))."""
 
-    def __init__(self, num_pages, latent_fmt, kpe_fmt, device="cuda", pool=None):
+    def __init__(self, num_pages, latent_fmt, kpe_fmt, device="cuda", pool=None, outlier_channels=None):
         self.num_pages, self.latent_fmt, self.kpe_fmt = int(num_pages), int(latent_fmt), int(kpe_fmt)
+        self.outlier_channels = None
+        if outlier_channels is not None:
+            ch = [int(c) for c in outlier_channels]
+            self.outlier_channels = (ctypes.c_int32 * len(ch))(*ch)
         nbytes = mla_cache_pool_bytes(self.num_pages, self.latent_fmt, self.kpe_fmt)
         if nbytes == 0:
             raise ValueError("invalid cache descriptor")
@@ -133,7 +145,9 @@ class CacheLayer:
         self.layout = mla_cache_page_layout(self.latent_fmt, self.kpe_fmt)
 
     def c_struct(self):
-        return _CacheLayer(self.num_pages, self.latent_fmt, self.kpe_fmt, 0, self.pool.data_ptr())
+        oc = None if self.outlier_channels is None else ctypes.cast(self.outlier_channels,
+                                                                      ctypes.POINTER(ctypes.c_int32))
+        return _CacheLayer(self.num_pages, self.latent_fmt, self.kpe_fmt, 0, self.pool.data_ptr(), oc)
 
 
 def mla_cache_page_layout(latent_fmt, kpe_fmt):
@@ -146,6 +160,20 @@ def mla_cache_page_layout(latent_fmt, kpe_fmt):
 def mla_cache_pool_bytes(num_pages, latent_fmt, kpe_fmt):
     c = _CacheLayer(num_pages, latent_fmt, kpe_fmt, 0, None)
     return int(lib.mla_cache_pool_bytes(ctypes.byref(c)))
+
+
+def mla_select_outlier_channels(c_sample, out=None, stream=None):
+    """Protected channels of FMT_INT8_OUTLIER from a calibration sample
+    (bf16 [n, 512] on the GPU): the OUTLIER_CHANNELS channels with the
+    largest max |x|, increasing; returns the int32 device tensor."""
+    n = c_sample.shape[0]
+    _need(c_sample, torch.bfloat16, (n, KV_LORA_RANK), "c_sample")
+    if out is None:
+        out = torch.empty(OUTLIER_CHANNELS, dtype=torch.int32, device=c_sample.device)
+    _need(out, torch.int32, (OUTLIER_CHANNELS,), "out")
+    _check("mla_select_outlier_channels", lib.mla_select_outlier_channels(_ptr(c_sample), n, _ptr(out),
+                                                                          _stream(stream)))
+    return out
 
 
 def mla_decode_workspace_bytes(batch, heads, num_splits=0):

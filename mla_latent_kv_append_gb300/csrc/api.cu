@@ -37,10 +37,21 @@ static bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)
 
 static bool heads_ok(int H) { return H >= 16 && H <= 128 && H % 16 == 0; }
 
-static bool cache_ok(const mla_cache_layer* c, PageLayout* L) {
+bool cache_check(const mla_cache_layer* c, PageLayout* L, OutlierSet* o) {
   if (!c || c->num_pages <= 0 || c->reserved != 0 || !c->pool) return false;
   if (!aligned(c->pool, 256)) return false;
-  return compute_layout(c->latent_fmt, c->kpe_fmt, L);
+  if (!compute_layout(c->latent_fmt, c->kpe_fmt, L)) return false;
+  for (int k = 0; k < kOutSlots; ++k) o->ch[k] = -1;
+  for (int k = 0; k < kDc / 32; ++k) o->mask[k] = 0u;
+  if (c->latent_fmt != MLA_FMT_INT8_OUTLIER) return c->outlier_channels == nullptr;
+  if (!c->outlier_channels) return false;
+  for (int k = 0; k < kNOut; ++k) {
+    const int32_t ch = c->outlier_channels[k];
+    if (ch < 0 || ch >= kDc || (k > 0 && ch <= c->outlier_channels[k - 1])) return false;
+    o->ch[k] = (int16_t)ch;
+    o->mask[ch >> 5] |= 1u << (ch & 31);
+  }
+  return true;
 }
 
 // Context splits of a decode call: the caller's count, else one CTA per SM
@@ -59,7 +70,7 @@ using namespace mla;
 
 extern "C" {
 
-int32_t mla_abi_version(void) { return 104; }
+int32_t mla_abi_version(void) { return 105; }
 
 const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
 
@@ -93,6 +104,7 @@ mla_status mla_cache_page_layout(const mla_cache_layer* cache, mla_page_layout* 
   out->kpe_row_bytes = L.kpe_row;
   out->kpe_scale_off = L.kpe_scale_off;
   out->bound_off = L.bound_off;
+  out->outlier_off = L.outlier_off;
   return MLA_OK;
 }
 
@@ -107,12 +119,20 @@ mla_status mla_cache_append(const mla_cache_layer* cache, const uint16_t* c_new,
                             const uint16_t* kpe_new, const int32_t* slot, int32_t n,
                             int32_t* dev_err, mla_stream_t stream) {
   PageLayout L;
-  if (!cache_ok(cache, &L) || n < 0) return MLA_ERR_INVALID_ARG;
+  OutlierSet outl;
+  if (!cache_check(cache, &L, &outl) || n < 0) return MLA_ERR_INVALID_ARG;
   if (n == 0) return MLA_OK;
   if (!c_new || !kpe_new || !slot) return MLA_ERR_INVALID_ARG;
   if (!aligned(c_new, 16) || !aligned(kpe_new, 16) || !aligned(slot, 4)) return MLA_ERR_INVALID_ARG;
   if (dev_err && !aligned(dev_err, 4)) return MLA_ERR_INVALID_ARG;
-  return launch_append(cache, L, c_new, kpe_new, slot, n, dev_err, (cudaStream_t)stream);
+  return launch_append(cache, L, outl, c_new, kpe_new, slot, n, dev_err, (cudaStream_t)stream);
+}
+
+mla_status mla_select_outlier_channels(const uint16_t* c_sample, int32_t n, int32_t* channels_out,
+                                       mla_stream_t stream) {
+  if (n < 1 || !c_sample || !channels_out || !aligned(c_sample, 16) || !aligned(channels_out, 4))
+    return MLA_ERR_INVALID_ARG;
+  return launch_select_outliers(c_sample, n, channels_out, (cudaStream_t)stream);
 }
 
 mla_status mla_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_lat, int32_t batch,
@@ -160,7 +180,8 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
                                void* workspace, size_t workspace_bytes_, float* o_lat,
                                float* lse, int32_t* dev_err, mla_stream_t stream) {
   PageLayout L;
-  if (!cache_ok(cache, &L)) return MLA_ERR_INVALID_ARG;
+  OutlierSet outl;
+  if (!cache_check(cache, &L, &outl)) return MLA_ERR_INVALID_ARG;
   if (batch < 0 || batch > kMaxBatch || !heads_ok(heads) || num_splits < 0 || num_splits > kMaxSplits)
     return MLA_ERR_INVALID_ARG;
   if (batch == 0) return MLA_OK;
@@ -192,6 +213,7 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
   p.H = heads;
   p.G = G;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.outl = outl;
   p.wait_ns = wait_limit_ns();
   p.ws = carve_workspace(workspace, batch, heads, G);
   p.o_lat = o_lat;

@@ -127,8 +127,8 @@ __device__ __forceinline__ void quant_asym4(const float* x, float& s_out, float&
 }
 
 template <int LF, int KF>
-__global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool, PageLayout L, int64_t num_slots,
-                                                     const uint16_t* __restrict__ c_new,
+__global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool, PageLayout L, OutlierSet outl,
+                                                     int64_t num_slots, const uint16_t* __restrict__ c_new,
                                                      const uint16_t* __restrict__ kpe_new,
                                                      const int32_t* __restrict__ slot, int n,
                                                      int32_t* dev_err) {
@@ -159,6 +159,29 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
       unpack16(v0, v1, x);
       float* scale = reinterpret_cast<float*>(blk + L.scale_off);
       float mb;      // this lane's share of the bound M_t (before the level factor)
+      float mv = 0.f;  // INT8_OUTLIER: the largest protected magnitude of this lane's group
+      if (LF == MLA_FMT_INT8_OUTLIER) {
+        // protected channels of group `lane`: store their input bits in
+        // their slot's row, then count them as 0 for the INT8 rule
+        const uint32_t pm = (outl.mask[lane >> 1] >> (16 * (lane & 1))) & 0xFFFFu;
+        if (pm) {
+          const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          uint16_t* ov = reinterpret_cast<uint16_t*>(blk + L.outlier_off);
+          for (int k = 0; k < kNOut; ++k) {
+            if ((outl.ch[k] >> 4) != lane) continue;
+            const int ci = outl.ch[k] & 15;
+            uint32_t bits = 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (i == ci) bits = (w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+            ov[k * kBlockTokens + t] = (uint16_t)bits;
+            mv = fmaxf(mv, fabsf(__uint_as_float(bits << 16)));
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if ((pm >> i) & 1u) x[i] = 0.f;
+        }
+      }
       if (is_int8_latent(LF)) {
         // lane = 16-channel chunk; a group of GS channels spans GS / 16
         // lanes (absmax by shuffles, every lane then derives the same
@@ -216,10 +239,14 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
       // the token's bound: the largest |c_hat| its codes can reach, the max
       // over groups of (levels a side) x s (asymmetric: s (|z - 7.5| + 7.5))
 #pragma unroll
-      for (int o = 16; o; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+      for (int o = 16; o; o >>= 1) {
+        mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+        if (LF == MLA_FMT_INT8_OUTLIER) mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+      }
       if (lane == 0) {
         const float lv = is_int8_latent(LF) ? 127.f : (LF == MLA_FMT_INT4_SYM ? 7.f : 1.f);
-        reinterpret_cast<float*>(blk + L.bound_off)[t] = LF == MLA_FMT_INT4_ASYM ? mb : __fmul_rn(lv, mb);
+        const float bd = LF == MLA_FMT_INT4_ASYM ? mb : __fmul_rn(lv, mb);
+        reinterpret_cast<float*>(blk + L.bound_off)[t] = LF == MLA_FMT_INT8_OUTLIER ? fmaxf(bd, mv) : bd;
       }
     }
 
@@ -289,8 +316,39 @@ __global__ void __launch_bounds__(256) append_kernel(uint8_t* __restrict__ pool,
   }
 }
 
+// Calibration of the INT8_OUTLIER protected set: one block, thread c takes
+// latent channel c's max |x| over the n sample rows (row-major, so each row
+// is one coalesced sweep), ranks it against the other 511 (larger maxima
+// first, ties to the lower index) and, when it ranks below 25, writes c at
+// its position among the selected channels in increasing order.
+__global__ void __launch_bounds__(kDc) select_outliers_kernel(const uint16_t* __restrict__ c, int n,
+                                                              int32_t* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  __shared__ float amax[kDc];
+  __shared__ int sel[kDc];
+  const int ch = threadIdx.x;
+  float m = 0.f;
+#pragma unroll 8
+  for (int i = 0; i < n; ++i) m = fmaxf(m, fabsf(bf16f(c[(size_t)i * kDc + ch])));
+  amax[ch] = m;
+  __syncthreads();
+  int rank = 0;
+  for (int k = 0; k < kDc; ++k) {
+    const float v = amax[k];
+    rank += (v > m || (v == m && k < ch)) ? 1 : 0;
+  }
+  sel[ch] = rank < kNOut ? 1 : 0;
+  __syncthreads();
+  if (sel[ch]) {
+    int pos = 0;
+    for (int k = 0; k < ch; ++k) pos += sel[k];
+    out[pos] = ch;
+  }
+}
+
 template <int LF, int KF>
-mla_status launch_t(const mla_cache_layer* cache, const PageLayout& L, const uint16_t* c_new,
+mla_status launch_t(const mla_cache_layer* cache, const PageLayout& L, const OutlierSet& outl, const uint16_t* c_new,
                     const uint16_t* kpe_new, const int32_t* slot, int n, int32_t* dev_err,
                     cudaStream_t stream) {
   const int warps_per_block = 8;
@@ -299,18 +357,22 @@ mla_status launch_t(const mla_cache_layer* cache, const PageLayout& L, const uin
   int64_t cap = (int64_t)(sms > 0 ? sms : 1) * 16;
   int grid = (int)(want < cap ? want : cap);
   return cuda_status(launch_pdl(append_kernel<LF, KF>, dim3(grid), dim3(32 * warps_per_block), 0, stream,
-                                (uint8_t*)cache->pool, L, (int64_t)cache->num_pages * kPage, c_new, kpe_new, slot,
-                                n, dev_err));
+                                (uint8_t*)cache->pool, L, outl, (int64_t)cache->num_pages * kPage, c_new, kpe_new,
+                                slot, n, dev_err));
 }
 
 }  // namespace
 
-mla_status launch_append(const mla_cache_layer* cache, const PageLayout& L, const uint16_t* c_new,
-                         const uint16_t* kpe_new, const int32_t* slot, int n, int32_t* dev_err,
-                         cudaStream_t stream) {
+mla_status launch_select_outliers(const uint16_t* c_sample, int n, int32_t* out, cudaStream_t stream) {
+  return cuda_status(launch_pdl(select_outliers_kernel, dim3(1), dim3(kDc), 0, stream, c_sample, n, out));
+}
+
+mla_status launch_append(const mla_cache_layer* cache, const PageLayout& L, const OutlierSet& outl,
+                         const uint16_t* c_new, const uint16_t* kpe_new, const int32_t* slot, int n,
+                         int32_t* dev_err, cudaStream_t stream) {
   const int lf = cache->latent_fmt, kf = cache->kpe_fmt;
 #define MLA_APPEND_CASE(A, K) \
-  if (lf == A && kf == K) return launch_t<A, K>(cache, L, c_new, kpe_new, slot, n, dev_err, stream);
+  if (lf == A && kf == K) return launch_t<A, K>(cache, L, outl, c_new, kpe_new, slot, n, dev_err, stream);
   MLA_APPEND_CASE(MLA_FMT_BF16, MLA_FMT_BF16)
   MLA_APPEND_CASE(MLA_FMT_BF16, MLA_FMT_INT8_SYM)
   MLA_APPEND_CASE(MLA_FMT_INT8_SYM, MLA_FMT_BF16)
@@ -327,6 +389,8 @@ mla_status launch_append(const mla_cache_layer* cache, const PageLayout& L, cons
   MLA_APPEND_CASE(MLA_FMT_INT8_G32, MLA_FMT_INT8_SYM)
   MLA_APPEND_CASE(MLA_FMT_INT8_G64, MLA_FMT_INT8_SYM)
   MLA_APPEND_CASE(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM)
+  MLA_APPEND_CASE(MLA_FMT_INT8_OUTLIER, MLA_FMT_BF16)
+  MLA_APPEND_CASE(MLA_FMT_INT8_OUTLIER, MLA_FMT_INT8_SYM)
 #undef MLA_APPEND_CASE
   return MLA_ERR_UNSUPPORTED;
 }

@@ -104,6 +104,14 @@ __device__ void dequant_chunk(const DecodeParams& p, int b, int t0, int len, flo
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           v[j] = __fmul_rn((float)(int8_t)(w >> (8 * j)), sc[(ch[j] / latent_group_size(LF)) * kBlockTokens + t]);
+        if (LF == MLA_FMT_INT8_OUTLIER) {      // protected channels: the stored bf16 value
+          const uint16_t* ov = reinterpret_cast<const uint16_t*>(blk + p.L.outlier_off);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if ((p.outl.mask[ch[j] >> 5] >> (ch[j] & 31)) & 1u)
+              for (int k = 0; k < kNOut; ++k)
+                if (p.outl.ch[k] == ch[j]) v[j] = bf16f(ov[k * kBlockTokens + t]);
+        }
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) s_c[t * kCS + ch[j]] = v[j];
@@ -688,6 +696,8 @@ mla_status launch_combine(const DecodeParams& p, cudaStream_t stream) {
   MLA_COMBINE_CASE(MLA_FMT_INT8_G32, MLA_FMT_INT8_SYM)
   MLA_COMBINE_CASE(MLA_FMT_INT8_G64, MLA_FMT_INT8_SYM)
   MLA_COMBINE_CASE(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM)
+  MLA_COMBINE_CASE(MLA_FMT_INT8_OUTLIER, MLA_FMT_BF16)
+  MLA_COMBINE_CASE(MLA_FMT_INT8_OUTLIER, MLA_FMT_INT8_SYM)
 #undef MLA_COMBINE_CASE
   return MLA_ERR_UNSUPPORTED;
 }

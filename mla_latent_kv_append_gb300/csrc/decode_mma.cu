@@ -58,6 +58,7 @@ struct Fmt {
   static constexpr bool kLatBf16 = LF == MLA_FMT_BF16;
   static constexpr bool kLatInt4 = LF == MLA_FMT_INT4_ASYM || LF == MLA_FMT_INT4_SYM;
   static constexpr bool kLatSym4 = LF == MLA_FMT_INT4_SYM;       // zero-point fixed at 8 (nibble = code + 8)
+  static constexpr bool kLatOut = LF == MLA_FMT_INT8_OUTLIER;    // INT8 plus 25 protected bf16 channels
   static constexpr bool kKpeBf16 = KF == MLA_FMT_BF16;
   static constexpr bool kKpeInt4 = KF == MLA_FMT_INT4_SYM;
   static constexpr int kRow = kLatBf16 ? 1024 : (is_int8_latent(LF) ? 512 : 256);
@@ -69,7 +70,6 @@ struct Fmt {
   // 2j+1 and 8+2j, 8+2j+1) for bf16 and 8-channel groups, else permuted
   // (thread j holds channels 4j .. 4j+3)
   static constexpr bool kStdLayout = kLatBf16 || kLatG8;
-  static constexpr int kNG = kDc / kGS;                          // scale groups per token
   // quantized latents: the softmax warps also accumulate, per head row, the
   // weight of the fp16 P V products (sum of (p_t M_t)^2, M_t the token's
   // stored bound on |c_hat|), from which the combine decides whether the row
@@ -77,13 +77,17 @@ struct Fmt {
   static constexpr bool kRisk = !kLatBf16;
   static constexpr int kScaleOff = kBlockTokens * kRow;
   static constexpr int kZeroOff = kScaleOff + (kLatBf16 ? 0 : (kDc / kGS) * kBlockTokens * 4);
-  static constexpr int kKpeOff = kZeroOff + (LF == MLA_FMT_INT4_ASYM ? kNLG * kBlockTokens * 4 : 0);
+  static constexpr int kOutOff = kZeroOff + (LF == MLA_FMT_INT4_ASYM ? kNLG * kBlockTokens * 4 : 0);
+  static constexpr int kKpeOff = kOutOff + (kLatOut ? kOutFieldBytes : 0);
   static constexpr int kKScaleOff = kKpeOff + kBlockTokens * kKRow;
   static constexpr int kBoundOff = kKScaleOff + (kKpeBf16 ? 0 : kNKG * kBlockTokens * 4);
   static constexpr int kBlock = kBoundOff + (kLatBf16 ? 0 : kBlockTokens * 4);
   static constexpr int kStages = kBlock <= 24 * 1024 ? 6 : (kBlock <= 40 * 1024 ? 4 : 3);
   static constexpr int kXPartBytes = 2 * kCW * kHT * kXStride * 8;   // partial scores [buf][warp][row][pair]
-  static constexpr int kPBytes = 4 * kHT * kPStride * 2;              // P tiles [buf][hi, lo]
+  // P tiles per buffer: fp16 P (bf16 hi for a bf16 latent), bf16 lo; with
+  // protected channels also bf16 hi and lo of P for their P V products
+  static constexpr int kPTiles = kLatOut ? 4 : 2;
+  static constexpr int kPBytes = 2 * kPTiles * kHT * kPStride * 2;    // [buf][tile][16][kPStride]
   static constexpr int kFixed = kStages * kBlock + kXPartBytes + kPBytes + (2 * kHT + kCW) * 4 + kStages * 8 + kStages * 4;
   // shared-memory offsets that vector accesses rely on: stages and the P
   // tiles (16 B), the bounds array after alpha / amax (float4 reads)
@@ -191,6 +195,13 @@ __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0
 // d = a * b + c for m16n8k8 (two A registers, one B register)
 __device__ __forceinline__ void mma_f16_k8(float* d, uint32_t a0, uint32_t a1, uint32_t b0, const float* c) {
   asm("mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%8,%9,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+// d = a * b + c for m16n8k8 bf16
+__device__ __forceinline__ void mma_bf16_k8(float* d, uint32_t a0, uint32_t a1, uint32_t b0, const float* c) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%8,%9,%10};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(b0), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
@@ -304,16 +315,19 @@ __device__ __forceinline__ int seq_of_chunk(const int32_t* cum, int B, int c) {
 struct QueryRaw {            // this thread's fp32 query values, before range scaling
   float4 x[4][2];            // q_lat: [group][row r / r+8], the 4 channels this thread feeds
   float kx[2][4];            // q_pe: [row][4 channels]
+  float ox[2][2];            // protected channels (INT8_OUTLIER): [row][slot 4w + 2j + e]
 };
 
 struct ChunkRegs {           // one chunk's B operands, kept from QK^T for PV
   uint32_t bq[4][4][2];      // exact codes (or code - zero): [group][ntile][reg]
   uint32_t s2h[4][4];        // fp16 scale pairs of the C-fragment tokens: [group][ntile]
+  uint32_t ov[2][2];         // protected values (bf16 token pairs of slot 4w + r): [k step][reg]
 };
 
 struct Query {
   uint32_t hi[4][4], lo[4][4];   // A fragments of q_lat (hi + lo split) for the warp's 4 groups
   uint32_t ka[4];                // A fragment of q_pe for the warp's k_pe group / chunk
+  uint32_t oh[2], ol[2];         // m16n8k8 A fragments (bf16 hi + lo) of the warp's protected channels
 };
 
 // Loads this thread's share of q_lat / q_pe and returns its largest magnitude.
@@ -366,6 +380,18 @@ __device__ __forceinline__ float load_query_raw(const DecodeParams& p, int b, in
     }
   }
   float amax = 0.f;
+  if (F::kLatOut) {
+    // the warp's protected slots 4w .. 4w+3 (k = slot - 4w of an m16n8k8 step;
+    // threads j = 0, 1 feed k = 2j, 2j + 1, threads 2, 3 the zero half)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int sl = 4 * w + 2 * j + e;
+      const int ch = (j < 2 && sl < kNOut) ? p.outl.ch[sl] : -1;
+      q.ox[0][e] = ch >= 0 ? ql0[ch] : 0.f;
+      q.ox[1][e] = ch >= 0 ? ql1[ch] : 0.f;
+      amax = fmaxf(amax, fmaxf(fabsf(q.ox[0][e]), fabsf(q.ox[1][e])));
+    }
+  }
 #pragma unroll
   for (int g = 0; g < 4; ++g)
 #pragma unroll
@@ -402,6 +428,10 @@ __device__ __forceinline__ void finish_query(const QueryRaw& raw, float up, Quer
       q.lo[g][rr] = l01;
       q.lo[g][rr + 2] = l23;
     }
+  if (F::kLatOut) {
+    split_bf16(raw.ox[0][0] * up, raw.ox[0][1] * up, q.oh[0], q.ol[0]);
+    split_bf16(raw.ox[1][0] * up, raw.ox[1][1] * up, q.oh[1], q.ol[1]);
+  }
   if (F::kKpeBf16) {
     q.ka[0] = pack_bf16(raw.kx[0][0] * up, raw.kx[0][1] * up);
     q.ka[1] = pack_bf16(raw.kx[1][0] * up, raw.kx[1][1] * up);
@@ -422,7 +452,8 @@ __device__ __forceinline__ void finish_query(const QueryRaw& raw, float up, Quer
 // nv: its valid tokens.
 template <int LF, int KF>
 __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int lane, const Query& q,
-                                         uint32_t (&bq)[4][4][2], uint32_t (&s2h)[4][4], float (&acc)[4][4]) {
+                                         uint32_t (&bq)[4][4][2], uint32_t (&s2h)[4][4], uint32_t (&ov)[2][2],
+                                         float (&acc)[4][4]) {
   using F = Fmt<LF, KF>;
   const int r = lane >> 2, j = lane & 3;
   const bool partial = nv < kChunk;     // includes nv == 0 (no data: everything is masked)
@@ -607,19 +638,57 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
       scale_acc(acc[n], d, s2);
     }
   }
+  if (F::kLatOut && 4 * w < kNOut) {
+    // protected channels, slots 4w .. 4w+3 (rows [slot][32 tokens] of bf16):
+    // QK^T adds q (bf16 hi + lo) x the stored values, one m16n8k8 step with
+    // k = slot (B: slots 2j, 2j+1 of token 8n + r; zero for j >= 2 and for
+    // slots past the 25th, whose rows do not exist); the P V operand (token
+    // pairs of slot 4w + r, zero past the chunk's end) is kept for step C
+    const uint16_t* ovs = reinterpret_cast<const uint16_t*>(st + F::kOutOff);
+    const int s0 = 4 * w + 2 * j;
+#pragma unroll
+    for (int n = 0; n < 4; ++n) {
+      uint32_t b = 0u;
+      if (j < 2) {
+        const uint32_t v0 = s0 < kNOut ? ovs[s0 * kBlockTokens + 8 * n + r] : 0u;
+        const uint32_t v1 = s0 + 1 < kNOut ? ovs[(s0 + 1) * kBlockTokens + 8 * n + r] : 0u;
+        b = v0 | (v1 << 16);
+      }
+      mma_bf16_k8(acc[n], q.oh[0], q.oh[1], b, acc[n]);
+      mma_bf16_k8(acc[n], q.ol[0], q.ol[1], b, acc[n]);
+    }
+    const int sl = 4 * w + r;
+#pragma unroll
+    for (int ks2 = 0; ks2 < 2; ++ks2)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = 16 * ks2 + 8 * e + 2 * j;
+        uint32_t v = (r < 4 && sl < kNOut) ? *reinterpret_cast<const uint32_t*>(ovs + sl * kBlockTokens + tok) : 0u;
+        if (partial) v &= (tok < nv ? 0x0000FFFFu : 0u) | (tok + 1 < nv ? 0xFFFF0000u : 0u);
+        ov[ks2][e] = v;
+      }
+  }
 }
 
 // Step C of one chunk for warp w: rescale o by the chunk's alpha and add
-// P V with the operands bqv / scales s2v kept from its step A.  alpha_s:
-// [2][16]; ptab: the P tiles [2 buf][hi, lo][16][kPStride].
+// P V with the operands bqv / scales s2v kept from its step A (and, with
+// protected channels, their P V into oo with the operands ovv).  alpha_s:
+// [2][16]; ptab: the P tiles [2 buf][kPTiles][16][kPStride].
 template <int LF, int KF>
-__device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha_s, const uint16_t* ptab, int buf,
-                                         const uint32_t (&bqv)[4][4][2], const uint32_t (&s2v)[4][4], int lane) {
+__device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], float (&oo)[4], const float* alpha_s,
+                                         const uint16_t* ptab, int buf, const uint32_t (&bqv)[4][4][2],
+                                         const uint32_t (&s2v)[4][4], const uint32_t (&ovv)[2][2], int w, int lane) {
   using F = Fmt<LF, KF>;
   const int r = lane >> 2;
     {
     const float al0 = alpha_s[buf * kHT + r], al1 = alpha_s[buf * kHT + r + 8];
     if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+      if (F::kLatOut) {
+        oo[0] *= al0;
+        oo[1] *= al0;
+        oo[2] *= al1;
+        oo[3] *= al1;
+      }
 #pragma unroll
       for (int g = 0; g < 4; ++g)
 #pragma unroll
@@ -635,7 +704,7 @@ __device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha
   }
   uint32_t pa[2][2][4];      // [hi/lo][k step][reg]
   {
-    const uint32_t pbase = smem_u32(ptab) + (2 * buf) * kHT * kPStride * 2 +
+    const uint32_t pbase = smem_u32(ptab) + (F::kPTiles * buf) * kHT * kPStride * 2 +
                            ((lane & 7) + 8 * ((lane >> 3) & 1)) * kPStride * 2 + 8 * (lane >> 4) * 2;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
@@ -674,6 +743,20 @@ __device__ __forceinline__ void pv_chunk(float (&o)[4][2][4], const float* alpha
 #pragma unroll
         for (int e = 0; e < 2; ++e) mma_f16(o[g][e], ag, vt[2 * ks][e], vt[2 * ks + 1][e], o[g][e]);
       }
+    }
+  }
+  if (F::kLatOut && 4 * w < kNOut) {
+    // protected channels: oo [16 heads][slots 4w + 2j, +1] += P (bf16 hi + lo)
+    // x values (m16n8k16, k = tokens, n = slot 4w + r; columns 4..7 are zero)
+    const uint32_t pb = smem_u32(ptab) + (F::kPTiles * buf + 2) * kHT * kPStride * 2 +
+                        ((lane & 7) + 8 * ((lane >> 3) & 1)) * kPStride * 2 + 8 * (lane >> 4) * 2;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      uint32_t ph[4], pl[4];
+      ldsm_x4(pb + 32 * ks, ph[0], ph[1], ph[2], ph[3]);
+      ldsm_x4(pb + kHT * kPStride * 2 + 32 * ks, pl[0], pl[1], pl[2], pl[3]);
+      mma_bf16(oo, ph, ovv[ks][0], ovv[ks][1], oo);
+      mma_bf16(oo, pl, ovv[ks][0], ovv[ks][1], oo);
     }
   }
 }
@@ -715,8 +798,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   float2* xpart = reinterpret_cast<float2*>(smem + F::kStages * F::kBlock);   // [2][8 warps][16 rows][kXStride]
-  uint16_t* ptab = reinterpret_cast<uint16_t*>(xpart + 2 * kCW * kHT * kXStride);  // [2 buf][hi, lo][16][kPStride]
-  float* alpha_s = reinterpret_cast<float*>(ptab + 4 * kHT * kPStride);        // [2][16]
+  uint16_t* ptab = reinterpret_cast<uint16_t*>(xpart + 2 * kCW * kHT * kXStride);  // [2 buf][kPTiles][16][kPStride]
+  float* alpha_s = reinterpret_cast<float*>(ptab + 2 * F::kPTiles * kHT * kPStride);   // [2][16]
   float* amax_s = alpha_s + 2 * kHT;                                           // [8]
   float* mbuf = amax_s + kCW;                      // [2][32] token bounds M_t of chunks i & 1 (float4 reads)
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(mbuf + 64);
@@ -776,7 +859,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   if (x >= Ge) return;
   const int c_lo = (int)range_lo(C, x, Ge), c_hi = (int)range_lo(C, x + 1, Ge);
 
-  const int nch = c_hi - c_lo;
   if (warp >= kCW) {
     // ======================= softmax / loader warpgroup =======================
     ws_regs_dec();
@@ -895,7 +977,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
         const float a0 = pv[0] * mb4.x, a1 = pv[1] * mb4.y, a2 = pv[2] * mb4.z, a3 = pv[3] * mb4.w;
         e2 = fmaf(e2 * al, al, fmaf(a0, a0, fmaf(a1, a1, fmaf(a2, a2, a3 * a3))));
       }
-      uint2* prow = reinterpret_cast<uint2*>(ptab + ((2 * buf) * kHT + hr) * kPStride) + tq;
+      uint2* prow = reinterpret_cast<uint2*>(ptab + ((F::kPTiles * buf) * kHT + hr) * kPStride) + tq;
       if (F::kLatBf16) {
         uint32_t h0w, l0w, h1w, l1w;
         split_bf16(pv[0], pv[1], h0w, l0w);
@@ -904,6 +986,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
         prow[kHT * kPStride / 4] = make_uint2(l0w, l1w);
       } else {
         prow[0] = make_uint2(pack_f16(pv[0], pv[1]), pack_f16(pv[2], pv[3]));
+      }
+      if (F::kLatOut) {                        // bf16 hi + lo of P for the protected channels
+        uint32_t h0w, l0w, h1w, l1w;
+        split_bf16(pv[0], pv[1], h0w, l0w);
+        split_bf16(pv[2], pv[3], h1w, l1w);
+        prow[2 * kHT * kPStride / 4] = make_uint2(h0w, h1w);
+        prow[3 * kHT * kPStride / 4] = make_uint2(l0w, l1w);
       }
       if (tq == 0) alpha_s[buf * kHT + hr] = al;
       __syncwarp();                            // the warp's P and alpha stores, then one arrival
@@ -939,6 +1028,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   Query q;
   float cw = 0.f;
   float o[4][2][4];
+  float oo[4] = {0.f, 0.f, 0.f, 0.f};     // protected channels (INT8_OUTLIER): rows r, r+8 x slots 4w+2j, +1
   ChunkRegs ra, rb;
   bool pending = false;
   int b = -1, s = 0, i = 0;
@@ -962,8 +1052,34 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
         *reinterpret_cast<float2*>(o1 + base + 2 * j) = make_float2(o[g][0][2], o[g][0][3]);
         *reinterpret_cast<float2*>(o1 + base + 8 + 2 * j) = make_float2(o[g][1][2], o[g][1][3]);
       } else {
-        *reinterpret_cast<float4*>(o0 + base + 4 * j) = make_float4(o[g][0][0], o[g][0][1], o[g][1][0], o[g][1][1]);
-        *reinterpret_cast<float4*>(o1 + base + 4 * j) = make_float4(o[g][0][2], o[g][0][3], o[g][1][2], o[g][1][3]);
+        const float4 v0 = make_float4(o[g][0][0], o[g][0][1], o[g][1][0], o[g][1][1]);
+        const float4 v1 = make_float4(o[g][0][2], o[g][0][3], o[g][1][2], o[g][1][3]);
+        const int c0 = base + 4 * j;
+        // protected channels are written below by their slot's owner
+        const uint32_t pm = F::kLatOut ? (p.outl.mask[c0 >> 5] >> (c0 & 31)) & 0xFu : 0u;
+        if (pm == 0u) {
+          *reinterpret_cast<float4*>(o0 + c0) = v0;
+          *reinterpret_cast<float4*>(o1 + c0) = v1;
+        } else {
+          const float a0[4] = {v0.x, v0.y, v0.z, v0.w}, a1[4] = {v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (!((pm >> e) & 1u)) {
+              o0[c0 + e] = a0[e];
+              o1[c0 + e] = a1[e];
+            }
+        }
+      }
+    }
+    if (F::kLatOut && j < 2) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int sl = 4 * w + 2 * j + e;
+        if (sl < kNOut) {
+          const int ch = p.outl.ch[sl];
+          o0[ch] = oo[e];
+          o1[ch] = oo[2 + e];
+        }
       }
     }
   };
@@ -975,7 +1091,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
       return false;
     }
-    pv_chunk<LF, KF>(o, alpha_s, ptab, pi & 1, prev.bq, prev.s2h, lane);
+    pv_chunk<LF, KF>(o, oo, alpha_s, ptab, pi & 1, prev.bq, prev.s2h, prev.ov, w, lane);
     pending = false;
     return true;
   };
@@ -1013,6 +1129,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
         for (int e = 0; e < 2; ++e)
 #pragma unroll
           for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) oo[k] = 0.f;
     }
     if (!mbar_wait_warp(smem_u32(&full_bar[s]), phase, p.wait_ns)) {
       set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
@@ -1020,7 +1138,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
     }
     const int nv = meta[s];
     float acc[4][4];
-    qk_chunk<LF, KF>(stages + s * F::kBlock, nv, w, lane, q, cur.bq, cur.s2h, acc);
+    qk_chunk<LF, KF>(stages + s * F::kBlock, nv, w, lane, q, cur.bq, cur.s2h, cur.ov, acc);
     {
       float2* xw = xpart + (((size_t)(i & 1) * kCW + w) * kHT + r) * kXStride + j;
 #pragma unroll
@@ -1071,6 +1189,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       for (int e = 0; e < 2; ++e)
 #pragma unroll
         for (int k = 0; k < 4; ++k) o[g][e][k] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) oo[k] = 0.f;
     for (int bb = b >= 0 ? b : seq_of_chunk(cum, p.B, c_lo); bb < p.B && cum[bb] < c_hi; ++bb)
       if (cum[bb] < cum[bb + 1]) flush_o(bb);
   }
@@ -1128,6 +1248,8 @@ mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream) {
   MLA_MMA_CASE(MLA_FMT_INT8_G32, MLA_FMT_INT8_SYM)
   MLA_MMA_CASE(MLA_FMT_INT8_G64, MLA_FMT_INT8_SYM)
   MLA_MMA_CASE(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM)
+  MLA_MMA_CASE(MLA_FMT_INT8_OUTLIER, MLA_FMT_BF16)
+  MLA_MMA_CASE(MLA_FMT_INT8_OUTLIER, MLA_FMT_INT8_SYM)
 #undef MLA_MMA_CASE
   return MLA_ERR_UNSUPPORTED;
 }

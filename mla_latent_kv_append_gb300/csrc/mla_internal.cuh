@@ -18,6 +18,9 @@ constexpr int kLG = MLA_LATENT_GROUP;      // 16
 constexpr int kKG = MLA_KPE_GROUP;         // 8
 constexpr int kNLG = kDc / kLG;            // 32 latent groups
 constexpr int kNKG = kDr / kKG;            // 8 k_pe groups
+constexpr int kNOut = MLA_OUTLIER_CHANNELS;  // 25 protected channels (INT8_OUTLIER)
+constexpr int kOutSlots = 32;              // their slots in the decode kernel (8 warps x 4)
+constexpr int kOutFieldBytes = 1664;       // bf16 [25][32 tokens] = 1600 B, padded to 128
 constexpr int kChunk = 32;                 // decode work unit: 32 tokens
 constexpr int kMaxBatch = 4096;
 constexpr int kMaxSplits = 65535;          // decode grid dimension y
@@ -34,6 +37,15 @@ struct PageLayout {
   int64_t kpe_off, kpe_row;
   int64_t kpe_scale_off;
   int64_t bound_off;
+  int64_t outlier_off;
+};
+
+// The protected channels of an INT8_OUTLIER layer, passed to the kernels by
+// value: slot k < 25 holds channel ch[k] (increasing), slots 25..31 hold -1;
+// bit c of mask is set for a protected channel c.
+struct OutlierSet {
+  int16_t ch[kOutSlots];
+  uint32_t mask[kDc / 32];
 };
 
 // Channels per scale group of a quantized latent format (16 unless one of
@@ -45,7 +57,7 @@ __host__ __device__ constexpr int latent_group_size(int latent_fmt) {
          : latent_fmt == MLA_FMT_INT8_TOKEN ? kDc : kLG;
 }
 __host__ __device__ constexpr bool is_int8_latent(int latent_fmt) {
-  return latent_fmt == MLA_FMT_INT8_SYM || (latent_fmt >= MLA_FMT_INT8_G8 && latent_fmt <= MLA_FMT_INT8_TOKEN);
+  return latent_fmt == MLA_FMT_INT8_SYM || (latent_fmt >= MLA_FMT_INT8_G8 && latent_fmt <= MLA_FMT_INT8_OUTLIER);
 }
 
 __host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, PageLayout* L) {
@@ -60,6 +72,10 @@ __host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, Page
       row = kDc;
       break;
     case MLA_FMT_INT8_SYM: row = kDc; break;
+    case MLA_FMT_INT8_OUTLIER:
+      if (kpe_fmt != MLA_FMT_BF16 && kpe_fmt != MLA_FMT_INT8_SYM) return false;
+      row = kDc;
+      break;
     case MLA_FMT_INT4_ASYM:
     case MLA_FMT_INT4_SYM: row = kDc / 2; break;
     default: return false;
@@ -75,6 +91,8 @@ __host__ __device__ inline bool compute_layout(int latent_fmt, int kpe_fmt, Page
     off += (int64_t)(kDc / latent_group_size(latent_fmt)) * kBlockTokens * 4;
   }
   if (latent_fmt == MLA_FMT_INT4_ASYM) { L->zero_off = off; off += (int64_t)kNLG * kBlockTokens * 4; }
+  L->outlier_off = -1;
+  if (latent_fmt == MLA_FMT_INT8_OUTLIER) { L->outlier_off = off; off += kOutFieldBytes; }
   L->kpe_off = off;
   L->kpe_row = kpe_fmt == MLA_FMT_BF16 ? 2 * kDr : (kpe_fmt == MLA_FMT_INT8_SYM ? kDr : kDr / 2);
   off += kBlockTokens * L->kpe_row;
@@ -202,14 +220,18 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // Host side launch helpers (api.cu)
 int device_sm_count();
+// Checks a layer descriptor (pool, formats, protected channels) and fills its
+// page layout and protected set (empty unless INT8_OUTLIER).
+bool cache_check(const mla_cache_layer* c, PageLayout* L, OutlierSet* o);
 uint64_t wait_limit_ns();                // set by mla_set_wait_limit_ns
 mla_status launch_status();
 mla_status cuda_status(cudaError_t e);   // records the error string on failure
 
 // Launchers implemented in the kernel translation units.
-mla_status launch_append(const mla_cache_layer* cache, const PageLayout& L, const uint16_t* c_new,
-                         const uint16_t* kpe_new, const int32_t* slot, int n, int32_t* dev_err,
-                         cudaStream_t stream);
+mla_status launch_append(const mla_cache_layer* cache, const PageLayout& L, const OutlierSet& outl,
+                         const uint16_t* c_new, const uint16_t* kpe_new, const int32_t* slot, int n,
+                         int32_t* dev_err, cudaStream_t stream);
+mla_status launch_select_outliers(const uint16_t* c_sample, int n, int32_t* out, cudaStream_t stream);
 mla_status launch_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_lat, int B, int H,
                            cudaStream_t stream);
 mla_status launch_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o, int B, int H,
@@ -231,6 +253,7 @@ struct DecodeParams {
                           // prefill's lengths): read it only after waiting on that kernel
   int B, H, G;
   float scale_log2;       // softmax_scale * log2(e)
+  OutlierSet outl;        // INT8_OUTLIER: the protected channels
   uint64_t wait_ns;       // bound on every wait inside the decode kernel (wait_limit_ns())
   Workspace ws;
   float* o_lat;

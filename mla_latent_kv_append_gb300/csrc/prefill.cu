@@ -53,9 +53,8 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
                                 int32_t heads, float softmax_scale, void* workspace, size_t workspace_bytes_,
                                 float* o_lat, float* lse, int32_t* dev_err, mla_stream_t stream) {
   PageLayout L;
-  if (!cache || cache->num_pages <= 0 || cache->reserved != 0 || !cache->pool || !aligned_to(cache->pool, 256) ||
-      !compute_layout(cache->latent_fmt, cache->kpe_fmt, &L))
-    return MLA_ERR_INVALID_ARG;
+  OutlierSet outl;
+  if (!cache_check(cache, &L, &outl)) return MLA_ERR_INVALID_ARG;
   if (n < 0 || ctx_before < 0 || heads < 16 || heads > 128 || heads % 16) return MLA_ERR_INVALID_ARG;
   if (n == 0) return MLA_OK;
   if (max_pages <= 0 || (int64_t)max_pages * kPage > (int64_t)INT32_MAX) return MLA_ERR_INVALID_ARG;
@@ -101,6 +100,7 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
     p.H = heads;
     p.G = G;
     p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.outl = outl;
     p.wait_ns = wait_limit_ns();
     p.ws = carve_workspace(split_ws, s, heads, G);
     p.o_lat = o_lat + (size_t)i0 * heads * kDc;

@@ -142,6 +142,15 @@ def latent_bf16(seed, layer, b, t0, t1, kind=KIND_LATENT, stats=None):
     return out
 
 
+# The rows a layer's protected channels (outlier-protected format) are
+# calibrated on: the first CALIBRATION_TOKENS latent rows of sequence 0.
+CALIBRATION_TOKENS = 256
+
+
+def calibration_latent_bf16(seed, layer):
+    return latent_bf16(seed, layer, 0, 0, CALIBRATION_TOKENS, stats=channel_stats(seed, layer))
+
+
 def kpe_bf16(seed, layer, b, t0, t1, cos_tab, sin_tab, kind=KIND_KPE):
     """k_pe rows of sequence b, positions t0..t1-1 -> uint16 [t1-t0, 64]."""
     key = stream_key(seed, layer, kind)

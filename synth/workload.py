@@ -12,6 +12,11 @@ A workload may also carry a prefill: P tokens of one further sequence
 decode step, into spare pages of the same pools (the mixed serving step:
 prefill quantize-on-write plus batched decode).
 
+The outlier-protected format's protected channels (per layer) come from the
+library's calibration call over the rows ``synth.calibration_latent_bf16``
+gives on the host (the first synth.CALIBRATION_TOKENS latent rows of
+sequence 0), from which the oracle makes its own selection.
+
 Host twins of every tensor come from ``synth`` (NumPy) for the oracle.
 """
 
@@ -44,8 +49,15 @@ class Workload:
         self.block_table_host = bt
         self.block_table = torch.from_numpy(bt).to(device)
         self.seq_lens_dev = torch.tensor(self.seq_lens, dtype=torch.int32, device=device)
-        self.caches = [mla.CacheLayer(self.num_pages + self.prefill_pages, latent_fmt, kpe_fmt, device=device)
-                       for _ in range(self.L)]
+        self.outliers = [None] * self.L
+        if latent_fmt == mla.FMT_INT8_OUTLIER:
+            for l in range(self.L):
+                sample = torch.empty((synth.CALIBRATION_TOKENS, synth.D_C), dtype=torch.bfloat16, device=device)
+                sd.latent_into(sample, seed, l, 0, 0, sd.LayerStats(seed, l, device))
+                self.outliers[l] = mla.mla_select_outlier_channels(sample).cpu().tolist()
+        self.caches = [mla.CacheLayer(self.num_pages + self.prefill_pages, latent_fmt, kpe_fmt, device=device,
+                                      outlier_channels=self.outliers[l])
+                       for l in range(self.L)]
         self.rope = sd.RopeTables(max(1, self.prefill, max(self.seq_lens) if self.seq_lens else 1), device)
         self.w_uk = [sd.w_uk(seed, l, self.H, device) for l in range(self.L)]
         self.w_uv = [sd.w_uv(seed, l, self.H, device) for l in range(self.L)]
@@ -137,6 +149,10 @@ class Workload:
         T = self.seq_lens[b]
         cos, sin = synth.rope_tables(max(1, T))
         return synth.sequence_bf16(self.seed, layer, b, T, cos, sin, stats=synth.channel_stats(self.seed, layer))
+
+    def host_calibration_sample(self, layer):
+        """bf16 bits of the rows the protected channels are calibrated on."""
+        return synth.calibration_latent_bf16(self.seed, layer)
 
     def host_prefill(self, layer):
         """bf16 bits of the prefill tokens (sequence B, positions 0..P-1)."""

@@ -9,11 +9,12 @@ from oracle import quant as Q
 
 F_BF16, F_INT8, F_INT4, F_INT4S = 0, 1, 2, 3
 F_I8G8, F_I8G32, F_I8G64, F_I8TOK = 4, 5, 6, 7
-INT8_GROUP = {F_INT8: 16, F_I8G8: 8, F_I8G32: 32, F_I8G64: 64, F_I8TOK: 512}
+F_I8OUT = 8
+INT8_GROUP = {F_INT8: 16, F_I8G8: 8, F_I8G32: 32, F_I8G64: 64, F_I8TOK: 512, F_I8OUT: 16}
 ALL_FORMATS = ([(lf, kf) for lf in (F_BF16, F_INT8, F_INT4, F_INT4S) for kf in (F_BF16, F_INT8, F_INT4S)] +
                [(lf, F_INT8) for lf in (F_I8G8, F_I8G32, F_I8G64, F_I8TOK)])
 FMT_NAME = {F_BF16: "bf16", F_INT8: "int8", F_INT4: "int4", F_INT4S: "int4sym", F_I8G8: "int8g8",
-            F_I8G32: "int8g32", F_I8G64: "int8g64", F_I8TOK: "int8tok"}
+            F_I8G32: "int8g32", F_I8G64: "int8g64", F_I8TOK: "int8tok", F_I8OUT: "int8out"}
 
 ATTN_TOL = 2e-3          # max relative error of attention outputs (per row, inf-norm)
 
@@ -55,6 +56,10 @@ def read_tokens(pool_np, layout, latent_fmt, kpe_fmt, slots):
     else:
         out["c_scale"] = fp32_field(layout.scale_off, 512 // INT8_GROUP.get(latent_fmt, 16))
         out["c_bound"] = fp32_field(layout.bound_off, 1)[:, 0]
+        if latent_fmt == F_I8OUT:
+            idx = (base + layout.outlier_off)[:, None, None] + ((np.arange(25)[None, :] * 32 + u[:, None]) * 2)[..., None] \
+                + np.arange(2)
+            out["c_outlier_bits"] = pool_np[idx].reshape(n, 25, 2).copy().view(np.uint16)[..., 0]
         if latent_fmt in INT8_GROUP:
             codes = logical.reshape(n, row).view(np.int8).copy()
             if latent_fmt == F_I8G8:         # word j of a chunk: channels 2j, 2j+1, 8+2j, 8+2j+1
@@ -106,15 +111,18 @@ def _nibbles(logical, n, nchunk, channels=512):
     return codes
 
 
-def assert_fields_match(got, c_bits, k_bits, latent_fmt, kpe_fmt):
+def assert_fields_match(got, c_bits, k_bits, latent_fmt, kpe_fmt, outliers=None):
     """Bit-exact comparison of stored fields with the oracle's quantization."""
-    exp = Q.quantize_token_rows(synth.bf16_to_f32(c_bits), synth.bf16_to_f32(k_bits), latent_fmt, kpe_fmt)
+    exp = Q.quantize_token_rows(synth.bf16_to_f32(c_bits), synth.bf16_to_f32(k_bits), latent_fmt, kpe_fmt,
+                                outliers=outliers)
     if latent_fmt == F_BF16:
         assert np.array_equal(got["c_bits"], c_bits)
     else:
         assert np.array_equal(got["c_codes"].astype(np.int16), exp["c_codes"].astype(np.int16)), "latent codes differ"
         assert np.array_equal(got["c_scale"].view(np.uint32), exp["c_scale"].view(np.uint32)), "scales differ"
         assert np.array_equal(got["c_bound"].view(np.uint32), exp["c_bound"].view(np.uint32)), "bounds differ"
+        if latent_fmt == F_I8OUT:
+            assert np.array_equal(got["c_outlier_bits"], c_bits[:, np.asarray(outliers)]), "protected values differ"
         if latent_fmt == F_INT4:
             assert np.array_equal(got["c_zero"].view(np.uint32), exp["c_zero"].view(np.uint32)), "zeros differ"
     if kpe_fmt == F_BF16:
@@ -140,10 +148,16 @@ class OracleCache:
         c_bits, k_bits = self.wl.host_sequence(layer, b)
         return c_bits, k_bits
 
+    def outliers(self, layer):
+        """The oracle's own calibration of the protected channels (outlier format)."""
+        if self.wl.latent_fmt != F_I8OUT:
+            return None
+        return Q.select_outlier_channels(synth.bf16_to_f32(synth.calibration_latent_bf16(self.wl.seed, layer)))
+
     def decode(self, layer, b):
         """(q_lat, o_lat, lse, o) of the oracle for sequence b of `layer`."""
         qn, qp, wuk, wuv = self.query(layer)
         c_bits, k_bits = self.sequence(layer, b)
         d = Q.quantize_token_rows(synth.bf16_to_f32(c_bits), synth.bf16_to_f32(k_bits), self.wl.latent_fmt,
-                                  self.wl.kpe_fmt)
+                                  self.wl.kpe_fmt, outliers=self.outliers(layer))
         return A.absorbed_decode_full(qn[b], qp[b], wuk, wuv, d["c_hat"], d["kpe_hat"])

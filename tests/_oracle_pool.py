@@ -33,13 +33,21 @@ def tokens_bf16(seed, layer, b, T, t0, t1, stats, cos, sin):
     return np.concatenate(cs), np.concatenate(ks)
 
 
+def oracle_outliers(seed, layer, lf):
+    """The oracle's calibration of a layer's protected channels (outlier format only)."""
+    if lf != Q.FMT_INT8_OUTLIER:
+        return None
+    return Q.select_outlier_channels(synth.bf16_to_f32(synth.calibration_latent_bf16(seed, layer)))
+
+
 def range_partials(task):
     """(layer, b, m [H], l [H], o [H, 512]) of the oracle over tokens [t0, t1)."""
     seed, layer, b, B, T, H, lf, kf, t0, t1 = task
     stats = synth.channel_stats(seed, layer)
     cos, sin = synth.rope_tables(t1)
     c, k = tokens_bf16(seed, layer, b, T, t0, t1, stats, cos, sin)
-    d = Q.quantize_token_rows(synth.bf16_to_f32(c), synth.bf16_to_f32(k), lf, kf)
+    d = Q.quantize_token_rows(synth.bf16_to_f32(c), synth.bf16_to_f32(k), lf, kf,
+                              outliers=oracle_outliers(seed, layer, lf))
     qn = synth.bf16_to_f32(synth.q_nope_bf16(seed, layer, B, H))[b]
     qp = synth.bf16_to_f32(synth.q_pe_bf16(seed, layer, B, H))[b]
     wuk = synth.bf16_to_f32(synth.w_uk_bf16(seed, layer, H))

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
-    assert lib.abi_version() == 104
+    assert lib.abi_version() == 105
 
 
 def test_layouts_match_the_accounting(lib):
@@ -57,7 +57,7 @@ def test_layouts_match_the_accounting(lib):
     assert lib.mla_cache_pool_bytes(10, 1, 1) == 10 * 64 * 740
     assert lib.mla_cache_pool_bytes(10, 2, 3) == 10 * 64 * 580   # the 7.6 KB-per-token scheme, with metadata
     assert lib.mla_cache_pool_bytes(0, 1, 1) == 0
-    assert lib.mla_cache_pool_bytes(4, 8, 1) == 0
+    assert lib.mla_cache_pool_bytes(4, 9, 1) == 0
     assert lib.mla_cache_pool_bytes(4, 1, 2) == 0     # asymmetric INT4 k_pe is not a cache format
 
 
@@ -141,3 +141,37 @@ def test_wait_limit_hook(lib):
     finally:
         lib.mla_set_wait_limit_ns(prev)
     assert prev == 10 ** 10
+
+
+def test_outlier_format_descriptor_rules(lib):
+    """INT8_OUTLIER layouts, and the host checks of the protected set: present,
+    25 strictly increasing channels in [0, 512), absent for other formats."""
+    from oracle import accounting as acc
+    for kf in (0, 1):
+        L = lib.mla_cache_page_layout(8, kf)
+        # the pages' 690 B (+64 for INT8 k_pe) and scales, the bound, 2 B of padding
+        assert L.page_bytes == 64 * (acc.layer_bytes(8, kf, metadata=True) + 4 + 2)
+        assert L.outlier_off == L.scale_off + 32 * 32 * 4 and L.outlier_off % 128 == 0
+        assert L.kpe_off == L.outlier_off + 1664
+    assert lib.mla_cache_pool_bytes(2, 8, 3) == 0                 # 4-bit k_pe is not offered with it
+    assert lib.mla_cache_page_layout(1, 1).outlier_off == -1
+    raw = lib.lib
+    fake = ctypes.c_void_p(0x10000)
+    good = list(range(0, 500, 20))
+    assert len(good) == 25
+
+    def call(fmt, channels):
+        arr = None if channels is None else (ctypes.c_int32 * len(channels))(*channels)
+        cs = lib._CacheLayer(4, fmt, 0, 0, 0x100000,
+                             None if arr is None else ctypes.cast(arr, ctypes.POINTER(ctypes.c_int32)))
+        return raw.mla_cache_append(ctypes.byref(cs), fake, fake, fake, 0, None, None)   # n = 0: no launch
+    assert call(8, good) == 0
+    assert call(8, None) == 1
+    assert call(8, [good[1]] + [good[0]] + good[2:]) == 1       # not increasing
+    assert call(8, good[:24] + [good[23]]) == 1                  # repeated
+    assert call(8, good[:24] + [512]) == 1                       # out of range
+    assert call(8, [-1] + good[1:]) == 1
+    assert call(1, good) == 1                                    # other formats take none
+    assert call(1, None) == 0
+    assert raw.mla_select_outlier_channels(fake, 0, fake, None) == 1
+    assert raw.mla_select_outlier_channels(ctypes.c_void_p(0x10002), 4, fake, None) == 1

@@ -23,7 +23,7 @@ import synth
 from oracle import attention as A
 from synth.workload import DecodeStep, Workload
 from tests._helpers import ATTN_TOL, assert_fields_match, read_tokens
-from tests._oracle_pool import make_pool, oracle_outputs, tokens_bf16
+from tests._oracle_pool import make_pool, oracle_outliers, oracle_outputs, tokens_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -34,6 +34,7 @@ CASES = [
     ("v2lite_int4_kpe4_32k", (0, 26)),
     ("v2lite_int8_per_token", (0, 13, 26)),
     ("v2lite_int8_64blocks", (0, 26)),
+    ("v2lite_int8_outlier", (0, 13, 26)),
     ("long_int4_1m", SAMPLED),
     ("long_bf16_256k", SAMPLED),
     ("mixed_h64_int8", None),
@@ -64,7 +65,7 @@ def check_stored_windows(wl, layers, rng, seqs_per_layer=3, windows=6, width=64)
                 t1 = min(T, t0 + width)
                 c, k = tokens_bf16(wl.seed, l, b, T, t0, t1, stats, cos, sin)
                 got = read_tokens(pool_np, wl.caches[l].layout, lf, kf, wl.slots(b, t0, t1))
-                assert_fields_match(got, c, k, lf, kf)
+                assert_fields_match(got, c, k, lf, kf, outliers=oracle_outliers(wl.seed, l, lf))
         del pool_np
 
 
@@ -100,4 +101,4 @@ def test_full_size_parity(pool, name, layers):
         for l in layers[:1] + layers[-1:]:
             c, k = wl.host_prefill(l)
             got = read_tokens(wl.caches[l].pool.cpu().numpy(), wl.caches[l].layout, lf, kf, wl.slot_pre_host)
-            assert_fields_match(got, c, k, lf, kf)
+            assert_fields_match(got, c, k, lf, kf, outliers=oracle_outliers(wl.seed, l, lf))
