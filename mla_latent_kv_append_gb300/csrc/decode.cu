@@ -445,8 +445,12 @@ __device__ __forceinline__ bool merge_head(const DecodeParams& p, int b, int h, 
   return true;
 }
 
+// One block per SM (64 registers a thread): at two per SM the 32-register
+// limit spilled the merge and the exact path's live state, which cost more
+// (4K INT8 call 26.6 against 19.7 us, step 0.908 against 0.772 ms) than the
+// SM it leaves to the next kernel's early blocks.
 template <int LF, int KF>
-__global__ void __launch_bounds__(kCombThreads, 2) combine_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(DecodeParams p) {
   pdl_launch_dependents();
   pdl_wait();
   extern __shared__ __align__(16) float short_smem[];
