@@ -456,17 +456,20 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
                                          float (&acc)[4][4]) {
   using F = Fmt<LF, KF>;
   const int r = lane >> 2, j = lane & 3;
-  const bool partial = nv < kChunk;     // includes nv == 0 (no data: everything is masked)
-  // Tokens past nv hold stale or unwritten bytes.  Their scores need no mask
+  // Tokens past nv (nv may be 0: no data, everything masked) hold stale or
+  // unwritten bytes.  Their scores need no mask
   // here (the softmax replaces them with -inf by selection), but everything
   // PV multiplies with their zero P must be finite: their scales and
   // zero-points are masked bitwise.  mc[n]: the C-fragment token pair
   // (8n + 2j, 8n + 2j + 1), as f16x2 lanes; mb[n]: the B-operand token 8n + r.
+  // The masks are applied to full chunks too: one branch-free instance of
+  // this step measured faster (32K INT4 call 0.282 against 0.295 ms) than
+  // either a run-time test or a separate instance for full chunks.
   uint32_t mc[4], mb[4];
 #pragma unroll
   for (int n = 0; n < 4; ++n) {
-    mc[n] = partial ? (8 * n + 2 * j < nv ? 0x0000FFFFu : 0u) | (8 * n + 2 * j + 1 < nv ? 0xFFFF0000u : 0u) : ~0u;
-    mb[n] = partial ? (8 * n + r < nv ? ~0u : 0u) : ~0u;
+    mc[n] = (8 * n + 2 * j < nv ? 0x0000FFFFu : 0u) | (8 * n + 2 * j + 1 < nv ? 0xFFFF0000u : 0u);
+    mb[n] = 8 * n + r < nv ? ~0u : 0u;
   }
   const uint32_t st_a = smem_u32(st);
   const float* sc = reinterpret_cast<const float*>(st + F::kScaleOff);
@@ -481,13 +484,14 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
       ldsm_x4(st_a + lane * F::kRow + latent_chunk_pos(ch + 1, lane) * 16, t0, t1, t2, t3);
       bq[g][0][1] = t0; bq[g][1][1] = t1; bq[g][2][1] = t2; bq[g][3][1] = t3;
     }
-    if (partial) {       // PV reads these values: zero the tokens past the end
+    // PV reads these values: zero the tokens past the end
 #pragma unroll
-      for (int n = 0; n < 4; ++n)
-        if (8 * n + r >= nv)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-          for (int g = 0; g < 4; ++g) bq[g][n][0] = bq[g][n][1] = 0u;
-    }
+      for (int g = 0; g < 4; ++g) {
+        bq[g][n][0] &= mb[n];
+        bq[g][n][1] &= mb[n];
+      }
   } else if (F::kLatInt4) {
     const float* zp = reinterpret_cast<const float*>(st + F::kZeroOff);
     const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f), km64 = __floats2half2_rn(-64.f, -64.f);
@@ -664,7 +668,7 @@ __device__ __forceinline__ void qk_chunk(const uint8_t* st, int nv, int w, int l
       for (int e = 0; e < 2; ++e) {
         const int tok = 16 * ks2 + 8 * e + 2 * j;
         uint32_t v = (r < 4 && sl < kNOut) ? *reinterpret_cast<const uint32_t*>(ovs + sl * kBlockTokens + tok) : 0u;
-        if (partial) v &= (tok < nv ? 0x0000FFFFu : 0u) | (tok + 1 < nv ? 0xFFFF0000u : 0u);
+        v &= (tok < nv ? 0x0000FFFFu : 0u) | (tok + 1 < nv ? 0xFFFF0000u : 0u);
         ov[ks2][e] = v;
       }
   }
