@@ -956,11 +956,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
       }
       const float4 sm = make_float4(s01.x, s01.y, s23.x, s23.y);
       float xv[4] = {sm.x * cw, sm.y * cw, sm.z * cw, sm.w * cw};
-      if (nv < kChunk) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (4 * tq + k >= nv) xv[k] = -INFINITY;
-      }
+      for (int k = 0; k < 4; ++k) xv[k] = 4 * tq + k < nv ? xv[k] : -INFINITY;
       float mx = fmaxf(fmaxf(xv[0], xv[1]), fmaxf(xv[2], xv[3]));
 #pragma unroll
       for (int off = 1; off < 8; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -1151,13 +1148,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
         xw[8 * kXStride + 4 * n] = make_float2(acc[n][2], acc[n][3]);
       }
     }
-    if (tid == 0) {
+    if (w == 0) {                  // warp-uniform: every lane stores the same count and scale
       nvq[i & 1] = nv;
       cwq[i & 1] = cw;
-    }
-    if (F::kRisk && w == 0) {      // the tokens' stored bounds (0 past the chunk's end)
-      const float* bnd = reinterpret_cast<const float*>(stages + s * F::kBlock + F::kBoundOff);
-      mbuf[(i & 1) * 32 + lane] = lane < nv ? bnd[lane] : 0.f;
+      if (F::kRisk) {              // the tokens' stored bounds (0 past the chunk's end)
+        const float* bnd = reinterpret_cast<const float*>(stages + s * F::kBlock + F::kBoundOff);
+        mbuf[(i & 1) * 32 + lane] = lane < nv ? bnd[lane] : 0.f;
+      }
     }
     __syncwarp();                              // the warp's partial-score stores, then one arrival
     if (lane == 0) mbar_arrive(smem_u32(&bx[i & 1]));

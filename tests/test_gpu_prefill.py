@@ -26,7 +26,12 @@ class Chunk:
         self.lf, self.kf, self.ctx_before, self.n, self.H, self.seed, self.layer = lf, kf, ctx_before, n, H, seed, layer
         self.T = T = ctx_before + n
         pages = (T + 63) // 64
-        self.cache = mla.CacheLayer(pages + spare_pages, lf, kf)
+        outl = None
+        if lf == mla.FMT_INT8_OUTLIER:     # the library's calibration on the workload's sample rows
+            sample = torch.empty((synth.CALIBRATION_TOKENS, synth.D_C), dtype=torch.bfloat16, device="cuda")
+            sd.latent_into(sample, seed, layer, 0, 0, sd.LayerStats(seed, layer))
+            outl = mla.mla_select_outlier_channels(sample).cpu().tolist()
+        self.cache = mla.CacheLayer(pages + spare_pages, lf, kf, outlier_channels=outl)
         self.cache.pool.fill_(0xFF)
         perm = synth.page_permutation(seed, pages + spare_pages)[:pages].astype(np.int32)
         self.block_table = torch.from_numpy(perm).cuda()
@@ -65,7 +70,10 @@ class Chunk:
         cos, sin = synth.rope_tables(max(1, self.T))
         c = synth.latent_bf16(seed, layer, 0, 0, self.T, stats=synth.channel_stats(seed, layer))
         k = synth.kpe_bf16(seed, layer, 0, 0, self.T, cos, sin)
-        d = Q.quantize_token_rows(synth.bf16_to_f32(c), synth.bf16_to_f32(k), self.lf, self.kf)
+        outl = None
+        if self.lf == Q.FMT_INT8_OUTLIER:  # the oracle's own calibration
+            outl = Q.select_outlier_channels(synth.bf16_to_f32(synth.calibration_latent_bf16(seed, layer)))
+        d = Q.quantize_token_rows(synth.bf16_to_f32(c), synth.bf16_to_f32(k), self.lf, self.kf, outliers=outl)
         qn = synth.bf16_to_f32(synth.prefill_q_nope_bf16(seed, layer, rows, H))
         qp = synth.bf16_to_f32(synth.prefill_q_pe_bf16(seed, layer, rows, H))
         wuk = synth.bf16_to_f32(synth.w_uk_bf16(seed, layer, H))
@@ -96,7 +104,7 @@ FORMATS = [(mla.FMT_INT8_SYM, mla.FMT_INT8_SYM), (mla.FMT_INT4_ASYM, mla.FMT_INT
            (mla.FMT_INT4_SYM, mla.FMT_INT4_SYM), (mla.FMT_INT8_G8, mla.FMT_INT8_SYM),
            (mla.FMT_INT8_TOKEN, mla.FMT_INT8_SYM), (mla.FMT_INT8_G32, mla.FMT_INT8_SYM),
            (mla.FMT_INT8_G64, mla.FMT_INT8_SYM), (mla.FMT_INT4_ASYM, mla.FMT_INT4_SYM),
-           (mla.FMT_BF16, mla.FMT_INT8_SYM)]
+           (mla.FMT_BF16, mla.FMT_INT8_SYM), (mla.FMT_INT8_OUTLIER, mla.FMT_BF16)]
 
 
 @pytest.mark.parametrize("lf,kf", FORMATS, ids=["%s-%s" % (FMT_NAME[a], FMT_NAME[b]) for a, b in FORMATS])
@@ -180,3 +188,10 @@ def test_full_size_prefill_sampled(name):
         worst = max(worst, e1, e2)
         assert e1 < ATTN_TOL and e2 < ATTN_TOL and e3 < ATTN_TOL, (name, i, e1, e2, e3)
     print("%s prefill: %d rows compared, worst max-rel error %.2e" % (name, len(rows), worst))
+
+
+def test_prefill_outlier_format_past_the_exact_length():
+    """The outlier-protected format with prefixes long enough for the split
+    path (query rows at 301 .. 700 tokens), 32 heads."""
+    check(Chunk(mla.FMT_INT8_OUTLIER, mla.FMT_INT8_SYM, 300, 400, 32, seed=91),
+          rows=list(range(0, 400, 7)) + [399])
