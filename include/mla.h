@@ -308,6 +308,30 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
                                float* lse, int32_t* dev_err, mla_stream_t stream);
 
 /*
+ * mla_decode_absorbed_unabsorb - mla_decode_absorbed followed by
+ * mla_out_unabsorb on its o_lat, in one call: o[b][h] = o_lat[b][h] @ W_UV[h]
+ * ([TU] "步骤2", V_i = C^KV W_i^upV, the output side of the absorption).
+ * The arguments are mla_decode_absorbed's plus
+ *   w_uv  device bf16 [H][512][128], 16-byte aligned (as mla_out_unabsorb)
+ *   o     device fp32 [B][H][128], 16-byte aligned
+ * Both must be non-NULL (MLA_ERR_INVALID_ARG otherwise).  o_lat and lse are
+ * written as by mla_decode_absorbed.  When the batch takes the combine's
+ * one-block-per-(sequence, head) grid (about 8 to 32 context splits per
+ * sequence, e.g. a few sequences of a few thousand tokens), that block
+ * projects its row right after merging it (fp32 multiply-adds over bf16
+ * W_UV), which removes a kernel from the decode step's critical path;
+ * otherwise the call launches the unabsorb kernel after the combine.  The
+ * two ways differ only in the order of the fp32 sums.
+ */
+mla_status mla_decode_absorbed_unabsorb(const mla_cache_layer* cache, const float* q_lat,
+                                        const uint16_t* q_pe, const int32_t* block_table,
+                                        int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                                        int32_t heads, float softmax_scale, int32_t num_splits,
+                                        void* workspace, size_t workspace_bytes, float* o_lat,
+                                        float* lse, const uint16_t* w_uv, float* o, int32_t* dev_err,
+                                        mla_stream_t stream);
+
+/*
  * mla_decode_absorbed_noalloc - the same decode as mla_decode_absorbed for
  * callers that cannot allocate device memory: a plugin handed only its input
  * and output buffers, code running during CUDA-graph capture (cudaMalloc is

@@ -20,7 +20,8 @@ plus ``CacheLayer`` (one layer's pool, formats and, for the outlier-protected
 format, its protected channels), ``mla_select_outlier_channels`` (their
 calibration), ``mla_cache_page_layout``,
 ``mla_cache_pool_bytes``, ``mla_decode_workspace_bytes``,
-``mla_decode_absorbed_noalloc`` (the decode for callers that cannot allocate),
+``mla_decode_absorbed_unabsorb`` (the decode and the output projection in
+one call), ``mla_decode_absorbed_noalloc`` (the decode for callers that cannot allocate),
 ``mla_prefill_absorbed`` / ``mla_prefill_workspace_bytes`` (causal attention
 of a prefill chunk) and ``mla_lse_merge`` (merges per-part results of a context-sharded decode;
 the host side of that exchange is in ``sharded``).
@@ -84,6 +85,7 @@ def _load():
         "mla_q_absorb": (I32, [P, P, P, I32, I32, P]),
         "mla_decode_workspace_bytes": (SZ, [I32, I32, I32]),
         "mla_decode_absorbed": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, SZ, P, P, P, P]),
+        "mla_decode_absorbed_unabsorb": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, SZ, P, P, P, P, P, P]),
         "mla_out_unabsorb": (I32, [P, P, P, I32, I32, P]),
         "mla_decode_absorbed_noalloc": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, P, P, P]),
         "mla_lse_merge": (I32, [P, P, I32, I32, I32, P, P, P]),
@@ -222,6 +224,28 @@ def mla_decode_absorbed(cache, q_lat, q_pe, block_table, seq_lens, workspace, o_
         ctypes.byref(cs), _ptr(q_lat), _ptr(q_pe), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H,
         scale, int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o_lat),
         _ptr(lse), _ptr(dev_err), _stream(stream)))
+
+
+def mla_decode_absorbed_unabsorb(cache, q_lat, q_pe, block_table, seq_lens, workspace, o_lat, w_uv, o, lse=None,
+                                 dev_err=None, softmax_scale=None, num_splits=0, stream=None):
+    """mla_decode_absorbed then mla_out_unabsorb on its o_lat, in one call
+    (the projection fused into the combine where its grid allows)."""
+    B, H = q_lat.shape[0], q_lat.shape[1]
+    _need(q_lat, torch.float32, (B, H, KV_LORA_RANK), "q_lat")
+    _need(q_pe, torch.bfloat16, (B, H, ROPE_DIM), "q_pe")
+    _need(block_table, torch.int32, (B, block_table.shape[1]), "block_table")
+    _need(seq_lens, torch.int32, (B,), "seq_lens")
+    _need(o_lat, torch.float32, (B, H, KV_LORA_RANK), "o_lat")
+    _need(w_uv, torch.bfloat16, (H, KV_LORA_RANK, V_DIM), "w_uv")
+    _need(o, torch.float32, (B, H, V_DIM), "o")
+    if lse is not None:
+        _need(lse, torch.float32, (B, H), "lse")
+    scale = DEFAULT_SOFTMAX_SCALE if softmax_scale is None else float(softmax_scale)
+    cs = cache.c_struct()
+    _check("mla_decode_absorbed_unabsorb", lib.mla_decode_absorbed_unabsorb(
+        ctypes.byref(cs), _ptr(q_lat), _ptr(q_pe), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H,
+        scale, int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o_lat),
+        _ptr(lse), _ptr(w_uv), _ptr(o), _ptr(dev_err), _stream(stream)))
 
 
 def mla_decode_absorbed_noalloc(cache, q_lat, q_pe, block_table, seq_lens, o_lat, lse=None, dev_err=None,

@@ -70,7 +70,7 @@ using namespace mla;
 
 extern "C" {
 
-int32_t mla_abi_version(void) { return 105; }
+int32_t mla_abi_version(void) { return 106; }
 
 const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
 
@@ -173,12 +173,13 @@ size_t mla_decode_workspace_bytes(int32_t batch, int32_t heads, int32_t num_spli
   return (size_t)workspace_bytes(batch, heads, decode_grid(num_splits, heads));
 }
 
-mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
+static mla_status decode_call(const mla_cache_layer* cache, const float* q_lat,
                                const uint16_t* q_pe, const int32_t* block_table,
                                int32_t max_pages, const int32_t* seq_lens, int32_t batch,
                                int32_t heads, float softmax_scale, int32_t num_splits,
                                void* workspace, size_t workspace_bytes_, float* o_lat,
-                               float* lse, int32_t* dev_err, mla_stream_t stream) {
+                               float* lse, const uint16_t* w_uv, float* o, int32_t* dev_err,
+                               mla_stream_t stream) {
   PageLayout L;
   OutlierSet outl;
   if (!cache_check(cache, &L, &outl)) return MLA_ERR_INVALID_ARG;
@@ -194,6 +195,8 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
       (dev_err && !aligned(dev_err, 4)))
     return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
+  if ((w_uv == nullptr) != (o == nullptr) || (w_uv && (!aligned(w_uv, 16) || !aligned(o, 16))))
+    return MLA_ERR_INVALID_ARG;
   int G = decode_grid(num_splits, heads);
   if ((int64_t)workspace_bytes_ < workspace_bytes(batch, heads, G)) return MLA_ERR_INVALID_ARG;
   DecodeParams p;
@@ -218,8 +221,32 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
   p.ws = carve_workspace(workspace, batch, heads, G);
   p.o_lat = o_lat;
   p.lse = lse;
+  p.w_uv = w_uv;
+  p.o = o;
   p.dev_err = dev_err;
   return launch_decode(p, (cudaStream_t)stream);
+}
+
+mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
+                               const uint16_t* q_pe, const int32_t* block_table,
+                               int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                               int32_t heads, float softmax_scale, int32_t num_splits,
+                               void* workspace, size_t workspace_bytes_, float* o_lat,
+                               float* lse, int32_t* dev_err, mla_stream_t stream) {
+  return decode_call(cache, q_lat, q_pe, block_table, max_pages, seq_lens, batch, heads, softmax_scale, num_splits,
+                     workspace, workspace_bytes_, o_lat, lse, nullptr, nullptr, dev_err, stream);
+}
+
+mla_status mla_decode_absorbed_unabsorb(const mla_cache_layer* cache, const float* q_lat,
+                                        const uint16_t* q_pe, const int32_t* block_table,
+                                        int32_t max_pages, const int32_t* seq_lens, int32_t batch,
+                                        int32_t heads, float softmax_scale, int32_t num_splits,
+                                        void* workspace, size_t workspace_bytes_, float* o_lat,
+                                        float* lse, const uint16_t* w_uv, float* o, int32_t* dev_err,
+                                        mla_stream_t stream) {
+  if (!w_uv || !o) return MLA_ERR_INVALID_ARG;
+  return decode_call(cache, q_lat, q_pe, block_table, max_pages, seq_lens, batch, heads, softmax_scale, num_splits,
+                     workspace, workspace_bytes_, o_lat, lse, w_uv, o, dev_err, stream);
 }
 
 }  // extern "C"

@@ -356,6 +356,44 @@ __device__ __forceinline__ void exact_rows(const DecodeParams& p, int b, int h0,
   }
 }
 
+// The output projection of rows b, h0 + j (bit j of `rows` set) that this
+// block has just written to o_lat: o[b][h][v] = sum_c o_lat[b][h][c]
+// W_UV[h][c][v] in fp32 (juejin tutorial "步骤2", V_i = C^KV W_i^upV, with
+// W_UV[h] = W_i^upV).  Thread (v pair, 32-channel part) sums its part for
+// two columns from bf16 pairs of W_UV (coalesced across the column pairs);
+// the 16 parts are added through shared memory.  sm: 8 KB.  Every thread
+// of the block takes part.
+__device__ __forceinline__ void unabsorb_rows(const DecodeParams& p, int b, int h0, uint32_t rows, float* sm) {
+  const int tid = threadIdx.x, vp = tid & 63, kp = tid >> 6;
+  float2* red2 = reinterpret_cast<float2*>(sm);              // [16 parts][64 column pairs]
+  for (int jh = 0; jh < kShortHeads; ++jh) {
+    if (!((rows >> jh) & 1u)) continue;
+    const int h = h0 + jh;
+    const float* ol = p.o_lat + ((size_t)b * p.H + h) * kDc + 32 * kp;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(p.w_uv + ((size_t)h * kDc + 32 * kp) * kDv) + vp;
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+    for (int c = 0; c < 32; ++c) {
+      const float x = ol[c];
+      const uint32_t wv = __ldg(w + c * (kDv / 2));
+      a0 = fmaf(x, bf16lo(wv), a0);
+      a1 = fmaf(x, bf16hi(wv), a1);
+    }
+    red2[kp * 64 + vp] = make_float2(a0, a1);
+    __syncthreads();
+    if (tid < 64) {
+      float2 sum = red2[tid];
+#pragma unroll
+      for (int k = 1; k < 16; ++k) {
+        sum.x += red2[k * 64 + tid].x;
+        sum.y += red2[k * 64 + tid].y;
+      }
+      *reinterpret_cast<float2*>(p.o + ((size_t)b * p.H + h) * kDv + 2 * tid) = sum;
+    }
+    __syncthreads();
+  }
+}
+
 // Merge of sequence b, head h in a 1024-thread block (combine_kernel's
 // grid): writes o_lat and lse and returns true, or returns false (in every
 // thread) when the row carries too much weight of fp16 P V products against
@@ -464,15 +502,29 @@ __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(DecodeParams p
   const int len = checked_len(p, b, tid == 0);
   if (cum[b] == cum[b + 1]) {
     if (tid < kDc / 4) reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.o && tid < kDv / 4) reinterpret_cast<float4*>(p.o + ((size_t)b * p.H + h) * kDv)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
     return;
   }
   // Rows recomputed exactly: the eight heads of a short sequence (by the
   // block of every eighth head), or this head when its merge asks for it
   // (computed with its seven neighbours, written alone).  One call site.
-  const bool done = len < kExactLen ? h % kShortHeads != 0 : merge_head<LF>(p, b, h, sw, red, parts);
-  if (done) return;
-  exact_rows<LF, KF>(p, b, h - h % kShortHeads, len, len < kExactLen ? 0xffu : 1u << (h % kShortHeads), short_smem);
+  // With the output projection requested, the block projects the rows it
+  // wrote.
+  const bool merged = len >= kExactLen && merge_head<LF>(p, b, h, sw, red, parts);
+  if (merged || (len < kExactLen && h % kShortHeads != 0)) {
+    if (merged && p.o) {
+      __syncthreads();                      // the row's o_lat stores, before every thread reads them
+      unabsorb_rows(p, b, h - h % kShortHeads, 1u << (h % kShortHeads), short_smem);
+    }
+    return;
+  }
+  const uint32_t rows = len < kExactLen ? 0xffu : 1u << (h % kShortHeads);
+  exact_rows<LF, KF>(p, b, h - h % kShortHeads, len, rows, short_smem);
+  if (p.o) {
+    __syncthreads();
+    unabsorb_rows(p, b, h - h % kShortHeads, rows, short_smem);
+  }
 }
 
 // The same merge in two other grids, for the shapes where one block per
@@ -648,8 +700,12 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
 
 namespace {
 
+// Launches the combine in the grid that suits the batch; *fused tells
+// whether that grid also ran the requested output projection (the per-head
+// grid does; the others leave it to out_unabsorb_kernel).
 template <int LF, int KF>
-mla_status launch_combine_t(const DecodeParams& p, cudaStream_t stream) {
+mla_status launch_combine_t(const DecodeParams& p, cudaStream_t stream, bool* fused) {
+  *fused = false;
   static int configured[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -677,13 +733,14 @@ mla_status launch_combine_t(const DecodeParams& p, cudaStream_t stream) {
   if (c > 1 && !kRiskFmt<LF>)
     return cuda_status(launch_pdl(combine_grouped_kernel<LF, KF>, dim3(p.B, p.H, c), dim3(kCombThreads),
                                   kShortSmemBytes, stream, p));
+  *fused = true;
   return cuda_status(
       launch_pdl(combine_kernel<LF, KF>, dim3(p.B, p.H), dim3(kCombThreads), kShortSmemBytes, stream, p));
 }
 
-mla_status launch_combine(const DecodeParams& p, cudaStream_t stream) {
+mla_status launch_combine(const DecodeParams& p, cudaStream_t stream, bool* fused) {
 #define MLA_COMBINE_CASE(A, K) \
-  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_combine_t<A, K>(p, stream);
+  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_combine_t<A, K>(p, stream, fused);
   MLA_COMBINE_CASE(MLA_FMT_BF16, MLA_FMT_BF16)
   MLA_COMBINE_CASE(MLA_FMT_BF16, MLA_FMT_INT8_SYM)
   MLA_COMBINE_CASE(MLA_FMT_INT8_SYM, MLA_FMT_BF16)
@@ -711,7 +768,10 @@ mla_status launch_combine(const DecodeParams& p, cudaStream_t stream) {
 mla_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
   const mla_status st = launch_decode_mma(p, stream);
   if (st != MLA_OK) return st;
-  return launch_combine(p, stream);
+  bool fused = false;
+  const mla_status sc = launch_combine(p, stream, &fused);
+  if (sc != MLA_OK || !p.o || fused) return sc;
+  return launch_out_unabsorb(p.o_lat, p.w_uv, p.o, p.B, p.H, stream);
 }
 
 }  // namespace mla

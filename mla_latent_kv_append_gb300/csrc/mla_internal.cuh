@@ -258,6 +258,8 @@ struct DecodeParams {
   Workspace ws;
   float* o_lat;
   float* lse;
+  const uint16_t* w_uv;   // with o: the output projection follows the merge (nullptr: not requested)
+  float* o;
   int32_t* dev_err;
 };
 mla_status launch_decode(const DecodeParams& p, cudaStream_t stream);

@@ -105,6 +105,8 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
     p.ws = carve_workspace(split_ws, s, heads, G);
     p.o_lat = o_lat + (size_t)i0 * heads * kDc;
     p.lse = lse ? lse + (size_t)i0 * heads : nullptr;
+    p.w_uv = nullptr;
+    p.o = nullptr;
     p.dev_err = dev_err;
     const mla_status ds = launch_decode(p, st);
     if (ds != MLA_OK) return ds;

@@ -168,8 +168,8 @@ class Workload:
 
 class DecodeStep:
     """Buffers and the per-layer call sequence of one decode step:
-    [prefill append ->] append -> absorb -> decode (+combine) -> unabsorb,
-    for every layer.  The appends and the absorb of a layer depend only on
+    [prefill append ->] append -> absorb -> decode (+ combine + unabsorb, one
+    call), for every layer.  The appends and the absorb of a layer depend only on
     the layer's inputs, so the appends run on a side stream beside the
     absorb and the decode waits for both."""
 
@@ -196,12 +196,12 @@ class DecodeStep:
                 mla.mla_cache_append(wl.caches[l], wl.c_new[l], wl.kpe_new[l], wl.slot_new, self.dev_err)
             mla.mla_q_absorb(wl.q_nope[l], wl.w_uk[l], self.q_lat)
             main.wait_stream(self.side)
-            mla.mla_decode_absorbed(wl.caches[l], self.q_lat, wl.q_pe[l], wl.block_table, wl.seq_lens_dev,
-                                    self.workspace, self.o_lat, None if self.lse is None else self.lse[l],
-                                    self.dev_err, num_splits=self.num_splits)
+            mla.mla_decode_absorbed_unabsorb(wl.caches[l], self.q_lat, wl.q_pe[l], wl.block_table, wl.seq_lens_dev,
+                                             self.workspace, self.o_lat, wl.w_uv[l], self.o[l],
+                                             lse=None if self.lse is None else self.lse[l], dev_err=self.dev_err,
+                                             num_splits=self.num_splits)
             if keep_o_lat is not None:
                 keep_o_lat[l].copy_(self.o_lat)
-            mla.mla_out_unabsorb(self.o_lat, wl.w_uv[l], self.o[l])
         return self.o
 
 

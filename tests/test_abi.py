@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
-    assert lib.abi_version() == 105
+    assert lib.abi_version() == 106
 
 
 def test_layouts_match_the_accounting(lib):
@@ -99,6 +99,12 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert raw.mla_decode_absorbed(*args(1 << 30, 0.0, 2)) == 1
     assert raw.mla_decode_absorbed(*args(1 << 30, 0.07, 5000)) == 1
     assert raw.mla_decode_absorbed(*args(1 << 30, 0.07, 0)) == 0
+    # the decode with the output projection: both of w_uv and o, 16-byte aligned
+    fused = lambda w, o: (ctypes.byref(cs), fake, fake, fake, 4, fake, 2, 16, 0.07, 3, ctypes.c_void_p(0x200000),
+                          1 << 30, fake, None, w, o, None, None)
+    assert raw.mla_decode_absorbed_unabsorb(*fused(None, fake)) == 1
+    assert raw.mla_decode_absorbed_unabsorb(*fused(fake, None)) == 1
+    assert raw.mla_decode_absorbed_unabsorb(*fused(ctypes.c_void_p(0x10008), fake)) == 1
     # decode: the batch's chunk capacity B * max_pages * 2 must stay below 2^31
     big = (ctypes.byref(cs), fake, fake, fake, 1 << 18, fake, 4096, 16, 0.07, 3, ctypes.c_void_p(0x200000), 1 << 40,
            fake, None, None, None)

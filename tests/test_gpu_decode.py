@@ -149,3 +149,29 @@ def test_poisoned_page_tails(lf, kf):
         c.pool.fill_(0xFF)
     wl.fill()
     run_and_check(wl)
+
+
+@pytest.mark.parametrize("lens,H", [([4096] * 8, 16), ([4096, 100, 0, 3000], 32), ([300] * 40, 16), ([70000], 16)],
+                         ids=["per-head-grid", "short-and-empty", "grouped-grid", "one-long"])
+def test_decode_with_unabsorb_matches_the_two_calls(lens, H):
+    """mla_decode_absorbed_unabsorb against mla_decode_absorbed followed by
+    mla_out_unabsorb: o_lat and lse bit for bit (the same kernels), o within
+    fp32 summation order, in each combine grid (the per-head grid projects
+    inside the combine, including rows of the exact path)."""
+    wl = Workload(1, H, lens, mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, seed=17)
+    step = DecodeStep(wl)
+    step.run()
+    torch.cuda.synchronize()
+    o_f, ol_f, lse_f = step.o[0].clone(), step.o_lat.clone(), step.lse[0].clone()
+    mla.mla_decode_absorbed(wl.caches[0], step.q_lat, wl.q_pe[0], wl.block_table, wl.seq_lens_dev, step.workspace,
+                            step.o_lat, step.lse[0], step.dev_err)
+    o_s = torch.empty_like(o_f)
+    mla.mla_out_unabsorb(step.o_lat, wl.w_uv[0], o_s)
+    torch.cuda.synchronize()
+    assert step.dev_err.item() == 0
+    assert torch.equal(ol_f, step.o_lat) and torch.equal(lse_f, step.lse[0])
+    scale = o_s.abs().amax(dim=-1, keepdim=True).clamp_min(1e-30)
+    assert float(((o_f - o_s).abs() / scale).max()) < 1e-5
+    for b, T in enumerate(lens):
+        if T == 0:
+            assert torch.all(o_f[b] == 0)
