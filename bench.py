@@ -585,7 +585,11 @@ def run_ours(args, cfg, rank, world, local_rank):
                      else "fallback 6.8 TB/s"},
         "e2e": {"value": tokens_per_step / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": args.steps * layers * (6 if wl.prefill else 5),
+        # per layer: append (and the prefill's append), absorb, then the
+        # decode call's kernels (the unabsorb is fused into the combine for
+        # some batch shapes)
+        "gpu_launches": args.steps * layers * ((3 if wl.prefill else 2) + mla.mla_decode_kernel_count(
+            wl.caches[0], wl.B, wl.H, args.num_splits, with_unabsorb=True)),
         "device_error_word": err_word,
         "clocks": clk,
         "prefill_append": pre,

@@ -323,6 +323,16 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
  * otherwise the call launches the unabsorb kernel after the combine.  The
  * two ways differ only in the order of the fp32 sums.
  */
+/*
+ * mla_decode_kernel_count - how many kernels one mla_decode_absorbed call
+ * (with_unabsorb = 0) or mla_decode_absorbed_unabsorb call (1) launches for
+ * this batch shape: the split kernel and the combine, plus the unabsorb
+ * kernel when the combine's grid does not project the rows itself.  0 for
+ * batch 0, -1 for arguments the calls would reject.  Host only.
+ */
+int32_t mla_decode_kernel_count(const mla_cache_layer* cache, int32_t batch, int32_t heads, int32_t num_splits,
+                                int32_t with_unabsorb);
+
 mla_status mla_decode_absorbed_unabsorb(const mla_cache_layer* cache, const float* q_lat,
                                         const uint16_t* q_pe, const int32_t* block_table,
                                         int32_t max_pages, const int32_t* seq_lens, int32_t batch,

@@ -86,6 +86,7 @@ def _load():
         "mla_decode_workspace_bytes": (SZ, [I32, I32, I32]),
         "mla_decode_absorbed": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, SZ, P, P, P, P]),
         "mla_decode_absorbed_unabsorb": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, SZ, P, P, P, P, P, P]),
+        "mla_decode_kernel_count": (I32, [CP, I32, I32, I32, I32]),
         "mla_out_unabsorb": (I32, [P, P, P, I32, I32, P]),
         "mla_decode_absorbed_noalloc": (I32, [CP, P, P, P, I32, P, I32, I32, F32, I32, P, P, P, P]),
         "mla_lse_merge": (I32, [P, P, I32, I32, I32, P, P, P]),
@@ -224,6 +225,11 @@ def mla_decode_absorbed(cache, q_lat, q_pe, block_table, seq_lens, workspace, o_
         ctypes.byref(cs), _ptr(q_lat), _ptr(q_pe), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, H,
         scale, int(num_splits), _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(o_lat),
         _ptr(lse), _ptr(dev_err), _stream(stream)))
+
+
+def mla_decode_kernel_count(cache, batch, heads, num_splits=0, with_unabsorb=False):
+    cs = cache.c_struct()
+    return int(lib.mla_decode_kernel_count(ctypes.byref(cs), batch, heads, num_splits, 1 if with_unabsorb else 0))
 
 
 def mla_decode_absorbed_unabsorb(cache, q_lat, q_pe, block_table, seq_lens, workspace, o_lat, w_uv, o, lse=None,

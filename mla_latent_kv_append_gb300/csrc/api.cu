@@ -237,6 +237,17 @@ mla_status mla_decode_absorbed(const mla_cache_layer* cache, const float* q_lat,
                      workspace, workspace_bytes_, o_lat, lse, nullptr, nullptr, dev_err, stream);
 }
 
+int32_t mla_decode_kernel_count(const mla_cache_layer* cache, int32_t batch, int32_t heads, int32_t num_splits,
+                                int32_t with_unabsorb) {
+  if (!cache || batch < 0 || batch > kMaxBatch || !heads_ok(heads) || num_splits < 0 || num_splits > kMaxSplits)
+    return -1;
+  PageLayout L;
+  if (!compute_layout(cache->latent_fmt, cache->kpe_fmt, &L)) return -1;
+  if (batch == 0) return 0;
+  const int fused = combine_grid(cache->latent_fmt, batch, decode_grid(num_splits, heads)) == 1;
+  return 2 + (with_unabsorb && !fused ? 1 : 0);
+}
+
 mla_status mla_decode_absorbed_unabsorb(const mla_cache_layer* cache, const float* q_lat,
                                         const uint16_t* q_pe, const int32_t* block_table,
                                         int32_t max_pages, const int32_t* seq_lens, int32_t batch,

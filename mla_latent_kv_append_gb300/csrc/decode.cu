@@ -698,6 +698,18 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
 
 }  // namespace
 
+// The combine's grid for B sequences over G splits (G / B: the average
+// number of partial slots per sequence): 0 = grouped (8 heads per block,
+// G < 8 B), 1 = one block per (sequence, head), C > 1 = each head's channels
+// sliced over C blocks (~19 slots or more per part; not for quantized
+// latents, whose rows may need the exact path, which a slice cannot decide).
+int combine_grid(int latent_fmt, int B, int G) {
+  if (G < 8 * B) return 0;
+  int c = 1;
+  while (c < 8 && (int64_t)2 * c * 16 * B <= G) c *= 2;
+  return latent_fmt == MLA_FMT_BF16 ? c : 1;
+}
+
 namespace {
 
 // Launches the combine in the grid that suits the batch; *fused tells
@@ -722,15 +734,11 @@ mla_status launch_combine_t(const DecodeParams& p, cudaStream_t stream, bool* fu
     if (st != MLA_OK) return st;
     if (dev >= 0 && dev < 64) configured_g[dev] = 1;
   }
-  // G / B: the average number of partial slots per sequence
-  if (p.G < 8 * p.B)
+  const int c = combine_grid(LF, p.B, p.G);
+  if (c == 0)
     return cuda_status(launch_pdl(combine_grouped_kernel<LF, KF>, dim3(p.B, p.H / kCombGroupHeads, 1),
                                   dim3(kCombThreads), kShortSmemBytes, stream, p));
-  int c = 1;                             // channel slices: ~19 slots or more per part
-  while (c < 8 && (int64_t)2 * c * 16 * p.B <= p.G) c *= 2;
-  // a slice sees only part of a row, so rows that may need the exact path
-  // (quantized latents) take the per-head grid
-  if (c > 1 && !kRiskFmt<LF>)
+  if (c > 1)
     return cuda_status(launch_pdl(combine_grouped_kernel<LF, KF>, dim3(p.B, p.H, c), dim3(kCombThreads),
                                   kShortSmemBytes, stream, p));
   *fused = true;

@@ -263,6 +263,7 @@ struct DecodeParams {
   int32_t* dev_err;
 };
 mla_status launch_decode(const DecodeParams& p, cudaStream_t stream);
+int combine_grid(int latent_fmt, int B, int G);   // decode.cu
 mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream);   // decode kernel only
 
 }  // namespace mla

@@ -43,7 +43,7 @@ Readings taken where the pages are open:
   codes are 0); k_pe stays bf16, as in the row "B: latent8+kpe16" it
   extends.  512 + 2 x 25 + 128 = 690 code bytes per layer reproduce all
   three printed figures, which 24 or 26 channels do not (INT8 k_pe would
-  need 57 protected channels, 11 %, for the same bytes; the round 5 % with
+  need 57 protected channels, 11 %, for the same bytes; a whole 5 % with
   row B's bf16 k_pe is the plainer reading).  The protected set comes from
   calibration: the K channels with the largest max |x| over a sample of
   rows (ties to the lower index).

@@ -181,3 +181,18 @@ def test_outlier_format_descriptor_rules(lib):
     assert call(1, None) == 0
     assert raw.mla_select_outlier_channels(fake, 0, fake, None) == 1
     assert raw.mla_select_outlier_channels(ctypes.c_void_p(0x10002), 4, fake, None) == 1
+
+
+def test_decode_kernel_count(lib):
+    """Kernels per decode call: split kernel + combine, plus the unabsorb
+    kernel unless the combine's per-head grid projects the rows itself."""
+    cnt = lambda lf, B, H, G, u: lib.lib.mla_decode_kernel_count(
+        ctypes.byref(lib._CacheLayer(4, lf, 1 if lf else 0, 0, 0x100000)), B, H, G, u)
+    assert cnt(1, 8, 16, 152, 0) == 2
+    assert cnt(1, 8, 16, 152, 1) == 2        # ~19 splits per sequence: per-head grid, fused
+    assert cnt(1, 32, 16, 152, 1) == 3       # grouped grid: separate unabsorb
+    assert cnt(0, 1, 16, 152, 1) == 3        # bf16, one long sequence: channel-sliced grid
+    assert cnt(1, 1, 16, 152, 1) == 2        # quantized: per-head grid (the exact path needs whole rows)
+    assert cnt(1, 0, 16, 152, 1) == 0
+    assert cnt(1, 8, 24, 152, 1) == -1
+    assert cnt(9, 8, 16, 152, 1) == -1
