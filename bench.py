@@ -39,6 +39,8 @@ CONFIGS = {
                              "INT8 latent (32 groups) + INT8 k_pe, 64-token pages"),
     "v2lite_int4_32k": dict(layers=27, heads=16, batch=32, ctx=32768, latent="int4", kpe="int8",
                             desc="V2-Lite shapes, batch 32, context 32768, asymmetric INT4 latent + INT8 k_pe"),
+    "v2lite_int8_32k": dict(layers=27, heads=16, batch=32, ctx=32768, latent="int8", kpe="int8",
+                            desc="V2-Lite shapes, batch 32, context 32768, INT8 latent (32 groups) + INT8 k_pe"),
     "v2lite_int4_kpe4_32k": dict(layers=27, heads=16, batch=32, ctx=32768, latent="int4", kpe="int4sym",
                                  desc="V2-Lite shapes, batch 32, context 32768, asymmetric INT4 latent + "
                                       "symmetric INT4 k_pe (the 7.6 KB-per-token scheme; 580 B per token-layer "

@@ -31,6 +31,7 @@ SAMPLED = (0, 13, 26)
 CASES = [
     ("v2lite_int8", None),
     ("v2lite_int4_32k", SAMPLED),
+    ("v2lite_int8_32k", (0, 26)),
     ("v2lite_int4_kpe4_32k", (0, 26)),
     ("v2lite_int8_per_token", (0, 13, 26)),
     ("v2lite_int8_64blocks", (0, 26)),
