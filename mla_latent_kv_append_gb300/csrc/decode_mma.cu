@@ -909,7 +909,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
     int b = -1, s = 0;
     bool dead = false;
     // Flush of sequence bb's partial: m, l and, with a quantized latent,
-    // e2 = sum_t (p_t M_t)^2 over the row (M_t the bounds warpgroup's bound
+    // e2 = sum_t (p_t M_t)^2 over the row (M_t the token's stored bound
     // on |c_hat_t|), the weight of the fp16 P V products.
     auto flush_ml = [&](int bb) {
       float e = e2;
