@@ -509,6 +509,25 @@ def run_ours(args, cfg, rank, world, local_rank):
             b.record(stream)
         torch.cuda.synchronize()
         attn_ms = a.elapsed_time(b) / preps
+        path = mla.mla_prefill_path_taken(0, wl.prefill, wl.H)
+        # the other implementation of the same call, for comparison
+        other = mla.PREFILL_DECODE_KERNELS if path == mla.PREFILL_TENSOR_CORES else mla.PREFILL_TENSOR_CORES
+        prev_path = mla.mla_set_prefill_path(other)
+        ows = torch.empty(mla.mla_prefill_workspace_bytes(wl.prefill, wl.H), dtype=torch.uint8, device="cuda")
+        ograph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ograph, stream=stream):
+            mla.mla_prefill_absorbed(wl.caches[0], pstep.q_lat, wl.q_pe_pre[0], wl.prefill_block_table, 0,
+                                     ows, pstep.o_lat, pstep.lse[0], pstep.dev_err)
+        mla.mla_set_prefill_path(prev_path)
+        with torch.cuda.stream(stream):
+            ograph.replay()
+            a.record(stream)
+            for _ in range(preps):
+                ograph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        other_ms = a.elapsed_time(b) / preps
+        del ograph, ows
         flops = prefill_flops(wl.prefill, wl.H)
         tpk, tpk_kind = tensor_peak()
         achieved_t = flops / (attn_ms * 1e-3) / 1e12
@@ -516,7 +535,10 @@ def run_ours(args, cfg, rank, world, local_rank):
                  "launch_ms": attn_ms, "achieved": achieved_t, "peak": tpk, "unit": "TFLOP/s",
                  "frac": achieved_t / tpk, "peak_source": "%s bf16_tflops (MEASURED_PEAKS.json)" % tpk_kind,
                  "ms_with_absorb_unabsorb": full_ms, "device_error_word": int(pstep.dev_err.item()),
-                 "kernel": "mla_prefill_absorbed (split-K decode kernels over the causal prefixes + combine)"}
+                 "kernel": ("mla_prefill_absorbed (tcgen05 tensor-core path: key tiles, query split, "
+                            "128x128 tiles, exact fixup)" if path == mla.PREFILL_TENSOR_CORES else
+                            "mla_prefill_absorbed (split-K decode kernels over the causal prefixes + combine)"),
+                 ("decode_kernels_ms" if other == mla.PREFILL_DECODE_KERNELS else "tensor_cores_ms"): other_ms}
         del pstep, fgraph, agraph
         torch.cuda.empty_cache()
 

@@ -372,10 +372,42 @@ mla_status mla_decode_absorbed_noalloc(const mla_cache_layer* cache, const float
 
 /*
  * mla_prefill_workspace_bytes - bytes of device workspace mla_prefill_absorbed
- * needs for a chunk of n query tokens and this head count (0 for invalid
- * arguments).  Bounded in n: queries are processed in slices of 2048.
+ * needs for a chunk of n query tokens and this head count under the current
+ * prefill path setting (0 for invalid arguments).  Bounded in n: queries are
+ * processed in slices of 2048 (decode kernels) or 1024 (tensor cores); the
+ * tensor-core path adds the key tiles of up to 16384 positions (~38 MB).
  */
 size_t mla_prefill_workspace_bytes(int32_t n, int32_t heads);
+
+/*
+ * Prefill implementations (mla_set_prefill_path):
+ *   MLA_PREFILL_AUTO           tensor cores when n * heads >= 8192 and
+ *                              256 < ctx_before + n <= 16384, else the
+ *                              decode kernels (the default)
+ *   MLA_PREFILL_DECODE_KERNELS always the split-K decode kernels
+ *   MLA_PREFILL_TENSOR_CORES   always tensor cores; a call with
+ *                              ctx_before + n > 16384 returns
+ *                              MLA_ERR_UNSUPPORTED
+ * Both compute the same attention within the same bound (§ prefill below).
+ */
+#define MLA_PREFILL_AUTO 0
+#define MLA_PREFILL_DECODE_KERNELS 1
+#define MLA_PREFILL_TENSOR_CORES 2
+
+/*
+ * mla_set_prefill_path - selects the implementation of the prefill calls this
+ * process makes afterwards (and the size mla_prefill_workspace_bytes
+ * returns); returns the previous setting, or -1 (nothing changed) for an
+ * unknown value.
+ */
+int32_t mla_set_prefill_path(int32_t path);
+
+/*
+ * mla_prefill_path_taken - the implementation (MLA_PREFILL_DECODE_KERNELS or
+ * MLA_PREFILL_TENSOR_CORES) a prefill call with these sizes takes under the
+ * current setting; -1 for invalid sizes.
+ */
+int32_t mla_prefill_path_taken(int32_t ctx_before, int32_t n, int32_t heads);
 
 /*
  * mla_prefill_absorbed - causal absorbed attention of a prefill chunk: the
@@ -383,8 +415,13 @@ size_t mla_prefill_workspace_bytes(int32_t n, int32_t heads);
  * (chunked prefill when ctx_before > 0).  Query i sits at position
  * ctx_before + i and attends to the cached positions 0 .. ctx_before + i,
  * its own token included; per query this is the decode of [EN] §2.1 over
- * that prefix, computed by the same split-K kernels with the queries as the
- * batch.
+ * that prefix.  Tensor-core path: the cached tokens are dequantized once
+ * into fp16 (hi, lo) key tiles and a tcgen05 kernel runs 128 query rows
+ * against 128 keys at a time (scores from three fp16 products, P and V in
+ * fp16, fp32 accumulation); decode-kernel path: the split-K decode kernels
+ * with the queries as the batch.  On both, rows that see fewer than 256
+ * tokens, and rows whose softmax weight sits on tokens whose latents cancel
+ * (the decode's precision check), are recomputed exactly in fp32.
  *   q_lat       fp32 [n][H][512]  (mla_q_absorb with batch = n)
  *   q_pe        bf16 [n][H][64]
  *   block_table int32 [max_pages]: the sequence's page ids; positions up to

@@ -23,7 +23,9 @@ calibration), ``mla_cache_page_layout``,
 ``mla_decode_absorbed_unabsorb`` (the decode and the output projection in
 one call), ``mla_decode_absorbed_noalloc`` (the decode for callers that cannot allocate),
 ``mla_prefill_absorbed`` / ``mla_prefill_workspace_bytes`` (causal attention
-of a prefill chunk) and ``mla_lse_merge`` (merges per-part results of a context-sharded decode;
+of a prefill chunk; ``mla_set_prefill_path`` / ``mla_prefill_path_taken``
+choose and report its implementation: tcgen05 tensor cores or the decode
+kernels) and ``mla_lse_merge`` (merges per-part results of a context-sharded decode;
 the host side of that exchange is in ``sharded``).
 """
 
@@ -39,6 +41,10 @@ LIB_PATH = os.path.join(_HERE, "libmla_gb300.so")
 FMT_BF16, FMT_INT8_SYM, FMT_INT4_ASYM, FMT_INT4_SYM = 0, 1, 2, 3
 FMT_INT8_G8, FMT_INT8_G32, FMT_INT8_G64, FMT_INT8_TOKEN = 4, 5, 6, 7    # INT8 latent, other block counts
 FMT_INT8_OUTLIER = 8        # INT8 latent with OUTLIER_CHANNELS protected bf16 channels
+
+PREFILL_AUTO = 0            # mla_set_prefill_path: tensor cores for large chunks, else decode kernels
+PREFILL_DECODE_KERNELS = 1
+PREFILL_TENSOR_CORES = 2
 OUTLIER_CHANNELS = 25
 DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT = 1, 2, 4, 8
 KV_LORA_RANK, ROPE_DIM, QK_NOPE_DIM, V_DIM, PAGE_TOKENS = 512, 64, 128, 128, 64
@@ -93,6 +99,8 @@ def _load():
         "mla_prefill_workspace_bytes": (SZ, [I32, I32]),
         "mla_prefill_absorbed": (I32, [CP, P, P, P, I32, I32, I32, I32, F32, P, SZ, P, P, P, P]),
         "mla_set_wait_limit_ns": (ctypes.c_int64, [ctypes.c_int64]),
+        "mla_set_prefill_path": (I32, [I32]),
+        "mla_prefill_path_taken": (I32, [I32, I32, I32]),
         "mla_select_outlier_channels": (I32, [P, I32, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -309,6 +317,21 @@ def mla_lse_merge(o_parts, lse_parts, o_lat, lse=None, stream=None):
         _need(lse, torch.float32, (B, H), "lse")
     _check("mla_lse_merge", lib.mla_lse_merge(_ptr(o_parts), _ptr(lse_parts), R, B, H, _ptr(o_lat), _ptr(lse),
                                               _stream(stream)))
+
+
+def mla_set_prefill_path(path):
+    """Select the prefill implementation for later calls (PREFILL_AUTO,
+    PREFILL_DECODE_KERNELS or PREFILL_TENSOR_CORES); returns the previous one."""
+    prev = int(lib.mla_set_prefill_path(int(path)))
+    if prev < 0:
+        raise ValueError("unknown prefill path %r" % (path,))
+    return prev
+
+
+def mla_prefill_path_taken(ctx_before, n, heads):
+    """PREFILL_DECODE_KERNELS or PREFILL_TENSOR_CORES: the implementation a
+    prefill call with these sizes takes under the current setting."""
+    return int(lib.mla_prefill_path_taken(int(ctx_before), int(n), int(heads)))
 
 
 def mla_set_wait_limit_ns(ns):

@@ -70,7 +70,7 @@ using namespace mla;
 
 extern "C" {
 
-int32_t mla_abi_version(void) { return 106; }
+int32_t mla_abi_version(void) { return 107; }
 
 const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
 

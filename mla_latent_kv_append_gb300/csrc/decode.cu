@@ -22,6 +22,7 @@
 //
 // This translation unit holds the combine kernels with the exact
 // short-sequence path (fp32 CUDA cores, dequantized block in shared memory).
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "mla_internal.cuh"
@@ -696,6 +697,102 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
   exact_rows<LF, KF>(p, b, h0, len, 0xffu, short_smem);
 }
 
+// ---------------------------------------------------------------------------
+// Support kernels of the tensor-core prefill (prefill_tc.cu).
+//
+// prefill_keys_kernel: grid (ceil(len / 128) * 4), block kKeyThreads.  Block
+// x dequantizes tokens 32x .. 32x + 31 of the sequence (block-table row 0)
+// as the oracle defines x_hat and writes each value as an fp16 pair
+// (hi = rn(x), lo = rn(x - hi)) into the key tiles the tensor-core kernel
+// copies from: tile kt = token / 128 holds, per 64-channel block kb (0..8:
+// latent channels 64kb.., k_pe channels for kb = 8), a 128-token x 64-channel
+// hi block and then the lo block, 16 KB each, rows 128 B with the 16-byte
+// chunks of row r permuted by XOR with r mod 8 (the tensor core's 128-byte
+// swizzle).  Tokens at or past len, or on a page outside the pool, are 0.
+// mt[token] = the stored bound on |x_hat| (0 for bf16 latents, which keep no
+// bound: their fp16 rounding is exact).
+constexpr int kKeyThreads = 256;
+constexpr int kKeySmemBytes = (int)sizeof(float) * (kChunk * kCS + kChunk * kKS) + (int)sizeof(int32_t) * 2 * kChunk;
+constexpr int kTcBlockBytes = 16384;
+
+template <int LF, int KF>
+__global__ void __launch_bounds__(kKeyThreads) prefill_keys_kernel(const DecodeParams p, int len, uint8_t* kws,
+                                                                   float* mt) {
+  extern __shared__ float key_smem[];
+  float* s_c = key_smem;
+  float* s_k = s_c + kChunk * kCS;
+  int32_t* s_valid = reinterpret_cast<int32_t*>(s_k + kChunk * kKS);
+  int32_t* s_page = s_valid + kChunk;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int t0 = blockIdx.x * kChunk;
+  dequant_chunk<LF, KF, kKeyThreads>(p, 0, t0, len, s_c, s_k, s_valid, s_page);
+  __syncthreads();
+  const int tid = threadIdx.x;
+  if (tid < kChunk) {
+    float bound = 0.f;
+    if (LF != MLA_FMT_BF16 && s_valid[tid]) {
+      const uint8_t* blk = p.pool + s_page[tid] * p.L.page_bytes + (int64_t)((t0 >> 5) & 1) * p.L.block_bytes;
+      bound = reinterpret_cast<const float*>(blk + p.L.bound_off)[tid];
+    }
+    mt[t0 + tid] = bound;
+  }
+  constexpr int kPieces = (kDc + kDr) / 8;         // 16-byte pieces of 8 channels per token
+  for (int i = tid; i < kChunk * kPieces; i += kKeyThreads) {
+    const int t = i / kPieces, c8 = i % kPieces;
+    const float* src = c8 < kDc / 8 ? s_c + t * kCS + 8 * c8 : s_k + t * kKS + 8 * c8 - kDc;
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 h = __floats2half2_rn(src[2 * k], src[2 * k + 1]);
+      const float2 hf = __half22float2(h);
+      const __half2 r = __floats2half2_rn(src[2 * k] - hf.x, src[2 * k + 1] - hf.y);
+      hi[k] = *reinterpret_cast<const uint32_t*>(&h);
+      lo[k] = *reinterpret_cast<const uint32_t*>(&r);
+    }
+    const int tok = t0 + t, row = tok & 127, kb = c8 >> 3;
+    uint8_t* dst = kws + ((int64_t)(tok >> 7) * 9 + kb) * 2 * kTcBlockBytes + row * 128 + (((c8 & 7) ^ (row & 7)) << 4);
+    *reinterpret_cast<uint4*>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(dst + kTcBlockBytes) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+// exact_fixup_kernel: grid (B, H / 8), block kCombThreads.  After the
+// tensor-core prefill of B query rows (batch row b = query token, length
+// p.seq_lens[b]), recomputes exactly in fp32 the heads h0 .. h0 + 7 of row b
+// that need it: all of them when the row sees fewer than kExactLen tokens,
+// else (quantized latents) those whose recorded check fails,
+// risk[r] > kRiskRatio * max(omax[2r], omax[2r + 1]) with r = b H + h, the
+// same criterion as the decode's combine (risk = sqrt(sum_t (w_t M_t)^2),
+// omax = |o_lat|_inf of each 256-channel half).
+template <int LF, int KF>
+__global__ void __launch_bounds__(kCombThreads, 1) exact_fixup_kernel(const DecodeParams p, const float* risk,
+                                                                      const float* omax) {
+  extern __shared__ float short_smem[];
+  __shared__ uint32_t s_rows;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int b = blockIdx.x, h0 = blockIdx.y * kShortHeads;
+  const int len = checked_len(p, b, false);
+  if (threadIdx.x < 32) {
+    bool need = false;
+    if (threadIdx.x < kShortHeads) {
+      if (len < kExactLen) {
+        need = true;
+      } else if (kRiskFmt<LF>) {
+        const size_t r = (size_t)b * p.H + h0 + threadIdx.x;
+        need = risk[r] > kRiskRatio * fmaxf(omax[2 * r], omax[2 * r + 1]);
+      }
+    }
+    const uint32_t bits = __ballot_sync(0xffffffffu, need);
+    if (threadIdx.x == 0) s_rows = bits;
+  }
+  __syncthreads();
+  const uint32_t rows = s_rows;
+  if (rows == 0 || len == 0) return;
+  exact_rows<LF, KF>(p, b, h0, len, rows, short_smem);
+}
+
 }  // namespace
 
 // The combine's grid for B sequences over G splits (G / B: the average
@@ -781,5 +878,67 @@ mla_status launch_decode(const DecodeParams& p, cudaStream_t stream) {
   if (sc != MLA_OK || !p.o || fused) return sc;
   return launch_out_unabsorb(p.o_lat, p.w_uv, p.o, p.B, p.H, stream);
 }
+
+namespace {
+
+// Raises a kernel's dynamic shared-memory limit once per device.
+template <typename K>
+mla_status allow_smem(K kernel, int bytes, int* configured) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && configured[dev]) return MLA_OK;
+  const mla_status st = cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  if (st == MLA_OK && dev >= 0 && dev < 64) configured[dev] = 1;
+  return st;
+}
+
+template <int LF, int KF>
+mla_status launch_prefill_keys_t(const DecodeParams& p, int len, void* kws, float* mt, cudaStream_t stream) {
+  static int configured[64] = {0};
+  const mla_status st = allow_smem(prefill_keys_kernel<LF, KF>, kKeySmemBytes, configured);
+  if (st != MLA_OK) return st;
+  const int blocks = (len + 127) / 128 * 4;
+  return cuda_status(launch_pdl(prefill_keys_kernel<LF, KF>, dim3(blocks), dim3(kKeyThreads), kKeySmemBytes, stream,
+                                p, len, (uint8_t*)kws, mt));
+}
+
+template <int LF, int KF>
+mla_status launch_exact_fixup_t(const DecodeParams& p, const float* risk, const float* omax, cudaStream_t stream) {
+  static int configured[64] = {0};
+  const mla_status st = allow_smem(exact_fixup_kernel<LF, KF>, kShortSmemBytes, configured);
+  if (st != MLA_OK) return st;
+  return cuda_status(launch_pdl(exact_fixup_kernel<LF, KF>, dim3(p.B, p.H / kShortHeads), dim3(kCombThreads),
+                                kShortSmemBytes, stream, p, risk, omax));
+}
+
+}  // namespace
+
+#define MLA_FORMAT_PAIRS(X)                                                                                \
+  X(MLA_FMT_BF16, MLA_FMT_BF16) X(MLA_FMT_BF16, MLA_FMT_INT8_SYM) X(MLA_FMT_INT8_SYM, MLA_FMT_BF16)         \
+  X(MLA_FMT_INT8_SYM, MLA_FMT_INT8_SYM) X(MLA_FMT_INT4_ASYM, MLA_FMT_BF16)                                 \
+  X(MLA_FMT_INT4_ASYM, MLA_FMT_INT8_SYM) X(MLA_FMT_INT4_SYM, MLA_FMT_BF16)                                 \
+  X(MLA_FMT_INT4_SYM, MLA_FMT_INT8_SYM) X(MLA_FMT_BF16, MLA_FMT_INT4_SYM)                                  \
+  X(MLA_FMT_INT8_SYM, MLA_FMT_INT4_SYM) X(MLA_FMT_INT4_ASYM, MLA_FMT_INT4_SYM)                             \
+  X(MLA_FMT_INT4_SYM, MLA_FMT_INT4_SYM) X(MLA_FMT_INT8_G8, MLA_FMT_INT8_SYM)                               \
+  X(MLA_FMT_INT8_G32, MLA_FMT_INT8_SYM) X(MLA_FMT_INT8_G64, MLA_FMT_INT8_SYM)                              \
+  X(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM) X(MLA_FMT_INT8_OUTLIER, MLA_FMT_BF16)                            \
+  X(MLA_FMT_INT8_OUTLIER, MLA_FMT_INT8_SYM)
+
+mla_status launch_prefill_keys(const DecodeParams& p, int len, void* kws, float* mt, cudaStream_t stream) {
+#define MLA_KEYS_CASE(A, K) \
+  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_prefill_keys_t<A, K>(p, len, kws, mt, stream);
+  MLA_FORMAT_PAIRS(MLA_KEYS_CASE)
+#undef MLA_KEYS_CASE
+  return MLA_ERR_UNSUPPORTED;
+}
+
+mla_status launch_exact_fixup(const DecodeParams& p, const float* risk, const float* omax, cudaStream_t stream) {
+#define MLA_FIXUP_CASE(A, K) \
+  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_exact_fixup_t<A, K>(p, risk, omax, stream);
+  MLA_FORMAT_PAIRS(MLA_FIXUP_CASE)
+#undef MLA_FIXUP_CASE
+  return MLA_ERR_UNSUPPORTED;
+}
+#undef MLA_FORMAT_PAIRS
 
 }  // namespace mla

@@ -266,4 +266,35 @@ mla_status launch_decode(const DecodeParams& p, cudaStream_t stream);
 int combine_grid(int latent_fmt, int B, int G);   // decode.cu
 mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream);   // decode kernel only
 
+// Tensor-core prefill support (decode.cu): the key tiles of tokens 0 .. len - 1
+// of block-table row 0 (fp16 hi / lo pairs, 128 tokens x 9 channel blocks x
+// 2 x 16 KB per tile, swizzled) with the tokens' bounds mt[len rounded up to
+// 128]; and the exact fp32 recomputation of the rows that need it.
+mla_status launch_prefill_keys(const DecodeParams& p, int len, void* kws, float* mt, cudaStream_t stream);
+mla_status launch_exact_fixup(const DecodeParams& p, const float* risk, const float* omax, cudaStream_t stream);
+
+// Tensor-core prefill (prefill_tc.cu).  A tile holds 128 rows (queries or
+// keys) x 9 channel blocks x (hi, lo) x 16 KB.
+constexpr int kTcTileBytes = 9 * 2 * 16384;
+struct TcParams {
+  const uint8_t* qws;     // [row tile][kb][hi, lo][16 KB]
+  const uint8_t* kws;     // [key tile][kb][hi, lo][16 KB]
+  const float* mt;        // [key tiles * 128] bound on |x_hat| per token
+  int R;                  // query rows of the slice (token-major: r = i H + h)
+  int H;
+  int qpos0;              // position of the slice's first query token
+  int n_rt;               // row tiles, ceil(R / 128)
+  float scale_log2;
+  int risk;               // record the precision check (quantized latents)
+  float* o_lat;           // [R][512]
+  float* lse;             // [R] or nullptr
+  float* risk_out;        // [R]: sqrt(sum_t (w_t M_t)^2)
+  float* omax;            // [R][2]: |o_lat|_inf of each 256-channel half
+  int32_t* dev_err;
+  uint64_t wait_ns;
+};
+mla_status launch_q_split(const float* q_lat, const uint16_t* q_pe, int R, int n_rt, uint8_t* qws,
+                          cudaStream_t stream);
+mla_status launch_prefill_tc(const TcParams& p, cudaStream_t stream);
+
 }  // namespace mla

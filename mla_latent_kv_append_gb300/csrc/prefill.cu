@@ -5,14 +5,25 @@
 // tokens, appended before the call, included).  In absorbed form each query
 // row is exactly a decode query over a prefix of one sequence ("Absorbed MLA
 // Cache Optimization on DeepSeek-V2-Lite — Technical Report" §2.1: attention
-// straight from the cached latent), so the chunk runs through the decode
-// kernels: the queries become the batch, every batch row shares the
-// sequence's block-table row (row stride 0), and row i's length is
-// ctx_before + i + 1.  The split-K partition then balances the triangle of
-// (query, key) pairs over the SMs by 32-token chunks, and the log-sum-exp
-// combine writes normalised rows.  Queries go in slices of kSlice so the
-// split-K workspace stays bounded for long chunks.
+// straight from the cached latent).  Two implementations:
+//
+//  * tensor cores (prefill_tc.cu): every cached token dequantized once into
+//    fp16 (hi, lo) key tiles, the queries split the same way, and a tcgen05
+//    kernel over 128-row x 128-key tiles; rows that see fewer than 256
+//    tokens, or fail the precision check, are recomputed exactly afterwards.
+//    Used when the chunk has enough rows to fill the GPU and the prefix fits
+//    the key tiles (kTcMaxKeys tokens).
+//  * the decode kernels: the queries become the batch, every batch row
+//    shares the sequence's block-table row (row stride 0), and row i's
+//    length is ctx_before + i + 1.  The split-K partition then balances the
+//    triangle of (query, key) pairs over the SMs by 32-token chunks, and the
+//    log-sum-exp combine writes normalised rows.
+//
+// Queries go in slices (kSlice / kTcSlice tokens) so the workspace stays
+// bounded for long chunks.
 #include <math.h>
+
+#include <atomic>
 
 #include "mla_internal.cuh"
 
@@ -35,6 +46,65 @@ int prefill_grid() {
 
 bool aligned_to(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
+// ---- tensor-core path
+constexpr int kTcSlice = 1024;           // query tokens per launch
+constexpr int kTcMaxKeys = 16384;        // positions the key tiles hold
+constexpr int64_t kTcMinRows = 8192;     // automatic choice: rows (n x H) that fill the GPU
+constexpr int kTcExactLen = 256;         // rows below this length are recomputed exactly anyway
+
+std::atomic<int> g_prefill_path{MLA_PREFILL_AUTO};
+
+struct TcWorkspace {
+  uint8_t* kws;
+  uint8_t* qws;
+  float* mt;
+  int32_t* lens;
+  float* risk;
+  float* omax;
+};
+
+int64_t tc_row_tiles(int64_t rows) { return (rows + 127) / 128; }
+
+int64_t tc_workspace_bytes(int n, int heads, TcWorkspace* w, void* base) {
+  const int64_t s = n < kTcSlice ? (n > 0 ? n : 1) : kTcSlice;
+  const int64_t rows = s * heads;
+  const int64_t sizes[6] = {(int64_t)(kTcMaxKeys / 128) * kTcTileBytes, tc_row_tiles(rows) * kTcTileBytes,
+                            align256((int64_t)kTcMaxKeys * 4), align256(s * 4), align256(rows * 4),
+                            align256(rows * 8)};
+  int64_t off = 0;
+  char* b = (char*)base;
+  void* ptrs[6];
+  for (int i = 0; i < 6; ++i) {
+    ptrs[i] = b ? b + off : nullptr;
+    off += sizes[i];
+  }
+  if (w) {
+    w->kws = (uint8_t*)ptrs[0];
+    w->qws = (uint8_t*)ptrs[1];
+    w->mt = (float*)ptrs[2];
+    w->lens = (int32_t*)ptrs[3];
+    w->risk = (float*)ptrs[4];
+    w->omax = (float*)ptrs[5];
+  }
+  return off;
+}
+
+int64_t decode_path_bytes(int n, int heads) {
+  const int s = n < kSlice ? (n > 0 ? n : 1) : kSlice;
+  return lengths_bytes() + workspace_bytes(s, heads, prefill_grid());
+}
+
+// The path a call takes: 1 = decode kernels, 2 = tensor cores.  ctx_before
+// < 0: the choice made without knowing it (the workspace size).
+int choose_path(int ctx_before, int n, int heads) {
+  const int forced = g_prefill_path.load(std::memory_order_relaxed);
+  if (forced != MLA_PREFILL_AUTO) return forced;
+  if ((int64_t)n * heads < kTcMinRows) return MLA_PREFILL_DECODE_KERNELS;
+  if (ctx_before < 0) return MLA_PREFILL_TENSOR_CORES;
+  const int64_t keys = (int64_t)ctx_before + n;
+  return keys <= kTcMaxKeys && keys > kTcExactLen ? MLA_PREFILL_TENSOR_CORES : MLA_PREFILL_DECODE_KERNELS;
+}
+
 }  // namespace
 }  // namespace mla
 
@@ -44,8 +114,20 @@ extern "C" {
 
 size_t mla_prefill_workspace_bytes(int32_t n, int32_t heads) {
   if (n < 0 || heads < 16 || heads > 128 || heads % 16) return 0;
-  const int s = n < kSlice ? (n > 0 ? n : 1) : kSlice;
-  return (size_t)(lengths_bytes() + workspace_bytes(s, heads, prefill_grid()));
+  const int64_t dec = decode_path_bytes(n, heads);
+  if (choose_path(-1, n, heads) != MLA_PREFILL_TENSOR_CORES) return (size_t)dec;
+  const int64_t tc = tc_workspace_bytes(n, heads, nullptr, nullptr);
+  return (size_t)(tc > dec ? tc : dec);
+}
+
+int32_t mla_prefill_path_taken(int32_t ctx_before, int32_t n, int32_t heads) {
+  if (n < 0 || ctx_before < 0 || heads < 16 || heads > 128 || heads % 16) return -1;
+  return choose_path(ctx_before, n, heads);
+}
+
+int32_t mla_set_prefill_path(int32_t path) {
+  if (path != MLA_PREFILL_AUTO && path != MLA_PREFILL_DECODE_KERNELS && path != MLA_PREFILL_TENSOR_CORES) return -1;
+  return g_prefill_path.exchange(path);
 }
 
 mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat, const uint16_t* q_pe,
@@ -59,18 +141,90 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
   if (n == 0) return MLA_OK;
   if (max_pages <= 0 || (int64_t)max_pages * kPage > (int64_t)INT32_MAX) return MLA_ERR_INVALID_ARG;
   if ((int64_t)ctx_before + n > (int64_t)max_pages * kPage) return MLA_ERR_INVALID_ARG;
-  // every 32-token chunk of a slice gets a 32-bit index
-  if ((int64_t)(n < kSlice ? n : kSlice) * max_pages * (kPage / kChunk) > (int64_t)INT32_MAX)
-    return MLA_ERR_INVALID_ARG;
   if (!q_lat || !q_pe || !block_table || !workspace || !o_lat) return MLA_ERR_INVALID_ARG;
   if (!aligned_to(q_lat, 16) || !aligned_to(q_pe, 16) || !aligned_to(block_table, 4) ||
       !aligned_to(workspace, 256) || !aligned_to(o_lat, 16) || (lse && !aligned_to(lse, 4)) ||
       (dev_err && !aligned_to(dev_err, 4)))
     return MLA_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return MLA_ERR_INVALID_ARG;
-  if (workspace_bytes_ < mla_prefill_workspace_bytes(n, heads)) return MLA_ERR_INVALID_ARG;
-
+  const int path = choose_path(ctx_before, n, heads);
   const cudaStream_t st = (cudaStream_t)stream;
+  if (path == MLA_PREFILL_TENSOR_CORES) {
+    if ((int64_t)ctx_before + n > kTcMaxKeys) return MLA_ERR_UNSUPPORTED;
+    TcWorkspace w;
+    if ((int64_t)workspace_bytes_ < tc_workspace_bytes(n, heads, &w, workspace)) return MLA_ERR_INVALID_ARG;
+    DecodeParams p;
+    p.pool = (const uint8_t*)cache->pool;
+    p.L = L;
+    p.latent_fmt = cache->latent_fmt;
+    p.kpe_fmt = cache->kpe_fmt;
+    p.num_pages = cache->num_pages;
+    p.block_table = block_table;
+    p.max_pages = max_pages;
+    p.bt_stride = 0;
+    p.seq_lens = w.lens;
+    p.lens_after_wait = 1;
+    p.H = heads;
+    p.G = 0;
+    p.scale_log2 = softmax_scale * 1.4426950408889634f;
+    p.outl = outl;
+    p.wait_ns = wait_limit_ns();
+    p.ws = Workspace{};
+    p.w_uv = nullptr;
+    p.o = nullptr;
+    p.dev_err = dev_err;
+    const int keys = ctx_before + n;
+    mla_status ks = launch_prefill_keys(p, keys, w.kws, w.mt, st);
+    if (ks != MLA_OK) return ks;
+    for (int i0 = 0; i0 < n; i0 += kTcSlice) {
+      const int s = n - i0 < kTcSlice ? n - i0 : kTcSlice;
+      const int R = s * heads;
+      const int n_rt = (int)tc_row_tiles(R);
+      // the fixup's per-row lengths; a plain launch, after the previous
+      // slice's fixup has finished with them
+      causal_lengths_kernel<<<(s + 255) / 256, 256, 0, st>>>(w.lens, s, ctx_before + i0);
+      const mla_status ls = launch_status();
+      if (ls != MLA_OK) return ls;
+      const float* ql = q_lat + (size_t)i0 * heads * kDc;
+      const uint16_t* qp = q_pe + (size_t)i0 * heads * kDr;
+      float* ol = o_lat + (size_t)i0 * heads * kDc;
+      float* lo = lse ? lse + (size_t)i0 * heads : nullptr;
+      ks = launch_q_split(ql, qp, R, n_rt, w.qws, st);
+      if (ks != MLA_OK) return ks;
+      TcParams t;
+      t.qws = w.qws;
+      t.kws = w.kws;
+      t.mt = w.mt;
+      t.R = R;
+      t.H = heads;
+      t.qpos0 = ctx_before + i0;
+      t.n_rt = n_rt;
+      t.scale_log2 = p.scale_log2;
+      t.risk = cache->latent_fmt != MLA_FMT_BF16;
+      t.o_lat = ol;
+      t.lse = lo;
+      t.risk_out = w.risk;
+      t.omax = w.omax;
+      t.dev_err = dev_err;
+      t.wait_ns = p.wait_ns;
+      ks = launch_prefill_tc(t, st);
+      if (ks != MLA_OK) return ks;
+      DecodeParams f = p;
+      f.q_lat = ql;
+      f.q_pe = qp;
+      f.B = s;
+      f.o_lat = ol;
+      f.lse = lo;
+      ks = launch_exact_fixup(f, w.risk, w.omax, st);
+      if (ks != MLA_OK) return ks;
+    }
+    return MLA_OK;
+  }
+  // every 32-token chunk of a slice gets a 32-bit index
+  if ((int64_t)(n < kSlice ? n : kSlice) * max_pages * (kPage / kChunk) > (int64_t)INT32_MAX)
+    return MLA_ERR_INVALID_ARG;
+  if ((int64_t)workspace_bytes_ < decode_path_bytes(n, heads)) return MLA_ERR_INVALID_ARG;
+
   const int G = prefill_grid();
   int32_t* lens = (int32_t*)workspace;
   void* split_ws = (char*)workspace + lengths_bytes();

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     raw = ctypes.CDLL(lib.LIB_PATH)
     for n in names:
         assert hasattr(raw, n), n
-    assert lib.abi_version() == 106
+    assert lib.abi_version() == 107
 
 
 def test_layouts_match_the_accounting(lib):
@@ -133,6 +133,39 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert raw.mla_prefill_workspace_bytes(100, 16) <= raw.mla_prefill_workspace_bytes(5000, 16)
     assert raw.mla_prefill_workspace_bytes(5000, 16) == raw.mla_prefill_workspace_bytes(50000, 16)
     assert raw.mla_status_string(4) == b"device-side bounds error"
+
+
+def test_prefill_path_hook(lib):
+    """The prefill path setting: set, read back, reject an unknown value,
+    and the workspace size it implies (the tensor-core path adds the key
+    tiles of 16384 positions and the query tiles of a 1024-token slice, 288
+    KB per 128 rows, to per-row check figures)."""
+    prev = lib.mla_set_prefill_path(lib.PREFILL_DECODE_KERNELS)
+    try:
+        dec = lib.mla_prefill_workspace_bytes(8192, 64)
+        assert lib.mla_set_prefill_path(lib.PREFILL_TENSOR_CORES) == lib.PREFILL_DECODE_KERNELS
+        tile = 9 * 2 * 16384
+        rows = 1024 * 64
+        tc = 128 * tile + rows // 128 * tile + 16384 * 4 + 1024 * 4 + rows * 4 + rows * 8
+        assert lib.mla_prefill_workspace_bytes(8192, 64) == max(tc, dec)
+        # a 100-token chunk at 16 heads: one 1600-row slice, 13 row tiles
+        tc_small = 128 * tile + 13 * tile + 16384 * 4 + 512 + 6400 + 12800
+        assert lib.mla_prefill_workspace_bytes(100, 16) == max(tc_small, lib.mla_prefill_workspace_bytes(1, 16))
+        assert lib.mla_prefill_path_taken(10**6, 8192, 64) == lib.PREFILL_TENSOR_CORES
+        assert lib.mla_set_prefill_path(lib.PREFILL_AUTO) == lib.PREFILL_TENSOR_CORES
+        assert lib.mla_prefill_path_taken(0, 8192, 64) == lib.PREFILL_TENSOR_CORES
+        assert lib.mla_prefill_path_taken(16384 - 8191, 8192, 64) == lib.PREFILL_DECODE_KERNELS
+        assert lib.mla_prefill_path_taken(0, 200, 64) == lib.PREFILL_DECODE_KERNELS      # every row < 256 tokens
+        assert lib.mla_prefill_path_taken(300, 100, 16) == lib.PREFILL_DECODE_KERNELS    # 1600 rows
+        assert lib.mla_prefill_path_taken(0, 8192, 24) == -1
+        # automatic: the tensor-core size only from 8192 rows on
+        assert lib.mla_prefill_workspace_bytes(100, 16) < tc_small
+        assert lib.mla_prefill_workspace_bytes(8192, 64) == max(tc, dec)
+        with pytest.raises(ValueError):
+            lib.mla_set_prefill_path(7)
+    finally:
+        lib.mla_set_prefill_path(prev)
+    assert prev == lib.PREFILL_AUTO
 
 
 def test_wait_limit_hook(lib):

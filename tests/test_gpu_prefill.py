@@ -18,6 +18,17 @@ from tests._helpers import ATTN_TOL, FMT_NAME
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True, params=["decode_kernels", "auto"])
+def prefill_path(request):
+    """Every test runs on the decode-kernel path and on the automatic choice
+    (the tensor cores for chunks of 8192 rows or more and prefixes of 257 to
+    16384 tokens)."""
+    prev = mla.mla_set_prefill_path(mla.PREFILL_DECODE_KERNELS if request.param == "decode_kernels"
+                                    else mla.PREFILL_AUTO)
+    yield request.param
+    mla.mla_set_prefill_path(prev)
+
+
 class Chunk:
     """One sequence of T = ctx_before + n tokens in a paged cache (pages in a
     seeded order, the pool's other bytes 0xFF), plus the chunk's queries."""
