@@ -757,40 +757,52 @@ __global__ void __launch_bounds__(kKeyThreads) prefill_keys_kernel(const DecodeP
   }
 }
 
-// exact_fixup_kernel: grid (B, H / 8), block kCombThreads.  After the
-// tensor-core prefill of B query rows (batch row b = query token, length
-// p.seq_lens[b]), recomputes exactly in fp32 the heads h0 .. h0 + 7 of row b
-// that need it: all of them when the row sees fewer than kExactLen tokens,
-// else (quantized latents) those whose recorded check fails,
-// risk[r] > kRiskRatio * max(omax[2r], omax[2r + 1]) with r = b H + h, the
-// same criterion as the decode's combine (risk = sqrt(sum_t (w_t M_t)^2),
-// omax = |o_lat|_inf of each 256-channel half).
+// exact_fixup_kernel: block kCombThreads, a grid of at most two blocks per
+// SM.  After the tensor-core prefill of B query rows (batch row b = query
+// token, length p.seq_lens[b]), recomputes exactly in fp32 the heads h0 ..
+// h0 + 7 of row b that need it: all of them when the row sees fewer than
+// kExactLen tokens, else (quantized latents) those whose recorded check
+// fails, risk[r] > kRiskRatio * max(omax[2r], omax[2r + 1]) with r = b H + h,
+// the same criterion as the decode's combine (risk = sqrt(sum_t (w_t
+// M_t)^2), omax = |o_lat|_inf of each 256-channel half).  Block x takes the
+// (row, 8-head group) items x, x + G, x + 2G, .. (G = gridDim.x), 128 at a
+// time: its threads test the 128 items' 8 heads at once, then the block
+// recomputes the items that need it, one after the other.  The stride
+// spreads the short rows at the start of a chunk over every block.
+constexpr int kFixupBatch = kCombThreads / kShortHeads;     // items tested per round: 128
+
 template <int LF, int KF>
 __global__ void __launch_bounds__(kCombThreads, 1) exact_fixup_kernel(const DecodeParams p, const float* risk,
                                                                       const float* omax) {
   extern __shared__ float short_smem[];
-  __shared__ uint32_t s_rows;
+  __shared__ uint32_t s_bits[kFixupBatch];
   pdl_launch_dependents();
   pdl_wait();
-  const int b = blockIdx.x, h0 = blockIdx.y * kShortHeads;
-  const int len = checked_len(p, b, false);
-  if (threadIdx.x < 32) {
+  const int groups = p.H / kShortHeads, items = p.B * groups;
+  for (int first = blockIdx.x; first < items; first += gridDim.x * kFixupBatch) {
+    __syncthreads();                               // the previous round's readers of s_bits are done
+    const int it = first + gridDim.x * (threadIdx.x / kShortHeads);
     bool need = false;
-    if (threadIdx.x < kShortHeads) {
+    if (it < items) {
+      const int b = it / groups, j = threadIdx.x % kShortHeads;
+      const int len = checked_len(p, b, false);
       if (len < kExactLen) {
-        need = true;
+        need = len > 0;
       } else if (kRiskFmt<LF>) {
-        const size_t r = (size_t)b * p.H + h0 + threadIdx.x;
+        const size_t r = (size_t)b * p.H + (it % groups) * kShortHeads + j;
         need = risk[r] > kRiskRatio * fmaxf(omax[2 * r], omax[2 * r + 1]);
       }
     }
-    const uint32_t bits = __ballot_sync(0xffffffffu, need);
-    if (threadIdx.x == 0) s_rows = bits;
+    const uint32_t bal = __ballot_sync(0xffffffffu, need);
+    if (threadIdx.x % kShortHeads == 0) s_bits[threadIdx.x / kShortHeads] = (bal >> (threadIdx.x & 31)) & 0xffu;
+    __syncthreads();
+    for (int i = 0; i < kFixupBatch; ++i) {
+      const uint32_t rows = s_bits[i];
+      if (rows == 0) continue;
+      const int item = first + gridDim.x * i, b = item / groups;
+      exact_rows<LF, KF>(p, b, (item % groups) * kShortHeads, checked_len(p, b, false), rows, short_smem);
+    }
   }
-  __syncthreads();
-  const uint32_t rows = s_rows;
-  if (rows == 0 || len == 0) return;
-  exact_rows<LF, KF>(p, b, h0, len, rows, short_smem);
 }
 
 }  // namespace
@@ -907,7 +919,10 @@ mla_status launch_exact_fixup_t(const DecodeParams& p, const float* risk, const 
   static int configured[64] = {0};
   const mla_status st = allow_smem(exact_fixup_kernel<LF, KF>, kShortSmemBytes, configured);
   if (st != MLA_OK) return st;
-  return cuda_status(launch_pdl(exact_fixup_kernel<LF, KF>, dim3(p.B, p.H / kShortHeads), dim3(kCombThreads),
+  const int items = p.B * (p.H / kShortHeads);
+  const int sms = device_sm_count();
+  const int cap = 2 * (sms > 0 ? sms : 1);
+  return cuda_status(launch_pdl(exact_fixup_kernel<LF, KF>, dim3(items < cap ? items : cap), dim3(kCombThreads),
                                 kShortSmemBytes, stream, p, risk, omax));
 }
 
