@@ -40,9 +40,13 @@
 // (warp w reads TMEM lanes 32 (w mod 4) ..) and the epilogue.
 //
 // TMEM (512 columns): S double-buffered in columns 0..127 / 128..255, the
-// O half in 256..511.  Shared memory (1024-aligned): two 64 KB stages of
-// (Q_hi, Q_lo, K_hi, K_lo) channel blocks, the 64 KB V tile (four 64-channel
-// blocks of K_hi), the 32 KB P tile, then the barriers.
+// O half in 256..511.  Shared memory (1024-aligned): a ring of three 64 KB
+// slots, the 32 KB P tile, then the barriers.  The ring carries, per key
+// tile j, nine QK items (Q_hi, Q_lo, K_hi, K_lo of one 64-channel block)
+// and then the V item of tile j - 1 (the half's four 64-channel blocks of
+// K_hi), in the order the MMAs consume them; three slots keep two 64 KB
+// items in flight while the MMAs work on the third (with two stages the
+// MMAs waited ~25 % of the time for data).
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -56,10 +60,9 @@ constexpr int kTcKeys = 128;                    // keys per tile
 constexpr int kTcKB = (kDc + kDr) / 64;         // 9 channel blocks of the contraction
 constexpr int kBlk = kTcTileBytes / (2 * kTcKB);  // one 128 x 64 fp16 block: 16 KB
 constexpr int kTileBytes = kTcTileBytes;        // hi + lo blocks of one 128-row tile
-constexpr int kStageBytes = 4 * kBlk;           // Q_hi, Q_lo, K_hi, K_lo of one channel block
-constexpr int kStages = 2;
-constexpr int kVOff = kStages * kStageBytes;
-constexpr int kPOff = kVOff + 4 * kBlk;
+constexpr int kStageBytes = 4 * kBlk;           // a ring slot: one QK item or one V item
+constexpr int kStages = 3;
+constexpr int kPOff = kStages * kStageBytes;
 constexpr int kBarOff = kPOff + 2 * kBlk;
 constexpr int kTcSmem = kBarOff + 128 + 1024;   // barriers, TMEM address; 1024-byte alignment slack
 constexpr int kTcThreads = 192;
@@ -67,8 +70,7 @@ constexpr float kRescaleSlack = 8.f;            // raise the running max only pa
 constexpr uint64_t kDrainNs = 2000000000ull;    // bound on the final waits for this CTA's own copies / MMAs
 
 // barrier indices (8 bytes each at kBarOff)
-enum { kFull0 = 0, kEmpty0 = 2, kVFull = 4, kVEmpty = 5, kSFull0 = 6, kPFull = 8, kPVDone = 9, kFin = 10,
-       kNumBars = 11 };
+enum { kFull0 = 0, kEmpty0 = kStages, kSFull0 = 2 * kStages, kPFull = kSFull0 + 2, kPVDone, kFin, kNumBars };
 
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -282,37 +284,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
   pdl_wait();
 
   if (warp == 0) {
-    // ---- loader: stages of tile j, then V of tile j - 1 (the MMA order)
+    // ---- loader: the ring items in the MMA order (QK items of tile j, then
+    // the V item of tile j - 1)
     if (lane == 0) {
       const uint8_t* qt = p.qws + (int64_t)rt * kTileBytes;
-      uint32_t ks = 0, nv = 0;
+      uint32_t it = 0;
       bool ok = true;
       for (int j = 0; j <= J && ok; ++j) {
-        if (j < J) {
-          const uint8_t* kt = p.kws + (int64_t)j * kTileBytes;
-          for (int kb = 0; kb < kTcKB; ++kb) {
-            const uint32_t s = ks & 1;
-            if (ks >= kStages && !bar_wait(bars + 8 * (kEmpty0 + s), ((ks >> 1) & 1) ^ 1, p.wait_ns, abort)) {
-              ok = false;
-              break;
-            }
-            const uint32_t dst = sb + s * kStageBytes, full = bars + 8 * (kFull0 + s);
-            bar_expect(full, kStageBytes);
-            bulk_copy(dst, qt + (int64_t)kb * 2 * kBlk, 2 * kBlk, full);              // Q_hi, Q_lo
-            bulk_copy(dst + 2 * kBlk, kt + (int64_t)kb * 2 * kBlk, 2 * kBlk, full);   // K_hi, K_lo
-            ++ks;
-          }
-        }
-        if (ok && j >= 1) {
-          if (nv >= 1 && !bar_wait(bars + 8 * kVEmpty, (nv - 1) & 1, p.wait_ns, abort)) {
+        for (int kb = (j < J ? 0 : kTcKB); kb <= kTcKB && ok; ++kb) {
+          if (kb == kTcKB && j == 0) break;            // no V item before the first tile's
+          const uint32_t s = it % kStages;
+          if (it >= kStages && !bar_wait(bars + 8 * (kEmpty0 + s), ((it / kStages) & 1) ^ 1, p.wait_ns, abort)) {
             ok = false;
             break;
           }
-          const uint8_t* kt = p.kws + (int64_t)(j - 1) * kTileBytes;
-          bar_expect(bars + 8 * kVFull, 4 * kBlk);
-          for (int c = 0; c < 4; ++c)
-            bulk_copy(sb + kVOff + c * kBlk, kt + (int64_t)(4 * half + c) * 2 * kBlk, kBlk, bars + 8 * kVFull);
-          ++nv;
+          const uint32_t dst = sb + s * kStageBytes, full = bars + 8 * (kFull0 + s);
+          bar_expect(full, kStageBytes);
+          if (kb < kTcKB) {
+            const uint8_t* kt = p.kws + (int64_t)j * kTileBytes;
+            bulk_copy(dst, qt + (int64_t)kb * 2 * kBlk, 2 * kBlk, full);              // Q_hi, Q_lo
+            bulk_copy(dst + 2 * kBlk, kt + (int64_t)kb * 2 * kBlk, 2 * kBlk, full);   // K_hi, K_lo
+          } else {
+            const uint8_t* kt = p.kws + (int64_t)(j - 1) * kTileBytes;
+            for (int c = 0; c < 4; ++c)                                             // V: K_hi of the half
+              bulk_copy(dst + c * kBlk, kt + (int64_t)(4 * half + c) * 2 * kBlk, kBlk, full);
+          }
+          ++it;
         }
       }
       if (!ok) {
@@ -321,21 +318,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
       }
       // the copies in flight land before the CTA exits
       for (uint32_t s = 0; s < kStages; ++s)
-        if (ks > s) drain_wait(bars + 8 * (kFull0 + s), ((ks - 1 - s) >> 1) & 1);
-      if (nv) drain_wait(bars + 8 * kVFull, (nv - 1) & 1);
+        if (it > s) drain_wait(bars + 8 * (kFull0 + s), ((it - 1 - s) / kStages) & 1);
     }
   } else if (warp == 1) {
-    // ---- MMA issuer: QK(j) into S[j & 1], then PV(j - 1)
+    // ---- MMA issuer: QK(j) into S[j & 1], then PV(j - 1), one ring item each
     if (lane == 0) {
       constexpr uint32_t kIdQK = f16_idesc(kTcKeys, false), kIdPV = f16_idesc(256, true);
-      uint32_t ks = 0;
+      uint32_t it = 0;
       bool ok = true;
       for (int j = 0; j <= J && ok; ++j) {
         if (j < J) {
           const uint32_t d = tbase + (uint32_t)((j & 1) * kTcKeys);
-          for (int kb = 0; kb < kTcKB; ++kb, ++ks) {
-            const uint32_t s = ks & 1;
-            if (!bar_wait(bars + 8 * (kFull0 + s), (ks >> 1) & 1, p.wait_ns, abort)) {
+          for (int kb = 0; kb < kTcKB; ++kb, ++it) {
+            const uint32_t s = it % kStages;
+            if (!bar_wait(bars + 8 * (kFull0 + s), (it / kStages) & 1, p.wait_ns, abort)) {
               ok = false;
               break;
             }
@@ -356,21 +352,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
           umma_commit(bars + 8 * (kSFull0 + (j & 1)));
         }
         if (j >= 1) {
-          const uint32_t jp = (uint32_t)(j - 1);
+          const uint32_t jp = (uint32_t)(j - 1), s = it % kStages;
           if (!bar_wait(bars + 8 * kPFull, jp & 1, p.wait_ns, abort) ||
-              !bar_wait(bars + 8 * kVFull, jp & 1, p.wait_ns, abort)) {
+              !bar_wait(bars + 8 * (kFull0 + s), (it / kStages) & 1, p.wait_ns, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint32_t v = sb + s * kStageBytes;
 #pragma unroll
           for (int k = 0; k < kTcKeys / 16; ++k) {
             const uint64_t a = sw128_desc(sb + kPOff + (k >> 2) * kBlk + (k & 3) * 32, 16, 1024);
-            const uint64_t b = sw128_desc(sb + kVOff + k * 2048, kBlk, 1024);
+            const uint64_t b = sw128_desc(v + k * 2048, kBlk, 1024);
             umma(tbase + 256, a, b, kIdPV, (jp | (uint32_t)k) != 0);
           }
-          umma_commit(bars + 8 * kVEmpty);
+          umma_commit(bars + 8 * (kEmpty0 + s));
           umma_commit(bars + 8 * kPVDone);
+          ++it;
         }
       }
       if (!ok) {
