@@ -496,8 +496,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         p.omax[2 * row + half] = om;
       }
     } else {
+      // given up: the row reads as attention over nothing (o_lat 0, lse
+      // -inf, nothing for the fixup to check), finite like the decode's
+      // empty partials
       set_err(p.dev_err, MLA_DEVERR_TIMEOUT);
       *abort = 1;
+      if (live) {
+        float* orow = p.o_lat + (int64_t)row * kDc + 256 * half;
+        for (int v = 0; v < 64; ++v) reinterpret_cast<float4*>(orow)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (half == 0) {
+          if (p.lse) p.lse[row] = -INFINITY;
+          p.risk_out[row] = 0.f;
+        }
+        p.omax[2 * row + half] = 0.f;
+      }
     }
   }
   tc_fence_before();
