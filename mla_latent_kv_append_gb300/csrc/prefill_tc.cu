@@ -39,8 +39,9 @@
 // allocates TMEM and its lane 0 issues the MMAs, warps 2..5 run the softmax
 // (warp w reads TMEM lanes 32 (w mod 4) ..) and the epilogue.
 //
-// TMEM (512 columns): S double-buffered in columns 0..127 / 128..255, the
-// O half in 256..511.  Shared memory (1024-aligned): a ring of three 64 KB
+// TMEM (512 columns): S in columns 0..255 (Q_hi K_hi + Q_lo K_hi in 0..127,
+// Q_hi K_lo in 128..255: the two Q_hi products are one N = 256 MMA), the O
+// half in 256..511.  Shared memory (1024-aligned): a ring of three 64 KB
 // slots, the 32 KB P tile, then the barriers.  The ring carries, per key
 // tile j, nine QK items (Q_hi, Q_lo, K_hi, K_lo of one 64-channel block)
 // and then the V item of tile j - 1 (the half's four 64-channel blocks of
@@ -70,7 +71,7 @@ constexpr float kRescaleSlack = 8.f;            // raise the running max only pa
 constexpr uint64_t kDrainNs = 2000000000ull;    // bound on the final waits for this CTA's own copies / MMAs
 
 // barrier indices (8 bytes each at kBarOff)
-enum { kFull0 = 0, kEmpty0 = kStages, kSFull0 = 2 * kStages, kPFull = kSFull0 + 2, kPVDone, kFin, kNumBars };
+enum { kFull0 = 0, kEmpty0 = kStages, kSFull = 2 * kStages, kSRead, kPFull, kPVDone, kFin, kNumBars };
 
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
   const int J = (p.qpos0 + rlast / p.H + kTcKeys) / kTcKeys;   // key tiles the tile's last row reaches
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNumBars; ++i) bar_init(bars + 8 * i, i == kPFull ? 128 : 1);
+    for (int i = 0; i < kNumBars; ++i) bar_init(bars + 8 * i, i == kPFull || i == kSRead ? 128 : 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -321,14 +322,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
         if (it > s) drain_wait(bars + 8 * (kFull0 + s), ((it - 1 - s) / kStages) & 1);
     }
   } else if (warp == 1) {
-    // ---- MMA issuer: QK(j) into S[j & 1], then PV(j - 1), one ring item each
+    // ---- MMA issuer: QK(j) into S once the softmax has read S(j - 1), then
+    // PV(j - 1) (which keeps the pipe busy while the softmax reads S(j)), one
+    // ring item each
     if (lane == 0) {
-      constexpr uint32_t kIdQK = f16_idesc(kTcKeys, false), kIdPV = f16_idesc(256, true);
+      constexpr uint32_t kIdQK = f16_idesc(kTcKeys, false), kIdQK2 = f16_idesc(2 * kTcKeys, false),
+                         kIdPV = f16_idesc(256, true);
       uint32_t it = 0;
       bool ok = true;
       for (int j = 0; j <= J && ok; ++j) {
         if (j < J) {
-          const uint32_t d = tbase + (uint32_t)((j & 1) * kTcKeys);
+          if (j >= 1 && !bar_wait(bars + 8 * kSRead, (j - 1) & 1, p.wait_ns, abort)) {
+            ok = false;
+            break;
+          }
+          const uint32_t d = tbase;
           for (int kb = 0; kb < kTcKB; ++kb, ++it) {
             const uint32_t s = it % kStages;
             if (!bar_wait(bars + 8 * (kFull0 + s), (it / kStages) & 1, p.wait_ns, abort)) {
@@ -336,20 +344,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
               break;
             }
             tc_fence_after();
-            const uint32_t a_hi = sb + s * kStageBytes, a_lo = a_hi + kBlk, b_hi = a_hi + 2 * kBlk,
-                           b_lo = a_hi + 3 * kBlk;
+            // B = [K_hi; K_lo] as one 256-row operand (the lo block follows
+            // the hi block): Q_hi is read once for both of its products
+            const uint32_t a_hi = sb + s * kStageBytes, a_lo = a_hi + kBlk, b_hi = a_hi + 2 * kBlk;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const uint64_t ah = sw128_desc(a_hi + 32 * k, 16, 1024), al = sw128_desc(a_lo + 32 * k, 16, 1024);
-              const uint64_t bh = sw128_desc(b_hi + 32 * k, 16, 1024), bl = sw128_desc(b_lo + 32 * k, 16, 1024);
-              umma(d, ah, bh, kIdQK, (kb | k) != 0);
-              umma(d, ah, bl, kIdQK, 1u);
-              umma(d, al, bh, kIdQK, 1u);
+              const uint64_t bh = sw128_desc(b_hi + 32 * k, 16, 1024);
+              umma(d, ah, bh, kIdQK2, (kb | k) != 0);    // columns 0..127: Q_hi K_hi; 128..255: Q_hi K_lo
+              umma(d, al, bh, kIdQK, 1u);               // columns 0..127: + Q_lo K_hi
             }
             umma_commit(bars + 8 * (kEmpty0 + s));
           }
           if (!ok) break;
-          umma_commit(bars + 8 * (kSFull0 + (j & 1)));
+          umma_commit(bars + 8 * kSFull);
         }
         if (j >= 1) {
           const uint32_t jp = (uint32_t)(j - 1), s = it % kStages;
@@ -391,14 +399,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
     float m_run = -INFINITY, l = 0.f, e2 = 0.f;
     bool ok = true;
     for (int j = 0; j < J; ++j) {
-      if (!warp_wait(bars + 8 * (kSFull0 + (j & 1)), (j >> 1) & 1, p.wait_ns, abort)) {
+      if (!warp_wait(bars + 8 * kSFull, j & 1, p.wait_ns, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
       float x[kTcKeys];
 #pragma unroll
-      for (int c = 0; c < kTcKeys / 32; ++c) tmem_load(tl + (uint32_t)((j & 1) * kTcKeys + 32 * c), x + 32 * c);
+      for (int c = 0; c < kTcKeys / 32; ++c) {
+        float y[32];
+        tmem_load(tl + (uint32_t)(32 * c), x + 32 * c);
+        tmem_load(tl + (uint32_t)(kTcKeys + 32 * c), y);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[32 * c + i] += y[i];
+      }
+      // S is in registers: QK(j + 1) may overwrite it
+      tc_fence_before();
+      bar_arrive(bars + 8 * kSRead);
       const int kpos0 = j * kTcKeys;
       float mx = -INFINITY;
       if (kpos0 + kTcKeys - 1 > qpos) {
