@@ -143,3 +143,11 @@ def test_tc_prefill_zero_wait_limit_gives_up_cleanly():
     torch.cuda.synchronize()
     assert err.item() == 0
     assert np.array_equal(o.cpu().numpy(), ref_ol) and np.array_equal(lse.cpu().numpy(), ref_lse)
+
+
+def test_tc_prefill_at_the_key_limit():
+    """Prefixes that end exactly at the key tiles' 16384 positions (all 128
+    key tiles, the last query's row tile sweeping every one): sampled rows,
+    the last query included."""
+    ch = Chunk(mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM, 16384 - 40, 40, 16, seed=100)
+    check(ch, [0, 1, 17, 38, 39])
