@@ -374,8 +374,9 @@ mla_status mla_decode_absorbed_noalloc(const mla_cache_layer* cache, const float
  * mla_prefill_workspace_bytes - bytes of device workspace mla_prefill_absorbed
  * needs for a chunk of n query tokens and this head count under the current
  * prefill path setting (0 for invalid arguments).  Bounded in n: queries are
- * processed in slices of 2048 (decode kernels) or 1024 (tensor cores); the
- * tensor-core path adds the key tiles of up to 16384 positions (~38 MB).
+ * processed in slices of 2048 (decode kernels) or 4096 (tensor cores: 288 KB
+ * of query tiles per 128 rows, ~600 MB at 64 heads); the tensor-core path
+ * adds the key tiles of up to 16384 positions (~38 MB).
  */
 size_t mla_prefill_workspace_bytes(int32_t n, int32_t heads);
 

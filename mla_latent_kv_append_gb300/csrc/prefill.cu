@@ -47,7 +47,7 @@ int prefill_grid() {
 bool aligned_to(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
 // ---- tensor-core path
-constexpr int kTcSlice = 1024;           // query tokens per launch
+constexpr int kTcSlice = 4096;           // query tokens per launch (1024: +4 % time; 8192: no gain)
 constexpr int kTcMaxKeys = 16384;        // positions the key tiles hold
 constexpr int64_t kTcMinRows = 8192;     // automatic choice: rows (n x H) that fill the GPU
 constexpr int kTcExactLen = 256;         // rows below this length are recomputed exactly anyway

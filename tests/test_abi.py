@@ -138,15 +138,15 @@ def test_invalid_arguments_rejected_on_host(lib):
 def test_prefill_path_hook(lib):
     """The prefill path setting: set, read back, reject an unknown value,
     and the workspace size it implies (the tensor-core path adds the key
-    tiles of 16384 positions and the query tiles of a 1024-token slice, 288
+    tiles of 16384 positions and the query tiles of a 4096-token slice, 288
     KB per 128 rows, to per-row check figures)."""
     prev = lib.mla_set_prefill_path(lib.PREFILL_DECODE_KERNELS)
     try:
         dec = lib.mla_prefill_workspace_bytes(8192, 64)
         assert lib.mla_set_prefill_path(lib.PREFILL_TENSOR_CORES) == lib.PREFILL_DECODE_KERNELS
         tile = 9 * 2 * 16384
-        rows = 1024 * 64
-        tc = 128 * tile + rows // 128 * tile + 16384 * 4 + 1024 * 4 + rows * 4 + rows * 8
+        rows = 4096 * 64
+        tc = 128 * tile + rows // 128 * tile + 16384 * 4 + 4096 * 4 + rows * 4 + rows * 8
         assert lib.mla_prefill_workspace_bytes(8192, 64) == max(tc, dec)
         # a 100-token chunk at 16 heads: one 1600-row slice, 13 row tiles
         tc_small = 128 * tile + 13 * tile + 16384 * 4 + 512 + 6400 + 12800

@@ -43,11 +43,11 @@ def test_tc_prefill_shapes(ctx_before, n, H):
 
 
 def test_tc_prefill_slices():
-    """1100 queries: two slices of 1024 query tokens; rows around the
+    """4200 queries: two slices of 4096 query tokens; rows around the
     boundary, the first and the last, and a sample."""
-    ch = Chunk(mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM, 10, 1100, 16, seed=97)
+    ch = Chunk(mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM, 10, 4200, 16, seed=97)
     rng = np.random.default_rng(97)
-    rows = sorted(set([0, 1, 1022, 1023, 1024, 1025, 1099] + [int(r) for r in rng.integers(0, 1100, 12)]))
+    rows = sorted(set([0, 1, 4094, 4095, 4096, 4097, 4199] + [int(r) for r in rng.integers(0, 4200, 12)]))
     check(ch, rows)
 
 
