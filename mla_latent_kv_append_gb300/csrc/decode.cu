@@ -269,8 +269,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 // tokens.  sm: kShortSmemBytes of shared memory.  Each combine kernel has a
 // single call site (inlined: as a call it left spill code on the combine's
 // common path, and a second inlined copy slowed that path down).
-template <int LF, int KF>
-__device__ __forceinline__ void exact_rows(const DecodeParams& p, int b, int h0, int len, uint32_t rows, float* sm) {
+//
+// exact_core is the computation over tokens t_begin .. len - 1 (t_begin a
+// multiple of 32); with kPart it writes, instead of the normalised rows, the
+// eight heads' partial state to part[8][kPartStride]: running maximum (log2
+// domain), weight sum, then the 512 unnormalised channels.
+constexpr int kPartStride = 2 + kDc;
+
+template <int LF, int KF, bool kPart>
+__device__ __forceinline__ void exact_core(const DecodeParams& p, int b, int h0, int t_begin, int len, uint32_t rows,
+                                           float* sm, float* part) {
   float* s_c = sm;                                 // [32][kCS]
   float* s_k = s_c + kChunk * kCS;                 // [32][kKS]
   float* s_q = s_k + kChunk * kKS;                 // [8][kQS]
@@ -289,7 +297,7 @@ __device__ __forceinline__ void exact_rows(const DecodeParams& p, int b, int h0,
   const int c = tid & (kDc - 1), hb = (tid / kDc) * 4;
   float m = -INFINITY, l = 0.f;                    // warps 0..7: head `warp`'s running max and weight sum
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int t0 = 0; t0 < len; t0 += kChunk) {
+  for (int t0 = t_begin; t0 < len; t0 += kChunk) {
     __syncthreads();                               // the previous block's readers are done; s_q in place
     dequant_chunk<LF, KF, kCombThreads>(p, b, t0, len, s_c, s_k, s_valid, s_page);
     __syncthreads();
@@ -344,6 +352,15 @@ __device__ __forceinline__ void exact_rows(const DecodeParams& p, int b, int h0,
       acc[3] = fmaf(w.w, v, acc[3]);
     }
   }
+  if (kPart) {
+    if (warp < kShortHeads && lane == 0) {
+      part[warp * kPartStride] = m;
+      part[warp * kPartStride + 1] = l;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) part[(hb + j) * kPartStride + 2 + c] = acc[j];
+    return;
+  }
   if (warp < kShortHeads && lane == 0) {
     s_ml[2 * warp] = m;
     s_ml[2 * warp + 1] = l;
@@ -355,6 +372,11 @@ __device__ __forceinline__ void exact_rows(const DecodeParams& p, int b, int h0,
     const float lj = s_ml[2 * (hb + j) + 1];
     if ((rows >> (hb + j)) & 1) p.o_lat[(row0 + hb + j) * kDc + c] = lj > 0.f ? acc[j] / lj : 0.f;
   }
+}
+
+template <int LF, int KF>
+__device__ __forceinline__ void exact_rows(const DecodeParams& p, int b, int h0, int len, uint32_t rows, float* sm) {
+  exact_core<LF, KF, false>(p, b, h0, 0, len, rows, sm, nullptr);
 }
 
 // The output projection of rows b, h0 + j (bit j of `rows` set) that this
@@ -767,15 +789,18 @@ __global__ void __launch_bounds__(kKeyThreads) prefill_keys_kernel(const DecodeP
 // M_t)^2), omax = |o_lat|_inf of each 256-channel half).  Block x takes the
 // (row, 8-head group) items x, x + G, x + 2G, .. (G = gridDim.x), 128 at a
 // time: its threads test the 128 items' 8 heads at once, then the block
-// recomputes the items that need it, one after the other.  The stride
-// spreads the short rows at the start of a chunk over every block.
+// recomputes the short items that need it, one after the other, and queues
+// the long ones (up to kSplitCap per launch; past that it recomputes them
+// itself) for exact_split_kernel, which spreads each over many blocks.  The
+// stride spreads the short rows at the start of a chunk over every block.
 constexpr int kFixupBatch = kCombThreads / kShortHeads;     // items tested per round: 128
 
 template <int LF, int KF>
 __global__ void __launch_bounds__(kCombThreads, 1) exact_fixup_kernel(const DecodeParams p, const float* risk,
-                                                                      const float* omax) {
+                                                                      const float* omax, SplitQueue q) {
   extern __shared__ float short_smem[];
   __shared__ uint32_t s_bits[kFixupBatch];
+  __shared__ int s_slot;
   pdl_launch_dependents();
   pdl_wait();
   const int groups = p.H / kShortHeads, items = p.B * groups;
@@ -799,8 +824,77 @@ __global__ void __launch_bounds__(kCombThreads, 1) exact_fixup_kernel(const Deco
     for (int i = 0; i < kFixupBatch; ++i) {
       const uint32_t rows = s_bits[i];
       if (rows == 0) continue;
-      const int item = first + gridDim.x * i, b = item / groups;
-      exact_rows<LF, KF>(p, b, (item % groups) * kShortHeads, checked_len(p, b, false), rows, short_smem);
+      const int item = first + gridDim.x * i, b = item / groups, h0 = (item % groups) * kShortHeads;
+      const int len = checked_len(p, b, false);
+      if (len >= kExactLen) {          // a long row: queued for the split recomputation if there is room
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          const int slot = atomicAdd(q.count, 1);
+          s_slot = slot;
+          if (slot < kSplitCap) {
+            q.items[4 * slot] = b;
+            q.items[4 * slot + 1] = h0;
+            q.items[4 * slot + 2] = (int)rows;
+            q.items[4 * slot + 3] = len;
+          }
+        }
+        __syncthreads();
+        if (s_slot < kSplitCap) continue;
+      }
+      exact_rows<LF, KF>(p, b, h0, len, rows, short_smem);
+    }
+  }
+}
+
+// exact_split_kernel: block kCombThreads, a grid of at most two blocks per
+// SM.  The long rows the fixup queued (q.items[0 .. min(*q.count, cap)))
+// are recomputed exactly over kSplitParts contiguous token ranges each, one
+// (item, range) per block at a time: the block writes the range's partial
+// state, and the block that completes an item's last range (a counter per
+// item) merges the partials into o_lat and lse (M = max m, L = sum 2^(m - M)
+// l, o = sum 2^(m - M) o / L).  One block recomputing a 9K-token row alone
+// took ~2.9 ms.
+template <int LF, int KF>
+__global__ void __launch_bounds__(kCombThreads, 1) exact_split_kernel(const DecodeParams p, SplitQueue q) {
+  extern __shared__ float short_smem[];
+  __shared__ int s_last;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int n = min(*q.count, kSplitCap);
+  for (int unit = blockIdx.x; unit < n * kSplitParts; unit += gridDim.x) {
+    const int item = unit / kSplitParts, part = unit % kSplitParts;
+    const int b = q.items[4 * item], h0 = q.items[4 * item + 1], len = q.items[4 * item + 3];
+    const uint32_t rows = (uint32_t)q.items[4 * item + 2];
+    const int chunks = (len + kChunk - 1) / kChunk;
+    const int c0 = chunks * part / kSplitParts, c1 = chunks * (part + 1) / kSplitParts;
+    float* out = q.parts + ((size_t)item * kSplitParts + part) * kShortHeads * kPartStride;
+    __syncthreads();
+    exact_core<LF, KF, true>(p, b, h0, c0 * kChunk, min(c1 * kChunk, len), rows, short_smem, out);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(q.done + item, 1) == kSplitParts - 1;
+    __syncthreads();
+    if (!s_last) continue;
+    __threadfence();
+    const int c = threadIdx.x & (kDc - 1), hb = (threadIdx.x / kDc) * 4;
+    const float* base = q.parts + (size_t)item * kSplitParts * kShortHeads * kPartStride;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int h = hb + j;
+      float M = -INFINITY;
+      for (int r = 0; r < kSplitParts; ++r) M = fmaxf(M, __ldcg(base + (r * kShortHeads + h) * kPartStride));
+      float L = 0.f, o = 0.f;
+      for (int r = 0; r < kSplitParts; ++r) {
+        const float* pr = base + (r * kShortHeads + h) * kPartStride;
+        const float w = M == -INFINITY ? 0.f : exp2f(__ldcg(pr) - M);
+        L = fmaf(w, __ldcg(pr + 1), L);
+        o = fmaf(w, __ldcg(pr + 2 + c), o);
+      }
+      if ((rows >> h) & 1) {
+        const size_t row = (size_t)b * p.H + h0 + h;
+        p.o_lat[row * kDc + c] = L > 0.f ? o / L : 0.f;
+        if (c == 0 && p.lse) p.lse[row] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+      }
     }
   }
 }
@@ -915,15 +1009,21 @@ mla_status launch_prefill_keys_t(const DecodeParams& p, int len, void* kws, floa
 }
 
 template <int LF, int KF>
-mla_status launch_exact_fixup_t(const DecodeParams& p, const float* risk, const float* omax, cudaStream_t stream) {
-  static int configured[64] = {0};
-  const mla_status st = allow_smem(exact_fixup_kernel<LF, KF>, kShortSmemBytes, configured);
+mla_status launch_exact_fixup_t(const DecodeParams& p, const float* risk, const float* omax, const SplitQueue& q,
+                                cudaStream_t stream) {
+  static int configured[64] = {0}, configured_s[64] = {0};
+  mla_status st = allow_smem(exact_fixup_kernel<LF, KF>, kShortSmemBytes, configured);
+  if (st != MLA_OK) return st;
+  st = allow_smem(exact_split_kernel<LF, KF>, kShortSmemBytes, configured_s);
   if (st != MLA_OK) return st;
   const int items = p.B * (p.H / kShortHeads);
   const int sms = device_sm_count();
   const int cap = 2 * (sms > 0 ? sms : 1);
-  return cuda_status(launch_pdl(exact_fixup_kernel<LF, KF>, dim3(items < cap ? items : cap), dim3(kCombThreads),
-                                kShortSmemBytes, stream, p, risk, omax));
+  st = cuda_status(launch_pdl(exact_fixup_kernel<LF, KF>, dim3(items < cap ? items : cap), dim3(kCombThreads),
+                              kShortSmemBytes, stream, p, risk, omax, q));
+  if (st != MLA_OK) return st;
+  return cuda_status(launch_pdl(exact_split_kernel<LF, KF>, dim3(cap), dim3(kCombThreads), kShortSmemBytes, stream,
+                                p, q));
 }
 
 }  // namespace
@@ -947,9 +1047,10 @@ mla_status launch_prefill_keys(const DecodeParams& p, int len, void* kws, float*
   return MLA_ERR_UNSUPPORTED;
 }
 
-mla_status launch_exact_fixup(const DecodeParams& p, const float* risk, const float* omax, cudaStream_t stream) {
+mla_status launch_exact_fixup(const DecodeParams& p, const float* risk, const float* omax, const SplitQueue& q,
+                              cudaStream_t stream) {
 #define MLA_FIXUP_CASE(A, K) \
-  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_exact_fixup_t<A, K>(p, risk, omax, stream);
+  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_exact_fixup_t<A, K>(p, risk, omax, q, stream);
   MLA_FORMAT_PAIRS(MLA_FIXUP_CASE)
 #undef MLA_FIXUP_CASE
   return MLA_ERR_UNSUPPORTED;

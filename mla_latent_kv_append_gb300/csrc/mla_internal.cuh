@@ -271,7 +271,35 @@ mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream);   // d
 // 2 x 16 KB per tile, swizzled) with the tokens' bounds mt[len rounded up to
 // 128]; and the exact fp32 recomputation of the rows that need it.
 mla_status launch_prefill_keys(const DecodeParams& p, int len, void* kws, float* mt, cudaStream_t stream);
-mla_status launch_exact_fixup(const DecodeParams& p, const float* risk, const float* omax, cudaStream_t stream);
+// The long rows the fixup hands to the split recomputation: *count items
+// (b, h0, row mask, length), each recomputed over kSplitParts token ranges
+// whose partial states (8 heads x (max, sum, 512 channels)) go to parts;
+// done[i] counts the finished ranges of item i.  count and done start at 0.
+constexpr int kSplitCap = 64;
+constexpr int kSplitParts = 32;
+struct SplitQueue {
+  int32_t* count;
+  int32_t* done;      // [kSplitCap]
+  int32_t* items;     // [kSplitCap][4]
+  float* parts;       // [kSplitCap][kSplitParts][8][2 + 512]
+};
+__host__ __device__ inline int64_t split_queue_bytes() {
+  return align256((int64_t)(1 + kSplitCap) * 4) + align256((int64_t)kSplitCap * 16) +
+         (int64_t)kSplitCap * kSplitParts * 8 * (2 + kDc) * 4;
+}
+__host__ __device__ inline SplitQueue carve_split_queue(void* base) {
+  char* c = (char*)base;
+  SplitQueue q;
+  q.count = (int32_t*)c;
+  q.done = q.count + 1;
+  c += align256((int64_t)(1 + kSplitCap) * 4);
+  q.items = (int32_t*)c;
+  c += align256((int64_t)kSplitCap * 16);
+  q.parts = (float*)c;
+  return q;
+}
+mla_status launch_exact_fixup(const DecodeParams& p, const float* risk, const float* omax, const SplitQueue& q,
+                              cudaStream_t stream);
 
 // Tensor-core prefill (prefill_tc.cu).  A tile holds 128 rows (queries or
 // keys) x 9 channel blocks x (hi, lo) x 16 KB.

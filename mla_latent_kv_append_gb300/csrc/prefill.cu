@@ -32,9 +32,11 @@ namespace {
 
 constexpr int kSlice = 2048;
 
-// len[i] = base + i + 1 for the slice's rows
-__global__ void causal_lengths_kernel(int32_t* len, int n, int base) {
+// len[i] = base + i + 1 for the slice's rows; zero[0 .. nzero) = 0 (the
+// tensor-core path's queue counters)
+__global__ void causal_lengths_kernel(int32_t* len, int n, int base, int32_t* zero, int nzero) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) len[i] = base + i + 1;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += gridDim.x * blockDim.x) zero[i] = 0;
 }
 
 int64_t lengths_bytes() { return align256((int64_t)kSlice * 4); }
@@ -61,6 +63,7 @@ struct TcWorkspace {
   int32_t* lens;
   float* risk;
   float* omax;
+  SplitQueue queue;
 };
 
 int64_t tc_row_tiles(int64_t rows) { return (rows + 127) / 128; }
@@ -68,13 +71,13 @@ int64_t tc_row_tiles(int64_t rows) { return (rows + 127) / 128; }
 int64_t tc_workspace_bytes(int n, int heads, TcWorkspace* w, void* base) {
   const int64_t s = n < kTcSlice ? (n > 0 ? n : 1) : kTcSlice;
   const int64_t rows = s * heads;
-  const int64_t sizes[6] = {(int64_t)(kTcMaxKeys / 128) * kTcTileBytes, tc_row_tiles(rows) * kTcTileBytes,
+  const int64_t sizes[7] = {(int64_t)(kTcMaxKeys / 128) * kTcTileBytes, tc_row_tiles(rows) * kTcTileBytes,
                             align256((int64_t)kTcMaxKeys * 4), align256(s * 4), align256(rows * 4),
-                            align256(rows * 8)};
+                            align256(rows * 8), split_queue_bytes()};
   int64_t off = 0;
   char* b = (char*)base;
-  void* ptrs[6];
-  for (int i = 0; i < 6; ++i) {
+  void* ptrs[7];
+  for (int i = 0; i < 7; ++i) {
     ptrs[i] = b ? b + off : nullptr;
     off += sizes[i];
   }
@@ -85,6 +88,7 @@ int64_t tc_workspace_bytes(int n, int heads, TcWorkspace* w, void* base) {
     w->lens = (int32_t*)ptrs[3];
     w->risk = (float*)ptrs[4];
     w->omax = (float*)ptrs[5];
+    w->queue = carve_split_queue(ptrs[6] ? ptrs[6] : (void*)nullptr);
   }
   return off;
 }
@@ -182,7 +186,8 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
       const int n_rt = (int)tc_row_tiles(R);
       // the fixup's per-row lengths; a plain launch, after the previous
       // slice's fixup has finished with them
-      causal_lengths_kernel<<<(s + 255) / 256, 256, 0, st>>>(w.lens, s, ctx_before + i0);
+      causal_lengths_kernel<<<(s + 255) / 256, 256, 0, st>>>(w.lens, s, ctx_before + i0, w.queue.count,
+                                                             1 + kSplitCap);
       const mla_status ls = launch_status();
       if (ls != MLA_OK) return ls;
       const float* ql = q_lat + (size_t)i0 * heads * kDc;
@@ -215,7 +220,7 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
       f.B = s;
       f.o_lat = ol;
       f.lse = lo;
-      ks = launch_exact_fixup(f, w.risk, w.omax, st);
+      ks = launch_exact_fixup(f, w.risk, w.omax, w.queue, st);
       if (ks != MLA_OK) return ks;
     }
     return MLA_OK;
@@ -234,7 +239,7 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
     // finished with the lengths and the split-K workspace.  Its stores are
     // visible to the decode kernel only once that kernel has waited on it
     // (lens_after_wait)
-    causal_lengths_kernel<<<(s + 255) / 256, 256, 0, st>>>(lens, s, ctx_before + i0);
+    causal_lengths_kernel<<<(s + 255) / 256, 256, 0, st>>>(lens, s, ctx_before + i0, nullptr, 0);
     const mla_status ls = launch_status();
     if (ls != MLA_OK) return ls;
     DecodeParams p;

@@ -146,10 +146,13 @@ def test_prefill_path_hook(lib):
         assert lib.mla_set_prefill_path(lib.PREFILL_TENSOR_CORES) == lib.PREFILL_DECODE_KERNELS
         tile = 9 * 2 * 16384
         rows = 4096 * 64
-        tc = 128 * tile + rows // 128 * tile + 16384 * 4 + 4096 * 4 + rows * 4 + rows * 8
+        # the queue of long rows for the split exact recomputation: counters,
+        # 64 items, 64 x 32 ranges x 8 heads x (2 + 512) floats
+        queue = 512 + 1024 + 64 * 32 * 8 * 514 * 4
+        tc = 128 * tile + rows // 128 * tile + 16384 * 4 + 4096 * 4 + rows * 4 + rows * 8 + queue
         assert lib.mla_prefill_workspace_bytes(8192, 64) == max(tc, dec)
         # a 100-token chunk at 16 heads: one 1600-row slice, 13 row tiles
-        tc_small = 128 * tile + 13 * tile + 16384 * 4 + 512 + 6400 + 12800
+        tc_small = 128 * tile + 13 * tile + 16384 * 4 + 512 + 6400 + 12800 + queue
         assert lib.mla_prefill_workspace_bytes(100, 16) == max(tc_small, lib.mla_prefill_workspace_bytes(1, 16))
         assert lib.mla_prefill_path_taken(10**6, 8192, 64) == lib.PREFILL_TENSOR_CORES
         assert lib.mla_set_prefill_path(lib.PREFILL_AUTO) == lib.PREFILL_TENSOR_CORES
