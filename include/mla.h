@@ -382,9 +382,10 @@ size_t mla_prefill_workspace_bytes(int32_t n, int32_t heads);
 
 /*
  * Prefill implementations (mla_set_prefill_path):
- *   MLA_PREFILL_AUTO           tensor cores when n * heads >= 8192 and
- *                              256 < ctx_before + n <= 16384, else the
- *                              decode kernels (the default)
+ *   MLA_PREFILL_AUTO           tensor cores when 256 < ctx_before + n <=
+ *                              16384 and either n * heads >= 8192, or
+ *                              n * heads >= 2048 and ctx_before + n >= 4096;
+ *                              else the decode kernels (the default)
  *   MLA_PREFILL_DECODE_KERNELS always the split-K decode kernels
  *   MLA_PREFILL_TENSOR_CORES   always tensor cores; a call with
  *                              ctx_before + n > 16384 returns

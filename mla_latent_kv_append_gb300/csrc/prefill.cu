@@ -51,8 +51,15 @@ bool aligned_to(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) ==
 // ---- tensor-core path
 constexpr int kTcSlice = 4096;           // query tokens per launch (1024: +4 % time; 8192: no gain)
 constexpr int kTcMaxKeys = 16384;        // positions the key tiles hold
-constexpr int64_t kTcMinRows = 8192;     // automatic choice: rows (n x H) that fill the GPU
-constexpr int kTcExactLen = 256;         // rows below this length are recomputed exactly anyway
+// The automatic choice (measured on GB300 against the decode kernels, INT8,
+// 16 and 64 heads, 0 to 8192 positions before the chunk): the tensor cores
+// from 8192 rows (n x H) on, or from 2048 rows once the chunk's prefixes
+// reach 4096 positions; never when every row sees at most 256 positions
+// (they are all recomputed exactly).
+constexpr int64_t kTcMinRows = 8192;
+constexpr int64_t kTcMinRowsLong = 2048;
+constexpr int kTcLongKeys = 4096;
+constexpr int kTcExactLen = 256;
 
 std::atomic<int> g_prefill_path{MLA_PREFILL_AUTO};
 
@@ -103,10 +110,12 @@ int64_t decode_path_bytes(int n, int heads) {
 int choose_path(int ctx_before, int n, int heads) {
   const int forced = g_prefill_path.load(std::memory_order_relaxed);
   if (forced != MLA_PREFILL_AUTO) return forced;
-  if ((int64_t)n * heads < kTcMinRows) return MLA_PREFILL_DECODE_KERNELS;
-  if (ctx_before < 0) return MLA_PREFILL_TENSOR_CORES;
+  const int64_t rows = (int64_t)n * heads;
+  if (rows < kTcMinRowsLong) return MLA_PREFILL_DECODE_KERNELS;
+  if (ctx_before < 0) return MLA_PREFILL_TENSOR_CORES;      // the workspace covers either path
   const int64_t keys = (int64_t)ctx_before + n;
-  return keys <= kTcMaxKeys && keys > kTcExactLen ? MLA_PREFILL_TENSOR_CORES : MLA_PREFILL_DECODE_KERNELS;
+  if (keys <= kTcExactLen || keys > kTcMaxKeys) return MLA_PREFILL_DECODE_KERNELS;
+  return rows >= kTcMinRows || keys >= kTcLongKeys ? MLA_PREFILL_TENSOR_CORES : MLA_PREFILL_DECODE_KERNELS;
 }
 
 }  // namespace

@@ -160,8 +160,11 @@ def test_prefill_path_hook(lib):
         assert lib.mla_prefill_path_taken(16384 - 8191, 8192, 64) == lib.PREFILL_DECODE_KERNELS
         assert lib.mla_prefill_path_taken(0, 200, 64) == lib.PREFILL_DECODE_KERNELS      # every row < 256 tokens
         assert lib.mla_prefill_path_taken(300, 100, 16) == lib.PREFILL_DECODE_KERNELS    # 1600 rows
+        assert lib.mla_prefill_path_taken(8192, 128, 16) == lib.PREFILL_TENSOR_CORES     # 2048 rows, long prefixes
+        assert lib.mla_prefill_path_taken(1024, 128, 16) == lib.PREFILL_DECODE_KERNELS   # 2048 rows, short prefixes
+        assert lib.mla_prefill_path_taken(0, 512, 16) == lib.PREFILL_TENSOR_CORES        # 8192 rows
         assert lib.mla_prefill_path_taken(0, 8192, 24) == -1
-        # automatic: the tensor-core size only from 8192 rows on
+        # automatic: the tensor-core size only from 2048 rows on
         assert lib.mla_prefill_workspace_bytes(100, 16) < tc_small
         assert lib.mla_prefill_workspace_bytes(8192, 64) == max(tc, dec)
         with pytest.raises(ValueError):
