@@ -273,12 +273,15 @@ __device__ __forceinline__ float warp_sum(float v) {
 // exact_core is the computation over tokens t_begin .. len - 1 (t_begin a
 // multiple of 32); with kPart it writes, instead of the normalised rows, the
 // eight heads' partial state to part[8][kPartStride]: running maximum (log2
-// domain), weight sum, then the 512 unnormalised channels.
+// domain), weight sum, then the 512 unnormalised channels.  With a table
+// (x_hat of the sequence's first tokens in fp32, [token][576], written by
+// prefill_keys_kernel) each block of tokens is read from it instead of being
+// dequantized from the pages.
 constexpr int kPartStride = 2 + kDc;
 
 template <int LF, int KF, bool kPart>
 __device__ __forceinline__ void exact_core(const DecodeParams& p, int b, int h0, int t_begin, int len, uint32_t rows,
-                                           float* sm, float* part) {
+                                           float* sm, float* part, const float* table = nullptr) {
   float* s_c = sm;                                 // [32][kCS]
   float* s_k = s_c + kChunk * kCS;                 // [32][kKS]
   float* s_q = s_k + kChunk * kKS;                 // [8][kQS]
@@ -299,7 +302,20 @@ __device__ __forceinline__ void exact_core(const DecodeParams& p, int b, int h0,
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int t0 = t_begin; t0 < len; t0 += kChunk) {
     __syncthreads();                               // the previous block's readers are done; s_q in place
-    dequant_chunk<LF, KF, kCombThreads>(p, b, t0, len, s_c, s_k, s_valid, s_page);
+    if (table) {
+      for (int i = tid; i < kChunk * (kDc + kDr) / 4; i += kCombThreads) {
+        const int t = i / ((kDc + kDr) / 4), c4 = 4 * (i % ((kDc + kDr) / 4));
+        const float4 v = *reinterpret_cast<const float4*>(table + (size_t)(t0 + t) * (kDc + kDr) + c4);
+        float* d = c4 < kDc ? s_c + t * kCS + c4 : s_k + t * kKS + c4 - kDc;
+        d[0] = v.x;
+        d[1] = v.y;
+        d[2] = v.z;
+        d[3] = v.w;
+      }
+      if (tid < kChunk) s_valid[tid] = t0 + tid < len;
+    } else {
+      dequant_chunk<LF, KF, kCombThreads>(p, b, t0, len, s_c, s_k, s_valid, s_page);
+    }
     __syncthreads();
     for (int u = 0; u < 8; u += 2) {
       const int ta = st0 + u;
@@ -732,14 +748,15 @@ __global__ void __launch_bounds__(kCombThreads, 2) combine_grouped_kernel(Decode
 // chunks of row r permuted by XOR with r mod 8 (the tensor core's 128-byte
 // swizzle).  Tokens at or past len, or on a page outside the pool, are 0.
 // mt[token] = the stored bound on |x_hat| (0 for bf16 latents, which keep no
-// bound: their fp16 rounding is exact).
+// bound: their fp16 rounding is exact).  table (if not null): x_hat of
+// tokens 0 .. kExactLen - 1 in fp32, [token][576].
 constexpr int kKeyThreads = 256;
 constexpr int kKeySmemBytes = (int)sizeof(float) * (kChunk * kCS + kChunk * kKS) + (int)sizeof(int32_t) * 2 * kChunk;
 constexpr int kTcBlockBytes = 16384;
 
 template <int LF, int KF>
 __global__ void __launch_bounds__(kKeyThreads) prefill_keys_kernel(const DecodeParams p, int len, uint8_t* kws,
-                                                                   float* mt) {
+                                                                   float* mt, float* table) {
   extern __shared__ float key_smem[];
   float* s_c = key_smem;
   float* s_k = s_c + kChunk * kCS;
@@ -758,6 +775,12 @@ __global__ void __launch_bounds__(kKeyThreads) prefill_keys_kernel(const DecodeP
       bound = reinterpret_cast<const float*>(blk + p.L.bound_off)[tid];
     }
     mt[t0 + tid] = bound;
+  }
+  if (table && t0 < kExactLen) {       // x_hat of the first tokens for the short rows' exact recomputation
+    for (int i = tid; i < kChunk * (kDc + kDr); i += kKeyThreads) {
+      const int t = i / (kDc + kDr), c = i % (kDc + kDr);
+      table[(size_t)(t0 + t) * (kDc + kDr) + c] = c < kDc ? s_c[t * kCS + c] : s_k[t * kKS + c - kDc];
+    }
   }
   constexpr int kPieces = (kDc + kDr) / 8;         // 16-byte pieces of 8 channels per token
   for (int i = tid; i < kChunk * kPieces; i += kKeyThreads) {
@@ -797,7 +820,8 @@ constexpr int kFixupBatch = kCombThreads / kShortHeads;     // items tested per 
 
 template <int LF, int KF>
 __global__ void __launch_bounds__(kCombThreads, 1) exact_fixup_kernel(const DecodeParams p, const float* risk,
-                                                                      const float* omax, SplitQueue q) {
+                                                                      const float* omax, SplitQueue q,
+                                                                      const float* table) {
   extern __shared__ float short_smem[];
   __shared__ uint32_t s_bits[kFixupBatch];
   __shared__ int s_slot;
@@ -841,7 +865,10 @@ __global__ void __launch_bounds__(kCombThreads, 1) exact_fixup_kernel(const Deco
         __syncthreads();
         if (s_slot < kSplitCap) continue;
       }
-      exact_rows<LF, KF>(p, b, h0, len, rows, short_smem);
+      if (len < kExactLen && table)
+        exact_core<LF, KF, false>(p, b, h0, 0, len, rows, short_smem, nullptr, table);
+      else
+        exact_rows<LF, KF>(p, b, h0, len, rows, short_smem);
     }
   }
 }
@@ -999,18 +1026,19 @@ mla_status allow_smem(K kernel, int bytes, int* configured) {
 }
 
 template <int LF, int KF>
-mla_status launch_prefill_keys_t(const DecodeParams& p, int len, void* kws, float* mt, cudaStream_t stream) {
+mla_status launch_prefill_keys_t(const DecodeParams& p, int len, void* kws, float* mt, float* table,
+                                 cudaStream_t stream) {
   static int configured[64] = {0};
   const mla_status st = allow_smem(prefill_keys_kernel<LF, KF>, kKeySmemBytes, configured);
   if (st != MLA_OK) return st;
   const int blocks = (len + 127) / 128 * 4;
   return cuda_status(launch_pdl(prefill_keys_kernel<LF, KF>, dim3(blocks), dim3(kKeyThreads), kKeySmemBytes, stream,
-                                p, len, (uint8_t*)kws, mt));
+                                p, len, (uint8_t*)kws, mt, table));
 }
 
 template <int LF, int KF>
 mla_status launch_exact_fixup_t(const DecodeParams& p, const float* risk, const float* omax, const SplitQueue& q,
-                                cudaStream_t stream) {
+                                const float* table, cudaStream_t stream) {
   static int configured[64] = {0}, configured_s[64] = {0};
   mla_status st = allow_smem(exact_fixup_kernel<LF, KF>, kShortSmemBytes, configured);
   if (st != MLA_OK) return st;
@@ -1020,7 +1048,7 @@ mla_status launch_exact_fixup_t(const DecodeParams& p, const float* risk, const 
   const int sms = device_sm_count();
   const int cap = 2 * (sms > 0 ? sms : 1);
   st = cuda_status(launch_pdl(exact_fixup_kernel<LF, KF>, dim3(items < cap ? items : cap), dim3(kCombThreads),
-                              kShortSmemBytes, stream, p, risk, omax, q));
+                              kShortSmemBytes, stream, p, risk, omax, q, table));
   if (st != MLA_OK) return st;
   return cuda_status(launch_pdl(exact_split_kernel<LF, KF>, dim3(cap), dim3(kCombThreads), kShortSmemBytes, stream,
                                 p, q));
@@ -1039,18 +1067,19 @@ mla_status launch_exact_fixup_t(const DecodeParams& p, const float* risk, const 
   X(MLA_FMT_INT8_TOKEN, MLA_FMT_INT8_SYM) X(MLA_FMT_INT8_OUTLIER, MLA_FMT_BF16)                            \
   X(MLA_FMT_INT8_OUTLIER, MLA_FMT_INT8_SYM)
 
-mla_status launch_prefill_keys(const DecodeParams& p, int len, void* kws, float* mt, cudaStream_t stream) {
+mla_status launch_prefill_keys(const DecodeParams& p, int len, void* kws, float* mt, float* table,
+                               cudaStream_t stream) {
 #define MLA_KEYS_CASE(A, K) \
-  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_prefill_keys_t<A, K>(p, len, kws, mt, stream);
+  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_prefill_keys_t<A, K>(p, len, kws, mt, table, stream);
   MLA_FORMAT_PAIRS(MLA_KEYS_CASE)
 #undef MLA_KEYS_CASE
   return MLA_ERR_UNSUPPORTED;
 }
 
 mla_status launch_exact_fixup(const DecodeParams& p, const float* risk, const float* omax, const SplitQueue& q,
-                              cudaStream_t stream) {
+                              const float* table, cudaStream_t stream) {
 #define MLA_FIXUP_CASE(A, K) \
-  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_exact_fixup_t<A, K>(p, risk, omax, q, stream);
+  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_exact_fixup_t<A, K>(p, risk, omax, q, table, stream);
   MLA_FORMAT_PAIRS(MLA_FIXUP_CASE)
 #undef MLA_FIXUP_CASE
   return MLA_ERR_UNSUPPORTED;

@@ -269,8 +269,11 @@ mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream);   // d
 // Tensor-core prefill support (decode.cu): the key tiles of tokens 0 .. len - 1
 // of block-table row 0 (fp16 hi / lo pairs, 128 tokens x 9 channel blocks x
 // 2 x 16 KB per tile, swizzled) with the tokens' bounds mt[len rounded up to
-// 128]; and the exact fp32 recomputation of the rows that need it.
-mla_status launch_prefill_keys(const DecodeParams& p, int len, void* kws, float* mt, cudaStream_t stream);
+// 128] and, if table is not null, x_hat of tokens 0 .. 255 in fp32
+// ([token][576]); and the exact fp32 recomputation of the rows that need it
+// (short rows read their tokens from the table).
+mla_status launch_prefill_keys(const DecodeParams& p, int len, void* kws, float* mt, float* table,
+                               cudaStream_t stream);
 // The long rows the fixup hands to the split recomputation: *count items
 // (b, h0, row mask, length), each recomputed over kSplitParts token ranges
 // whose partial states (8 heads x (max, sum, 512 channels)) go to parts;
@@ -299,7 +302,7 @@ __host__ __device__ inline SplitQueue carve_split_queue(void* base) {
   return q;
 }
 mla_status launch_exact_fixup(const DecodeParams& p, const float* risk, const float* omax, const SplitQueue& q,
-                              cudaStream_t stream);
+                              const float* table, cudaStream_t stream);
 
 // Tensor-core prefill (prefill_tc.cu).  A tile holds 128 rows (queries or
 // keys) x 9 channel blocks x (hi, lo) x 16 KB.

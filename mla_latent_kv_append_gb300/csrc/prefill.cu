@@ -71,6 +71,7 @@ struct TcWorkspace {
   float* risk;
   float* omax;
   SplitQueue queue;
+  float* table;          // x_hat of positions 0 .. 255, fp32 [256][576]
 };
 
 int64_t tc_row_tiles(int64_t rows) { return (rows + 127) / 128; }
@@ -78,13 +79,13 @@ int64_t tc_row_tiles(int64_t rows) { return (rows + 127) / 128; }
 int64_t tc_workspace_bytes(int n, int heads, TcWorkspace* w, void* base) {
   const int64_t s = n < kTcSlice ? (n > 0 ? n : 1) : kTcSlice;
   const int64_t rows = s * heads;
-  const int64_t sizes[7] = {(int64_t)(kTcMaxKeys / 128) * kTcTileBytes, tc_row_tiles(rows) * kTcTileBytes,
+  const int64_t sizes[8] = {(int64_t)(kTcMaxKeys / 128) * kTcTileBytes, tc_row_tiles(rows) * kTcTileBytes,
                             align256((int64_t)kTcMaxKeys * 4), align256(s * 4), align256(rows * 4),
-                            align256(rows * 8), split_queue_bytes()};
+                            align256(rows * 8), split_queue_bytes(), (int64_t)kTcExactLen * (kDc + kDr) * 4};
   int64_t off = 0;
   char* b = (char*)base;
-  void* ptrs[7];
-  for (int i = 0; i < 7; ++i) {
+  void* ptrs[8];
+  for (int i = 0; i < 8; ++i) {
     ptrs[i] = b ? b + off : nullptr;
     off += sizes[i];
   }
@@ -96,6 +97,7 @@ int64_t tc_workspace_bytes(int n, int heads, TcWorkspace* w, void* base) {
     w->risk = (float*)ptrs[4];
     w->omax = (float*)ptrs[5];
     w->queue = carve_split_queue(ptrs[6] ? ptrs[6] : (void*)nullptr);
+    w->table = (float*)ptrs[7];
   }
   return off;
 }
@@ -187,7 +189,9 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
     p.o = nullptr;
     p.dev_err = dev_err;
     const int keys = ctx_before + n;
-    mla_status ks = launch_prefill_keys(p, keys, w.kws, w.mt, st);
+    // the short rows' table is needed only when some query sees < 256 positions
+    float* table = ctx_before + 1 < kTcExactLen ? w.table : nullptr;
+    mla_status ks = launch_prefill_keys(p, keys, w.kws, w.mt, table, st);
     if (ks != MLA_OK) return ks;
     for (int i0 = 0; i0 < n; i0 += kTcSlice) {
       const int s = n - i0 < kTcSlice ? n - i0 : kTcSlice;
@@ -229,7 +233,7 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
       f.B = s;
       f.o_lat = ol;
       f.lse = lo;
-      ks = launch_exact_fixup(f, w.risk, w.omax, w.queue, st);
+      ks = launch_exact_fixup(f, w.risk, w.omax, w.queue, table, st);
       if (ks != MLA_OK) return ks;
     }
     return MLA_OK;

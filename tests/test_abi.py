@@ -148,7 +148,7 @@ def test_prefill_path_hook(lib):
         rows = 4096 * 64
         # the queue of long rows for the split exact recomputation: counters,
         # 64 items, 64 x 32 ranges x 8 heads x (2 + 512) floats
-        queue = 512 + 1024 + 64 * 32 * 8 * 514 * 4
+        queue = 512 + 1024 + 64 * 32 * 8 * 514 * 4 + 256 * 576 * 4    # + x_hat of the first 256 positions
         tc = 128 * tile + rows // 128 * tile + 16384 * 4 + 4096 * 4 + rows * 4 + rows * 8 + queue
         assert lib.mla_prefill_workspace_bytes(8192, 64) == max(tc, dec)
         # a 100-token chunk at 16 heads: one 1600-row slice, 13 row tiles
