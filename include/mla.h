@@ -376,19 +376,19 @@ mla_status mla_decode_absorbed_noalloc(const mla_cache_layer* cache, const float
  * prefill path setting (0 for invalid arguments).  Bounded in n: queries are
  * processed in slices of 2048 (decode kernels) or 4096 (tensor cores: 288 KB
  * of query tiles per 128 rows, ~600 MB at 64 heads); the tensor-core path
- * adds the key tiles of up to 16384 positions (~38 MB).
+ * adds the key tiles of up to 65536 positions (~151 MB).
  */
 size_t mla_prefill_workspace_bytes(int32_t n, int32_t heads);
 
 /*
  * Prefill implementations (mla_set_prefill_path):
  *   MLA_PREFILL_AUTO           tensor cores when 256 < ctx_before + n <=
- *                              16384 and either n * heads >= 8192, or
+ *                              65536 and either n * heads >= 8192, or
  *                              n * heads >= 2048 and ctx_before + n >= 4096;
  *                              else the decode kernels (the default)
  *   MLA_PREFILL_DECODE_KERNELS always the split-K decode kernels
  *   MLA_PREFILL_TENSOR_CORES   always tensor cores; a call with
- *                              ctx_before + n > 16384 returns
+ *                              ctx_before + n > 65536 returns
  *                              MLA_ERR_UNSUPPORTED
  * Both compute the same attention within the same bound (§ prefill below).
  */

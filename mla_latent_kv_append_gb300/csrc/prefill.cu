@@ -50,7 +50,7 @@ bool aligned_to(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) ==
 
 // ---- tensor-core path
 constexpr int kTcSlice = 4096;           // query tokens per launch (1024: +4 % time; 8192: no gain)
-constexpr int kTcMaxKeys = 16384;        // positions the key tiles hold
+constexpr int kTcMaxKeys = 65536;        // positions the key tiles hold (151 MB)
 // The automatic choice (measured on GB300 against the decode kernels, INT8,
 // 16 and 64 heads, 0 to 8192 positions before the chunk): the tensor cores
 // from 8192 rows (n x H) on, or from 2048 rows once the chunk's prefixes

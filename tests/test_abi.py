@@ -138,7 +138,7 @@ def test_invalid_arguments_rejected_on_host(lib):
 def test_prefill_path_hook(lib):
     """The prefill path setting: set, read back, reject an unknown value,
     and the workspace size it implies (the tensor-core path adds the key
-    tiles of 16384 positions and the query tiles of a 4096-token slice, 288
+    tiles of 65536 positions and the query tiles of a 4096-token slice, 288
     KB per 128 rows, to per-row check figures)."""
     prev = lib.mla_set_prefill_path(lib.PREFILL_DECODE_KERNELS)
     try:
@@ -149,15 +149,15 @@ def test_prefill_path_hook(lib):
         # the queue of long rows for the split exact recomputation: counters,
         # 64 items, 64 x 32 ranges x 8 heads x (2 + 512) floats
         queue = 512 + 1024 + 64 * 32 * 8 * 514 * 4 + 256 * 576 * 4    # + x_hat of the first 256 positions
-        tc = 128 * tile + rows // 128 * tile + 16384 * 4 + 4096 * 4 + rows * 4 + rows * 8 + queue
+        tc = 512 * tile + rows // 128 * tile + 65536 * 4 + 4096 * 4 + rows * 4 + rows * 8 + queue
         assert lib.mla_prefill_workspace_bytes(8192, 64) == max(tc, dec)
         # a 100-token chunk at 16 heads: one 1600-row slice, 13 row tiles
-        tc_small = 128 * tile + 13 * tile + 16384 * 4 + 512 + 6400 + 12800 + queue
+        tc_small = 512 * tile + 13 * tile + 65536 * 4 + 512 + 6400 + 12800 + queue
         assert lib.mla_prefill_workspace_bytes(100, 16) == max(tc_small, lib.mla_prefill_workspace_bytes(1, 16))
         assert lib.mla_prefill_path_taken(10**6, 8192, 64) == lib.PREFILL_TENSOR_CORES
         assert lib.mla_set_prefill_path(lib.PREFILL_AUTO) == lib.PREFILL_TENSOR_CORES
         assert lib.mla_prefill_path_taken(0, 8192, 64) == lib.PREFILL_TENSOR_CORES
-        assert lib.mla_prefill_path_taken(16384 - 8191, 8192, 64) == lib.PREFILL_DECODE_KERNELS
+        assert lib.mla_prefill_path_taken(65536 - 8191, 8192, 64) == lib.PREFILL_DECODE_KERNELS
         assert lib.mla_prefill_path_taken(0, 200, 64) == lib.PREFILL_DECODE_KERNELS      # every row < 256 tokens
         assert lib.mla_prefill_path_taken(300, 100, 16) == lib.PREFILL_DECODE_KERNELS    # 1600 rows
         assert lib.mla_prefill_path_taken(8192, 128, 16) == lib.PREFILL_TENSOR_CORES     # 2048 rows, long prefixes

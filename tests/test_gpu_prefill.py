@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True, params=["decode_kernels", "auto"])
 def prefill_path(request):
     """Every test runs on the decode-kernel path and on the automatic choice
-    (the tensor cores for prefixes of 257 to 16384 tokens and 8192 rows or
+    (the tensor cores for prefixes of 257 to 65536 tokens and 8192 rows or
     more, or 2048 rows or more once the prefixes reach 4096 tokens)."""
     prev = mla.mla_set_prefill_path(mla.PREFILL_DECODE_KERNELS if request.param == "decode_kernels"
                                     else mla.PREFILL_AUTO)

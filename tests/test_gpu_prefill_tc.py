@@ -52,16 +52,16 @@ def test_tc_prefill_slices():
 
 
 def test_tc_prefill_too_long_is_unsupported():
-    """The key tiles hold 16384 positions: a longer prefix is refused
+    """The key tiles hold 65536 positions: a longer prefix is refused
     before anything is launched."""
     import torch
     ch = Chunk(mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, 0, 64, 16, seed=98)
-    bt = torch.zeros(300, dtype=torch.int32, device="cuda")
+    bt = torch.zeros(1100, dtype=torch.int32, device="cuda")
     q_lat = torch.zeros((64, 16, 512), dtype=torch.float32, device="cuda")
     ws = torch.empty(mla.mla_prefill_workspace_bytes(64, 16), dtype=torch.uint8, device="cuda")
     o_lat = torch.empty((64, 16, 512), dtype=torch.float32, device="cuda")
     with pytest.raises(RuntimeError, match="unsupported"):
-        mla.mla_prefill_absorbed(ch.cache, q_lat, ch.q_pe, bt, 16384 - 63, ws, o_lat)
+        mla.mla_prefill_absorbed(ch.cache, q_lat, ch.q_pe, bt, 65536 - 63, ws, o_lat)
 
 
 @pytest.mark.parametrize("lf", [mla.FMT_INT8_SYM, mla.FMT_INT4_ASYM], ids=["int8", "int4"])
@@ -146,8 +146,8 @@ def test_tc_prefill_zero_wait_limit_gives_up_cleanly():
 
 
 def test_tc_prefill_at_the_key_limit():
-    """Prefixes that end exactly at the key tiles' 16384 positions (all 128
+    """Prefixes that end exactly at the key tiles' 65536 positions (all 512
     key tiles, the last query's row tile sweeping every one): sampled rows,
     the last query included."""
-    ch = Chunk(mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM, 16384 - 40, 40, 16, seed=100)
+    ch = Chunk(mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM, 65536 - 40, 40, 16, seed=100)
     check(ch, [0, 1, 17, 38, 39])
