@@ -11,7 +11,7 @@ import pytest
 
 import mla_latent_kv_append_gb300 as mla
 from tests._helpers import FMT_NAME
-from tests.test_gpu_prefill import FORMATS, Chunk, check
+from tests.test_gpu_prefill import Chunk, check
 
 pytestmark = pytest.mark.gpu
 
@@ -23,7 +23,15 @@ def tensor_core_path():
     mla.mla_set_prefill_path(prev)
 
 
-@pytest.mark.parametrize("lf,kf", FORMATS, ids=["%s-%s" % (FMT_NAME[a], FMT_NAME[b]) for a, b in FORMATS])
+# every (latent, k_pe) pair the library supports: the key pass is compiled per pair
+ALL_PAIRS = ([(lf, kf) for lf in (mla.FMT_BF16, mla.FMT_INT8_SYM, mla.FMT_INT4_ASYM, mla.FMT_INT4_SYM)
+              for kf in (mla.FMT_BF16, mla.FMT_INT8_SYM, mla.FMT_INT4_SYM)] +
+             [(lf, mla.FMT_INT8_SYM) for lf in (mla.FMT_INT8_G8, mla.FMT_INT8_G32, mla.FMT_INT8_G64,
+                                                mla.FMT_INT8_TOKEN)] +
+             [(mla.FMT_INT8_OUTLIER, mla.FMT_BF16), (mla.FMT_INT8_OUTLIER, mla.FMT_INT8_SYM)])
+
+
+@pytest.mark.parametrize("lf,kf", ALL_PAIRS, ids=["%s-%s" % (FMT_NAME[a], FMT_NAME[b]) for a, b in ALL_PAIRS])
 def test_tc_prefill_formats(lf, kf):
     """100 queries after 260 cached tokens (prefixes 261 .. 360: three key
     tiles, the causal edge inside the third), every query row."""
