@@ -159,3 +159,22 @@ def test_tc_prefill_at_the_key_limit():
     the last query included."""
     ch = Chunk(mla.FMT_INT4_ASYM, mla.FMT_INT8_SYM, 65536 - 40, 40, 16, seed=100)
     check(ch, [0, 1, 17, 38, 39])
+
+
+def test_tc_prefill_bad_page_is_flagged():
+    """A page id outside the pool in the sequence's block table: the key pass
+    reports MLA_DEVERR_PAGE and reads that page's tokens as 0; the call
+    completes and every output stays finite."""
+    import torch
+    ch = Chunk(mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, 300, 200, 16, seed=101)
+    ch.block_table[2] = ch.cache.num_pages + 5
+    q_lat = torch.empty((200, 16, 512), dtype=torch.float32, device="cuda")
+    mla.mla_q_absorb(ch.q_nope, ch.w_uk, q_lat)
+    ws = torch.empty(mla.mla_prefill_workspace_bytes(200, 16), dtype=torch.uint8, device="cuda")
+    o_lat = torch.full((200, 16, 512), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((200, 16), float("nan"), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.mla_prefill_absorbed(ch.cache, q_lat, ch.q_pe, ch.block_table, 300, ws, o_lat, lse, err)
+    torch.cuda.synchronize()
+    assert err.item() == mla.DEVERR_PAGE
+    assert torch.isfinite(o_lat).all() and torch.isfinite(lse).all()
