@@ -273,15 +273,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 // exact_core is the computation over tokens t_begin .. len - 1 (t_begin a
 // multiple of 32); with kPart it writes, instead of the normalised rows, the
 // eight heads' partial state to part[8][kPartStride]: running maximum (log2
-// domain), weight sum, then the 512 unnormalised channels.  With a table
-// (x_hat of the sequence's first tokens in fp32, [token][576], written by
-// prefill_keys_kernel) each block of tokens is read from it instead of being
-// dequantized from the pages.
+// domain), weight sum, then the 512 unnormalised channels.
 constexpr int kPartStride = 2 + kDc;
 
 template <int LF, int KF, bool kPart>
 __device__ __forceinline__ void exact_core(const DecodeParams& p, int b, int h0, int t_begin, int len, uint32_t rows,
-                                           float* sm, float* part, const float* table = nullptr) {
+                                           float* sm, float* part) {
   float* s_c = sm;                                 // [32][kCS]
   float* s_k = s_c + kChunk * kCS;                 // [32][kKS]
   float* s_q = s_k + kChunk * kKS;                 // [8][kQS]
@@ -302,20 +299,7 @@ __device__ __forceinline__ void exact_core(const DecodeParams& p, int b, int h0,
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int t0 = t_begin; t0 < len; t0 += kChunk) {
     __syncthreads();                               // the previous block's readers are done; s_q in place
-    if (table) {
-      for (int i = tid; i < kChunk * (kDc + kDr) / 4; i += kCombThreads) {
-        const int t = i / ((kDc + kDr) / 4), c4 = 4 * (i % ((kDc + kDr) / 4));
-        const float4 v = *reinterpret_cast<const float4*>(table + (size_t)(t0 + t) * (kDc + kDr) + c4);
-        float* d = c4 < kDc ? s_c + t * kCS + c4 : s_k + t * kKS + c4 - kDc;
-        d[0] = v.x;
-        d[1] = v.y;
-        d[2] = v.z;
-        d[3] = v.w;
-      }
-      if (tid < kChunk) s_valid[tid] = t0 + tid < len;
-    } else {
-      dequant_chunk<LF, KF, kCombThreads>(p, b, t0, len, s_c, s_k, s_valid, s_page);
-    }
+    dequant_chunk<LF, KF, kCombThreads>(p, b, t0, len, s_c, s_k, s_valid, s_page);
     __syncthreads();
     for (int u = 0; u < 8; u += 2) {
       const int ta = st0 + u;
@@ -812,7 +796,8 @@ __global__ void __launch_bounds__(kKeyThreads) prefill_keys_kernel(const DecodeP
 // M_t)^2), omax = |o_lat|_inf of each 256-channel half).  Block x takes the
 // (row, 8-head group) items x, x + G, x + 2G, .. (G = gridDim.x), 128 at a
 // time: its threads test the 128 items' 8 heads at once, then the block
-// recomputes the short items that need it, one after the other, and queues
+// recomputes the short items (unless skip_short: short_rows_kernel in
+// prefill_tc.cu takes them) one after the other, and queues
 // the long ones (up to kSplitCap per launch; past that it recomputes them
 // itself) for exact_split_kernel, which spreads each over many blocks.  The
 // stride spreads the short rows at the start of a chunk over every block.
@@ -821,7 +806,7 @@ constexpr int kFixupBatch = kCombThreads / kShortHeads;     // items tested per 
 template <int LF, int KF>
 __global__ void __launch_bounds__(kCombThreads, 1) exact_fixup_kernel(const DecodeParams p, const float* risk,
                                                                       const float* omax, SplitQueue q,
-                                                                      const float* table) {
+                                                                      int skip_short) {
   extern __shared__ float short_smem[];
   __shared__ uint32_t s_bits[kFixupBatch];
   __shared__ int s_slot;
@@ -836,7 +821,7 @@ __global__ void __launch_bounds__(kCombThreads, 1) exact_fixup_kernel(const Deco
       const int b = it / groups, j = threadIdx.x % kShortHeads;
       const int len = checked_len(p, b, false);
       if (len < kExactLen) {
-        need = len > 0;
+        need = !skip_short && len > 0;
       } else if (kRiskFmt<LF>) {
         const size_t r = (size_t)b * p.H + (it % groups) * kShortHeads + j;
         need = risk[r] > kRiskRatio * fmaxf(omax[2 * r], omax[2 * r + 1]);
@@ -865,10 +850,7 @@ __global__ void __launch_bounds__(kCombThreads, 1) exact_fixup_kernel(const Deco
         __syncthreads();
         if (s_slot < kSplitCap) continue;
       }
-      if (len < kExactLen && table)
-        exact_core<LF, KF, false>(p, b, h0, 0, len, rows, short_smem, nullptr, table);
-      else
-        exact_rows<LF, KF>(p, b, h0, len, rows, short_smem);
+      exact_rows<LF, KF>(p, b, h0, len, rows, short_smem);
     }
   }
 }
@@ -1038,7 +1020,7 @@ mla_status launch_prefill_keys_t(const DecodeParams& p, int len, void* kws, floa
 
 template <int LF, int KF>
 mla_status launch_exact_fixup_t(const DecodeParams& p, const float* risk, const float* omax, const SplitQueue& q,
-                                const float* table, cudaStream_t stream) {
+                                int skip_short, cudaStream_t stream) {
   static int configured[64] = {0}, configured_s[64] = {0};
   mla_status st = allow_smem(exact_fixup_kernel<LF, KF>, kShortSmemBytes, configured);
   if (st != MLA_OK) return st;
@@ -1048,7 +1030,7 @@ mla_status launch_exact_fixup_t(const DecodeParams& p, const float* risk, const 
   const int sms = device_sm_count();
   const int cap = 2 * (sms > 0 ? sms : 1);
   st = cuda_status(launch_pdl(exact_fixup_kernel<LF, KF>, dim3(items < cap ? items : cap), dim3(kCombThreads),
-                              kShortSmemBytes, stream, p, risk, omax, q, table));
+                              kShortSmemBytes, stream, p, risk, omax, q, skip_short));
   if (st != MLA_OK) return st;
   return cuda_status(launch_pdl(exact_split_kernel<LF, KF>, dim3(cap), dim3(kCombThreads), kShortSmemBytes, stream,
                                 p, q));
@@ -1077,9 +1059,9 @@ mla_status launch_prefill_keys(const DecodeParams& p, int len, void* kws, float*
 }
 
 mla_status launch_exact_fixup(const DecodeParams& p, const float* risk, const float* omax, const SplitQueue& q,
-                              const float* table, cudaStream_t stream) {
+                              int skip_short, cudaStream_t stream) {
 #define MLA_FIXUP_CASE(A, K) \
-  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_exact_fixup_t<A, K>(p, risk, omax, q, table, stream);
+  if (p.latent_fmt == A && p.kpe_fmt == K) return launch_exact_fixup_t<A, K>(p, risk, omax, q, skip_short, stream);
   MLA_FORMAT_PAIRS(MLA_FIXUP_CASE)
 #undef MLA_FIXUP_CASE
   return MLA_ERR_UNSUPPORTED;

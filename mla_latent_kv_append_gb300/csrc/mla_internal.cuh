@@ -271,7 +271,7 @@ mla_status launch_decode_mma(const DecodeParams& p, cudaStream_t stream);   // d
 // 2 x 16 KB per tile, swizzled) with the tokens' bounds mt[len rounded up to
 // 128] and, if table is not null, x_hat of tokens 0 .. 255 in fp32
 // ([token][576]); and the exact fp32 recomputation of the rows that need it
-// (short rows read their tokens from the table).
+// (with skip_short, not the rows shorter than 256 positions).
 mla_status launch_prefill_keys(const DecodeParams& p, int len, void* kws, float* mt, float* table,
                                cudaStream_t stream);
 // The long rows the fixup hands to the split recomputation: *count items
@@ -302,7 +302,7 @@ __host__ __device__ inline SplitQueue carve_split_queue(void* base) {
   return q;
 }
 mla_status launch_exact_fixup(const DecodeParams& p, const float* risk, const float* omax, const SplitQueue& q,
-                              const float* table, cudaStream_t stream);
+                              int skip_short, cudaStream_t stream);
 
 // Tensor-core prefill (prefill_tc.cu).  A tile holds 128 rows (queries or
 // keys) x 9 channel blocks x (hi, lo) x 16 KB.
@@ -327,5 +327,9 @@ struct TcParams {
 mla_status launch_q_split(const float* q_lat, const uint16_t* q_pe, int R, int n_rt, uint8_t* qws,
                           cudaStream_t stream);
 mla_status launch_prefill_tc(const TcParams& p, cudaStream_t stream);
+// The exact fp32 attention of query tokens 0 .. n_short - 1 of a slice (their
+// positions qpos0 + i all below 255), every head, from the fp32 x_hat table.
+mla_status launch_short_rows(const float* table, const float* q_lat, const uint16_t* q_pe, int H, int n_short,
+                             int qpos0, float scale_log2, float* o_lat, float* lse, cudaStream_t stream);
 
 }  // namespace mla

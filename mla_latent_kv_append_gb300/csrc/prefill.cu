@@ -233,8 +233,15 @@ mla_status mla_prefill_absorbed(const mla_cache_layer* cache, const float* q_lat
       f.B = s;
       f.o_lat = ol;
       f.lse = lo;
-      ks = launch_exact_fixup(f, w.risk, w.omax, w.queue, table, st);
+      ks = launch_exact_fixup(f, w.risk, w.omax, w.queue, table != nullptr, st);
       if (ks != MLA_OK) return ks;
+      // the slice's rows below 256 positions: exact, from the x_hat table
+      const int n_short = table ? (kTcExactLen - 1 - (ctx_before + i0) < s ? kTcExactLen - 1 - (ctx_before + i0) : s)
+                                : 0;
+      if (n_short > 0) {
+        ks = launch_short_rows(table, ql, qp, heads, n_short, ctx_before + i0, p.scale_log2, ol, lo, st);
+        if (ks != MLA_OK) return ks;
+      }
     }
     return MLA_OK;
   }

@@ -538,6 +538,137 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(const TcParam
   }
 }
 
+// short_rows_kernel: grid (ceil(n_short / 4), H / 8), block kSRThreads.
+// The exact fp32 attention of the query rows that see fewer than 256
+// positions (query tokens i < n_short of the slice, position qpos0 + i):
+// the rule every prefill and decode path shares for short rows, where the
+// fp16 roundings of P and V do not average out.  CTA (x, y) takes tokens
+// 4x .. 4x + 3 and heads 8y .. 8y + 7 (32 rows); the positions' x_hat come
+// from the fp32 table the key pass wrote ([256][576]), 32 at a time.  Warp w
+// owns rows 2w, 2w + 1: lane k scores position k of the block for both
+// (float4 loads, consecutive rows of the table tile: conflict-free with the
+// padded stride), the warp runs the two rows' online softmax by shuffles
+// (log2 domain), and lane L accumulates channels 4L + 128m (m = 0..3) of O
+// for both rows, so a float4 load of a position's channels covers 512
+// contiguous bytes.
+constexpr int kSRThreads = 512;
+constexpr int kSRTok = 4, kSRHeads = 8, kSRRows = kSRTok * kSRHeads, kSRKeys = 32;
+constexpr int kSRStride = kDc + kDr + 4;        // padded row (floats): stride / 4 odd
+constexpr int kSRSmem = (int)sizeof(float) * (kSRRows + kSRKeys) * kSRStride;
+static_assert(kSRThreads / 32 * 2 == kSRRows, "a warp per row pair");
+
+__global__ void __launch_bounds__(kSRThreads, 1) short_rows_kernel(const float* table, const float* q_lat,
+                                                                   const uint16_t* q_pe, int H, int n_short,
+                                                                   int qpos0, float scale_log2, float* o_lat,
+                                                                   float* lse) {
+  extern __shared__ float sr_smem[];
+  float* sQ = sr_smem;                              // [32 rows][kSRStride]
+  float* sX = sQ + kSRRows * kSRStride;             // [32 positions][kSRStride]
+  pdl_launch_dependents();
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = blockIdx.x * kSRTok, h0 = blockIdx.y * kSRHeads;
+  // row r = (token i0 + r / 8, head h0 + r % 8)
+  for (int idx = tid; idx < kSRRows * (kDc + kDr); idx += kSRThreads) {
+    const int r = idx / (kDc + kDr), c = idx % (kDc + kDr);
+    const int i = min(i0 + r / kSRHeads, n_short - 1), h = h0 + r % kSRHeads;
+    const size_t row = (size_t)i * H + h;
+    sQ[r * kSRStride + c] = c < kDc ? q_lat[row * kDc + c] : bf16f(q_pe[row * kDr + c - kDc]);
+  }
+  const int maxlen = qpos0 + min(i0 + kSRTok, n_short);    // positions the CTA's longest row sees (< 256)
+  const int r0 = 2 * warp;                                  // this warp's rows r0, r0 + 1
+  const int len0 = qpos0 + min(i0 + r0 / kSRHeads, n_short - 1) + 1;
+  const int len1 = qpos0 + min(i0 + (r0 + 1) / kSRHeads, n_short - 1) + 1;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  float acc0[16], acc1[16];
+#pragma unroll
+  for (int v = 0; v < 16; ++v) acc0[v] = acc1[v] = 0.f;
+  for (int t0 = 0; t0 < maxlen; t0 += kSRKeys) {
+    __syncthreads();                                // the previous block's readers of sX are done
+    for (int idx = tid; idx < kSRKeys * (kDc + kDr) / 4; idx += kSRThreads) {
+      const int k = idx / ((kDc + kDr) / 4), c4 = 4 * (idx % ((kDc + kDr) / 4));
+      *reinterpret_cast<float4*>(sX + k * kSRStride + c4) =
+          *reinterpret_cast<const float4*>(table + (size_t)(t0 + k) * (kDc + kDr) + c4);
+    }
+    __syncthreads();
+    // scores of position t0 + lane for rows r0, r0 + 1
+    float a = 0.f, b = 0.f;
+    const float* q0 = sQ + r0 * kSRStride;
+    const float* xk = sX + lane * kSRStride;
+#pragma unroll 4
+    for (int c = 0; c < kDc + kDr; c += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(xk + c);
+      const float4 u = *reinterpret_cast<const float4*>(q0 + c);
+      const float4 w = *reinterpret_cast<const float4*>(q0 + kSRStride + c);
+      a = fmaf(u.x, x.x, fmaf(u.y, x.y, fmaf(u.z, x.z, fmaf(u.w, x.w, a))));
+      b = fmaf(w.x, x.x, fmaf(w.y, x.y, fmaf(w.z, x.z, fmaf(w.w, x.w, b))));
+    }
+    const int k = t0 + lane;
+    a = k < len0 ? a * scale_log2 : -INFINITY;
+    b = k < len1 ? b * scale_log2 : -INFINITY;
+    float ma = a, mb = b;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, off));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, off));
+    }
+    const float n0 = fmaxf(m0, ma), n1 = fmaxf(m1, mb);      // position 0 is always visible: finite
+    const float al0 = exp2f(m0 - n0), al1 = exp2f(m1 - n1);
+    const float pa = exp2f(a - n0), pb = exp2f(b - n1);
+    float sa = pa, sb = pb;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) {
+      sa += __shfl_xor_sync(0xffffffffu, sa, off);
+      sb += __shfl_xor_sync(0xffffffffu, sb, off);
+    }
+    l0 = fmaf(l0, al0, sa);
+    l1 = fmaf(l1, al1, sb);
+    m0 = n0;
+    m1 = n1;
+#pragma unroll
+    for (int v = 0; v < 16; ++v) {
+      acc0[v] *= al0;
+      acc1[v] *= al1;
+    }
+    // O += P X: position j's weights come from lane j by shuffle
+    const int kend = min(kSRKeys, maxlen - t0);
+    for (int j = 0; j < kend; ++j) {
+      const float w0 = __shfl_sync(0xffffffffu, pa, j), w1 = __shfl_sync(0xffffffffu, pb, j);
+      const float* xr = sX + j * kSRStride + 4 * lane;
+#pragma unroll
+      for (int mq = 0; mq < 4; ++mq) {
+        const float4 x = *reinterpret_cast<const float4*>(xr + 128 * mq);
+        acc0[4 * mq] = fmaf(w0, x.x, acc0[4 * mq]);
+        acc0[4 * mq + 1] = fmaf(w0, x.y, acc0[4 * mq + 1]);
+        acc0[4 * mq + 2] = fmaf(w0, x.z, acc0[4 * mq + 2]);
+        acc0[4 * mq + 3] = fmaf(w0, x.w, acc0[4 * mq + 3]);
+        acc1[4 * mq] = fmaf(w1, x.x, acc1[4 * mq]);
+        acc1[4 * mq + 1] = fmaf(w1, x.y, acc1[4 * mq + 1]);
+        acc1[4 * mq + 2] = fmaf(w1, x.z, acc1[4 * mq + 2]);
+        acc1[4 * mq + 3] = fmaf(w1, x.w, acc1[4 * mq + 3]);
+      }
+    }
+  }
+  const int ia = i0 + r0 / kSRHeads, ib = i0 + (r0 + 1) / kSRHeads;
+  const int ha = h0 + r0 % kSRHeads, hb = h0 + (r0 + 1) % kSRHeads;
+  if (lane == 0 && lse) {
+    if (ia < n_short) lse[(size_t)ia * H + ha] = (m0 + log2f(l0)) * 0.69314718055994531f;
+    if (ib < n_short) lse[(size_t)ib * H + hb] = (m1 + log2f(l1)) * 0.69314718055994531f;
+  }
+  const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+#pragma unroll
+  for (int mq = 0; mq < 4; ++mq) {
+    if (ia < n_short)
+      *reinterpret_cast<float4*>(o_lat + ((size_t)ia * H + ha) * kDc + 4 * lane + 128 * mq) =
+          make_float4(acc0[4 * mq] * inv0, acc0[4 * mq + 1] * inv0, acc0[4 * mq + 2] * inv0,
+                      acc0[4 * mq + 3] * inv0);
+    if (ib < n_short)
+      *reinterpret_cast<float4*>(o_lat + ((size_t)ib * H + hb) * kDc + 4 * lane + 128 * mq) =
+          make_float4(acc1[4 * mq] * inv1, acc1[4 * mq + 1] * inv1, acc1[4 * mq + 2] * inv1,
+                      acc1[4 * mq + 3] * inv1);
+  }
+}
+
 // Raises the kernels' shared-memory limit once per device.
 mla_status tc_configure() {
   static int configured[64] = {0};
@@ -558,6 +689,22 @@ mla_status launch_q_split(const float* q_lat, const uint16_t* q_pe, int R, int n
   const int64_t blocks = (pieces + 255) / 256;
   const int grid = (int)(blocks < 8 * 152 ? blocks : 8 * 152);
   return cuda_status(launch_pdl(q_split_kernel, dim3(grid), dim3(256), 0, stream, q_lat, q_pe, R, n_rt, qws));
+}
+
+mla_status launch_short_rows(const float* table, const float* q_lat, const uint16_t* q_pe, int H, int n_short,
+                             int qpos0, float scale_log2, float* o_lat, float* lse, cudaStream_t stream) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    const mla_status st =
+        cuda_status(cudaFuncSetAttribute(short_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSRSmem));
+    if (st != MLA_OK) return st;
+    if (dev >= 0 && dev < 64) configured[dev] = 1;
+  }
+  return cuda_status(launch_pdl(short_rows_kernel, dim3((n_short + kSRTok - 1) / kSRTok, H / kSRHeads),
+                                dim3(kSRThreads), kSRSmem, stream, table, q_lat, q_pe, H, n_short, qpos0,
+                                scale_log2, o_lat, lse));
 }
 
 mla_status launch_prefill_tc(const TcParams& p, cudaStream_t stream) {
