@@ -10,8 +10,10 @@
 // cores with mma.sync.m16n8k16 (bf16 in, fp32 accumulate).  The weight tile
 // of a CTA is staged once in shared memory (rows padded so that ldmatrix is
 // conflict-free) and read with ldmatrix.trans; the activations stream through
-// 16-row tiles.  Their cost is reading the weights once (2 MiB per 16 heads
-// each), so a CTA covers one head and one column tile.
+// 16-row tiles.  A decode batch's cost is reading the weights once (2 MiB per
+// 16 heads each), so a CTA covers one head and one column tile; a prefill
+// chunk's batch (512 rows or more) takes the *_big kernels, whose CTA keeps
+// a head's whole weight and whose warps take whole row tiles.
 //   absorb:   A = q_nope (bf16, exact), B = W_UK: products exact in fp32.
 //   unabsorb: A = o_lat (fp32) split into three bf16 pieces (hi + mid + lo
 //             carry all 24 significant bits), B = W_UV: three MMAs per step.
@@ -195,6 +197,151 @@ __global__ void __launch_bounds__(128) out_unabsorb_kernel(const float* __restri
   }
 }
 
+// ---------------------------------------------------------------------------
+// Batches of a prefill chunk (B >= kBigB): a CTA keeps the whole weight of
+// one head in shared memory and its eight warps each take whole 16-row
+// tiles (all output columns, the whole contraction), so every activation
+// row is read and (unabsorb) split once; the small-batch kernels above read
+// each weight tile once instead, which is what a decode batch is bound by.
+// grid (H, Z): CTA (h, z) takes the tiles [T z / Z, T (z + 1) / Z) of head
+// h, warp w every eighth of them.
+// ---------------------------------------------------------------------------
+constexpr int kBigB = 512;
+constexpr int kBigThreads = 256;
+constexpr int kBigAbWS = kDc + 8;                                  // W_UK row stride (bf16): 1040 B
+constexpr int kBigUnWS = kDv + 8;                                  // W_UV row stride (bf16): 272 B
+constexpr int kBigAbSmem = kDn * kBigAbWS * 2;                     // 133,120 B
+constexpr int kBigUnSmem = kDc * kBigUnWS * 2;                     // 139,264 B
+
+// q_lat tile: 16 rows x 128 columns (quarter cq of 512) per warp unit; the
+// A fragments (bf16 pairs of q_nope) come straight from global memory.
+__global__ void __launch_bounds__(kBigThreads, 1) q_absorb_big_kernel(const uint16_t* __restrict__ q_nope,
+                                                                      const uint16_t* __restrict__ w_uk,
+                                                                      float* __restrict__ q_lat, int B, int H) {
+  extern __shared__ __align__(16) uint16_t big_ws[];
+  pdl_launch_dependents();
+  const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, j = lane & 3;
+  const uint16_t* wsrc = w_uk + (size_t)h * kDn * kDc;
+  for (int i = tid; i < kDn * (kDc / 8); i += kBigThreads) {
+    const int k = i / (kDc / 8), c = i % (kDc / 8);
+    *reinterpret_cast<uint4*>(big_ws + k * kBigAbWS + 8 * c) = *reinterpret_cast<const uint4*>(wsrc + (size_t)k * kDc + 8 * c);
+  }
+  __syncthreads();
+  pdl_wait();
+  const uint32_t b_base = smem_addr(big_ws) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kBigAbWS + 8 * (lane >> 4)) * 2;
+  const int tiles = (B + 15) / 16, units = 4 * tiles;
+  const int u_lo = (int)((int64_t)units * blockIdx.y / gridDim.y);
+  const int u_hi = (int)((int64_t)units * (blockIdx.y + 1) / gridDim.y);
+  for (int u = u_lo + warp; u < u_hi; u += kBigThreads / 32) {
+    const int b0 = 16 * (u >> 2), cq = 128 * (u & 3);
+    const bool ok0 = b0 + r < B, ok1 = b0 + r + 8 < B;
+    const uint32_t* a0p = reinterpret_cast<const uint32_t*>(q_nope + ((size_t)(b0 + r) * H + h) * kDn) + j;
+    const uint32_t* a1p = reinterpret_cast<const uint32_t*>(q_nope + ((size_t)(b0 + r + 8) * H + h) * kDn) + j;
+    uint32_t a[8][4];
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      a[ks][0] = ok0 ? a0p[8 * ks] : 0u;
+      a[ks][1] = ok1 ? a1p[8 * ks] : 0u;
+      a[ks][2] = ok0 ? a0p[8 * ks + 4] : 0u;
+      a[ks][3] = ok1 ? a1p[8 * ks + 4] : 0u;
+    }
+    float acc[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+      for (int pr = 0; pr < 8; ++pr) {
+        uint32_t bf[4];
+        ldsm_x4_t(b_base + (16 * ks * kBigAbWS + cq + 16 * pr) * 2, bf);
+        mma_bf16(acc[2 * pr], a[ks], bf[0], bf[1]);
+        mma_bf16(acc[2 * pr + 1], a[ks], bf[2], bf[3]);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      const int col = cq + 8 * nt + 2 * j;
+      if (ok0) *reinterpret_cast<float2*>(q_lat + ((size_t)(b0 + r) * H + h) * kDc + col) = make_float2(acc[nt][0], acc[nt][1]);
+      if (ok1)
+        *reinterpret_cast<float2*>(q_lat + ((size_t)(b0 + r + 8) * H + h) * kDc + col) =
+            make_float2(acc[nt][2], acc[nt][3]);
+    }
+  }
+}
+
+// o tile: 16 rows x all 128 columns per warp unit, K = 512 in 32 steps; the
+// fp32 A fragments come from global memory one step ahead and are split
+// into three bf16 pieces once.
+__global__ void __launch_bounds__(kBigThreads, 1) out_unabsorb_big_kernel(const float* __restrict__ o_lat,
+                                                                          const uint16_t* __restrict__ w_uv,
+                                                                          float* __restrict__ o, int B, int H) {
+  extern __shared__ __align__(16) uint16_t big_ws[];
+  pdl_launch_dependents();
+  const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, j = lane & 3;
+  const uint16_t* wsrc = w_uv + (size_t)h * kDc * kDv;
+  for (int i = tid; i < kDc * (kDv / 8); i += kBigThreads) {
+    const int k = i / (kDv / 8), c = i % (kDv / 8);
+    *reinterpret_cast<uint4*>(big_ws + k * kBigUnWS + 8 * c) = *reinterpret_cast<const uint4*>(wsrc + (size_t)k * kDv + 8 * c);
+  }
+  __syncthreads();
+  pdl_wait();
+  const uint32_t b_base = smem_addr(big_ws) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kBigUnWS + 8 * (lane >> 4)) * 2;
+  const int tiles = (B + 15) / 16;
+  const int t_lo = (int)((int64_t)tiles * blockIdx.y / gridDim.y);
+  const int t_hi = (int)((int64_t)tiles * (blockIdx.y + 1) / gridDim.y);
+  const float2 z = make_float2(0.f, 0.f);
+  for (int t = t_lo + warp; t < t_hi; t += kBigThreads / 32) {
+    const int b0 = 16 * t;
+    const bool ok0 = b0 + r < B, ok1 = b0 + r + 8 < B;
+    const float* a0p = o_lat + ((size_t)(b0 + r) * H + h) * kDc + 2 * j;
+    const float* a1p = o_lat + ((size_t)(b0 + r + 8) * H + h) * kDc + 2 * j;
+    float acc[16][4];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    float2 x[4];
+    x[0] = ok0 ? *reinterpret_cast<const float2*>(a0p) : z;
+    x[1] = ok1 ? *reinterpret_cast<const float2*>(a1p) : z;
+    x[2] = ok0 ? *reinterpret_cast<const float2*>(a0p + 8) : z;
+    x[3] = ok1 ? *reinterpret_cast<const float2*>(a1p + 8) : z;
+#pragma unroll 1
+    for (int ks = 0; ks < kDc / 16; ++ks) {
+      uint32_t a[3][4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split3(x[e].x, x[e].y, a[0][e], a[1][e], a[2][e]);
+      if (ks + 1 < kDc / 16) {                      // the next step's fragments, in flight during this one
+        const int o1 = 16 * (ks + 1);
+        x[0] = ok0 ? *reinterpret_cast<const float2*>(a0p + o1) : z;
+        x[1] = ok1 ? *reinterpret_cast<const float2*>(a1p + o1) : z;
+        x[2] = ok0 ? *reinterpret_cast<const float2*>(a0p + o1 + 8) : z;
+        x[3] = ok1 ? *reinterpret_cast<const float2*>(a1p + o1 + 8) : z;
+      }
+#pragma unroll
+      for (int pr = 0; pr < 8; ++pr) {
+        uint32_t bf[4];
+        ldsm_x4_t(b_base + (16 * ks * kBigUnWS + 16 * pr) * 2, bf);
+#pragma unroll
+        for (int part3 = 0; part3 < 3; ++part3) {
+          mma_bf16(acc[2 * pr], a[part3], bf[0], bf[1]);
+          mma_bf16(acc[2 * pr + 1], a[part3], bf[2], bf[3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      const int col = 8 * nt + 2 * j;
+      if (ok0) *reinterpret_cast<float2*>(o + ((size_t)(b0 + r) * H + h) * kDv + col) = make_float2(acc[nt][0], acc[nt][1]);
+      if (ok1) *reinterpret_cast<float2*>(o + ((size_t)(b0 + r + 8) * H + h) * kDv + col) = make_float2(acc[nt][2], acc[nt][3]);
+    }
+  }
+}
+
+// CTAs per head for the large-batch kernels: about one wave of one CTA per SM.
+int big_splits(int H) {
+  const int sms = device_sm_count();
+  const int z = (sms > 0 ? sms : 152) / H;
+  return z < 1 ? 1 : z;
+}
+
 }  // namespace
 
 // Large batches (a prefill chunk's queries) split their 16-row tiles over
@@ -205,14 +352,39 @@ static int batch_splits(int B) {
   return z < 1 ? 1 : (z > 32 ? 32 : z);
 }
 
+// Raises a kernel's dynamic shared-memory limit once per device.
+template <typename K>
+static mla_status allow_big_smem(K kernel, int bytes, int* configured) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && configured[dev]) return MLA_OK;
+  const mla_status st = cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  if (st == MLA_OK && dev >= 0 && dev < 64) configured[dev] = 1;
+  return st;
+}
+
 mla_status launch_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* q_lat, int B, int H,
                            cudaStream_t stream) {
+  if (B >= kBigB) {
+    static int configured[64] = {0};
+    const mla_status st = allow_big_smem(q_absorb_big_kernel, kBigAbSmem, configured);
+    if (st != MLA_OK) return st;
+    return cuda_status(launch_pdl(q_absorb_big_kernel, dim3(H, big_splits(H)), dim3(kBigThreads), kBigAbSmem, stream,
+                                  q_nope, w_uk, q_lat, B, H));
+  }
   return cuda_status(launch_pdl(q_absorb_kernel, dim3(H, kDc / kAbN, batch_splits(B)), dim3(128), 0, stream, q_nope,
                                 w_uk, q_lat, B, H));
 }
 
 mla_status launch_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* o, int B, int H,
                                cudaStream_t stream) {
+  if (B >= kBigB) {
+    static int configured[64] = {0};
+    const mla_status st = allow_big_smem(out_unabsorb_big_kernel, kBigUnSmem, configured);
+    if (st != MLA_OK) return st;
+    return cuda_status(launch_pdl(out_unabsorb_big_kernel, dim3(H, big_splits(H)), dim3(kBigThreads), kBigUnSmem,
+                                  stream, o_lat, w_uv, o, B, H));
+  }
   return cuda_status(launch_pdl(out_unabsorb_kernel, dim3(H, kDv / kUnN, batch_splits(B)), dim3(128), 0, stream, o_lat,
                                 w_uv, o, B, H));
 }

@@ -57,12 +57,12 @@ def test_zero_batch_is_noop():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("B", [1000, 4100])
-def test_large_batches_split_over_the_grid(B):
-    """Prefill-sized batches: the 16-row tiles are split over several CTAs
-    per weight tile (a ragged last tile included); sampled rows of both
-    projections against the oracle."""
-    seed, layer, H = 7, 0, 16
+@pytest.mark.parametrize("B,H", [(1000, 16), (4100, 16), (600, 64), (513, 128)])
+def test_large_batches_split_over_the_grid(B, H):
+    """Prefill-sized batches (512 rows and more: a CTA per head keeps the
+    head's whole weight, each warp takes whole 16-row tiles; a ragged last
+    tile included); sampled rows of both projections against the oracle."""
+    seed, layer = 7, 0
     rng = np.random.default_rng(B)
     rows = sorted(set([0, 15, 16, B - 17, B - 1] + [int(r) for r in rng.integers(0, B, 20)]))
     qn = sd.q_nope(seed, layer, B, H)
