@@ -203,8 +203,11 @@ __global__ void __launch_bounds__(128) out_unabsorb_kernel(const float* __restri
 // tiles (all output columns, the whole contraction), so every activation
 // row is read and (unabsorb) split once; the small-batch kernels above read
 // each weight tile once instead, which is what a decode batch is bound by.
-// grid (H, Z): CTA (h, z) takes the tiles [T z / Z, T (z + 1) / Z) of head
-// h, warp w every eighth of them.
+// The work is H x U units (head-major; a unit is a 16-row tile, or for the
+// absorb a tile's quarter of the 512 output columns).  Of G CTAs (about one
+// per SM, big_grid), CTA c takes the contiguous units [H U c / G,
+// H U (c + 1) / G) and warp w every eighth unit of each head in that range;
+// the CTA loads a head's weight when its range enters the head.
 // ---------------------------------------------------------------------------
 constexpr int kBigB = 512;
 constexpr int kBigThreads = 256;
@@ -220,53 +223,68 @@ __global__ void __launch_bounds__(kBigThreads, 1) q_absorb_big_kernel(const uint
                                                                       float* __restrict__ q_lat, int B, int H) {
   extern __shared__ __align__(16) uint16_t big_ws[];
   pdl_launch_dependents();
-  const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, j = lane & 3;
-  const uint16_t* wsrc = w_uk + (size_t)h * kDn * kDc;
-  for (int i = tid; i < kDn * (kDc / 8); i += kBigThreads) {
-    const int k = i / (kDc / 8), c = i % (kDc / 8);
-    *reinterpret_cast<uint4*>(big_ws + k * kBigAbWS + 8 * c) = *reinterpret_cast<const uint4*>(wsrc + (size_t)k * kDc + 8 * c);
-  }
-  __syncthreads();
-  pdl_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, j = lane & 3;
   const uint32_t b_base = smem_addr(big_ws) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kBigAbWS + 8 * (lane >> 4)) * 2;
-  const int tiles = (B + 15) / 16, units = 4 * tiles;
-  const int u_lo = (int)((int64_t)units * blockIdx.y / gridDim.y);
-  const int u_hi = (int)((int64_t)units * (blockIdx.y + 1) / gridDim.y);
-  for (int u = u_lo + warp; u < u_hi; u += kBigThreads / 32) {
-    const int b0 = 16 * (u >> 2), cq = 128 * (u & 3);
-    const bool ok0 = b0 + r < B, ok1 = b0 + r + 8 < B;
-    const uint32_t* a0p = reinterpret_cast<const uint32_t*>(q_nope + ((size_t)(b0 + r) * H + h) * kDn) + j;
-    const uint32_t* a1p = reinterpret_cast<const uint32_t*>(q_nope + ((size_t)(b0 + r + 8) * H + h) * kDn) + j;
-    uint32_t a[8][4];
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      a[ks][0] = ok0 ? a0p[8 * ks] : 0u;
-      a[ks][1] = ok1 ? a1p[8 * ks] : 0u;
-      a[ks][2] = ok0 ? a0p[8 * ks + 4] : 0u;
-      a[ks][3] = ok1 ? a1p[8 * ks + 4] : 0u;
+  const int tiles = (B + 15) / 16;
+  const int64_t per_head = 4 * (int64_t)tiles, total = per_head * H;
+  const int64_t u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
+  bool waited = false;
+  for (int h = (int)(u_lo / per_head); (int64_t)h * per_head < u_hi; ++h) {
+    // the previous head's units are done with the weight before it is replaced
+    if (waited) __syncthreads();
+    const uint16_t* wsrc = w_uk + (size_t)h * kDn * kDc;
+    for (int i = tid; i < kDn * (kDc / 8); i += kBigThreads) {
+      const int k = i / (kDc / 8), c = i % (kDc / 8);
+      *reinterpret_cast<uint4*>(big_ws + k * kBigAbWS + 8 * c) =
+          *reinterpret_cast<const uint4*>(wsrc + (size_t)k * kDc + 8 * c);
     }
-    float acc[16][4];
+    __syncthreads();
+    if (!waited) {
+      pdl_wait();                                   // no kernel writes the weights: only q_nope waits
+      waited = true;
+    }
+    const int64_t h0 = (int64_t)h * per_head;
+    const int v_lo = (int)((u_lo > h0 ? u_lo : h0) - h0);
+    const int v_hi = (int)((u_hi < h0 + per_head ? u_hi : h0 + per_head) - h0);
+    for (int u = v_lo + warp; u < v_hi; u += kBigThreads / 32) {
+      const int b0 = 16 * (u >> 2), cq = 128 * (u & 3);
+      const bool ok0 = b0 + r < B, ok1 = b0 + r + 8 < B;
+      const uint32_t* a0p = reinterpret_cast<const uint32_t*>(q_nope + ((size_t)(b0 + r) * H + h) * kDn) + j;
+      const uint32_t* a1p = reinterpret_cast<const uint32_t*>(q_nope + ((size_t)(b0 + r + 8) * H + h) * kDn) + j;
+      uint32_t a[8][4];
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      for (int ks = 0; ks < 8; ++ks) {
+        a[ks][0] = ok0 ? a0p[8 * ks] : 0u;
+        a[ks][1] = ok1 ? a1p[8 * ks] : 0u;
+        a[ks][2] = ok0 ? a0p[8 * ks + 4] : 0u;
+        a[ks][3] = ok1 ? a1p[8 * ks + 4] : 0u;
+      }
+      float acc[16][4];
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
+      for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
 #pragma unroll
-      for (int pr = 0; pr < 8; ++pr) {
-        uint32_t bf[4];
-        ldsm_x4_t(b_base + (16 * ks * kBigAbWS + cq + 16 * pr) * 2, bf);
-        mma_bf16(acc[2 * pr], a[ks], bf[0], bf[1]);
-        mma_bf16(acc[2 * pr + 1], a[ks], bf[2], bf[3]);
+      for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+        for (int pr = 0; pr < 8; ++pr) {
+          uint32_t bf[4];
+          ldsm_x4_t(b_base + (16 * ks * kBigAbWS + cq + 16 * pr) * 2, bf);
+          mma_bf16(acc[2 * pr], a[ks], bf[0], bf[1]);
+          mma_bf16(acc[2 * pr + 1], a[ks], bf[2], bf[3]);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int col = cq + 8 * nt + 2 * j;
+        if (ok0)
+          *reinterpret_cast<float2*>(q_lat + ((size_t)(b0 + r) * H + h) * kDc + col) =
+              make_float2(acc[nt][0], acc[nt][1]);
+        if (ok1)
+          *reinterpret_cast<float2*>(q_lat + ((size_t)(b0 + r + 8) * H + h) * kDc + col) =
+              make_float2(acc[nt][2], acc[nt][3]);
       }
     }
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int col = cq + 8 * nt + 2 * j;
-      if (ok0) *reinterpret_cast<float2*>(q_lat + ((size_t)(b0 + r) * H + h) * kDc + col) = make_float2(acc[nt][0], acc[nt][1]);
-      if (ok1)
-        *reinterpret_cast<float2*>(q_lat + ((size_t)(b0 + r + 8) * H + h) * kDc + col) =
-            make_float2(acc[nt][2], acc[nt][3]);
-    }
   }
+  if (!waited) pdl_wait();
 }
 
 // o tile: 16 rows x all 128 columns per warp unit, K = 512 in 32 steps; the
@@ -277,69 +295,88 @@ __global__ void __launch_bounds__(kBigThreads, 1) out_unabsorb_big_kernel(const 
                                                                           float* __restrict__ o, int B, int H) {
   extern __shared__ __align__(16) uint16_t big_ws[];
   pdl_launch_dependents();
-  const int h = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, j = lane & 3;
-  const uint16_t* wsrc = w_uv + (size_t)h * kDc * kDv;
-  for (int i = tid; i < kDc * (kDv / 8); i += kBigThreads) {
-    const int k = i / (kDv / 8), c = i % (kDv / 8);
-    *reinterpret_cast<uint4*>(big_ws + k * kBigUnWS + 8 * c) = *reinterpret_cast<const uint4*>(wsrc + (size_t)k * kDv + 8 * c);
-  }
-  __syncthreads();
-  pdl_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, r = lane >> 2, j = lane & 3;
   const uint32_t b_base = smem_addr(big_ws) + (((lane & 7) + 8 * ((lane >> 3) & 1)) * kBigUnWS + 8 * (lane >> 4)) * 2;
-  const int tiles = (B + 15) / 16;
-  const int t_lo = (int)((int64_t)tiles * blockIdx.y / gridDim.y);
-  const int t_hi = (int)((int64_t)tiles * (blockIdx.y + 1) / gridDim.y);
+  const int64_t per_head = (B + 15) / 16, total = per_head * H;
+  const int64_t u_lo = total * blockIdx.x / gridDim.x, u_hi = total * (blockIdx.x + 1) / gridDim.x;
   const float2 z = make_float2(0.f, 0.f);
-  for (int t = t_lo + warp; t < t_hi; t += kBigThreads / 32) {
-    const int b0 = 16 * t;
-    const bool ok0 = b0 + r < B, ok1 = b0 + r + 8 < B;
-    const float* a0p = o_lat + ((size_t)(b0 + r) * H + h) * kDc + 2 * j;
-    const float* a1p = o_lat + ((size_t)(b0 + r + 8) * H + h) * kDc + 2 * j;
-    float acc[16][4];
+  bool waited = false;
+  for (int h = (int)(u_lo / per_head); (int64_t)h * per_head < u_hi; ++h) {
+    if (waited) __syncthreads();
+    const uint16_t* wsrc = w_uv + (size_t)h * kDc * kDv;
+    for (int i = tid; i < kDc * (kDv / 8); i += kBigThreads) {
+      const int k = i / (kDv / 8), c = i % (kDv / 8);
+      *reinterpret_cast<uint4*>(big_ws + k * kBigUnWS + 8 * c) =
+          *reinterpret_cast<const uint4*>(wsrc + (size_t)k * kDv + 8 * c);
+    }
+    __syncthreads();
+    if (!waited) {
+      pdl_wait();
+      waited = true;
+    }
+    const int64_t h0 = (int64_t)h * per_head;
+    const int t_lo = (int)((u_lo > h0 ? u_lo : h0) - h0);
+    const int t_hi = (int)((u_hi < h0 + per_head ? u_hi : h0 + per_head) - h0);
+    for (int t = t_lo + warp; t < t_hi; t += kBigThreads / 32) {
+      const int b0 = 16 * t;
+      const bool ok0 = b0 + r < B, ok1 = b0 + r + 8 < B;
+      const float* a0p = o_lat + ((size_t)(b0 + r) * H + h) * kDc + 2 * j;
+      const float* a1p = o_lat + ((size_t)(b0 + r + 8) * H + h) * kDc + 2 * j;
+      float acc[16][4];
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-    float2 x[4];
-    x[0] = ok0 ? *reinterpret_cast<const float2*>(a0p) : z;
-    x[1] = ok1 ? *reinterpret_cast<const float2*>(a1p) : z;
-    x[2] = ok0 ? *reinterpret_cast<const float2*>(a0p + 8) : z;
-    x[3] = ok1 ? *reinterpret_cast<const float2*>(a1p + 8) : z;
+      for (int nt = 0; nt < 16; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+      float2 x[4];
+      x[0] = ok0 ? *reinterpret_cast<const float2*>(a0p) : z;
+      x[1] = ok1 ? *reinterpret_cast<const float2*>(a1p) : z;
+      x[2] = ok0 ? *reinterpret_cast<const float2*>(a0p + 8) : z;
+      x[3] = ok1 ? *reinterpret_cast<const float2*>(a1p + 8) : z;
 #pragma unroll 1
-    for (int ks = 0; ks < kDc / 16; ++ks) {
-      uint32_t a[3][4];
+      for (int ks = 0; ks < kDc / 16; ++ks) {
+        uint32_t a[3][4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) split3(x[e].x, x[e].y, a[0][e], a[1][e], a[2][e]);
-      if (ks + 1 < kDc / 16) {                      // the next step's fragments, in flight during this one
-        const int o1 = 16 * (ks + 1);
-        x[0] = ok0 ? *reinterpret_cast<const float2*>(a0p + o1) : z;
-        x[1] = ok1 ? *reinterpret_cast<const float2*>(a1p + o1) : z;
-        x[2] = ok0 ? *reinterpret_cast<const float2*>(a0p + o1 + 8) : z;
-        x[3] = ok1 ? *reinterpret_cast<const float2*>(a1p + o1 + 8) : z;
-      }
+        for (int e = 0; e < 4; ++e) split3(x[e].x, x[e].y, a[0][e], a[1][e], a[2][e]);
+        if (ks + 1 < kDc / 16) {                    // the next step's fragments, in flight during this one
+          const int o1 = 16 * (ks + 1);
+          x[0] = ok0 ? *reinterpret_cast<const float2*>(a0p + o1) : z;
+          x[1] = ok1 ? *reinterpret_cast<const float2*>(a1p + o1) : z;
+          x[2] = ok0 ? *reinterpret_cast<const float2*>(a0p + o1 + 8) : z;
+          x[3] = ok1 ? *reinterpret_cast<const float2*>(a1p + o1 + 8) : z;
+        }
 #pragma unroll
-      for (int pr = 0; pr < 8; ++pr) {
-        uint32_t bf[4];
-        ldsm_x4_t(b_base + (16 * ks * kBigUnWS + 16 * pr) * 2, bf);
+        for (int pr = 0; pr < 8; ++pr) {
+          uint32_t bf[4];
+          ldsm_x4_t(b_base + (16 * ks * kBigUnWS + 16 * pr) * 2, bf);
 #pragma unroll
-        for (int part3 = 0; part3 < 3; ++part3) {
-          mma_bf16(acc[2 * pr], a[part3], bf[0], bf[1]);
-          mma_bf16(acc[2 * pr + 1], a[part3], bf[2], bf[3]);
+          for (int part3 = 0; part3 < 3; ++part3) {
+            mma_bf16(acc[2 * pr], a[part3], bf[0], bf[1]);
+            mma_bf16(acc[2 * pr + 1], a[part3], bf[2], bf[3]);
+          }
         }
       }
-    }
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const int col = 8 * nt + 2 * j;
-      if (ok0) *reinterpret_cast<float2*>(o + ((size_t)(b0 + r) * H + h) * kDv + col) = make_float2(acc[nt][0], acc[nt][1]);
-      if (ok1) *reinterpret_cast<float2*>(o + ((size_t)(b0 + r + 8) * H + h) * kDv + col) = make_float2(acc[nt][2], acc[nt][3]);
+      for (int nt = 0; nt < 16; ++nt) {
+        const int col = 8 * nt + 2 * j;
+        if (ok0)
+          *reinterpret_cast<float2*>(o + ((size_t)(b0 + r) * H + h) * kDv + col) = make_float2(acc[nt][0], acc[nt][1]);
+        if (ok1)
+          *reinterpret_cast<float2*>(o + ((size_t)(b0 + r + 8) * H + h) * kDv + col) =
+              make_float2(acc[nt][2], acc[nt][3]);
+      }
     }
   }
+  if (!waited) pdl_wait();
 }
 
-// CTAs per head for the large-batch kernels: about one wave of one CTA per SM.
-int big_splits(int H) {
-  const int sms = device_sm_count();
-  const int z = (sms > 0 ? sms : 152) / H;
-  return z < 1 ? 1 : z;
+// CTAs of the large-batch kernels.  H * floor(SMs / H) CTAs split every head
+// evenly (no CTA loads two weights); when that leaves more than a tenth of
+// the SMs idle and each CTA still gets 64 units or more, one CTA per SM,
+// whose ranges may cross a head boundary (a second weight load).
+int big_grid(int64_t units, int H) {
+  const int sms = device_sm_count() > 0 ? device_sm_count() : 152;
+  const int64_t aligned = (int64_t)H * (sms / H);
+  int64_t g = aligned;
+  if (aligned == 0 || (10 * aligned < 9 * (int64_t)sms && units >= 64 * (int64_t)sms)) g = sms;
+  return (int)(units < g ? (units > 0 ? units : 1) : g);
 }
 
 }  // namespace
@@ -369,8 +406,9 @@ mla_status launch_q_absorb(const uint16_t* q_nope, const uint16_t* w_uk, float* 
     static int configured[64] = {0};
     const mla_status st = allow_big_smem(q_absorb_big_kernel, kBigAbSmem, configured);
     if (st != MLA_OK) return st;
-    return cuda_status(launch_pdl(q_absorb_big_kernel, dim3(H, big_splits(H)), dim3(kBigThreads), kBigAbSmem, stream,
-                                  q_nope, w_uk, q_lat, B, H));
+    const dim3 grid(big_grid(4 * (int64_t)((B + 15) / 16) * H, H));
+    return cuda_status(launch_pdl(q_absorb_big_kernel, grid, dim3(kBigThreads), kBigAbSmem, stream, q_nope, w_uk,
+                                  q_lat, B, H));
   }
   return cuda_status(launch_pdl(q_absorb_kernel, dim3(H, kDc / kAbN, batch_splits(B)), dim3(128), 0, stream, q_nope,
                                 w_uk, q_lat, B, H));
@@ -382,8 +420,9 @@ mla_status launch_out_unabsorb(const float* o_lat, const uint16_t* w_uv, float* 
     static int configured[64] = {0};
     const mla_status st = allow_big_smem(out_unabsorb_big_kernel, kBigUnSmem, configured);
     if (st != MLA_OK) return st;
-    return cuda_status(launch_pdl(out_unabsorb_big_kernel, dim3(H, big_splits(H)), dim3(kBigThreads), kBigUnSmem,
-                                  stream, o_lat, w_uv, o, B, H));
+    const dim3 grid(big_grid((int64_t)((B + 15) / 16) * H, H));
+    return cuda_status(launch_pdl(out_unabsorb_big_kernel, grid, dim3(kBigThreads), kBigUnSmem, stream, o_lat, w_uv,
+                                  o, B, H));
   }
   return cuda_status(launch_pdl(out_unabsorb_kernel, dim3(H, kDv / kUnN, batch_splits(B)), dim3(128), 0, stream, o_lat,
                                 w_uv, o, B, H));
