@@ -57,11 +57,15 @@ def test_zero_batch_is_noop():
     torch.cuda.synchronize()
 
 
-@pytest.mark.parametrize("B,H", [(1000, 16), (4100, 16), (600, 64), (513, 128)])
+@pytest.mark.parametrize("B,H", [(1000, 16), (4100, 16), (600, 64), (513, 128), (2432, 64), (2048, 128)])
 def test_large_batches_split_over_the_grid(B, H):
-    """Prefill-sized batches (512 rows and more: a CTA per head keeps the
-    head's whole weight, each warp takes whole 16-row tiles; a ragged last
-    tile included); sampled rows of both projections against the oracle."""
+    """Prefill-sized batches (512 rows and more: a CTA keeps a head's whole
+    weight, each warp takes whole 16-row tiles; a ragged last tile
+    included); sampled rows of both projections against the oracle.  Grids:
+    16 heads split every head over 9 CTAs; 600 x 64 and 513 x 128 run the
+    absorb on one CTA per SM with ranges crossing head boundaries and the
+    unabsorb head-aligned; 2432 x 64 and 2048 x 128 cross head boundaries in
+    both."""
     seed, layer = 7, 0
     rng = np.random.default_rng(B)
     rows = sorted(set([0, 15, 16, B - 17, B - 1] + [int(r) for r in rng.integers(0, B, 20)]))
