@@ -623,6 +623,64 @@ def run_ours(args, cfg, rank, world, local_rank):
     return out, seq_lens
 
 
+def aux_kernels(steps):
+    """The two calls off the decode step: the merge of a context-sharded
+    decode (mla_lse_merge, one launch per layer and step on the gathered
+    parts) and the outlier format's calibration (mla_select_outlier_channels,
+    once per layer).  Each is timed alone, warm, with CUDA events on its
+    stream over `steps` calls; achieved = algorithmic bytes / call time (the
+    small cases stay in L2 between calls; the largest merge does not)."""
+    import torch
+    import synth
+    import mla_latent_kv_append_gb300 as mla
+    dev = torch.device("cuda")
+    clocks = Clocks(torch.cuda.current_device())
+    clocks.start()
+    stream = torch.cuda.Stream()
+    peak, peak_kind = hbm_peak()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            a.record(stream)
+            for _ in range(steps):
+                fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    out = {"merge": [], "select_outliers": []}
+    g = torch.Generator(device=dev)
+    g.manual_seed(SEED)
+    for desc, (R, B, H) in [("V2-Lite INT4 32K batch, one layer, 8 context shards", (8, 32, 16)),
+                            ("one long sequence, one layer, 8 context shards", (8, 1, 16)),
+                            ("4096 sequences x 16 heads, 8 shards (> L2)", (8, 4096, 16))]:
+        o_parts = torch.randn((R, B, H, mla.KV_LORA_RANK), generator=g, device=dev)
+        lse_parts = torch.randn((R, B, H), generator=g, device=dev) * 4
+        o_lat = torch.empty((B, H, mla.KV_LORA_RANK), device=dev)
+        lse = torch.empty((B, H), device=dev)
+        ms = timed(lambda: mla.mla_lse_merge(o_parts, lse_parts, o_lat, lse, stream=stream))
+        nbytes = (R + 1) * B * H * (4 * mla.KV_LORA_RANK + 4)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out["merge"].append({"workload": desc, "parts": R, "batch": B, "heads": H, "bytes_per_launch": nbytes,
+                             "launch_us": ms * 1e3, "achieved": gbs, "frac": gbs / peak})
+        del o_parts, lse_parts, o_lat, lse
+    for n in (synth.CALIBRATION_TOKENS, 65536):
+        sample = (torch.randn((n, mla.KV_LORA_RANK), generator=g, device=dev) * 3).to(torch.bfloat16)
+        chans = torch.empty(mla.OUTLIER_CHANNELS, dtype=torch.int32, device=dev)
+        ms = timed(lambda: mla.mla_select_outlier_channels(sample, chans, stream=stream))
+        nbytes = n * 2 * mla.KV_LORA_RANK + 4 * mla.OUTLIER_CHANNELS
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out["select_outliers"].append({"tokens": n, "bytes_per_launch": nbytes, "launch_us": ms * 1e3,
+                                       "achieved": gbs, "frac": gbs / peak,
+                                       "note": "one CTA by design (a calibration call, off the step)"})
+    return {"aux": "calls off the decode step", "unit": "GB/s", "peak": peak,
+            "peak_source": "%s hbm_gbs (MEASURED_PEAKS.json)" % peak_kind, "steps": steps,
+            "clocks": clocks.stop(), **out}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -633,6 +691,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (testing only)")
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--aux", action="store_true",
+                    help="time the merge and calibration calls (one JSON line) instead of the step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -662,6 +722,12 @@ def main():
         print(json.dumps(line))
         return 0
 
+    if args.aux:
+        if rank == 0:
+            import torch
+            torch.cuda.set_device(local_rank)
+            print(json.dumps(aux_kernels(max(1, args.steps))))
+        return 0
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
