@@ -417,17 +417,53 @@ __device__ __forceinline__ void unabsorb_rows(const DecodeParams& p, int b, int 
   }
 }
 
+// The projection of one merged row (o_lat in shared memory, `row`) by
+// W_UV[h]: the arithmetic of unabsorb_rows, with every weight load of a
+// thread in flight at once and no re-read of the row from global memory.
+__device__ __forceinline__ void unabsorb_row(const DecodeParams& p, int b, int h, const float* row, float* sm) {
+  const int tid = threadIdx.x, vp = tid & 63, kp = tid >> 6;
+  float2* red2 = reinterpret_cast<float2*>(sm);              // [16 parts][64 column pairs]
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(p.w_uv + ((size_t)h * kDc + 32 * kp) * kDv) + vp;
+  uint32_t wv[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) wv[c] = __ldg(w + c * (kDv / 2));
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const float x = row[32 * kp + c];
+    a0 = fmaf(x, bf16lo(wv[c]), a0);
+    a1 = fmaf(x, bf16hi(wv[c]), a1);
+  }
+  red2[kp * 64 + vp] = make_float2(a0, a1);
+  __syncthreads();
+  if (tid < 64) {
+    float2 sum = red2[tid];
+#pragma unroll
+    for (int k = 1; k < 16; ++k) {
+      sum.x += red2[k * 64 + tid].x;
+      sum.y += red2[k * 64 + tid].y;
+    }
+    *reinterpret_cast<float2*>(p.o + ((size_t)b * p.H + h) * kDv + 2 * tid) = sum;
+  }
+}
+
 // Merge of sequence b, head h in a 1024-thread block (combine_kernel's
-// grid): writes o_lat and lse and returns true, or returns false (in every
-// thread) when the row carries too much weight of fp16 P V products against
-// its merged output and must be recomputed exactly.
+// grid) over the S slots from x0 on: writes o_lat and lse and returns true,
+// or returns false (in every thread) when the row carries too much weight of
+// fp16 P V products against its merged output and must be recomputed
+// exactly.  The loads that do not wait for the maximum (every slot's figures,
+// one per thread, and each thread's first kMergePre partial rows) are issued
+// together: the merge is a few L2 round trips, not one per step.  (Three rows
+// cover the ~20 slots of a 4K-token batch; the outlier format's combine has
+// registers for two.)
 template <int LF>
-__device__ __forceinline__ bool merge_head(const DecodeParams& p, int b, int h, float* sw, float* red,
+constexpr int kMergePre = LF == MLA_FMT_INT8_OUTLIER ? 2 : 3;
+template <int LF>
+__device__ __forceinline__ bool merge_head(const DecodeParams& p, int b, int h, int x0, int S, float* sw, float* red,
                                            float4 (*parts)[kDc / 4]) {
   const int tid = threadIdx.x;
   const int quad = tid & (kDc / 4 - 1), part = tid / (kDc / 4);
   float4* out = reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc) + quad;
-  const int x0 = p.ws.span[2 * b], S = p.ws.span[2 * b + 1] - x0 + 1;
   const float* mp = p.ws.m + (size_t)(x0 + b) * p.H + h;
   const float* lp = p.ws.l + (size_t)(x0 + b) * p.H + h;
   const float* ep = p.ws.e2 + (size_t)(x0 + b) * p.H + h;
@@ -441,24 +477,47 @@ __device__ __forceinline__ bool merge_head(const DecodeParams& p, int b, int h, 
     if (kRiskFmt<LF>) E2 = *ep;
     if (part == 0) acc = __ldcg(o4);
   } else {
-    float mloc = -INFINITY;
-    for (int t = tid; t < S; t += kCombThreads) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
+    const size_t ostride = (size_t)p.H * (kDc / 4);
+    float m0 = -INFINITY, l0 = 0.f, e0 = 0.f;
+    if (tid < S) {
+      m0 = mp[(size_t)tid * p.H];
+      l0 = lp[(size_t)tid * p.H];
+      if (kRiskFmt<LF>) e0 = ep[(size_t)tid * p.H];
+    }
+    float4 pre[kMergePre<LF>];
+#pragma unroll
+    for (int k = 0; k < kMergePre<LF>; ++k) {
+      const int t = part + kCombParts * k;
+      pre[k] = t < S ? __ldcg(o4 + (size_t)t * ostride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float mloc = m0;
+    for (int t = tid + kCombThreads; t < S; t += kCombThreads) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
     M = block_reduce(mloc, true, red);
     float lloc = 0.f, eloc = 0.f;
     for (int t = tid; t < S; t += kCombThreads) {
-      const float m = mp[(size_t)t * p.H];
+      const float m = t == tid ? m0 : mp[(size_t)t * p.H];
       const float w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
       if (t < kCombSlots) sw[t] = w;
       if (w != 0.f) {
-        lloc = fmaf(w, lp[(size_t)t * p.H], lloc);
-        if (kRiskFmt<LF>) eloc = fmaf(w * w, ep[(size_t)t * p.H], eloc);
+        lloc = fmaf(w, t == tid ? l0 : lp[(size_t)t * p.H], lloc);
+        if (kRiskFmt<LF>) eloc = fmaf(w * w, t == tid ? e0 : ep[(size_t)t * p.H], eloc);
       }
     }
     L = block_reduce(lloc, false, red);   // also orders the sw writes before the reads below
     if (kRiskFmt<LF>) E2 = block_reduce(eloc, false, red);
-    const size_t ostride = (size_t)p.H * (kDc / 4);
+#pragma unroll
+    for (int k = 0; k < kMergePre<LF>; ++k) {   // slots part + 8 k < 24 <= kCombSlots: weights in sw
+      const int t = part + kCombParts * k;
+      if (t < S) {
+        const float w = sw[t];
+        acc.x = fmaf(w, pre[k].x, acc.x);
+        acc.y = fmaf(w, pre[k].y, acc.y);
+        acc.z = fmaf(w, pre[k].z, acc.z);
+        acc.w = fmaf(w, pre[k].w, acc.w);
+      }
+    }
 #pragma unroll 8
-    for (int t = part; t < S; t += kCombParts) {
+    for (int t = part + kCombParts * kMergePre<LF>; t < S; t += kCombParts) {
       float w;
       if (t < kCombSlots) {
         w = sw[t];
@@ -495,14 +554,16 @@ __device__ __forceinline__ bool merge_head(const DecodeParams& p, int b, int h, 
     if (L > 0.f && sqrtf(E2) > kRiskRatio * amax) return false;
     if (part > 0) return true;
   }
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
   if (L > 0.f) {
     const float inv = 1.f / L;
-    *out = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    v = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
     if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = (M + log2f(L)) * 0.69314718055994531f;
   } else {
-    *out = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
   }
+  *out = v;
+  parts[0][quad] = v;                    // the row again, for the projection (part 0 read parts[] above)
   return true;
 }
 
@@ -514,15 +575,18 @@ template <int LF, int KF>
 __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(DecodeParams p) {
   pdl_launch_dependents();
   pdl_wait();
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   extern __shared__ __align__(16) float short_smem[];
   __shared__ float sw[kCombSlots];
   __shared__ float red[kCombThreads / 32];
   __shared__ float4 parts[kCombParts - 1][kDc / 4];
-  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   const int32_t* cum = p.ws.cum;
   // a length out of range ran as 0 in the split kernel; it is reported here,
   // after the wait, so that no earlier kernel's write to dev_err can land later
   const int len = checked_len(p, b, tid == 0);
+  // the slot range, loaded with the length and the chunk counts (unused for
+  // an empty sequence, whose span entries nothing wrote)
+  const int x0 = p.ws.span[2 * b], x1 = p.ws.span[2 * b + 1];
   if (cum[b] == cum[b + 1]) {
     if (tid < kDc / 4) reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.o && tid < kDv / 4) reinterpret_cast<float4*>(p.o + ((size_t)b * p.H + h) * kDv)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -534,11 +598,11 @@ __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(DecodeParams p
   // (computed with its seven neighbours, written alone).  One call site.
   // With the output projection requested, the block projects the rows it
   // wrote.
-  const bool merged = len >= kExactLen && merge_head<LF>(p, b, h, sw, red, parts);
+  const bool merged = len >= kExactLen && merge_head<LF>(p, b, h, x0, x1 - x0 + 1, sw, red, parts);
   if (merged || (len < kExactLen && h % kShortHeads != 0)) {
     if (merged && p.o) {
-      __syncthreads();                      // the row's o_lat stores, before every thread reads them
-      unabsorb_rows(p, b, h - h % kShortHeads, 1u << (h % kShortHeads), short_smem);
+      __syncthreads();                      // the merged row in parts[0], before every thread reads it
+      unabsorb_row(p, b, h, reinterpret_cast<const float*>(parts[0]), short_smem);
     }
     return;
   }
