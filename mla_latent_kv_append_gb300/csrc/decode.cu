@@ -490,21 +490,48 @@ __device__ __forceinline__ bool merge_head(const DecodeParams& p, int b, int h, 
       const int t = part + kCombParts * k;
       pre[k] = t < S ? __ldcg(o4 + (size_t)t * ostride) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float mloc = m0;
-    for (int t = tid + kCombThreads; t < S; t += kCombThreads) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
-    M = block_reduce(mloc, true, red);
-    float lloc = 0.f, eloc = 0.f;
-    for (int t = tid; t < S; t += kCombThreads) {
-      const float m = t == tid ? m0 : mp[(size_t)t * p.H];
-      const float w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
-      if (t < kCombSlots) sw[t] = w;
-      if (w != 0.f) {
-        lloc = fmaf(w, t == tid ? l0 : lp[(size_t)t * p.H], lloc);
-        if (kRiskFmt<LF>) eloc = fmaf(w * w, t == tid ? e0 : ep[(size_t)t * p.H], eloc);
+    if (S <= 32) {
+      // every slot's figures sit in warp 0: its shuffles give the block's
+      // maximum and sums (the same trees as block_reduce, whose other warps
+      // would add zeros), and one barrier publishes them with the weights
+      if (tid < 32) {
+        M = warp_max(m0);
+        const float w = (M == -INFINITY || m0 == -INFINITY) ? 0.f : exp2f(m0 - M);
+        sw[tid] = w;
+        float lloc = 0.f, eloc = 0.f;
+        if (w != 0.f) {
+          lloc = fmaf(w, l0, 0.f);
+          if (kRiskFmt<LF>) eloc = fmaf(w * w, e0, 0.f);
+        }
+        lloc = warp_sum(lloc);
+        if (kRiskFmt<LF>) eloc = warp_sum(eloc);
+        if (tid == 0) {                  // past the 32 weights: sw's last entries are free here
+          sw[kCombSlots - 3] = M;
+          sw[kCombSlots - 2] = lloc;
+          sw[kCombSlots - 1] = eloc;
+        }
       }
+      __syncthreads();
+      M = sw[kCombSlots - 3];
+      L = sw[kCombSlots - 2];
+      if (kRiskFmt<LF>) E2 = sw[kCombSlots - 1];
+    } else {
+      float mloc = m0;
+      for (int t = tid + kCombThreads; t < S; t += kCombThreads) mloc = fmaxf(mloc, mp[(size_t)t * p.H]);
+      M = block_reduce(mloc, true, red);
+      float lloc = 0.f, eloc = 0.f;
+      for (int t = tid; t < S; t += kCombThreads) {
+        const float m = t == tid ? m0 : mp[(size_t)t * p.H];
+        const float w = (M == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - M);
+        if (t < kCombSlots) sw[t] = w;
+        if (w != 0.f) {
+          lloc = fmaf(w, t == tid ? l0 : lp[(size_t)t * p.H], lloc);
+          if (kRiskFmt<LF>) eloc = fmaf(w * w, t == tid ? e0 : ep[(size_t)t * p.H], eloc);
+        }
+      }
+      L = block_reduce(lloc, false, red);   // also orders the sw writes before the reads below
+      if (kRiskFmt<LF>) E2 = block_reduce(eloc, false, red);
     }
-    L = block_reduce(lloc, false, red);   // also orders the sw writes before the reads below
-    if (kRiskFmt<LF>) E2 = block_reduce(eloc, false, red);
 #pragma unroll
     for (int k = 0; k < kMergePre<LF>; ++k) {   // slots part + 8 k < 24 <= kCombSlots: weights in sw
       const int t = part + kCombParts * k;
