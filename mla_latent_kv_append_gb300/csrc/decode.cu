@@ -447,6 +447,43 @@ __device__ __forceinline__ void unabsorb_row(const DecodeParams& p, int b, int h
   }
 }
 
+// For combine_kernel, before its wait: the chunk prefix sums at b and
+// b + 1, their total, b's length, and the splits x0 .. x1 that wrote
+// sequence b's slots, all derived from the call's lengths as the split kernel
+// derives them.  The split kernel's partition gives split x the chunks
+// [C x / Ge, C (x + 1) / Ge), Ge = min(G, C), so chunk c lies in split
+// ceil((c + 1) Ge / C) - 1.  Run by warp 0; out: [c0, c1, C, len, x0, x1].
+__device__ __forceinline__ void chunk_prefix(const DecodeParams& p, int b, int* out) {
+  const int lane = threadIdx.x & 31;
+  int carry = 0;
+  for (int base = 0; base < p.B; base += 32) {
+    const int bb = base + lane;
+    const int len = bb < p.B ? checked_len(p, bb, false) : 0;
+    int v = (len + kChunk - 1) / kChunk;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += t;
+    }
+    if (bb == b) {
+      out[1] = carry + v;
+      out[3] = len;
+    }
+    if (bb + 1 == b) out[0] = carry + v;
+    carry += __shfl_sync(0xffffffffu, v, 31);
+  }
+  __syncwarp();
+  if (lane == 0) {
+    if (b == 0) out[0] = 0;
+    out[2] = carry;
+    const int c0 = out[0], c1 = out[1], C = carry, Ge = p.G < C ? p.G : C;
+    if (c0 < c1) {                       // C > 0
+      out[4] = (int)(((int64_t)(c0 + 1) * Ge + C - 1) / C) - 1;
+      out[5] = (int)(((int64_t)c1 * Ge + C - 1) / C) - 1;
+    }
+  }
+}
+
 // Merge of sequence b, head h in a 1024-thread block (combine_kernel's
 // grid) over the S slots from x0 on: writes o_lat and lse and returns true,
 // or returns false (in every thread) when the row carries too much weight of
@@ -601,20 +638,43 @@ __device__ __forceinline__ bool merge_head(const DecodeParams& p, int b, int h, 
 template <int LF, int KF>
 __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(DecodeParams p) {
   pdl_launch_dependents();
-  pdl_wait();
   const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
   extern __shared__ __align__(16) float short_smem[];
   __shared__ float sw[kCombSlots];
   __shared__ float red[kCombThreads / 32];
   __shared__ float4 parts[kCombParts - 1][kDc / 4];
-  const int32_t* cum = p.ws.cum;
+  __shared__ int pre_c[6];
+  // The lengths are a call input that no kernel in flight writes (except the
+  // prefill's per-row lengths, which the kernel just before writes): the
+  // sequence's chunk range and slot range come from them before the wait,
+  // while the split kernel finishes.  This grid serves batches of at most
+  // G / 8 sequences.
+  const bool early = !p.lens_after_wait;
+  if (early) {
+    if (tid < 32) chunk_prefix(p, b, pre_c);
+    __syncthreads();
+  }
+  pdl_wait();
   // a length out of range ran as 0 in the split kernel; it is reported here,
   // after the wait, so that no earlier kernel's write to dev_err can land later
-  const int len = checked_len(p, b, tid == 0);
-  // the slot range, loaded with the length and the chunk counts (unused for
-  // an empty sequence, whose span entries nothing wrote)
-  const int x0 = p.ws.span[2 * b], x1 = p.ws.span[2 * b + 1];
-  if (cum[b] == cum[b + 1]) {
+  int len, c0, c1, x0, x1;
+  if (early) {
+    if (tid == 0) checked_len(p, b, true);
+    c0 = pre_c[0];
+    c1 = pre_c[1];
+    len = pre_c[3];
+    x0 = pre_c[4];
+    x1 = pre_c[5];
+  } else {
+    // loaded together (the span entries are unused for an empty sequence,
+    // whose entries nothing wrote)
+    len = checked_len(p, b, tid == 0);
+    c0 = p.ws.cum[b];
+    c1 = p.ws.cum[b + 1];
+    x0 = p.ws.span[2 * b];
+    x1 = p.ws.span[2 * b + 1];
+  }
+  if (c0 == c1) {
     if (tid < kDc / 4) reinterpret_cast<float4*>(p.o_lat + ((size_t)b * p.H + h) * kDc)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.o && tid < kDv / 4) reinterpret_cast<float4*>(p.o + ((size_t)b * p.H + h) * kDv)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.lse && tid == 0) p.lse[(size_t)b * p.H + h] = -INFINITY;
