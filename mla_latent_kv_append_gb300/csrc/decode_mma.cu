@@ -854,18 +854,26 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
   // overlap the previous kernel's tail; the workspace, queries and cache wait
   // for it.  The prefill's per-row lengths were waited for above: only
   // griddepcontrol.wait makes the lengths kernel's stores visible.
-  pdl_wait();
-  if (lead)
-    for (int i = tid; i <= p.B; i += kWsThreads) p.ws.cum[i] = cum[i];
+  // The register split needs nothing from the previous kernel either: each
+  // role resizes its allocation first, then waits (split_wait).
+  auto split_wait = [&]() {
+    pdl_wait();
+    if (lead)
+      for (int i = tid; i <= p.B; i += kWsThreads) p.ws.cum[i] = cum[i];
+  };
 
   const int C = cum[p.B];
   const int Ge = G < C ? G : C;
-  if (x >= Ge) return;
+  if (x >= Ge) {
+    split_wait();
+    return;
+  }
   const int c_lo = (int)range_lo(C, x, Ge), c_hi = (int)range_lo(C, x + 1, Ge);
 
   if (warp >= kCW) {
     // ======================= softmax / loader warpgroup =======================
     ws_regs_dec();
+    split_wait();
     const int t = tid - kThreads;              // 0..127: row hr, tokens 4 tq .. 4 tq + 3
     const int hr = t >> 3, tq = t & 7;
     int ld_c = c_lo, ld_b = 0, ld_len = 0, pl_page = -1, pl_t0 = 0;
@@ -1025,6 +1033,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) decode_mma_kernel(DecodeParams 
 
   // ============================= compute warps =============================
   ws_regs_inc();
+  split_wait();
   const int w = warp, r = lane >> 2, j = lane & 3;
   Query q;
   float cw = 0.f;
