@@ -196,12 +196,13 @@ constexpr bool kRiskFmt = LF != MLA_FMT_BF16;
 // combine_kernel: grid (B, H), block 1024: merge the partials of sequence b,
 // head h (the grid for ~8 to ~32 slots per sequence).  CTAs
 // span[2b] .. span[2b+1] wrote slots x + b.  The slots' maxima and sums are
-// read in parallel (one slot per thread), the block reduces them; then each
-// eighth of the block accumulates 4 channels per thread over every eighth
-// slot (a long context spreads one sequence over every SM, so there can be
-// ~150 slots) and the eighths are summed through shared memory.  Every slot in
-// the span was written (o finite, weight 0 for an empty one), so the loads
-// are unconditional and eight of them are in flight at a time.
+// read in parallel (one slot per thread) and reduced (by warp 0 alone when
+// there are at most 32 slots, else by the block); then each eighth of the
+// block accumulates 4 channels per thread over every eighth slot (a long
+// context spreads one sequence over every SM, so there can be ~150 slots)
+// and the eighths are summed through shared memory.  Every slot in the span
+// was written (o finite, weight 0 for an empty one), so the loads are
+// unconditional; a thread's first partial rows load with the slot figures.
 constexpr int kCombSlots = 1024;     // weights cached in shared memory
 constexpr int kCombThreads = 1024;
 constexpr int kCombParts = kCombThreads / (kDc / 4);
