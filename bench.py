@@ -1,6 +1,6 @@
 """Benchmark: absorbed MLA decode over a quantized paged latent cache.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference] [--aux]
 
 A step is one decode step of the whole model: for every layer, append the new
 token of every sequence (quantize-on-write), absorb the query, run the
@@ -14,6 +14,11 @@ before the timed region.  Prints one JSON line on rank 0.
 --impl reference times the CPU oracle (NumPy, fp64 attention) on the same
 workload: each step is a bounded sample (one sequence through all layers,
 layers spread over the host cores).
+
+--aux times, instead of the step, the two calls that are not part of it:
+the merge of a context-sharded decode (mla_lse_merge) and the outlier
+format's calibration (mla_select_outlier_channels); one JSON line of GB/s
+against the measured HBM peak.
 """
 
 import argparse
