@@ -84,6 +84,33 @@ def test_combine_grids(ns):
     run_and_check(wl, num_splits=ns)
 
 
+def _slot_counts(lens, G):
+    """Slots per sequence under the split kernel's partition (split x takes
+    chunks [C x / Ge, C (x + 1) / Ge), Ge = min(G, C)): the splits holding
+    a sequence's first through last 32-token chunk."""
+    chunks = [(t + 31) // 32 for t in lens]
+    C = sum(chunks)
+    Ge = min(G, C)
+    def split(c):
+        return ((c + 1) * Ge + C - 1) // C - 1
+    out, c0 = [], 0
+    for n in chunks:
+        out.append(split(c0 + n - 1) - split(c0) + 1 if n else 0)
+        c0 += n
+    return out
+
+
+def test_combine_slot_reduction_boundary():
+    """The per-head combine reduces the slot figures in one warp when a
+    sequence has at most 32 slots and across the block otherwise: one call
+    with a 32-slot and a 33-slot sequence (and a 4-slot one), against the
+    oracle."""
+    lens, G = [2472, 2536, 300], 67
+    assert _slot_counts(lens, G) == [32, 33, 4]
+    wl = Workload(1, 16, lens, mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, seed=83)
+    run_and_check(wl, num_splits=G)
+
+
 def test_64_heads_mixed_lengths():
     wl = Workload(1, 64, [1000, 37, 2500], mla.FMT_INT8_SYM, mla.FMT_INT8_SYM, seed=79)
     run_and_check(wl)
